@@ -1,0 +1,412 @@
+"""Throughput of the K3 LatentMoE layer on GB300 (one JSON line on stdout).
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
+                [--workload decode_t1|decode_t64|prefill_t4096|chain8_t256]
+
+A step is one forward of the whole layer (router, permutation, routed
+experts, latent norm, up projection and shared experts) over one batch of
+synthetic K3-shape input. Default workload: K3 decode, T=1 token per step,
+tokens rotating through a seeded pool of 64 so that different experts are
+read each step, and the L2 is flushed (256 MB write) between timed steps.
+
+value: tokens/s with inputs resident in HBM (CUDA events around each
+forward, summed over K steps); e2e: the same through k3moe_forward_host
+with pinned host buffers (copies inside the timed region); roofline: the
+dominant kernel's algorithmic bytes per launch over its event-timed average
+duration against the measured HBM copy bandwidth; cpu_baseline: the fp64
+oracle on the host cores on a bounded sample of the same workload.
+
+With torchrun (N > 1) every rank runs an independent replica of the layer
+(the layer does not shard across GPUs); rank 0 prints the line.
+--impl reference times the CPU oracle (the reference arm of this build).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import k3synth  # noqa: E402
+
+METRIC = "MoE-layer tokens/s at K3 shape; HBM GB/s (decode) / FP4 TFLOP/s (prefill)"
+UNIT = "tokens/s"
+POOL = 64
+FLUSH_BYTES = 256 << 20
+
+WORKLOADS = {
+    "decode_t1": dict(T=1, layers=1, desc="K3-shape single layer, decode T=1 "
+                      "(tokens rotate through a seeded pool of 64)"),
+    "decode_t64": dict(T=64, layers=1, desc="K3-shape single layer, decode batch T=64, "
+                       "covering construction: all 896 experts touched"),
+    "prefill_t4096": dict(T=4096, layers=1, desc="K3-shape single layer, prefill T=4096, "
+                          "Zipf(1.1) expert popularity via router bias"),
+    "chain8_t256": dict(T=256, layers=8, desc="8 stacked K3-shape layers, T=256, RMSNorm "
+                        "between layers"),
+}
+ZIPF_ALPHA = 0.55
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+# ---- algorithmic bytes per kernel launch (K3 layer, weights + activations) ------
+
+def kernel_bytes(shape, T, n_touched):
+    H, L, E, I, S, k = (shape.hidden, shape.latent, shape.n_experts, shape.moe_inter,
+                        shape.shared_inter, shape.topk)
+    per_w13 = 2 * (I * L // 2 + I * L // 32)
+    per_w2 = L * I // 2 + L * I // 32
+    return {
+        "dense_x_gemv": 2 * (E * H + L * H + 2 * S * H) + 2 * T * H + 4 * T * (E + L + S),
+        "expert_w13_gemv": n_touched * per_w13 + 2 * T * L + 2 * T * k * I,
+        "expert_w2_gemv": n_touched * per_w2 + 2 * T * k * I + 4 * T * L,
+        "up_shared_gemv": 2 * (H * L + H * S) + 4 * T * (L + S) + 2 * T * H,
+    }
+
+
+def layer_bytes(shape, T, n_touched):
+    return sum(kernel_bytes(shape, T, n_touched).values())
+
+
+# ---- inputs ----------------------------------------------------------------------
+
+def make_inputs(workload, seed=0, layer_index=0):
+    shape = k3synth.K3
+    d = k3synth.make_layer(shape, seed, layer_index, k3synth.K3_RECIPE)
+    T = WORKLOADS[workload]["T"]
+    if workload == "decode_t1":
+        x = k3synth.make_tokens(shape, seed, POOL, stream=7)
+    elif workload == "decode_t64":
+        d = k3synth.with_bias(d, np.zeros(shape.n_experts, np.float32))
+        x = k3synth.covering_tokens(shape, d, seed, T)
+    elif workload == "prefill_t4096":
+        d = k3synth.with_bias(d, k3synth.zipf_bias(shape, seed, layer_index, ZIPF_ALPHA))
+        x = k3synth.make_tokens(shape, seed, T, stream=11)
+    else:
+        x = k3synth.make_tokens(shape, seed, T, stream=13)
+    return shape, d, x
+
+
+class ClockSampler:
+    """nvidia-smi clock and throttle-reason samples during the timed region."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [v.strip() for v in ln.split(",")]
+            if len(f) < 7:
+                continue
+            try:
+                sm.append(float(f[0]))
+                smax = float(f[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def traffic_for(kernel, workload):
+    """DRAM bytes per launch of `kernel` from a committed ncu summary, if the
+    kernel's source is unchanged since the capture (else None)."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        table = json.load(f)
+    ent = table.get(f"{kernel}@{workload}")
+    if not ent:
+        return None
+    src = os.path.join(ROOT, "mxfp4_routed_expert_gb300", "csrc", ent["source"])
+    if not os.path.exists(src):
+        return None
+    with open(src, "rb") as f:
+        if hashlib.sha256(f.read()).hexdigest() != ent["sha256"]:
+            return None
+    return ent["bytes_per_launch"]
+
+
+# ---- oracle timing (CPU baseline and reference arm) ----------------------------------
+
+def time_oracle(shape, d, x, n_tokens):
+    import oracle
+    oracle.build()
+    rows = np.arange(min(n_tokens, x.shape[0]), dtype=np.int32)
+    t0 = time.perf_counter()
+    oracle.layer_forward(shape, d, x, rows=rows)
+    dt = time.perf_counter() - t0
+    return rows.size, dt
+
+
+def omp_threads(n_rows):
+    n = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    return max(1, min(n, n_rows))
+
+
+# ---- native arm ------------------------------------------------------------------------
+
+def run_native(args, rank, world):
+    import torch
+    import mxfp4_routed_expert_gb300 as km
+    from mxfp4_routed_expert_gb300 import build as kbuild
+    kbuild.build()
+    dev = int(os.environ.get("LOCAL_RANK", 0))
+    torch.cuda.set_device(dev)
+    wl = WORKLOADS[args.workload]
+    T, n_layers = wl["T"], wl["layers"]
+
+    shape, d0, xpool = make_inputs(args.workload)
+    h = km.k3moe_create(km.make_config(shape, max_layers=n_layers, max_tokens=T, device=dev))
+    w, keep = km.layer_weights(d0, shape.n_experts, km.K3MOE_HOST)
+    km.k3moe_load_layer(h, 0, w)
+    del keep
+    oracle_layer = d0
+    for li in range(1, n_layers):
+        _, dl, _ = make_inputs(args.workload, layer_index=li)
+        w, keep = km.layer_weights(dl, shape.n_experts, km.K3MOE_HOST)
+        km.k3moe_load_layer(h, li, w)
+        del keep, dl
+
+    xs = torch.from_numpy(xpool.view(np.int16).copy()).cuda()
+    npool = xs.shape[0] // T
+    y = torch.empty((T, shape.hidden), dtype=torch.int16, device="cuda")
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    counts_log = torch.empty((args.steps, shape.n_experts), dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def fwd(i):
+        xi = xs[(i % npool) * T:(i % npool) * T + T]
+        if n_layers > 1:
+            km.k3moe_forward_chain(h, 0, n_layers, xi, y, T, stream)
+        else:
+            km.k3moe_forward(h, 0, xi, y, T, stream)
+
+    for i in range(args.warmup):
+        flush.zero_()
+        fwd(i)
+    torch.cuda.synchronize()
+    assert km.k3moe_sync_status(h) == 0
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    clocks = ClockSampler(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    km.k3moe_set_profiling(h, True)
+    for i in range(args.steps):
+        flush.zero_()                      # L2 flush, outside the timed events
+        starts[i].record(stream)
+        fwd(args.warmup + i)
+        ends[i].record(stream)
+        km.k3moe_get_routing(h, counts=counts_log[i], stream=stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    stats = km.k3moe_profile_read(h)
+    km.k3moe_set_profiling(h, False)
+    st = km.k3moe_sync_status(h)
+    assert st == 0, km.strerror(st)
+    total_ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends))
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * T * args.steps / (total_ms / 1e3)
+
+    touched = (counts_log.cpu().numpy() > 0).sum(1)
+    n_touched = float(touched.mean())
+    hbm_peak, bf16_peak, peak_src = measured_peaks()
+    kb = kernel_bytes(shape, T, n_touched)
+    by_name = {n: (l, ms) for n, l, ms in stats}
+    ranked = sorted(((ms, n) for n, (l, ms) in by_name.items()), reverse=True)
+    dom = ranked[0][1]
+    launches, dom_ms = by_name[dom]
+    avg_ms = dom_ms / launches
+    if dom in kb:
+        alg = kb[dom] if n_layers == 1 else kb[dom]
+        achieved = alg / (avg_ms / 1e3) / 1e9
+        roof = {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1),
+                "peak": hbm_peak, "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
+                "traffic": traffic_for(dom, args.workload), "alg_bytes_per_launch": int(alg),
+                "avg_launch_ms": round(avg_ms, 5), "peak_source": f"{peak_src} hbm_gbs"}
+    else:
+        roof = {"kernel": dom, "bound": "hbm", "achieved": None, "peak": hbm_peak,
+                "unit": "GB/s", "frac": None, "traffic": None}
+    step_bytes = layer_bytes(shape, T, n_touched) * n_layers
+    layer_gbs = step_bytes / (ms_per_step / 1e3) / 1e9
+    kernels = {n: {"launches": l, "avg_ms": round(ms / l, 5),
+                   "share": round(ms / sum(m for _, m in by_name.values()), 4)}
+               for n, (l, ms) in by_name.items()}
+    gpu_launches = sum(l for l, _ in by_name.values())
+
+    # ---- e2e through the public host-buffer entry point --------------------------------
+    e2e = None
+    if n_layers == 1:
+        xh = torch.from_numpy(xpool.view(np.int16).copy()).pin_memory()
+        yh = torch.empty((T, shape.hidden), dtype=torch.int16).pin_memory()
+        for i in range(2):
+            km.k3moe_forward_host(h, 0, xh[(i % npool) * T:(i % npool) * T + T], yh, T, stream)
+        tot = 0.0
+        for i in range(args.steps):
+            flush.zero_()
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            km.k3moe_forward_host(h, 0, xh[(i % npool) * T:(i % npool) * T + T], yh, T, stream)
+            tot += time.perf_counter() - t0
+        e2e = {"value": round(world * T * args.steps / tot, 2), "unit": UNIT,
+               "h2d_bytes_per_step": T * shape.hidden * 2,
+               "d2h_bytes_per_step": T * shape.hidden * 2}
+
+    # ---- CPU baseline: the oracle on a bounded sample ---------------------------------------
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        n_tok = {1: 16, 64: 16, 4096: 16, 256: 16}[T]
+        xs_host = xpool if T == 1 else xpool[:T]
+        nrow, dt = time_oracle(shape, oracle_layer, xs_host, n_tok)
+        cpu = {"value": round(nrow / dt / n_layers, 4), "unit": UNIT,
+               "cores": omp_threads(nrow), "kind": "oracle",
+               "sample": f"{nrow} tokens of the workload through one layer (fp64 C oracle, "
+                         f"OpenMP over tokens), {dt:.1f} s"
+                         + ("; chain value = per-layer rate / 8" if n_layers > 1 else "")}
+    km.k3moe_destroy(h)
+    if rank != 0:
+        return None
+    return {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "mxfp4w-bf16a-f32acc",
+        "data": "synthetic (seeded K3-shape layer, random-init weights)",
+        "config": {"workload": args.workload, "description": wl["desc"], "tokens_per_step": T,
+                   "layers": n_layers, "hidden": shape.hidden, "latent": shape.latent,
+                   "n_experts": shape.n_experts, "topk": shape.topk,
+                   "moe_inter": shape.moe_inter, "shared_inter": shape.shared_inter,
+                   "parallelism": f"replicas x{world}",
+                   "l2": "256 MB flush between timed steps; working set > L2",
+                   "experts_touched_per_step": n_touched},
+        "hbm_gbs_layer": round(layer_gbs, 1), "hbm_frac_layer": round(layer_gbs / hbm_peak, 4),
+        "roofline": roof, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": gpu_launches, "clocks": clk,
+    }
+
+
+def run_reference(args, rank, world):
+    """The oracle as the reference arm: each step is the oracle on one bounded
+    sample of the workload (T=1: the whole step; larger T: 4 tokens)."""
+    wl = WORKLOADS[args.workload]
+    T, n_layers = wl["T"], wl["layers"]
+    shape, d, x = make_inputs(args.workload)
+    import oracle
+    oracle.build()
+    per = 1 if T == 1 else 4
+    for i in range(args.warmup):
+        oracle.layer_forward(shape, d, x, rows=np.array([i % x.shape[0]], np.int32))
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        rows = (np.arange(per) + i * per) % x.shape[0]
+        oracle.layer_forward(shape, d, x, rows=rows.astype(np.int32))
+    dt = time.perf_counter() - t0
+    value = per * args.steps / dt / n_layers
+    cores = omp_threads(per)
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded K3-shape layer, random-init weights)",
+        "config": {"workload": args.workload, "description": wl["desc"],
+                   "tokens_per_step": T, "layers": n_layers},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "kind": "oracle",
+                         "cores": cores,
+                         "sample": f"{per} token(s) per step through one layer (fp64 C oracle)"
+                                   + ("; chain value = per-layer rate / 8" if n_layers > 1 else "")},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--workload", choices=list(WORKLOADS), default="decode_t1")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        print(json.dumps(run_reference(args, rank, world)), flush=True)
+        return
+    if world > 1:
+        import torch
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        torch.distributed.init_process_group("nccl")
+    out = run_native(args, rank, world)
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+    if out is not None:
+        print(json.dumps(out), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,196 @@
+/*
+ * k3moe: the Kimi K3 LatentMoE routed-expert layer on one GB300 (sm_103a).
+ *
+ * C ABI of libk3moe.so. Plain pointers and sizes only.
+ *
+ * What one layer computes (kimi-k3-in-c README, Part II section 9 "Picking 16
+ * experts of 896", k3_router and k3_moe; colibri docs/kimi_k3.md, "Stable
+ * LatentMoE"), for every token x (a row of x[T, hidden]):
+ *   1. router: logit_e = x . Wr_e, sc_e = sigmoid(logit_e), ch_e = sc_e + bias_e;
+ *      the topk experts with the largest ch (equal ch: lower id first) are
+ *      picked and weighted by their UNBIASED sc, renormalised to sum 1 (when
+ *      renorm is set) and multiplied by routed_scale;
+ *   2. z = Wdown . x                                   (hidden -> latent);
+ *   3. acc = sum_j w_j * W2_e(SiTU(W1_e z, W3_e z))    over the picked experts,
+ *      whose weights are MXFP4 (README section 4: e2m1 nibbles, two per byte,
+ *      low nibble = even column, bit 3 = sign, one ue8m0 scale per 32 columns,
+ *      w = v * 2^(scale - 127)) and are used as stored, never re-encoded;
+ *   4. n = RMSNorm(acc) * latent_gain                  (norm of the aggregate);
+ *   5. y = Wup . n + Ws2 . SiTU(Ws1 x, Ws3 x)          (shared experts on the
+ *      original x, added unweighted);
+ *   SiTU(g, u) = b1*tanh(g/b1)*sigmoid(g) * b2*tanh(u/b2).
+ *
+ * Conventions (taken from the README's engine): refuse rather than guess a
+ * missing configuration value; never drop an expert silently; never leave a
+ * half-built state behind after an error.
+ *
+ * All entry points return 0 (K3MOE_OK) or a negative K3MOE_ERR_* code.
+ * Errors found on the host are returned immediately. Errors found by a kernel
+ * (an index out of range, a bounded wait that ran out) are latched in a device
+ * word and returned by k3moe_sync_status.
+ *
+ * Threading: a handle may be used by one host thread at a time.
+ */
+#ifndef K3MOE_H
+#define K3MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define K3MOE_ABI_VERSION 1
+
+#if defined(__GNUC__)
+#define K3MOE_API __attribute__((visibility("default")))
+#else
+#define K3MOE_API
+#endif
+
+enum {
+    K3MOE_OK = 0,
+    K3MOE_ERR_INVALID_ARG = -1,   /* NULL handle/pointer, bad layer index, T out of range */
+    K3MOE_ERR_CONFIG = -2,        /* a configuration field is missing (0), NaN or negative */
+    K3MOE_ERR_SHAPE = -3,         /* sizes the kernels do not support (see k3moe_config) */
+    K3MOE_ERR_OOM = -4,           /* not enough free device memory; nothing was allocated */
+    K3MOE_ERR_BAD_SCALE = -5,     /* an expert holds scale byte 255 (NaN in MX); layer not loaded */
+    K3MOE_ERR_NOT_LOADED = -6,    /* forward on a layer that was never loaded */
+    K3MOE_ERR_CUDA = -7,          /* a CUDA runtime call failed */
+    K3MOE_ERR_TIMEOUT = -8,       /* a device-side bounded wait gave up */
+    K3MOE_ERR_DEVICE = -9         /* a device-side index check failed */
+};
+
+/* Where the pointees of a k3moe_layer_weights live. */
+enum { K3MOE_HOST = 0, K3MOE_DEVICE = 1 };
+
+typedef struct k3moe k3moe;
+
+/* Layer configuration (the MoE fields of the README's K3Cfg). Every field is
+ * required: a zero, negative or NaN value returns K3MOE_ERR_CONFIG, except the
+ * two flags, which must be 0 or 1.
+ * Supported sizes (else K3MOE_ERR_SHAPE): hidden, latent, moe_inter and
+ * shared_inter multiples of 64; 1 <= topk <= 32; topk <= n_experts <= 1024;
+ * max_tokens <= 65536 / topk.
+ * K3: hidden 7168, latent 3584, n_experts 896, topk 16, moe_inter 3072,
+ * shared_inter 6144 (two shared experts fused), rms_eps 1e-5, situ_b1 4,
+ * situ_b2 25, routed_scale 1, renorm 1, latent_norm 1. */
+typedef struct {
+    uint32_t struct_size;   /* sizeof(k3moe_config), checked */
+    int32_t hidden;         /* H: width of x and y */
+    int32_t latent;         /* L: expert latent width */
+    int32_t n_experts;      /* E: routed experts */
+    int32_t topk;           /* k: experts per token */
+    int32_t moe_inter;      /* I: routed expert inner width */
+    int32_t shared_inter;   /* S: fused shared-expert inner width */
+    int32_t max_layers;     /* layers this handle can hold */
+    int32_t max_tokens;     /* largest T of one forward (sizes the workspace) */
+    int32_t device;         /* CUDA device ordinal */
+    int32_t renorm;         /* 1: renormalise the picked weights to sum 1 */
+    int32_t latent_norm;    /* 1: RMSNorm the aggregate with latent_gain */
+    float rms_eps;          /* eps inside the square root of RMSNorm */
+    float situ_b1;          /* SiTU gate cap */
+    float situ_b2;          /* SiTU up cap */
+    float routed_scale;     /* multiplies the routed weights */
+} k3moe_config;
+
+/* One layer's weights in the checkpoint layout (row = output, row-major).
+ * bf16 tensors are raw bfloat16 bit patterns. The six expert arrays hold one
+ * pointer per expert (E entries each; the arrays themselves are host memory);
+ * the pointees, like every other pointer here, live where `where` says.
+ * Bytes are copied unchanged into library-owned device memory. */
+typedef struct {
+    uint32_t struct_size;          /* sizeof(k3moe_layer_weights), checked */
+    int32_t where;                 /* K3MOE_HOST or K3MOE_DEVICE */
+    const void *router_w;          /* bf16 [E, H] */
+    const float *router_bias;      /* fp32 [E]; NULL means no bias */
+    const void *down_w;            /* bf16 [L, H] */
+    const void *up_w;              /* bf16 [H, L] */
+    const void *latent_gain;       /* bf16 [L]; required when latent_norm = 1 */
+    const void *shared_w1;         /* bf16 [S, H] (gate) */
+    const void *shared_w3;         /* bf16 [S, H] (up) */
+    const void *shared_w2;         /* bf16 [H, S] */
+    const uint8_t *const *w1_packed;  /* [E] -> [I, L/2] e2m1 pairs (gate) */
+    const uint8_t *const *w1_scale;   /* [E] -> [I, L/32] ue8m0 */
+    const uint8_t *const *w3_packed;  /* [E] -> [I, L/2] (up) */
+    const uint8_t *const *w3_scale;   /* [E] -> [I, L/32] */
+    const uint8_t *const *w2_packed;  /* [E] -> [L, I/2] (down, back to the latent) */
+    const uint8_t *const *w2_scale;   /* [E] -> [L, I/32] */
+} k3moe_layer_weights;
+
+/* Creates a handle on cfg->device and allocates its workspace (sized by
+ * max_tokens). On error *out is NULL and nothing stays allocated. */
+K3MOE_API int k3moe_create(const k3moe_config *cfg, k3moe **out);
+
+/* Copies one layer's weights to the device (synchronous). Free device memory
+ * is checked against the whole layer before anything is allocated
+ * (K3MOE_ERR_OOM). Every scale byte is checked: 255 returns
+ * K3MOE_ERR_BAD_SCALE and the layer stays unloaded. Reloading a slot replaces
+ * it. layer is in [0, max_layers). */
+K3MOE_API int k3moe_load_layer(k3moe *h, int layer, const k3moe_layer_weights *w);
+
+/* One layer on T tokens: x [T, H] bf16 -> y [T, H] bf16, both device pointers
+ * (x and y must not overlap). Asynchronous on `stream` (a cudaStream_t; NULL
+ * is the legacy default stream). 1 <= T <= max_tokens. The routing of the
+ * call stays readable through k3moe_get_routing until the next forward. */
+K3MOE_API int k3moe_forward(k3moe *h, int layer, const void *x, void *y, int T, void *stream);
+
+/* Layers first_layer .. first_layer + n_layers - 1 applied in sequence, with
+ * x_next = bf16(RMSNorm(y) with unit gain and rms_eps) between two layers.
+ * x, y: device [T, H] bf16. The routing of the last layer stays readable. */
+K3MOE_API int k3moe_forward_chain(k3moe *h, int first_layer, int n_layers, const void *x, void *y,
+                        int T, void *stream);
+
+/* k3moe_forward with HOST buffers: copies x to the device, runs the layer,
+ * copies y back and synchronises `stream`. Pinned host memory is faster but
+ * not required. */
+K3MOE_API int k3moe_forward_host(k3moe *h, int layer, const void *x_host, void *y_host, int T,
+                       void *stream);
+
+/* Copies the routing of the last forward into caller-owned device buffers
+ * (any may be NULL), asynchronously on `stream`:
+ *   ids [T, k] int32 and w [T, k] fp32, slot j in descending ch order;
+ *   counts [E] int32; offsets [E+1] int32 (exclusive prefix sum of counts);
+ *   perm [T*k] int32: flat pair indices t*k+j grouped by expert (ascending),
+ *   and by ascending token inside an expert. */
+K3MOE_API int k3moe_get_routing(k3moe *h, int32_t *ids, float *w, int32_t *counts, int32_t *offsets,
+                      int32_t *perm, void *stream);
+
+/* Intermediates of the last forward, for parity diagnosis. Copies `bytes`
+ * bytes (at most the tensor's size for the last T) into caller device memory.
+ *   K3MOE_T_Z       fp32 [T, L]   latent down projection
+ *   K3MOE_T_ACC     fp32 [T, L]   weighted sum of expert outputs (before the norm)
+ *   K3MOE_T_SHARED  fp32 [T, S]   SiTU of the shared experts
+ *   K3MOE_T_LOGITS  fp32 [T, E]   router logits */
+enum { K3MOE_T_Z = 1, K3MOE_T_ACC = 2, K3MOE_T_SHARED = 3, K3MOE_T_LOGITS = 4 };
+K3MOE_API int k3moe_get_intermediate(k3moe *h, int which, void *dst, size_t bytes, void *stream);
+
+/* Synchronises the device and returns (then clears) the first latched
+ * device-side error, or the first asynchronous CUDA error. */
+K3MOE_API int k3moe_sync_status(k3moe *h);
+
+/* Per-kernel timing: with profiling on, every kernel a forward launches is
+ * bracketed by CUDA events on the launching stream. k3moe_profile_read
+ * synchronises, aggregates per kernel name and resets the record. */
+typedef struct {
+    char name[48];        /* kernel name */
+    int32_t launches;     /* launches recorded */
+    double total_ms;      /* sum of event-timed durations */
+} k3moe_kernel_stat;
+K3MOE_API int k3moe_set_profiling(k3moe *h, int enable);
+K3MOE_API int k3moe_profile_read(k3moe *h, k3moe_kernel_stat *out, int max_entries, int *n_entries);
+
+/* Frees every device allocation of the handle. NULL is ignored. */
+K3MOE_API void k3moe_destroy(k3moe *h);
+
+/* Static description of a return code. */
+K3MOE_API const char *k3moe_strerror(int code);
+
+/* K3MOE_ABI_VERSION of the library. */
+K3MOE_API int k3moe_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* K3MOE_H */

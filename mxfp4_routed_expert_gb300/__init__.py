@@ -1,0 +1,260 @@
+"""Python binding of libk3moe (the Kimi K3 LatentMoE layer on GB300).
+
+Argument marshalling only: every step of the layer runs in the library's CUDA
+kernels. The functions carry the C names of include/k3moe.h. Device pointers
+may be given as integers or as torch tensors (their data_ptr is used); the
+stream as an integer handle, a torch.cuda.Stream, or None (the legacy default
+stream).
+
+Loading fails loudly when libk3moe.so has not been built: there is no CPU or
+PyTorch fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libk3moe.so")
+
+K3MOE_OK = 0
+K3MOE_ERR_INVALID_ARG = -1
+K3MOE_ERR_CONFIG = -2
+K3MOE_ERR_SHAPE = -3
+K3MOE_ERR_OOM = -4
+K3MOE_ERR_BAD_SCALE = -5
+K3MOE_ERR_NOT_LOADED = -6
+K3MOE_ERR_CUDA = -7
+K3MOE_ERR_TIMEOUT = -8
+K3MOE_ERR_DEVICE = -9
+K3MOE_HOST, K3MOE_DEVICE = 0, 1
+K3MOE_T_Z, K3MOE_T_ACC, K3MOE_T_SHARED, K3MOE_T_LOGITS = 1, 2, 3, 4
+
+# Every symbol include/k3moe.h declares.
+EXPORTS = ("k3moe_create", "k3moe_load_layer", "k3moe_forward", "k3moe_forward_chain",
+           "k3moe_forward_host", "k3moe_get_routing", "k3moe_get_intermediate",
+           "k3moe_sync_status", "k3moe_set_profiling", "k3moe_profile_read", "k3moe_destroy",
+           "k3moe_strerror", "k3moe_abi_version")
+
+
+class K3MoEError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {strerror(code)} ({code})")
+
+
+class k3moe_config(ctypes.Structure):
+    _fields_ = [("struct_size", ctypes.c_uint32), ("hidden", ctypes.c_int32),
+                ("latent", ctypes.c_int32), ("n_experts", ctypes.c_int32),
+                ("topk", ctypes.c_int32), ("moe_inter", ctypes.c_int32),
+                ("shared_inter", ctypes.c_int32), ("max_layers", ctypes.c_int32),
+                ("max_tokens", ctypes.c_int32), ("device", ctypes.c_int32),
+                ("renorm", ctypes.c_int32), ("latent_norm", ctypes.c_int32),
+                ("rms_eps", ctypes.c_float), ("situ_b1", ctypes.c_float),
+                ("situ_b2", ctypes.c_float), ("routed_scale", ctypes.c_float)]
+
+
+_PP = ctypes.POINTER(ctypes.c_void_p)
+
+
+class k3moe_layer_weights(ctypes.Structure):
+    _fields_ = [("struct_size", ctypes.c_uint32), ("where", ctypes.c_int32),
+                ("router_w", ctypes.c_void_p), ("router_bias", ctypes.c_void_p),
+                ("down_w", ctypes.c_void_p), ("up_w", ctypes.c_void_p),
+                ("latent_gain", ctypes.c_void_p), ("shared_w1", ctypes.c_void_p),
+                ("shared_w3", ctypes.c_void_p), ("shared_w2", ctypes.c_void_p),
+                ("w1_packed", _PP), ("w1_scale", _PP), ("w3_packed", _PP), ("w3_scale", _PP),
+                ("w2_packed", _PP), ("w2_scale", _PP)]
+
+
+class k3moe_kernel_stat(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char * 48), ("launches", ctypes.c_int32),
+                ("total_ms", ctypes.c_double)]
+
+
+_lib = None
+
+
+def lib():
+    """The loaded libk3moe.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -m mxfp4_routed_expert_gb300.build` (no fallback exists)")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        L.k3moe_create.argtypes = [ctypes.POINTER(k3moe_config), ctypes.POINTER(vp)]
+        L.k3moe_load_layer.argtypes = [vp, i, ctypes.POINTER(k3moe_layer_weights)]
+        L.k3moe_forward.argtypes = [vp, i, vp, vp, i, vp]
+        L.k3moe_forward_chain.argtypes = [vp, i, i, vp, vp, i, vp]
+        L.k3moe_forward_host.argtypes = [vp, i, vp, vp, i, vp]
+        L.k3moe_get_routing.argtypes = [vp, vp, vp, vp, vp, vp, vp]
+        L.k3moe_get_intermediate.argtypes = [vp, i, vp, sz, vp]
+        L.k3moe_sync_status.argtypes = [vp]
+        L.k3moe_set_profiling.argtypes = [vp, i]
+        L.k3moe_profile_read.argtypes = [vp, ctypes.POINTER(k3moe_kernel_stat), i,
+                                         ctypes.POINTER(ctypes.c_int)]
+        L.k3moe_destroy.argtypes = [vp]
+        L.k3moe_destroy.restype = None
+        L.k3moe_strerror.argtypes = [i]
+        L.k3moe_strerror.restype = ctypes.c_char_p
+        L.k3moe_abi_version.restype = i
+        for n in EXPORTS:
+            if n not in ("k3moe_destroy", "k3moe_strerror"):
+                getattr(L, n).restype = i if n != "k3moe_destroy" else None
+        _lib = L
+    return _lib
+
+
+def strerror(code: int) -> str:
+    return lib().k3moe_strerror(int(code)).decode()
+
+
+def _ptr(v):
+    if v is None:
+        return None
+    if isinstance(v, int):
+        return ctypes.c_void_p(v)
+    if hasattr(v, "data_ptr"):
+        return ctypes.c_void_p(v.data_ptr())
+    if isinstance(v, np.ndarray):
+        return ctypes.c_void_p(v.ctypes.data)
+    raise TypeError(f"cannot pass {type(v)} as a pointer")
+
+
+def _stream(s):
+    if s is None:
+        return None
+    if isinstance(s, int):
+        return ctypes.c_void_p(s)
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(rc: int, what: str) -> int:
+    if rc != K3MOE_OK:
+        raise K3MoEError(rc, what)
+    return rc
+
+
+def make_config(shape, max_layers: int = 1, max_tokens: int = 1, device: int = 0,
+                latent_norm: int = 1) -> k3moe_config:
+    """k3moe_config from a layer shape (any object with the K3Cfg field names)."""
+    c = k3moe_config()
+    c.struct_size = ctypes.sizeof(k3moe_config)
+    c.hidden, c.latent, c.n_experts = shape.hidden, shape.latent, shape.n_experts
+    c.topk, c.moe_inter, c.shared_inter = shape.topk, shape.moe_inter, shape.shared_inter
+    c.max_layers, c.max_tokens, c.device = max_layers, max_tokens, device
+    c.renorm, c.latent_norm = int(shape.renorm), int(latent_norm)
+    c.rms_eps, c.situ_b1, c.situ_b2 = shape.rms_eps, shape.situ_b1, shape.situ_b2
+    c.routed_scale = shape.routed_scale
+    return c
+
+
+def k3moe_create(cfg: k3moe_config) -> int:
+    h = ctypes.c_void_p()
+    _check(lib().k3moe_create(ctypes.byref(cfg), ctypes.byref(h)), "k3moe_create")
+    return h.value
+
+
+def k3moe_destroy(h: int) -> None:
+    lib().k3moe_destroy(ctypes.c_void_p(h))
+
+
+def layer_weights(tensors: dict, n_experts: int, where: int = K3MOE_HOST):
+    """k3moe_layer_weights pointing into `tensors` (numpy arrays for HOST, torch
+    CUDA tensors for DEVICE) in the checkpoint layout; expert arrays are
+    [E, rows, cols] and are split into per-expert pointers. Returns the struct
+    and the objects that must stay alive while it is used."""
+    keep = []
+
+    def addr(v):
+        if v is None:
+            return None
+        if isinstance(v, np.ndarray):
+            assert v.flags["C_CONTIGUOUS"]
+            return v.ctypes.data
+        assert v.is_contiguous()
+        return v.data_ptr()
+
+    def per_expert(v):
+        base = addr(v)
+        stride = (v.nbytes if isinstance(v, np.ndarray) else v.numel() * v.element_size()) // n_experts
+        arr = (ctypes.c_void_p * n_experts)(*[base + e * stride for e in range(n_experts)])
+        keep.append(arr)
+        return ctypes.cast(arr, _PP)
+
+    w = k3moe_layer_weights()
+    w.struct_size = ctypes.sizeof(k3moe_layer_weights)
+    w.where = where
+    w.router_w = addr(tensors["router_w"])
+    w.router_bias = addr(tensors.get("router_bias"))
+    w.down_w = addr(tensors["down_w"])
+    w.up_w = addr(tensors["up_w"])
+    w.latent_gain = addr(tensors.get("latent_gain"))
+    w.shared_w1 = addr(tensors["sh_w1"])
+    w.shared_w3 = addr(tensors["sh_w3"])
+    w.shared_w2 = addr(tensors["sh_w2"])
+    w.w1_packed, w.w1_scale = per_expert(tensors["w1p"]), per_expert(tensors["w1s"])
+    w.w3_packed, w.w3_scale = per_expert(tensors["w3p"]), per_expert(tensors["w3s"])
+    w.w2_packed, w.w2_scale = per_expert(tensors["w2p"]), per_expert(tensors["w2s"])
+    keep.append(tensors)
+    return w, keep
+
+
+def k3moe_load_layer(h: int, layer: int, weights: k3moe_layer_weights) -> int:
+    return _check(lib().k3moe_load_layer(ctypes.c_void_p(h), layer, ctypes.byref(weights)),
+                  "k3moe_load_layer")
+
+
+def k3moe_forward(h: int, layer: int, x, y, T: int, stream=None) -> int:
+    return _check(lib().k3moe_forward(ctypes.c_void_p(h), layer, _ptr(x), _ptr(y), T,
+                                      _stream(stream)), "k3moe_forward")
+
+
+def k3moe_forward_chain(h: int, first_layer: int, n_layers: int, x, y, T: int, stream=None) -> int:
+    return _check(lib().k3moe_forward_chain(ctypes.c_void_p(h), first_layer, n_layers, _ptr(x),
+                                            _ptr(y), T, _stream(stream)), "k3moe_forward_chain")
+
+
+def k3moe_forward_host(h: int, layer: int, x_host, y_host, T: int, stream=None) -> int:
+    return _check(lib().k3moe_forward_host(ctypes.c_void_p(h), layer, _ptr(x_host),
+                                           _ptr(y_host), T, _stream(stream)),
+                  "k3moe_forward_host")
+
+
+def k3moe_get_routing(h: int, ids=None, w=None, counts=None, offsets=None, perm=None,
+                      stream=None) -> int:
+    return _check(lib().k3moe_get_routing(ctypes.c_void_p(h), _ptr(ids), _ptr(w), _ptr(counts),
+                                          _ptr(offsets), _ptr(perm), _stream(stream)),
+                  "k3moe_get_routing")
+
+
+def k3moe_get_intermediate(h: int, which: int, dst, nbytes: int, stream=None) -> int:
+    return _check(lib().k3moe_get_intermediate(ctypes.c_void_p(h), which, _ptr(dst), nbytes,
+                                               _stream(stream)), "k3moe_get_intermediate")
+
+
+def k3moe_sync_status(h: int) -> int:
+    return lib().k3moe_sync_status(ctypes.c_void_p(h))
+
+
+def k3moe_set_profiling(h: int, enable: bool) -> int:
+    return _check(lib().k3moe_set_profiling(ctypes.c_void_p(h), int(bool(enable))),
+                  "k3moe_set_profiling")
+
+
+def k3moe_profile_read(h: int, max_entries: int = 32):
+    """[(name, launches, total_ms)] since the last read."""
+    arr = (k3moe_kernel_stat * max_entries)()
+    n = ctypes.c_int(0)
+    _check(lib().k3moe_profile_read(ctypes.c_void_p(h), arr, max_entries, ctypes.byref(n)),
+           "k3moe_profile_read")
+    return [(arr[i].name.decode(), arr[i].launches, arr[i].total_ms)
+            for i in range(min(n.value, max_entries))]
+
+
+def k3moe_abi_version() -> int:
+    return lib().k3moe_abi_version()

@@ -1,0 +1,545 @@
+// Host side of the C ABI declared in include/k3moe.h: argument and
+// configuration checks, device allocation, weight loading and validation, the
+// launch sequence of one layer, routing/intermediate readback and timing.
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <new>
+#include <string>
+
+#include "k3moe_internal.cuh"
+
+using namespace k3;
+
+namespace {
+
+size_t al256(size_t n) { return (n + 255) & ~size_t(255); }
+
+int check_config(const k3moe_config *c)
+{
+    if (!c) return K3MOE_ERR_INVALID_ARG;
+    if (c->struct_size != sizeof(k3moe_config)) return K3MOE_ERR_CONFIG;
+    const int32_t pos[] = {c->hidden, c->latent, c->n_experts, c->topk, c->moe_inter,
+                           c->shared_inter, c->max_layers, c->max_tokens};
+    for (int32_t v : pos)
+        if (v <= 0) return K3MOE_ERR_CONFIG;
+    if (c->device < 0) return K3MOE_ERR_CONFIG;
+    if ((c->renorm != 0 && c->renorm != 1) || (c->latent_norm != 0 && c->latent_norm != 1))
+        return K3MOE_ERR_CONFIG;
+    const float fl[] = {c->rms_eps, c->situ_b1, c->situ_b2, c->routed_scale};
+    for (float v : fl)
+        if (!std::isfinite(v) || v <= 0.f) return K3MOE_ERR_CONFIG;
+    if (c->hidden % 64 || c->latent % 64 || c->moe_inter % 64 || c->shared_inter % 64)
+        return K3MOE_ERR_SHAPE;
+    if (c->topk > kMaxTopk || c->topk > c->n_experts || c->n_experts > kMaxExperts)
+        return K3MOE_ERR_SHAPE;
+    if (c->latent > 4096 || c->moe_inter > 8192) return K3MOE_ERR_SHAPE;
+    if ((long long)c->max_tokens * c->topk > 65536) return K3MOE_ERR_SHAPE;
+    // fp16 partial sums in the expert GEMVs: |SiTU| <= b1*b2 must stay small
+    if ((double)c->situ_b1 * c->situ_b2 > 512.0) return K3MOE_ERR_SHAPE;
+    return K3MOE_OK;
+}
+
+struct Carve {
+    char *base;
+    size_t off = 0;
+    template <typename T>
+    T *take(size_t count)
+    {
+        T *p = reinterpret_cast<T *>(base ? base + off : nullptr);
+        off += al256(count * sizeof(T));
+        return p;
+    }
+};
+
+// Lays out the workspace; with base == nullptr only measures it.
+size_t carve_workspace(const k3moe_config &c, char *base, Workspace *ws)
+{
+    const size_t Tm = (size_t)c.max_tokens, E = c.n_experts, L = c.latent, S = c.shared_inter;
+    const size_t H = c.hidden, K = c.topk, I = c.moe_inter;
+    Carve cv{base};
+    Workspace w;
+    w.logits = cv.take<float>(Tm * E);
+    w.z = cv.take<float>(Tm * L);
+    w.z16 = cv.take<__half>(Tm * L);
+    w.zexp = cv.take<int>(Tm);
+    w.cat = cv.take<float>(Tm * (L + S));
+    w.ids = cv.take<int>(Tm * K);
+    w.wts = cv.take<float>(Tm * K);
+    w.counts = cv.take<int>(E);
+    w.offsets = cv.take<int>(E + 1);
+    w.perm = cv.take<int>(Tm * K);
+    w.touched = cv.take<int>(E);
+    w.n_touched = cv.take<int>(1);
+    w.h16 = cv.take<__half>(Tm * K * I);
+    w.acc = cv.take<float>(Tm * L);
+    w.xbuf0 = cv.take<__nv_bfloat16>(Tm * H);
+    w.xbuf1 = cv.take<__nv_bfloat16>(Tm * H);
+    w.err = cv.take<int>(4);
+    w.block = base;
+    w.bytes = cv.off;
+    if (ws) *ws = w;
+    return cv.off;
+}
+
+struct LayerSizes {
+    size_t router, bias, down, up, gain, sh13, sh2, e13p, e13s, e2p, e2s;
+    size_t total;
+};
+
+LayerSizes layer_sizes(const k3moe_config &c)
+{
+    const size_t E = c.n_experts, H = c.hidden, L = c.latent, S = c.shared_inter, I = c.moe_inter;
+    LayerSizes z;
+    z.router = E * H * 2;
+    z.bias = E * 4;
+    z.down = L * H * 2;
+    z.up = H * L * 2;
+    z.gain = L * 2;
+    z.sh13 = S * H * 2;
+    z.sh2 = H * S * 2;
+    z.e13p = E * I * (L / 2);
+    z.e13s = E * I * (L / kGroup);
+    z.e2p = E * L * (I / 2);
+    z.e2s = E * L * (I / kGroup);
+    z.total = al256(z.router) + al256(z.bias) + al256(z.down) + al256(z.up) + al256(z.gain) +
+              2 * al256(z.sh13) + al256(z.sh2) + 2 * al256(z.e13p) + 2 * al256(z.e13s) +
+              al256(z.e2p) + al256(z.e2s);
+    return z;
+}
+
+cudaEvent_t get_event(k3moe *h)
+{
+    if (!h->event_pool.empty()) {
+        cudaEvent_t e = h->event_pool.back();
+        h->event_pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    cudaEventCreate(&e);
+    return e;
+}
+
+// Brackets one kernel launch with events when profiling is on.
+struct Prof {
+    k3moe *h;
+    const char *name;
+    cudaStream_t s;
+    cudaEvent_t a = nullptr;
+    Prof(k3moe *h_, const char *n, cudaStream_t s_) : h(h_), name(n), s(s_)
+    {
+        if (h->profiling) {
+            a = get_event(h);
+            cudaEventRecord(a, s);
+        }
+    }
+    ~Prof()
+    {
+        if (a) {
+            cudaEvent_t b = get_event(h);
+            cudaEventRecord(b, s);
+            h->prof.push_back({name, a, b});
+        }
+    }
+};
+
+int run_layer(k3moe *h, const LayerDev &w, const __nv_bfloat16 *x, __nv_bfloat16 *y, int T,
+              cudaStream_t s)
+{
+    cudaError_t e;
+#define K3_STEP(name, call)                        \
+    {                                              \
+        Prof p_(h, name, s);                       \
+        e = (call);                                \
+    }                                              \
+    if (e != cudaSuccess) return K3MOE_ERR_CUDA;
+    K3_STEP("dense_x_gemv", launch_dense_x(*h, w, x, T, s));
+    K3_STEP("route_topk", launch_route(*h, w, T, s));
+    K3_STEP("permute", launch_perm(*h, T, s));
+    K3_STEP("expert_w13_gemv", launch_expert_w13(*h, w, T, s));
+    K3_STEP("expert_w2_gemv", launch_expert_w2(*h, w, T, s));
+    K3_STEP("latent_rmsnorm", launch_latent_norm(*h, w, T, s));
+    K3_STEP("up_shared_gemv", launch_up(*h, w, y, T, s));
+#undef K3_STEP
+    h->last_T = T;
+    return K3MOE_OK;
+}
+
+bool overlap(const void *a, size_t na, const void *b, size_t nb)
+{
+    const char *pa = (const char *)a, *pb = (const char *)b;
+    return pa < pb + nb && pb < pa + na;
+}
+
+void free_layer(LayerDev &l)
+{
+    if (l.block) cudaFree(l.block);
+    l = LayerDev();
+}
+
+}  // namespace
+
+extern "C" {
+
+int k3moe_abi_version(void) { return K3MOE_ABI_VERSION; }
+
+const char *k3moe_strerror(int code)
+{
+    switch (code) {
+    case K3MOE_OK: return "ok";
+    case K3MOE_ERR_INVALID_ARG: return "invalid argument";
+    case K3MOE_ERR_CONFIG: return "configuration field missing or invalid";
+    case K3MOE_ERR_SHAPE: return "unsupported layer shape";
+    case K3MOE_ERR_OOM: return "not enough device memory";
+    case K3MOE_ERR_BAD_SCALE: return "expert scale byte 255 (NaN) found";
+    case K3MOE_ERR_NOT_LOADED: return "layer not loaded";
+    case K3MOE_ERR_CUDA: return "CUDA runtime error";
+    case K3MOE_ERR_TIMEOUT: return "device-side wait timed out";
+    case K3MOE_ERR_DEVICE: return "device-side index check failed";
+    default: return "unknown error";
+    }
+}
+
+int k3moe_create(const k3moe_config *cfg, k3moe **out)
+{
+    if (!out) return K3MOE_ERR_INVALID_ARG;
+    *out = nullptr;
+    const int rc = check_config(cfg);
+    if (rc != K3MOE_OK) return rc;
+    int ndev = 0;
+    if (cudaGetDeviceCount(&ndev) != cudaSuccess || cfg->device >= ndev) return K3MOE_ERR_CUDA;
+    if (cudaSetDevice(cfg->device) != cudaSuccess) return K3MOE_ERR_CUDA;
+    k3moe *h = new (std::nothrow) k3moe();
+    if (!h) return K3MOE_ERR_OOM;
+    h->cfg = *cfg;
+    cudaDeviceGetAttribute(&h->sm_count, cudaDevAttrMultiProcessorCount, cfg->device);
+    const size_t need = carve_workspace(*cfg, nullptr, nullptr);
+    size_t fr = 0, tot = 0;
+    if (cudaMemGetInfo(&fr, &tot) != cudaSuccess) {
+        delete h;
+        return K3MOE_ERR_CUDA;
+    }
+    if (need + (64u << 20) > fr) {
+        delete h;
+        return K3MOE_ERR_OOM;
+    }
+    void *blk = nullptr;
+    if (cudaMalloc(&blk, need) != cudaSuccess) {
+        cudaGetLastError();
+        delete h;
+        return K3MOE_ERR_OOM;
+    }
+    carve_workspace(*cfg, (char *)blk, &h->ws);
+    if (cudaMemset(blk, 0, need) != cudaSuccess) {
+        cudaFree(blk);
+        delete h;
+        return K3MOE_ERR_CUDA;
+    }
+    h->layers.resize((size_t)cfg->max_layers);
+    *out = h;
+    return K3MOE_OK;
+}
+
+void k3moe_destroy(k3moe *h)
+{
+    if (!h) return;
+    cudaSetDevice(h->cfg.device);
+    for (auto &l : h->layers) free_layer(l);
+    if (h->ws.block) cudaFree(h->ws.block);
+    for (auto &r : h->prof) {
+        cudaEventDestroy(r.a);
+        cudaEventDestroy(r.b);
+    }
+    for (auto e : h->event_pool) cudaEventDestroy(e);
+    delete h;
+}
+
+int k3moe_load_layer(k3moe *h, int layer, const k3moe_layer_weights *w)
+{
+    if (!h || !w) return K3MOE_ERR_INVALID_ARG;
+    if (w->struct_size != sizeof(k3moe_layer_weights)) return K3MOE_ERR_INVALID_ARG;
+    if (layer < 0 || layer >= h->cfg.max_layers) return K3MOE_ERR_INVALID_ARG;
+    if (w->where != K3MOE_HOST && w->where != K3MOE_DEVICE) return K3MOE_ERR_INVALID_ARG;
+    const k3moe_config &c = h->cfg;
+    if (!w->router_w || !w->down_w || !w->up_w || !w->shared_w1 || !w->shared_w3 ||
+        !w->shared_w2 || !w->w1_packed || !w->w1_scale || !w->w3_packed || !w->w3_scale ||
+        !w->w2_packed || !w->w2_scale)
+        return K3MOE_ERR_INVALID_ARG;
+    if (c.latent_norm && !w->latent_gain) return K3MOE_ERR_INVALID_ARG;
+    for (int e = 0; e < c.n_experts; e++)
+        if (!w->w1_packed[e] || !w->w1_scale[e] || !w->w3_packed[e] || !w->w3_scale[e] ||
+            !w->w2_packed[e] || !w->w2_scale[e])
+            return K3MOE_ERR_INVALID_ARG;
+    if (cudaSetDevice(c.device) != cudaSuccess) return K3MOE_ERR_CUDA;
+
+    const LayerSizes z = layer_sizes(c);
+    size_t fr = 0, tot = 0;
+    if (cudaMemGetInfo(&fr, &tot) != cudaSuccess) return K3MOE_ERR_CUDA;
+    if (z.total + (256u << 20) > fr) return K3MOE_ERR_OOM;   // checked before any allocation
+    void *blk = nullptr;
+    if (cudaMalloc(&blk, z.total) != cudaSuccess) {
+        cudaGetLastError();
+        return K3MOE_ERR_OOM;
+    }
+    LayerDev L;
+    L.block = blk;
+    L.bytes = z.total;
+    Carve cv{(char *)blk};
+    __nv_bfloat16 *router = cv.take<__nv_bfloat16>(z.router / 2);
+    float *bias = cv.take<float>(z.bias / 4);
+    __nv_bfloat16 *down = cv.take<__nv_bfloat16>(z.down / 2);
+    __nv_bfloat16 *up = cv.take<__nv_bfloat16>(z.up / 2);
+    __nv_bfloat16 *gain = cv.take<__nv_bfloat16>(z.gain / 2);
+    __nv_bfloat16 *sh1 = cv.take<__nv_bfloat16>(z.sh13 / 2);
+    __nv_bfloat16 *sh3 = cv.take<__nv_bfloat16>(z.sh13 / 2);
+    __nv_bfloat16 *sh2 = cv.take<__nv_bfloat16>(z.sh2 / 2);
+    uint8_t *w1p = cv.take<uint8_t>(z.e13p), *w1s = cv.take<uint8_t>(z.e13s);
+    uint8_t *w3p = cv.take<uint8_t>(z.e13p), *w3s = cv.take<uint8_t>(z.e13s);
+    uint8_t *w2p = cv.take<uint8_t>(z.e2p), *w2s = cv.take<uint8_t>(z.e2s);
+
+    const cudaMemcpyKind kind =
+        w->where == K3MOE_HOST ? cudaMemcpyHostToDevice : cudaMemcpyDeviceToDevice;
+    int rc = K3MOE_OK;
+    int *flag = h->ws.err + 2;   // scratch word for the scale scan
+#define K3_CP(dst, src, n)                                               \
+    if (rc == K3MOE_OK && cudaMemcpy((dst), (src), (n), kind) != cudaSuccess) \
+        rc = K3MOE_ERR_CUDA;
+    K3_CP(router, w->router_w, z.router);
+    if (w->router_bias) {
+        K3_CP(bias, w->router_bias, z.bias);
+    } else if (rc == K3MOE_OK && cudaMemset(bias, 0, z.bias) != cudaSuccess) {
+        rc = K3MOE_ERR_CUDA;
+    }
+    K3_CP(down, w->down_w, z.down);
+    K3_CP(up, w->up_w, z.up);
+    if (w->latent_gain) K3_CP(gain, w->latent_gain, z.gain);
+    K3_CP(sh1, w->shared_w1, z.sh13);
+    K3_CP(sh3, w->shared_w3, z.sh13);
+    K3_CP(sh2, w->shared_w2, z.sh2);
+    const size_t pe13 = (size_t)c.moe_inter * (c.latent / 2), se13 = (size_t)c.moe_inter * (c.latent / kGroup);
+    const size_t pe2 = (size_t)c.latent * (c.moe_inter / 2), se2 = (size_t)c.latent * (c.moe_inter / kGroup);
+    for (int e = 0; e < c.n_experts && rc == K3MOE_OK; e++) {
+        K3_CP(w1p + e * pe13, w->w1_packed[e], pe13);
+        K3_CP(w1s + e * se13, w->w1_scale[e], se13);
+        K3_CP(w3p + e * pe13, w->w3_packed[e], pe13);
+        K3_CP(w3s + e * se13, w->w3_scale[e], se13);
+        K3_CP(w2p + e * pe2, w->w2_packed[e], pe2);
+        K3_CP(w2s + e * se2, w->w2_scale[e], se2);
+    }
+#undef K3_CP
+    if (rc == K3MOE_OK) {
+        int bad = 0;
+        if (cudaMemset(flag, 0, sizeof(int)) != cudaSuccess ||
+            launch_scale_scan(w1s, z.e13s, flag, 0) != cudaSuccess ||
+            launch_scale_scan(w3s, z.e13s, flag, 0) != cudaSuccess ||
+            launch_scale_scan(w2s, z.e2s, flag, 0) != cudaSuccess ||
+            cudaMemcpy(&bad, flag, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+            rc = K3MOE_ERR_CUDA;
+        else if (bad)
+            rc = K3MOE_ERR_BAD_SCALE;
+        cudaMemset(flag, 0, sizeof(int));
+    }
+    if (rc != K3MOE_OK) {
+        cudaFree(blk);
+        return rc;
+    }
+    L.router_w = router;
+    L.bias = bias;
+    L.down_w = down;
+    L.up_w = up;
+    L.gain = c.latent_norm ? gain : nullptr;
+    L.sh_w1 = sh1;
+    L.sh_w3 = sh3;
+    L.sh_w2 = sh2;
+    L.w1p = w1p;
+    L.w1s = w1s;
+    L.w3p = w3p;
+    L.w3s = w3s;
+    L.w2p = w2p;
+    L.w2s = w2s;
+    L.loaded = true;
+    free_layer(h->layers[(size_t)layer]);
+    h->layers[(size_t)layer] = L;
+    return K3MOE_OK;
+}
+
+int k3moe_forward(k3moe *h, int layer, const void *x, void *y, int T, void *stream)
+{
+    if (!h || !x || !y) return K3MOE_ERR_INVALID_ARG;
+    if (layer < 0 || layer >= h->cfg.max_layers) return K3MOE_ERR_INVALID_ARG;
+    if (T < 1 || T > h->cfg.max_tokens) return K3MOE_ERR_INVALID_ARG;
+    const size_t nb = (size_t)T * h->cfg.hidden * 2;
+    if (overlap(x, nb, y, nb)) return K3MOE_ERR_INVALID_ARG;
+    const LayerDev &w = h->layers[(size_t)layer];
+    if (!w.loaded) return K3MOE_ERR_NOT_LOADED;
+    if (cudaSetDevice(h->cfg.device) != cudaSuccess) return K3MOE_ERR_CUDA;
+    return run_layer(h, w, (const __nv_bfloat16 *)x, (__nv_bfloat16 *)y, T, (cudaStream_t)stream);
+}
+
+int k3moe_forward_chain(k3moe *h, int first_layer, int n_layers, const void *x, void *y, int T,
+                        void *stream)
+{
+    if (!h || !x || !y || n_layers < 1) return K3MOE_ERR_INVALID_ARG;
+    if (first_layer < 0 || first_layer + n_layers > h->cfg.max_layers) return K3MOE_ERR_INVALID_ARG;
+    if (T < 1 || T > h->cfg.max_tokens) return K3MOE_ERR_INVALID_ARG;
+    const size_t nb = (size_t)T * h->cfg.hidden * 2;
+    if (overlap(x, nb, y, nb)) return K3MOE_ERR_INVALID_ARG;
+    for (int l = first_layer; l < first_layer + n_layers; l++)
+        if (!h->layers[(size_t)l].loaded) return K3MOE_ERR_NOT_LOADED;
+    if (cudaSetDevice(h->cfg.device) != cudaSuccess) return K3MOE_ERR_CUDA;
+    cudaStream_t s = (cudaStream_t)stream;
+    const __nv_bfloat16 *cur = (const __nv_bfloat16 *)x;
+    for (int i = 0; i < n_layers; i++) {
+        const bool last = i == n_layers - 1;
+        __nv_bfloat16 *out = last ? (__nv_bfloat16 *)y : h->ws.xbuf0;
+        int rc = run_layer(h, h->layers[(size_t)(first_layer + i)], cur, out, T, s);
+        if (rc != K3MOE_OK) return rc;
+        if (!last) {
+            cudaError_t e;
+            {
+                Prof p(h, "chain_glue_rmsnorm", s);
+                e = launch_chain_glue(*h, h->ws.xbuf0, h->ws.xbuf1, T, s);
+            }
+            if (e != cudaSuccess) return K3MOE_ERR_CUDA;
+            cur = h->ws.xbuf1;
+        }
+    }
+    return K3MOE_OK;
+}
+
+int k3moe_forward_host(k3moe *h, int layer, const void *x_host, void *y_host, int T, void *stream)
+{
+    if (!h || !x_host || !y_host) return K3MOE_ERR_INVALID_ARG;
+    if (layer < 0 || layer >= h->cfg.max_layers) return K3MOE_ERR_INVALID_ARG;
+    if (T < 1 || T > h->cfg.max_tokens) return K3MOE_ERR_INVALID_ARG;
+    if (!h->layers[(size_t)layer].loaded) return K3MOE_ERR_NOT_LOADED;
+    if (cudaSetDevice(h->cfg.device) != cudaSuccess) return K3MOE_ERR_CUDA;
+    cudaStream_t s = (cudaStream_t)stream;
+    const size_t nb = (size_t)T * h->cfg.hidden * 2;
+    if (cudaMemcpyAsync(h->ws.xbuf0, x_host, nb, cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return K3MOE_ERR_CUDA;
+    int rc = run_layer(h, h->layers[(size_t)layer], h->ws.xbuf0, h->ws.xbuf1, T, s);
+    if (rc != K3MOE_OK) return rc;
+    if (cudaMemcpyAsync(y_host, h->ws.xbuf1, nb, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return K3MOE_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return K3MOE_ERR_CUDA;
+    return K3MOE_OK;
+}
+
+int k3moe_get_routing(k3moe *h, int32_t *ids, float *w, int32_t *counts, int32_t *offsets,
+                      int32_t *perm, void *stream)
+{
+    if (!h) return K3MOE_ERR_INVALID_ARG;
+    if (h->last_T <= 0) return K3MOE_ERR_NOT_LOADED;
+    if (cudaSetDevice(h->cfg.device) != cudaSuccess) return K3MOE_ERR_CUDA;
+    cudaStream_t s = (cudaStream_t)stream;
+    const size_t TK = (size_t)h->last_T * h->cfg.topk, E = h->cfg.n_experts;
+    const cudaMemcpyKind d2d = cudaMemcpyDeviceToDevice;
+    if ((ids && cudaMemcpyAsync(ids, h->ws.ids, TK * 4, d2d, s) != cudaSuccess) ||
+        (w && cudaMemcpyAsync(w, h->ws.wts, TK * 4, d2d, s) != cudaSuccess) ||
+        (counts && cudaMemcpyAsync(counts, h->ws.counts, E * 4, d2d, s) != cudaSuccess) ||
+        (offsets && cudaMemcpyAsync(offsets, h->ws.offsets, (E + 1) * 4, d2d, s) != cudaSuccess) ||
+        (perm && cudaMemcpyAsync(perm, h->ws.perm, TK * 4, d2d, s) != cudaSuccess))
+        return K3MOE_ERR_CUDA;
+    return K3MOE_OK;
+}
+
+int k3moe_get_intermediate(k3moe *h, int which, void *dst, size_t bytes, void *stream)
+{
+    if (!h || !dst) return K3MOE_ERR_INVALID_ARG;
+    if (h->last_T <= 0) return K3MOE_ERR_NOT_LOADED;
+    if (cudaSetDevice(h->cfg.device) != cudaSuccess) return K3MOE_ERR_CUDA;
+    cudaStream_t s = (cudaStream_t)stream;
+    const size_t T = (size_t)h->last_T, L = h->cfg.latent, S = h->cfg.shared_inter;
+    const size_t E = h->cfg.n_experts;
+    cudaError_t e;
+    switch (which) {
+    case K3MOE_T_Z:
+        if (bytes > T * L * 4) return K3MOE_ERR_INVALID_ARG;
+        e = cudaMemcpyAsync(dst, h->ws.z, bytes, cudaMemcpyDeviceToDevice, s);
+        break;
+    case K3MOE_T_ACC:
+        if (bytes > T * L * 4) return K3MOE_ERR_INVALID_ARG;
+        e = cudaMemcpyAsync(dst, h->ws.acc, bytes, cudaMemcpyDeviceToDevice, s);
+        break;
+    case K3MOE_T_LOGITS:
+        if (bytes > T * E * 4) return K3MOE_ERR_INVALID_ARG;
+        e = cudaMemcpyAsync(dst, h->ws.logits, bytes, cudaMemcpyDeviceToDevice, s);
+        break;
+    case K3MOE_T_SHARED: {
+        if (bytes != T * S * 4) return K3MOE_ERR_INVALID_ARG;
+        e = cudaMemcpy2DAsync(dst, S * 4, h->ws.cat + L, (L + S) * 4, S * 4, T,
+                              cudaMemcpyDeviceToDevice, s);
+        break;
+    }
+    default:
+        return K3MOE_ERR_INVALID_ARG;
+    }
+    return e == cudaSuccess ? K3MOE_OK : K3MOE_ERR_CUDA;
+}
+
+int k3moe_sync_status(k3moe *h)
+{
+    if (!h) return K3MOE_ERR_INVALID_ARG;
+    if (cudaSetDevice(h->cfg.device) != cudaSuccess) return K3MOE_ERR_CUDA;
+    if (cudaDeviceSynchronize() != cudaSuccess) {
+        cudaGetLastError();
+        return K3MOE_ERR_CUDA;
+    }
+    int word[2] = {0, 0};
+    if (cudaMemcpy(word, h->ws.err, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return K3MOE_ERR_CUDA;
+    if (word[0] != kErrNone) {
+        cudaMemset(h->ws.err, 0, 2 * sizeof(int));
+        return word[0] == kErrTimeout ? K3MOE_ERR_TIMEOUT : K3MOE_ERR_DEVICE;
+    }
+    if (cudaGetLastError() != cudaSuccess) return K3MOE_ERR_CUDA;
+    return K3MOE_OK;
+}
+
+int k3moe_set_profiling(k3moe *h, int enable)
+{
+    if (!h) return K3MOE_ERR_INVALID_ARG;
+    h->profiling = enable != 0;
+    return K3MOE_OK;
+}
+
+int k3moe_profile_read(k3moe *h, k3moe_kernel_stat *out, int max_entries, int *n_entries)
+{
+    if (!h || (!out && max_entries > 0)) return K3MOE_ERR_INVALID_ARG;
+    if (cudaSetDevice(h->cfg.device) != cudaSuccess) return K3MOE_ERR_CUDA;
+    std::map<std::string, std::pair<int, double>> agg;
+    std::vector<std::string> order;
+    int rc = K3MOE_OK;
+    for (auto &r : h->prof) {
+        float ms = 0.f;
+        if (cudaEventSynchronize(r.b) != cudaSuccess || cudaEventElapsedTime(&ms, r.a, r.b) != cudaSuccess)
+            rc = K3MOE_ERR_CUDA;
+        auto it = agg.find(r.name);
+        if (it == agg.end()) {
+            order.push_back(r.name);
+            agg[r.name] = {1, (double)ms};
+        } else {
+            it->second.first += 1;
+            it->second.second += ms;
+        }
+        h->event_pool.push_back(r.a);
+        h->event_pool.push_back(r.b);
+    }
+    h->prof.clear();
+    int n = 0;
+    for (auto &name : order) {
+        if (n < max_entries) {
+            std::memset(&out[n], 0, sizeof(k3moe_kernel_stat));
+            std::strncpy(out[n].name, name.c_str(), sizeof(out[n].name) - 1);
+            out[n].launches = agg[name].first;
+            out[n].total_ms = agg[name].second;
+        }
+        n++;
+    }
+    if (n_entries) *n_entries = n;
+    return rc;
+}
+
+}  // extern "C"

@@ -1,0 +1,212 @@
+"""CUDA path vs the fp64 oracle, through the C ABI (GPU).
+
+Ids and the permutation must match exactly (inputs pass the routing margin
+guard); y, z, the latent aggregate and the shared-expert activations must be
+within normwise max relative error 2e-2 and cosine >= 0.9995.
+"""
+import numpy as np
+import pytest
+
+import k3synth
+import oracle
+from _harness import (Layer, assert_close, bf16_to_f64, check_routing, guarded_tokens)
+
+pytestmark = pytest.mark.gpu
+
+MID = k3synth.Shape(hidden=1024, latent=512, n_experts=64, topk=8, moe_inter=512,
+                    shared_inter=1024)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from mxfp4_routed_expert_gb300 import build
+    build.build()
+
+
+def run_case(shape, recipe, seed, T, stream=0, check_intermediates=True):
+    import mxfp4_routed_expert_gb300 as km
+    d = k3synth.make_layer(shape, seed, 0, recipe)
+    x, _ = guarded_tokens(shape, d, seed, T, stream)
+    lay = Layer(shape, [d], max_tokens=T)
+    try:
+        y = lay.forward(x)
+        r = lay.routing(T)
+        z = lay.intermediate(km.K3MOE_T_Z, T, shape.latent)
+        acc = lay.intermediate(km.K3MOE_T_ACC, T, shape.latent)
+        sh = lay.intermediate(km.K3MOE_T_SHARED, T, shape.shared_inter)
+    finally:
+        lay.close()
+    ref, tr = oracle.layer_forward(shape, d, x, trace=True)
+    check_routing(r, shape, x, tr["ids"], tr["w"])
+    if check_intermediates:
+        assert_close(z, tr["z"], "z", rel=1e-4, cos=0.9999999)
+        assert_close(sh, tr["shared"], "shared SiTU", rel=1e-3, cos=0.99999)
+        assert_close(acc, tr["acc"], "latent aggregate")
+    return assert_close(bf16_to_f64(y), ref)
+
+
+@pytest.mark.parametrize("T", [4, 1, 2, 3, 37])
+def test_tiny(T):
+    run_case(k3synth.TINY, k3synth.TINY_RECIPE, 0, T)
+
+
+@pytest.mark.parametrize("T", [1, 5, 33])
+def test_mid_shape(T):
+    run_case(MID, k3synth.TINY_RECIPE, 1, T)
+
+
+def test_mid_shape_no_bias_no_renorm():
+    shape = k3synth.replace(MID, renorm=0, routed_scale=0.5)
+    run_case(shape, k3synth.replace(k3synth.TINY_RECIPE, zero_bias=True), 2, 9)
+
+
+def test_bad_scale_rejected_and_layer_stays_unloaded():
+    import mxfp4_routed_expert_gb300 as km
+    d = k3synth.make_layer(k3synth.TINY, 0, 0, k3synth.TINY_RECIPE)
+    d["w2s"] = d["w2s"].copy()
+    d["w2s"][7, 3, 1] = 255
+    lay = Layer(k3synth.TINY, [None], max_tokens=4)
+    try:
+        with pytest.raises(km.K3MoEError) as ei:
+            lay.load(0, d)
+        assert ei.value.code == km.K3MOE_ERR_BAD_SCALE
+        with pytest.raises(km.K3MoEError) as ei:
+            lay.forward(k3synth.make_tokens(k3synth.TINY, 0, 4))
+        assert ei.value.code == km.K3MOE_ERR_NOT_LOADED
+    finally:
+        lay.close()
+
+
+def test_forward_argument_errors():
+    import torch
+    import mxfp4_routed_expert_gb300 as km
+    d = k3synth.make_layer(k3synth.TINY, 0, 0, k3synth.TINY_RECIPE)
+    lay = Layer(k3synth.TINY, [d], max_tokens=4)
+    try:
+        x = torch.zeros((8, 256), dtype=torch.int16, device="cuda")
+        y = torch.zeros_like(x)
+        for args, code in [((1, x, y, 4), km.K3MOE_ERR_INVALID_ARG),     # layer out of range
+                           ((0, x, y, 5), km.K3MOE_ERR_INVALID_ARG),     # T > max_tokens
+                           ((0, x, y, 0), km.K3MOE_ERR_INVALID_ARG),     # T = 0
+                           ((0, x, x, 4), km.K3MOE_ERR_INVALID_ARG)]:    # x and y overlap
+            with pytest.raises(km.K3MoEError) as ei:
+                km.k3moe_forward(lay.h, *args)
+            assert ei.value.code == code
+        assert km.k3moe_sync_status(lay.h) == 0
+    finally:
+        lay.close()
+
+
+def test_forward_host_matches_device_forward():
+    import mxfp4_routed_expert_gb300 as km
+    shape = k3synth.TINY
+    d = k3synth.make_layer(shape, 3, 0, k3synth.TINY_RECIPE)
+    x = k3synth.make_tokens(shape, 3, 6)
+    lay = Layer(shape, [d], max_tokens=6)
+    try:
+        y_dev = lay.forward(x)
+        y_host = np.empty_like(x)
+        km.k3moe_forward_host(lay.h, 0, x, y_host, 6)
+    finally:
+        lay.close()
+    np.testing.assert_array_equal(y_host, y_dev)
+
+
+def test_routing_is_deterministic_and_profiling_lists_kernels():
+    import mxfp4_routed_expert_gb300 as km
+    shape = MID
+    d = k3synth.make_layer(shape, 4, 0, k3synth.TINY_RECIPE)
+    x = k3synth.make_tokens(shape, 4, 20)
+    lay = Layer(shape, [d], max_tokens=20)
+    try:
+        km.k3moe_set_profiling(lay.h, True)
+        lay.forward(x)
+        a = lay.routing(20)
+        lay.forward(x)
+        b = lay.routing(20)
+        stats = km.k3moe_profile_read(lay.h)
+        km.k3moe_set_profiling(lay.h, False)
+    finally:
+        lay.close()
+    for k in ("ids", "counts", "offsets", "perm"):
+        np.testing.assert_array_equal(a[k], b[k])
+    names = {s[0] for s in stats}
+    assert {"dense_x_gemv", "route_topk", "permute", "expert_w13_gemv", "expert_w2_gemv",
+            "latent_rmsnorm", "up_shared_gemv"} <= names
+    assert all(s[1] == 2 and s[2] > 0 for s in stats)
+
+
+def test_chain_two_layers_tiny():
+    shape = k3synth.TINY
+    d0 = k3synth.make_layer(shape, 5, 0, k3synth.TINY_RECIPE)
+    d1 = k3synth.make_layer(shape, 5, 1, k3synth.TINY_RECIPE)
+    x, _ = guarded_tokens(shape, d0, 5, 8)
+    lay = Layer(shape, [d0, d1], max_tokens=8)
+    try:
+        y = lay.forward(x, layer=0, chain=2)
+        y0 = lay.forward(x, layer=0)
+    finally:
+        lay.close()
+    ref0 = oracle.layer_forward(shape, d0, x)
+    assert_close(bf16_to_f64(y0), ref0, "layer 0")
+    # layer 1 is checked against the oracle given the GPU's own layer-1 input
+    x1 = k3synth.round_bf16(oracle.chain_glue(bf16_to_f64(y0), shape.rms_eps))
+    _, _, margin = oracle.route(shape, d1, x1)
+    ref1 = oracle.layer_forward(shape, d1, x1)
+    ok = margin > 1e-5          # tokens whose layer-1 routing is not a near-tie
+    assert ok.sum() >= 6
+    assert_close(bf16_to_f64(y)[ok], ref1[ok], "layer 1 of the chain")
+
+
+# ---------------------------------------------------------------------------
+# K3-shape layer (about 16 GB on the device)
+
+@pytest.fixture(scope="module")
+def k3layer():
+    d = k3synth.make_layer(k3synth.K3, 0, 0, k3synth.K3_RECIPE)
+    lay = Layer(k3synth.K3, [d], max_tokens=64)
+    yield d, lay
+    lay.close()
+
+
+def test_k3_decode_T1(k3layer):
+    d, lay = k3layer
+    shape = k3synth.K3
+    pool, _ = guarded_tokens(shape, d, 0, 64, stream=7)
+    for t in (0, 13, 63):
+        x = pool[t:t + 1]
+        y = lay.forward(x)
+        r = lay.routing(1)
+        ref, tr = oracle.layer_forward(shape, d, x, trace=True)
+        check_routing(r, shape, x, tr["ids"], tr["w"])
+        assert_close(bf16_to_f64(y), ref, f"K3 T=1 token {t}")
+
+
+def test_k3_T64_covering(k3layer):
+    d, lay = k3layer
+    shape = k3synth.K3
+    d0 = k3synth.with_bias(d, np.zeros(shape.n_experts, np.float32))
+    lay.load(0, d0)
+    try:
+        x, _ = guarded_tokens(shape, d0, 0, 64,
+                              make=lambda att: k3synth.covering_tokens(shape, d0, 0, 64,
+                                                                       attempts=att))
+        y = lay.forward(x)
+        r = lay.routing(64)
+        assert (r["counts"] > 0).sum() == shape.n_experts       # every expert touched
+        ref, tr = oracle.layer_forward(shape, d0, x, trace=True)
+        check_routing(r, shape, x, tr["ids"], tr["w"])
+        assert_close(bf16_to_f64(y), ref, "K3 T=64 covering")
+    finally:
+        lay.load(0, d)
+
+
+def test_k3_T64_random(k3layer):
+    d, lay = k3layer
+    shape = k3synth.K3
+    x, _ = guarded_tokens(shape, d, 0, 64, stream=9)
+    y = lay.forward(x)
+    r = lay.routing(64)
+    ref, tr = oracle.layer_forward(shape, d, x, trace=True)
+    check_routing(r, shape, x, tr["ids"], tr["w"])
+    assert_close(bf16_to_f64(y), ref, "K3 T=64 random")
