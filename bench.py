@@ -74,10 +74,11 @@ def kernel_bytes(shape, T, n_touched):
     per_w13 = 2 * (I * L // 2 + I * L // 32)
     per_w2 = L * I // 2 + L * I // 32
     return {
-        "dense_x_gemv": 2 * (E * H + L * H + 2 * S * H) + 2 * T * H + 4 * T * (E + L + S),
+        "router_down_gemv": 2 * (E * H + L * H) + 2 * T * H + 4 * T * (E + L),
+        "shared_gate_up_gemv": 2 * (2 * S * H) + 2 * T * H + 4 * T * S,
         "expert_w13_gemv": n_touched * per_w13 + 2 * T * L + 2 * T * k * I,
         "expert_w2_gemv": n_touched * per_w2 + 2 * T * k * I + 4 * T * L,
-        "up_shared_gemv": 2 * (H * L + H * S) + 4 * T * (L + S) + 2 * T * H,
+        "norm_up_shared_gemv": 2 * (H * L + H * S) + 4 * T * (L + S) + 2 * T * H + 2 * L,
     }
 
 
@@ -105,43 +106,51 @@ def make_inputs(workload, seed=0, layer_index=0):
 
 
 class ClockSampler:
-    """nvidia-smi clock and throttle-reason samples during the timed region."""
+    """Polls nvidia-smi for SM clocks and throttle reasons in a background
+    thread; stop() keeps the samples taken inside [start, stop] (widened by one
+    polling period so a short region still gets its nearest samples)."""
     Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
          "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
          "clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
     def __init__(self, index):
         self.index = index
-        self.proc = None
-        self.lines = []
+        self.samples = []
+        self.stop_flag = threading.Event()
+        self.t = None
+
+    def _poll(self):
+        while not self.stop_flag.is_set():
+            try:
+                out = subprocess.run(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                      "--format=csv,noheader,nounits"], capture_output=True,
+                                     text=True, timeout=10).stdout.strip()
+                self.samples.append((time.perf_counter(), out))
+            except (OSError, subprocess.TimeoutExpired):
+                self.samples.append((time.perf_counter(), ""))
+                return
+            time.sleep(0.05)
 
     def start(self):
-        try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.t = threading.Thread(target=self._read, daemon=True)
-            self.t.start()
-        except OSError:
-            self.proc = None
-
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append(line.strip())
+        self.t = threading.Thread(target=self._poll, daemon=True)
+        self.t.start()
+        t0 = time.perf_counter()
+        while not self.samples and time.perf_counter() - t0 < 10:
+            time.sleep(0.01)
+        self.t_start = time.perf_counter()
 
     def stop(self):
-        if not self.proc:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-        sm, smax, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
-            f = [v.strip() for v in ln.split(",")]
+        t_end = time.perf_counter()
+        time.sleep(0.3)
+        self.stop_flag.set()
+        self.t.join(timeout=15)
+        period = 0.3
+        sm, smax, reasons, n = [], None, set(), 0
+        for ts, line in self.samples:
+            if not (self.t_start - period <= ts <= t_end + period):
+                continue
+            f = [v.strip() for v in line.split(",")]
             if len(f) < 7:
                 continue
             try:
@@ -149,11 +158,13 @@ class ClockSampler:
                 smax = float(f[1])
             except ValueError:
                 continue
-            for n, v in zip(names, f[3:7]):
+            n += 1
+            for name, v in zip(self.NAMES, f[3:7]):
                 if v.lower() == "active":
-                    reasons.add(n)
+                    reasons.add(name)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": n,
+                "window_s": round(t_end - self.t_start, 3)}
 
 
 def traffic_for(kernel, workload):
@@ -381,8 +392,8 @@ def run_reference(args, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--workload", choices=list(WORKLOADS), default="decode_t1")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -71,8 +71,9 @@ typedef struct k3moe k3moe;
  * required: a zero, negative or NaN value returns K3MOE_ERR_CONFIG, except the
  * two flags, which must be 0 or 1.
  * Supported sizes (else K3MOE_ERR_SHAPE): hidden, latent, moe_inter and
- * shared_inter multiples of 64; 1 <= topk <= 32; topk <= n_experts <= 1024;
- * max_tokens <= 65536 / topk.
+ * shared_inter multiples of 64; latent and moe_inter at most 4096;
+ * 1 <= topk <= 32; topk <= n_experts <= 1024; max_tokens <= 65536 / topk;
+ * situ_b1 * situ_b2 <= 512.
  * K3: hidden 7168, latent 3584, n_experts 896, topk 16, moe_inter 3072,
  * shared_inter 6144 (two shared experts fused), rms_eps 1e-5, situ_b1 4,
  * situ_b2 25, routed_scale 1, renorm 1, latent_norm 1. */

@@ -4,7 +4,6 @@
 #include <cmath>
 #include <cstdio>
 #include <cstring>
-#include <map>
 #include <new>
 #include <string>
 
@@ -34,7 +33,9 @@ int check_config(const k3moe_config *c)
         return K3MOE_ERR_SHAPE;
     if (c->topk > kMaxTopk || c->topk > c->n_experts || c->n_experts > kMaxExperts)
         return K3MOE_ERR_SHAPE;
-    if (c->latent > 4096 || c->moe_inter > 8192) return K3MOE_ERR_SHAPE;
+    // the expert GEMVs keep 4 column groups of 32 per lane in registers
+    if (c->latent > 4096 || c->moe_inter > 4096) return K3MOE_ERR_SHAPE;
+    if (!expert_smem_fits(*c)) return K3MOE_ERR_SHAPE;
     if ((long long)c->max_tokens * c->topk > 65536) return K3MOE_ERR_SHAPE;
     // fp16 partial sums in the expert GEMVs: |SiTU| <= b1*b2 must stay small
     if ((double)c->situ_b1 * c->situ_b2 > 512.0) return K3MOE_ERR_SHAPE;
@@ -109,8 +110,41 @@ LayerSizes layer_sizes(const k3moe_config &c)
     return z;
 }
 
+// Moves finished event pairs into the per-kernel totals and back into the
+// pool. Records complete in stream order, so a non-blocking harvest stops at
+// the first one still pending.
+int harvest(k3moe *h, bool blocking)
+{
+    int rc = K3MOE_OK;
+    while (!h->prof.empty()) {
+        ProfRec r = h->prof.front();
+        if (blocking) {
+            if (cudaEventSynchronize(r.b) != cudaSuccess) rc = K3MOE_ERR_CUDA;
+        } else if (cudaEventQuery(r.b) != cudaSuccess) {
+            cudaGetLastError();   // cudaErrorNotReady is not an error here
+            break;
+        }
+        float ms = 0.f;
+        if (cudaEventElapsedTime(&ms, r.a, r.b) != cudaSuccess) rc = K3MOE_ERR_CUDA;
+        size_t i = 0;
+        while (i < h->prof_names.size() && h->prof_names[i] != r.name) i++;
+        if (i == h->prof_names.size()) {
+            h->prof_names.push_back(r.name);
+            h->prof_launches.push_back(0);
+            h->prof_ms.push_back(0.0);
+        }
+        h->prof_launches[i] += 1;
+        h->prof_ms[i] += ms;
+        h->event_pool.push_back(r.a);
+        h->event_pool.push_back(r.b);
+        h->prof.pop_front();
+    }
+    return rc;
+}
+
 cudaEvent_t get_event(k3moe *h)
 {
+    if (h->event_pool.empty()) harvest(h, false);
     if (!h->event_pool.empty()) {
         cudaEvent_t e = h->event_pool.back();
         h->event_pool.pop_back();
@@ -154,13 +188,24 @@ int run_layer(k3moe *h, const LayerDev &w, const __nv_bfloat16 *x, __nv_bfloat16
         e = (call);                                \
     }                                              \
     if (e != cudaSuccess) return K3MOE_ERR_CUDA;
-    K3_STEP("dense_x_gemv", launch_dense_x(*h, w, x, T, s));
+    // stream s:    router+down -> route -> permute -> [join] -> experts -> up
+    // side stream:  [after router+down] shared-expert gate/up (overlaps route, permute)
+    K3_STEP("router_down_gemv", launch_dense_x(*h, w, x, T, s, 0));
+    if (cudaEventRecord(h->ev_fork, s) != cudaSuccess ||
+        cudaStreamWaitEvent(h->side, h->ev_fork, 0) != cudaSuccess)
+        return K3MOE_ERR_CUDA;
+    {
+        Prof p_(h, "shared_gate_up_gemv", h->side);
+        e = launch_dense_x(*h, w, x, T, h->side, 1);
+    }
+    if (e != cudaSuccess || cudaEventRecord(h->ev_join, h->side) != cudaSuccess)
+        return K3MOE_ERR_CUDA;
     K3_STEP("route_topk", launch_route(*h, w, T, s));
-    K3_STEP("permute", launch_perm(*h, T, s));
+    if (T > 1) K3_STEP("permute", launch_perm(*h, T, s));   // T == 1: written by route_topk
+    if (cudaStreamWaitEvent(s, h->ev_join, 0) != cudaSuccess) return K3MOE_ERR_CUDA;
     K3_STEP("expert_w13_gemv", launch_expert_w13(*h, w, T, s));
     K3_STEP("expert_w2_gemv", launch_expert_w2(*h, w, T, s));
-    K3_STEP("latent_rmsnorm", launch_latent_norm(*h, w, T, s));
-    K3_STEP("up_shared_gemv", launch_up(*h, w, y, T, s));
+    K3_STEP("norm_up_shared_gemv", launch_up(*h, w, y, T, s));
 #undef K3_STEP
     h->last_T = T;
     return K3MOE_OK;
@@ -231,7 +276,26 @@ int k3moe_create(const k3moe_config *cfg, k3moe **out)
         return K3MOE_ERR_OOM;
     }
     carve_workspace(*cfg, (char *)blk, &h->ws);
-    if (cudaMemset(blk, 0, need) != cudaSuccess) {
+    int prio_lo = 0, prio_hi = 0;
+    cudaDeviceGetStreamPriorityRange(&prio_lo, &prio_hi);
+    if (cudaStreamCreateWithPriority(&h->side, cudaStreamNonBlocking, prio_lo) != cudaSuccess ||
+        cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&h->ev_join, cudaEventDisableTiming) != cudaSuccess) {
+        cudaGetLastError();
+        if (h->side) cudaStreamDestroy(h->side);
+        if (h->ev_fork) cudaEventDestroy(h->ev_fork);
+        if (h->ev_join) cudaEventDestroy(h->ev_join);
+        cudaFree(blk);
+        delete h;
+        return K3MOE_ERR_CUDA;
+    }
+    if (cudaMemset(blk, 0, need) != cudaSuccess || init_dense_kernels(*h) != cudaSuccess ||
+        init_route_kernels(*cfg) != cudaSuccess || init_expert_kernels(*cfg) != cudaSuccess ||
+        cudaDeviceSynchronize() != cudaSuccess) {
+        cudaGetLastError();
+        cudaStreamDestroy(h->side);
+        cudaEventDestroy(h->ev_fork);
+        cudaEventDestroy(h->ev_join);
         cudaFree(blk);
         delete h;
         return K3MOE_ERR_CUDA;
@@ -252,6 +316,12 @@ void k3moe_destroy(k3moe *h)
         cudaEventDestroy(r.b);
     }
     for (auto e : h->event_pool) cudaEventDestroy(e);
+    if (h->side) {
+        cudaStreamSynchronize(h->side);
+        cudaStreamDestroy(h->side);
+    }
+    if (h->ev_fork) cudaEventDestroy(h->ev_fork);
+    if (h->ev_join) cudaEventDestroy(h->ev_join);
     delete h;
 }
 
@@ -501,7 +571,13 @@ int k3moe_sync_status(k3moe *h)
 int k3moe_set_profiling(k3moe *h, int enable)
 {
     if (!h) return K3MOE_ERR_INVALID_ARG;
+    if (cudaSetDevice(h->cfg.device) != cudaSuccess) return K3MOE_ERR_CUDA;
     h->profiling = enable != 0;
+    while (h->profiling && h->event_pool.size() < 512) {   // created outside any timed region
+        cudaEvent_t e = nullptr;
+        if (cudaEventCreate(&e) != cudaSuccess) return K3MOE_ERR_CUDA;
+        h->event_pool.push_back(e);
+    }
     return K3MOE_OK;
 }
 
@@ -509,36 +585,18 @@ int k3moe_profile_read(k3moe *h, k3moe_kernel_stat *out, int max_entries, int *n
 {
     if (!h || (!out && max_entries > 0)) return K3MOE_ERR_INVALID_ARG;
     if (cudaSetDevice(h->cfg.device) != cudaSuccess) return K3MOE_ERR_CUDA;
-    std::map<std::string, std::pair<int, double>> agg;
-    std::vector<std::string> order;
-    int rc = K3MOE_OK;
-    for (auto &r : h->prof) {
-        float ms = 0.f;
-        if (cudaEventSynchronize(r.b) != cudaSuccess || cudaEventElapsedTime(&ms, r.a, r.b) != cudaSuccess)
-            rc = K3MOE_ERR_CUDA;
-        auto it = agg.find(r.name);
-        if (it == agg.end()) {
-            order.push_back(r.name);
-            agg[r.name] = {1, (double)ms};
-        } else {
-            it->second.first += 1;
-            it->second.second += ms;
-        }
-        h->event_pool.push_back(r.a);
-        h->event_pool.push_back(r.b);
-    }
-    h->prof.clear();
-    int n = 0;
-    for (auto &name : order) {
-        if (n < max_entries) {
-            std::memset(&out[n], 0, sizeof(k3moe_kernel_stat));
-            std::strncpy(out[n].name, name.c_str(), sizeof(out[n].name) - 1);
-            out[n].launches = agg[name].first;
-            out[n].total_ms = agg[name].second;
-        }
-        n++;
+    const int rc = harvest(h, true);
+    const int n = (int)h->prof_names.size();
+    for (int i = 0; i < n && i < max_entries; i++) {
+        std::memset(&out[i], 0, sizeof(k3moe_kernel_stat));
+        std::strncpy(out[i].name, h->prof_names[(size_t)i].c_str(), sizeof(out[i].name) - 1);
+        out[i].launches = h->prof_launches[(size_t)i];
+        out[i].total_ms = h->prof_ms[(size_t)i];
     }
     if (n_entries) *n_entries = n;
+    h->prof_names.clear();
+    h->prof_launches.clear();
+    h->prof_ms.clear();
     return rc;
 }
 

@@ -7,6 +7,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <deque>
 #include <string>
 #include <vector>
 
@@ -74,27 +75,43 @@ struct k3moe {
     std::vector<k3::LayerDev> layers;
     k3::Workspace ws;
     int last_T = 0;
+    // launch shapes fixed at create time (no per-launch host queries)
+    int grid_dense[3] = {0, 0, 0};   // k_dense_x resident-block cap for TB = 1, 2, 4
+    // side stream for the shared experts, which overlap routing and permutation
+    cudaStream_t side = nullptr;
+    cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
+    int grid_up[3] = {0, 0, 0};      // k_up for TB = 1, 2, 4
+    // per-kernel timing (k3moe_set_profiling)
     bool profiling = false;
-    std::vector<k3::ProfRec> prof;
+    std::deque<k3::ProfRec> prof;
     std::vector<cudaEvent_t> event_pool;
-    int err_sticky = 0;
+    std::vector<std::string> prof_names;
+    std::vector<int> prof_launches;
+    std::vector<double> prof_ms;
 };
 
 namespace k3 {
 
 // ---- launchers (each returns cudaGetLastError()) -----------------------------
+// part 0: router logits and latent down projection; part 1: shared-expert
+// gate/up with SiTU; part 2: both.
 cudaError_t launch_dense_x(const k3moe &h, const LayerDev &w, const __nv_bfloat16 *x, int T,
-                           cudaStream_t s);
+                           cudaStream_t s, int part);
 cudaError_t launch_route(const k3moe &h, const LayerDev &w, int T, cudaStream_t s);
 cudaError_t launch_perm(const k3moe &h, int T, cudaStream_t s);
 cudaError_t launch_expert_w13(const k3moe &h, const LayerDev &w, int T, cudaStream_t s);
 cudaError_t launch_expert_w2(const k3moe &h, const LayerDev &w, int T, cudaStream_t s);
-cudaError_t launch_latent_norm(const k3moe &h, const LayerDev &w, int T, cudaStream_t s);
 cudaError_t launch_up(const k3moe &h, const LayerDev &w, __nv_bfloat16 *y, int T,
                       cudaStream_t s);
 cudaError_t launch_chain_glue(const k3moe &h, const __nv_bfloat16 *y, __nv_bfloat16 *x_next,
                               int T, cudaStream_t s);
 cudaError_t launch_scale_scan(const uint8_t *p, size_t n, int *flag, cudaStream_t s);
+
+// ---- one-time set-up at k3moe_create (attributes, grid sizes) -------------------
+cudaError_t init_dense_kernels(k3moe &h);
+cudaError_t init_route_kernels(const k3moe_config &c);
+cudaError_t init_expert_kernels(const k3moe_config &c);
+bool expert_smem_fits(const k3moe_config &c);
 
 // ---- device helpers -----------------------------------------------------------
 __device__ __forceinline__ void set_err(int *err, int code, int detail)
@@ -106,7 +123,7 @@ __device__ __forceinline__ void set_err(int *err, int code, int detail)
 __device__ __forceinline__ uint4 ld_stream(const void *p)
 {
     uint4 r;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
                  : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
                  : "l"(p));
     return r;
@@ -123,6 +140,17 @@ __device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte)
         : "=r"(r)
         : "r"(byte));
     return r;
+}
+
+// Four bytes of e2m1 pairs -> four f16x2 (byte b -> o_b; low nibble -> low half).
+__device__ __forceinline__ void e2m1x8_to_f16x2x4(uint32_t w, uint32_t &o0, uint32_t &o1,
+                                                  uint32_t &o2, uint32_t &o3)
+{
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+        : "=r"(o0), "=r"(o1), "=r"(o2), "=r"(o3)
+        : "r"(w));
 }
 
 __device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c)
@@ -149,6 +177,125 @@ __device__ __forceinline__ float sigmoid_f(float v) { return 1.0f / (1.0f + expf
 __device__ __forceinline__ float situ_f(float g, float u, float b1, float b2)
 {
     return (b1 * tanhf(g / b1)) * sigmoid_f(g) * (b2 * tanhf(u / b2));
+}
+
+// ---- mbarrier / bulk-copy (TMA) helpers --------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Waits for the phase of `parity` to complete, for at most about two seconds;
+// on time-out latches kErrTimeout with `where` and returns false.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *err, int where)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            set_err(err, kErrTimeout, where);
+            return false;
+        }
+    }
+    return true;
+}
+
+// Bulk (non-tensor) TMA copy global -> shared, completing on `bar`.
+// dst, src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
+                                         uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_first()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_last()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// ---- programmatic dependent launch ----------------------------------------------
+// Every kernel of a forward lets the next one start launching at once, and
+// waits for the previous one to finish (and flush) before it reads anything
+// that kernel wrote.
+__device__ __forceinline__ void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), int grid, int block, size_t smem,
+                              cudaStream_t s, Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3((unsigned)block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
 __device__ __forceinline__ float warp_sum(float v)

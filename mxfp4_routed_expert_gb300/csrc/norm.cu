@@ -1,10 +1,7 @@
-// Latent RMSNorm of the aggregate, the glue between stacked layers, and the
-// load-time scale-byte check.
+// The glue between stacked layers and the load-time scale-byte check.
 //
-// RMSNorm: out = x / sqrt(mean(x^2) + eps) * gain, eps inside the square root
-// (kimi-k3-in-c README, Part II section 5, k3_rmsnorm), applied to the
-// weighted SUM of the expert outputs, not to each expert (section 9, k3_moe
-// step 4).
+// RMSNorm: out = x / sqrt(mean(x^2) + eps) (unit gain here), eps inside the
+// square root (kimi-k3-in-c README, Part II section 5, k3_rmsnorm).
 #include "k3moe_internal.cuh"
 
 namespace k3 {
@@ -22,34 +19,6 @@ __device__ __forceinline__ float block_sum_256(float v, float *red)
     return s;
 }
 
-// cat[t, 0:L] = acc[t] * inv_rms(acc[t]) * gain   (or acc[t] when gain is null)
-__global__ void __launch_bounds__(256) k_latent_norm(const float *acc, const __nv_bfloat16 *gain,
-                                                     float *cat, int L, int cat_ld, float eps)
-{
-    __shared__ float red[8];
-    const int t = blockIdx.x;
-    const float *a = acc + (size_t)t * L;
-    float *o = cat + (size_t)t * cat_ld;
-    if (!gain) {
-        for (int i = threadIdx.x; i < L; i += blockDim.x) o[i] = a[i];
-        return;
-    }
-    float ss = 0.f;
-    for (int i = threadIdx.x; i < L; i += blockDim.x) ss = fmaf(a[i], a[i], ss);
-    ss = block_sum_256(ss, red);
-    const float inv = 1.0f / sqrtf(ss / (float)L + eps);
-    for (int i = threadIdx.x; i < L; i += blockDim.x)
-        o[i] = a[i] * inv * __bfloat162float(gain[i]);
-}
-
-cudaError_t launch_latent_norm(const k3moe &h, const LayerDev &w, int T, cudaStream_t s)
-{
-    const k3moe_config &c = h.cfg;
-    k_latent_norm<<<T, 256, 0, s>>>(h.ws.acc, c.latent_norm ? w.gain : nullptr, h.ws.cat,
-                                    c.latent, c.latent + c.shared_inter, c.rms_eps);
-    return cudaGetLastError();
-}
-
 // x_next[t] = bf16(y[t] / sqrt(mean(y[t]^2) + eps)), unit gain.
 __global__ void __launch_bounds__(256) k_chain_glue(const __nv_bfloat16 *y, __nv_bfloat16 *xn,
                                                     int H, float eps)
@@ -57,6 +26,8 @@ __global__ void __launch_bounds__(256) k_chain_glue(const __nv_bfloat16 *y, __nv
     __shared__ float red[8];
     const int t = blockIdx.x;
     const __nv_bfloat16 *a = y + (size_t)t * H;
+    pdl_launch_dependents();
+    pdl_wait();
     float ss = 0.f;
     for (int i = threadIdx.x; i < H; i += blockDim.x) {
         const float v = __bfloat162float(a[i]);
@@ -71,8 +42,7 @@ __global__ void __launch_bounds__(256) k_chain_glue(const __nv_bfloat16 *y, __nv
 cudaError_t launch_chain_glue(const k3moe &h, const __nv_bfloat16 *y, __nv_bfloat16 *x_next,
                               int T, cudaStream_t s)
 {
-    k_chain_glue<<<T, 256, 0, s>>>(y, x_next, h.cfg.hidden, h.cfg.rms_eps);
-    return cudaGetLastError();
+    return launch_pdl(k_chain_glue, T, 256, 0, s, y, x_next, h.cfg.hidden, h.cfg.rms_eps);
 }
 
 // flag[0] += number of bytes equal to 255 in p[0, n).

@@ -109,7 +109,10 @@ def test_forward_host_matches_device_forward():
         km.k3moe_forward_host(lay.h, 0, x, y_host, 6)
     finally:
         lay.close()
-    np.testing.assert_array_equal(y_host, y_dev)
+    # the w2 scatter-add uses fp32 atomics, whose order varies between runs, so an
+    # output may differ by one bf16 unit in the last place
+    a, b = bf16_to_f64(y_host), bf16_to_f64(y_dev)
+    assert np.all(np.abs(a - b) <= np.abs(b) * 2.0 ** -7 + 1e-30)
 
 
 def test_routing_is_deterministic_and_profiling_lists_kernels():
@@ -131,8 +134,8 @@ def test_routing_is_deterministic_and_profiling_lists_kernels():
     for k in ("ids", "counts", "offsets", "perm"):
         np.testing.assert_array_equal(a[k], b[k])
     names = {s[0] for s in stats}
-    assert {"dense_x_gemv", "route_topk", "permute", "expert_w13_gemv", "expert_w2_gemv",
-            "latent_rmsnorm", "up_shared_gemv"} <= names
+    assert {"router_down_gemv", "shared_gate_up_gemv", "route_topk", "permute",
+            "expert_w13_gemv", "expert_w2_gemv", "norm_up_shared_gemv"} <= names
     assert all(s[1] == 2 and s[2] > 0 for s in stats)
 
 
