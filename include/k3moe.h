@@ -191,6 +191,37 @@ K3MOE_API const char *k3moe_strerror(int code);
 /* K3MOE_ABI_VERSION of the library. */
 K3MOE_API int k3moe_abi_version(void);
 
+/* ---- Router without allocation ------------------------------------------------
+ * The pages describe no such call; it exists for callers that may not
+ * allocate device memory (a plugin whose host framework owns every device
+ * buffer through its own pool, or a serving loop that forbids allocation
+ * after start-up). It needs no handle and calls no cudaMalloc, cudaFree or
+ * allocating library routine.
+ *
+ * Computes the router step of the layer for T tokens on the CURRENT device:
+ * logit = x . Wr_e, sc = sigmoid(logit), ch = sc + bias_e; the topk experts
+ * with the largest ch (equal ch: lower id first) go to ids [T, topk] int32 in
+ * descending ch order, their sc (renormalised to sum 1 when renorm = 1, then
+ * times routed_scale) to w [T, topk] fp32. x [T, hidden] and router_w
+ * [n_experts, hidden] are bf16, router_bias [n_experts] fp32 or NULL; all
+ * pointers are device memory owned by the caller. Asynchronous on `stream`.
+ *
+ * Scratch: the [T, n_experts] fp32 logits live in one static device array of
+ * K3MOE_ROUTE_STATIC_MAX_LOGITS floats (4 MiB) that every GPU loading this
+ * library keeps until the process exits. T * n_experts above that limit
+ * returns K3MOE_ERR_SHAPE. The first call on a device looks up the array's
+ * device address (cudaGetSymbolAddress); make that first call before any
+ * stream capture. All calls share the array, so calls that overlap on the GPU
+ * (other streams or host threads) race on it; nothing in it needs to start at
+ * zero. Errors: K3MOE_ERR_INVALID_ARG (NULL pointer, T < 1, hidden not a
+ * positive multiple of 8), K3MOE_ERR_CONFIG (renorm not 0/1, routed_scale not
+ * finite and > 0), K3MOE_ERR_SHAPE (topk not in [1, 32], topk > n_experts,
+ * n_experts > 1024, or the size limit), K3MOE_ERR_CUDA. */
+#define K3MOE_ROUTE_STATIC_MAX_LOGITS (1u << 20)
+K3MOE_API int k3moe_route_static(const void *x, const void *router_w, const float *router_bias,
+                                 int T, int hidden, int n_experts, int topk, int renorm,
+                                 float routed_scale, int32_t *ids, float *w, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

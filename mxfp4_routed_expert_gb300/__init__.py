@@ -36,7 +36,8 @@ K3MOE_T_Z, K3MOE_T_ACC, K3MOE_T_SHARED, K3MOE_T_LOGITS = 1, 2, 3, 4
 EXPORTS = ("k3moe_create", "k3moe_load_layer", "k3moe_forward", "k3moe_forward_chain",
            "k3moe_forward_host", "k3moe_get_routing", "k3moe_get_intermediate",
            "k3moe_sync_status", "k3moe_set_profiling", "k3moe_profile_read", "k3moe_destroy",
-           "k3moe_strerror", "k3moe_abi_version")
+           "k3moe_strerror", "k3moe_abi_version", "k3moe_route_static")
+K3MOE_ROUTE_STATIC_MAX_LOGITS = 1 << 20
 
 
 class K3MoEError(RuntimeError):
@@ -102,6 +103,7 @@ def lib():
         L.k3moe_strerror.argtypes = [i]
         L.k3moe_strerror.restype = ctypes.c_char_p
         L.k3moe_abi_version.restype = i
+        L.k3moe_route_static.argtypes = [vp, vp, vp, i, i, i, i, i, ctypes.c_float, vp, vp, vp]
         for n in EXPORTS:
             if n not in ("k3moe_destroy", "k3moe_strerror"):
                 getattr(L, n).restype = i if n != "k3moe_destroy" else None
@@ -258,3 +260,12 @@ def k3moe_profile_read(h: int, max_entries: int = 32):
 
 def k3moe_abi_version() -> int:
     return lib().k3moe_abi_version()
+
+
+def k3moe_route_static(x, router_w, router_bias, T: int, hidden: int, n_experts: int, topk: int,
+                       renorm: int, routed_scale: float, ids, w, stream=None) -> int:
+    """Router step without a handle or any allocation (see include/k3moe.h)."""
+    return _check(lib().k3moe_route_static(_ptr(x), _ptr(router_w), _ptr(router_bias), T, hidden,
+                                           n_experts, topk, renorm, float(routed_scale),
+                                           _ptr(ids), _ptr(w), _stream(stream)),
+                  "k3moe_route_static")
