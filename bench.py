@@ -13,7 +13,9 @@ value: tokens/s with inputs resident in HBM (CUDA events around each
 forward, summed over K steps); e2e: the same through k3moe_forward_host
 with pinned host buffers (copies inside the timed region); roofline: the
 dominant kernel's algorithmic bytes per launch over its event-timed average
-duration against the measured HBM copy bandwidth; cpu_baseline: the fp64
+duration (a second pass of the same K steps with every kernel bracketed by
+CUDA events; the first pass, which gives value, has no events between the
+kernels) against the measured HBM copy bandwidth; cpu_baseline: the fp64
 oracle on the host cores on a bounded sample of the same workload.
 
 With torchrun (N > 1) every rank runs an independent replica of the layer
@@ -53,6 +55,9 @@ WORKLOADS = {
                           "Zipf(1.1) expert popularity via router bias"),
     "chain8_t256": dict(T=256, layers=8, desc="8 stacked K3-shape layers, T=256, RMSNorm "
                         "between layers"),
+    # small case for ncu captures: K3 row shapes, 64 experts (1.2 GB), decode T=1
+    "decode_t1_e64": dict(T=1, layers=1, desc="K3 row shapes with 64 routed experts, decode T=1 "
+                          "(small case for profiler captures)"),
 }
 ZIPF_ALPHA = 0.55
 
@@ -89,10 +94,10 @@ def layer_bytes(shape, T, n_touched):
 # ---- inputs ----------------------------------------------------------------------
 
 def make_inputs(workload, seed=0, layer_index=0):
-    shape = k3synth.K3
+    shape = k3synth.K3 if workload != "decode_t1_e64" else k3synth.replace(k3synth.K3, n_experts=64)
     d = k3synth.make_layer(shape, seed, layer_index, k3synth.K3_RECIPE)
     T = WORKLOADS[workload]["T"]
-    if workload == "decode_t1":
+    if workload in ("decode_t1", "decode_t1_e64"):
         x = k3synth.make_tokens(shape, seed, POOL, stream=7)
     elif workload == "decode_t64":
         d = k3synth.with_bias(d, np.zeros(shape.n_experts, np.float32))
@@ -251,26 +256,37 @@ def run_native(args, rank, world):
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     clocks = ClockSampler(dev)
+
+    def timed_pass(profiled):
+        if profiled:
+            km.k3moe_set_profiling(h, True)
+        for i in range(args.steps):
+            flush.zero_()                      # L2 flush, outside the timed events
+            starts[i].record(stream)
+            fwd(args.warmup + i)
+            ends[i].record(stream)
+            km.k3moe_get_routing(h, counts=counts_log[i], stream=stream)
+        torch.cuda.synchronize()
+        stats = None
+        if profiled:
+            stats = km.k3moe_profile_read(h)
+            km.k3moe_set_profiling(h, False)
+        return sum(s.elapsed_time(e) for s, e in zip(starts, ends)), stats
+
+    # pass 1 (the measurement): no per-kernel events between the launches
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     clocks.start()
-    km.k3moe_set_profiling(h, True)
-    for i in range(args.steps):
-        flush.zero_()                      # L2 flush, outside the timed events
-        starts[i].record(stream)
-        fwd(args.warmup + i)
-        ends[i].record(stream)
-        km.k3moe_get_routing(h, counts=counts_log[i], stream=stream)
-    torch.cuda.synchronize()
+    total_ms, _ = timed_pass(False)
     if world > 1:
         torch.distributed.barrier()
     clk = clocks.stop()
-    stats = km.k3moe_profile_read(h)
-    km.k3moe_set_profiling(h, False)
+    # pass 2: the same steps with every kernel bracketed by CUDA events on its
+    # launching stream (per-kernel durations for the roofline)
+    prof_ms, stats = timed_pass(True)
     st = km.k3moe_sync_status(h)
     assert st == 0, km.strerror(st)
-    total_ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends))
     if world > 1:
         t = torch.tensor([total_ms], dtype=torch.float64, device="cuda")
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
@@ -302,11 +318,12 @@ def run_native(args, rank, world):
     kernels = {n: {"launches": l, "avg_ms": round(ms / l, 5),
                    "share": round(ms / sum(m for _, m in by_name.values()), 4)}
                for n, (l, ms) in by_name.items()}
+    kernels["_profiled_pass_ms_per_step"] = round(prof_ms / args.steps, 5)
     gpu_launches = sum(l for l, _ in by_name.values())
 
     # ---- e2e through the public host-buffer entry point --------------------------------
     e2e = None
-    if n_layers == 1:
+    if n_layers == 1 and not args.no_e2e:
         xh = torch.from_numpy(xpool.view(np.int16).copy()).pin_memory()
         yh = torch.empty((T, shape.hidden), dtype=torch.int16).pin_memory()
         for i in range(2):
@@ -397,6 +414,7 @@ def main():
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--workload", choices=list(WORKLOADS), default="decode_t1")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

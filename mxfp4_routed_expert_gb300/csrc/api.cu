@@ -63,14 +63,14 @@ size_t carve_workspace(const k3moe_config &c, char *base, Workspace *ws)
     Workspace w;
     w.logits = cv.take<float>(Tm * E);
     w.z = cv.take<float>(Tm * L);
-    w.z16 = cv.take<__half>(Tm * L);
-    w.zexp = cv.take<int>(Tm);
+    w.z16 = cv.take<__half>(Tm * (L + kZPad));
     w.cat = cv.take<float>(Tm * (L + S));
     w.ids = cv.take<int>(Tm * K);
     w.wts = cv.take<float>(Tm * K);
     w.counts = cv.take<int>(E);
     w.offsets = cv.take<int>(E + 1);
     w.perm = cv.take<int>(Tm * K);
+    w.pair_w = cv.take<float>(Tm * K);
     w.touched = cv.take<int>(E);
     w.n_touched = cv.take<int>(1);
     w.h16 = cv.take<__half>(Tm * K * I);
@@ -190,13 +190,16 @@ int run_layer(k3moe *h, const LayerDev &w, const __nv_bfloat16 *x, __nv_bfloat16
     if (e != cudaSuccess) return K3MOE_ERR_CUDA;
     // stream s:    router+down -> route -> permute -> [join] -> experts -> up
     // side stream:  [after router+down] shared-expert gate/up (overlaps route, permute)
-    K3_STEP("router_down_gemv", launch_dense_x(*h, w, x, T, s, 0));
+    const bool tma = T <= 2 && h->dense_tma_ok[T - 1];
+    K3_STEP("router_down_gemv", tma ? launch_dense_tma(*h, w, x, nullptr, T, s, 0)
+                                    : launch_dense_x(*h, w, x, T, s, 0));
     if (cudaEventRecord(h->ev_fork, s) != cudaSuccess ||
         cudaStreamWaitEvent(h->side, h->ev_fork, 0) != cudaSuccess)
         return K3MOE_ERR_CUDA;
     {
         Prof p_(h, "shared_gate_up_gemv", h->side);
-        e = launch_dense_x(*h, w, x, T, h->side, 1);
+        e = tma ? launch_dense_tma(*h, w, x, nullptr, T, h->side, 1)
+                : launch_dense_x(*h, w, x, T, h->side, 1);
     }
     if (e != cudaSuccess || cudaEventRecord(h->ev_join, h->side) != cudaSuccess)
         return K3MOE_ERR_CUDA;
@@ -205,7 +208,8 @@ int run_layer(k3moe *h, const LayerDev &w, const __nv_bfloat16 *x, __nv_bfloat16
     if (cudaStreamWaitEvent(s, h->ev_join, 0) != cudaSuccess) return K3MOE_ERR_CUDA;
     K3_STEP("expert_w13_gemv", launch_expert_w13(*h, w, T, s));
     K3_STEP("expert_w2_gemv", launch_expert_w2(*h, w, T, s));
-    K3_STEP("norm_up_shared_gemv", launch_up(*h, w, y, T, s));
+    K3_STEP("norm_up_shared_gemv", tma ? launch_dense_tma(*h, w, nullptr, y, T, s, 2)
+                                       : launch_up(*h, w, y, T, s));
 #undef K3_STEP
     h->last_T = T;
     return K3MOE_OK;
@@ -291,6 +295,7 @@ int k3moe_create(const k3moe_config *cfg, k3moe **out)
     }
     if (cudaMemset(blk, 0, need) != cudaSuccess || init_dense_kernels(*h) != cudaSuccess ||
         init_route_kernels(*cfg) != cudaSuccess || init_expert_kernels(*cfg) != cudaSuccess ||
+        init_dense_tma(*cfg) != cudaSuccess ||
         cudaDeviceSynchronize() != cudaSuccess) {
         cudaGetLastError();
         cudaStreamDestroy(h->side);
@@ -300,6 +305,8 @@ int k3moe_create(const k3moe_config *cfg, k3moe **out)
         delete h;
         return K3MOE_ERR_CUDA;
     }
+    h->dense_tma_ok[0] = dense_tma_fits(*cfg, 1);
+    h->dense_tma_ok[1] = dense_tma_fits(*cfg, 2);
     h->layers.resize((size_t)cfg->max_layers);
     *out = h;
     return K3MOE_OK;

@@ -1,0 +1,392 @@
+// bf16 weight-streaming GEMVs for one or two tokens (decode), TMA-fed.
+//
+// The three dense steps of the layer (kimi-k3-in-c README, Part II section 9,
+// k3_moe steps 1, 2, 5 and 6; bf16 widening is a 16-bit shift, section 5):
+//   RD: router logits x . Wr (E rows) and the latent down projection x . Wd
+//       (L rows), both fp32 outputs;
+//   SH: the fused shared experts' gate/up pair, SiTU-GLU applied per row pair;
+//   UP: y = Wu . n + Ws2 . s with n = RMSNorm(acc) * gain (the norm of the
+//       aggregate, section 9 step 4) and s the shared SiTU output, bf16 output.
+//
+// Persistent, one CTA per SM: one producer thread streams weight-row stages
+// through a shared-memory ring with bulk TMA copies (one copy per row piece),
+// eight consumer warps each own one row (RD, UP) or one gate/up row pair (SH)
+// of a stage. The activations of the TB tokens sit in shared memory as fp32
+// for the whole kernel; the producer starts streaming weights while the
+// consumers stage them. A unit is one row (or pair) per consumer warp over the
+// whole K; units are split evenly and contiguously over the CTAs.
+#include <algorithm>
+
+#include "k3moe_internal.cuh"
+
+namespace k3 {
+
+namespace {
+
+constexpr int kCW = 16;                 // consumer warps
+constexpr int kThreads = (kCW + 1) * 32;
+constexpr int kPieceBytes = 2048;       // bytes of one row piece (1024 bf16 columns)
+constexpr int kPieceCols = kPieceBytes / 2;
+constexpr int kMaxChunksPerLane = kPieceBytes / 16 / 32;   // 4
+constexpr int kSmemBudget = 227 * 1024;
+
+enum Mode : int { RD = 0, SH = 1, UP = 2 };
+
+struct DenseTArgs {
+    int mode, T, K;                     // K: input width (H for RD/SH, L+S for UP)
+    const __nv_bfloat16 *x;            // RD/SH: [T, H]
+    const float *acc;                  // UP: [T, L]
+    const float *cat;                  // UP: shared part at cat[:, L:], pitch L+S
+    const __nv_bfloat16 *gain;         // UP: [L] or null
+    float eps;
+    int L, S, E, H;
+    const __nv_bfloat16 *wa, *wb;      // RD: router, down; SH: w1, w3; UP: up, shared w2
+    float *out_a, *out_b;              // RD: logits [T,E], z [T,L]; SH: cat (+L), pitch L+S
+    __nv_bfloat16 *y;                  // UP: [T, H]
+    float b1, b2;
+    int units;                         // rows (RD: E+L, UP: H) or gate/up row pairs (SH: S)
+    int ns;                            // pipeline stages
+    int *err;
+};
+
+__device__ __forceinline__ int pieces_of(int cols) { return (cols + kPieceCols - 1) / kPieceCols; }
+
+// Piece p of a row: which matrix (0: wa, 1: wb), its first column inside that
+// matrix, its width, and where its activations start in the staged vector.
+// RD/SH rows are one matrix of H columns; UP rows are [Wu (L) | Ws2 (S)].
+struct Piece {
+    int mat, col0, ncol, xoff;
+};
+
+__device__ __forceinline__ Piece piece_info(const DenseTArgs &a, int p)
+{
+    Piece q;
+    if (a.mode != UP) {
+        q.mat = 0;
+        q.col0 = p * kPieceCols;
+        q.ncol = min(kPieceCols, a.H - q.col0);
+        q.xoff = q.col0;
+    } else {
+        const int pl = pieces_of(a.L);
+        q.mat = p < pl ? 0 : 1;
+        q.col0 = (p < pl ? p : p - pl) * kPieceCols;
+        q.ncol = min(kPieceCols, (p < pl ? a.L : a.S) - q.col0);
+        q.xoff = (p < pl ? 0 : a.L) + q.col0;
+    }
+    return q;
+}
+
+__device__ __forceinline__ int npieces_of(const DenseTArgs &a)
+{
+    return a.mode != UP ? pieces_of(a.H) : pieces_of(a.L) + pieces_of(a.S);
+}
+
+// acc += dot(8 bf16 weights, 8 bf16 activations): fp32 fused multiply-adds on
+// bf16 operands, two chains for instruction-level parallelism.
+__device__ __forceinline__ void dot8_bf16(const uint4 &w, const uint4 &x, float &a0, float &a1)
+{
+    asm("{\n\t.reg .b16 w0, w1, w2, w3, w4, w5, w6, w7, x0, x1, x2, x3, x4, x5, x6, x7;\n\t"
+        "mov.b32 {w0, w1}, %2;\n\tmov.b32 {w2, w3}, %3;\n\tmov.b32 {w4, w5}, %4;\n\tmov.b32 {w6, w7}, %5;\n\t"
+        "mov.b32 {x0, x1}, %6;\n\tmov.b32 {x2, x3}, %7;\n\tmov.b32 {x4, x5}, %8;\n\tmov.b32 {x6, x7}, %9;\n\t"
+        "fma.rn.f32.bf16 %0, w0, x0, %0;\n\tfma.rn.f32.bf16 %1, w1, x1, %1;\n\t"
+        "fma.rn.f32.bf16 %0, w2, x2, %0;\n\tfma.rn.f32.bf16 %1, w3, x3, %1;\n\t"
+        "fma.rn.f32.bf16 %0, w4, x4, %0;\n\tfma.rn.f32.bf16 %1, w5, x5, %1;\n\t"
+        "fma.rn.f32.bf16 %0, w6, x6, %0;\n\tfma.rn.f32.bf16 %1, w7, x7, %1;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "r"(w.x), "r"(w.y), "r"(w.z), "r"(w.w), "r"(x.x), "r"(x.y), "r"(x.z), "r"(x.w));
+}
+
+template <int TB>
+__global__ void __launch_bounds__(kThreads, 1) k_dense_tma(DenseTArgs a)
+{
+    extern __shared__ __align__(128) unsigned char sm[];
+    const bool sh = a.mode == SH;
+    // a stage holds one piece of every row of a group: 16 rows (RD, UP) or the
+    // gate and up rows of 16 pairs (SH)
+    const int rows_per_stage = sh ? 2 * kCW : kCW;
+    const int stage_bytes = rows_per_stage * kPieceBytes;
+    const int NS = a.ns;
+    __nv_bfloat16 *xs = reinterpret_cast<__nv_bfloat16 *>(sm + NS * stage_bytes);   // [TB][K]
+    uint64_t *full = reinterpret_cast<uint64_t *>(xs + TB * a.K);
+    uint64_t *empty = full + NS;
+    __shared__ float red[TB][kCW];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int npieces = npieces_of(a);
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NS; i++) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], kCW);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+    pdl_launch_dependents();
+    pdl_wait();
+
+    // balanced contiguous range of rows (or pairs) of this CTA
+    const int r0 = (int)((long long)a.units * blockIdx.x / gridDim.x);
+    const int r1 = (int)((long long)a.units * (blockIdx.x + 1) / gridDim.x);
+
+    if (warp == kCW) {
+        // ---------------- producer warp: weight pieces only ----------------
+        // lane 0 waits for the slot and posts the byte count, then each lane
+        // issues the copy of one row piece
+        const uint64_t pol = l2_policy_evict_first();
+        int slot = 0, issued = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int g0 = r0; g0 < r1 && ok; g0 += kCW) {
+            const int ng = min(kCW, r1 - g0);
+            for (int p = 0; p < npieces; p++) {
+                int good = 1;
+                if (lane == 0) good = mbar_wait(&empty[slot], phase ^ 1u, a.err, 400 + slot) ? 1 : 0;
+                good = __shfl_sync(0xffffffffu, good, 0);
+                if (!good) {
+                    ok = false;
+                    break;
+                }
+                const Piece q = piece_info(a, p);
+                const uint32_t nb = (uint32_t)q.ncol * 2u;
+                unsigned char *st = sm + slot * stage_bytes;
+                if (lane == 0) mbar_expect_tx(&full[slot], nb * (uint32_t)(sh ? 2 * ng : ng));
+                __syncwarp();
+                // lane l: unit l % 16 of the group; for SH lanes 16-31 take the up rows
+                const int i = lane & (kCW - 1), h = lane >> 4;
+                if (i < ng && (sh || h == 0)) {
+                    const int r = g0 + i;
+                    const __nv_bfloat16 *row;
+                    if (a.mode == RD)
+                        row = r < a.E ? a.wa + (size_t)r * a.H : a.wb + (size_t)(r - a.E) * a.H;
+                    else if (sh)
+                        row = (h == 0 ? a.wa : a.wb) + (size_t)r * a.H;
+                    else
+                        row = q.mat == 0 ? a.wa + (size_t)r * a.L : a.wb + (size_t)r * a.S;
+                    bulk_g2s(st + (h * kCW + i) * kPieceBytes, row + q.col0, nb, &full[slot], pol);
+                }
+                issued++;
+                if (++slot == NS) {
+                    slot = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+        if (lane == 0) {
+            const int n = issued < NS ? issued : NS;
+            for (int j = issued - n; j < issued; j++)
+                mbar_wait(&full[j % NS], (uint32_t)(j / NS) & 1u, a.err, 401);
+        }
+        return;
+    }
+
+    // ---------------- consumers: stage the activations as bf16 ----------------
+    const int nct = kCW * 32;
+    if (a.mode != UP) {
+        const int nv = TB * a.H / 8;
+        for (int i = threadIdx.x; i < nv; i += nct) {
+            const int t = (8 * i) / a.H;
+            reinterpret_cast<uint4 *>(xs)[i] =
+                t < a.T ? reinterpret_cast<const uint4 *>(a.x)[i] : make_uint4(0u, 0u, 0u, 0u);
+        }
+        asm volatile("bar.sync 1, %0;" ::"r"(nct));
+    } else {
+        // [RMSNorm(acc) * gain | shared SiTU], rounded to bf16
+        float ss[TB];
+#pragma unroll
+        for (int t = 0; t < TB; t++) {
+            ss[t] = 0.f;
+            for (int i = threadIdx.x; i < a.L / 4; i += nct) {
+                if (t < a.T) {
+                    const float4 v = reinterpret_cast<const float4 *>(a.acc + (size_t)t * a.L)[i];
+                    ss[t] += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+                }
+            }
+            ss[t] = warp_sum(ss[t]);
+            if (lane == 0) red[t][warp] = ss[t];
+        }
+        asm volatile("bar.sync 1, %0;" ::"r"(nct));
+#pragma unroll
+        for (int t = 0; t < TB; t++) {
+            float inv = 1.f;
+            if (a.gain) {
+                float tot = 0.f;
+#pragma unroll
+                for (int w = 0; w < kCW; w++) tot += red[t][w];
+                inv = 1.0f / sqrtf(tot / (float)a.L + a.eps);
+            }
+            for (int i = threadIdx.x; i < a.K / 2; i += nct) {
+                float2 v = make_float2(0.f, 0.f);
+                if (t < a.T) {
+                    if (2 * i < a.L) {
+                        v = reinterpret_cast<const float2 *>(a.acc + (size_t)t * a.L)[i];
+                        if (a.gain) {
+                            v.x *= inv * __bfloat162float(a.gain[2 * i]);
+                            v.y *= inv * __bfloat162float(a.gain[2 * i + 1]);
+                        }
+                    } else {
+                        v = reinterpret_cast<const float2 *>(a.cat + (size_t)t * a.K)[i];
+                    }
+                }
+                reinterpret_cast<__nv_bfloat162 *>(xs + t * a.K)[i] = __floats2bfloat162_rn(v.x, v.y);
+            }
+        }
+        asm volatile("bar.sync 1, %0;" ::"r"(nct));
+    }
+
+    // ---------------- consumers: stream ----------------
+    // warp w takes unit w of every group: row g0 + w (RD, UP) or the gate and
+    // up rows of pair g0 + w (SH)
+    int slot = 0;
+    uint32_t phase = 0;
+    for (int g0 = r0; g0 < r1; g0 += kCW) {
+        const int ng = min(kCW, r1 - g0);
+        const bool have = warp < ng;
+        float a0[TB], a1[TB], b0[TB], b1[TB];
+#pragma unroll
+        for (int t = 0; t < TB; t++) a0[t] = a1[t] = b0[t] = b1[t] = 0.f;
+        for (int p = 0; p < npieces; p++) {
+            if (!mbar_wait(&full[slot], phase, a.err, 410 + slot)) return;
+            if (have) {
+                const unsigned char *st = sm + slot * stage_bytes;
+                const Piece pc = piece_info(a, p);
+                const int nch = pc.ncol / 8;
+                const unsigned char *ra = st + warp * kPieceBytes;
+                const unsigned char *rb = st + (kCW + warp) * kPieceBytes;
+#pragma unroll
+                for (int q = 0; q < kMaxChunksPerLane; q++) {
+                    const int c = lane + 32 * q;
+                    if (c < nch) {
+                        const uint4 wa = *reinterpret_cast<const uint4 *>(ra + 16 * c);
+                        uint4 wb = make_uint4(0u, 0u, 0u, 0u);
+                        if (sh) wb = *reinterpret_cast<const uint4 *>(rb + 16 * c);
+#pragma unroll
+                        for (int t = 0; t < TB; t++) {
+                            const uint4 xv = *reinterpret_cast<const uint4 *>(xs + t * a.K + pc.xoff + 8 * c);
+                            dot8_bf16(wa, xv, a0[t], a1[t]);
+                            if (sh) dot8_bf16(wb, xv, b0[t], b1[t]);
+                        }
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[slot]);
+            if (++slot == NS) {
+                slot = 0;
+                phase ^= 1u;
+            }
+        }
+        float va[TB], vb[TB];
+#pragma unroll
+        for (int t = 0; t < TB; t++) {
+            va[t] = warp_sum(a0[t] + a1[t]);
+            vb[t] = sh ? warp_sum(b0[t] + b1[t]) : 0.f;
+        }
+        if (have && lane < TB && lane < a.T) {
+            const int t = lane;
+            float v0 = 0.f, v1 = 0.f;
+#pragma unroll
+            for (int q = 0; q < TB; q++)
+                if (q == t) {
+                    v0 = va[q];
+                    v1 = vb[q];
+                }
+            const int r = g0 + warp;
+            if (a.mode == RD) {
+                if (r < a.E) a.out_a[(size_t)t * a.E + r] = v0;
+                else a.out_b[(size_t)t * a.L + (r - a.E)] = v0;
+            } else if (sh) {
+                a.out_a[(size_t)t * (a.L + a.S) + a.L + r] = situ_f(v0, v1, a.b1, a.b2);
+            } else {
+                a.y[(size_t)t * a.H + r] = __float2bfloat16_rn(v0);
+            }
+        }
+    }
+}
+
+// Stages that fit beside the activations, at most 8.
+int stages_for(int mode, int K, int TB)
+{
+    const int stage = (mode == SH ? 2 * kCW : kCW) * kPieceBytes;
+    const int avail = kSmemBudget - TB * K * 2 - 2 * 8 * 8 - 1024;
+    const int ns = avail / stage;
+    return ns > 8 ? 8 : ns;
+}
+
+size_t dense_tma_smem(int mode, int K, int TB, int ns)
+{
+    return (size_t)ns * (mode == SH ? 2 * kCW : kCW) * kPieceBytes + (size_t)TB * K * 2 +
+           2 * ns * sizeof(uint64_t);
+}
+
+}  // namespace
+
+bool dense_tma_fits(const k3moe_config &c, int TB)
+{
+    return stages_for(SH, c.hidden, TB) >= 2 && stages_for(RD, c.hidden, TB) >= 2 &&
+           stages_for(UP, c.latent + c.shared_inter, TB) >= 2;
+}
+
+cudaError_t init_dense_tma(const k3moe_config &c)
+{
+    (void)c;
+    // dynamic shared memory never exceeds the budget minus 1 KB (stages_for),
+    // which leaves room for the kernel's static arrays
+    cudaError_t e = cudaFuncSetAttribute(k_dense_tma<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kSmemBudget - 1024);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(k_dense_tma<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kSmemBudget - 1024);
+}
+
+// part: 0 = router + down, 1 = shared gate/up, 2 = up (with the latent norm)
+cudaError_t launch_dense_tma(const k3moe &h, const LayerDev &w, const __nv_bfloat16 *x,
+                             __nv_bfloat16 *y, int T, cudaStream_t s, int part)
+{
+    const k3moe_config &c = h.cfg;
+    DenseTArgs a = {};
+    a.T = T;
+    a.L = c.latent;
+    a.S = c.shared_inter;
+    a.E = c.n_experts;
+    a.H = c.hidden;
+    a.b1 = c.situ_b1;
+    a.b2 = c.situ_b2;
+    a.eps = c.rms_eps;
+    a.err = h.ws.err;
+    a.x = x;
+    if (part == 0) {
+        a.mode = RD;
+        a.K = c.hidden;
+        a.wa = w.router_w;
+        a.wb = w.down_w;
+        a.out_a = h.ws.logits;
+        a.out_b = h.ws.z;
+        a.units = c.n_experts + c.latent;
+    } else if (part == 1) {
+        a.mode = SH;
+        a.K = c.hidden;
+        a.wa = w.sh_w1;
+        a.wb = w.sh_w3;
+        a.out_a = h.ws.cat;
+        a.units = c.shared_inter;
+    } else {
+        a.mode = UP;
+        a.K = c.latent + c.shared_inter;
+        a.wa = w.up_w;
+        a.wb = w.sh_w2;
+        a.acc = h.ws.acc;
+        a.cat = h.ws.cat;
+        a.gain = c.latent_norm ? w.gain : nullptr;
+        a.y = y;
+        a.units = c.hidden;
+    }
+    const int TB = T == 1 ? 1 : 2;
+    a.ns = stages_for(a.mode, a.K, TB);
+    const int groups = (a.units + kCW - 1) / kCW;
+    const int grid = groups < h.sm_count ? groups : h.sm_count;
+    const size_t smem = dense_tma_smem(a.mode, a.K, TB, a.ns);
+    return TB == 1 ? launch_pdl(k_dense_tma<1>, grid, kThreads, smem, s, a)
+                   : launch_pdl(k_dense_tma<2>, grid, kThreads, smem, s, a);
+}
+
+}  // namespace k3

@@ -12,14 +12,13 @@
 // Both kernels are persistent and warp-specialised (one CTA per SM):
 //   - one producer thread streams the weight rows through a ring of shared
 //     memory stages with bulk TMA copies (cp.async.bulk + mbarrier); a stage
-//     is 8 consecutive rows (of W1 and W3, or of W2) plus their scale bytes,
-//     and the first stage of a work unit also carries the unit's activation
-//     row;
-//   - eight consumer warps each take one row of every stage; lane l owns the
+//     is 16 consecutive rows (of W1 and W3, or of W2) plus their scale bytes,
+//     and a stage that starts a new (token, expert) pair also carries that
+//     pair's activation row;
+//   - sixteen consumer warps each take one row of every stage; lane l owns the
 //     column groups l, l+32, l+64, l+96 and keeps their activations in
-//     registers for the whole unit; after the unit's 8 stages one
-//     transpose-reduction across the warp gives each row's dot product.
-// A work unit is (pair, 64 weight rows), where a pair is one (token, expert)
+//     registers for the unit; a warp reduction gives each row's dot product.
+// A work unit is (pair, 16 or 64 weight rows), where a pair is one (token, expert)
 // assignment; units are ordered by (expert, row block, pair) so a second
 // token of the same expert re-reads rows the L2 has just seen.
 //
@@ -32,13 +31,18 @@
 
 namespace k3 {
 
-constexpr int kCW = 8;                  // consumer warps
+constexpr int kCW = 16;                 // consumer warps
 constexpr int kThreads = (kCW + 1) * 32;
-constexpr int kRowsPerWarp = 2;          // rows of one stage each consumer warp takes
+constexpr int kRowsPerWarp = 1;          // rows of one stage each consumer warp takes
 constexpr int kStageRows = kCW * kRowsPerWarp;          // 16
-constexpr int kUnitStages = 4;
-constexpr int kUnitRows = kStageRows * kUnitStages;     // 64
-constexpr int kUnitVals = kRowsPerWarp * kUnitStages;   // dot products per warp and unit
+// Stages per work unit: w13 units are one stage (fine-grained balance across
+// CTAs); w2 stages are smaller, so its units span four stages to amortise the
+// per-unit bookkeeping.
+template <bool W13> struct UnitShape {
+    static constexpr int stages = W13 ? 1 : 4;
+    static constexpr int rows = kStageRows * stages;
+    static constexpr int vals = kRowsPerWarp * stages;   // dot products per warp and unit
+};
 constexpr int kMaxQ = 4;                 // column groups per lane (K <= 4096)
 constexpr int kW13Stages = 3;
 constexpr int kW2Stages = 6;
@@ -47,7 +51,8 @@ struct StageMeta {
     int p;      // pair slot (perm order)
     int t;      // token
     int rb;     // row block
-    float f;    // w13: 2^zexp[t] (undoes the fp16 scaling of z); w2: routing weight
+    float f;    // w2: routing weight of the pair (w13 reads its factor from the z row)
+    int fresh;  // 1: the stage carries a new activation row (the pair changed)
 };
 
 struct ExpTArgs {
@@ -56,10 +61,9 @@ struct ExpTArgs {
     int R;          // rows per expert (I for w13, L for w2)
     int L, k, E, T;
     const int *offsets, *perm;
-    const __half *z16;     // w13 input [T, L]
-    const int *zexp;       // [T]
+    const __half *z16;     // w13 input [T, L + kZPad] (exponent in the padding)
     __half *h16;           // w13 output / w2 input [T*k, I]
-    const float *wts;      // [T, k]
+    const float *pair_w;   // [T*k] routing weight per pair slot
     float *acc;            // [T, L]
     float b1, b2;
     long long units;       // T*k*(R/64)
@@ -67,6 +71,7 @@ struct ExpTArgs {
 };
 
 __host__ __device__ constexpr int al128(int n) { return (n + 127) & ~127; }
+__host__ __device__ constexpr int ilog2c(int n) { return n <= 1 ? 0 : 1 + ilog2c(n / 2); }
 
 // Byte offsets inside one stage.
 struct StageLayout {
@@ -80,7 +85,7 @@ struct StageLayout {
         off_sa = two ? 2 * kStageRows * kb : kStageRows * kb;
         off_sb = off_sa + kStageRows * g;
         off_x = al128(off_sb + (two ? kStageRows * g : 0));
-        bytes = al128(off_x + 2 * K);
+        bytes = al128(off_x + 2 * (K + kZPad));
     }
 };
 
@@ -109,7 +114,9 @@ __device__ __forceinline__ float chunk_dot(const uint4 w, const uint32_t (&x)[16
         h0 = hfma2(a2, x[4 * q + 2], h0);
         h1 = hfma2(a3, x[4 * q + 3], h1);
     }
-    return f16x2_sum(h0) + f16x2_sum(h1);
+    uint32_t h;
+    asm("add.rn.f16x2 %0, %1, %2;" : "=r"(h) : "r"(h0), "r"(h1));
+    return f16x2_sum(h);
 }
 
 // Warp sum of each of v[0..N) (N a power of two, 2..32). Each halving step
@@ -142,6 +149,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tma(ExpTArgs a)
 {
     extern __shared__ __align__(128) unsigned char sm[];
     constexpr int NS = W13 ? kW13Stages : kW2Stages;
+    constexpr int kUnitStages = UnitShape<W13>::stages;
+    constexpr int kUnitRows = UnitShape<W13>::rows;
+    constexpr int kUnitVals = UnitShape<W13>::vals;
     const StageLayout lay(a.K, W13);
     uint64_t *full = reinterpret_cast<uint64_t *>(sm + NS * lay.bytes);
     uint64_t *empty = full + NS;
@@ -173,27 +183,47 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tma(ExpTArgs a)
         if (lane == 0) {
             const uint64_t pol_stream = l2_policy_evict_first();
             const uint64_t pol_keep = l2_policy_evict_last();
-            int slot = 0, issued = 0;
+            int slot = 0, issued = 0, prev_p = -1;
             uint32_t phase = 0;
             bool ok = true;
-            for (long long u = u0; u < u1 && ok; u++) {
-                const int e = find_expert(offs, a.E, u, RB);
-                const int off = offs[e], cnt = offs[e + 1] - off;
+            // unit decode from the shared-memory offsets; the two global loads a
+            // unit needs (token of the pair, its routing weight) are issued one
+            // unit ahead so that their latency overlaps the current unit's copies
+            struct U {
+                int e, cnt, rb, p;
+                bool bad;
+            };
+            auto decode = [&](long long u) {
+                U d;
+                d.e = find_expert(offs, a.E, u, RB);
+                const int off = offs[d.e];
+                d.cnt = offs[d.e + 1] - off;
                 const long long local = u - (long long)off * RB;
-                if (cnt <= 0 || local < 0 || local >= (long long)cnt * RB ||
-                    off + cnt > a.T * a.k) {
+                d.bad = d.cnt <= 0 || local < 0 || local >= (long long)d.cnt * RB ||
+                        off + d.cnt > a.T * a.k;
+                d.rb = d.bad ? 0 : (int)(local / d.cnt);
+                d.p = d.bad ? 0 : off + (int)(local % d.cnt);
+                return d;
+            };
+            U cur = decode(u0 < u1 ? u0 : 0);
+            int pf_cur = u0 < u1 ? a.perm[cur.p] : 0;
+            float w_cur = (!W13 && u0 < u1) ? a.pair_w[cur.p] : 0.f;
+            for (long long u = u0; u < u1 && ok; u++) {
+                U nxt = cur;
+                int pf_nxt = 0;
+                float w_nxt = 0.f;
+                if (u + 1 < u1) {
+                    nxt = decode(u + 1);
+                    pf_nxt = a.perm[nxt.p];
+                    if (!W13) w_nxt = a.pair_w[nxt.p];
+                }
+                const int e = cur.e, rb = cur.rb, p = cur.p, cnt = cur.cnt;
+                const int t = pf_cur / a.k;
+                if (cur.bad || t < 0 || t >= a.T) {
                     set_err(a.err, kErrBounds, (int)u);
                     break;
                 }
-                const int rb = (int)(local / cnt), i = (int)(local % cnt);
-                const int p = off + i;
-                const int pf = a.perm[p];
-                const int t = pf / a.k;
-                if (t < 0 || t >= a.T) {
-                    set_err(a.err, kErrBounds, (int)u);
-                    break;
-                }
-                const float f = W13 ? __uint_as_float((uint32_t)(127 + a.zexp[t]) << 23) : a.wts[pf];
+                const float f = w_cur;
                 const uint64_t pol = (cnt == 1) ? pol_stream : pol_keep;
                 const uint8_t *PA = a.pa + (size_t)e * eb, *SA = a.sa + (size_t)e * es;
                 const uint8_t *PB = W13 ? a.pb + (size_t)e * eb : nullptr;
@@ -203,11 +233,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tma(ExpTArgs a)
                         ok = false;
                         break;
                     }
-                    meta[slot] = StageMeta{p, t, rb, f};
+                    const int fresh = (s == 0 && p != prev_p) ? 1 : 0;
+                    if (s == 0) prev_p = p;
+                    meta[slot] = StageMeta{p, t, rb, f, fresh};
                     unsigned char *st = sm + slot * lay.bytes;
                     const int row0 = rb * kUnitRows + s * kStageRows;
                     uint32_t bytes = (uint32_t)(kStageRows * (lay.kb + lay.g)) * (W13 ? 2u : 1u);
-                    if (s == 0) bytes += 2u * a.K;
+                    const uint32_t xbytes = W13 ? 2u * (a.K + kZPad) : 2u * a.K;
+                    if (fresh) bytes += xbytes;
                     mbar_expect_tx(&full[slot], bytes);
                     bulk_g2s(st, PA + (size_t)row0 * lay.kb, kStageRows * lay.kb, &full[slot], pol);
                     bulk_g2s(st + lay.off_sa, SA + (size_t)row0 * lay.g, kStageRows * lay.g,
@@ -218,9 +251,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tma(ExpTArgs a)
                         bulk_g2s(st + lay.off_sb, SB + (size_t)row0 * lay.g, kStageRows * lay.g,
                                  &full[slot], pol);
                     }
-                    if (s == 0) {
-                        const __half *xsrc = W13 ? a.z16 + (size_t)t * a.K : a.h16 + (size_t)p * a.K;
-                        bulk_g2s(st + lay.off_x, xsrc, 2u * a.K, &full[slot], pol_keep);
+                    if (fresh) {
+                        const __half *xsrc = W13 ? a.z16 + (size_t)t * (a.K + kZPad)
+                                                 : a.h16 + (size_t)p * a.K;
+                        bulk_g2s(st + lay.off_x, xsrc, xbytes, &full[slot], pol_keep);
                     }
                     issued++;
                     if (++slot == NS) {
@@ -228,6 +262,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tma(ExpTArgs a)
                         phase ^= 1u;
                     }
                 }
+                cur = nxt;
+                pf_cur = pf_nxt;
+                w_cur = w_nxt;
             }
             // drain: no bulk copy may still target shared memory when the CTA exits
             const int n = issued < NS ? issued : NS;
@@ -241,6 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tma(ExpTArgs a)
     int slot = 0;
     uint32_t phase = 0;
     uint32_t xr[kMaxQ][16];
+    float fz = 1.f;
     for (long long u = u0; u < u1; u++) {
         float va[kUnitVals], vb[kUnitVals];
         int p = 0, t = 0, rb = 0;
@@ -258,7 +296,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tma(ExpTArgs a)
                 p = m.p;
                 t = m.t;
                 rb = m.rb;
-                f = m.f;
+                if (!W13) f = m.f;
+                // the activation row is reloaded only when the pair changes; w13's
+                // output factor 2^e (undoing z's fp16 scaling) rides in its padding
+                if (W13 && m.fresh)
+                    fz = __uint_as_float((uint32_t)(127 + *reinterpret_cast<const int *>(
+                                                              st + lay.off_x + 2 * a.K))
+                                         << 23);
+                if (m.fresh)
 #pragma unroll
                 for (int q = 0; q < kMaxQ; q++) {
                     const int g = lane + 32 * q;
@@ -306,28 +351,35 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tma(ExpTArgs a)
             }
         }
         if (!ok) return;
-        // value i = 2*s + hr belongs to row rb*64 + s*16 + hr*8 + warp
+        // value i (stage i / kRowsPerWarp, row hr = i % kRowsPerWarp of the warp)
+        // belongs to row rb*64 + stage*16 + hr*kCW + warp
         if (W13) {
-            float v[2 * kUnitVals];
+            constexpr int N = 2 * kUnitVals;
+            constexpr int sft = 5 - ilog2c(N);
+            float v[N];
 #pragma unroll
             for (int i = 0; i < kUnitVals; i++) {
                 v[i] = va[i];
                 v[kUnitVals + i] = vb[i];
             }
-            // lane l ends with v[l >> 1]: the gate of value l/2 for l < 16, its up at l + 16
-            const float r = transpose_reduce<2 * kUnitVals>(v, lane);
+            // lane l ends with v[l >> sft]: gate values first, their up values 16 lanes on
+            const float r = transpose_reduce<N>(v, lane);
             const float up = __shfl_down_sync(0xffffffffu, r, 16);
-            if (lane < 16 && (lane & 1) == 0) {
-                const int i = lane >> 1;
-                const int row = rb * kUnitRows + (i >> 1) * kStageRows + (i & 1) * kCW + warp;
-                a.h16[(size_t)p * a.R + row] = __float2half_rn(situ_f(r * f, up * f, a.b1, a.b2));
+            if (lane < 16 && (lane & ((1 << sft) - 1)) == 0) {
+                const int i = lane >> sft;
+                const int row = rb * kUnitRows + (i / kRowsPerWarp) * kStageRows +
+                                (i % kRowsPerWarp) * kCW + warp;
+                a.h16[(size_t)p * a.R + row] = __float2half_rn(situ_f(r * fz, up * fz, a.b1, a.b2));
             }
         } else {
-            // lane l ends with va[l >> 2]
-            const float r = transpose_reduce<kUnitVals>(va, lane);
-            if ((lane & 3) == 0) {
-                const int i = lane >> 2;
-                const int row = rb * kUnitRows + (i >> 1) * kStageRows + (i & 1) * kCW + warp;
+            constexpr int N = kUnitVals;
+            constexpr int sft = 5 - ilog2c(N);
+            // lane l ends with va[l >> sft]
+            const float r = transpose_reduce<N>(va, lane);
+            if ((lane & ((1 << sft) - 1)) == 0) {
+                const int i = lane >> sft;
+                const int row = rb * kUnitRows + (i / kRowsPerWarp) * kStageRows +
+                                (i % kRowsPerWarp) * kCW + warp;
                 atomicAdd(&a.acc[(size_t)t * a.L + row], f * r);
             }
         }
@@ -369,9 +421,8 @@ static ExpTArgs base_args(const k3moe &h, int T)
     a.offsets = h.ws.offsets;
     a.perm = h.ws.perm;
     a.z16 = h.ws.z16;
-    a.zexp = h.ws.zexp;
     a.h16 = h.ws.h16;
-    a.wts = h.ws.wts;
+    a.pair_w = h.ws.pair_w;
     a.acc = h.ws.acc;
     a.b1 = c.situ_b1;
     a.b2 = c.situ_b2;
@@ -388,7 +439,7 @@ cudaError_t launch_expert_w13(const k3moe &h, const LayerDev &w, int T, cudaStre
     a.sb = w.w3s;
     a.K = h.cfg.latent;
     a.R = h.cfg.moe_inter;
-    a.units = (long long)T * h.cfg.topk * (a.R / kUnitRows);
+    a.units = (long long)T * h.cfg.topk * (a.R / UnitShape<true>::rows);
     const int grid = (int)(a.units < h.sm_count ? a.units : h.sm_count);
     return launch_pdl(k_expert_tma<true>, grid, kThreads, exp_smem(a.K, true, a.E), s, a);
 }
@@ -402,7 +453,7 @@ cudaError_t launch_expert_w2(const k3moe &h, const LayerDev &w, int T, cudaStrea
     a.sb = nullptr;
     a.K = h.cfg.moe_inter;
     a.R = h.cfg.latent;
-    a.units = (long long)T * h.cfg.topk * (a.R / kUnitRows);
+    a.units = (long long)T * h.cfg.topk * (a.R / UnitShape<false>::rows);
     const int grid = (int)(a.units < h.sm_count ? a.units : h.sm_count);
     return launch_pdl(k_expert_tma<false>, grid, kThreads, exp_smem(a.K, false, a.E), s, a);
 }

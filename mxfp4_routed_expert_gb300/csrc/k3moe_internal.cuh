@@ -18,6 +18,7 @@ namespace k3 {
 constexpr int kGroup = 32;          // MXFP4 columns per ue8m0 scale
 constexpr int kMaxExperts = 1024;   // router select keeps 32 scores per lane
 constexpr int kMaxTopk = 32;
+constexpr int kZPad = 16;           // fp16 padding after each z16 row (holds its exponent)
 
 // Device error codes latched in Workspace::err (first one wins).
 enum : int { kErrNone = 0, kErrBounds = 1, kErrTimeout = 2 };
@@ -45,14 +46,15 @@ struct Workspace {
     size_t bytes = 0;
     float *logits = nullptr;      // [Tm, E]
     float *z = nullptr;           // [Tm, L]   latent (fp32, from the down projection)
-    __half *z16 = nullptr;        // [Tm, L]   z * 2^-zexp[t] in fp16 (expert GEMV input)
-    int *zexp = nullptr;          // [Tm]
+    __half *z16 = nullptr;        // [Tm, L + kZPad]: z * 2^-e in fp16, then e as an int32
+                                  //   in the row's padding (expert GEMV input)
     float *cat = nullptr;         // [Tm, L+S] normalised latent | shared SiTU
     int *ids = nullptr;           // [Tm, k]
     float *wts = nullptr;         // [Tm, k]
     int *counts = nullptr;        // [E]
     int *offsets = nullptr;       // [E+1]
     int *perm = nullptr;          // [Tm*k]
+    float *pair_w = nullptr;      // [Tm*k] routing weight of each pair slot (perm order)
     int *touched = nullptr;       // [E]  experts with at least one token, ascending
     int *n_touched = nullptr;     // [1]
     __half *h16 = nullptr;        // [Tm*k, I] SiTU output per (token, expert) pair, perm order
@@ -81,6 +83,7 @@ struct k3moe {
     cudaStream_t side = nullptr;
     cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
     int grid_up[3] = {0, 0, 0};      // k_up for TB = 1, 2, 4
+    bool dense_tma_ok[2] = {false, false};   // TMA-fed dense GEMVs usable for T = 1, 2
     // per-kernel timing (k3moe_set_profiling)
     bool profiling = false;
     std::deque<k3::ProfRec> prof;
@@ -111,6 +114,12 @@ cudaError_t launch_scale_scan(const uint8_t *p, size_t n, int *flag, cudaStream_
 cudaError_t init_dense_kernels(k3moe &h);
 cudaError_t init_route_kernels(const k3moe_config &c);
 cudaError_t init_expert_kernels(const k3moe_config &c);
+cudaError_t init_dense_tma(const k3moe_config &c);
+bool dense_tma_fits(const k3moe_config &c, int TB);
+// TMA-fed dense GEMVs for T <= 2. part 0: router + down; 1: shared gate/up;
+// 2: latent norm + up + shared down.
+cudaError_t launch_dense_tma(const k3moe &h, const LayerDev &w, const __nv_bfloat16 *x,
+                             __nv_bfloat16 *y, int T, cudaStream_t s, int part);
 bool expert_smem_fits(const k3moe_config &c);
 
 // ---- device helpers -----------------------------------------------------------

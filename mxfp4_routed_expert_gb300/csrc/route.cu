@@ -26,12 +26,12 @@ struct RouteArgs {
     int *ids;              // [T, k]
     float *wts;            // [T, k]
     const float *z;        // [T, L]
-    __half *z16;           // [T, L]
-    int *zexp;             // [T]
+    __half *z16;           // [T, L + kZPad]: scaled fp16 z, then the exponent (int32)
     float *acc;            // [T, L]
     int L;
     int fuse_perm;         // T == 1: also write counts/offsets/perm/touched
     int *counts, *offsets, *perm, *touched, *n_touched;
+    float *pair_w;
     int *err;
 };
 
@@ -174,11 +174,11 @@ __global__ void __launch_bounds__(kRouteThreads) k_route(RouteArgs a)
     for (int q = 0; q < kZPer; q++) {
         const int i = tid + q * kRouteThreads;
         if (i < a.L) {
-            a.z16[(size_t)t * a.L + i] = __float2half_rn(zv[q] * zsc);
+            a.z16[(size_t)t * (a.L + kZPad) + i] = __float2half_rn(zv[q] * zsc);
             a.acc[(size_t)t * a.L + i] = 0.f;
         }
     }
-    if (tid == 0) a.zexp[t] = ex;
+    if (tid == 0) *reinterpret_cast<int *>(a.z16 + (size_t)t * (a.L + kZPad) + a.L) = ex;
 
     // ---- warp 0: selection order (ch desc, id asc), weights, and for T == 1
     //      the permutation tables ----
@@ -199,10 +199,12 @@ __global__ void __launch_bounds__(kRouteThreads) k_route(RouteArgs a)
         for (int o = 16; o > 0; o >>= 1) ssum += __shfl_xor_sync(0xffffffffu, ssum, o);
         if (have) {
             const bool rn = a.renorm && ssum > 0.f;
+            const float wv = (rn ? sc / ssum : sc) * a.routed_scale;
             a.ids[(size_t)t * a.k + rank] = e;
-            a.wts[(size_t)t * a.k + rank] = (rn ? sc / ssum : sc) * a.routed_scale;
+            a.wts[(size_t)t * a.k + rank] = wv;
             if (a.fuse_perm) {   // single token: one pair per picked expert, in id order
                 a.perm[id_rank] = rank;
+                a.pair_w[id_rank] = wv;
                 a.touched[id_rank] = e;
             }
         }
@@ -237,7 +239,6 @@ cudaError_t launch_route(const k3moe &h, const LayerDev &w, int T, cudaStream_t 
     a.wts = h.ws.wts;
     a.z = h.ws.z;
     a.z16 = h.ws.z16;
-    a.zexp = h.ws.zexp;
     a.acc = h.ws.acc;
     a.L = c.latent;
     a.fuse_perm = T == 1;
@@ -246,6 +247,7 @@ cudaError_t launch_route(const k3moe &h, const LayerDev &w, int T, cudaStream_t 
     a.perm = h.ws.perm;
     a.touched = h.ws.touched;
     a.n_touched = h.ws.n_touched;
+    a.pair_w = h.ws.pair_w;
     a.err = h.ws.err;
     return launch_pdl(k_route, T, kRouteThreads, 0, s, a);
 }
@@ -254,8 +256,10 @@ cudaError_t launch_route(const k3moe &h, const LayerDev &w, int T, cudaStream_t 
 
 struct PermArgs {
     const int *ids;   // [T, k]
+    const float *wts; // [T, k]
     int T, k, E;
     int *counts, *offsets, *perm, *touched, *n_touched;
+    float *pair_w;    // [T*k] weight of each pair slot
     int *err;
 };
 
@@ -342,6 +346,7 @@ __global__ void __launch_bounds__(1024) k_perm(PermArgs a)
             if (ee >= 0 && ee < a.E) {
                 const int pos = base[ee] + atomicAdd(&hist[warp * a.E + ee], 1);
                 a.perm[pos] = t * a.k + lane;
+                a.pair_w[pos] = a.wts[(size_t)t * a.k + lane];
             }
         }
         __syncwarp();
@@ -353,6 +358,8 @@ cudaError_t launch_perm(const k3moe &h, int T, cudaStream_t s)
     const k3moe_config &c = h.cfg;
     PermArgs a;
     a.ids = h.ws.ids;
+    a.wts = h.ws.wts;
+    a.pair_w = h.ws.pair_w;
     a.T = T;
     a.k = c.topk;
     a.E = c.n_experts;
