@@ -75,6 +75,9 @@ size_t carve_workspace(const k3moe_config &c, char *base, Workspace *ws)
     w.n_touched = cv.take<int>(1);
     w.h16 = cv.take<__half>(Tm * K * I);
     w.acc = cv.take<float>(Tm * L);
+    w.act = cv.take<__nv_bfloat16>(Tm * (L + S));
+    w.gemm_part = cv.take<float>(dense_gemm_part_floats(c));
+    w.gemm_tiles = cv.take<int>(dense_gemm_tile_counters(c));
     w.xbuf0 = cv.take<__nv_bfloat16>(Tm * H);
     w.xbuf1 = cv.take<__nv_bfloat16>(Tm * H);
     w.err = cv.take<int>(4);
@@ -191,15 +194,21 @@ int run_layer(k3moe *h, const LayerDev &w, const __nv_bfloat16 *x, __nv_bfloat16
     // stream s:    router+down -> route -> permute -> [join] -> experts -> up
     // side stream:  [after router+down] shared-expert gate/up (overlaps route, permute)
     const bool tma = T <= 2 && h->dense_tma_ok[T - 1];
-    K3_STEP("router_down_gemv", tma ? launch_dense_tma(*h, w, x, nullptr, T, s, 0)
-                                    : launch_dense_x(*h, w, x, T, s, 0));
+    const bool gemm = T >= kGemmMinTokens && h->gemm_ok;
+    if (gemm) {
+        K3_STEP("router_down_gemm", launch_dense_gemm(*h, w, x, nullptr, T, s, 0));
+    } else {
+        K3_STEP("router_down_gemv", tma ? launch_dense_tma(*h, w, x, nullptr, T, s, 0)
+                                        : launch_dense_x(*h, w, x, T, s, 0));
+    }
     if (cudaEventRecord(h->ev_fork, s) != cudaSuccess ||
         cudaStreamWaitEvent(h->side, h->ev_fork, 0) != cudaSuccess)
         return K3MOE_ERR_CUDA;
     {
-        Prof p_(h, "shared_gate_up_gemv", h->side);
-        e = tma ? launch_dense_tma(*h, w, x, nullptr, T, h->side, 1)
-                : launch_dense_x(*h, w, x, T, h->side, 1);
+        Prof p_(h, gemm ? "shared_gate_up_gemm" : "shared_gate_up_gemv", h->side);
+        e = gemm ? launch_dense_gemm(*h, w, x, nullptr, T, h->side, 1)
+                 : tma ? launch_dense_tma(*h, w, x, nullptr, T, h->side, 1)
+                       : launch_dense_x(*h, w, x, T, h->side, 1);
     }
     if (e != cudaSuccess || cudaEventRecord(h->ev_join, h->side) != cudaSuccess)
         return K3MOE_ERR_CUDA;
@@ -208,8 +217,13 @@ int run_layer(k3moe *h, const LayerDev &w, const __nv_bfloat16 *x, __nv_bfloat16
     if (cudaStreamWaitEvent(s, h->ev_join, 0) != cudaSuccess) return K3MOE_ERR_CUDA;
     K3_STEP("expert_w13_gemv", launch_expert_w13(*h, w, T, s));
     K3_STEP("expert_w2_gemv", launch_expert_w2(*h, w, T, s));
-    K3_STEP("norm_up_shared_gemv", tma ? launch_dense_tma(*h, w, nullptr, y, T, s, 2)
-                                       : launch_up(*h, w, y, T, s));
+    if (gemm) {
+        K3_STEP("latent_rmsnorm", launch_norm_act(*h, w, T, s));
+        K3_STEP("up_shared_gemm", launch_dense_gemm(*h, w, nullptr, y, T, s, 2));
+    } else {
+        K3_STEP("norm_up_shared_gemv", tma ? launch_dense_tma(*h, w, nullptr, y, T, s, 2)
+                                           : launch_up(*h, w, y, T, s));
+    }
 #undef K3_STEP
     h->last_T = T;
     return K3MOE_OK;
@@ -295,7 +309,7 @@ int k3moe_create(const k3moe_config *cfg, k3moe **out)
     }
     if (cudaMemset(blk, 0, need) != cudaSuccess || init_dense_kernels(*h) != cudaSuccess ||
         init_route_kernels(*cfg) != cudaSuccess || init_expert_kernels(*cfg) != cudaSuccess ||
-        init_dense_tma(*cfg) != cudaSuccess ||
+        init_dense_tma(*cfg) != cudaSuccess || init_dense_gemm() != cudaSuccess ||
         cudaDeviceSynchronize() != cudaSuccess) {
         cudaGetLastError();
         cudaStreamDestroy(h->side);
@@ -307,6 +321,9 @@ int k3moe_create(const k3moe_config *cfg, k3moe **out)
     }
     h->dense_tma_ok[0] = dense_tma_fits(*cfg, 1);
     h->dense_tma_ok[1] = dense_tma_fits(*cfg, 2);
+    // every TMA box of the GEMMs must lie inside its tensor: 128-row weight tiles
+    h->gemm_ok = cfg->n_experts >= 128 && cfg->latent >= 128 && cfg->shared_inter >= 128 &&
+                 cfg->hidden >= 128;
     h->layers.resize((size_t)cfg->max_layers);
     *out = h;
     return K3MOE_OK;

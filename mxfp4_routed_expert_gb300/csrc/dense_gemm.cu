@@ -1,0 +1,377 @@
+// Dense projections of the layer as tcgen05 tensor-core GEMMs (prefill and
+// batched decode, T >= 16).
+//
+// The steps (kimi-k3-in-c README, Part II section 9, k3_moe steps 1, 2, 5, 6):
+//   RD: router logits x . Wr (E rows) and latent down projection x . Wd (L rows);
+//   SH: the fused shared experts' gate/up pair with SiTU-GLU in the epilogue;
+//   UP: y = Wu . n + Ws2 . s over the concatenated K = L + S.
+//
+// Orientation: the weight rows are the MMA's M (A operand, 128-row tiles) and
+// the tokens its N (B operand, 16..256 per tile), so small token counts waste
+// no tensor work on padding rows. A and B are K-major bf16 tiles of 64 columns
+// (128 bytes, 128-byte swizzle) loaded by TMA into a ring of shared-memory
+// stages; one thread issues tcgen05.mma (kind::f16, fp32 accumulators in
+// TMEM) and commits each stage back to the producer; after the last k-tile all
+// four warps read the accumulators with tcgen05.ld and run the epilogue. When
+// the (M, N) tile grid is too small to occupy the GPU, K is split across CTAs
+// whose fp32 partials meet in global memory by atomic addition; the last CTA
+// of a tile (counted in global memory) applies the epilogue.
+#include <algorithm>
+
+#include "k3moe_internal.cuh"
+#include "tc_common.cuh"
+
+namespace k3 {
+
+namespace {
+
+constexpr int BM = 128, BK = 64;
+constexpr int kThreads = 128;
+constexpr int kSmemBudget = 227 * 1024;
+
+enum Mode : int { RD = 0, SH = 1, UP = 2 };
+
+struct GemmArgs {
+    int mode;
+    int T;           // tokens (N extent)
+    int BN;          // N tile (multiple of 16, <= 256)
+    int KT;          // k-tiles in total
+    int KTA;         // UP: k-tiles taken from map a0 (the rest from a1); RD: m-tiles of map a0
+    int splits;      // split-K factor
+    int ns;          // pipeline stages
+    int E, L, S, H;
+    float *logits, *z;          // RD outputs (fp32 [T,E], [T,L])
+    float *cat;                 // SH: fp32 copy of the shared SiTU at cat[:, L:] (pitch L+S)
+    __nv_bfloat16 *act;         // SH: bf16 shared SiTU at act[:, L:] (pitch L+S)
+    __nv_bfloat16 *y;           // UP output [T, H]
+    float b1, b2;
+    float *part;                // split-K partials [T, 2*R] fp32 (zeroed), R = rows of the mode
+    int *tile_count;            // split-K arrival counters per (m-tile, n-tile), left at 0
+    int *err;
+};
+
+__device__ __forceinline__ void epilogue_store(const GemmArgs &g, int row, int n, float v0, float v1)
+{
+    if (g.mode == RD) {
+        if (row < g.E) g.logits[(size_t)n * g.E + row] = v0;
+        else g.z[(size_t)n * g.L + (row - g.E)] = v0;
+    } else if (g.mode == SH) {
+        const float s = situ_f(v0, v1, g.b1, g.b2);
+        g.cat[(size_t)n * (g.L + g.S) + g.L + row] = s;
+        g.act[(size_t)n * (g.L + g.S) + g.L + row] = __float2bfloat16_rn(s);
+    } else {
+        g.y[(size_t)n * g.H + row] = __float2bfloat16_rn(v0);
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    k_dense_gemm(const __grid_constant__ CUtensorMap a0, const __grid_constant__ CUtensorMap a1,
+                 const __grid_constant__ CUtensorMap b, GemmArgs g)
+{
+    extern __shared__ unsigned char raw[];
+    unsigned char *sm = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const bool dual = g.mode == SH;
+    const int a_bytes = BM * BK * 2, b_bytes = g.BN * BK * 2;
+    const int stage_bytes = (dual ? 2 : 1) * a_bytes + b_bytes;
+    uint64_t *full = reinterpret_cast<uint64_t *>(sm + g.ns * stage_bytes);
+    uint64_t *empty = full + g.ns;
+    uint64_t *done = empty + g.ns;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(done + 1);
+    __shared__ int last_flag;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nt = blockIdx.x, mt = blockIdx.y, ks = blockIdx.z;
+    const uint32_t tcols = dual ? 2u * (uint32_t)g.BN : (uint32_t)g.BN;
+    uint32_t alloc_cols = 32;
+    while (alloc_cols < tcols) alloc_cols <<= 1;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < g.ns; i++) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        mbar_init(done, 1);
+        fence_mbar_init();
+        tc::prefetch_map(&a0);
+        tc::prefetch_map(&a1);
+        tc::prefetch_map(&b);
+    }
+    if (warp == 2) tc::tmem_alloc(tslot, alloc_cols);
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    pdl_launch_dependents();
+    pdl_wait();
+    const uint32_t tmem = *tslot;
+
+    // k-tile range of this split
+    const int kt0 = (int)((long long)g.KT * ks / g.splits);
+    const int kt1 = (int)((long long)g.KT * (ks + 1) / g.splits);
+    const int n0 = nt * g.BN;
+    // RD: m-tiles [0, KTA) come from the router map, the rest from the down map
+    const CUtensorMap *amap = &a0;
+    int arow = mt * BM;
+    if (g.mode == RD && mt >= g.KTA) {
+        amap = &a1;
+        arow = (mt - g.KTA) * BM;
+    }
+
+    if (warp == 0 && lane == 0) {
+        // ---------------- TMA producer ----------------
+        for (int kt = kt0; kt < kt1; kt++) {
+            const int i = kt - kt0, s = i % g.ns;
+            const uint32_t ph = (uint32_t)(i / g.ns) & 1u;
+            if (!mbar_wait(&empty[s], ph ^ 1u, g.err, 500)) break;
+            unsigned char *st = sm + s * stage_bytes;
+            mbar_expect_tx(&full[s], (uint32_t)stage_bytes);
+            if (g.mode == UP) {
+                const bool first = kt < g.KTA;
+                tc::tma_load_2d(st, first ? &a0 : &a1, (first ? kt : kt - g.KTA) * BK, arow, &full[s]);
+            } else {
+                tc::tma_load_2d(st, amap, kt * BK, arow, &full[s]);
+                if (dual) tc::tma_load_2d(st + a_bytes, &a1, kt * BK, arow, &full[s]);
+            }
+            tc::tma_load_2d(st + (dual ? 2 : 1) * a_bytes, &b, kt * BK, n0, &full[s]);
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ---------------- MMA issuer ----------------
+        const uint32_t idesc = tc::idesc_bf16(BM, g.BN);
+        for (int kt = kt0; kt < kt1; kt++) {
+            const int i = kt - kt0, s = i % g.ns;
+            const uint32_t ph = (uint32_t)(i / g.ns) & 1u;
+            if (!mbar_wait(&full[s], ph, g.err, 501)) break;
+            tc::fence_after();
+            const uint32_t sa = tc::su32(sm + s * stage_bytes);
+            const uint32_t sb = sa + (dual ? 2 : 1) * a_bytes;
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; kk++) {
+                const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
+                tc::mma_bf16(tmem, tc::desc_sw128(sa + kk * 32), tc::desc_sw128(sb + kk * 32), idesc, acc);
+                if (dual)
+                    tc::mma_bf16(tmem + (uint32_t)g.BN, tc::desc_sw128(sa + a_bytes + kk * 32),
+                                 tc::desc_sw128(sb + kk * 32), idesc, acc);
+            }
+            tc::commit(&empty[s]);
+        }
+        tc::commit(done);
+    }
+    __syncwarp();
+
+    // ---------------- epilogue: all four warps ----------------
+    const bool have_acc = kt1 > kt0;
+    if (have_acc) mbar_wait(done, 0, g.err, 502);
+    tc::fence_after();
+    const int row_in_tile = warp * 32 + lane;
+    // rows of this tile in the mode's row numbering
+    int row;
+    bool row_ok;
+    if (g.mode == RD) {
+        row = mt < g.KTA ? mt * BM + row_in_tile : g.E + (mt - g.KTA) * BM + row_in_tile;
+        row_ok = mt < g.KTA ? row < g.E : (row - g.E) < g.L;
+    } else {
+        row = mt * BM + row_in_tile;
+        row_ok = row < (g.mode == SH ? g.S : g.H);
+    }
+    const int R = g.mode == RD ? g.E + g.L : (g.mode == SH ? g.S : g.H);
+    const uint32_t tbase = tmem + ((uint32_t)(warp * 32) << 16);
+
+    if (g.splits == 1) {
+        for (int c = 0; c < g.BN; c += 16) {
+            float v0[16], v1[16];
+            tc::tmem_ld16(tbase + (uint32_t)c, v0);
+            if (dual) tc::tmem_ld16(tbase + (uint32_t)(g.BN + c), v1);
+#pragma unroll
+            for (int j = 0; j < 16; j++) {
+                const int n = n0 + c + j;
+                if (row_ok && n < g.T) epilogue_store(g, row, n, v0[j], dual ? v1[j] : 0.f);
+            }
+        }
+    } else {
+        // partial sums meet in g.part; the last CTA of the tile finishes it
+        if (have_acc) {
+            for (int c = 0; c < g.BN; c += 16) {
+                float v0[16], v1[16];
+                tc::tmem_ld16(tbase + (uint32_t)c, v0);
+                if (dual) tc::tmem_ld16(tbase + (uint32_t)(g.BN + c), v1);
+#pragma unroll
+                for (int j = 0; j < 16; j++) {
+                    const int n = n0 + c + j;
+                    if (row_ok && n < g.T) {
+                        atomicAdd(&g.part[(size_t)n * 2 * R + row], v0[j]);
+                        if (dual) atomicAdd(&g.part[(size_t)n * 2 * R + R + row], v1[j]);
+                    }
+                }
+            }
+        }
+        __threadfence();
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            int *cnt = &g.tile_count[mt * gridDim.x + nt];
+            const int prev = atomicAdd(cnt, 1);
+            last_flag = prev == g.splits - 1;
+            if (last_flag) *cnt = 0;   // leave the counter ready for the next launch
+        }
+        __syncthreads();
+        if (last_flag) {
+            __threadfence();
+            for (int c = 0; c < g.BN; c++) {
+                const int n = n0 + c;
+                if (row_ok && n < g.T) {
+                    float *pp = &g.part[(size_t)n * 2 * R];
+                    const float v0 = __ldcg(&pp[row]);
+                    const float v1 = dual ? __ldcg(&pp[R + row]) : 0.f;
+                    pp[row] = 0.f;          // leave the partials zeroed for the next launch
+                    if (dual) pp[R + row] = 0.f;
+                    epilogue_store(g, row, n, v0, v1);
+                }
+            }
+        }
+    }
+    tc::fence_before();
+    __syncthreads();
+    if (warp == 2) {
+        tc::fence_after();
+        tc::tmem_dealloc(tmem, alloc_cols);
+    }
+}
+
+// N tile: a multiple of 16 no larger than T (every TMA box stays inside the
+// token extent), at most 256.
+int pick_bn(int T)
+{
+    int bn = (T / 16) * 16;
+    return bn > 256 ? 256 : bn;
+}
+
+int stages_for(int mode, int BN)
+{
+    const int stage = (mode == SH ? 2 : 1) * BM * BK * 2 + BN * BK * 2;
+    int ns = (kSmemBudget - 2048) / stage;
+    return ns > 8 ? 8 : ns;
+}
+
+}  // namespace
+
+cudaError_t init_dense_gemm()
+{
+    return cudaFuncSetAttribute(k_dense_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kSmemBudget - 1024);
+}
+
+size_t dense_gemm_part_floats(const k3moe_config &c)
+{
+    const int R = std::max(std::max(c.n_experts + c.latent, c.shared_inter), c.hidden);
+    return (size_t)kSplitTokensMax * 2 * (size_t)R;
+}
+
+size_t dense_gemm_tile_counters(const k3moe_config &c)
+{
+    const int R = std::max(std::max(c.n_experts + c.latent, c.shared_inter), c.hidden);
+    return (size_t)((R + BM - 1) / BM + 8) * (size_t)((kSplitTokensMax + 15) / 16);
+}
+
+// part: 0 = router + down, 1 = shared gate/up, 2 = up + shared down (needs the
+// normed latent in act[:, :L] and the shared SiTU in act[:, L:]).
+cudaError_t launch_dense_gemm(const k3moe &h, const LayerDev &w, const __nv_bfloat16 *x,
+                              __nv_bfloat16 *y, int T, cudaStream_t s, int part)
+{
+    const k3moe_config &c = h.cfg;
+    GemmArgs g = {};
+    g.mode = part;
+    g.T = T;
+    g.BN = pick_bn(T);
+    g.E = c.n_experts;
+    g.L = c.latent;
+    g.S = c.shared_inter;
+    g.H = c.hidden;
+    g.logits = h.ws.logits;
+    g.z = h.ws.z;
+    g.cat = h.ws.cat;
+    g.act = h.ws.act;
+    g.y = y;
+    g.b1 = c.situ_b1;
+    g.b2 = c.situ_b2;
+    g.part = h.ws.gemm_part;
+    g.tile_count = h.ws.gemm_tiles;
+    g.err = h.ws.err;
+    CUtensorMap a0, a1, b;
+    int mtiles;
+    bool ok = true;
+    if (part == 0) {
+        const int mta = (c.n_experts + BM - 1) / BM;
+        mtiles = mta + (c.latent + BM - 1) / BM;
+        g.KTA = mta;
+        g.KT = c.hidden / BK;
+        ok = tc::make_map_bf16_sw128(&a0, w.router_w, c.n_experts, c.hidden, c.hidden, BM) &&
+             tc::make_map_bf16_sw128(&a1, w.down_w, c.latent, c.hidden, c.hidden, BM) &&
+             tc::make_map_bf16_sw128(&b, x, T, c.hidden, c.hidden, g.BN);
+    } else if (part == 1) {
+        mtiles = (c.shared_inter + BM - 1) / BM;
+        g.KT = c.hidden / BK;
+        ok = tc::make_map_bf16_sw128(&a0, w.sh_w1, c.shared_inter, c.hidden, c.hidden, BM) &&
+             tc::make_map_bf16_sw128(&a1, w.sh_w3, c.shared_inter, c.hidden, c.hidden, BM) &&
+             tc::make_map_bf16_sw128(&b, x, T, c.hidden, c.hidden, g.BN);
+    } else {
+        mtiles = (c.hidden + BM - 1) / BM;
+        g.KTA = c.latent / BK;
+        g.KT = (c.latent + c.shared_inter) / BK;
+        ok = tc::make_map_bf16_sw128(&a0, w.up_w, c.hidden, c.latent, c.latent, BM) &&
+             tc::make_map_bf16_sw128(&a1, w.sh_w2, c.hidden, c.shared_inter, c.shared_inter, BM) &&
+             tc::make_map_bf16_sw128(&b, h.ws.act, T, c.latent + c.shared_inter,
+                                     c.latent + c.shared_inter, g.BN);
+    }
+    if (!ok) return cudaErrorInvalidValue;
+    const int ntiles = (T + g.BN - 1) / g.BN;
+    int splits = 1;
+    if (T <= kSplitTokensMax) {
+        while (splits < 8 && mtiles * ntiles * splits * 2 <= h.sm_count && g.KT / (splits * 2) >= 4)
+            splits *= 2;
+    }
+    g.splits = splits;
+    g.ns = stages_for(part, g.BN);
+    const size_t smem = (size_t)g.ns * ((part == 1 ? 2 : 1) * BM * BK * 2 + g.BN * BK * 2) + 1024 + 256;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)ntiles, (unsigned)mtiles, (unsigned)splits);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k_dense_gemm, a0, a1, b, g);
+}
+
+// act[t, 0:L] = bf16(acc[t] / sqrt(mean(acc[t]^2) + eps) * gain): the latent
+// norm of the aggregate for the tensor-core up projection.
+__global__ void __launch_bounds__(256) k_norm_act(const float *acc, const __nv_bfloat16 *gain,
+                                                  __nv_bfloat16 *act, int L, int ld, float eps)
+{
+    __shared__ float red[8];
+    pdl_launch_dependents();
+    pdl_wait();
+    const int t = blockIdx.x;
+    const float *a = acc + (size_t)t * L;
+    float ss = 0.f;
+    for (int i = threadIdx.x; i < L; i += blockDim.x) ss = fmaf(a[i], a[i], ss);
+    ss = warp_sum(ss);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    float tot = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; i++) tot += red[i];
+    const float inv = gain ? 1.0f / sqrtf(tot / (float)L + eps) : 1.f;
+    for (int i = threadIdx.x; i < L; i += blockDim.x)
+        act[(size_t)t * ld + i] = __float2bfloat16_rn(gain ? a[i] * inv * __bfloat162float(gain[i]) : a[i]);
+}
+
+cudaError_t launch_norm_act(const k3moe &h, const LayerDev &w, int T, cudaStream_t s)
+{
+    const k3moe_config &c = h.cfg;
+    return launch_pdl(k_norm_act, T, 256, 0, s, (const float *)h.ws.acc,
+                      (const __nv_bfloat16 *)(c.latent_norm ? w.gain : nullptr), h.ws.act, c.latent,
+                      c.latent + c.shared_inter, c.rms_eps);
+}
+
+}  // namespace k3

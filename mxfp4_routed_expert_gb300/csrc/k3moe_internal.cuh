@@ -19,6 +19,8 @@ constexpr int kGroup = 32;          // MXFP4 columns per ue8m0 scale
 constexpr int kMaxExperts = 1024;   // router select keeps 32 scores per lane
 constexpr int kMaxTopk = 32;
 constexpr int kZPad = 16;           // fp16 padding after each z16 row (holds its exponent)
+constexpr int kSplitTokensMax = 128;  // tensor-core GEMMs split K only up to this many tokens
+constexpr int kGemmMinTokens = 16;    // tensor-core dense GEMMs from this many tokens on
 
 // Device error codes latched in Workspace::err (first one wins).
 enum : int { kErrNone = 0, kErrBounds = 1, kErrTimeout = 2 };
@@ -59,6 +61,9 @@ struct Workspace {
     int *n_touched = nullptr;     // [1]
     __half *h16 = nullptr;        // [Tm*k, I] SiTU output per (token, expert) pair, perm order
     float *acc = nullptr;         // [Tm, L]
+    __nv_bfloat16 *act = nullptr;     // [Tm, L+S] bf16 [normed latent | shared SiTU] (GEMM path)
+    float *gemm_part = nullptr;       // split-K partial sums (kept zeroed between launches)
+    int *gemm_tiles = nullptr;        // split-K arrival counters (kept at zero)
     __nv_bfloat16 *xbuf0 = nullptr;   // [Tm, H] staging (host forward, chain)
     __nv_bfloat16 *xbuf1 = nullptr;   // [Tm, H]
     int *err = nullptr;           // [4] device error word + detail
@@ -84,6 +89,7 @@ struct k3moe {
     cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
     int grid_up[3] = {0, 0, 0};      // k_up for TB = 1, 2, 4
     bool dense_tma_ok[2] = {false, false};   // TMA-fed dense GEMVs usable for T = 1, 2
+    bool gemm_ok = false;                    // tensor-core dense GEMMs usable (T >= 16)
     // per-kernel timing (k3moe_set_profiling)
     bool profiling = false;
     std::deque<k3::ProfRec> prof;
@@ -115,6 +121,14 @@ cudaError_t init_dense_kernels(k3moe &h);
 cudaError_t init_route_kernels(const k3moe_config &c);
 cudaError_t init_expert_kernels(const k3moe_config &c);
 cudaError_t init_dense_tma(const k3moe_config &c);
+cudaError_t init_dense_gemm();
+size_t dense_gemm_part_floats(const k3moe_config &c);
+size_t dense_gemm_tile_counters(const k3moe_config &c);
+// tcgen05 dense GEMMs (T >= 16). part 0: router + down; 1: shared gate/up;
+// 2: up + shared down (reads Workspace::act).
+cudaError_t launch_dense_gemm(const k3moe &h, const LayerDev &w, const __nv_bfloat16 *x,
+                              __nv_bfloat16 *y, int T, cudaStream_t s, int part);
+cudaError_t launch_norm_act(const k3moe &h, const LayerDev &w, int T, cudaStream_t s);
 bool dense_tma_fits(const k3moe_config &c, int TB);
 // TMA-fed dense GEMVs for T <= 2. part 0: router + down; 1: shared gate/up;
 // 2: latent norm + up + shared down.

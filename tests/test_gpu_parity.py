@@ -55,6 +55,17 @@ def test_mid_shape(T):
     run_case(MID, k3synth.TINY_RECIPE, 1, T)
 
 
+# 128 experts: every weight matrix has at least 128 rows, so T >= 16 runs the
+# dense projections on the tcgen05 tensor-core GEMMs (T <= 128 with split-K)
+WIDE = k3synth.Shape(hidden=1024, latent=512, n_experts=128, topk=8, moe_inter=512,
+                     shared_inter=1024)
+
+
+@pytest.mark.parametrize("T", [16, 37, 100, 300])
+def test_tensor_core_dense_path(T):
+    run_case(WIDE, k3synth.TINY_RECIPE, 6, T)
+
+
 def test_mid_shape_no_bias_no_renorm():
     shape = k3synth.replace(MID, renorm=0, routed_scale=0.5)
     run_case(shape, k3synth.replace(k3synth.TINY_RECIPE, zero_bias=True), 2, 9)
