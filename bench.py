@@ -59,7 +59,6 @@ WORKLOADS = {
     "decode_t1_e64": dict(T=1, layers=1, desc="K3 row shapes with 64 routed experts, decode T=1 "
                           "(small case for profiler captures)"),
 }
-ZIPF_ALPHA = 0.55
 
 
 def measured_peaks():
@@ -103,7 +102,7 @@ def make_inputs(workload, seed=0, layer_index=0):
         d = k3synth.with_bias(d, np.zeros(shape.n_experts, np.float32))
         x = k3synth.covering_tokens(shape, d, seed, T)
     elif workload == "prefill_t4096":
-        d = k3synth.with_bias(d, k3synth.zipf_bias(shape, seed, layer_index, ZIPF_ALPHA))
+        d = k3synth.with_bias(d, k3synth.zipf_bias(shape, seed, layer_index, k3synth.K3_ZIPF_ALPHA))
         x = k3synth.make_tokens(shape, seed, T, stream=11)
     else:
         x = k3synth.make_tokens(shape, seed, T, stream=13)

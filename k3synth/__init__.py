@@ -218,6 +218,15 @@ def make_layer(shape: Shape, seed: int, layer: int = 0,
     return d
 
 
+def make_router(shape: Shape, seed: int, layer: int = 0,
+                recipe: WeightRecipe = K3_RECIPE) -> dict:
+    """Only the router tensors of make_layer (same streams, same values)."""
+    E, H = shape.n_experts, shape.hidden
+    return {"router_w": normal_bf16((E, H), key(seed, TROUTER, layer), 0.0, recipe.dense_sigma),
+            "router_bias": (np.zeros(E, np.float32) if recipe.zero_bias
+                            else normal_f32((E,), key(seed, TBIAS, layer), 0.0, recipe.bias_sigma))}
+
+
 def make_tokens(shape: Shape, seed: int, T: int, stream: int = 0,
                 attempts: np.ndarray | None = None, sigma: float = 1.0) -> np.ndarray:
     """x [T, H] bf16 bits, row t drawn from its own stream (seed, stream, t, attempt[t])."""
@@ -253,6 +262,12 @@ def covering_tokens(shape: Shape, layer: dict, seed: int, T: int, a: float = 15.
         for j in range(k):
             out64[t] += a * dirs[(k * t + j) % E]
     return round_bf16(out64)
+
+
+# Bias strength that gives the K3 prefill workload a Zipf(1.1) expert popularity
+# (pick counts sorted by rank fall with slope -1.1 in log-log over ranks
+# 1..256); written by tests/golden/calibrate_zipf.py into zipf_alpha.json.
+K3_ZIPF_ALPHA = 0.059509
 
 
 def zipf_bias(shape: Shape, seed: int, layer: int, alpha: float, s: float = 1.1) -> np.ndarray:

@@ -178,7 +178,7 @@ def test_chain_two_layers_tiny():
 @pytest.fixture(scope="module")
 def k3layer():
     d = k3synth.make_layer(k3synth.K3, 0, 0, k3synth.K3_RECIPE)
-    lay = Layer(k3synth.K3, [d], max_tokens=64)
+    lay = Layer(k3synth.K3, [d], max_tokens=4096)
     yield d, lay
     lay.close()
 
@@ -224,3 +224,25 @@ def test_k3_T64_random(k3layer):
     ref, tr = oracle.layer_forward(shape, d, x, trace=True)
     check_routing(r, shape, x, tr["ids"], tr["w"])
     assert_close(bf16_to_f64(y), ref, "K3 T=64 random")
+
+
+def test_k3_T4096_zipf_prefill(k3layer):
+    """Prefill: 4096 tokens, Zipf(1.1) expert popularity through the router
+    bias. Ids and the permutation are checked on every token, y on 64 sampled
+    tokens (every 64th) against the oracle."""
+    d, lay = k3layer
+    shape = k3synth.K3
+    dz = k3synth.with_bias(d, k3synth.zipf_bias(shape, 0, 0, k3synth.K3_ZIPF_ALPHA))
+    lay.load(0, dz)
+    try:
+        T = 4096
+        x, _ = guarded_tokens(shape, dz, 0, T, stream=11)
+        y = lay.forward(x)
+        r = lay.routing(T)
+        ids, w, _ = oracle.route(shape, dz, x)
+        check_routing(r, shape, x, ids, w)
+        rows = np.arange(0, T, 64, dtype=np.int32)
+        ref = oracle.layer_forward(shape, dz, x, rows=rows)
+        assert_close(bf16_to_f64(y)[rows], ref, "K3 T=4096 Zipf (sampled rows)")
+    finally:
+        lay.load(0, d)
