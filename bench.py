@@ -222,6 +222,8 @@ def run_native(args, rank, world):
 
     shape, d0, xpool = make_inputs(args.workload)
     h = km.k3moe_create(km.make_config(shape, max_layers=n_layers, max_tokens=T, device=dev))
+    km.k3moe_set_expert_path(h, {"auto": km.K3MOE_EXPERT_AUTO, "gemv": km.K3MOE_EXPERT_GEMV,
+                                 "gemm": km.K3MOE_EXPERT_GEMM}[args.expert_path])
     w, keep = km.layer_weights(d0, shape.n_experts, km.K3MOE_HOST)
     km.k3moe_load_layer(h, 0, w)
     del keep
@@ -412,6 +414,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--workload", choices=list(WORKLOADS), default="decode_t1")
+    ap.add_argument("--expert-path", choices=["auto", "gemv", "gemm"], default="auto",
+                    help="routed-expert kernels: auto (grouped GEMM from T >= 16), per-pair GEMVs, or GEMM")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()

@@ -171,6 +171,23 @@ K3MOE_API int k3moe_get_intermediate(k3moe *h, int which, void *dst, size_t byte
  * device-side error, or the first asynchronous CUDA error. */
 K3MOE_API int k3moe_sync_status(k3moe *h);
 
+/* Which routed-expert kernels a forward uses (same arithmetic, kimi-k3-in-c
+ * README, Part II section 9, k3_moe step 3; results agree to fp32 rounding
+ * order and fp16 operand rounding):
+ *   K3MOE_EXPERT_AUTO  (default) the grouped tensor-core GEMM when the batch
+ *                      holds at least 128 (token, expert) pairs and T >= 16,
+ *                      else the per-pair GEMVs;
+ *   K3MOE_EXPERT_GEMV  always the per-pair GEMVs (streaming dequantisation);
+ *   K3MOE_EXPERT_GEMM  the grouped GEMM whenever T * topk >= 128 (below that
+ *                      the GEMVs run: its n-tile needs 128 pair rows).
+ * The grouped GEMM needs latent and moe_inter to be multiples of 128 and
+ * max_tokens * topk >= 128; asking for K3MOE_EXPERT_GEMM on a handle whose
+ * shape does not allow it returns K3MOE_ERR_SHAPE and leaves the mode as it
+ * was. Returns K3MOE_ERR_INVALID_ARG for an unknown mode. Takes effect at the
+ * next forward; not thread-safe with a forward on the same handle. */
+enum { K3MOE_EXPERT_AUTO = 0, K3MOE_EXPERT_GEMV = 1, K3MOE_EXPERT_GEMM = 2 };
+K3MOE_API int k3moe_set_expert_path(k3moe *h, int mode);
+
 /* Per-kernel timing: with profiling on, every kernel a forward launches is
  * bracketed by CUDA events on the launching stream. k3moe_profile_read
  * synchronises, aggregates per kernel name and resets the record. */

@@ -36,8 +36,9 @@ K3MOE_T_Z, K3MOE_T_ACC, K3MOE_T_SHARED, K3MOE_T_LOGITS = 1, 2, 3, 4
 EXPORTS = ("k3moe_create", "k3moe_load_layer", "k3moe_forward", "k3moe_forward_chain",
            "k3moe_forward_host", "k3moe_get_routing", "k3moe_get_intermediate",
            "k3moe_sync_status", "k3moe_set_profiling", "k3moe_profile_read", "k3moe_destroy",
-           "k3moe_strerror", "k3moe_abi_version", "k3moe_route_static")
+           "k3moe_strerror", "k3moe_abi_version", "k3moe_route_static", "k3moe_set_expert_path")
 K3MOE_ROUTE_STATIC_MAX_LOGITS = 1 << 20
+K3MOE_EXPERT_AUTO, K3MOE_EXPERT_GEMV, K3MOE_EXPERT_GEMM = 0, 1, 2
 
 
 class K3MoEError(RuntimeError):
@@ -96,6 +97,7 @@ def lib():
         L.k3moe_get_intermediate.argtypes = [vp, i, vp, sz, vp]
         L.k3moe_sync_status.argtypes = [vp]
         L.k3moe_set_profiling.argtypes = [vp, i]
+        L.k3moe_set_expert_path.argtypes = [vp, i]
         L.k3moe_profile_read.argtypes = [vp, ctypes.POINTER(k3moe_kernel_stat), i,
                                          ctypes.POINTER(ctypes.c_int)]
         L.k3moe_destroy.argtypes = [vp]
@@ -246,6 +248,12 @@ def k3moe_sync_status(h: int) -> int:
 def k3moe_set_profiling(h: int, enable: bool) -> int:
     return _check(lib().k3moe_set_profiling(ctypes.c_void_p(h), int(bool(enable))),
                   "k3moe_set_profiling")
+
+
+def k3moe_set_expert_path(h: int, mode: int) -> int:
+    """K3MOE_EXPERT_AUTO / _GEMV / _GEMM: which routed-expert kernels forwards use."""
+    return _check(lib().k3moe_set_expert_path(ctypes.c_void_p(h), int(mode)),
+                  "k3moe_set_expert_path")
 
 
 def k3moe_profile_read(h: int, max_entries: int = 32):

@@ -75,6 +75,10 @@ size_t carve_workspace(const k3moe_config &c, char *base, Workspace *ws)
     w.n_touched = cv.take<int>(1);
     w.h16 = cv.take<__half>(Tm * K * I);
     w.acc = cv.take<float>(Tm * L);
+    const bool eg = expert_gemm_ok(c);
+    w.zperm = cv.take<__half>(eg ? Tm * K * (L + kZPad) : 0);
+    w.tiles = cv.take<int2>(eg ? expert_gemm_max_tiles(c) : 0);
+    w.n_tiles = cv.take<int>(1);
     w.act = cv.take<__nv_bfloat16>(Tm * (L + S));
     w.gemm_part = cv.take<float>(dense_gemm_part_floats(c));
     w.gemm_tiles = cv.take<int>(dense_gemm_tile_counters(c));
@@ -88,7 +92,7 @@ size_t carve_workspace(const k3moe_config &c, char *base, Workspace *ws)
 }
 
 struct LayerSizes {
-    size_t router, bias, down, up, gain, sh13, sh2, e13p, e13s, e2p, e2s;
+    size_t router, bias, down, up, gain, sh13, sh2, e13p, e13s, e2p, e2s, e13m, e2m;
     size_t total;
 };
 
@@ -107,9 +111,11 @@ LayerSizes layer_sizes(const k3moe_config &c)
     z.e13s = E * I * (L / kGroup);
     z.e2p = E * L * (I / 2);
     z.e2s = E * L * (I / kGroup);
+    z.e13m = E * I;
+    z.e2m = E * L;
     z.total = al256(z.router) + al256(z.bias) + al256(z.down) + al256(z.up) + al256(z.gain) +
               2 * al256(z.sh13) + al256(z.sh2) + 2 * al256(z.e13p) + 2 * al256(z.e13s) +
-              al256(z.e2p) + al256(z.e2s);
+              al256(z.e2p) + al256(z.e2s) + 2 * al256(z.e13m) + al256(z.e2m);
     return z;
 }
 
@@ -181,6 +187,14 @@ struct Prof {
     }
 };
 
+// Grouped tensor-core expert GEMM or per-pair GEMVs for this batch.
+bool use_expert_gemm(const k3moe &h, int T)
+{
+    if (!h.egemm_ok || h.expert_path == K3MOE_EXPERT_GEMV) return false;
+    if (T * h.cfg.topk < expert_gemm_min_pairs()) return false;
+    return h.expert_path == K3MOE_EXPERT_GEMM || T >= kGemmMinTokens;
+}
+
 int run_layer(k3moe *h, const LayerDev &w, const __nv_bfloat16 *x, __nv_bfloat16 *y, int T,
               cudaStream_t s)
 {
@@ -195,6 +209,7 @@ int run_layer(k3moe *h, const LayerDev &w, const __nv_bfloat16 *x, __nv_bfloat16
     // side stream:  [after router+down] shared-expert gate/up (overlaps route, permute)
     const bool tma = T <= 2 && h->dense_tma_ok[T - 1];
     const bool gemm = T >= kGemmMinTokens && h->gemm_ok;
+    const bool egemm = use_expert_gemm(*h, T);
     if (gemm) {
         K3_STEP("router_down_gemm", launch_dense_gemm(*h, w, x, nullptr, T, s, 0));
     } else {
@@ -215,8 +230,15 @@ int run_layer(k3moe *h, const LayerDev &w, const __nv_bfloat16 *x, __nv_bfloat16
     K3_STEP("route_topk", launch_route(*h, w, T, s));
     if (T > 1) K3_STEP("permute", launch_perm(*h, T, s));   // T == 1: written by route_topk
     if (cudaStreamWaitEvent(s, h->ev_join, 0) != cudaSuccess) return K3MOE_ERR_CUDA;
-    K3_STEP("expert_w13_gemv", launch_expert_w13(*h, w, T, s));
-    K3_STEP("expert_w2_gemv", launch_expert_w2(*h, w, T, s));
+    if (egemm) {
+        K3_STEP("expert_tiles", launch_expert_tiles(*h, s));
+        K3_STEP("gather_latent", launch_gather_latent(*h, T, s));
+        K3_STEP("expert_w13_gemm", launch_expert_gemm(*h, w, T, s, true));
+        K3_STEP("expert_w2_gemm", launch_expert_gemm(*h, w, T, s, false));
+    } else {
+        K3_STEP("expert_w13_gemv", launch_expert_w13(*h, w, T, s));
+        K3_STEP("expert_w2_gemv", launch_expert_w2(*h, w, T, s));
+    }
     if (gemm) {
         K3_STEP("latent_rmsnorm", launch_norm_act(*h, w, T, s));
         K3_STEP("up_shared_gemm", launch_dense_gemm(*h, w, nullptr, y, T, s, 2));
@@ -310,6 +332,7 @@ int k3moe_create(const k3moe_config *cfg, k3moe **out)
     if (cudaMemset(blk, 0, need) != cudaSuccess || init_dense_kernels(*h) != cudaSuccess ||
         init_route_kernels(*cfg) != cudaSuccess || init_expert_kernels(*cfg) != cudaSuccess ||
         init_dense_tma(*cfg) != cudaSuccess || init_dense_gemm() != cudaSuccess ||
+        init_expert_gemm() != cudaSuccess ||
         cudaDeviceSynchronize() != cudaSuccess) {
         cudaGetLastError();
         cudaStreamDestroy(h->side);
@@ -324,6 +347,7 @@ int k3moe_create(const k3moe_config *cfg, k3moe **out)
     // every TMA box of the GEMMs must lie inside its tensor: 128-row weight tiles
     h->gemm_ok = cfg->n_experts >= 128 && cfg->latent >= 128 && cfg->shared_inter >= 128 &&
                  cfg->hidden >= 128;
+    h->egemm_ok = expert_gemm_ok(*cfg);
     h->layers.resize((size_t)cfg->max_layers);
     *out = h;
     return K3MOE_OK;
@@ -391,6 +415,8 @@ int k3moe_load_layer(k3moe *h, int layer, const k3moe_layer_weights *w)
     uint8_t *w1p = cv.take<uint8_t>(z.e13p), *w1s = cv.take<uint8_t>(z.e13s);
     uint8_t *w3p = cv.take<uint8_t>(z.e13p), *w3s = cv.take<uint8_t>(z.e13s);
     uint8_t *w2p = cv.take<uint8_t>(z.e2p), *w2s = cv.take<uint8_t>(z.e2s);
+    uint8_t *w1m = cv.take<uint8_t>(z.e13m), *w3m = cv.take<uint8_t>(z.e13m);
+    uint8_t *w2m = cv.take<uint8_t>(z.e2m);
 
     const cudaMemcpyKind kind =
         w->where == K3MOE_HOST ? cudaMemcpyHostToDevice : cudaMemcpyDeviceToDevice;
@@ -428,6 +454,9 @@ int k3moe_load_layer(k3moe *h, int layer, const k3moe_layer_weights *w)
             launch_scale_scan(w1s, z.e13s, flag, 0) != cudaSuccess ||
             launch_scale_scan(w3s, z.e13s, flag, 0) != cudaSuccess ||
             launch_scale_scan(w2s, z.e2s, flag, 0) != cudaSuccess ||
+            launch_row_scale_max(w1s, z.e13m, c.latent / kGroup, w1m) != cudaSuccess ||
+            launch_row_scale_max(w3s, z.e13m, c.latent / kGroup, w3m) != cudaSuccess ||
+            launch_row_scale_max(w2s, z.e2m, c.moe_inter / kGroup, w2m) != cudaSuccess ||
             cudaMemcpy(&bad, flag, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
             rc = K3MOE_ERR_CUDA;
         else if (bad)
@@ -452,6 +481,9 @@ int k3moe_load_layer(k3moe *h, int layer, const k3moe_layer_weights *w)
     L.w3s = w3s;
     L.w2p = w2p;
     L.w2s = w2s;
+    L.w1max = w1m;
+    L.w3max = w3m;
+    L.w2max = w2m;
     L.loaded = true;
     free_layer(h->layers[(size_t)layer]);
     h->layers[(size_t)layer] = L;
@@ -589,6 +621,16 @@ int k3moe_sync_status(k3moe *h)
         return word[0] == kErrTimeout ? K3MOE_ERR_TIMEOUT : K3MOE_ERR_DEVICE;
     }
     if (cudaGetLastError() != cudaSuccess) return K3MOE_ERR_CUDA;
+    return K3MOE_OK;
+}
+
+int k3moe_set_expert_path(k3moe *h, int mode)
+{
+    if (!h) return K3MOE_ERR_INVALID_ARG;
+    if (mode != K3MOE_EXPERT_AUTO && mode != K3MOE_EXPERT_GEMV && mode != K3MOE_EXPERT_GEMM)
+        return K3MOE_ERR_INVALID_ARG;
+    if (mode == K3MOE_EXPERT_GEMM && !h->egemm_ok) return K3MOE_ERR_SHAPE;
+    h->expert_path = mode;
     return K3MOE_OK;
 }
 

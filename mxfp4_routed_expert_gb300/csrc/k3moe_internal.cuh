@@ -40,6 +40,9 @@ struct LayerDev {
     const uint8_t *w1p = nullptr, *w1s = nullptr;   // [E][I][L/2], [E][I][L/32]
     const uint8_t *w3p = nullptr, *w3s = nullptr;
     const uint8_t *w2p = nullptr, *w2s = nullptr;   // [E][L][I/2], [E][L][I/32]
+    // largest scale byte of each expert row (tensor-core expert GEMM operand rebasing)
+    const uint8_t *w1max = nullptr, *w3max = nullptr;   // [E][I]
+    const uint8_t *w2max = nullptr;                     // [E][L]
 };
 
 // Per-handle scratch, sized for max_tokens (Tm).
@@ -61,6 +64,9 @@ struct Workspace {
     int *n_touched = nullptr;     // [1]
     __half *h16 = nullptr;        // [Tm*k, I] SiTU output per (token, expert) pair, perm order
     float *acc = nullptr;         // [Tm, L]
+    __half *zperm = nullptr;      // [Tm*k, L + kZPad] z16 rows gathered in pair order (expert GEMM)
+    int2 *tiles = nullptr;        // (expert, n-tile) list of the expert GEMM
+    int *n_tiles = nullptr;       // [1]
     __nv_bfloat16 *act = nullptr;     // [Tm, L+S] bf16 [normed latent | shared SiTU] (GEMM path)
     float *gemm_part = nullptr;       // split-K partial sums (kept zeroed between launches)
     int *gemm_tiles = nullptr;        // split-K arrival counters (kept at zero)
@@ -90,6 +96,8 @@ struct k3moe {
     int grid_up[3] = {0, 0, 0};      // k_up for TB = 1, 2, 4
     bool dense_tma_ok[2] = {false, false};   // TMA-fed dense GEMVs usable for T = 1, 2
     bool gemm_ok = false;                    // tensor-core dense GEMMs usable (T >= 16)
+    bool egemm_ok = false;                   // tensor-core expert GEMM usable (shape)
+    int expert_path = K3MOE_EXPERT_AUTO;     // k3moe_set_expert_path
     // per-kernel timing (k3moe_set_profiling)
     bool profiling = false;
     std::deque<k3::ProfRec> prof;
@@ -129,6 +137,16 @@ size_t dense_gemm_tile_counters(const k3moe_config &c);
 cudaError_t launch_dense_gemm(const k3moe &h, const LayerDev &w, const __nv_bfloat16 *x,
                               __nv_bfloat16 *y, int T, cudaStream_t s, int part);
 cudaError_t launch_norm_act(const k3moe &h, const LayerDev &w, int T, cudaStream_t s);
+// tcgen05 grouped expert GEMM (many pairs per expert): the n-tile list, the
+// latent gathered into pair order, then W1/W3 (w13) or W2.
+bool expert_gemm_ok(const k3moe_config &c);
+size_t expert_gemm_max_tiles(const k3moe_config &c);
+int expert_gemm_min_pairs();
+cudaError_t init_expert_gemm();
+cudaError_t launch_expert_tiles(const k3moe &h, cudaStream_t s);
+cudaError_t launch_gather_latent(const k3moe &h, int T, cudaStream_t s);
+cudaError_t launch_expert_gemm(const k3moe &h, const LayerDev &w, int T, cudaStream_t s, bool w13);
+cudaError_t launch_row_scale_max(const uint8_t *s, size_t rows, int G, uint8_t *out);
 bool dense_tma_fits(const k3moe_config &c, int TB);
 // TMA-fed dense GEMVs for T <= 2. part 0: router + down; 1: shared gate/up;
 // 2: latent norm + up + shared down.

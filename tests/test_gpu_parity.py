@@ -23,12 +23,16 @@ def _built():
     build.build()
 
 
-def run_case(shape, recipe, seed, T, stream=0, check_intermediates=True):
+def run_case(shape, recipe, seed, T, stream=0, check_intermediates=True, expert_path=None,
+             d=None):
     import mxfp4_routed_expert_gb300 as km
-    d = k3synth.make_layer(shape, seed, 0, recipe)
+    if d is None:
+        d = k3synth.make_layer(shape, seed, 0, recipe)
     x, _ = guarded_tokens(shape, d, seed, T, stream)
     lay = Layer(shape, [d], max_tokens=T)
     try:
+        if expert_path is not None:
+            km.k3moe_set_expert_path(lay.h, expert_path)
         y = lay.forward(x)
         r = lay.routing(T)
         z = lay.intermediate(km.K3MOE_T_Z, T, shape.latent)
@@ -64,6 +68,63 @@ WIDE = k3synth.Shape(hidden=1024, latent=512, n_experts=128, topk=8, moe_inter=5
 @pytest.mark.parametrize("T", [16, 37, 100, 300])
 def test_tensor_core_dense_path(T):
     run_case(WIDE, k3synth.TINY_RECIPE, 6, T)
+
+
+@pytest.mark.parametrize("T,path", [(16, "gemm"), (37, "gemv"), (300, "gemv"), (20, "gemm")])
+def test_expert_paths(T, path):
+    """Both routed-expert paths against the oracle: the per-pair GEMVs and the
+    grouped tcgen05 GEMM (T=16 with topk 8 is its smallest batch, 128 pairs)."""
+    import mxfp4_routed_expert_gb300 as km
+    mode = km.K3MOE_EXPERT_GEMM if path == "gemm" else km.K3MOE_EXPERT_GEMV
+    run_case(WIDE, k3synth.TINY_RECIPE, 6, T, expert_path=mode)
+
+
+@pytest.mark.parametrize("path", ["gemm", "gemv"])
+def test_expert_gemm_multi_tile(path):
+    """Four experts forced into every token's selection (+10 router bias): each
+    holds all 300 tokens, three n-tiles of the grouped GEMM (128, 128, 44)."""
+    import mxfp4_routed_expert_gb300 as km
+    d = k3synth.make_layer(WIDE, 8, 0, k3synth.TINY_RECIPE)
+    bias = np.asarray(d["router_bias"], np.float32).copy()
+    bias[[3, 40, 77, 127]] += 10.0
+    d = k3synth.with_bias(d, bias)
+    mode = km.K3MOE_EXPERT_GEMM if path == "gemm" else km.K3MOE_EXPERT_GEMV
+    run_case(WIDE, k3synth.TINY_RECIPE, 8, 300, expert_path=mode, d=d)
+
+
+def test_expert_path_selection_and_errors():
+    import mxfp4_routed_expert_gb300 as km
+    d = k3synth.make_layer(WIDE, 6, 0, k3synth.TINY_RECIPE)
+    x = k3synth.make_tokens(WIDE, 6, 37)
+    lay = Layer(WIDE, [d], max_tokens=37)
+    try:
+        with pytest.raises(km.K3MoEError) as ei:
+            km.k3moe_set_expert_path(lay.h, 7)
+        assert ei.value.code == km.K3MOE_ERR_INVALID_ARG
+        km.k3moe_set_profiling(lay.h, True)
+        lay.forward(x)                                   # auto: 296 pairs -> grouped GEMM
+        auto = {s[0] for s in km.k3moe_profile_read(lay.h)}
+        km.k3moe_set_expert_path(lay.h, km.K3MOE_EXPERT_GEMV)
+        lay.forward(x)
+        gemv = {s[0] for s in km.k3moe_profile_read(lay.h)}
+        km.k3moe_set_expert_path(lay.h, km.K3MOE_EXPERT_GEMM)
+        lay.forward(x[:8])                               # 64 pairs: below one n-tile -> GEMVs
+        small = {s[0] for s in km.k3moe_profile_read(lay.h)}
+        km.k3moe_set_profiling(lay.h, False)
+    finally:
+        lay.close()
+    gemm_names = {"expert_tiles", "gather_latent", "expert_w13_gemm", "expert_w2_gemm"}
+    gemv_names = {"expert_w13_gemv", "expert_w2_gemv"}
+    assert gemm_names <= auto and not (gemv_names & auto)
+    assert gemv_names <= gemv and not (gemm_names & gemv)
+    assert gemv_names <= small and not (gemm_names & small)
+    tiny = Layer(k3synth.TINY, [None], max_tokens=4)     # 16 pairs at most: no grouped GEMM
+    try:
+        with pytest.raises(km.K3MoEError) as ei:
+            km.k3moe_set_expert_path(tiny.h, km.K3MOE_EXPERT_GEMM)
+        assert ei.value.code == km.K3MOE_ERR_SHAPE
+    finally:
+        tiny.close()
 
 
 def test_mid_shape_no_bias_no_renorm():
@@ -145,8 +206,9 @@ def test_routing_is_deterministic_and_profiling_lists_kernels():
     for k in ("ids", "counts", "offsets", "perm"):
         np.testing.assert_array_equal(a[k], b[k])
     names = {s[0] for s in stats}
-    assert {"router_down_gemv", "shared_gate_up_gemv", "route_topk", "permute",
-            "expert_w13_gemv", "expert_w2_gemv", "norm_up_shared_gemv"} <= names
+    # T=20 (160 pairs): dense GEMVs (64 experts < 128 rows), grouped expert GEMM
+    assert {"router_down_gemv", "shared_gate_up_gemv", "route_topk", "permute", "expert_tiles",
+            "gather_latent", "expert_w13_gemm", "expert_w2_gemm", "norm_up_shared_gemv"} <= names
     assert all(s[1] == 2 and s[2] > 0 for s in stats)
 
 
@@ -216,14 +278,21 @@ def test_k3_T64_covering(k3layer):
 
 
 def test_k3_T64_random(k3layer):
+    """Both routed-expert paths (auto picks the grouped GEMM at T=64)."""
+    import mxfp4_routed_expert_gb300 as km
     d, lay = k3layer
     shape = k3synth.K3
     x, _ = guarded_tokens(shape, d, 0, 64, stream=9)
-    y = lay.forward(x)
-    r = lay.routing(64)
     ref, tr = oracle.layer_forward(shape, d, x, trace=True)
-    check_routing(r, shape, x, tr["ids"], tr["w"])
-    assert_close(bf16_to_f64(y), ref, "K3 T=64 random")
+    try:
+        for mode in (km.K3MOE_EXPERT_AUTO, km.K3MOE_EXPERT_GEMV):
+            km.k3moe_set_expert_path(lay.h, mode)
+            y = lay.forward(x)
+            r = lay.routing(64)
+            check_routing(r, shape, x, tr["ids"], tr["w"])
+            assert_close(bf16_to_f64(y), ref, f"K3 T=64 random, expert path {mode}")
+    finally:
+        km.k3moe_set_expert_path(lay.h, km.K3MOE_EXPERT_AUTO)
 
 
 def test_k3_T4096_zipf_prefill(k3layer):
