@@ -58,6 +58,10 @@ WORKLOADS = {
     # small case for ncu captures: K3 row shapes, 64 experts (1.2 GB), decode T=1
     "decode_t1_e64": dict(T=1, layers=1, desc="K3 row shapes with 64 routed experts, decode T=1 "
                           "(small case for profiler captures)"),
+    "batch_t64_e64": dict(T=64, layers=1, desc="K3 row shapes with 64 routed experts, T=64 "
+                          "(16 pairs per expert; small case for profiler captures)"),
+    "prefill_t512_e64": dict(T=512, layers=1, desc="K3 row shapes with 64 routed experts, T=512 "
+                             "(128 pairs per expert; small case for profiler captures)"),
 }
 
 
@@ -93,7 +97,8 @@ def layer_bytes(shape, T, n_touched):
 # ---- inputs ----------------------------------------------------------------------
 
 def make_inputs(workload, seed=0, layer_index=0):
-    shape = k3synth.K3 if workload != "decode_t1_e64" else k3synth.replace(k3synth.K3, n_experts=64)
+    shape = (k3synth.replace(k3synth.K3, n_experts=64) if workload.endswith("_e64")
+             else k3synth.K3)
     d = k3synth.make_layer(shape, seed, layer_index, k3synth.K3_RECIPE)
     T = WORKLOADS[workload]["T"]
     if workload in ("decode_t1", "decode_t1_e64"):
@@ -104,6 +109,8 @@ def make_inputs(workload, seed=0, layer_index=0):
     elif workload == "prefill_t4096":
         d = k3synth.with_bias(d, k3synth.zipf_bias(shape, seed, layer_index, k3synth.K3_ZIPF_ALPHA))
         x = k3synth.make_tokens(shape, seed, T, stream=11)
+    elif workload.endswith("_e64"):
+        x = k3synth.make_tokens(shape, seed, T, stream=15)
     else:
         x = k3synth.make_tokens(shape, seed, T, stream=13)
     return shape, d, x
@@ -343,7 +350,7 @@ def run_native(args, rank, world):
     # ---- CPU baseline: the oracle on a bounded sample ---------------------------------------
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        n_tok = {1: 16, 64: 16, 4096: 16, 256: 16}[T]
+        n_tok = 16
         xs_host = xpool if T == 1 else xpool[:T]
         nrow, dt = time_oracle(shape, oracle_layer, xs_host, n_tok)
         cpu = {"value": round(nrow / dt / n_layers, 4), "unit": UNIT,
