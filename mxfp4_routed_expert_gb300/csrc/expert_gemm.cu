@@ -8,23 +8,28 @@
 // stored.
 //
 // Work: the pairs of expert e (contiguous in permutation order) are cut into
-// n-tiles of at most 128; a work item is (n-tile, 128-row m-tile of the
-// matrix). Weight rows are the MMA's M, pairs its N, and both operands are
-// K-major rows: packed weights, and the pair-ordered fp16 activations (the
-// gathered latent z for W1/W3, the h rows for W2). Per 64-column k-tile:
-//   - one thread issues TMA for the raw packed tile (128 rows x 32 bytes per
-//     matrix) and the item's activation rows (16-row boxes of 128 bytes per
-//     row, 128-byte swizzle) into a deep ring;
-//   - eight converter warps widen the nibbles with cvt.rn.f16x2.e2m1x2 and
-//     multiply each 32-column group by 2^(s - smax_row), smax_row being the
-//     row's largest scale byte: every factor is a power of two <= 1, so the
-//     f16 operand is the exact weight / 2^(smax_row - 127) unless a row spans
-//     more than 24 binades of scales. They write the tile, in the swizzled
-//     K-major layout the tensor core reads, into a two-slot ring of its own
-//     (so the TMA ring stays deep enough to cover HBM latency);
-//   - one thread issues tcgen05.mma kind::f16 into fp32 TMEM accumulators
-//     (gate and up side by side for W1/W3), two accumulator sets so that the
-//     next item's MMAs overlap this item's epilogue;
+// n-tiles of at most 64; a work item is (n-tile, 128-row m-tile of the
+// matrix). Weight rows are the MMA's M, pairs its N. Per 128-column k-stage:
+//   - one thread issues TMA for the packed weight tile (128 rows x 64 bytes
+//     per matrix, 64-byte swizzle) and the item's pair-ordered fp16
+//     activation rows (the gathered latent z for W1/W3, the h rows for W2; two
+//     64-column halves in the 128-byte swizzled K-major layout, 16-row boxes)
+//     into a deep shared-memory ring;
+//   - sixteen converter warps (four per TMEM lane quadrant) widen the nibbles
+//     with cvt.rn.f16x2.e2m1x2 and multiply each 32-column group by
+//     2^(s - smax_row), smax_row being the row's largest scale byte: every
+//     factor is a power of two <= 1, so the f16 operand is the exact weight /
+//     2^(smax_row - 127) unless a row spans more than 24 binades of scales.
+//     They store it straight into tensor memory (tcgen05.st: row m in lane m,
+//     column c = columns 2c, 2c+1), the MMA's A operand, so that shared memory
+//     carries only packed weights and activations;
+//   - two threads issue tcgen05.mma kind::f16 (A from TMEM, B from shared
+//     memory) into fp32 TMEM accumulators, one each (W1/W3: gate and up; W2:
+//     the two halves of every k-stage, summed in the epilogue), with two
+//     accumulator sets so that the next item's MMAs overlap this item's
+//     epilogue; the rest of TMEM holds the A ring. An A slot is reused once
+//     the TMA stage of the k-stage that last held it is released, which both
+//     issuers' commits signal;
 //   - four epilogue warps read TMEM, multiply by 2^(smax_row - 127) and the
 //     token's activation exponent, then apply SiTU and store h (W1/W3), or
 //     scale by the pair's routing weight and scatter-add into the token's fp32
@@ -39,25 +44,35 @@ namespace k3 {
 
 namespace {
 
-constexpr int BM = 128, BK = 64, BN = 128;
-// warp roles: 0 TMA producer, 1 and 2 MMA issuers, 3 idle, 4..11 converters,
-// 12..15 epilogue (warp % 4 = its TMEM lane quadrant)
-constexpr int kConvWarp0 = 4, kConvWarps = 8;       // two converter threads per weight row
-constexpr int kEpiWarp0 = 12, kEpiWarps = 4;
-constexpr int kThreads = 16 * 32;
-constexpr int kRawRow = BK / 2;                     // packed bytes per row and k-tile
-#ifndef K3_EG_ASTAGES
-#define K3_EG_ASTAGES 2
-#endif
-constexpr int kAStages = K3_EG_ASTAGES;             // converted-tile ring
+constexpr int BM = 128, BK = 128, BN = 64;
+constexpr int kMinPairs = 128;                      // smallest batch (token, expert pairs) run here
+// warp roles: 0 TMA producer, 1 and 2 MMA issuers, 3 idle, 4..19 converters,
+// 20..23 epilogue (warp % 4 = its TMEM lane quadrant)
+constexpr int kConvWarp0 = 4, kConvWarps = 16;
+constexpr int kEpiWarp0 = 20, kEpiWarps = 4;
+constexpr int kThreads = 24 * 32;
+constexpr int kRawRow = BK / 2;                     // packed bytes per row and k-stage
+constexpr int kRawBytes = BM * kRawRow;             // one packed weight tile
 constexpr int kBoxRows = 16;                        // activation rows per TMA box
+constexpr int kBSub = BN * 128;                     // one 64-column half of the activation tile
+constexpr int kBBytes = 2 * kBSub;
 constexpr int kSmemBudget = 227 * 1024;
+// TMEM: kSets accumulator sets of two BN-column accumulators, then the A ring
+#ifndef K3_EG_SETS
+#define K3_EG_SETS 2
+#endif
+constexpr int kSets = K3_EG_SETS;
+constexpr uint32_t kSetCols = 2 * BN;
+constexpr uint32_t kARing0 = kSets * kSetCols;
+constexpr uint32_t kTmemCols = 512;
+
+constexpr int a_cols(bool dual) { return (dual ? 2 : 1) * BK / 2; }            // TMEM columns per A slot
+constexpr int a_stages(bool dual) { return (int)(kTmemCols - kARing0) / a_cols(dual); }
+constexpr int r_stage(bool dual) { return kBBytes + (dual ? 2 : 1) * kRawBytes; }
 
 constexpr size_t smem_bytes(bool dual, int ns)
 {
-    return (size_t)kAStages * (dual ? 2 : 1) * BM * BK * 2 +
-           (size_t)ns * (BN * BK * 2 + (dual ? 2 : 1) * BM * kRawRow) +
-           (size_t)(2 * ns + kAStages + 4) * 8 + 16 + 1024;
+    return (size_t)ns * r_stage(dual) + (size_t)(2 * ns + a_stages(dual) + 2 * kSets) * 8 + 16 + 1024;
 }
 
 // TMA ring depth: as many stages as the shared-memory budget holds (at most 12).
@@ -121,6 +136,41 @@ __device__ __forceinline__ float pow2_e8m0(int s)
     return __uint_as_float((uint32_t)min(max(s, 1), 254) << 23);
 }
 
+// 16 packed bytes (32 columns, one scale group) -> 16 f16x2 scaled by f.
+__device__ __forceinline__ void widen_group(uint4 w, uint32_t f, uint32_t *o)
+{
+    const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int j = 0; j < 4; j++) {
+        uint32_t h0, h1, h2, h3;
+        e2m1x8_to_f16x2x4(words[j], h0, h1, h2, h3);
+        o[4 * j + 0] = hmul2(h0, f);
+        o[4 * j + 1] = hmul2(h1, f);
+        o[4 * j + 2] = hmul2(h2, f);
+        o[4 * j + 3] = hmul2(h3, f);
+    }
+}
+
+// A from tensor memory, B from shared memory.
+__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                       uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t *v)
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+                 ::"r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]),
+                 "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+                 "r"(v[15])
+                 : "memory");
+}
+
 template <bool DUAL>
 __global__ void __launch_bounds__(kThreads, 1)
     k_expert_gemm(const __grid_constant__ CUtensorMap ra, const __grid_constant__ CUtensorMap rb,
@@ -130,25 +180,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     unsigned char *sm = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(raw_smem) + 1023) & ~static_cast<uintptr_t>(1023));
     constexpr int NM = DUAL ? 2 : 1;
-    constexpr int A_BYTES = BM * BK * 2;     // one converted f16 weight tile
-    constexpr int A_STAGE = NM * A_BYTES;
-    constexpr int B_BYTES = BN * BK * 2;     // activation tile (up to 128 pair rows)
-    constexpr int RAW_BYTES = BM * kRawRow;  // one packed weight tile
-    constexpr int R_STAGE = B_BYTES + NM * RAW_BYTES;
-    // TMEM: two accumulator sets of two 128-column accumulators. W1/W3: gate
-    // and up; W2: the two halves of each k-tile (summed in the epilogue), so
-    // that each MMA issuer owns one accumulator.
-    constexpr uint32_t SET_COLS = 2 * BN;
+    constexpr int R_STAGE = r_stage(DUAL);   // [B half 0 | B half 1 | packed W (one per matrix)]
     constexpr int NSR = ring_stages(DUAL);   // TMA ring depth
-    static_assert(NSR > kAStages, "converted slots are released through the TMA ring");
-    unsigned char *aring = sm;                               // [kAStages][A_STAGE]
-    unsigned char *rring = sm + kAStages * A_STAGE;          // [NSR][R_STAGE]: B, then raw
+    constexpr int NSA = a_stages(DUAL);      // TMEM A ring depth
+    constexpr int ACOLS = a_cols(DUAL);
+    static_assert(NSR > NSA, "A slots are released through the TMA ring");
+    unsigned char *rring = sm;
     uint64_t *full = reinterpret_cast<uint64_t *>(rring + NSR * R_STAGE);   // TMA landed
     uint64_t *rfree = full + NSR;                            // both issuers' MMAs on the stage done
-    uint64_t *aready = rfree + NSR;                          // [kAStages] converted tile written
-    uint64_t *tfull = aready + kAStages;                     // [2] accumulator set complete
-    uint64_t *tempty = tfull + 2;                            // [2] epilogue drained it
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(tempty + 2);
+    uint64_t *aready = rfree + NSR;                          // [NSA] A slot written
+    uint64_t *tfull = aready + NSA;                          // [kSets] accumulator set complete
+    uint64_t *tempty = tfull + kSets;                        // [kSets] epilogue drained it
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(tempty + kSets);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
@@ -156,8 +199,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&full[i], 1);
             mbar_init(&rfree[i], 2);
         }
-        for (int i = 0; i < kAStages; i++) mbar_init(&aready[i], kConvWarps);
-        for (int i = 0; i < 2; i++) {
+        for (int i = 0; i < NSA; i++) mbar_init(&aready[i], kConvWarps);
+        for (int i = 0; i < kSets; i++) {
             mbar_init(&tfull[i], 2);
             mbar_init(&tempty[i], kEpiWarps);
         }
@@ -166,7 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (DUAL) tc::prefetch_map(&rb);
         tc::prefetch_map(&bx);
     }
-    if (warp == 1) tc::tmem_alloc(tslot, 2 * SET_COLS);
+    if (warp == 1) tc::tmem_alloc(tslot, kTmemCols);
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
@@ -189,7 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int pair0 = g.offsets[td.x] + td.y * BN;
                 const int cnt = g.offsets[td.x + 1] - g.offsets[td.x];
                 const int nb = (min(BN, cnt - td.y * BN) + kBoxRows - 1) / kBoxRows;   // 16-row boxes
-                const uint32_t tx = (uint32_t)(nb * kBoxRows * BK * 2 + NM * RAW_BYTES);
+                const uint32_t tx = (uint32_t)(2 * nb * kBoxRows * 128 + NM * kRawBytes);
                 for (int kt = 0; kt < KT; kt++, it++, rp.next()) {
                     const int s = rp.slot;
                     if (!mbar_wait(&rfree[s], rp.phase ^ 1u, g.err, 600)) {
@@ -198,10 +241,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     unsigned char *st = rring + s * R_STAGE;
                     mbar_expect_tx(&full[s], tx);
-                    for (int b = 0; b < nb; b++)
-                        tc::tma_load_2d(st + b * kBoxRows * 128, &bx, kt * BK, pair0 + b * kBoxRows, &full[s]);
-                    tc::tma_load_2d(st + B_BYTES, &ra, kt * kRawRow, row0, &full[s]);
-                    if (DUAL) tc::tma_load_2d(st + B_BYTES + RAW_BYTES, &rb, kt * kRawRow, row0, &full[s]);
+                    for (int u = 0; u < 2; u++)
+                        for (int b = 0; b < nb; b++)
+                            tc::tma_load_2d(st + u * kBSub + b * kBoxRows * 128, &bx, kt * BK + u * 64,
+                                            pair0 + b * kBoxRows, &full[s]);
+                    tc::tma_load_2d(st + kBBytes, &ra, kt * kRawRow, row0, &full[s]);
+                    if (DUAL) tc::tma_load_2d(st + kBBytes + kRawBytes, &rb, kt * kRawRow, row0, &full[s]);
                 }
             }
             // copies still in flight land before the CTA exits (each stage holds at
@@ -214,17 +259,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1 || warp == 2) {
         // ---------------- MMA issuers ----------------
         // W1/W3: issuer q multiplies matrix q; W2: issuer q takes the k-steps
-        // 2q, 2q+1 of every k-tile. Each writes accumulator q of the set.
+        // 4q..4q+3 of every k-stage. Each writes accumulator q of the set.
         const int q = warp - 1;
         if (lane == 0) {
             int local = 0;
             RingPos<NSR> rp;
-            RingPos<kAStages> ap;
-            // shared-memory descriptors of slot 0; a byte offset o adds o >> 4
-            const uint64_t da0 = tc::desc_sw128(tc::su32(aring)) + (uint64_t)(DUAL ? (q * A_BYTES) >> 4 : 0);
+            RingPos<NSA> ap;
             const uint64_t db0 = tc::desc_sw128(tc::su32(rring));
-            const int kk0 = DUAL ? 0 : 2 * q;            // first k-step (of 16 columns)
-            constexpr int NK = DUAL ? BK / 16 : BK / 32; // k-steps per k-tile for this issuer
+            const int kk0 = DUAL ? 0 : 4 * q;            // first k-step (of 16 columns)
+            constexpr int NK = DUAL ? BK / 16 : BK / 32; // k-steps per k-stage for this issuer
             bool ok = true;
             for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, local++) {
                 const int tile = item / g.MT;
@@ -233,10 +276,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int n = ((min(BN, cnt - td.y * BN) + kBoxRows - 1) / kBoxRows) * kBoxRows;
                 const uint32_t idesc =
                     (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);  // f16 x f16 -> f32
-                const int b = local & 1;
-                if (!mbar_wait(&tempty[b], ((uint32_t)(local >> 1) & 1u) ^ 1u, g.err, 601)) break;
+                const int b = local % kSets;
+                if (!mbar_wait(&tempty[b], ((uint32_t)(local / kSets) & 1u) ^ 1u, g.err, 601)) break;
                 tc::fence_after();
-                const uint32_t d = tmem + (uint32_t)b * SET_COLS + (uint32_t)q * BN;
+                const uint32_t d = tmem + (uint32_t)b * kSetCols + (uint32_t)q * BN;
                 for (int kt = 0; kt < KT; kt++, rp.next(), ap.next()) {
                     // The converters arrive on aready only after their wait on the
                     // TMA barrier of this stage, so aready also orders the
@@ -246,79 +289,73 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     tc::fence_after();
-                    // K = 16 per MMA: 32 bytes along the swizzled rows
-                    const uint64_t da = da0 + (uint64_t)((ap.slot * A_STAGE) >> 4) + 2 * kk0;
-                    const uint64_t db = db0 + (uint64_t)((rp.slot * R_STAGE) >> 4) + 2 * kk0;
-                    tc::mma_bf16(d, da, db, idesc, kt > 0 ? 1u : 0u);
+                    const uint32_t a0 = tmem + kARing0 + (uint32_t)(ap.slot * ACOLS) + (DUAL ? (uint32_t)q * (BK / 2) : 0u);
+                    const uint64_t db = db0 + (uint64_t)((rp.slot * R_STAGE) >> 4);
 #pragma unroll
-                    for (int kk = 1; kk < NK; kk++) tc::mma_bf16(d, da + 2 * kk, db + 2 * kk, idesc, 1u);
+                    for (int i = 0; i < NK; i++) {
+                        const int kk = kk0 + i;
+                        // B: half kk / 4 of the activation tile, 32 bytes per k-step inside it
+                        const uint64_t bd = db + (uint64_t)(((kk >> 2) * kBSub + (kk & 3) * 32) >> 4);
+                        mma_ts(d, a0 + 8 * (uint32_t)kk, bd, idesc, (kt > 0 || i > 0) ? 1u : 0u);
+                    }
                     tc::commit(&rfree[rp.slot]);
                 }
                 if (ok) tc::commit(&tfull[b]);
             }
         }
     } else if (warp >= kConvWarp0 && warp < kConvWarp0 + kConvWarps) {
-        // ---------------- converters: packed e2m1 -> scaled f16, swizzled ----------------
-        const int ct = threadIdx.x - kConvWarp0 * 32;   // 0..255
-        const int row = ct >> 1, half = ct & 1;       // weight row of the tile, 32-column group of the k-tile
+        // ---------------- converters: packed e2m1 -> scaled f16 -> TMEM ----------------
+        const int qd = warp & 3;                      // TMEM lane quadrant
+        const int row = qd * 32 + lane;               // weight row of the tile (its TMEM lane)
+        const int sl = (warp - kConvWarp0) >> 2;      // 0..3: this warp's share of the k-stage
+        // W1/W3: matrix sl >> 1, 64 columns (two scale groups) from 64 * (sl & 1);
+        // W2: 32 columns (one scale group) from 32 * sl
+        const int m = DUAL ? (sl >> 1) : 0;
+        const int grp0 = DUAL ? 2 * (sl & 1) : sl;    // first scale group within the k-stage
+        constexpr int NGRP = DUAL ? 2 : 1;
+        const uint32_t tlane = (uint32_t)(qd * 32) << 16;
         const int G = g.K / kGroup;
-        RingPos<NSR> rp;          // TMA stage of this k-tile
-        RingPos<NSR> rq;          // TMA stage of the k-tile kAStages back (its MMAs free the slot)
-        RingPos<kAStages> ap;
-        int done = 0;             // k-tiles converted so far
+        const int swz = (row >> 1) & 3;              // 64-byte swizzle of the packed tile
+        RingPos<NSR> rp;          // TMA stage of this k-stage
+        RingPos<NSR> rq;          // TMA stage of the k-stage NSA back (its MMAs free the slot)
+        RingPos<NSA> ap;
+        int done = 0;             // k-stages converted so far
         bool ok = true;
         for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
             const int tile = item / g.MT, mt = item - tile * g.MT;
             const size_t grow = (size_t)g.tiles[tile].x * g.R + mt * BM + row;
-            const int smax0 = g.ma[grow];
-            const int smax1 = DUAL ? g.mb[grow] : 0;
-            const uint8_t *sc0 = g.sa + grow * (size_t)G + half;
-            const uint8_t *sc1 = DUAL ? g.sb + grow * (size_t)G + half : nullptr;
-            int s0 = sc0[0], s1 = DUAL ? sc1[0] : 0;
+            const int smax = m == 0 ? g.ma[grow] : g.mb[grow];
+            const uint8_t *sc = (m == 0 ? g.sa : g.sb) + grow * (size_t)G + grp0;
             for (int kt = 0; kt < KT; kt++, rp.next(), ap.next(), done++) {
-                // next k-tile's scale bytes load while this one converts
-                const int nx = kt + 1 < KT ? 2 * (kt + 1) : 2 * kt;
-                const int s0n = sc0[nx];
-                const int s1n = DUAL ? sc1[nx] : 0;
+                int sv[NGRP];
+#pragma unroll
+                for (int i = 0; i < NGRP; i++) sv[i] = sc[4 * kt + i];
                 if (!mbar_wait(&full[rp.slot], rp.phase, g.err, 604)) {
                     ok = false;
                     break;
                 }
-                if (done >= kAStages) {
+                if (done >= NSA) {
                     if (!mbar_wait(&rfree[rq.slot], rq.phase, g.err, 607)) {
                         ok = false;
                         break;
                     }
                     rq.next();
                 }
-                const unsigned char *rawp = rring + rp.slot * R_STAGE + B_BYTES;
-                unsigned char *ast = aring + ap.slot * A_STAGE;
+                tc::fence_after();
+                const unsigned char *rawp = rring + rp.slot * R_STAGE + kBBytes + m * kRawBytes + row * kRawRow;
+                const uint32_t acol = kARing0 + (uint32_t)(ap.slot * ACOLS) + (uint32_t)(m * (BK / 2));
 #pragma unroll
-                for (int m = 0; m < NM; m++) {
-                    const uint4 w = *reinterpret_cast<const uint4 *>(rawp + m * RAW_BYTES + row * kRawRow + half * 16);
-                    const uint32_t f = f16x2_pow2((m == 0 ? s0 : s1) - (m == 0 ? smax0 : smax1));
-                    const uint32_t words[4] = {w.x, w.y, w.z, w.w};
-                    unsigned char *arow = ast + m * A_BYTES + row * 128;
-#pragma unroll
-                    for (int j = 0; j < 4; j++) {
-                        // packed word j = columns 8j..8j+7 of the group = 16-byte chunk 4*half + j
-                        uint32_t h0, h1, h2, h3;
-                        e2m1x8_to_f16x2x4(words[j], h0, h1, h2, h3);
-                        uint4 o;
-                        o.x = hmul2(h0, f);
-                        o.y = hmul2(h1, f);
-                        o.z = hmul2(h2, f);
-                        o.w = hmul2(h3, f);
-                        const int c = 4 * half + j;
-                        *reinterpret_cast<uint4 *>(arow + ((c ^ (row & 7)) << 4)) = o;
-                    }
+                for (int i = 0; i < NGRP; i++) {
+                    const int c = grp0 + i;                   // 16-byte chunk = scale group of the row
+                    const uint4 w = *reinterpret_cast<const uint4 *>(rawp + ((c ^ swz) << 4));
+                    uint32_t v[16];
+                    widen_group(w, f16x2_pow2(sv[i] - smax), v);
+                    tmem_st16(tmem + tlane + acol + (uint32_t)(16 * c), v);
                 }
-                // make the generic-proxy stores visible to the tensor core
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                tc::fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&aready[ap.slot]);
-                s0 = s0n;
-                s1 = s1n;
             }
         }
     } else if (warp >= kEpiWarp0) {
@@ -336,10 +373,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const size_t grow = (size_t)td.x * g.R + row_in_e;
             const float rs0 = pow2_e8m0(g.ma[grow]);
             const float rs1 = DUAL ? pow2_e8m0(g.mb[grow]) : 0.f;
-            const int b = local & 1;
-            if (!mbar_wait(&tfull[b], (uint32_t)(local >> 1) & 1u, g.err, 606)) break;
+            const int b = local % kSets;
+            if (!mbar_wait(&tfull[b], (uint32_t)(local / kSets) & 1u, g.err, 606)) break;
             tc::fence_after();
-            const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)b * SET_COLS;
+            const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)b * kSetCols;
             for (int c0 = 0; c0 < n_valid; c0 += 16) {
                 // per-pair factors for columns c0..c0+15, one lane each, then broadcast
                 const int pl = pair0 + c0 + (lane & 15);
@@ -382,11 +419,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     if (warp == 1) {
         tc::fence_after();
-        tc::tmem_dealloc(tmem, 2 * SET_COLS);
+        tc::tmem_dealloc(tmem, kTmemCols);
     }
 }
 
-// n-tiles: (expert, j) for j < ceil(count_e / 128), experts ascending. One block.
+// n-tiles: (expert, j) for j < ceil(count_e / BN), experts ascending. One block.
 __global__ void __launch_bounds__(1024) k_expert_tiles(const int *counts, int E, int2 *tiles, int *n_tiles)
 {
     __shared__ int wsum[32];
@@ -438,6 +475,8 @@ __global__ void k_row_scale_max(const uint8_t *s, size_t rows, int G, uint8_t *o
     out[r] = (uint8_t)m;
 }
 
+// Packed weights [rows, cols bytes], boxes of box_cols x box_rows with the
+// 64-byte swizzle (16-byte chunk c of row r lands at chunk c ^ ((r >> 1) & 3)).
 bool make_map_u8(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, uint32_t box_cols,
                  uint32_t box_rows)
 {
@@ -448,7 +487,7 @@ bool make_map_u8(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols,
     const cuuint32_t box[2] = {box_cols, box_rows};
     const cuuint32_t estr[2] = {1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -471,7 +510,8 @@ bool make_map_f16_sw128(CUtensorMap *m, const void *base, uint64_t rows, uint64_
 
 bool expert_gemm_ok(const k3moe_config &c)
 {
-    return c.latent % BM == 0 && c.moe_inter % BM == 0 && (long long)c.max_tokens * c.topk >= BN;
+    return c.latent % BK == 0 && c.moe_inter % BK == 0 && c.latent % BM == 0 && c.moe_inter % BM == 0 &&
+           (long long)c.max_tokens * c.topk >= kMinPairs;
 }
 
 size_t expert_gemm_max_tiles(const k3moe_config &c)
@@ -479,7 +519,7 @@ size_t expert_gemm_max_tiles(const k3moe_config &c)
     return (size_t)((long long)c.max_tokens * c.topk / BN + c.n_experts + 1);
 }
 
-int expert_gemm_min_pairs() { return BN; }
+int expert_gemm_min_pairs() { return kMinPairs; }
 
 cudaError_t init_expert_gemm()
 {
@@ -508,7 +548,7 @@ cudaError_t launch_expert_gemm(const k3moe &h, const LayerDev &w, int T, cudaStr
 {
     const k3moe_config &c = h.cfg;
     const int pairs = T * c.topk;
-    if (pairs < BN) return cudaErrorInvalidValue;
+    if (pairs < kMinPairs) return cudaErrorInvalidValue;
     EgArgs g = {};
     g.k = c.topk;
     g.L = c.latent;
