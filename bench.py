@@ -70,28 +70,80 @@ def measured_peaks():
     if os.path.exists(p):
         with open(p) as f:
             d = json.load(f)
-        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
-    return 6800.0, 1900.0, "fallback"
+        return (float(d["hbm_gbs"]), float(d["bf16_tflops"]),
+                float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured")
+    return 6800.0, 1900.0, 1700.0, "fallback"
 
 
-# ---- algorithmic bytes per kernel launch (K3 layer, weights + activations) ------
+FP4_NOMINAL_TFLOPS = 13500.0      # dense FP4 tensor peak (nominal), context only
 
-def kernel_bytes(shape, T, n_touched):
+
+def roofline(kernel, model, avg_ms, hbm_peak, tc_peak, peak_src, workload):
+    """The dominant kernel against the roof it is closer to: HBM bandwidth for
+    its algorithmic bytes, or the f16/bf16 tensor peak (measured, sustained:
+    the kernel runs inside a long step) for its FLOPs."""
+    if not model:
+        return {"kernel": kernel, "bound": "hbm", "achieved": None, "peak": hbm_peak,
+                "unit": "GB/s", "frac": None, "traffic": None}
+    byt, fl = model
+    t = avg_ms / 1e3
+    gbs = byt / t / 1e9
+    tfl = fl / t / 1e12 if fl else 0.0
+    f_hbm, f_tc = gbs / hbm_peak, (tfl / tc_peak if fl else 0.0)
+    if f_tc > f_hbm:
+        roof = {"kernel": kernel, "bound": "tensor", "achieved": round(tfl, 2), "peak": tc_peak,
+                "unit": "TFLOP/s", "frac": round(f_tc, 4),
+                "peak_source": f"{peak_src} bf16_tflops_sustained (the kernel computes f16 x f16 -> f32)"}
+    else:
+        roof = {"kernel": kernel, "bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak,
+                "unit": "GB/s", "frac": round(f_hbm, 4), "peak_source": f"{peak_src} hbm_gbs"}
+    roof.update({"traffic": traffic_for(kernel, workload), "alg_bytes_per_launch": int(byt),
+                 "flops_per_launch": int(fl), "avg_launch_ms": round(avg_ms, 5),
+                 "hbm_frac": round(f_hbm, 4), "tensor_frac": round(f_tc, 4)})
+    if fl:
+        roof["fp4_nominal_frac"] = round(tfl / FP4_NOMINAL_TFLOPS, 4)
+    return roof
+
+
+# ---- algorithmic traffic and arithmetic per kernel launch -------------------------
+# Bytes: every weight byte the launch must read once plus its activation reads
+# and result writes (no re-reads). FLOPs: 2 per multiply-add of the
+# contraction (tensor-core kernels only).
+
+def kernel_model(shape, T, n_touched):
     H, L, E, I, S, k = (shape.hidden, shape.latent, shape.n_experts, shape.moe_inter,
                         shape.shared_inter, shape.topk)
-    per_w13 = 2 * (I * L // 2 + I * L // 32)
+    P = T * k                                            # (token, expert) pairs
+    per_w13 = 2 * (I * L // 2 + I * L // 32)             # packed W1 + W3 and their scales
     per_w2 = L * I // 2 + L * I // 32
+    rd = (2 * (E * H + L * H) + 2 * T * H + 4 * T * (E + L), 2 * T * H * (E + L))
+    sh = (2 * (2 * S * H) + 2 * T * H + 6 * T * S, 2 * T * H * 2 * S)
+    up = (2 * (H * L + H * S) + 2 * T * (L + S) + 2 * T * H, 2 * T * (L + S) * H)
+    w13 = (n_touched * per_w13 + 2 * P * L + 2 * P * I, 2 * P * L * 2 * I)
+    w2 = (n_touched * per_w2 + 2 * P * I + 8 * T * L, 2 * P * I * L)
     return {
-        "router_down_gemv": 2 * (E * H + L * H) + 2 * T * H + 4 * T * (E + L),
-        "shared_gate_up_gemv": 2 * (2 * S * H) + 2 * T * H + 4 * T * S,
-        "expert_w13_gemv": n_touched * per_w13 + 2 * T * L + 2 * T * k * I,
-        "expert_w2_gemv": n_touched * per_w2 + 2 * T * k * I + 4 * T * L,
-        "norm_up_shared_gemv": 2 * (H * L + H * S) + 4 * T * (L + S) + 2 * T * H + 2 * L,
+        "router_down_gemv": (rd[0], 0), "router_down_gemm": rd,
+        "shared_gate_up_gemv": (sh[0] - 2 * T * S, 0), "shared_gate_up_gemm": sh,
+        "route_topk": (4 * T * (E + L) + 2 * T * (L + 16) + 4 * T * L + 8 * T * k, 0),
+        "perm_count": (4 * P, 0), "perm_scan": (0, 0), "perm_place": (8 * P + 8 * P, 0),
+        "expert_tiles": (0, 0), "gather_latent": (4 * P * (L + 16), 0),
+        "expert_w13_gemv": (w13[0] - 2 * P * L + 2 * T * L, 0), "expert_w13_gemm": w13,
+        "expert_w2_gemv": (w2[0], 0), "expert_w2_gemm": w2,
+        "latent_rmsnorm": (4 * T * L + 2 * T * L + 2 * L, 0),
+        "norm_up_shared_gemv": (up[0] - 2 * T * (L + S) + 4 * T * (L + S) + 2 * L, 0),
+        "up_shared_gemm": up,
+        "chain_glue_rmsnorm": (4 * T * H, 0),
     }
 
 
 def layer_bytes(shape, T, n_touched):
-    return sum(kernel_bytes(shape, T, n_touched).values())
+    """Bytes of one layer's minimal traffic: every weight it reads once (the
+    dense projections, the shared experts and the touched experts) plus the
+    layer input and output."""
+    H, L, E, I, S = shape.hidden, shape.latent, shape.n_experts, shape.moe_inter, shape.shared_inter
+    dense = 2 * (E * H + L * H + 2 * S * H + H * L + H * S)
+    experts = n_touched * (3 * (I * L // 2 + I * L // 32))
+    return dense + experts + 4 * T * H
 
 
 # ---- inputs ----------------------------------------------------------------------
@@ -304,28 +356,26 @@ def run_native(args, rank, world):
 
     touched = (counts_log.cpu().numpy() > 0).sum(1)
     n_touched = float(touched.mean())
-    hbm_peak, bf16_peak, peak_src = measured_peaks()
-    kb = kernel_bytes(shape, T, n_touched)
+    hbm_peak, bf16_peak, bf16_sust, peak_src = measured_peaks()
+    model = kernel_model(shape, T, n_touched)
     by_name = {n: (l, ms) for n, l, ms in stats}
     ranked = sorted(((ms, n) for n, (l, ms) in by_name.items()), reverse=True)
     dom = ranked[0][1]
     launches, dom_ms = by_name[dom]
     avg_ms = dom_ms / launches
-    if dom in kb:
-        alg = kb[dom] if n_layers == 1 else kb[dom]
-        achieved = alg / (avg_ms / 1e3) / 1e9
-        roof = {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1),
-                "peak": hbm_peak, "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
-                "traffic": traffic_for(dom, args.workload), "alg_bytes_per_launch": int(alg),
-                "avg_launch_ms": round(avg_ms, 5), "peak_source": f"{peak_src} hbm_gbs"}
-    else:
-        roof = {"kernel": dom, "bound": "hbm", "achieved": None, "peak": hbm_peak,
-                "unit": "GB/s", "frac": None, "traffic": None}
+    roof = roofline(dom, model.get(dom), avg_ms, hbm_peak, bf16_sust, peak_src, args.workload)
     step_bytes = layer_bytes(shape, T, n_touched) * n_layers
     layer_gbs = step_bytes / (ms_per_step / 1e3) / 1e9
-    kernels = {n: {"launches": l, "avg_ms": round(ms / l, 5),
-                   "share": round(ms / sum(m for _, m in by_name.values()), 4)}
-               for n, (l, ms) in by_name.items()}
+    kernels = {}
+    for n, (l, ms) in by_name.items():
+        ent = {"launches": l, "avg_ms": round(ms / l, 5),
+               "share": round(ms / sum(m for _, m in by_name.values()), 4)}
+        byt, fl = model.get(n, (0, 0))
+        if byt:
+            ent["gbs"] = round(byt / (ms / l / 1e3) / 1e9, 1)
+        if fl:
+            ent["tflops"] = round(fl / (ms / l / 1e3) / 1e12, 2)
+        kernels[n] = ent
     kernels["_profiled_pass_ms_per_step"] = round(prof_ms / args.steps, 5)
     gpu_launches = sum(l for l, _ in by_name.values())
 

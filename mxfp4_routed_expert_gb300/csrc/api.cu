@@ -79,6 +79,7 @@ size_t carve_workspace(const k3moe_config &c, char *base, Workspace *ws)
     w.zperm = cv.take<__half>(eg ? Tm * K * (L + kZPad) : 0);
     w.tiles = cv.take<int2>(eg ? expert_gemm_max_tiles(c) : 0);
     w.n_tiles = cv.take<int>(1);
+    w.perm_hist = cv.take<int>((size_t)perm_chunks(c.max_tokens) * E);
     w.act = cv.take<__nv_bfloat16>(Tm * (L + S));
     w.gemm_part = cv.take<float>(dense_gemm_part_floats(c));
     w.gemm_tiles = cv.take<int>(dense_gemm_tile_counters(c));
@@ -228,7 +229,11 @@ int run_layer(k3moe *h, const LayerDev &w, const __nv_bfloat16 *x, __nv_bfloat16
     if (e != cudaSuccess || cudaEventRecord(h->ev_join, h->side) != cudaSuccess)
         return K3MOE_ERR_CUDA;
     K3_STEP("route_topk", launch_route(*h, w, T, s));
-    if (T > 1) K3_STEP("permute", launch_perm(*h, T, s));   // T == 1: written by route_topk
+    if (T > 1) {   // T == 1: written by route_topk
+        K3_STEP("perm_count", launch_perm(*h, T, s, 0));
+        K3_STEP("perm_scan", launch_perm(*h, T, s, 1));
+        K3_STEP("perm_place", launch_perm(*h, T, s, 2));
+    }
     if (cudaStreamWaitEvent(s, h->ev_join, 0) != cudaSuccess) return K3MOE_ERR_CUDA;
     if (egemm) {
         K3_STEP("expert_tiles", launch_expert_tiles(*h, s));

@@ -66,6 +66,7 @@ struct Workspace {
     float *acc = nullptr;         // [Tm, L]
     __half *zperm = nullptr;      // [Tm*k, L + kZPad] z16 rows gathered in pair order (expert GEMM)
     int2 *tiles = nullptr;        // (expert, n-tile) list of the expert GEMM
+    int *perm_hist = nullptr;     // [ceil(Tm/32), E] per-chunk expert counts, then chunk bases
     int *n_tiles = nullptr;       // [1]
     __nv_bfloat16 *act = nullptr;     // [Tm, L+S] bf16 [normed latent | shared SiTU] (GEMM path)
     float *gemm_part = nullptr;       // split-K partial sums (kept zeroed between launches)
@@ -115,7 +116,8 @@ namespace k3 {
 cudaError_t launch_dense_x(const k3moe &h, const LayerDev &w, const __nv_bfloat16 *x, int T,
                            cudaStream_t s, int part);
 cudaError_t launch_route(const k3moe &h, const LayerDev &w, int T, cudaStream_t s);
-cudaError_t launch_perm(const k3moe &h, int T, cudaStream_t s);
+cudaError_t launch_perm(const k3moe &h, int T, cudaStream_t s, int step);
+int perm_chunks(int T);
 cudaError_t launch_expert_w13(const k3moe &h, const LayerDev &w, int T, cudaStream_t s);
 cudaError_t launch_expert_w2(const k3moe &h, const LayerDev &w, int T, cudaStream_t s);
 cudaError_t launch_up(const k3moe &h, const LayerDev &w, __nv_bfloat16 *y, int T,

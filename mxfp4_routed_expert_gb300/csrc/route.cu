@@ -9,9 +9,10 @@
 // input: z scaled by a per-token power of two into fp16, and clears the
 // token's fp32 accumulator row.
 //
-// k_perm (one block): per-expert counts, exclusive offsets, and the pair list
-// grouped by expert with tokens in ascending order inside an expert, plus the
-// ascending list of experts that received at least one token.
+// Permutation (three launches over 32-token chunks, T > 1): per-expert
+// counts, exclusive offsets, and the pair list grouped by expert with tokens
+// in ascending order inside an expert, plus the ascending list of experts
+// that received at least one token. For T == 1 k_route writes these itself.
 #include <climits>
 
 #include "k3moe_internal.cuh"
@@ -292,44 +293,73 @@ __device__ __forceinline__ int block_excl_scan(int v, int *wsum, int *total)
     return r;
 }
 
-__global__ void __launch_bounds__(1024) k_perm(PermArgs a)
+// The permutation is a stable counting sort of the (token, slot) pairs by
+// expert, in three launches over chunks of kPermChunk tokens:
+//   1. per chunk (one warp), the number of its pairs that chose each expert;
+//   2. (one block, a thread per expert) each chunk's starting position per
+//      expert = the expert's offset + the pairs of earlier chunks, the expert
+//      counts, offsets and the list of touched experts;
+//   3. per chunk (one warp), its pairs placed in token order. The k experts of
+//      one token are distinct, so the lanes of a step never share a counter and
+//      tokens stay ascending inside every expert's run.
+constexpr int kPermChunk = 32;
+constexpr int kPermWarps = 8;            // chunks per block in steps 1 and 3
+
+__global__ void __launch_bounds__(kPermWarps * 32) k_perm_hist(PermArgs a, int *hist)
 {
-    extern __shared__ int sm[];
-    int *hist = sm;                       // [32][E]: per-warp counts, then per-warp bases
-    int *base = sm + 32 * a.E;            // [E]: expert offsets
-    __shared__ int wsum[32];
-    __shared__ int total_pairs, total_touched;
+    extern __shared__ int sh[];          // [kPermWarps][E]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int *h = sh + warp * a.E;
     pdl_launch_dependents();
     pdl_wait();
-    for (int i = threadIdx.x; i < 32 * a.E; i += blockDim.x) hist[i] = 0;
-    __syncthreads();
-    const int tpw = (a.T + 31) / 32;
-    const int tb = warp * tpw, te = min(a.T, tb + tpw);
-    for (int t = tb; t < te; t++) {
+    const int chunk = blockIdx.x * kPermWarps + warp;
+    const int t0 = chunk * kPermChunk;
+    if (t0 >= a.T) return;
+    for (int e = lane; e < a.E; e += 32) h[e] = 0;
+    __syncwarp();
+    const int t1 = min(a.T, t0 + kPermChunk);
+    for (int t = t0; t < t1; t++) {
         if (lane < a.k) {
             const int e = a.ids[(size_t)t * a.k + lane];
-            if (e >= 0 && e < a.E)
-                atomicAdd(&hist[warp * a.E + e], 1);
-            else
-                set_err(a.err, kErrBounds, t);
+            if (e >= 0 && e < a.E) h[e] += 1;      // distinct experts within a token
+            else set_err(a.err, kErrBounds, t);
         }
+        __syncwarp();
     }
-    __syncthreads();
-    // per expert: counts over warps -> per-warp running bases
+    int *out = hist + (size_t)chunk * a.E;
+    for (int e = lane; e < a.E; e += 32) out[e] = h[e];
+}
+
+__global__ void __launch_bounds__(1024) k_perm_scan(PermArgs a, int *hist, int n_chunks)
+{
+    __shared__ int wsum[32];
+    __shared__ int total_pairs, total_touched;
+    pdl_launch_dependents();
+    pdl_wait();
     const int e = threadIdx.x;
     int cnt = 0;
     if (e < a.E) {
-        for (int w = 0; w < 32; w++) {
-            const int c = hist[w * a.E + e];
-            hist[w * a.E + e] = cnt;
-            cnt += c;
+        // running sum over chunks, four loads in flight
+        int c = 0;
+        for (; c + 4 <= n_chunks; c += 4) {
+            int *p = hist + (size_t)c * a.E + e;
+            const int v0 = p[0], v1 = p[a.E], v2 = p[2 * (size_t)a.E], v3 = p[3 * (size_t)a.E];
+            p[0] = cnt;
+            p[a.E] = cnt + v0;
+            p[2 * (size_t)a.E] = cnt + v0 + v1;
+            p[3 * (size_t)a.E] = cnt + v0 + v1 + v2;
+            cnt += v0 + v1 + v2 + v3;
+        }
+        for (; c < n_chunks; c++) {
+            int *p = hist + (size_t)c * a.E + e;
+            const int v = *p;
+            *p = cnt;
+            cnt += v;
         }
     }
     const int off = block_excl_scan(e < a.E ? cnt : 0, wsum, &total_pairs);
     const int tpos = block_excl_scan((e < a.E && cnt > 0) ? 1 : 0, wsum, &total_touched);
     if (e < a.E) {
-        base[e] = off;
         a.counts[e] = cnt;
         a.offsets[e] = off;
         if (cnt > 0) a.touched[tpos] = e;
@@ -338,22 +368,40 @@ __global__ void __launch_bounds__(1024) k_perm(PermArgs a)
         a.offsets[a.E] = total_pairs;
         *a.n_touched = total_touched;
     }
-    __syncthreads();
-    // placement: each warp walks its tokens in order, so tokens stay ascending
-    for (int t = tb; t < te; t++) {
+}
+
+__global__ void __launch_bounds__(kPermWarps * 32) k_perm_place(PermArgs a, const int *hist)
+{
+    extern __shared__ int sh[];          // [kPermWarps][E]: next position per expert
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int *pos = sh + warp * a.E;
+    pdl_launch_dependents();
+    pdl_wait();
+    const int chunk = blockIdx.x * kPermWarps + warp;
+    const int t0 = chunk * kPermChunk;
+    if (t0 >= a.T) return;
+    const int *base = hist + (size_t)chunk * a.E;
+    for (int e = lane; e < a.E; e += 32) pos[e] = a.offsets[e] + base[e];
+    __syncwarp();
+    const int t1 = min(a.T, t0 + kPermChunk);
+    for (int t = t0; t < t1; t++) {
         if (lane < a.k) {
-            const int ee = a.ids[(size_t)t * a.k + lane];
-            if (ee >= 0 && ee < a.E) {
-                const int pos = base[ee] + atomicAdd(&hist[warp * a.E + ee], 1);
-                a.perm[pos] = t * a.k + lane;
-                a.pair_w[pos] = a.wts[(size_t)t * a.k + lane];
+            const int e = a.ids[(size_t)t * a.k + lane];
+            if (e >= 0 && e < a.E) {
+                const int p = pos[e]++;
+                a.perm[p] = t * a.k + lane;
+                a.pair_w[p] = a.wts[(size_t)t * a.k + lane];
             }
         }
         __syncwarp();
     }
 }
 
-cudaError_t launch_perm(const k3moe &h, int T, cudaStream_t s)
+int perm_chunks(int T) { return (T + kPermChunk - 1) / kPermChunk; }
+
+// step 0: chunk histograms; 1: chunk bases, counts, offsets, touched list;
+// 2: placement.
+cudaError_t launch_perm(const k3moe &h, int T, cudaStream_t s, int step)
 {
     const k3moe_config &c = h.cfg;
     PermArgs a;
@@ -369,14 +417,20 @@ cudaError_t launch_perm(const k3moe &h, int T, cudaStream_t s)
     a.touched = h.ws.touched;
     a.n_touched = h.ws.n_touched;
     a.err = h.ws.err;
-    const size_t smem = (size_t)33 * c.n_experts * sizeof(int);
-    return launch_pdl(k_perm, 1, 1024, smem, s, a);
+    const int nch = perm_chunks(T);
+    const int blocks = (nch + kPermWarps - 1) / kPermWarps;
+    const size_t smem = (size_t)kPermWarps * c.n_experts * sizeof(int);
+    if (step == 0) return launch_pdl(k_perm_hist, blocks, kPermWarps * 32, smem, s, a, h.ws.perm_hist);
+    if (step == 1) return launch_pdl(k_perm_scan, 1, 1024, 0, s, a, h.ws.perm_hist, nch);
+    return launch_pdl(k_perm_place, blocks, kPermWarps * 32, smem, s, a, (const int *)h.ws.perm_hist);
 }
 
 cudaError_t init_route_kernels(const k3moe_config &c)
 {
-    return cudaFuncSetAttribute(k_perm, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)((size_t)33 * c.n_experts * sizeof(int)));
+    const int smem = (int)((size_t)kPermWarps * c.n_experts * sizeof(int));
+    cudaError_t e = cudaFuncSetAttribute(k_perm_hist, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(k_perm_place, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
 }
 
 }  // namespace k3

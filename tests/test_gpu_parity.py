@@ -207,7 +207,8 @@ def test_routing_is_deterministic_and_profiling_lists_kernels():
         np.testing.assert_array_equal(a[k], b[k])
     names = {s[0] for s in stats}
     # T=20 (160 pairs): dense GEMVs (64 experts < 128 rows), grouped expert GEMM
-    assert {"router_down_gemv", "shared_gate_up_gemv", "route_topk", "permute", "expert_tiles",
+    assert {"router_down_gemv", "shared_gate_up_gemv", "route_topk", "perm_count", "perm_scan",
+            "perm_place", "expert_tiles",
             "gather_latent", "expert_w13_gemm", "expert_w2_gemm", "norm_up_shared_gemv"} <= names
     assert all(s[1] == 2 and s[2] > 0 for s in stats)
 
