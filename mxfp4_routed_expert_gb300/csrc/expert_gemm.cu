@@ -31,7 +31,8 @@
 //     the TMA stage of the k-stage that last held it is released, which both
 //     issuers' commits signal;
 //   - four epilogue warps read TMEM, multiply by 2^(smax_row - 127) and the
-//     token's activation exponent, then apply SiTU and store h (W1/W3), or
+//     token's activation exponent, then apply SiTU (hardware tanh) and store
+//     h (W1/W3), or
 //     scale by the pair's routing weight and scatter-add into the token's fp32
 //     latent accumulator (W2).
 // All waits are bounded (mbar_wait); a role that gives up latches the error
@@ -44,7 +45,7 @@ namespace k3 {
 
 namespace {
 
-constexpr int BM = 128, BK = 128, BN = 64;
+constexpr int BM = 128, BK = 128;
 constexpr int kMinPairs = 128;                      // smallest batch (token, expert pairs) run here
 // warp roles: 0 TMA producer, 1 and 2 MMA issuers, 3 idle, 4..19 converters,
 // 20..23 epilogue (warp % 4 = its TMEM lane quadrant)
@@ -54,34 +55,40 @@ constexpr int kThreads = 24 * 32;
 constexpr int kRawRow = BK / 2;                     // packed bytes per row and k-stage
 constexpr int kRawBytes = BM * kRawRow;             // one packed weight tile
 constexpr int kBoxRows = 16;                        // activation rows per TMA box
-constexpr int kBSub = BN * 128;                     // one 64-column half of the activation tile
-constexpr int kBBytes = 2 * kBSub;
 constexpr int kSmemBudget = 227 * 1024;
-// TMEM: kSets accumulator sets of two BN-column accumulators, then the A ring
-#ifndef K3_EG_SETS
-#define K3_EG_SETS 2
-#endif
-constexpr int kSets = K3_EG_SETS;
-constexpr uint32_t kSetCols = 2 * BN;
-constexpr uint32_t kARing0 = kSets * kSetCols;
 constexpr uint32_t kTmemCols = 512;
 
-constexpr int a_cols(bool dual) { return (dual ? 2 : 1) * BK / 2; }            // TMEM columns per A slot
-constexpr int a_stages(bool dual) { return (int)(kTmemCols - kARing0) / a_cols(dual); }
-constexpr int r_stage(bool dual) { return kBBytes + (dual ? 2 : 1) * kRawBytes; }
-
-constexpr size_t smem_bytes(bool dual, int ns)
-{
-    return (size_t)ns * r_stage(dual) + (size_t)(2 * ns + a_stages(dual) + 2 * kSets) * 8 + 16 + 1024;
-}
-
-// TMA ring depth: as many stages as the shared-memory budget holds (at most 12).
-constexpr int ring_stages(bool dual)
-{
-    int ns = 2;
-    while (ns < 12 && smem_bytes(dual, ns + 1) <= (size_t)kSmemBudget - 1024) ns++;
-    return ns;
-}
+// Launch geometry for W1/W3 (DUAL) or W2 with n-tiles of BN pairs. TMEM holds
+// SETS accumulator sets of two BN-column accumulators (two sets for BN = 64,
+// so that the epilogue overlaps the next item; one for BN = 128), then the
+// ring of converted A slots in the remaining 256 columns.
+template <bool DUAL, int BN>
+struct Geo {
+    static_assert(BN == 64 || BN == 128, "n-tile of 64 or 128 pairs");
+    static constexpr int NM = DUAL ? 2 : 1;
+    static constexpr int SETS = BN == 64 ? 2 : 1;
+    static constexpr uint32_t SET_COLS = 2 * BN;
+    static constexpr uint32_t ARING0 = SETS * SET_COLS;     // 256
+    static constexpr int ACOLS = NM * BK / 2;                // TMEM columns per A slot
+    static constexpr int NSA = (int)(kTmemCols - ARING0) / ACOLS;
+    static constexpr int BSUB = BN * 128;                    // one 64-column half of the activation tile
+    static constexpr int BBYTES = 2 * BSUB;
+    static constexpr int R_STAGE = BBYTES + NM * kRawBytes;  // [B half 0 | B half 1 | packed W per matrix]
+    static constexpr size_t smem(int ns)
+    {
+        return (size_t)ns * R_STAGE + (size_t)(2 * ns + NSA + 2 * SETS) * 8 + 16 + 1024;
+    }
+    static constexpr int ring()                              // TMA ring depth (at most 12)
+    {
+        int ns = 2;
+        while (ns < 12 && smem(ns + 1) <= (size_t)kSmemBudget - 1024) ns++;
+        return ns;
+    }
+    static constexpr int NSR = ring();
+    static constexpr size_t SMEM = smem(NSR);
+    static_assert(ARING0 == 256, "accumulators take half of TMEM");
+    static_assert(NSR > NSA, "A slots are released through the TMA ring");
+};
 
 // Position in a ring of N slots: slot index and the parity of its current use.
 template <int N>
@@ -109,7 +116,7 @@ struct EgArgs {
     const __half *zp;            // gathered latent [T*k, L + kZPad], exponent in the padding
     __half *h16;                 // [T*k, I]
     float *acc;                  // [T, L]
-    float b1, b2;
+    float b1, b2, ib1, ib2;      // SiTU bounds and their reciprocals
     int *err;
 };
 
@@ -134,6 +141,20 @@ __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b)
 __device__ __forceinline__ float pow2_e8m0(int s)
 {
     return __uint_as_float((uint32_t)min(max(s, 1), 254) << 23);
+}
+
+__device__ __forceinline__ float tanh_hw(float x)
+{
+    float y;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// SiTU with the hardware tanh (relative error about 2^-11), sigma(g) written
+// as (1 + tanh(g / 2)) / 2: b1 tanh(g / b1) sigma(g) b2 tanh(u / b2).
+__device__ __forceinline__ float situ_hw(float g, float u, float b1, float b2, float ib1, float ib2)
+{
+    return (b1 * b2) * tanh_hw(g * ib1) * tanh_hw(u * ib2) * fmaf(0.5f, tanh_hw(0.5f * g), 0.5f);
 }
 
 // 16 packed bytes (32 columns, one scale group) -> 16 f16x2 scaled by f.
@@ -171,20 +192,18 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t *v)
                  : "memory");
 }
 
-template <bool DUAL>
+template <bool DUAL, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     k_expert_gemm(const __grid_constant__ CUtensorMap ra, const __grid_constant__ CUtensorMap rb,
                   const __grid_constant__ CUtensorMap bx, EgArgs g)
 {
+    using GE = Geo<DUAL, BN>;
     extern __shared__ unsigned char raw_smem[];
     unsigned char *sm = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(raw_smem) + 1023) & ~static_cast<uintptr_t>(1023));
-    constexpr int NM = DUAL ? 2 : 1;
-    constexpr int R_STAGE = r_stage(DUAL);   // [B half 0 | B half 1 | packed W (one per matrix)]
-    constexpr int NSR = ring_stages(DUAL);   // TMA ring depth
-    constexpr int NSA = a_stages(DUAL);      // TMEM A ring depth
-    constexpr int ACOLS = a_cols(DUAL);
-    static_assert(NSR > NSA, "A slots are released through the TMA ring");
+    constexpr int NM = GE::NM, R_STAGE = GE::R_STAGE, NSR = GE::NSR, NSA = GE::NSA, ACOLS = GE::ACOLS;
+    constexpr int kSets = GE::SETS, kBSub = GE::BSUB, kBBytes = GE::BBYTES;
+    constexpr uint32_t kSetCols = GE::SET_COLS, kARing0 = GE::ARING0;
     unsigned char *rring = sm;
     uint64_t *full = reinterpret_cast<uint64_t *>(rring + NSR * R_STAGE);   // TMA landed
     uint64_t *rfree = full + NSR;                            // both issuers' MMAs on the stage done
@@ -403,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int p = pair0 + c0 + j;
                         if (DUAL)
                             g.h16[(size_t)p * g.I + row_in_e] =
-                                __float2half_rn(situ_f(v0[j] * rs0 * fj, v1[j] * rs1 * fj, g.b1, g.b2));
+                                __float2half_rn(situ_hw(v0[j] * rs0 * fj, v1[j] * rs1 * fj, g.b1, g.b2, g.ib1, g.ib2));
                         else
                             atomicAdd(&g.acc[(size_t)tj * g.L + row_in_e], fj * ((v0[j] + v1[j]) * rs0));
                     }
@@ -423,30 +442,43 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-// n-tiles: (expert, j) for j < ceil(count_e / BN), experts ascending. One block.
-__global__ void __launch_bounds__(1024) k_expert_tiles(const int *counts, int E, int2 *tiles, int *n_tiles)
+// n-tiles: (expert, j) for j < ceil(count_e / 64) and, in a second list,
+// j < ceil(count_e / 128); experts ascending. One block.
+__global__ void __launch_bounds__(1024) k_expert_tiles(const int *counts, int E, int2 *t64, int2 *t128,
+                                                       int *n_tiles)
 {
-    __shared__ int wsum[32];
+    __shared__ int wsum[2][32];
     pdl_launch_dependents();
     pdl_wait();
     const int e = threadIdx.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int nt = e < E ? (counts[e] + BN - 1) / BN : 0;
-    int incl = nt;
+    const int c = e < E ? counts[e] : 0;
+    const int nt[2] = {(c + 63) / 64, (c + 127) / 128};
+    int incl[2] = {nt[0], nt[1]};
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
+#pragma unroll
+        for (int l = 0; l < 2; l++) {
+            const int v = __shfl_up_sync(0xffffffffu, incl[l], o);
+            if (lane >= o) incl[l] += v;
+        }
     }
-    if (lane == 31) wsum[warp] = incl;
+    if (lane == 31) {
+        wsum[0][warp] = incl[0];
+        wsum[1][warp] = incl[1];
+    }
     __syncthreads();
-    int base = 0, total = 0;
-    for (int w = 0; w < 32; w++) {
-        if (w < warp) base += wsum[w];
-        total += wsum[w];
+#pragma unroll
+    for (int l = 0; l < 2; l++) {
+        int base = 0, total = 0;
+        for (int w = 0; w < 32; w++) {
+            if (w < warp) base += wsum[l][w];
+            total += wsum[l][w];
+        }
+        int2 *out = l == 0 ? t64 : t128;
+        const int first = base + incl[l] - nt[l];
+        for (int j = 0; j < nt[l]; j++) out[first + j] = make_int2(e, j);
+        if (threadIdx.x == 0) n_tiles[l] = total;
     }
-    const int first = base + incl - nt;
-    for (int j = 0; j < nt; j++) tiles[first + j] = make_int2(e, j);
-    if (threadIdx.x == 0) *n_tiles = total;
 }
 
 // zp[p] = z16[token of pair p] (L values and the exponent padding); one warp per pair.
@@ -516,24 +548,41 @@ bool expert_gemm_ok(const k3moe_config &c)
 
 size_t expert_gemm_max_tiles(const k3moe_config &c)
 {
-    return (size_t)((long long)c.max_tokens * c.topk / BN + c.n_experts + 1);
+    return (size_t)((long long)c.max_tokens * c.topk / 64 + c.n_experts + 1);   // the narrower n-tile
 }
 
 int expert_gemm_min_pairs() { return kMinPairs; }
 
+template <bool DUAL, int BN>
+cudaError_t set_smem()
+{
+    return cudaFuncSetAttribute(k_expert_gemm<DUAL, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)Geo<DUAL, BN>::SMEM);
+}
+
 cudaError_t init_expert_gemm()
 {
-    cudaError_t e = cudaFuncSetAttribute(k_expert_gemm<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem_bytes(true, ring_stages(true)));
-    if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(k_expert_gemm<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)smem_bytes(false, ring_stages(false)));
+    cudaError_t e = set_smem<true, 64>();
+    if (e == cudaSuccess) e = set_smem<false, 64>();
+    if (e == cudaSuccess) e = set_smem<true, 128>();
+    if (e == cudaSuccess) e = set_smem<false, 128>();
+    return e;
+}
+
+// n-tile width of a launch: 128 pairs when the experts average at least 64
+// pairs each (every converted weight tile then feeds twice the MMA work, with
+// one accumulator set), else 64 with two sets so that the epilogue overlaps the
+// next item.
+int expert_gemm_bn(const k3moe &h, int T, bool w13)
+{
+    (void)w13;   // the same rule has measured best for both matrices
+    return (long long)T * h.cfg.topk >= 64LL * h.cfg.n_experts ? 128 : 64;
 }
 
 cudaError_t launch_expert_tiles(const k3moe &h, cudaStream_t s)
 {
-    return launch_pdl(k_expert_tiles, 1, 1024, 0, s, (const int *)h.ws.counts, h.cfg.n_experts,
-                      h.ws.tiles, h.ws.n_tiles);
+    return launch_pdl(k_expert_tiles, 1, 1024, 0, s, (const int *)h.ws.counts, h.cfg.n_experts, h.ws.tiles,
+                      h.ws.tiles128, h.ws.n_tiles);
 }
 
 cudaError_t launch_gather_latent(const k3moe &h, int T, cudaStream_t s)
@@ -544,25 +593,27 @@ cudaError_t launch_gather_latent(const k3moe &h, int T, cudaStream_t s)
 }
 
 // W1/W3 (w13 = true: gathered latent -> h16) or W2 (h16 -> acc).
-cudaError_t launch_expert_gemm(const k3moe &h, const LayerDev &w, int T, cudaStream_t s, bool w13)
+cudaError_t launch_expert_gemm(const k3moe &h, const LayerDev &w, int T, int bn, cudaStream_t s, bool w13)
 {
     const k3moe_config &c = h.cfg;
     const int pairs = T * c.topk;
-    if (pairs < kMinPairs) return cudaErrorInvalidValue;
+    if (pairs < kMinPairs || (bn != 64 && bn != 128)) return cudaErrorInvalidValue;
     EgArgs g = {};
     g.k = c.topk;
     g.L = c.latent;
     g.I = c.moe_inter;
     g.offsets = h.ws.offsets;
     g.perm = h.ws.perm;
-    g.tiles = h.ws.tiles;
-    g.n_tiles = h.ws.n_tiles;
+    g.tiles = bn == 128 ? h.ws.tiles128 : h.ws.tiles;
+    g.n_tiles = h.ws.n_tiles + (bn == 128 ? 1 : 0);
     g.pair_w = h.ws.pair_w;
     g.zp = h.ws.zperm;
     g.h16 = h.ws.h16;
     g.acc = h.ws.acc;
     g.b1 = c.situ_b1;
     g.b2 = c.situ_b2;
+    g.ib1 = 1.f / c.situ_b1;
+    g.ib2 = 1.f / c.situ_b2;
     g.err = h.ws.err;
     g.K = w13 ? c.latent : c.moe_inter;
     g.R = w13 ? c.moe_inter : c.latent;
@@ -586,9 +637,11 @@ cudaError_t launch_expert_gemm(const k3moe &h, const LayerDev &w, int T, cudaStr
         rb = ra;
     }
     if (!ok) return cudaErrorInvalidValue;
-    const size_t smem = smem_bytes(w13, ring_stages(w13));
-    return w13 ? launch_pdl(k_expert_gemm<true>, h.sm_count, kThreads, smem, s, ra, rb, bx, g)
-               : launch_pdl(k_expert_gemm<false>, h.sm_count, kThreads, smem, s, ra, rb, bx, g);
+    if (bn == 128)
+        return w13 ? launch_pdl(k_expert_gemm<true, 128>, h.sm_count, kThreads, Geo<true, 128>::SMEM, s, ra, rb, bx, g)
+                   : launch_pdl(k_expert_gemm<false, 128>, h.sm_count, kThreads, Geo<false, 128>::SMEM, s, ra, rb, bx, g);
+    return w13 ? launch_pdl(k_expert_gemm<true, 64>, h.sm_count, kThreads, Geo<true, 64>::SMEM, s, ra, rb, bx, g)
+               : launch_pdl(k_expert_gemm<false, 64>, h.sm_count, kThreads, Geo<false, 64>::SMEM, s, ra, rb, bx, g);
 }
 
 cudaError_t launch_row_scale_max(const uint8_t *s, size_t rows, int G, uint8_t *out)

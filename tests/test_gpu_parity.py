@@ -92,6 +92,21 @@ def test_expert_gemm_multi_tile(path):
     run_case(WIDE, k3synth.TINY_RECIPE, 8, 300, expert_path=mode, d=d)
 
 
+@pytest.mark.parametrize("hot", [False, True])
+def test_expert_gemm_wide_ntiles(hot):
+    """T=1100 on the 128-expert shape: 8800 pairs, at least 64 per expert on
+    average, so the grouped GEMM cuts 128-pair n-tiles. With four experts forced
+    into every selection each of them holds 1100 pairs (nine n-tiles)."""
+    import mxfp4_routed_expert_gb300 as km
+    d = k3synth.make_layer(WIDE, 9, 0, k3synth.TINY_RECIPE)
+    if hot:
+        bias = np.asarray(d["router_bias"], np.float32).copy()
+        bias[[0, 31, 64, 100]] += 10.0
+        d = k3synth.with_bias(d, bias)
+    run_case(WIDE, k3synth.TINY_RECIPE, 9, 1100, expert_path=km.K3MOE_EXPERT_GEMM, d=d,
+             check_intermediates=not hot)
+
+
 def test_expert_path_selection_and_errors():
     import mxfp4_routed_expert_gb300 as km
     d = k3synth.make_layer(WIDE, 6, 0, k3synth.TINY_RECIPE)
