@@ -255,7 +255,7 @@ def traffic_for(kernel, workload):
 def time_oracle(shape, d, x, n_tokens):
     import oracle
     oracle.build()
-    rows = np.arange(min(n_tokens, x.shape[0]), dtype=np.int32)
+    rows = (np.arange(n_tokens) % x.shape[0]).astype(np.int32)   # the pool repeats when it is smaller
     t0 = time.perf_counter()
     oracle.layer_forward(shape, d, x, rows=rows)
     dt = time.perf_counter() - t0
@@ -400,13 +400,13 @@ def run_native(args, rank, world):
     # ---- CPU baseline: the oracle on a bounded sample ---------------------------------------
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        n_tok = 16
+        n_tok = 320                      # about 10-20 s of the oracle on the machine's cores
         xs_host = xpool if T == 1 else xpool[:T]
         nrow, dt = time_oracle(shape, oracle_layer, xs_host, n_tok)
         cpu = {"value": round(nrow / dt / n_layers, 4), "unit": UNIT,
                "cores": omp_threads(nrow), "kind": "oracle",
-               "sample": f"{nrow} tokens of the workload through one layer (fp64 C oracle, "
-                         f"OpenMP over tokens), {dt:.1f} s"
+               "sample": f"{nrow} token rows of the workload ({min(nrow, xs_host.shape[0])} distinct) "
+                         f"through one layer (fp64 C oracle, OpenMP over tokens), {dt:.1f} s"
                          + ("; chain value = per-layer rate / 8" if n_layers > 1 else "")}
     km.k3moe_destroy(h)
     if rank != 0:

@@ -207,35 +207,42 @@ int run_layer(k3moe *h, const LayerDev &w, const __nv_bfloat16 *x, __nv_bfloat16
         e = (call);                                \
     }                                              \
     if (e != cudaSuccess) return K3MOE_ERR_CUDA;
-    // stream s:    router+down -> route -> permute -> [join] -> experts -> up
-    // side stream:  [after router+down] shared-expert gate/up (overlaps route, permute)
+    // Decode (T <= 15), one stream with programmatic dependent launch:
+    //   router+down -> route -> shared gate/up -> experts -> up
+    // The shared gate/up kernel's producers stream weights before their wait
+    // on the router, so it runs alongside the single-block router on the
+    // other SMs; a side stream would add an event fork and join for no
+    // overlap (the experts need every SM once the shared experts hold them).
+    // Batched (T >= 16): the shared gate/up GEMM on a side stream after
+    // router+down, joined before the experts.
     const bool tma = T <= 2 && h->dense_tma_ok[T - 1];
     const bool gemm = T >= kGemmMinTokens && h->gemm_ok;
     const bool egemm = use_expert_gemm(*h, T);
     if (gemm) {
         K3_STEP("router_down_gemm", launch_dense_gemm(*h, w, x, nullptr, T, s, 0));
+        if (cudaEventRecord(h->ev_fork, s) != cudaSuccess ||
+            cudaStreamWaitEvent(h->side, h->ev_fork, 0) != cudaSuccess)
+            return K3MOE_ERR_CUDA;
+        {
+            Prof p_(h, "shared_gate_up_gemm", h->side);
+            e = launch_dense_gemm(*h, w, x, nullptr, T, h->side, 1);
+        }
+        if (e != cudaSuccess || cudaEventRecord(h->ev_join, h->side) != cudaSuccess)
+            return K3MOE_ERR_CUDA;
+        K3_STEP("route_topk", launch_route(*h, w, T, s));
     } else {
         K3_STEP("router_down_gemv", tma ? launch_dense_tma(*h, w, x, nullptr, T, s, 0)
                                         : launch_dense_x(*h, w, x, T, s, 0));
+        K3_STEP("route_topk", launch_route(*h, w, T, s));
+        K3_STEP("shared_gate_up_gemv", tma ? launch_dense_tma(*h, w, x, nullptr, T, s, 1)
+                                           : launch_dense_x(*h, w, x, T, s, 1));
     }
-    if (cudaEventRecord(h->ev_fork, s) != cudaSuccess ||
-        cudaStreamWaitEvent(h->side, h->ev_fork, 0) != cudaSuccess)
-        return K3MOE_ERR_CUDA;
-    {
-        Prof p_(h, gemm ? "shared_gate_up_gemm" : "shared_gate_up_gemv", h->side);
-        e = gemm ? launch_dense_gemm(*h, w, x, nullptr, T, h->side, 1)
-                 : tma ? launch_dense_tma(*h, w, x, nullptr, T, h->side, 1)
-                       : launch_dense_x(*h, w, x, T, h->side, 1);
-    }
-    if (e != cudaSuccess || cudaEventRecord(h->ev_join, h->side) != cudaSuccess)
-        return K3MOE_ERR_CUDA;
-    K3_STEP("route_topk", launch_route(*h, w, T, s));
     if (T > 1) {   // T == 1: written by route_topk
         K3_STEP("perm_count", launch_perm(*h, T, s, 0));
         K3_STEP("perm_scan", launch_perm(*h, T, s, 1));
         K3_STEP("perm_place", launch_perm(*h, T, s, 2));
     }
-    if (cudaStreamWaitEvent(s, h->ev_join, 0) != cudaSuccess) return K3MOE_ERR_CUDA;
+    if (gemm && cudaStreamWaitEvent(s, h->ev_join, 0) != cudaSuccess) return K3MOE_ERR_CUDA;
     if (egemm) {
         K3_STEP("expert_tiles", launch_expert_tiles(*h, s));
         K3_STEP("gather_latent", launch_gather_latent(*h, T, s));

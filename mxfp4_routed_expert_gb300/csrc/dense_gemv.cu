@@ -90,6 +90,7 @@ struct DenseXArgs {
     int cat_ld;
     float b1, b2;
     int u_begin, u_end;   // unit range of this launch: router, then down, then shared pairs
+    int wait;             // wait for the previous kernel (0: the launch reads only x)
 };
 
 constexpr int kGemvWarps = 8;
@@ -101,7 +102,7 @@ __global__ void __launch_bounds__(kGemvWarps * 32) k_dense_x(DenseXArgs a)
     extern __shared__ float xs[];   // [TB][H]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     pdl_launch_dependents();
-    pdl_wait();
+    if (a.wait) pdl_wait();
     const int nA = (a.E + 3) / 4, nB = a.L / 4;
     for (int t0 = 0; t0 < a.T; t0 += TB) {
         const int tb = min(TB, a.T - t0);
@@ -312,6 +313,9 @@ static cudaError_t run_dense_x(const k3moe &h, const DenseXArgs &a, int slot, cu
     const size_t smem = (size_t)TB * a.H * sizeof(float);
     const int want = (a.u_end - a.u_begin + kGemvWarps - 1) / kGemvWarps;
     const int grid = want < h.grid_dense[slot] ? want : h.grid_dense[slot];
+    // router+down opens the layer in plain stream order; the shared gate/up
+    // alone (u_begin > 0) reads only x and needs no wait
+    if (a.u_begin == 0) return launch_ordered(k_dense_x<TB>, grid, kGemvWarps * 32, smem, s, a);
     return launch_pdl(k_dense_x<TB>, grid, kGemvWarps * 32, smem, s, a);
 }
 
@@ -339,6 +343,7 @@ cudaError_t launch_dense_x(const k3moe &h, const LayerDev &w, const __nv_bfloat1
     const int nAB = (c.n_experts + 3) / 4 + c.latent / 4, nC = c.shared_inter / 2;
     a.u_begin = part == 1 ? nAB : 0;
     a.u_end = part == 0 ? nAB : nAB + nC;
+    a.wait = part != 1;
     if (T == 1) return run_dense_x<1>(h, a, 0, s);
     if (T == 2) return run_dense_x<2>(h, a, 1, s);
     return run_dense_x<4>(h, a, 2, s);

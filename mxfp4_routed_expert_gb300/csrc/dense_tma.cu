@@ -8,13 +8,17 @@
 //   UP: y = Wu . n + Ws2 . s with n = RMSNorm(acc) * gain (the norm of the
 //       aggregate, section 9 step 4) and s the shared SiTU output, bf16 output.
 //
-// Persistent, one CTA per SM: one producer thread streams weight-row stages
+// Persistent, one CTA per SM: a producer warp streams weight-row stages
 // through a shared-memory ring with bulk TMA copies (one copy per row piece),
-// eight consumer warps each own one row (RD, UP) or one gate/up row pair (SH)
-// of a stage. The activations of the TB tokens sit in shared memory as fp32
-// for the whole kernel; the producer starts streaming weights while the
-// consumers stage them. A unit is one row (or pair) per consumer warp over the
-// whole K; units are split evenly and contiguously over the CTAs.
+// sixteen consumer warps each own one row (RD, UP) or one gate/up row pair
+// (SH) of a stage. The activations of the TB tokens sit in shared memory as
+// bf16 for the whole kernel. The producer starts streaming weights before the
+// programmatic-launch wait on the previous kernel (weights do not depend on
+// it) while the consumers wait and then stage the activations. Router+down,
+// a layer's first kernel, is launched in plain stream order; the shared
+// gate/up, which reads only the layer input, then needs no wait at all. A unit is one
+// row (or pair) per consumer warp over the whole K; units are split evenly and
+// contiguously over the CTAs.
 #include <algorithm>
 
 #include "k3moe_internal.cuh"
@@ -45,6 +49,7 @@ struct DenseTArgs {
     __nv_bfloat16 *y;                  // UP: [T, H]
     float b1, b2;
     int units;                         // rows (RD: E+L, UP: H) or gate/up row pairs (SH: S)
+    int wait;                          // consumers wait for the previous kernel (0: they read only x)
     int ns;                            // pipeline stages
     int *err;
 };
@@ -122,7 +127,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_dense_tma(DenseTArgs a)
     }
     __syncthreads();
     pdl_launch_dependents();
-    pdl_wait();
+    // The producer reads weights only, which no earlier kernel writes: it
+    // starts filling the ring at once, while the kernel this one depends on
+    // drains. The consumers wait for it before they read activations.
+    if (warp != kCW && a.wait) pdl_wait();
 
     // balanced contiguous range of rows (or pairs) of this CTA
     const int r0 = (int)((long long)a.units * blockIdx.x / gridDim.x);
@@ -385,6 +393,13 @@ cudaError_t launch_dense_tma(const k3moe &h, const LayerDev &w, const __nv_bfloa
     const int groups = (a.units + kCW - 1) / kCW;
     const int grid = groups < h.sm_count ? groups : h.sm_count;
     const size_t smem = dense_tma_smem(a.mode, a.K, TB, a.ns);
+    // The shared gate/up reads only the layer input x and writes its own output
+    // rows; the layer's first kernel (router+down, launched in stream order)
+    // has already waited for everything the input depends on.
+    a.wait = a.mode != SH;
+    if (a.mode == RD)
+        return TB == 1 ? launch_ordered(k_dense_tma<1>, grid, kThreads, smem, s, a)
+                       : launch_ordered(k_dense_tma<2>, grid, kThreads, smem, s, a);
     return TB == 1 ? launch_pdl(k_dense_tma<1>, grid, kThreads, smem, s, a)
                    : launch_pdl(k_dense_tma<2>, grid, kThreads, smem, s, a);
 }

@@ -343,6 +343,24 @@ inline cudaError_t launch_pdl(void (*kern)(KArgs...), int grid, int block, size_
     return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
+// The same without programmatic serialization: the kernel starts only after
+// all earlier work on the stream has completed. A layer's first kernel uses
+// it, so that every later kernel of the layer may rely on the layer input
+// and on the previous forward having finished with the workspace.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_ordered(void (*kern)(KArgs...), int grid, int block, size_t smem,
+                                  cudaStream_t s, Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3((unsigned)block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = nullptr;
+    cfg.numAttrs = 0;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 __device__ __forceinline__ float warp_sum(float v)
 {
 #pragma unroll

@@ -87,6 +87,13 @@ __global__ void __launch_bounds__(kRouteThreads) k_route(RouteArgs a)
     __shared__ float sel_ch[kMaxTopk], sel_sc[kMaxTopk];
     __shared__ int sel_e[kMaxTopk];
     pdl_launch_dependents();
+    // the selection bias is a layer weight: read it before waiting on the router
+    float bv[kEPer];
+#pragma unroll
+    for (int j = 0; j < kEPer; j++) {
+        const int e = kEPer * tid + j;
+        bv[j] = e < a.E ? a.bias[e] : 0.f;
+    }
     pdl_wait();
 
     // ---- expert GEMV input: fp16 z with a per-token power-of-two scale ----
@@ -114,7 +121,7 @@ __global__ void __launch_bounds__(kRouteThreads) k_route(RouteArgs a)
         valid[j] = e < a.E;
         const float sgm = valid[j] ? sigmoid_f(lg[e]) : 0.f;
         scv[j] = sgm;
-        ch[j] = sgm + (valid[j] ? a.bias[e] : 0.f);
+        ch[j] = sgm + bv[j];
         key[j] = order_key(ch[j]);
     }
     // k-th largest key by a bitwise search: the largest thr with #(key >= thr) >= k
