@@ -101,7 +101,13 @@ def roofline(kernel, model, avg_ms, hbm_peak, tc_peak, peak_src, workload):
                  "flops_per_launch": int(fl), "avg_launch_ms": round(avg_ms, 5),
                  "hbm_frac": round(f_hbm, 4), "tensor_frac": round(f_tc, 4)})
     if fl:
+        # against the attainable roof min(peak, arithmetic intensity x HBM bandwidth)
+        ai = fl / byt
+        att = min(tc_peak, ai * hbm_peak / 1e3)
+        roof["attainable_tflops"] = round(att, 1)
+        roof["attainable_frac"] = round(tfl / att, 4)
         roof["fp4_nominal_frac"] = round(tfl / FP4_NOMINAL_TFLOPS, 4)
+        roof["fp4_attainable_frac"] = round(tfl / min(FP4_NOMINAL_TFLOPS, ai * hbm_peak / 1e3), 4)
     return roof
 
 
@@ -331,20 +337,21 @@ def run_native(args, rank, world):
         if profiled:
             stats = km.k3moe_profile_read(h)
             km.k3moe_set_profiling(h, False)
-        return sum(s.elapsed_time(e) for s, e in zip(starts, ends)), stats
+        times = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+        return sum(times), stats, times
 
     # pass 1 (the measurement): no per-kernel events between the launches
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     clocks.start()
-    total_ms, _ = timed_pass(False)
+    total_ms, _, step_times = timed_pass(False)
     if world > 1:
         torch.distributed.barrier()
     clk = clocks.stop()
     # pass 2: the same steps with every kernel bracketed by CUDA events on its
     # launching stream (per-kernel durations for the roofline)
-    prof_ms, stats = timed_pass(True)
+    prof_ms, stats, _ = timed_pass(True)
     st = km.k3moe_sync_status(h)
     assert st == 0, km.strerror(st)
     if world > 1:
@@ -424,6 +431,9 @@ def run_native(args, rank, world):
                    "l2": "256 MB flush between timed steps; working set > L2",
                    "experts_touched_per_step": n_touched},
         "hbm_gbs_layer": round(layer_gbs, 1), "hbm_frac_layer": round(layer_gbs / hbm_peak, 4),
+        "step_ms": {"median": round(float(np.median(step_times)), 5),
+                    "p10": round(float(np.percentile(step_times, 10)), 5),
+                    "p90": round(float(np.percentile(step_times, 90)), 5)},
         "roofline": roof, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": gpu_launches, "clocks": clk,
     }

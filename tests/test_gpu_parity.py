@@ -313,8 +313,10 @@ def test_k3_T64_random(k3layer):
 
 def test_k3_T4096_zipf_prefill(k3layer):
     """Prefill: 4096 tokens, Zipf(1.1) expert popularity through the router
-    bias. Ids and the permutation are checked on every token, y on 64 sampled
-    tokens (every 64th) against the oracle."""
+    bias. Ids and the permutation are checked on every token; y against the
+    oracle on every 16th token, on every token of the 4 least-picked experts
+    (ragged n-tiles) and on 32 tokens of each of the 4 most-picked ones (many
+    n-tiles)."""
     d, lay = k3layer
     shape = k3synth.K3
     dz = k3synth.with_bias(d, k3synth.zipf_bias(shape, 0, 0, k3synth.K3_ZIPF_ALPHA))
@@ -326,8 +328,43 @@ def test_k3_T4096_zipf_prefill(k3layer):
         r = lay.routing(T)
         ids, w, _ = oracle.route(shape, dz, x)
         check_routing(r, shape, x, ids, w)
-        rows = np.arange(0, T, 64, dtype=np.int32)
+        counts = np.bincount(ids.ravel(), minlength=shape.n_experts)
+        used = np.flatnonzero(counts)
+        cold = used[np.argsort(counts[used], kind="stable")[:4]]
+        hot = np.argsort(-counts, kind="stable")[:4]
+        rows = set(range(0, T, 16))
+        for e in cold:
+            rows.update(np.flatnonzero((ids == e).any(1)).tolist())
+        for e in hot:
+            rows.update(np.flatnonzero((ids == e).any(1))[:32].tolist())
+        rows = np.array(sorted(rows), dtype=np.int32)
         ref = oracle.layer_forward(shape, dz, x, rows=rows)
-        assert_close(bf16_to_f64(y)[rows], ref, "K3 T=4096 Zipf (sampled rows)")
+        assert_close(bf16_to_f64(y)[rows], ref, f"K3 T=4096 Zipf ({rows.size} sampled rows)")
     finally:
         lay.load(0, d)
+
+
+def test_k3_chain_two_layers_T256():
+    """Two stacked K3-shape layers at T=256 (the chain workload's batch): layer 0
+    against the oracle, layer 1 against the oracle given the GPU's own layer-1
+    input (RMSNorm of layer 0's output), both on 32 sampled tokens."""
+    shape = k3synth.K3
+    d0 = k3synth.make_layer(shape, 3, 0, k3synth.K3_RECIPE)
+    d1 = k3synth.make_layer(shape, 3, 1, k3synth.K3_RECIPE)
+    T = 256
+    x, _ = guarded_tokens(shape, d0, 3, T, stream=13)
+    lay = Layer(shape, [d0, d1], max_tokens=T)
+    try:
+        y = lay.forward(x, layer=0, chain=2)
+        y0 = lay.forward(x, layer=0)
+    finally:
+        lay.close()
+    rows = np.arange(0, T, 8, dtype=np.int32)
+    assert_close(bf16_to_f64(y0)[rows], oracle.layer_forward(shape, d0, x, rows=rows), "K3 chain layer 0")
+    x1 = k3synth.round_bf16(oracle.chain_glue(bf16_to_f64(y0), shape.rms_eps))
+    _, _, margin = oracle.route(shape, d1, x1)
+    ok = np.flatnonzero(margin > 1e-5)
+    sel = ok[:: max(1, ok.size // 32)][:32].astype(np.int32)
+    assert sel.size >= 24
+    ref1 = oracle.layer_forward(shape, d1, x1, rows=sel)
+    assert_close(bf16_to_f64(y)[sel], ref1, "K3 chain layer 1")
