@@ -70,13 +70,13 @@ struct Geo {
     static constexpr uint32_t SET_COLS = 2 * BN;
     static constexpr uint32_t ARING0 = SETS * SET_COLS;     // 256
     static constexpr int ACOLS = NM * BK / 2;                // TMEM columns per A slot
-    static constexpr int NSA = (int)(kTmemCols - ARING0) / ACOLS;
+    static constexpr int NSA_TMEM = (int)(kTmemCols - ARING0) / ACOLS;
     static constexpr int BSUB = BN * 128;                    // one 64-column half of the activation tile
     static constexpr int BBYTES = 2 * BSUB;
     static constexpr int R_STAGE = BBYTES + NM * kRawBytes;  // [B half 0 | B half 1 | packed W per matrix]
     static constexpr size_t smem(int ns)
     {
-        return (size_t)ns * R_STAGE + (size_t)(2 * ns + NSA + 2 * SETS) * 8 + 16 + 1024;
+        return (size_t)ns * R_STAGE + (size_t)(2 * ns + NSA_TMEM + 2 * SETS) * 8 + 16 + 1024;
     }
     static constexpr int ring()                              // TMA ring depth (at most 12)
     {
@@ -85,6 +85,10 @@ struct Geo {
         return ns;
     }
     static constexpr int NSR = ring();
+    // A slots: what TMEM holds, but leaving at least three TMA stages of
+    // prefetch beyond the converted ones (a TMA stage is refilled only after
+    // the MMAs of the stage it held), and at least two
+    static constexpr int NSA = NSA_TMEM < NSR - 3 ? NSA_TMEM : (NSR - 3 > 2 ? NSR - 3 : 2);
     static constexpr size_t SMEM = smem(NSR);
     static_assert(ARING0 == 256, "accumulators take half of TMEM");
     static_assert(NSR > NSA, "A slots are released through the TMA ring");
@@ -192,6 +196,70 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t *v)
                  : "memory");
 }
 
+// Epilogue of one item: the calling warp reads its TMEM lane quadrant
+// (rows 32 (warp % 4) .. + 31 of the tile) for the pair columns c_first,
+// c_first + c_step, ... (16 at a time), applies the row and token factors and
+// SiTU (W1/W3) or the weighted scatter-add (W2), then releases the
+// accumulator set.
+template <bool DUAL, int BN>
+__device__ __forceinline__ bool epilogue_item(const EgArgs &g, uint32_t tmem, int item, int local,
+                                              uint64_t *tfull, uint64_t *tempty, int c_first, int c_step)
+{
+    using GE = Geo<DUAL, BN>;
+    const int lane = threadIdx.x & 31;
+    const int q = (threadIdx.x >> 5) & 3;   // TMEM lanes 32q..32q+31
+    const int erow = q * 32 + lane;         // weight row of the tile
+    const int tile = item / g.MT, mt = item - tile * g.MT;
+    const int2 td = g.tiles[tile];
+    const int cnt = g.offsets[td.x + 1] - g.offsets[td.x];
+    const int n_valid = min(BN, cnt - td.y * BN);
+    const int pair0 = g.offsets[td.x] + td.y * BN;
+    const int row_in_e = mt * BM + erow;
+    const size_t grow = (size_t)td.x * g.R + row_in_e;
+    const float rs0 = pow2_e8m0(g.ma[grow]);
+    const float rs1 = DUAL ? pow2_e8m0(g.mb[grow]) : 0.f;
+    const int b = local % GE::SETS;
+    if (!mbar_wait(&tfull[b], (uint32_t)(local / GE::SETS) & 1u, g.err, 606)) return false;
+    tc::fence_after();
+    const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)b * GE::SET_COLS;
+    for (int c0 = c_first; c0 < n_valid; c0 += c_step) {
+        // per-pair factors for columns c0..c0+15, one lane each, then broadcast
+        const int pl = pair0 + c0 + (lane & 15);
+        const bool lv = c0 + (lane & 15) < n_valid;
+        float pf = 0.f;      // W1/W3: 2^(token exponent); W2: routing weight
+        int pt = 0;          // W2: token
+        if (lv) {
+            if (DUAL) {
+                const int ex = *reinterpret_cast<const int *>(g.zp + (size_t)pl * (g.L + kZPad) + g.L);
+                pf = __uint_as_float((uint32_t)(127 + ex) << 23);
+            } else {
+                pf = g.pair_w[pl];
+                pt = g.perm[pl] / g.k;
+            }
+        }
+        float v0[16], v1[16];
+        tc::tmem_ld16(tb + (uint32_t)c0, v0);
+        tc::tmem_ld16(tb + (uint32_t)(BN + c0), v1);
+#pragma unroll
+        for (int j = 0; j < 16; j++) {
+            const float fj = __shfl_sync(0xffffffffu, pf, j);
+            const int tj = DUAL ? 0 : __shfl_sync(0xffffffffu, pt, j);
+            if (c0 + j < n_valid) {
+                const int p = pair0 + c0 + j;
+                if (DUAL)
+                    g.h16[(size_t)p * g.I + row_in_e] =
+                        __float2half_rn(situ_hw(v0[j] * rs0 * fj, v1[j] * rs1 * fj, g.b1, g.b2, g.ib1, g.ib2));
+                else
+                    atomicAdd(&g.acc[(size_t)tj * g.L + row_in_e], fj * ((v0[j] + v1[j]) * rs0));
+            }
+        }
+    }
+    tc::fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&tempty[b]);
+    return true;
+}
+
 template <bool DUAL, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     k_expert_gemm(const __grid_constant__ CUtensorMap ra, const __grid_constant__ CUtensorMap rb,
@@ -221,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < NSA; i++) mbar_init(&aready[i], kConvWarps);
         for (int i = 0; i < kSets; i++) {
             mbar_init(&tfull[i], 2);
-            mbar_init(&tempty[i], kEpiWarps);
+            mbar_init(&tempty[i], kSets == 2 ? kEpiWarps : kConvWarps);
         }
         fence_mbar_init();
         tc::prefetch_map(&ra);
@@ -339,8 +407,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         RingPos<NSR> rq;          // TMA stage of the k-stage NSA back (its MMAs free the slot)
         RingPos<NSA> ap;
         int done = 0;             // k-stages converted so far
+        int local = 0;            // items of this CTA so far
         bool ok = true;
-        for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+        // With one accumulator set the issuers stop between items until the
+        // accumulators are drained, and the converters, whose A slots free up
+        // only when the next item's MMAs run, would idle: so they run the
+        // epilogue themselves (each warp a quarter of the pair columns of its
+        // lane quadrant) right after converting the first NSA k-stages of the
+        // next item.
+        for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, local++) {
             const int tile = item / g.MT, mt = item - tile * g.MT;
             const size_t grow = (size_t)g.tiles[tile].x * g.R + mt * BM + row;
             const int smax = m == 0 ? g.ma[grow] : g.mb[grow];
@@ -375,63 +450,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc::fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&aready[ap.slot]);
+                if (kSets == 1 && local > 0 && kt == min(NSA, KT) - 1 &&
+                    !epilogue_item<DUAL, BN>(g, tmem, item - (int)gridDim.x, local - 1, tfull, tempty, 16 * sl, 64)) {
+                    ok = false;
+                    break;
+                }
             }
         }
-    } else if (warp >= kEpiWarp0) {
-        // ---------------- epilogue ----------------
-        const int q = warp & 3;                 // TMEM lanes 32q..32q+31
-        const int erow = q * 32 + lane;         // weight row of the tile
+        if (kSets == 1 && ok && local > 0)
+            epilogue_item<DUAL, BN>(g, tmem, blockIdx.x + (local - 1) * (int)gridDim.x, local - 1, tfull, tempty,
+                                    16 * sl, 64);
+    } else if (kSets == 2 && warp >= kEpiWarp0) {
+        // ---------------- epilogue (two accumulator sets) ----------------
         int local = 0;
-        for (int item = blockIdx.x; item < n_items; item += gridDim.x, local++) {
-            const int tile = item / g.MT, mt = item - tile * g.MT;
-            const int2 td = g.tiles[tile];
-            const int cnt = g.offsets[td.x + 1] - g.offsets[td.x];
-            const int n_valid = min(BN, cnt - td.y * BN);
-            const int pair0 = g.offsets[td.x] + td.y * BN;
-            const int row_in_e = mt * BM + erow;
-            const size_t grow = (size_t)td.x * g.R + row_in_e;
-            const float rs0 = pow2_e8m0(g.ma[grow]);
-            const float rs1 = DUAL ? pow2_e8m0(g.mb[grow]) : 0.f;
-            const int b = local % kSets;
-            if (!mbar_wait(&tfull[b], (uint32_t)(local / kSets) & 1u, g.err, 606)) break;
-            tc::fence_after();
-            const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)b * kSetCols;
-            for (int c0 = 0; c0 < n_valid; c0 += 16) {
-                // per-pair factors for columns c0..c0+15, one lane each, then broadcast
-                const int pl = pair0 + c0 + (lane & 15);
-                const bool lv = c0 + (lane & 15) < n_valid;
-                float pf = 0.f;      // W1/W3: 2^(token exponent); W2: routing weight
-                int pt = 0;          // W2: token
-                if (lv) {
-                    if (DUAL) {
-                        const int ex = *reinterpret_cast<const int *>(g.zp + (size_t)pl * (g.L + kZPad) + g.L);
-                        pf = __uint_as_float((uint32_t)(127 + ex) << 23);
-                    } else {
-                        pf = g.pair_w[pl];
-                        pt = g.perm[pl] / g.k;
-                    }
-                }
-                float v0[16], v1[16];
-                tc::tmem_ld16(tb + (uint32_t)c0, v0);
-                tc::tmem_ld16(tb + (uint32_t)(BN + c0), v1);
-#pragma unroll
-                for (int j = 0; j < 16; j++) {
-                    const float fj = __shfl_sync(0xffffffffu, pf, j);
-                    const int tj = DUAL ? 0 : __shfl_sync(0xffffffffu, pt, j);
-                    if (c0 + j < n_valid) {
-                        const int p = pair0 + c0 + j;
-                        if (DUAL)
-                            g.h16[(size_t)p * g.I + row_in_e] =
-                                __float2half_rn(situ_hw(v0[j] * rs0 * fj, v1[j] * rs1 * fj, g.b1, g.b2, g.ib1, g.ib2));
-                        else
-                            atomicAdd(&g.acc[(size_t)tj * g.L + row_in_e], fj * ((v0[j] + v1[j]) * rs0));
-                    }
-                }
-            }
-            tc::fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&tempty[b]);
-        }
+        for (int item = blockIdx.x; item < n_items; item += gridDim.x, local++)
+            if (!epilogue_item<DUAL, BN>(g, tmem, item, local, tfull, tempty, 0, 16)) break;
     }
 
     tc::fence_before();
