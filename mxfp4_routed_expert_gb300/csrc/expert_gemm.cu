@@ -24,12 +24,14 @@
 //     column c = columns 2c, 2c+1), the MMA's A operand, so that shared memory
 //     carries only packed weights and activations;
 //   - two threads issue tcgen05.mma kind::f16 (A from TMEM, B from shared
-//     memory) into fp32 TMEM accumulators, one each (W1/W3: gate and up; W2:
-//     the two halves of every k-stage, summed in the epilogue), with two
-//     accumulator sets so that the next item's MMAs overlap this item's
-//     epilogue; the rest of TMEM holds the A ring. An A slot is reused once
-//     the TMA stage of the k-stage that last held it is released, which both
-//     issuers' commits signal;
+//     memory) into fp32 TMEM accumulators, one each. W1/W3: gate and up of
+//     the same 128 rows. W2: two adjacent 128-row m-tiles per item when the
+//     latent width allows (so each activation tile feeds 256 weight rows), else
+//     the two halves of every k-stage, summed in the epilogue. With 64-pair
+//     n-tiles two accumulator sets let the next item's MMAs overlap this
+//     item's epilogue; the rest of TMEM holds the A ring. An A slot is reused
+//     once the TMA stage of the k-stage that last held it is released, which
+//     both issuers' commits signal;
 //   - four epilogue warps read TMEM, multiply by 2^(smax_row - 127) and the
 //     token's activation exponent, then apply SiTU (hardware tanh) and store
 //     h (W1/W3), or
@@ -58,14 +60,19 @@ constexpr int kBoxRows = 16;                        // activation rows per TMA b
 constexpr int kSmemBudget = 227 * 1024;
 constexpr uint32_t kTmemCols = 512;
 
-// Launch geometry for W1/W3 (DUAL) or W2 with n-tiles of BN pairs. TMEM holds
+// Kernel modes: W1/W3 together (kW13), W2 with the two halves of each k-stage
+// on the two issuers (kW2), or W2 with two adjacent 128-row m-tiles per item
+// (kW2Pair: the activation tile then feeds twice the weight rows).
+enum : int { kW13 = 0, kW2 = 1, kW2Pair = 2 };
+
+// Launch geometry for a mode with n-tiles of BN pairs. TMEM holds
 // SETS accumulator sets of two BN-column accumulators (two sets for BN = 64,
 // so that the epilogue overlaps the next item; one for BN = 128), then the
 // ring of converted A slots in the remaining 256 columns.
-template <bool DUAL, int BN>
+template <int MODE, int BN>
 struct Geo {
     static_assert(BN == 64 || BN == 128, "n-tile of 64 or 128 pairs");
-    static constexpr int NM = DUAL ? 2 : 1;
+    static constexpr int NM = MODE == kW2 ? 1 : 2;           // weight tiles per k-stage
     static constexpr int SETS = BN == 64 ? 2 : 1;
     static constexpr uint32_t SET_COLS = 2 * BN;
     static constexpr uint32_t ARING0 = SETS * SET_COLS;     // 256
@@ -111,7 +118,8 @@ struct RingPos {
 struct EgArgs {
     const uint8_t *sa, *sb;      // scale rows [E*R, K/32] (W1 and W3, or W2)
     const uint8_t *ma, *mb;      // largest scale byte per row [E*R]
-    int K, R, MT;                // input width, rows per expert, m-tiles per expert
+    int K, R, MT;                // input width, rows per expert, items per expert along the rows
+    int mstep, mrow;             // rows per item (128, or 256 for kW2Pair); second tile's row offset
     int k, L, I;
     const int *offsets, *perm;
     const int2 *tiles;           // (expert, n-tile index) per n-tile
@@ -201,11 +209,12 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t *v)
 // c_first + c_step, ... (16 at a time), applies the row and token factors and
 // SiTU (W1/W3) or the weighted scatter-add (W2), then releases the
 // accumulator set.
-template <bool DUAL, int BN>
+template <int MODE, int BN>
 __device__ __forceinline__ bool epilogue_item(const EgArgs &g, uint32_t tmem, int item, int local,
                                               uint64_t *tfull, uint64_t *tempty, int c_first, int c_step)
 {
-    using GE = Geo<DUAL, BN>;
+    using GE = Geo<MODE, BN>;
+    constexpr bool IS13 = MODE == kW13;
     const int lane = threadIdx.x & 31;
     const int q = (threadIdx.x >> 5) & 3;   // TMEM lanes 32q..32q+31
     const int erow = q * 32 + lane;         // weight row of the tile
@@ -214,10 +223,10 @@ __device__ __forceinline__ bool epilogue_item(const EgArgs &g, uint32_t tmem, in
     const int cnt = g.offsets[td.x + 1] - g.offsets[td.x];
     const int n_valid = min(BN, cnt - td.y * BN);
     const int pair0 = g.offsets[td.x] + td.y * BN;
-    const int row_in_e = mt * BM + erow;
+    const int row_in_e = mt * g.mstep + erow;
     const size_t grow = (size_t)td.x * g.R + row_in_e;
     const float rs0 = pow2_e8m0(g.ma[grow]);
-    const float rs1 = DUAL ? pow2_e8m0(g.mb[grow]) : 0.f;
+    const float rs1 = GE::NM == 2 ? pow2_e8m0(g.mb[grow + g.mrow]) : 0.f;
     const int b = local % GE::SETS;
     if (!mbar_wait(&tfull[b], (uint32_t)(local / GE::SETS) & 1u, g.err, 606)) return false;
     tc::fence_after();
@@ -229,7 +238,7 @@ __device__ __forceinline__ bool epilogue_item(const EgArgs &g, uint32_t tmem, in
         float pf = 0.f;      // W1/W3: 2^(token exponent); W2: routing weight
         int pt = 0;          // W2: token
         if (lv) {
-            if (DUAL) {
+            if (IS13) {
                 const int ex = *reinterpret_cast<const int *>(g.zp + (size_t)pl * (g.L + kZPad) + g.L);
                 pf = __uint_as_float((uint32_t)(127 + ex) << 23);
             } else {
@@ -243,14 +252,19 @@ __device__ __forceinline__ bool epilogue_item(const EgArgs &g, uint32_t tmem, in
 #pragma unroll
         for (int j = 0; j < 16; j++) {
             const float fj = __shfl_sync(0xffffffffu, pf, j);
-            const int tj = DUAL ? 0 : __shfl_sync(0xffffffffu, pt, j);
+            const int tj = IS13 ? 0 : __shfl_sync(0xffffffffu, pt, j);
             if (c0 + j < n_valid) {
                 const int p = pair0 + c0 + j;
-                if (DUAL)
+                if (IS13) {
                     g.h16[(size_t)p * g.I + row_in_e] =
                         __float2half_rn(situ_hw(v0[j] * rs0 * fj, v1[j] * rs1 * fj, g.b1, g.b2, g.ib1, g.ib2));
-                else
+                } else if (MODE == kW2) {
                     atomicAdd(&g.acc[(size_t)tj * g.L + row_in_e], fj * ((v0[j] + v1[j]) * rs0));
+                } else {
+                    float *ar = g.acc + (size_t)tj * g.L + row_in_e;
+                    atomicAdd(ar, fj * (v0[j] * rs0));
+                    atomicAdd(ar + g.mrow, fj * (v1[j] * rs1));
+                }
             }
         }
     }
@@ -260,12 +274,13 @@ __device__ __forceinline__ bool epilogue_item(const EgArgs &g, uint32_t tmem, in
     return true;
 }
 
-template <bool DUAL, int BN>
+template <int MODE, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     k_expert_gemm(const __grid_constant__ CUtensorMap ra, const __grid_constant__ CUtensorMap rb,
                   const __grid_constant__ CUtensorMap bx, EgArgs g)
 {
-    using GE = Geo<DUAL, BN>;
+    using GE = Geo<MODE, BN>;
+    constexpr bool DUAL = GE::NM == 2;   // two weight tiles per k-stage, one per issuer
     extern __shared__ unsigned char raw_smem[];
     unsigned char *sm = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(raw_smem) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -315,7 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
                 const int tile = item / g.MT, mt = item - tile * g.MT;
                 const int2 td = g.tiles[tile];
-                const int row0 = td.x * g.R + mt * BM;          // row in the [E*R, K/2] view
+                const int row0 = td.x * g.R + mt * g.mstep;     // row in the [E*R, K/2] view
                 const int pair0 = g.offsets[td.x] + td.y * BN;
                 const int cnt = g.offsets[td.x + 1] - g.offsets[td.x];
                 const int nb = (min(BN, cnt - td.y * BN) + kBoxRows - 1) / kBoxRows;   // 16-row boxes
@@ -333,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             tc::tma_load_2d(st + u * kBSub + b * kBoxRows * 128, &bx, kt * BK + u * 64,
                                             pair0 + b * kBoxRows, &full[s]);
                     tc::tma_load_2d(st + kBBytes, &ra, kt * kRawRow, row0, &full[s]);
-                    if (DUAL) tc::tma_load_2d(st + kBBytes + kRawBytes, &rb, kt * kRawRow, row0, &full[s]);
+                    if (DUAL) tc::tma_load_2d(st + kBBytes + kRawBytes, &rb, kt * kRawRow, row0 + g.mrow, &full[s]);
                 }
             }
             // copies still in flight land before the CTA exits (each stage holds at
@@ -417,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // next item.
         for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, local++) {
             const int tile = item / g.MT, mt = item - tile * g.MT;
-            const size_t grow = (size_t)g.tiles[tile].x * g.R + mt * BM + row;
+            const size_t grow = (size_t)g.tiles[tile].x * g.R + mt * g.mstep + row + (m ? g.mrow : 0);
             const int smax = m == 0 ? g.ma[grow] : g.mb[grow];
             const uint8_t *sc = (m == 0 ? g.sa : g.sb) + grow * (size_t)G + grp0;
             for (int kt = 0; kt < KT; kt++, rp.next(), ap.next(), done++) {
@@ -451,20 +466,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&aready[ap.slot]);
                 if (kSets == 1 && local > 0 && kt == min(NSA, KT) - 1 &&
-                    !epilogue_item<DUAL, BN>(g, tmem, item - (int)gridDim.x, local - 1, tfull, tempty, 16 * sl, 64)) {
+                    !epilogue_item<MODE, BN>(g, tmem, item - (int)gridDim.x, local - 1, tfull, tempty, 16 * sl, 64)) {
                     ok = false;
                     break;
                 }
             }
         }
         if (kSets == 1 && ok && local > 0)
-            epilogue_item<DUAL, BN>(g, tmem, blockIdx.x + (local - 1) * (int)gridDim.x, local - 1, tfull, tempty,
+            epilogue_item<MODE, BN>(g, tmem, blockIdx.x + (local - 1) * (int)gridDim.x, local - 1, tfull, tempty,
                                     16 * sl, 64);
     } else if (kSets == 2 && warp >= kEpiWarp0) {
         // ---------------- epilogue (two accumulator sets) ----------------
         int local = 0;
         for (int item = blockIdx.x; item < n_items; item += gridDim.x, local++)
-            if (!epilogue_item<DUAL, BN>(g, tmem, item, local, tfull, tempty, 0, 16)) break;
+            if (!epilogue_item<MODE, BN>(g, tmem, item, local, tfull, tempty, 0, 16)) break;
     }
 
     tc::fence_before();
@@ -586,19 +601,21 @@ size_t expert_gemm_max_tiles(const k3moe_config &c)
 
 int expert_gemm_min_pairs() { return kMinPairs; }
 
-template <bool DUAL, int BN>
+template <int MODE, int BN>
 cudaError_t set_smem()
 {
-    return cudaFuncSetAttribute(k_expert_gemm<DUAL, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)Geo<DUAL, BN>::SMEM);
+    return cudaFuncSetAttribute(k_expert_gemm<MODE, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)Geo<MODE, BN>::SMEM);
 }
 
 cudaError_t init_expert_gemm()
 {
-    cudaError_t e = set_smem<true, 64>();
-    if (e == cudaSuccess) e = set_smem<false, 64>();
-    if (e == cudaSuccess) e = set_smem<true, 128>();
-    if (e == cudaSuccess) e = set_smem<false, 128>();
+    cudaError_t e = set_smem<kW13, 64>();
+    if (e == cudaSuccess) e = set_smem<kW2, 64>();
+    if (e == cudaSuccess) e = set_smem<kW2Pair, 64>();
+    if (e == cudaSuccess) e = set_smem<kW13, 128>();
+    if (e == cudaSuccess) e = set_smem<kW2, 128>();
+    if (e == cudaSuccess) e = set_smem<kW2Pair, 128>();
     return e;
 }
 
@@ -650,7 +667,11 @@ cudaError_t launch_expert_gemm(const k3moe &h, const LayerDev &w, int T, int bn,
     g.err = h.ws.err;
     g.K = w13 ? c.latent : c.moe_inter;
     g.R = w13 ? c.moe_inter : c.latent;
-    g.MT = g.R / BM;
+    // W2 takes two adjacent m-tiles per item when its rows allow it
+    const int mode = w13 ? kW13 : (c.latent % (2 * BM) == 0 ? kW2Pair : kW2);
+    g.mstep = mode == kW2Pair ? 2 * BM : BM;
+    g.mrow = mode == kW2Pair ? BM : 0;
+    g.MT = g.R / g.mstep;
     CUtensorMap ra, rb, bx;
     bool ok;
     const uint64_t rows = (uint64_t)c.n_experts * g.R;
@@ -663,18 +684,18 @@ cudaError_t launch_expert_gemm(const k3moe &h, const LayerDev &w, int T, int bn,
              make_map_u8(&rb, w.w3p, rows, g.K / 2, kRawRow, BM) &&
              make_map_f16_sw128(&bx, h.ws.zperm, pairs, c.latent, c.latent + kZPad, kBoxRows);
     } else {
-        g.sa = w.w2s;
-        g.ma = w.w2max;
+        g.sa = g.sb = w.w2s;
+        g.ma = g.mb = w.w2max;
         ok = make_map_u8(&ra, w.w2p, rows, g.K / 2, kRawRow, BM) &&
              make_map_f16_sw128(&bx, h.ws.h16, pairs, c.moe_inter, c.moe_inter, kBoxRows);
         rb = ra;
     }
     if (!ok) return cudaErrorInvalidValue;
+#define K3_EG_LAUNCH(M, N) launch_pdl(k_expert_gemm<M, N>, h.sm_count, kThreads, Geo<M, N>::SMEM, s, ra, rb, bx, g)
     if (bn == 128)
-        return w13 ? launch_pdl(k_expert_gemm<true, 128>, h.sm_count, kThreads, Geo<true, 128>::SMEM, s, ra, rb, bx, g)
-                   : launch_pdl(k_expert_gemm<false, 128>, h.sm_count, kThreads, Geo<false, 128>::SMEM, s, ra, rb, bx, g);
-    return w13 ? launch_pdl(k_expert_gemm<true, 64>, h.sm_count, kThreads, Geo<true, 64>::SMEM, s, ra, rb, bx, g)
-               : launch_pdl(k_expert_gemm<false, 64>, h.sm_count, kThreads, Geo<false, 64>::SMEM, s, ra, rb, bx, g);
+        return mode == kW13 ? K3_EG_LAUNCH(kW13, 128) : (mode == kW2 ? K3_EG_LAUNCH(kW2, 128) : K3_EG_LAUNCH(kW2Pair, 128));
+    return mode == kW13 ? K3_EG_LAUNCH(kW13, 64) : (mode == kW2 ? K3_EG_LAUNCH(kW2, 64) : K3_EG_LAUNCH(kW2Pair, 64));
+#undef K3_EG_LAUNCH
 }
 
 cudaError_t launch_row_scale_max(const uint8_t *s, size_t rows, int G, uint8_t *out)
