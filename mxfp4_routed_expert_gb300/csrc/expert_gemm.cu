@@ -10,11 +10,12 @@
 // Work: the pairs of expert e (contiguous in permutation order) are cut into
 // n-tiles of at most 64; a work item is (n-tile, 128-row m-tile of the
 // matrix). Weight rows are the MMA's M, pairs its N. Per 128-column k-stage:
-//   - one thread issues TMA for the packed weight tile (128 rows x 64 bytes
-//     per matrix, 64-byte swizzle) and the item's pair-ordered fp16
-//     activation rows (the gathered latent z for W1/W3, the h rows for W2; two
-//     64-column halves in the 128-byte swizzled K-major layout, 16-row boxes)
-//     into a deep shared-memory ring;
+//   - one thread issues TMA for the packed weight tiles (128 rows x 64 bytes
+//     per matrix, 64-byte swizzle) into a deep ring that the converters
+//     release as soon as they have read a stage, and another for the item's
+//     pair-ordered fp16 activation rows (the gathered latent z for W1/W3, the
+//     h rows for W2; two 64-column halves in the 128-byte swizzled K-major
+//     layout, 16-row boxes) into a ring that the MMAs release;
 //   - sixteen converter warps (four per TMEM lane quadrant) widen the nibbles
 //     with cvt.rn.f16x2.e2m1x2 and multiply each 32-column group by
 //     2^(s - smax_row), smax_row being the row's largest scale byte: every
@@ -30,9 +31,10 @@
 //     the two halves of every k-stage, summed in the epilogue. With 64-pair
 //     n-tiles two accumulator sets let the next item's MMAs overlap this
 //     item's epilogue; the rest of TMEM holds the A ring. An A slot is reused
-//     once the TMA stage of the k-stage that last held it is released, which
-//     both issuers' commits signal;
-//   - four epilogue warps read TMEM, multiply by 2^(smax_row - 127) and the
+//     once the activation stage of the k-stage that last held it is
+//     released, which both issuers' commits signal;
+//   - the epilogue (four dedicated warps with two accumulator sets, else the
+//     converter warps between items) reads TMEM, multiply by 2^(smax_row - 127) and the
 //     token's activation exponent, then apply SiTU (hardware tanh) and store
 //     h (W1/W3), or
 //     scale by the pair's routing weight and scatter-add into the token's fp32
@@ -49,7 +51,7 @@ namespace {
 
 constexpr int BM = 128, BK = 128;
 constexpr int kMinPairs = 128;                      // smallest batch (token, expert pairs) run here
-// warp roles: 0 TMA producer, 1 and 2 MMA issuers, 3 idle, 4..19 converters,
+// warp roles: 0 weight TMA producer, 1 and 2 MMA issuers, 3 activation TMA producer, 4..19 converters,
 // 20..23 epilogue (warp % 4 = its TMEM lane quadrant)
 constexpr int kConvWarp0 = 4, kConvWarps = 16;
 constexpr int kEpiWarp0 = 20, kEpiWarps = 4;
@@ -68,7 +70,10 @@ enum : int { kW13 = 0, kW2 = 1, kW2Pair = 2 };
 // Launch geometry for a mode with n-tiles of BN pairs. TMEM holds
 // SETS accumulator sets of two BN-column accumulators (two sets for BN = 64,
 // so that the epilogue overlaps the next item; one for BN = 128), then the
-// ring of converted A slots in the remaining 256 columns.
+// ring of converted A slots in the remaining 256 columns. Shared memory holds
+// two TMA rings: activation tiles (NB stages, released by the MMAs) and packed
+// weight tiles (NR stages, released by the converters as soon as they have
+// read them, so that weight loads run far ahead of the tensor cores).
 template <int MODE, int BN>
 struct Geo {
     static_assert(BN == 64 || BN == 128, "n-tile of 64 or 128 pairs");
@@ -77,28 +82,29 @@ struct Geo {
     static constexpr uint32_t SET_COLS = 2 * BN;
     static constexpr uint32_t ARING0 = SETS * SET_COLS;     // 256
     static constexpr int ACOLS = NM * BK / 2;                // TMEM columns per A slot
-    static constexpr int NSA_TMEM = (int)(kTmemCols - ARING0) / ACOLS;
+    static constexpr int NSA = (int)(kTmemCols - ARING0) / ACOLS;
     static constexpr int BSUB = BN * 128;                    // one 64-column half of the activation tile
-    static constexpr int BBYTES = 2 * BSUB;
-    static constexpr int R_STAGE = BBYTES + NM * kRawBytes;  // [B half 0 | B half 1 | packed W per matrix]
-    static constexpr size_t smem(int ns)
+    static constexpr int BBYTES = 2 * BSUB;                  // one activation stage [half 0 | half 1]
+    static constexpr int RBYTES = NM * kRawBytes;            // one weight stage [packed W per matrix]
+    static constexpr size_t smem(int nb, int nr)
     {
-        return (size_t)ns * R_STAGE + (size_t)(2 * ns + NSA_TMEM + 2 * SETS) * 8 + 16 + 1024;
+        return (size_t)nb * BBYTES + (size_t)nr * RBYTES + (size_t)(2 * nb + 2 * nr + NSA + 2 * SETS) * 8 + 16 +
+               1024;
     }
-    static constexpr int ring()                              // TMA ring depth (at most 12)
+    // activation stages: deep enough to cover an L2 fetch under load (about
+    // 2k cycles for a 32 KB stage) at the tensor-bound stage time
+    static constexpr int NB = BBYTES >= 32768 ? 5 : 6;
+    static constexpr int ring()                              // weight stages: what is left, at most 16
     {
-        int ns = 2;
-        while (ns < 12 && smem(ns + 1) <= (size_t)kSmemBudget - 1024) ns++;
-        return ns;
+        int nr = 2;
+        while (nr < 16 && smem(NB, nr + 1) <= (size_t)kSmemBudget) nr++;
+        return nr;
     }
-    static constexpr int NSR = ring();
-    // A slots: what TMEM holds, but leaving at least three TMA stages of
-    // prefetch beyond the converted ones (a TMA stage is refilled only after
-    // the MMAs of the stage it held), and at least two
-    static constexpr int NSA = NSA_TMEM < NSR - 3 ? NSA_TMEM : (NSR - 3 > 2 ? NSR - 3 : 2);
-    static constexpr size_t SMEM = smem(NSR);
+    static constexpr int NR = ring();
+    static constexpr size_t SMEM = smem(NB, NR);
     static_assert(ARING0 == 256, "accumulators take half of TMEM");
-    static_assert(NSR > NSA, "A slots are released through the TMA ring");
+    static_assert(NB >= NSA, "A slots are released through the activation ring");
+    static_assert(SMEM <= (size_t)kSmemBudget && NR >= 4, "shared memory");
 };
 
 // Position in a ring of N slots: slot index and the parity of its current use.
@@ -206,15 +212,17 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t *v)
 
 // Epilogue of one item: the calling warp reads its TMEM lane quadrant
 // (rows 32 (warp % 4) .. + 31 of the tile) for the pair columns c_first,
-// c_first + c_step, ... (16 at a time), applies the row and token factors and
+// c_first + CSTEP, ... (16 at a time), applies the row and token factors and
 // SiTU (W1/W3) or the weighted scatter-add (W2), then releases the
-// accumulator set.
-template <int MODE, int BN>
+// accumulator set. The per-pair factors are fetched before the wait for the
+// accumulators, so their latency overlaps the item's last MMAs.
+template <int MODE, int BN, int CSTEP>
 __device__ __forceinline__ bool epilogue_item(const EgArgs &g, uint32_t tmem, int item, int local,
-                                              uint64_t *tfull, uint64_t *tempty, int c_first, int c_step)
+                                              uint64_t *tfull, uint64_t *tempty, int c_first)
 {
     using GE = Geo<MODE, BN>;
     constexpr bool IS13 = MODE == kW13;
+    constexpr int NCH = BN / CSTEP;         // chunks of 16 columns per warp (upper bound)
     const int lane = threadIdx.x & 31;
     const int q = (threadIdx.x >> 5) & 3;   // TMEM lanes 32q..32q+31
     const int erow = q * 32 + lane;         // weight row of the tile
@@ -227,32 +235,40 @@ __device__ __forceinline__ bool epilogue_item(const EgArgs &g, uint32_t tmem, in
     const size_t grow = (size_t)td.x * g.R + row_in_e;
     const float rs0 = pow2_e8m0(g.ma[grow]);
     const float rs1 = GE::NM == 2 ? pow2_e8m0(g.mb[grow + g.mrow]) : 0.f;
+    // per-pair factors for the columns of each chunk, one lane each (lanes 16..31 repeat 0..15)
+    float pf[NCH];       // W1/W3: 2^(token exponent); W2: routing weight
+    int pt[NCH];         // W2: token
+#pragma unroll
+    for (int ci = 0; ci < NCH; ci++) {
+        const int c = c_first + ci * CSTEP + (lane & 15);
+        pf[ci] = 0.f;
+        pt[ci] = 0;
+        if (c < n_valid) {
+            const int pl = pair0 + c;
+            if (IS13) {
+                const int ex = *reinterpret_cast<const int *>(g.zp + (size_t)pl * (g.L + kZPad) + g.L);
+                pf[ci] = __uint_as_float((uint32_t)(127 + ex) << 23);
+            } else {
+                pf[ci] = g.pair_w[pl];
+                pt[ci] = g.perm[pl] / g.k;
+            }
+        }
+    }
     const int b = local % GE::SETS;
     if (!mbar_wait(&tfull[b], (uint32_t)(local / GE::SETS) & 1u, g.err, 606)) return false;
     tc::fence_after();
     const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)b * GE::SET_COLS;
-    for (int c0 = c_first; c0 < n_valid; c0 += c_step) {
-        // per-pair factors for columns c0..c0+15, one lane each, then broadcast
-        const int pl = pair0 + c0 + (lane & 15);
-        const bool lv = c0 + (lane & 15) < n_valid;
-        float pf = 0.f;      // W1/W3: 2^(token exponent); W2: routing weight
-        int pt = 0;          // W2: token
-        if (lv) {
-            if (IS13) {
-                const int ex = *reinterpret_cast<const int *>(g.zp + (size_t)pl * (g.L + kZPad) + g.L);
-                pf = __uint_as_float((uint32_t)(127 + ex) << 23);
-            } else {
-                pf = g.pair_w[pl];
-                pt = g.perm[pl] / g.k;
-            }
-        }
+#pragma unroll
+    for (int ci = 0; ci < NCH; ci++) {
+        const int c0 = c_first + ci * CSTEP;
+        if (c0 >= n_valid) break;
         float v0[16], v1[16];
         tc::tmem_ld16(tb + (uint32_t)c0, v0);
         tc::tmem_ld16(tb + (uint32_t)(BN + c0), v1);
 #pragma unroll
         for (int j = 0; j < 16; j++) {
-            const float fj = __shfl_sync(0xffffffffu, pf, j);
-            const int tj = IS13 ? 0 : __shfl_sync(0xffffffffu, pt, j);
+            const float fj = __shfl_sync(0xffffffffu, pf[ci], j);
+            const int tj = IS13 ? 0 : __shfl_sync(0xffffffffu, pt[ci], j);
             if (c0 + j < n_valid) {
                 const int p = pair0 + c0 + j;
                 if (IS13) {
@@ -277,29 +293,36 @@ __device__ __forceinline__ bool epilogue_item(const EgArgs &g, uint32_t tmem, in
 template <int MODE, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     k_expert_gemm(const __grid_constant__ CUtensorMap ra, const __grid_constant__ CUtensorMap rb,
-                  const __grid_constant__ CUtensorMap bx, EgArgs g)
+                  const __grid_constant__ CUtensorMap bx, const __grid_constant__ CUtensorMap bxf, EgArgs g)
 {
     using GE = Geo<MODE, BN>;
     constexpr bool DUAL = GE::NM == 2;   // two weight tiles per k-stage, one per issuer
     extern __shared__ unsigned char raw_smem[];
     unsigned char *sm = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(raw_smem) + 1023) & ~static_cast<uintptr_t>(1023));
-    constexpr int NM = GE::NM, R_STAGE = GE::R_STAGE, NSR = GE::NSR, NSA = GE::NSA, ACOLS = GE::ACOLS;
-    constexpr int kSets = GE::SETS, kBSub = GE::BSUB, kBBytes = GE::BBYTES;
+    constexpr int NB = GE::NB, NR = GE::NR, NSA = GE::NSA, ACOLS = GE::ACOLS;
+    constexpr int kSets = GE::SETS, kBSub = GE::BSUB, kBBytes = GE::BBYTES, kRBytes = GE::RBYTES;
     constexpr uint32_t kSetCols = GE::SET_COLS, kARing0 = GE::ARING0;
-    unsigned char *rring = sm;
-    uint64_t *full = reinterpret_cast<uint64_t *>(rring + NSR * R_STAGE);   // TMA landed
-    uint64_t *rfree = full + NSR;                            // both issuers' MMAs on the stage done
-    uint64_t *aready = rfree + NSR;                          // [NSA] A slot written
-    uint64_t *tfull = aready + NSA;                          // [kSets] accumulator set complete
-    uint64_t *tempty = tfull + kSets;                        // [kSets] epilogue drained it
+    unsigned char *bring = sm;                                // [NB] activation stages
+    unsigned char *wring = sm + NB * kBBytes;                 // [NR] packed weight stages
+    uint64_t *bfull = reinterpret_cast<uint64_t *>(wring + NR * kRBytes);   // activation tile landed
+    uint64_t *bfree = bfull + NB;                             // both issuers' MMAs on the stage done
+    uint64_t *wfull = bfree + NB;                             // weight tile landed
+    uint64_t *wfree = wfull + NR;                             // converters have read it
+    uint64_t *aready = wfree + NR;                            // [NSA] A slot written
+    uint64_t *tfull = aready + NSA;                           // [kSets] accumulator set complete
+    uint64_t *tempty = tfull + kSets;                         // [kSets] epilogue drained it
     uint32_t *tslot = reinterpret_cast<uint32_t *>(tempty + kSets);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < NSR; i++) {
-            mbar_init(&full[i], 1);
-            mbar_init(&rfree[i], 2);
+        for (int i = 0; i < NB; i++) {
+            mbar_init(&bfull[i], 1);
+            mbar_init(&bfree[i], 2);
+        }
+        for (int i = 0; i < NR; i++) {
+            mbar_init(&wfull[i], 1);
+            mbar_init(&wfree[i], kConvWarps);
         }
         for (int i = 0; i < NSA; i++) mbar_init(&aready[i], kConvWarps);
         for (int i = 0; i < kSets; i++) {
@@ -310,6 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::prefetch_map(&ra);
         if (DUAL) tc::prefetch_map(&rb);
         tc::prefetch_map(&bx);
+        tc::prefetch_map(&bxf);
     }
     if (warp == 1) tc::tmem_alloc(tslot, kTmemCols);
     tc::fence_before();
@@ -321,11 +345,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n_items = *g.n_tiles * g.MT;
     const int KT = g.K / BK;
 
-    if (warp == 0) {
-        // ---------------- TMA producer ----------------
+    if (warp == 0 || warp == 3) {
+        // ---------------- TMA producers: weights (warp 0), activations (warp 3) ----------------
+        // Each ring's stages are refilled in k-stage order once their consumers
+        // release them; before exiting, a producer waits for its own copies
+        // still in flight (a stage holds at most one unconsumed fill).
         if (lane == 0) {
-            int it = 0;
-            RingPos<NSR> rp;
+            const bool wts = warp == 0;
+            const int depth = wts ? NR : NB;
+            uint64_t *fullb = wts ? wfull : bfull;
+            uint64_t *freeb = wts ? wfree : bfree;
+            int it = 0, slot = 0;
+            uint32_t phase = 0;
             bool ok = true;
             for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
                 const int tile = item / g.MT, mt = item - tile * g.MT;
@@ -334,40 +365,55 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int pair0 = g.offsets[td.x] + td.y * BN;
                 const int cnt = g.offsets[td.x + 1] - g.offsets[td.x];
                 const int nb = (min(BN, cnt - td.y * BN) + kBoxRows - 1) / kBoxRows;   // 16-row boxes
-                const uint32_t tx = (uint32_t)(2 * nb * kBoxRows * 128 + NM * kRawBytes);
-                for (int kt = 0; kt < KT; kt++, it++, rp.next()) {
-                    const int s = rp.slot;
-                    if (!mbar_wait(&rfree[s], rp.phase ^ 1u, g.err, 600)) {
+                // a tile more than half full takes each 64-column half in one
+                // BN-row box (rows past its pairs are never read by the MMA),
+                // since a thread issues a TMA copy only every ~100 cycles
+                const bool whole = nb * kBoxRows > BN / 2;
+                const uint32_t tx = wts ? (uint32_t)kRBytes : (uint32_t)(2 * (whole ? BN : nb * kBoxRows) * 128);
+                for (int kt = 0; kt < KT; kt++, it++) {
+                    if (!mbar_wait(&freeb[slot], phase ^ 1u, g.err, wts ? 600 : 608)) {
                         ok = false;
                         break;
                     }
-                    unsigned char *st = rring + s * R_STAGE;
-                    mbar_expect_tx(&full[s], tx);
-                    for (int u = 0; u < 2; u++)
-                        for (int b = 0; b < nb; b++)
-                            tc::tma_load_2d(st + u * kBSub + b * kBoxRows * 128, &bx, kt * BK + u * 64,
-                                            pair0 + b * kBoxRows, &full[s]);
-                    tc::tma_load_2d(st + kBBytes, &ra, kt * kRawRow, row0, &full[s]);
-                    if (DUAL) tc::tma_load_2d(st + kBBytes + kRawBytes, &rb, kt * kRawRow, row0 + g.mrow, &full[s]);
+                    mbar_expect_tx(&fullb[slot], tx);
+                    if (wts) {
+                        unsigned char *st = wring + slot * kRBytes;
+                        tc::tma_load_2d(st, &ra, kt * kRawRow, row0, &fullb[slot]);
+                        if (DUAL) tc::tma_load_2d(st + kRawBytes, &rb, kt * kRawRow, row0 + g.mrow, &fullb[slot]);
+                    } else {
+                        unsigned char *st = bring + slot * kBBytes;
+                        for (int u = 0; u < 2; u++) {
+                            if (whole) {
+                                tc::tma_load_2d(st + u * kBSub, &bxf, kt * BK + u * 64, pair0, &fullb[slot]);
+                                continue;
+                            }
+                            for (int bx_ = 0; bx_ < nb; bx_++)
+                                tc::tma_load_2d(st + u * kBSub + bx_ * kBoxRows * 128, &bx, kt * BK + u * 64,
+                                                pair0 + bx_ * kBoxRows, &fullb[slot]);
+                        }
+                    }
+                    if (++slot == depth) {
+                        slot = 0;
+                        phase ^= 1u;
+                    }
                 }
             }
-            // copies still in flight land before the CTA exits (each stage holds at
-            // most one unconsumed fill: a refill waits for the previous one's MMAs)
-            for (int j = 1; j <= NSR && j <= it; j++) {
+            for (int j = 1; j <= depth && j <= it; j++) {
                 const int u = it - j;
-                mbar_wait(&full[u % NSR], (uint32_t)(u / NSR) & 1u, g.err, 605);
+                mbar_wait(&fullb[u % depth], (uint32_t)(u / depth) & 1u, g.err, 605);
             }
         }
     } else if (warp == 1 || warp == 2) {
         // ---------------- MMA issuers ----------------
-        // W1/W3: issuer q multiplies matrix q; W2: issuer q takes the k-steps
-        // 4q..4q+3 of every k-stage. Each writes accumulator q of the set.
+        // W1/W3 and paired W2: issuer q multiplies weight tile q; plain W2:
+        // issuer q takes the k-steps 4q..4q+3 of every k-stage. Each writes
+        // accumulator q of the set.
         const int q = warp - 1;
         if (lane == 0) {
             int local = 0;
-            RingPos<NSR> rp;
+            RingPos<NB> bp;
             RingPos<NSA> ap;
-            const uint64_t db0 = tc::desc_sw128(tc::su32(rring));
+            const uint64_t db0 = tc::desc_sw128(tc::su32(bring));
             const int kk0 = DUAL ? 0 : 4 * q;            // first k-step (of 16 columns)
             constexpr int NK = DUAL ? BK / 16 : BK / 32; // k-steps per k-stage for this issuer
             bool ok = true;
@@ -382,17 +428,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!mbar_wait(&tempty[b], ((uint32_t)(local / kSets) & 1u) ^ 1u, g.err, 601)) break;
                 tc::fence_after();
                 const uint32_t d = tmem + (uint32_t)b * kSetCols + (uint32_t)q * BN;
-                for (int kt = 0; kt < KT; kt++, rp.next(), ap.next()) {
-                    // The converters arrive on aready only after their wait on the
-                    // TMA barrier of this stage, so aready also orders the
-                    // activation tile's arrival before these MMAs.
-                    if (!mbar_wait(&aready[ap.slot], ap.phase, g.err, 603)) {
+                for (int kt = 0; kt < KT; kt++, bp.next(), ap.next()) {
+                    if (!mbar_wait(&aready[ap.slot], ap.phase, g.err, 603) ||
+                        !mbar_wait(&bfull[bp.slot], bp.phase, g.err, 609)) {
                         ok = false;
                         break;
                     }
                     tc::fence_after();
                     const uint32_t a0 = tmem + kARing0 + (uint32_t)(ap.slot * ACOLS) + (DUAL ? (uint32_t)q * (BK / 2) : 0u);
-                    const uint64_t db = db0 + (uint64_t)((rp.slot * R_STAGE) >> 4);
+                    const uint64_t db = db0 + (uint64_t)((bp.slot * kBBytes) >> 4);
 #pragma unroll
                     for (int i = 0; i < NK; i++) {
                         const int kk = kk0 + i;
@@ -400,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint64_t bd = db + (uint64_t)(((kk >> 2) * kBSub + (kk & 3) * 32) >> 4);
                         mma_ts(d, a0 + 8 * (uint32_t)kk, bd, idesc, (kt > 0 || i > 0) ? 1u : 0u);
                     }
-                    tc::commit(&rfree[rp.slot]);
+                    tc::commit(&bfree[bp.slot]);
                 }
                 if (ok) tc::commit(&tfull[b]);
             }
@@ -410,76 +454,79 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int qd = warp & 3;                      // TMEM lane quadrant
         const int row = qd * 32 + lane;               // weight row of the tile (its TMEM lane)
         const int sl = (warp - kConvWarp0) >> 2;      // 0..3: this warp's share of the k-stage
-        // W1/W3: matrix sl >> 1, 64 columns (two scale groups) from 64 * (sl & 1);
-        // W2: 32 columns (one scale group) from 32 * sl
+        // two weight tiles: tile sl >> 1, 64 columns (two scale groups) from 64 * (sl & 1);
+        // plain W2: 32 columns (one scale group) from 32 * sl
         const int m = DUAL ? (sl >> 1) : 0;
         const int grp0 = DUAL ? 2 * (sl & 1) : sl;    // first scale group within the k-stage
         constexpr int NGRP = DUAL ? 2 : 1;
         const uint32_t tlane = (uint32_t)(qd * 32) << 16;
         const int G = g.K / kGroup;
         const int swz = (row >> 1) & 3;              // 64-byte swizzle of the packed tile
-        RingPos<NSR> rp;          // TMA stage of this k-stage
-        RingPos<NSR> rq;          // TMA stage of the k-stage NSA back (its MMAs free the slot)
+        RingPos<NR> wp;           // weight stage of this k-stage
+        RingPos<NB> rq;           // activation stage of the k-stage NSA back (its MMAs free the A slot)
         RingPos<NSA> ap;
         int done = 0;             // k-stages converted so far
         int local = 0;            // items of this CTA so far
         bool ok = true;
         // With one accumulator set the issuers stop between items until the
-        // accumulators are drained, and the converters, whose A slots free up
-        // only when the next item's MMAs run, would idle: so they run the
-        // epilogue themselves (each warp a quarter of the pair columns of its
-        // lane quadrant) right after converting the first NSA k-stages of the
-        // next item.
+        // accumulators are drained, so the converters run the epilogue
+        // themselves (each warp a quarter of the pair columns of its lane
+        // quadrant) right after converting the next item's first k-stage,
+        // whose A slot frees up before the previous item's last MMAs end.
         for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, local++) {
             const int tile = item / g.MT, mt = item - tile * g.MT;
             const size_t grow = (size_t)g.tiles[tile].x * g.R + mt * g.mstep + row + (m ? g.mrow : 0);
             const int smax = m == 0 ? g.ma[grow] : g.mb[grow];
             const uint8_t *sc = (m == 0 ? g.sa : g.sb) + grow * (size_t)G + grp0;
-            for (int kt = 0; kt < KT; kt++, rp.next(), ap.next(), done++) {
+            for (int kt = 0; kt < KT; kt++, wp.next(), ap.next(), done++) {
                 int sv[NGRP];
 #pragma unroll
                 for (int i = 0; i < NGRP; i++) sv[i] = sc[4 * kt + i];
-                if (!mbar_wait(&full[rp.slot], rp.phase, g.err, 604)) {
+                if (!mbar_wait(&wfull[wp.slot], wp.phase, g.err, 604)) {
                     ok = false;
                     break;
                 }
                 if (done >= NSA) {
-                    if (!mbar_wait(&rfree[rq.slot], rq.phase, g.err, 607)) {
+                    if (!mbar_wait(&bfree[rq.slot], rq.phase, g.err, 607)) {
                         ok = false;
                         break;
                     }
                     rq.next();
                 }
                 tc::fence_after();
-                const unsigned char *rawp = rring + rp.slot * R_STAGE + kBBytes + m * kRawBytes + row * kRawRow;
+                const unsigned char *rawp = wring + wp.slot * kRBytes + m * kRawBytes + row * kRawRow;
                 const uint32_t acol = kARing0 + (uint32_t)(ap.slot * ACOLS) + (uint32_t)(m * (BK / 2));
+                uint4 w[NGRP];
+#pragma unroll
+                for (int i = 0; i < NGRP; i++)   // 16-byte chunk = scale group of the row
+                    w[i] = *reinterpret_cast<const uint4 *>(rawp + (((grp0 + i) ^ swz) << 4));
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&wfree[wp.slot]);
 #pragma unroll
                 for (int i = 0; i < NGRP; i++) {
-                    const int c = grp0 + i;                   // 16-byte chunk = scale group of the row
-                    const uint4 w = *reinterpret_cast<const uint4 *>(rawp + ((c ^ swz) << 4));
                     uint32_t v[16];
-                    widen_group(w, f16x2_pow2(sv[i] - smax), v);
-                    tmem_st16(tmem + tlane + acol + (uint32_t)(16 * c), v);
+                    widen_group(w[i], f16x2_pow2(sv[i] - smax), v);
+                    tmem_st16(tmem + tlane + acol + (uint32_t)(16 * (grp0 + i)), v);
                 }
                 asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
                 tc::fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&aready[ap.slot]);
-                if (kSets == 1 && local > 0 && kt == min(NSA, KT) - 1 &&
-                    !epilogue_item<MODE, BN>(g, tmem, item - (int)gridDim.x, local - 1, tfull, tempty, 16 * sl, 64)) {
+                if (kSets == 1 && local > 0 && kt == 0 &&
+                    !epilogue_item<MODE, BN, 64>(g, tmem, item - (int)gridDim.x, local - 1, tfull, tempty, 16 * sl)) {
                     ok = false;
                     break;
                 }
             }
         }
         if (kSets == 1 && ok && local > 0)
-            epilogue_item<MODE, BN>(g, tmem, blockIdx.x + (local - 1) * (int)gridDim.x, local - 1, tfull, tempty,
-                                    16 * sl, 64);
+            epilogue_item<MODE, BN, 64>(g, tmem, blockIdx.x + (local - 1) * (int)gridDim.x, local - 1, tfull, tempty,
+                                        16 * sl);
     } else if (kSets == 2 && warp >= kEpiWarp0) {
         // ---------------- epilogue (two accumulator sets) ----------------
         int local = 0;
         for (int item = blockIdx.x; item < n_items; item += gridDim.x, local++)
-            if (!epilogue_item<MODE, BN>(g, tmem, item, local, tfull, tempty, 0, 16)) break;
+            if (!epilogue_item<MODE, BN, 16>(g, tmem, item, local, tfull, tempty, 0)) break;
     }
 
     tc::fence_before();
@@ -672,7 +719,7 @@ cudaError_t launch_expert_gemm(const k3moe &h, const LayerDev &w, int T, int bn,
     g.mstep = mode == kW2Pair ? 2 * BM : BM;
     g.mrow = mode == kW2Pair ? BM : 0;
     g.MT = g.R / g.mstep;
-    CUtensorMap ra, rb, bx;
+    CUtensorMap ra, rb, bx, bxf;
     bool ok;
     const uint64_t rows = (uint64_t)c.n_experts * g.R;
     if (w13) {
@@ -682,16 +729,18 @@ cudaError_t launch_expert_gemm(const k3moe &h, const LayerDev &w, int T, int bn,
         g.mb = w.w3max;
         ok = make_map_u8(&ra, w.w1p, rows, g.K / 2, kRawRow, BM) &&
              make_map_u8(&rb, w.w3p, rows, g.K / 2, kRawRow, BM) &&
-             make_map_f16_sw128(&bx, h.ws.zperm, pairs, c.latent, c.latent + kZPad, kBoxRows);
+             make_map_f16_sw128(&bx, h.ws.zperm, pairs, c.latent, c.latent + kZPad, kBoxRows) &&
+             make_map_f16_sw128(&bxf, h.ws.zperm, pairs, c.latent, c.latent + kZPad, bn);
     } else {
         g.sa = g.sb = w.w2s;
         g.ma = g.mb = w.w2max;
         ok = make_map_u8(&ra, w.w2p, rows, g.K / 2, kRawRow, BM) &&
-             make_map_f16_sw128(&bx, h.ws.h16, pairs, c.moe_inter, c.moe_inter, kBoxRows);
+             make_map_f16_sw128(&bx, h.ws.h16, pairs, c.moe_inter, c.moe_inter, kBoxRows) &&
+             make_map_f16_sw128(&bxf, h.ws.h16, pairs, c.moe_inter, c.moe_inter, bn);
         rb = ra;
     }
     if (!ok) return cudaErrorInvalidValue;
-#define K3_EG_LAUNCH(M, N) launch_pdl(k_expert_gemm<M, N>, h.sm_count, kThreads, Geo<M, N>::SMEM, s, ra, rb, bx, g)
+#define K3_EG_LAUNCH(M, N) launch_pdl(k_expert_gemm<M, N>, h.sm_count, kThreads, Geo<M, N>::SMEM, s, ra, rb, bx, bxf, g)
     if (bn == 128)
         return mode == kW13 ? K3_EG_LAUNCH(kW13, 128) : (mode == kW2 ? K3_EG_LAUNCH(kW2, 128) : K3_EG_LAUNCH(kW2Pair, 128));
     return mode == kW13 ? K3_EG_LAUNCH(kW13, 64) : (mode == kW2 ? K3_EG_LAUNCH(kW2, 64) : K3_EG_LAUNCH(kW2Pair, 64));
