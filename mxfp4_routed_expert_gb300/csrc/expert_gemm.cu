@@ -190,6 +190,25 @@ __device__ __forceinline__ void widen_group(uint4 w, uint32_t f, uint32_t *o)
     }
 }
 
+// One lane of a converged warp.
+__device__ __forceinline__ bool elect_one()
+{
+    uint32_t p;
+    asm volatile("{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\tselp.u32 %0, 1, 0, e;\n\t}" : "=r"(p));
+    return p != 0;
+}
+
+// A bounded barrier wait of the MMA issuer: by the calling thread, or (WARP)
+// by lane 0 with the outcome taken by the whole warp.
+template <bool WARP>
+__device__ __forceinline__ bool issuer_wait(uint64_t *bar, uint32_t parity, int *err, int where)
+{
+    if (!WARP) return mbar_wait(bar, parity, err, where);
+    bool ok = true;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, err, where);
+    return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+}
+
 // A from tensor memory, B from shared memory.
 __device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
                                        uint32_t accumulate)
@@ -293,7 +312,8 @@ __device__ __forceinline__ bool epilogue_item(const EgArgs &g, uint32_t tmem, in
 template <int MODE, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     k_expert_gemm(const __grid_constant__ CUtensorMap ra, const __grid_constant__ CUtensorMap rb,
-                  const __grid_constant__ CUtensorMap bx, const __grid_constant__ CUtensorMap bxf, EgArgs g)
+                  const __grid_constant__ CUtensorMap bx, const __grid_constant__ CUtensorMap bxm,
+                  const __grid_constant__ CUtensorMap bxf, EgArgs g)
 {
     using GE = Geo<MODE, BN>;
     constexpr bool DUAL = GE::NM == 2;   // two weight tiles per k-stage, one per issuer
@@ -333,6 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::prefetch_map(&ra);
         if (DUAL) tc::prefetch_map(&rb);
         tc::prefetch_map(&bx);
+        tc::prefetch_map(&bxm);
         tc::prefetch_map(&bxf);
     }
     if (warp == 1) tc::tmem_alloc(tslot, kTmemCols);
@@ -364,12 +385,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int row0 = td.x * g.R + mt * g.mstep;     // row in the [E*R, K/2] view
                 const int pair0 = g.offsets[td.x] + td.y * BN;
                 const int cnt = g.offsets[td.x + 1] - g.offsets[td.x];
-                const int nb = (min(BN, cnt - td.y * BN) + kBoxRows - 1) / kBoxRows;   // 16-row boxes
-                // a tile more than half full takes each 64-column half in one
-                // BN-row box (rows past its pairs are never read by the MMA),
-                // since a thread issues a TMA copy only every ~100 cycles
-                const bool whole = nb * kBoxRows > BN / 2;
-                const uint32_t tx = wts ? (uint32_t)kRBytes : (uint32_t)(2 * (whole ? BN : nb * kBoxRows) * 128);
+                const int nv = min(BN, cnt - td.y * BN);
+                // Activation rows per 64-column half: up to 32 pairs in 16-row
+                // boxes, else one box of 64 or BN rows (rows past the tile's
+                // pairs are never read by the MMA). A thread issues a TMA copy
+                // only every ~100 cycles, so a stage takes at most four.
+                const int nb = nv <= 32 ? (nv + kBoxRows - 1) / kBoxRows : 1;
+                const int brows = nv <= 32 ? nb * kBoxRows : (nv <= 64 ? 64 : BN);
+                const CUtensorMap *bmap = nv <= 32 ? &bx : (nv <= 64 ? &bxm : &bxf);
+                const uint32_t tx = wts ? (uint32_t)kRBytes : (uint32_t)(2 * brows * 128);
                 for (int kt = 0; kt < KT; kt++, it++) {
                     if (!mbar_wait(&freeb[slot], phase ^ 1u, g.err, wts ? 600 : 608)) {
                         ok = false;
@@ -382,15 +406,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (DUAL) tc::tma_load_2d(st + kRawBytes, &rb, kt * kRawRow, row0 + g.mrow, &fullb[slot]);
                     } else {
                         unsigned char *st = bring + slot * kBBytes;
-                        for (int u = 0; u < 2; u++) {
-                            if (whole) {
-                                tc::tma_load_2d(st + u * kBSub, &bxf, kt * BK + u * 64, pair0, &fullb[slot]);
-                                continue;
-                            }
+                        for (int u = 0; u < 2; u++)
                             for (int bx_ = 0; bx_ < nb; bx_++)
-                                tc::tma_load_2d(st + u * kBSub + bx_ * kBoxRows * 128, &bx, kt * BK + u * 64,
+                                tc::tma_load_2d(st + u * kBSub + bx_ * kBoxRows * 128, bmap, kt * BK + u * 64,
                                                 pair0 + bx_ * kBoxRows, &fullb[slot]);
-                        }
                     }
                     if (++slot == depth) {
                         slot = 0;
@@ -408,8 +427,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         // W1/W3 and paired W2: issuer q multiplies weight tile q; plain W2:
         // issuer q takes the k-steps 4q..4q+3 of every k-stage. Each writes
         // accumulator q of the set.
+        // With 64-pair n-tiles (small N, where the issue rate bounds the
+        // stage) the whole warp runs the loop, so that its descriptor
+        // arithmetic is warp-uniform: lane 0 polls the barriers and one
+        // elected lane issues. With 128-pair n-tiles lane 0 alone runs it,
+        // which measured faster there.
+        constexpr bool kWarpIssue = BN == 64;
         const int q = warp - 1;
-        if (lane == 0) {
+        if (kWarpIssue || lane == 0) {
             int local = 0;
             RingPos<NB> bp;
             RingPos<NSA> ap;
@@ -425,28 +450,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t idesc =
                     (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);  // f16 x f16 -> f32
                 const int b = local % kSets;
-                if (!mbar_wait(&tempty[b], ((uint32_t)(local / kSets) & 1u) ^ 1u, g.err, 601)) break;
+                if (!issuer_wait<kWarpIssue>(&tempty[b], ((uint32_t)(local / kSets) & 1u) ^ 1u, g.err, 601)) break;
                 tc::fence_after();
                 const uint32_t d = tmem + (uint32_t)b * kSetCols + (uint32_t)q * BN;
                 for (int kt = 0; kt < KT; kt++, bp.next(), ap.next()) {
-                    if (!mbar_wait(&aready[ap.slot], ap.phase, g.err, 603) ||
-                        !mbar_wait(&bfull[bp.slot], bp.phase, g.err, 609)) {
+                    if (!issuer_wait<kWarpIssue>(&aready[ap.slot], ap.phase, g.err, 603) ||
+                        !issuer_wait<kWarpIssue>(&bfull[bp.slot], bp.phase, g.err, 609)) {
                         ok = false;
                         break;
                     }
                     tc::fence_after();
                     const uint32_t a0 = tmem + kARing0 + (uint32_t)(ap.slot * ACOLS) + (DUAL ? (uint32_t)q * (BK / 2) : 0u);
                     const uint64_t db = db0 + (uint64_t)((bp.slot * kBBytes) >> 4);
+                    if (!kWarpIssue || elect_one()) {
 #pragma unroll
-                    for (int i = 0; i < NK; i++) {
-                        const int kk = kk0 + i;
-                        // B: half kk / 4 of the activation tile, 32 bytes per k-step inside it
-                        const uint64_t bd = db + (uint64_t)(((kk >> 2) * kBSub + (kk & 3) * 32) >> 4);
-                        mma_ts(d, a0 + 8 * (uint32_t)kk, bd, idesc, (kt > 0 || i > 0) ? 1u : 0u);
+                        for (int i = 0; i < NK; i++) {
+                            const int kk = kk0 + i;
+                            // B: half kk / 4 of the activation tile, 32 bytes per k-step inside it
+                            const uint64_t bd = db + (uint64_t)(((kk >> 2) * kBSub + (kk & 3) * 32) >> 4);
+                            mma_ts(d, a0 + 8 * (uint32_t)kk, bd, idesc, (kt > 0 || i > 0) ? 1u : 0u);
+                        }
+                        tc::commit(&bfree[bp.slot]);
                     }
-                    tc::commit(&bfree[bp.slot]);
+                    if (kWarpIssue) __syncwarp();
                 }
-                if (ok) tc::commit(&tfull[b]);
+                if (ok && (!kWarpIssue || elect_one())) tc::commit(&tfull[b]);
+                if (kWarpIssue) __syncwarp();
             }
         }
     } else if (warp >= kConvWarp0 && warp < kConvWarp0 + kConvWarps) {
@@ -719,7 +748,7 @@ cudaError_t launch_expert_gemm(const k3moe &h, const LayerDev &w, int T, int bn,
     g.mstep = mode == kW2Pair ? 2 * BM : BM;
     g.mrow = mode == kW2Pair ? BM : 0;
     g.MT = g.R / g.mstep;
-    CUtensorMap ra, rb, bx, bxf;
+    CUtensorMap ra, rb, bx, bxm, bxf;
     bool ok;
     const uint64_t rows = (uint64_t)c.n_experts * g.R;
     if (w13) {
@@ -730,17 +759,19 @@ cudaError_t launch_expert_gemm(const k3moe &h, const LayerDev &w, int T, int bn,
         ok = make_map_u8(&ra, w.w1p, rows, g.K / 2, kRawRow, BM) &&
              make_map_u8(&rb, w.w3p, rows, g.K / 2, kRawRow, BM) &&
              make_map_f16_sw128(&bx, h.ws.zperm, pairs, c.latent, c.latent + kZPad, kBoxRows) &&
+             make_map_f16_sw128(&bxm, h.ws.zperm, pairs, c.latent, c.latent + kZPad, 64) &&
              make_map_f16_sw128(&bxf, h.ws.zperm, pairs, c.latent, c.latent + kZPad, bn);
     } else {
         g.sa = g.sb = w.w2s;
         g.ma = g.mb = w.w2max;
         ok = make_map_u8(&ra, w.w2p, rows, g.K / 2, kRawRow, BM) &&
              make_map_f16_sw128(&bx, h.ws.h16, pairs, c.moe_inter, c.moe_inter, kBoxRows) &&
+             make_map_f16_sw128(&bxm, h.ws.h16, pairs, c.moe_inter, c.moe_inter, 64) &&
              make_map_f16_sw128(&bxf, h.ws.h16, pairs, c.moe_inter, c.moe_inter, bn);
         rb = ra;
     }
     if (!ok) return cudaErrorInvalidValue;
-#define K3_EG_LAUNCH(M, N) launch_pdl(k_expert_gemm<M, N>, h.sm_count, kThreads, Geo<M, N>::SMEM, s, ra, rb, bx, bxf, g)
+#define K3_EG_LAUNCH(M, N) launch_pdl(k_expert_gemm<M, N>, h.sm_count, kThreads, Geo<M, N>::SMEM, s, ra, rb, bx, bxm, bxf, g)
     if (bn == 128)
         return mode == kW13 ? K3_EG_LAUNCH(kW13, 128) : (mode == kW2 ? K3_EG_LAUNCH(kW2, 128) : K3_EG_LAUNCH(kW2Pair, 128));
     return mode == kW13 ? K3_EG_LAUNCH(kW13, 64) : (mode == kW2 ? K3_EG_LAUNCH(kW2, 64) : K3_EG_LAUNCH(kW2Pair, 64));
