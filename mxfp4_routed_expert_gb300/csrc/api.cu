@@ -78,8 +78,7 @@ size_t carve_workspace(const k3moe_config &c, char *base, Workspace *ws)
     const bool eg = expert_gemm_ok(c);
     w.zperm = cv.take<__half>(eg ? Tm * K * (L + kZPad) : 0);
     w.tiles = cv.take<int2>(eg ? expert_gemm_max_tiles(c) : 0);
-    w.tiles128 = cv.take<int2>(eg ? expert_gemm_max_tiles(c) : 0);
-    w.n_tiles = cv.take<int>(2);
+    w.n_tiles = cv.take<int>(1);
     w.perm_hist = cv.take<int>((size_t)perm_chunks(c.max_tokens) * E);
     w.act = cv.take<__nv_bfloat16>(Tm * (L + S));
     w.gemm_part = cv.take<float>(dense_gemm_part_floats(c));
@@ -244,10 +243,10 @@ int run_layer(k3moe *h, const LayerDev &w, const __nv_bfloat16 *x, __nv_bfloat16
     }
     if (gemm && cudaStreamWaitEvent(s, h->ev_join, 0) != cudaSuccess) return K3MOE_ERR_CUDA;
     if (egemm) {
-        K3_STEP("expert_tiles", launch_expert_tiles(*h, s));
+        K3_STEP("expert_tiles", launch_expert_tiles(*h, T, s));
         K3_STEP("gather_latent", launch_gather_latent(*h, T, s));
-        K3_STEP("expert_w13_gemm", launch_expert_gemm(*h, w, T, expert_gemm_bn(*h, T, true), s, true));
-        K3_STEP("expert_w2_gemm", launch_expert_gemm(*h, w, T, expert_gemm_bn(*h, T, false), s, false));
+        K3_STEP("expert_w13_gemm", launch_expert_gemm(*h, w, T, s, true));
+        K3_STEP("expert_w2_gemm", launch_expert_gemm(*h, w, T, s, false));
     } else {
         K3_STEP("expert_w13_gemv", launch_expert_w13(*h, w, T, s));
         K3_STEP("expert_w2_gemv", launch_expert_w2(*h, w, T, s));

@@ -68,19 +68,19 @@ constexpr uint32_t kTmemCols = 512;
 enum : int { kW13 = 0, kW2 = 1, kW2Pair = 2 };
 
 // Launch geometry for a mode with n-tiles of BN pairs. TMEM holds
-// SETS accumulator sets of two BN-column accumulators (two sets for BN = 64,
+// SETS accumulator sets of two BN-column accumulators (two sets for BN <= 64,
 // so that the epilogue overlaps the next item; one for BN = 128), then the
-// ring of converted A slots in the remaining 256 columns. Shared memory holds
+// ring of converted A slots in the remaining columns (256, or 384 for BN = 32). Shared memory holds
 // two TMA rings: activation tiles (NB stages, released by the MMAs) and packed
 // weight tiles (NR stages, released by the converters as soon as they have
 // read them, so that weight loads run far ahead of the tensor cores).
 template <int MODE, int BN>
 struct Geo {
-    static_assert(BN == 64 || BN == 128, "n-tile of 64 or 128 pairs");
+    static_assert(BN == 32 || BN == 64 || BN == 128, "n-tile of 32, 64 or 128 pairs");
     static constexpr int NM = MODE == kW2 ? 1 : 2;           // weight tiles per k-stage
-    static constexpr int SETS = BN == 64 ? 2 : 1;
+    static constexpr int SETS = BN <= 64 ? 2 : 1;
     static constexpr uint32_t SET_COLS = 2 * BN;
-    static constexpr uint32_t ARING0 = SETS * SET_COLS;     // 256
+    static constexpr uint32_t ARING0 = SETS * SET_COLS;     // 128 or 256
     static constexpr int ACOLS = NM * BK / 2;                // TMEM columns per A slot
     static constexpr int NSA = (int)(kTmemCols - ARING0) / ACOLS;
     static constexpr int BSUB = BN * 128;                    // one 64-column half of the activation tile
@@ -102,7 +102,7 @@ struct Geo {
     }
     static constexpr int NR = ring();
     static constexpr size_t SMEM = smem(NB, NR);
-    static_assert(ARING0 == 256, "accumulators take half of TMEM");
+    static_assert(ARING0 <= 256 && NSA >= 2, "accumulators leave room for two A slots");
     static_assert(NB >= NSA, "A slots are released through the activation ring");
     static_assert(SMEM <= (size_t)kSmemBudget && NR >= 4, "shared memory");
 };
@@ -241,7 +241,7 @@ __device__ __forceinline__ bool epilogue_item(const EgArgs &g, uint32_t tmem, in
 {
     using GE = Geo<MODE, BN>;
     constexpr bool IS13 = MODE == kW13;
-    constexpr int NCH = BN / CSTEP;         // chunks of 16 columns per warp (upper bound)
+    constexpr int NCH = BN / CSTEP > 0 ? BN / CSTEP : 1;   // chunks of 16 columns per warp (upper bound)
     const int lane = threadIdx.x & 31;
     const int q = (threadIdx.x >> 5) & 3;   // TMEM lanes 32q..32q+31
     const int erow = q * 32 + lane;         // weight row of the tile
@@ -427,12 +427,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // W1/W3 and paired W2: issuer q multiplies weight tile q; plain W2:
         // issuer q takes the k-steps 4q..4q+3 of every k-stage. Each writes
         // accumulator q of the set.
-        // With 64-pair n-tiles (small N, where the issue rate bounds the
+        // With 32- and 64-pair n-tiles (small N, where the issue rate bounds the
         // stage) the whole warp runs the loop, so that its descriptor
         // arithmetic is warp-uniform: lane 0 polls the barriers and one
         // elected lane issues. With 128-pair n-tiles lane 0 alone runs it,
         // which measured faster there.
-        constexpr bool kWarpIssue = BN == 64;
+        constexpr bool kWarpIssue = BN <= 64;
         const int q = warp - 1;
         if (kWarpIssue || lane == 0) {
             int local = 0;
@@ -566,43 +566,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-// n-tiles: (expert, j) for j < ceil(count_e / 64) and, in a second list,
-// j < ceil(count_e / 128); experts ascending. One block.
-__global__ void __launch_bounds__(1024) k_expert_tiles(const int *counts, int E, int2 *t64, int2 *t128,
-                                                       int *n_tiles)
+// n-tiles of at most bn pairs: (expert, j) for j < ceil(count_e / bn),
+// experts ascending. One block.
+__global__ void __launch_bounds__(1024) k_expert_tiles(const int *counts, int E, int bn, int2 *tiles, int *n_tiles)
 {
-    __shared__ int wsum[2][32];
+    __shared__ int wsum[32];
     pdl_launch_dependents();
     pdl_wait();
     const int e = threadIdx.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int c = e < E ? counts[e] : 0;
-    const int nt[2] = {(c + 63) / 64, (c + 127) / 128};
-    int incl[2] = {nt[0], nt[1]};
+    const int nt = (c + bn - 1) / bn;
+    int incl = nt;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-#pragma unroll
-        for (int l = 0; l < 2; l++) {
-            const int v = __shfl_up_sync(0xffffffffu, incl[l], o);
-            if (lane >= o) incl[l] += v;
-        }
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
     }
-    if (lane == 31) {
-        wsum[0][warp] = incl[0];
-        wsum[1][warp] = incl[1];
-    }
+    if (lane == 31) wsum[warp] = incl;
     __syncthreads();
-#pragma unroll
-    for (int l = 0; l < 2; l++) {
-        int base = 0, total = 0;
-        for (int w = 0; w < 32; w++) {
-            if (w < warp) base += wsum[l][w];
-            total += wsum[l][w];
-        }
-        int2 *out = l == 0 ? t64 : t128;
-        const int first = base + incl[l] - nt[l];
-        for (int j = 0; j < nt[l]; j++) out[first + j] = make_int2(e, j);
-        if (threadIdx.x == 0) n_tiles[l] = total;
+    int base = 0, total = 0;
+    for (int w = 0; w < 32; w++) {
+        if (w < warp) base += wsum[w];
+        total += wsum[w];
     }
+    const int first = base + incl - nt;
+    for (int j = 0; j < nt; j++) tiles[first + j] = make_int2(e, j);
+    if (threadIdx.x == 0) *n_tiles = total;
 }
 
 // zp[p] = z16[token of pair p] (L values and the exponent padding); one warp per pair.
@@ -672,7 +661,7 @@ bool expert_gemm_ok(const k3moe_config &c)
 
 size_t expert_gemm_max_tiles(const k3moe_config &c)
 {
-    return (size_t)((long long)c.max_tokens * c.topk / 64 + c.n_experts + 1);   // the narrower n-tile
+    return (size_t)((long long)c.max_tokens * c.topk / 32 + c.n_experts + 1);   // the narrowest n-tile
 }
 
 int expert_gemm_min_pairs() { return kMinPairs; }
@@ -686,7 +675,10 @@ cudaError_t set_smem()
 
 cudaError_t init_expert_gemm()
 {
-    cudaError_t e = set_smem<kW13, 64>();
+    cudaError_t e = set_smem<kW13, 32>();
+    if (e == cudaSuccess) e = set_smem<kW2, 32>();
+    if (e == cudaSuccess) e = set_smem<kW2Pair, 32>();
+    if (e == cudaSuccess) e = set_smem<kW13, 64>();
     if (e == cudaSuccess) e = set_smem<kW2, 64>();
     if (e == cudaSuccess) e = set_smem<kW2Pair, 64>();
     if (e == cudaSuccess) e = set_smem<kW13, 128>();
@@ -695,20 +687,20 @@ cudaError_t init_expert_gemm()
     return e;
 }
 
-// n-tile width of a launch: 128 pairs when the experts average at least 64
-// pairs each (every converted weight tile then feeds twice the MMA work, with
-// one accumulator set), else 64 with two sets so that the epilogue overlaps the
-// next item.
-int expert_gemm_bn(const k3moe &h, int T, bool w13)
+// n-tile width of a launch, from the average pairs per expert: 32 when the
+// experts see a few tokens each (narrow accumulators leave TMEM for a third A
+// slot), 64 below 64 pairs (two accumulator sets), else 128 (every converted
+// weight tile then feeds twice the MMA work, with one set).
+int expert_gemm_bn(const k3moe &h, int T)
 {
-    (void)w13;   // the same rule has measured best for both matrices
-    return (long long)T * h.cfg.topk >= 64LL * h.cfg.n_experts ? 128 : 64;
+    const long long pairs = (long long)T * h.cfg.topk, E = h.cfg.n_experts;
+    return pairs <= 4 * E ? 32 : (pairs < 64 * E ? 64 : 128);
 }
 
-cudaError_t launch_expert_tiles(const k3moe &h, cudaStream_t s)
+cudaError_t launch_expert_tiles(const k3moe &h, int T, cudaStream_t s)
 {
-    return launch_pdl(k_expert_tiles, 1, 1024, 0, s, (const int *)h.ws.counts, h.cfg.n_experts, h.ws.tiles,
-                      h.ws.tiles128, h.ws.n_tiles);
+    return launch_pdl(k_expert_tiles, 1, 1024, 0, s, (const int *)h.ws.counts, h.cfg.n_experts,
+                      expert_gemm_bn(h, T), h.ws.tiles, h.ws.n_tiles);
 }
 
 cudaError_t launch_gather_latent(const k3moe &h, int T, cudaStream_t s)
@@ -719,19 +711,20 @@ cudaError_t launch_gather_latent(const k3moe &h, int T, cudaStream_t s)
 }
 
 // W1/W3 (w13 = true: gathered latent -> h16) or W2 (h16 -> acc).
-cudaError_t launch_expert_gemm(const k3moe &h, const LayerDev &w, int T, int bn, cudaStream_t s, bool w13)
+cudaError_t launch_expert_gemm(const k3moe &h, const LayerDev &w, int T, cudaStream_t s, bool w13)
 {
     const k3moe_config &c = h.cfg;
     const int pairs = T * c.topk;
-    if (pairs < kMinPairs || (bn != 64 && bn != 128)) return cudaErrorInvalidValue;
+    const int bn = expert_gemm_bn(h, T);   // the width the tile list was built for
+    if (pairs < kMinPairs) return cudaErrorInvalidValue;
     EgArgs g = {};
     g.k = c.topk;
     g.L = c.latent;
     g.I = c.moe_inter;
     g.offsets = h.ws.offsets;
     g.perm = h.ws.perm;
-    g.tiles = bn == 128 ? h.ws.tiles128 : h.ws.tiles;
-    g.n_tiles = h.ws.n_tiles + (bn == 128 ? 1 : 0);
+    g.tiles = h.ws.tiles;
+    g.n_tiles = h.ws.n_tiles;
     g.pair_w = h.ws.pair_w;
     g.zp = h.ws.zperm;
     g.h16 = h.ws.h16;
@@ -759,14 +752,14 @@ cudaError_t launch_expert_gemm(const k3moe &h, const LayerDev &w, int T, int bn,
         ok = make_map_u8(&ra, w.w1p, rows, g.K / 2, kRawRow, BM) &&
              make_map_u8(&rb, w.w3p, rows, g.K / 2, kRawRow, BM) &&
              make_map_f16_sw128(&bx, h.ws.zperm, pairs, c.latent, c.latent + kZPad, kBoxRows) &&
-             make_map_f16_sw128(&bxm, h.ws.zperm, pairs, c.latent, c.latent + kZPad, 64) &&
+             make_map_f16_sw128(&bxm, h.ws.zperm, pairs, c.latent, c.latent + kZPad, bn < 64 ? bn : 64) &&
              make_map_f16_sw128(&bxf, h.ws.zperm, pairs, c.latent, c.latent + kZPad, bn);
     } else {
         g.sa = g.sb = w.w2s;
         g.ma = g.mb = w.w2max;
         ok = make_map_u8(&ra, w.w2p, rows, g.K / 2, kRawRow, BM) &&
              make_map_f16_sw128(&bx, h.ws.h16, pairs, c.moe_inter, c.moe_inter, kBoxRows) &&
-             make_map_f16_sw128(&bxm, h.ws.h16, pairs, c.moe_inter, c.moe_inter, 64) &&
+             make_map_f16_sw128(&bxm, h.ws.h16, pairs, c.moe_inter, c.moe_inter, bn < 64 ? bn : 64) &&
              make_map_f16_sw128(&bxf, h.ws.h16, pairs, c.moe_inter, c.moe_inter, bn);
         rb = ra;
     }
@@ -774,7 +767,9 @@ cudaError_t launch_expert_gemm(const k3moe &h, const LayerDev &w, int T, int bn,
 #define K3_EG_LAUNCH(M, N) launch_pdl(k_expert_gemm<M, N>, h.sm_count, kThreads, Geo<M, N>::SMEM, s, ra, rb, bx, bxm, bxf, g)
     if (bn == 128)
         return mode == kW13 ? K3_EG_LAUNCH(kW13, 128) : (mode == kW2 ? K3_EG_LAUNCH(kW2, 128) : K3_EG_LAUNCH(kW2Pair, 128));
-    return mode == kW13 ? K3_EG_LAUNCH(kW13, 64) : (mode == kW2 ? K3_EG_LAUNCH(kW2, 64) : K3_EG_LAUNCH(kW2Pair, 64));
+    if (bn == 64)
+        return mode == kW13 ? K3_EG_LAUNCH(kW13, 64) : (mode == kW2 ? K3_EG_LAUNCH(kW2, 64) : K3_EG_LAUNCH(kW2Pair, 64));
+    return mode == kW13 ? K3_EG_LAUNCH(kW13, 32) : (mode == kW2 ? K3_EG_LAUNCH(kW2, 32) : K3_EG_LAUNCH(kW2Pair, 32));
 #undef K3_EG_LAUNCH
 }
 

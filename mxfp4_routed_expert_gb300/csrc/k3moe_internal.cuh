@@ -65,10 +65,9 @@ struct Workspace {
     __half *h16 = nullptr;        // [Tm*k, I] SiTU output per (token, expert) pair, perm order
     float *acc = nullptr;         // [Tm, L]
     __half *zperm = nullptr;      // [Tm*k, L + kZPad] z16 rows gathered in pair order (expert GEMM)
-    int2 *tiles = nullptr;        // (expert, n-tile) list of the expert GEMM, 64-pair n-tiles
-    int2 *tiles128 = nullptr;     // the same with 128-pair n-tiles
+    int2 *tiles = nullptr;        // (expert, n-tile) list of the expert GEMM
     int *perm_hist = nullptr;     // [ceil(Tm/32), E] per-chunk expert counts, then chunk bases
-    int *n_tiles = nullptr;       // [2]: lengths of the two lists
+    int *n_tiles = nullptr;       // length of the list
     __nv_bfloat16 *act = nullptr;     // [Tm, L+S] bf16 [normed latent | shared SiTU] (GEMM path)
     float *gemm_part = nullptr;       // split-K partial sums (kept zeroed between launches)
     int *gemm_tiles = nullptr;        // split-K arrival counters (kept at zero)
@@ -146,10 +145,10 @@ bool expert_gemm_ok(const k3moe_config &c);
 size_t expert_gemm_max_tiles(const k3moe_config &c);
 int expert_gemm_min_pairs();
 cudaError_t init_expert_gemm();
-int expert_gemm_bn(const k3moe &h, int T, bool w13);
-cudaError_t launch_expert_tiles(const k3moe &h, cudaStream_t s);
+int expert_gemm_bn(const k3moe &h, int T);
+cudaError_t launch_expert_tiles(const k3moe &h, int T, cudaStream_t s);
 cudaError_t launch_gather_latent(const k3moe &h, int T, cudaStream_t s);
-cudaError_t launch_expert_gemm(const k3moe &h, const LayerDev &w, int T, int bn, cudaStream_t s, bool w13);
+cudaError_t launch_expert_gemm(const k3moe &h, const LayerDev &w, int T, cudaStream_t s, bool w13);
 cudaError_t launch_row_scale_max(const uint8_t *s, size_t rows, int G, uint8_t *out);
 bool dense_tma_fits(const k3moe_config &c, int TB);
 // TMA-fed dense GEMVs for T <= 2. part 0: router + down; 1: shared gate/up;

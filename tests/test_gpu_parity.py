@@ -82,7 +82,8 @@ def test_expert_paths(T, path):
 @pytest.mark.parametrize("path", ["gemm", "gemv"])
 def test_expert_gemm_multi_tile(path):
     """Four experts forced into every token's selection (+10 router bias): each
-    holds all 300 tokens, three n-tiles of the grouped GEMM (128, 128, 44)."""
+    holds all 300 tokens, five n-tiles of the grouped GEMM (2400 pairs on 128
+    experts take 64-pair tiles: 4 x 64 + 44)."""
     import mxfp4_routed_expert_gb300 as km
     d = k3synth.make_layer(WIDE, 8, 0, k3synth.TINY_RECIPE)
     bias = np.asarray(d["router_bias"], np.float32).copy()
@@ -90,6 +91,19 @@ def test_expert_gemm_multi_tile(path):
     d = k3synth.with_bias(d, bias)
     mode = km.K3MOE_EXPERT_GEMM if path == "gemm" else km.K3MOE_EXPERT_GEMV
     run_case(WIDE, k3synth.TINY_RECIPE, 8, 300, expert_path=mode, d=d)
+
+
+@pytest.mark.parametrize("T", [40, 64])
+def test_expert_gemm_narrow_ntiles(T):
+    """At most four pairs per expert on average (T*8 <= 4*128) selects 32-pair
+    n-tiles; four experts forced into every selection then hold T pairs each,
+    two n-tiles (32 + 8 at T=40, 32 + 32 at T=64)."""
+    import mxfp4_routed_expert_gb300 as km
+    d = k3synth.make_layer(WIDE, 10, 0, k3synth.TINY_RECIPE)
+    bias = np.asarray(d["router_bias"], np.float32).copy()
+    bias[[5, 50, 90, 126]] += 10.0
+    d = k3synth.with_bias(d, bias)
+    run_case(WIDE, k3synth.TINY_RECIPE, 10, T, expert_path=km.K3MOE_EXPERT_GEMM, d=d)
 
 
 @pytest.mark.parametrize("hot", [False, True])
