@@ -198,15 +198,12 @@ __device__ __forceinline__ bool elect_one()
     return p != 0;
 }
 
-// A bounded barrier wait of the MMA issuer: by the calling thread, or (WARP)
-// by lane 0 with the outcome taken by the whole warp.
-template <bool WARP>
-__device__ __forceinline__ bool issuer_wait(uint64_t *bar, uint32_t parity, int *err, int where)
+// A bounded barrier wait by every lane of a converged warp, which takes the
+// outcome only if all lanes saw the phase complete.
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, int *err, int where)
 {
-    if (!WARP) return mbar_wait(bar, parity, err, where);
-    bool ok = true;
-    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, err, where);
-    return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    const bool ok = mbar_wait(bar, parity, err, where);
+    return __all_sync(0xffffffffu, ok) != 0;
 }
 
 // A from tensor memory, B from shared memory.
@@ -427,14 +424,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // W1/W3 and paired W2: issuer q multiplies weight tile q; plain W2:
         // issuer q takes the k-steps 4q..4q+3 of every k-stage. Each writes
         // accumulator q of the set.
-        // With 32- and 64-pair n-tiles (small N, where the issue rate bounds the
-        // stage) the whole warp runs the loop, so that its descriptor
-        // arithmetic is warp-uniform: lane 0 polls the barriers and one
-        // elected lane issues. With 128-pair n-tiles lane 0 alone runs it,
-        // which measured faster there.
-        constexpr bool kWarpIssue = BN <= 64;
+        // The whole warp runs the loop, so that its descriptor arithmetic is
+        // warp-uniform; all lanes poll the barriers and one elected lane
+        // issues (faster than one thread running it alone, most of all at
+        // small N where the issue rate bounds the stage).
         const int q = warp - 1;
-        if (kWarpIssue || lane == 0) {
+        {
             int local = 0;
             RingPos<NB> bp;
             RingPos<NSA> ap;
@@ -450,19 +445,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t idesc =
                     (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);  // f16 x f16 -> f32
                 const int b = local % kSets;
-                if (!issuer_wait<kWarpIssue>(&tempty[b], ((uint32_t)(local / kSets) & 1u) ^ 1u, g.err, 601)) break;
+                if (!warp_wait(&tempty[b], ((uint32_t)(local / kSets) & 1u) ^ 1u, g.err, 601)) break;
                 tc::fence_after();
                 const uint32_t d = tmem + (uint32_t)b * kSetCols + (uint32_t)q * BN;
                 for (int kt = 0; kt < KT; kt++, bp.next(), ap.next()) {
-                    if (!issuer_wait<kWarpIssue>(&aready[ap.slot], ap.phase, g.err, 603) ||
-                        !issuer_wait<kWarpIssue>(&bfull[bp.slot], bp.phase, g.err, 609)) {
+                    if (!warp_wait(&aready[ap.slot], ap.phase, g.err, 603) ||
+                        !warp_wait(&bfull[bp.slot], bp.phase, g.err, 609)) {
                         ok = false;
                         break;
                     }
                     tc::fence_after();
                     const uint32_t a0 = tmem + kARing0 + (uint32_t)(ap.slot * ACOLS) + (DUAL ? (uint32_t)q * (BK / 2) : 0u);
                     const uint64_t db = db0 + (uint64_t)((bp.slot * kBBytes) >> 4);
-                    if (!kWarpIssue || elect_one()) {
+                    if (elect_one()) {
 #pragma unroll
                         for (int i = 0; i < NK; i++) {
                             const int kk = kk0 + i;
@@ -472,10 +467,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         tc::commit(&bfree[bp.slot]);
                     }
-                    if (kWarpIssue) __syncwarp();
+                    __syncwarp();
                 }
-                if (ok && (!kWarpIssue || elect_one())) tc::commit(&tfull[b]);
-                if (kWarpIssue) __syncwarp();
+                if (ok && elect_one()) tc::commit(&tfull[b]);
+                __syncwarp();
             }
         }
     } else if (warp >= kConvWarp0 && warp < kConvWarp0 + kConvWarps) {
