@@ -339,9 +339,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < NR; i++) {
             mbar_init(&wfull[i], 1);
-            mbar_init(&wfree[i], kConvWarps);
+            mbar_init(&wfree[i], kConvWarps / 2);   // the warps of one parity read a stage
         }
-        for (int i = 0; i < NSA; i++) mbar_init(&aready[i], kConvWarps);
+        for (int i = 0; i < NSA; i++) mbar_init(&aready[i], kConvWarps / 2);
         for (int i = 0; i < kSets; i++) {
             mbar_init(&tfull[i], 2);
             mbar_init(&tempty[i], kSets == 2 ? kEpiWarps : kConvWarps);
@@ -475,47 +475,54 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp >= kConvWarp0 && warp < kConvWarp0 + kConvWarps) {
         // ---------------- converters: packed e2m1 -> scaled f16 -> TMEM ----------------
+        // The warps alternate k-stages (sl & 1 = the parity of the stages a warp
+        // takes), so that each warp's fixed per-stage cost (barrier waits and
+        // arrivals) spreads over two stage times. Per stage, the eight warps
+        // of a parity cover the four lane quadrants twice: one weight tile
+        // each (all four scale groups), or for plain W2 two scale groups each.
         const int qd = warp & 3;                      // TMEM lane quadrant
         const int row = qd * 32 + lane;               // weight row of the tile (its TMEM lane)
-        const int sl = (warp - kConvWarp0) >> 2;      // 0..3: this warp's share of the k-stage
-        // two weight tiles: tile sl >> 1, 64 columns (two scale groups) from 64 * (sl & 1);
-        // plain W2: 32 columns (one scale group) from 32 * sl
-        const int m = DUAL ? (sl >> 1) : 0;
-        const int grp0 = DUAL ? 2 * (sl & 1) : sl;    // first scale group within the k-stage
-        constexpr int NGRP = DUAL ? 2 : 1;
+        const int sl = (warp - kConvWarp0) >> 2;      // 0..3
+        const int par = sl & 1;
+        const int m = DUAL ? (sl >> 1) : 0;           // weight tile
+        const int grp0 = DUAL ? 0 : 2 * (sl >> 1);    // first scale group within the k-stage
+        constexpr int NGRP = DUAL ? 4 : 2;
         const uint32_t tlane = (uint32_t)(qd * 32) << 16;
         const int G = g.K / kGroup;
         const int swz = (row >> 1) & 3;              // 64-byte swizzle of the packed tile
         RingPos<NR> wp;           // weight stage of this k-stage
         RingPos<NB> rq;           // activation stage of the k-stage NSA back (its MMAs free the A slot)
         RingPos<NSA> ap;
-        int done = 0;             // k-stages converted so far
+        int done = 0;             // k-stages of this CTA so far
         int local = 0;            // items of this CTA so far
         bool ok = true;
         // With one accumulator set the issuers stop between items until the
         // accumulators are drained, so the converters run the epilogue
         // themselves (each warp a quarter of the pair columns of its lane
-        // quadrant) right after converting the next item's first k-stage,
-        // whose A slot frees up before the previous item's last MMAs end.
+        // quadrant) right after converting their first k-stage of the next
+        // item, whose A slot frees up before the previous item's last MMAs end.
         for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, local++) {
             const int tile = item / g.MT, mt = item - tile * g.MT;
             const size_t grow = (size_t)g.tiles[tile].x * g.R + mt * g.mstep + row + (m ? g.mrow : 0);
             const int smax = m == 0 ? g.ma[grow] : g.mb[grow];
-            const uint8_t *sc = (m == 0 ? g.sa : g.sb) + grow * (size_t)G + grp0;
+            const uint8_t *sc = (m == 0 ? g.sa : g.sb) + grow * (size_t)G + grp0;   // G % 4 == 0
+            bool epi = kSets == 1 && local > 0;      // previous item's epilogue still to run
             for (int kt = 0; kt < KT; kt++, wp.next(), ap.next(), done++) {
-                int sv[NGRP];
-#pragma unroll
-                for (int i = 0; i < NGRP; i++) sv[i] = sc[4 * kt + i];
-                if (!mbar_wait(&wfull[wp.slot], wp.phase, g.err, 604)) {
-                    ok = false;
-                    break;
-                }
+                const bool mine = (done & 1) == par;
                 if (done >= NSA) {
-                    if (!mbar_wait(&bfree[rq.slot], rq.phase, g.err, 607)) {
+                    if (mine && !mbar_wait(&bfree[rq.slot], rq.phase, g.err, 607)) {
                         ok = false;
                         break;
                     }
                     rq.next();
+                }
+                if (!mine) continue;
+                uint32_t sv4;
+                if (NGRP == 4) sv4 = *reinterpret_cast<const uint32_t *>(sc + 4 * kt);
+                else sv4 = *reinterpret_cast<const uint16_t *>(sc + 4 * kt);
+                if (!mbar_wait(&wfull[wp.slot], wp.phase, g.err, 604)) {
+                    ok = false;
+                    break;
                 }
                 tc::fence_after();
                 const unsigned char *rawp = wring + wp.slot * kRBytes + m * kRawBytes + row * kRawRow;
@@ -529,19 +536,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int i = 0; i < NGRP; i++) {
                     uint32_t v[16];
-                    widen_group(w[i], f16x2_pow2(sv[i] - smax), v);
+                    widen_group(w[i], f16x2_pow2((int)((sv4 >> (8 * i)) & 0xffu) - smax), v);
                     tmem_st16(tmem + tlane + acol + (uint32_t)(16 * (grp0 + i)), v);
                 }
                 asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
                 tc::fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&aready[ap.slot]);
-                if (kSets == 1 && local > 0 && kt == 0 &&
-                    !epilogue_item<MODE, BN, 64>(g, tmem, item - (int)gridDim.x, local - 1, tfull, tempty, 16 * sl)) {
-                    ok = false;
-                    break;
+                if (epi) {
+                    epi = false;
+                    if (!epilogue_item<MODE, BN, 64>(g, tmem, item - (int)gridDim.x, local - 1, tfull, tempty,
+                                                     16 * sl)) {
+                        ok = false;
+                        break;
+                    }
                 }
             }
+            if (ok && epi &&   // an item with no k-stage of this warp's parity
+                !epilogue_item<MODE, BN, 64>(g, tmem, item - (int)gridDim.x, local - 1, tfull, tempty, 16 * sl))
+                ok = false;
         }
         if (kSets == 1 && ok && local > 0)
             epilogue_item<MODE, BN, 64>(g, tmem, blockIdx.x + (local - 1) * (int)gridDim.x, local - 1, tfull, tempty,

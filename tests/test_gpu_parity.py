@@ -106,6 +106,19 @@ def test_expert_gemm_narrow_ntiles(T):
     run_case(WIDE, k3synth.TINY_RECIPE, 10, T, expert_path=km.K3MOE_EXPERT_GEMM, d=d)
 
 
+# latent 384: three 128-row m-tiles of W2, which the grouped GEMM runs one per
+# item with the k-stage split across its two MMA issuers (no m-tile pairing)
+ODD_LATENT = k3synth.Shape(hidden=1024, latent=384, n_experts=128, topk=8, moe_inter=512,
+                           shared_inter=1024)
+
+
+@pytest.mark.parametrize("T", [48, 200])
+def test_expert_gemm_unpaired_w2(T):
+    """The unpaired W2 mode at 32-pair (T=48) and 64-pair (T=200) n-tiles."""
+    import mxfp4_routed_expert_gb300 as km
+    run_case(ODD_LATENT, k3synth.TINY_RECIPE, 11, T, expert_path=km.K3MOE_EXPERT_GEMM)
+
+
 @pytest.mark.parametrize("hot", [False, True])
 def test_expert_gemm_wide_ntiles(hot):
     """T=1100 on the 128-expert shape: 8800 pairs, at least 64 per expert on
