@@ -58,6 +58,9 @@ WORKLOADS = {
     # small case for ncu captures: K3 row shapes, 64 experts (1.2 GB), decode T=1
     "decode_t1_e64": dict(T=1, layers=1, desc="K3 row shapes with 64 routed experts, decode T=1 "
                           "(small case for profiler captures)"),
+    "batch_t16_e64": dict(T=16, layers=1, desc="K3 row shapes with 64 routed experts, T=16 "
+                          "(4 pairs per expert, the 32-pair n-tiles of decode T=64; small case "
+                          "for profiler captures)"),
     "batch_t64_e64": dict(T=64, layers=1, desc="K3 row shapes with 64 routed experts, T=64 "
                           "(16 pairs per expert; small case for profiler captures)"),
     "prefill_t512_e64": dict(T=512, layers=1, desc="K3 row shapes with 64 routed experts, T=512 "
