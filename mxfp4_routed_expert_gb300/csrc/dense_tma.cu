@@ -8,8 +8,11 @@
 //   UP: y = Wu . n + Ws2 . s with n = RMSNorm(acc) * gain (the norm of the
 //       aggregate, section 9 step 4) and s the shared SiTU output, bf16 output.
 //
-// Persistent, one CTA per SM: a producer warp streams weight-row stages
-// through a shared-memory ring with bulk TMA copies (one copy per row piece),
+// Persistent, one CTA per SM: a producer thread streams weight-row stages
+// through a shared-memory ring with 3D tensor TMA copies: a matrix viewed as
+// (64 columns, column blocks, rows) lands 16 rows x 1024 columns of a stage in
+// one copy (4- and 1-row boxes take the rows of a partial group), since a
+// thread issues a TMA copy only every ~150 cycles;
 // sixteen consumer warps each own one row (RD, UP) or one gate/up row pair
 // (SH) of a stage. The activations of the TB tokens sit in shared memory as
 // bf16 for the whole kernel. The producer starts streaming weights before the
@@ -21,7 +24,8 @@
 // contiguously over the CTAs.
 #include <algorithm>
 
-#include "k3moe_internal.cuh"
+#include "decode_common.cuh"
+#include "tc_common.cuh"
 
 namespace k3 {
 
@@ -56,6 +60,26 @@ struct DenseTArgs {
 
 __device__ __forceinline__ int pieces_of(int cols) { return (cols + kPieceCols - 1) / kPieceCols; }
 
+// Row tensor maps of one weight matrix (boxes of 16, 4 and 1 rows, 1024 columns).
+struct RowMaps {
+    CUtensorMap m16, m4, m1;
+};
+struct DenseMaps {
+    RowMaps a, b;   // the mode's two matrices (RD: router, down; SH: w1, w3; UP: up, shared w2)
+};
+constexpr int kPieceBlocks = kPieceCols / 64;
+
+// Rows [r, r + n) of a matrix, column blocks from y0, into consecutive
+// kPieceBytes rows at dst: 16-row boxes, then 4-row, then single rows.
+__device__ __forceinline__ void load_rows(const RowMaps &m, unsigned char *dst, int r, int n, int y0,
+                                          uint64_t *bar, uint64_t pol)
+{
+    int i = 0;
+    for (; n - i >= 16; i += 16) tc::tma_load_3d(dst + i * kPieceBytes, &m.m16, 0, y0, r + i, bar, pol);
+    for (; n - i >= 4; i += 4) tc::tma_load_3d(dst + i * kPieceBytes, &m.m4, 0, y0, r + i, bar, pol);
+    for (; i < n; i++) tc::tma_load_3d(dst + i * kPieceBytes, &m.m1, 0, y0, r + i, bar, pol);
+}
+
 // Piece p of a row: which matrix (0: wa, 1: wb), its first column inside that
 // matrix, its width, and where its activations start in the staged vector.
 // RD/SH rows are one matrix of H columns; UP rows are [Wu (L) | Ws2 (S)].
@@ -86,23 +110,8 @@ __device__ __forceinline__ int npieces_of(const DenseTArgs &a)
     return a.mode != UP ? pieces_of(a.H) : pieces_of(a.L) + pieces_of(a.S);
 }
 
-// acc += dot(8 bf16 weights, 8 bf16 activations): fp32 fused multiply-adds on
-// bf16 operands, two chains for instruction-level parallelism.
-__device__ __forceinline__ void dot8_bf16(const uint4 &w, const uint4 &x, float &a0, float &a1)
-{
-    asm("{\n\t.reg .b16 w0, w1, w2, w3, w4, w5, w6, w7, x0, x1, x2, x3, x4, x5, x6, x7;\n\t"
-        "mov.b32 {w0, w1}, %2;\n\tmov.b32 {w2, w3}, %3;\n\tmov.b32 {w4, w5}, %4;\n\tmov.b32 {w6, w7}, %5;\n\t"
-        "mov.b32 {x0, x1}, %6;\n\tmov.b32 {x2, x3}, %7;\n\tmov.b32 {x4, x5}, %8;\n\tmov.b32 {x6, x7}, %9;\n\t"
-        "fma.rn.f32.bf16 %0, w0, x0, %0;\n\tfma.rn.f32.bf16 %1, w1, x1, %1;\n\t"
-        "fma.rn.f32.bf16 %0, w2, x2, %0;\n\tfma.rn.f32.bf16 %1, w3, x3, %1;\n\t"
-        "fma.rn.f32.bf16 %0, w4, x4, %0;\n\tfma.rn.f32.bf16 %1, w5, x5, %1;\n\t"
-        "fma.rn.f32.bf16 %0, w6, x6, %0;\n\tfma.rn.f32.bf16 %1, w7, x7, %1;\n\t}"
-        : "+f"(a0), "+f"(a1)
-        : "r"(w.x), "r"(w.y), "r"(w.z), "r"(w.w), "r"(x.x), "r"(x.y), "r"(x.z), "r"(x.w));
-}
-
 template <int TB>
-__global__ void __launch_bounds__(kThreads, 1) k_dense_tma(DenseTArgs a)
+__global__ void __launch_bounds__(kThreads, 1) k_dense_tma(const __grid_constant__ DenseMaps mp, DenseTArgs a)
 {
     extern __shared__ __align__(128) unsigned char sm[];
     const bool sh = a.mode == SH;
@@ -125,6 +134,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_dense_tma(DenseTArgs a)
         }
         fence_mbar_init();
     }
+    if (threadIdx.x == kCW * 32) {
+        tc::prefetch_map(&mp.a.m16);
+        tc::prefetch_map(&mp.b.m16);
+    }
     __syncthreads();
     pdl_launch_dependents();
     // The producer reads weights only, which no earlier kernel writes: it
@@ -137,49 +150,41 @@ __global__ void __launch_bounds__(kThreads, 1) k_dense_tma(DenseTArgs a)
     const int r1 = (int)((long long)a.units * (blockIdx.x + 1) / gridDim.x);
 
     if (warp == kCW) {
-        // ---------------- producer warp: weight pieces only ----------------
-        // lane 0 waits for the slot and posts the byte count, then each lane
-        // issues the copy of one row piece
-        const uint64_t pol = l2_policy_evict_first();
-        int slot = 0, issued = 0;
-        uint32_t phase = 0;
-        bool ok = true;
-        for (int g0 = r0; g0 < r1 && ok; g0 += kCW) {
-            const int ng = min(kCW, r1 - g0);
-            for (int p = 0; p < npieces; p++) {
-                int good = 1;
-                if (lane == 0) good = mbar_wait(&empty[slot], phase ^ 1u, a.err, 400 + slot) ? 1 : 0;
-                good = __shfl_sync(0xffffffffu, good, 0);
-                if (!good) {
-                    ok = false;
-                    break;
-                }
-                const Piece q = piece_info(a, p);
-                const uint32_t nb = (uint32_t)q.ncol * 2u;
-                unsigned char *st = sm + slot * stage_bytes;
-                if (lane == 0) mbar_expect_tx(&full[slot], nb * (uint32_t)(sh ? 2 * ng : ng));
-                __syncwarp();
-                // lane l: unit l % 16 of the group; for SH lanes 16-31 take the up rows
-                const int i = lane & (kCW - 1), h = lane >> 4;
-                if (i < ng && (sh || h == 0)) {
-                    const int r = g0 + i;
-                    const __nv_bfloat16 *row;
-                    if (a.mode == RD)
-                        row = r < a.E ? a.wa + (size_t)r * a.H : a.wb + (size_t)(r - a.E) * a.H;
-                    else if (sh)
-                        row = (h == 0 ? a.wa : a.wb) + (size_t)r * a.H;
-                    else
-                        row = q.mat == 0 ? a.wa + (size_t)r * a.L : a.wb + (size_t)r * a.S;
-                    bulk_g2s(st + (h * kCW + i) * kPieceBytes, row + q.col0, nb, &full[slot], pol);
-                }
-                issued++;
-                if (++slot == NS) {
-                    slot = 0;
-                    phase ^= 1u;
+        // ---------------- producer thread: weight pieces only ----------------
+        if (lane == 0) {
+            const uint64_t pol = l2_policy_evict_first();
+            int slot = 0, issued = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int g0 = r0; g0 < r1 && ok; g0 += kCW) {
+                const int ng = min(kCW, r1 - g0);
+                for (int p = 0; p < npieces; p++) {
+                    if (!mbar_wait(&empty[slot], phase ^ 1u, a.err, 400 + slot)) {
+                        ok = false;
+                        break;
+                    }
+                    const Piece q = piece_info(a, p);
+                    unsigned char *st = sm + slot * stage_bytes;
+                    // whole boxes land: a piece's columns past the matrix read as zeros
+                    mbar_expect_tx(&full[slot], (uint32_t)((sh ? 2 : 1) * ng * kPieceBytes));
+                    const int y0 = (q.col0 / kPieceCols) * kPieceBlocks;
+                    if (a.mode == RD) {
+                        const int nr = max(0, min(ng, a.E - g0));   // router rows, then down rows
+                        if (nr > 0) load_rows(mp.a, st, g0, nr, y0, &full[slot], pol);
+                        if (ng > nr) load_rows(mp.b, st + nr * kPieceBytes, g0 + nr - a.E, ng - nr, y0, &full[slot], pol);
+                    } else if (sh) {
+                        load_rows(mp.a, st, g0, ng, y0, &full[slot], pol);
+                        load_rows(mp.b, st + kCW * kPieceBytes, g0, ng, y0, &full[slot], pol);
+                    } else {
+                        load_rows(q.mat == 0 ? mp.a : mp.b, st, g0, ng, y0, &full[slot], pol);
+                    }
+                    issued++;
+                    if (++slot == NS) {
+                        slot = 0;
+                        phase ^= 1u;
+                    }
                 }
             }
-        }
-        if (lane == 0) {
             const int n = issued < NS ? issued : NS;
             for (int j = issued - n; j < issued; j++)
                 mbar_wait(&full[j % NS], (uint32_t)(j / NS) & 1u, a.err, 401);
@@ -330,8 +335,16 @@ size_t dense_tma_smem(int mode, int K, int TB, int ns)
 
 bool dense_tma_fits(const k3moe_config &c, int TB)
 {
-    return stages_for(SH, c.hidden, TB) >= 2 && stages_for(RD, c.hidden, TB) >= 2 &&
+    return c.hidden % 64 == 0 && c.latent % 64 == 0 && c.shared_inter % 64 == 0 &&   // row maps
+           stages_for(SH, c.hidden, TB) >= 2 && stages_for(RD, c.hidden, TB) >= 2 &&
            stages_for(UP, c.latent + c.shared_inter, TB) >= 2;
+}
+
+static bool make_row_maps(RowMaps *m, const void *base, int rows, int cols)
+{
+    return tc::make_map_bf16_rows(&m->m16, base, rows, cols, kPieceBlocks, 16) &&
+           tc::make_map_bf16_rows(&m->m4, base, rows, cols, kPieceBlocks, 4) &&
+           tc::make_map_bf16_rows(&m->m1, base, rows, cols, kPieceBlocks, 1);
 }
 
 cudaError_t init_dense_tma(const k3moe_config &c)
@@ -388,6 +401,18 @@ cudaError_t launch_dense_tma(const k3moe &h, const LayerDev &w, const __nv_bfloa
         a.y = y;
         a.units = c.hidden;
     }
+    DenseMaps mp;
+    bool ok;
+    if (part == 0)
+        ok = make_row_maps(&mp.a, w.router_w, c.n_experts, c.hidden) &&
+             make_row_maps(&mp.b, w.down_w, c.latent, c.hidden);
+    else if (part == 1)
+        ok = make_row_maps(&mp.a, w.sh_w1, c.shared_inter, c.hidden) &&
+             make_row_maps(&mp.b, w.sh_w3, c.shared_inter, c.hidden);
+    else
+        ok = make_row_maps(&mp.a, w.up_w, c.hidden, c.latent) &&
+             make_row_maps(&mp.b, w.sh_w2, c.hidden, c.shared_inter);
+    if (!ok) return cudaErrorInvalidValue;
     const int TB = T == 1 ? 1 : 2;
     a.ns = stages_for(a.mode, a.K, TB);
     const int groups = (a.units + kCW - 1) / kCW;
@@ -398,10 +423,10 @@ cudaError_t launch_dense_tma(const k3moe &h, const LayerDev &w, const __nv_bfloa
     // has already waited for everything the input depends on.
     a.wait = a.mode != SH;
     if (a.mode == RD)
-        return TB == 1 ? launch_ordered(k_dense_tma<1>, grid, kThreads, smem, s, a)
-                       : launch_ordered(k_dense_tma<2>, grid, kThreads, smem, s, a);
-    return TB == 1 ? launch_pdl(k_dense_tma<1>, grid, kThreads, smem, s, a)
-                   : launch_pdl(k_dense_tma<2>, grid, kThreads, smem, s, a);
+        return TB == 1 ? launch_ordered(k_dense_tma<1>, grid, kThreads, smem, s, mp, a)
+                       : launch_ordered(k_dense_tma<2>, grid, kThreads, smem, s, mp, a);
+    return TB == 1 ? launch_pdl(k_dense_tma<1>, grid, kThreads, smem, s, mp, a)
+                   : launch_pdl(k_dense_tma<2>, grid, kThreads, smem, s, mp, a);
 }
 
 }  // namespace k3

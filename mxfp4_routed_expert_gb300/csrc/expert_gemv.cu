@@ -27,7 +27,7 @@
 //   (README section 9, k3_moe step 3 and k3_situ_glu).
 // k_w2_tma: h . W2 rows, times the pair's routing weight, scatter-added into
 //   the token's fp32 latent accumulator.
-#include "k3moe_internal.cuh"
+#include "decode_common.cuh"
 
 namespace k3 {
 
@@ -97,26 +97,6 @@ __device__ __forceinline__ int find_expert(const int *offsets, int E, long long 
         if ((long long)offsets[mid] * RB <= u) lo = mid; else hi = mid;
     }
     return lo;
-}
-
-// 32 nibbles (one 16-byte chunk) against 32 fp16 activations held as 16 f16x2;
-// two partial accumulators for instruction-level parallelism.
-__device__ __forceinline__ float chunk_dot(const uint4 w, const uint32_t (&x)[16])
-{
-    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-    uint32_t h0 = 0u, h1 = 0u;
-#pragma unroll
-    for (int q = 0; q < 4; q++) {
-        uint32_t a0, a1, a2, a3;
-        e2m1x8_to_f16x2x4(ww[q], a0, a1, a2, a3);
-        h0 = hfma2(a0, x[4 * q], h0);
-        h1 = hfma2(a1, x[4 * q + 1], h1);
-        h0 = hfma2(a2, x[4 * q + 2], h0);
-        h1 = hfma2(a3, x[4 * q + 3], h1);
-    }
-    uint32_t h;
-    asm("add.rn.f16x2 %0, %1, %2;" : "=r"(h) : "r"(h0), "r"(h1));
-    return f16x2_sum(h);
 }
 
 // Warp sum of each of v[0..N) (N a power of two, 2..32). Each halving step

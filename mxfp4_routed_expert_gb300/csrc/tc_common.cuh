@@ -80,6 +80,34 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
         : "memory");
 }
 
+// 3D tile (x, y, z) with an L2 cache policy.
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, int c0, int c1, int c2,
+                                            uint64_t *bar, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(su32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(su32(bar)), "l"(policy)
+        : "memory");
+}
+
+// A bf16 [rows, cols] row-major matrix viewed as (64 columns, cols / 64 blocks,
+// rows), box {64, blocks, box_rows}: one copy lands box_rows rows of
+// 64 * blocks columns each, row after row, unswizzled. cols % 64 == 0.
+inline bool make_map_bf16_rows(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, uint32_t blocks,
+                               uint32_t box_rows)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn || cols % 64) return false;
+    const cuuint64_t dims[3] = {64, cols / 64, rows};
+    const cuuint64_t strides[2] = {128, cols * 2};
+    const cuuint32_t box[3] = {64, blocks, box_rows};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 __device__ __forceinline__ void prefetch_map(const CUtensorMap *map)
 {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
