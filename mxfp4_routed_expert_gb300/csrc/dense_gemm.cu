@@ -235,12 +235,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-// N tile: a multiple of 16 no larger than T (every TMA box stays inside the
-// token extent), at most 256.
-int pick_bn(int T)
+// N tile: a multiple of 16 no larger than T, at most 256. When the tile grid
+// spans several waves of the GPU, the width that minimises waves x (N + a
+// per-tile overhead worth 32 columns) is taken, so that the last wave is not
+// nearly empty (tiles past T read zero rows and store nothing).
+int pick_bn(int T, int mtiles, int sms)
 {
     int bn = (T / 16) * 16;
-    return bn > 256 ? 256 : bn;
+    if (bn > 256) bn = 256;
+    if (T < 512) return bn;
+    long long best = -1;
+    int pick = bn;
+    for (int c = bn; c >= 128; c -= 16) {
+        const long long tiles = (long long)mtiles * ((T + c - 1) / c);
+        const long long cost = ((tiles + sms - 1) / sms) * (c + 32);
+        if (best < 0 || cost < best) {
+            best = cost;
+            pick = c;
+        }
+    }
+    return pick;
 }
 
 int stages_for(int mode, int BN)
@@ -279,7 +293,7 @@ cudaError_t launch_dense_gemm(const k3moe &h, const LayerDev &w, const __nv_bflo
     GemmArgs g = {};
     g.mode = part;
     g.T = T;
-    g.BN = pick_bn(T);
+
     g.E = c.n_experts;
     g.L = c.latent;
     g.S = c.shared_inter;
@@ -300,6 +314,7 @@ cudaError_t launch_dense_gemm(const k3moe &h, const LayerDev &w, const __nv_bflo
     if (part == 0) {
         const int mta = (c.n_experts + BM - 1) / BM;
         mtiles = mta + (c.latent + BM - 1) / BM;
+        g.BN = pick_bn(T, mtiles, h.sm_count);
         g.KTA = mta;
         g.KT = c.hidden / BK;
         ok = tc::make_map_bf16_sw128(&a0, w.router_w, c.n_experts, c.hidden, c.hidden, BM) &&
@@ -307,12 +322,14 @@ cudaError_t launch_dense_gemm(const k3moe &h, const LayerDev &w, const __nv_bflo
              tc::make_map_bf16_sw128(&b, x, T, c.hidden, c.hidden, g.BN);
     } else if (part == 1) {
         mtiles = (c.shared_inter + BM - 1) / BM;
+        g.BN = pick_bn(T, mtiles, h.sm_count);
         g.KT = c.hidden / BK;
         ok = tc::make_map_bf16_sw128(&a0, w.sh_w1, c.shared_inter, c.hidden, c.hidden, BM) &&
              tc::make_map_bf16_sw128(&a1, w.sh_w3, c.shared_inter, c.hidden, c.hidden, BM) &&
              tc::make_map_bf16_sw128(&b, x, T, c.hidden, c.hidden, g.BN);
     } else {
         mtiles = (c.hidden + BM - 1) / BM;
+        g.BN = pick_bn(T, mtiles, h.sm_count);
         g.KTA = c.latent / BK;
         g.KT = (c.latent + c.shared_inter) / BK;
         ok = tc::make_map_bf16_sw128(&a0, w.up_w, c.hidden, c.latent, c.latent, BM) &&
