@@ -496,6 +496,7 @@ int k3moe_load_layer(k3moe *h, int layer, const k3moe_layer_weights *w)
     L.w1max = w1m;
     L.w3max = w3m;
     L.w2max = w2m;
+    if (dense_tma_fits(c, 1)) build_dense_tma_maps(c, L);   // else the maps are never used
     L.loaded = true;
     free_layer(h->layers[(size_t)layer]);
     h->layers[(size_t)layer] = L;
@@ -555,6 +556,23 @@ int k3moe_forward_host(k3moe *h, int layer, const void *x_host, void *y_host, in
     if (cudaSetDevice(h->cfg.device) != cudaSuccess) return K3MOE_ERR_CUDA;
     cudaStream_t s = (cudaStream_t)stream;
     const size_t nb = (size_t)T * h->cfg.hidden * 2;
+    // One or two tokens run the TMA-fed decode GEMVs, whose last kernel writes
+    // each output element once with a plain store: a pinned (device-mapped) y
+    // is written in place, saving the copy back. (x stays a copy: every CTA
+    // of the first kernels stages all of it.)
+    if (T <= 2 && h->dense_tma_ok[T - 1]) {
+        cudaPointerAttributes ay{};
+        if (cudaPointerGetAttributes(&ay, y_host) == cudaSuccess && ay.type == cudaMemoryTypeHost &&
+            ay.devicePointer) {
+            if (cudaMemcpyAsync(h->ws.xbuf0, x_host, nb, cudaMemcpyHostToDevice, s) != cudaSuccess)
+                return K3MOE_ERR_CUDA;
+            const int rc =
+                run_layer(h, h->layers[(size_t)layer], h->ws.xbuf0, (__nv_bfloat16 *)ay.devicePointer, T, s);
+            if (rc != K3MOE_OK) return rc;
+            return cudaStreamSynchronize(s) == cudaSuccess ? K3MOE_OK : K3MOE_ERR_CUDA;
+        }
+        cudaGetLastError();   // pageable y: the copy path below
+    }
     if (cudaMemcpyAsync(h->ws.xbuf0, x_host, nb, cudaMemcpyHostToDevice, s) != cudaSuccess)
         return K3MOE_ERR_CUDA;
     int rc = run_layer(h, h->layers[(size_t)layer], h->ws.xbuf0, h->ws.xbuf1, T, s);

@@ -23,6 +23,7 @@
 // row (or pair) per consumer warp over the whole K; units are split evenly and
 // contiguously over the CTAs.
 #include <algorithm>
+#include <cstring>
 
 #include "decode_common.cuh"
 #include "tc_common.cuh"
@@ -347,6 +348,33 @@ static bool make_row_maps(RowMaps *m, const void *base, int rows, int cols)
            tc::make_map_bf16_rows(&m->m1, base, rows, cols, kPieceBlocks, 1);
 }
 
+static bool make_dense_maps(const k3moe_config &c, const LayerDev &w, int part, DenseMaps *mp)
+{
+    if (part == 0)
+        return make_row_maps(&mp->a, w.router_w, c.n_experts, c.hidden) &&
+               make_row_maps(&mp->b, w.down_w, c.latent, c.hidden);
+    if (part == 1)
+        return make_row_maps(&mp->a, w.sh_w1, c.shared_inter, c.hidden) &&
+               make_row_maps(&mp->b, w.sh_w3, c.shared_inter, c.hidden);
+    return make_row_maps(&mp->a, w.up_w, c.hidden, c.latent) &&
+           make_row_maps(&mp->b, w.sh_w2, c.hidden, c.shared_inter);
+}
+
+static_assert(sizeof(DenseMaps) == 6 * sizeof(CUtensorMap), "six maps per part");
+
+// The maps of a loaded layer depend only on its weight pointers: built once.
+bool build_dense_tma_maps(const k3moe_config &c, LayerDev &w)
+{
+    w.dense_maps_ok = false;
+    for (int part = 0; part < 3; part++) {
+        DenseMaps mp;
+        if (!make_dense_maps(c, w, part, &mp)) return false;
+        memcpy(w.dense_maps[part], &mp, sizeof(mp));
+    }
+    w.dense_maps_ok = true;
+    return true;
+}
+
 cudaError_t init_dense_tma(const k3moe_config &c)
 {
     (void)c;
@@ -402,17 +430,8 @@ cudaError_t launch_dense_tma(const k3moe &h, const LayerDev &w, const __nv_bfloa
         a.units = c.hidden;
     }
     DenseMaps mp;
-    bool ok;
-    if (part == 0)
-        ok = make_row_maps(&mp.a, w.router_w, c.n_experts, c.hidden) &&
-             make_row_maps(&mp.b, w.down_w, c.latent, c.hidden);
-    else if (part == 1)
-        ok = make_row_maps(&mp.a, w.sh_w1, c.shared_inter, c.hidden) &&
-             make_row_maps(&mp.b, w.sh_w3, c.shared_inter, c.hidden);
-    else
-        ok = make_row_maps(&mp.a, w.up_w, c.hidden, c.latent) &&
-             make_row_maps(&mp.b, w.sh_w2, c.hidden, c.shared_inter);
-    if (!ok) return cudaErrorInvalidValue;
+    if (w.dense_maps_ok) memcpy(&mp, w.dense_maps[part], sizeof(mp));
+    else if (!make_dense_maps(c, w, part, &mp)) return cudaErrorInvalidValue;
     const int TB = T == 1 ? 1 : 2;
     a.ns = stages_for(a.mode, a.K, TB);
     const int groups = (a.units + kCW - 1) / kCW;

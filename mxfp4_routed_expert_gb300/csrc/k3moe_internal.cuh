@@ -2,6 +2,7 @@
 // launchers and small device helpers shared by the kernel files.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -43,6 +44,10 @@ struct LayerDev {
     // largest scale byte of each expert row (tensor-core expert GEMM operand rebasing)
     const uint8_t *w1max = nullptr, *w3max = nullptr;   // [E][I]
     const uint8_t *w2max = nullptr;                     // [E][L]
+    // row tensor maps of the dense decode GEMVs (router+down, shared gate/up,
+    // up+shared down; six each), built once at load
+    CUtensorMap dense_maps[3][6];
+    bool dense_maps_ok = false;
 };
 
 // Per-handle scratch, sized for max_tokens (Tm).
@@ -151,6 +156,7 @@ cudaError_t launch_gather_latent(const k3moe &h, int T, cudaStream_t s);
 cudaError_t launch_expert_gemm(const k3moe &h, const LayerDev &w, int T, cudaStream_t s, bool w13);
 cudaError_t launch_row_scale_max(const uint8_t *s, size_t rows, int G, uint8_t *out);
 bool dense_tma_fits(const k3moe_config &c, int TB);
+bool build_dense_tma_maps(const k3moe_config &c, LayerDev &w);
 // TMA-fed dense GEMVs for T <= 2. part 0: router + down; 1: shared gate/up;
 // 2: latent norm + up + shared down.
 cudaError_t launch_dense_tma(const k3moe &h, const LayerDev &w, const __nv_bfloat16 *x,

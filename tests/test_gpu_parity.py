@@ -229,6 +229,36 @@ def test_forward_host_matches_device_forward():
     assert np.all(np.abs(a - b) <= np.abs(b) * 2.0 ** -7 + 1e-30)
 
 
+@pytest.mark.parametrize("T", [1, 2])
+@pytest.mark.parametrize("pinned", [True, False])
+def test_forward_host_single_tokens(T, pinned):
+    """One or two tokens through host buffers: a pinned y is written in place by
+    the last decode kernel, a pageable one is copied back; both match the device
+    forward."""
+    import torch
+    import mxfp4_routed_expert_gb300 as km
+    shape = MID
+    d = k3synth.make_layer(shape, 15, 0, k3synth.TINY_RECIPE)
+    x, _ = guarded_tokens(shape, d, 15, T)
+    lay = Layer(shape, [d], max_tokens=2)
+    try:
+        y_dev = lay.forward(x)
+        if pinned:
+            xh = torch.from_numpy(x.view(np.int16).copy()).pin_memory()
+            yh = torch.full((T, shape.hidden), -1, dtype=torch.int16).pin_memory()
+            km.k3moe_forward_host(lay.h, 0, xh, yh, T)
+            y_host = yh.numpy().view(np.uint16)
+        else:
+            y_host = np.empty_like(x)
+            km.k3moe_forward_host(lay.h, 0, x, y_host, T)
+        assert km.k3moe_sync_status(lay.h) == 0
+    finally:
+        lay.close()
+    a, b = bf16_to_f64(y_host), bf16_to_f64(y_dev)
+    assert np.all(np.abs(a - b) <= np.abs(b) * 2.0 ** -7 + 1e-30)
+    assert_close(a, oracle.layer_forward(shape, d, x), f"host buffers T={T}")
+
+
 def test_routing_is_deterministic_and_profiling_lists_kernels():
     import mxfp4_routed_expert_gb300 as km
     shape = MID
