@@ -145,8 +145,8 @@ K3MOE_API int k3moe_forward_chain(k3moe *h, int first_layer, int n_layers, const
 
 /* k3moe_forward with HOST buffers: copies x to the device, runs the layer,
  * copies y back and synchronises `stream`. Pinned host memory is faster but
- * not required; for T <= 2 a pinned (device-mapped) y is written in place by
- * the last kernel, without a copy back. */
+ * not required; a pinned (device-mapped) y is written in place by the
+ * layer's last kernel, without a copy back. */
 K3MOE_API int k3moe_forward_host(k3moe *h, int layer, const void *x_host, void *y_host, int T,
                        void *stream);
 

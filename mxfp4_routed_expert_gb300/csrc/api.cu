@@ -556,11 +556,10 @@ int k3moe_forward_host(k3moe *h, int layer, const void *x_host, void *y_host, in
     if (cudaSetDevice(h->cfg.device) != cudaSuccess) return K3MOE_ERR_CUDA;
     cudaStream_t s = (cudaStream_t)stream;
     const size_t nb = (size_t)T * h->cfg.hidden * 2;
-    // One or two tokens run the TMA-fed decode GEMVs, whose last kernel writes
-    // each output element once with a plain store: a pinned (device-mapped) y
-    // is written in place, saving the copy back. (x stays a copy: every CTA
-    // of the first kernels stages all of it.)
-    if (T <= 2 && h->dense_tma_ok[T - 1]) {
+    // The layer's last kernel writes each output element once with a plain
+    // store: a pinned (device-mapped) y is written in place, saving the copy
+    // back. (x stays a copy: the first kernels read it from many CTAs.)
+    {
         cudaPointerAttributes ay{};
         if (cudaPointerGetAttributes(&ay, y_host) == cudaSuccess && ay.type == cudaMemoryTypeHost &&
             ay.devicePointer) {

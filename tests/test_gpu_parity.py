@@ -229,18 +229,19 @@ def test_forward_host_matches_device_forward():
     assert np.all(np.abs(a - b) <= np.abs(b) * 2.0 ** -7 + 1e-30)
 
 
-@pytest.mark.parametrize("T", [1, 2])
+@pytest.mark.parametrize("shape_T", [("mid", 1), ("mid", 2), ("wide", 37)])
 @pytest.mark.parametrize("pinned", [True, False])
-def test_forward_host_single_tokens(T, pinned):
-    """One or two tokens through host buffers: a pinned y is written in place by
-    the last decode kernel, a pageable one is copied back; both match the device
-    forward."""
+def test_forward_host_buffers(shape_T, pinned):
+    """Host buffers at one or two tokens (decode GEMVs) and at 37 (tensor-core
+    GEMMs): a pinned y is written in place by the layer's last kernel, a
+    pageable one is copied back; both match the device forward."""
     import torch
     import mxfp4_routed_expert_gb300 as km
-    shape = MID
+    name, T = shape_T
+    shape = {"mid": MID, "wide": WIDE}[name]
     d = k3synth.make_layer(shape, 15, 0, k3synth.TINY_RECIPE)
     x, _ = guarded_tokens(shape, d, 15, T)
-    lay = Layer(shape, [d], max_tokens=2)
+    lay = Layer(shape, [d], max_tokens=T)
     try:
         y_dev = lay.forward(x)
         if pinned:
@@ -254,8 +255,10 @@ def test_forward_host_single_tokens(T, pinned):
         assert km.k3moe_sync_status(lay.h) == 0
     finally:
         lay.close()
+    # the fp32 atomics of the expert scatter-add vary their order between runs:
+    # the two outputs agree to a bf16 unit of the output's scale
     a, b = bf16_to_f64(y_host), bf16_to_f64(y_dev)
-    assert np.all(np.abs(a - b) <= np.abs(b) * 2.0 ** -7 + 1e-30)
+    assert np.max(np.abs(a - b)) <= np.max(np.abs(b)) * 2.0 ** -7
     assert_close(a, oracle.layer_forward(shape, d, x), f"host buffers T={T}")
 
 
