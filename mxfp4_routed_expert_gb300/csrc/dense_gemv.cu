@@ -173,6 +173,10 @@ __global__ void __launch_bounds__(kGemvWarps * 32) k_dense_x(DenseXArgs a)
         }
         __syncthreads();
     }
+    // Without the dependency wait at the start, wait before exiting: the next
+    // kernel waits only for this one, whose completion must imply that of
+    // every earlier kernel of the forward.
+    if (!a.wait && threadIdx.x == 0) pdl_wait();
 }
 
 struct UpArgs {

@@ -19,7 +19,8 @@
 // programmatic-launch wait on the previous kernel (weights do not depend on
 // it) while the consumers wait and then stage the activations. Router+down,
 // a layer's first kernel, is launched in plain stream order; the shared
-// gate/up, which reads only the layer input, then needs no wait at all. A unit is one
+// gate/up, which reads only the layer input, waits only before it exits (so
+// that its completion implies its predecessors'). A unit is one
 // row (or pair) per consumer warp over the whole K; units are split evenly and
 // contiguously over the CTAs.
 #include <algorithm>
@@ -315,6 +316,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_dense_tma(const __grid_constant
             }
         }
     }
+    // A kernel that skipped its dependency wait still waits before it exits:
+    // the next kernel waits only for this one, and this one's completion must
+    // imply that of every earlier kernel of the forward.
+    if (!a.wait && threadIdx.x == 0) pdl_wait();
 }
 
 // Stages that fit beside the activations, at most 8.

@@ -323,7 +323,10 @@ __device__ __forceinline__ uint64_t l2_policy_evict_last()
 // ---- programmatic dependent launch ----------------------------------------------
 // Every kernel of a forward lets the next one start launching at once, and
 // waits for the previous one to finish (and flush) before it reads anything
-// that kernel wrote.
+// that kernel wrote. The wait covers only the immediately preceding kernel,
+// so a kernel whose inputs need no wait (it reads only the layer input)
+// still waits before it exits: every kernel's completion then implies the
+// completion of all earlier kernels of the stream.
 __device__ __forceinline__ void pdl_launch_dependents()
 {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
