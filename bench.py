@@ -1,7 +1,7 @@
 """Throughput of the K3 LatentMoE layer on GB300 (one JSON line on stdout).
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
-                [--workload decode_t1|decode_t64|prefill_t4096|chain8_t256]
+                [--workload decode_t1|decode_t64|prefill_t4096|chain8_t256|decode_t1_tier|...]
 
 A step is one forward of the whole layer (router, permutation, routed
 experts, latent norm, up projection and shared experts) over one batch of
@@ -65,7 +65,19 @@ WORKLOADS = {
                           "(16 pairs per expert; small case for profiler captures)"),
     "prefill_t512_e64": dict(T=512, layers=1, desc="K3 row shapes with 64 routed experts, T=512 "
                              "(128 pairs per expert; small case for profiler captures)"),
+    # expert tier: routed experts in pinned host memory, 896 device slots
+    # shared by two layers; each step is one forward of one layer (alternating)
+    "decode_t1_tier": dict(T=1, layers=2, tier=896, alternate=True,
+                           desc="two K3-shape layers with their routed experts in host memory "
+                                "and 896 device slots (expert tier); decode T=1, steps alternate "
+                                "layers, tokens from a seeded pool of 2048"),
+    "decode_t64_tier": dict(T=64, layers=2, tier=896, alternate=True,
+                            desc="two K3-shape layers with their routed experts in host memory "
+                                 "and 896 device slots (expert tier); T=64 covering construction "
+                                 "(all 896 experts per forward), steps alternate layers, so every "
+                                 "forward copies in all of its experts"),
 }
+TIER_POOL = 2048
 
 
 def measured_peaks():
@@ -142,6 +154,7 @@ def kernel_model(shape, T, n_touched):
         "norm_up_shared_gemv": (up[0] - 2 * T * (L + S) + 4 * T * (L + S) + 2 * L, 0),
         "up_shared_gemm": up,
         "chain_glue_rmsnorm": (4 * T * H, 0),
+        "tier_plan": (0, 0), "tier_fill": (0, 0),   # set from the tier's counters
     }
 
 
@@ -164,7 +177,9 @@ def make_inputs(workload, seed=0, layer_index=0):
     T = WORKLOADS[workload]["T"]
     if workload in ("decode_t1", "decode_t1_e64"):
         x = k3synth.make_tokens(shape, seed, POOL, stream=7)
-    elif workload == "decode_t64":
+    elif workload == "decode_t1_tier":
+        x = k3synth.make_tokens(shape, seed, TIER_POOL, stream=17)
+    elif workload in ("decode_t64", "decode_t64_tier"):
         d = k3synth.with_bias(d, np.zeros(shape.n_experts, np.float32))
         x = k3synth.covering_tokens(shape, d, seed, T)
     elif workload == "prefill_t4096":
@@ -259,6 +274,23 @@ def traffic_for(kernel, workload):
     return ent["bytes_per_launch"]
 
 
+def host_link_gbs():
+    """Pinned host -> device copy bandwidth (1 GiB, best of 3, CUDA events)."""
+    import torch
+    src = torch.empty(1 << 30, dtype=torch.uint8).pin_memory()
+    dst = torch.empty(1 << 30, dtype=torch.uint8, device="cuda")
+    best = 0.0
+    for _ in range(3):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        dst.copy_(src, non_blocking=True)
+        b.record()
+        torch.cuda.synchronize()
+        best = max(best, src.numel() / (a.elapsed_time(b) / 1e3) / 1e9)
+    del src, dst
+    return round(best, 1)
+
+
 # ---- oracle timing (CPU baseline and reference arm) ----------------------------------
 
 def time_oracle(shape, d, x, n_tokens):
@@ -292,25 +324,37 @@ def run_native(args, rank, world):
     h = km.k3moe_create(km.make_config(shape, max_layers=n_layers, max_tokens=T, device=dev))
     km.k3moe_set_expert_path(h, {"auto": km.K3MOE_EXPERT_AUTO, "gemv": km.K3MOE_EXPERT_GEMV,
                                  "gemm": km.K3MOE_EXPERT_GEMM}[args.expert_path])
+    alternate = wl.get("alternate", False)   # one layer per step, layers in turn (else a chain)
+    if wl.get("tier"):
+        km.k3moe_set_expert_tier(h, wl["tier"])
     w, keep = km.layer_weights(d0, shape.n_experts, km.K3MOE_HOST)
     km.k3moe_load_layer(h, 0, w)
     del keep
     oracle_layer = d0
+    xpools = [xpool]
     for li in range(1, n_layers):
-        _, dl, _ = make_inputs(args.workload, layer_index=li)
+        _, dl, xl = make_inputs(args.workload, layer_index=li)
         w, keep = km.layer_weights(dl, shape.n_experts, km.K3MOE_HOST)
         km.k3moe_load_layer(h, li, w)
+        xpools.append(xl)
         del keep, dl
+    if not alternate:
+        xpools = xpools[:1]
 
-    xs = torch.from_numpy(xpool.view(np.int16).copy()).cuda()
-    npool = xs.shape[0] // T
+    xs = [torch.from_numpy(xp.view(np.int16).copy()).cuda() for xp in xpools]
+    npool = xs[0].shape[0] // T
     y = torch.empty((T, shape.hidden), dtype=torch.int16, device="cuda")
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     counts_log = torch.empty((args.steps, shape.n_experts), dtype=torch.int32, device="cuda")
     stream = torch.cuda.current_stream()
 
     def fwd(i):
-        xi = xs[(i % npool) * T:(i % npool) * T + T]
+        if alternate:
+            li = i % n_layers
+            j = (i // n_layers) % npool
+            km.k3moe_forward(h, li, xs[li][j * T:j * T + T], y, T, stream)
+            return
+        xi = xs[0][(i % npool) * T:(i % npool) * T + T]
         if n_layers > 1:
             km.k3moe_forward_chain(h, 0, n_layers, xi, y, T, stream)
         else:
@@ -347,11 +391,13 @@ def run_native(args, rank, world):
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
+    tier0 = km.k3moe_get_tier_stats(h) if wl.get("tier") else None
     clocks.start()
     total_ms, _, step_times = timed_pass(False)
     if world > 1:
         torch.distributed.barrier()
     clk = clocks.stop()
+    tier1 = km.k3moe_get_tier_stats(h) if wl.get("tier") else None
     # pass 2: the same steps with every kernel bracketed by CUDA events on its
     # launching stream (per-kernel durations for the roofline)
     prof_ms, stats, _ = timed_pass(True)
@@ -368,13 +414,35 @@ def run_native(args, rank, world):
     n_touched = float(touched.mean())
     hbm_peak, bf16_peak, bf16_sust, peak_src = measured_peaks()
     model = kernel_model(shape, T, n_touched)
+    tier = None
+    if wl.get("tier"):
+        tier2 = km.k3moe_get_tier_stats(h)   # after the profiled pass: its own counts
+        fill_per_step = (tier2["bytes_filled"] - tier1["bytes_filled"]) / args.steps
+        model["tier_fill"] = (2 * fill_per_step, 0)   # read over the host link, written to HBM
+        d = {k: tier1[k] - tier0[k] for k in ("hits", "misses", "bytes_filled")}
+        link = host_link_gbs()
+        tier = {"slots": tier1["slots"], "hits": d["hits"], "misses": d["misses"],
+                "hit_rate": round(d["hits"] / max(1, d["hits"] + d["misses"]), 4),
+                "bytes_filled_per_step": int(d["bytes_filled"] / args.steps),
+                "host_link_copy_gbs": link}
     by_name = {n: (l, ms) for n, l, ms in stats}
     ranked = sorted(((ms, n) for n, (l, ms) in by_name.items()), reverse=True)
     dom = ranked[0][1]
     launches, dom_ms = by_name[dom]
     avg_ms = dom_ms / launches
-    roof = roofline(dom, model.get(dom), avg_ms, hbm_peak, bf16_sust, peak_src, args.workload)
-    step_bytes = layer_bytes(shape, T, n_touched) * n_layers
+    if dom == "tier_fill":
+        # the copy of missed experts reads host memory over the host link
+        gbs = (model["tier_fill"][0] / 2) / (avg_ms / 1e3) / 1e9
+        roof = {"kernel": dom, "bound": "host_link", "achieved": round(gbs, 1),
+                "peak": tier["host_link_copy_gbs"], "unit": "GB/s",
+                "frac": round(gbs / tier["host_link_copy_gbs"], 4),
+                "peak_source": "pinned host -> device copy measured in this run", "traffic": None,
+                "alg_bytes_per_launch": int(model["tier_fill"][0] / 2), "flops_per_launch": 0,
+                "avg_launch_ms": round(avg_ms, 5)}
+    else:
+        roof = roofline(dom, model.get(dom), avg_ms, hbm_peak, bf16_sust, peak_src, args.workload)
+    layers_per_step = 1 if alternate else n_layers
+    step_bytes = layer_bytes(shape, T, n_touched) * layers_per_step
     layer_gbs = step_bytes / (ms_per_step / 1e3) / 1e9
     kernels = {}
     for n, (l, ms) in by_name.items():
@@ -413,11 +481,11 @@ def run_native(args, rank, world):
         n_tok = 320                      # about 10-20 s of the oracle on the machine's cores
         xs_host = xpool if T == 1 else xpool[:T]
         nrow, dt = time_oracle(shape, oracle_layer, xs_host, n_tok)
-        cpu = {"value": round(nrow / dt / n_layers, 4), "unit": UNIT,
+        cpu = {"value": round(nrow / dt / layers_per_step, 4), "unit": UNIT,
                "cores": omp_threads(nrow), "kind": "oracle",
                "sample": f"{nrow} token rows of the workload ({min(nrow, xs_host.shape[0])} distinct) "
                          f"through one layer (fp64 C oracle, OpenMP over tokens), {dt:.1f} s"
-                         + ("; chain value = per-layer rate / 8" if n_layers > 1 else "")}
+                         + (f"; chain value = per-layer rate / {n_layers}" if layers_per_step > 1 else "")}
     km.k3moe_destroy(h)
     if rank != 0:
         return None
@@ -439,6 +507,7 @@ def run_native(args, rank, world):
                     "p90": round(float(np.percentile(step_times, 90)), 5)},
         "roofline": roof, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": gpu_launches, "clocks": clk,
+        **({"tier": tier} if tier else {}),
     }
 
 
@@ -471,7 +540,7 @@ def run_reference(args, rank, world):
         "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "kind": "oracle",
                          "cores": cores,
                          "sample": f"{per} token(s) per step through one layer (fp64 C oracle)"
-                                   + ("; chain value = per-layer rate / 8" if n_layers > 1 else "")},
+                                   + (f"; chain value = per-layer rate / {n_layers}" if layers_per_step > 1 else "")},
         "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }

@@ -189,6 +189,45 @@ K3MOE_API int k3moe_sync_status(k3moe *h);
 enum { K3MOE_EXPERT_AUTO = 0, K3MOE_EXPERT_GEMV = 1, K3MOE_EXPERT_GEMM = 2 };
 K3MOE_API int k3moe_set_expert_path(k3moe *h, int mode);
 
+/* ---- Expert tier: host memory holds the routed experts, device slots cache them
+ * (kimi-k3-in-c README, Part II section 12, "An LRU cache for the experts";
+ * host memory over NVLink-C2C takes the place of the pages' disk, device
+ * memory that of their RAM). For a pool of layers whose routed experts do not
+ * all fit in device memory.
+ *
+ * k3moe_set_expert_tier must come before the first k3moe_load_layer. With
+ * slots > 0, every layer loaded afterwards keeps its routed-expert tensors
+ * (packed nibbles, scales, and the largest scale byte of each row) in one
+ * pinned, device-mapped host block that the library allocates and owns; its
+ * router, projections and shared experts stay in device memory. The handle
+ * keeps `slots` expert slots in device memory (slots * ~17.56 MB at K3 size),
+ * shared by all layers. Every forward, after routing, one kernel stamps the
+ * slots of the touched experts already resident (hits) and gives each other
+ * touched expert (miss) a slot that this forward does not use: a free one
+ * first, else the one used longest ago (equal age: the lower slot); a second
+ * kernel copies the missed experts from the host block into their slots; the
+ * expert kernels then read the slots. The host takes no part (no
+ * synchronisation, no copy calls). Results are those of the resident layer.
+ * slots must be >= n_experts (the most one forward touches) and <= 16384;
+ * slots = 0 turns the tier off. Reloading a tiered layer frees its slots.
+ * Errors: K3MOE_ERR_INVALID_ARG (NULL handle, a layer already loaded, slots
+ * out of range), K3MOE_ERR_SHAPE (an expert array of a size not a multiple of
+ * 16 bytes), K3MOE_ERR_OOM (the slots do not fit in free device memory; a
+ * later load_layer returns it when the host block cannot be pinned),
+ * K3MOE_ERR_CUDA. */
+K3MOE_API int k3moe_set_expert_tier(k3moe *h, int slots);
+
+typedef struct {
+    int32_t struct_size;    /* sizeof(k3moe_tier_stats), set by the caller */
+    int32_t slots;          /* 0: tier off */
+    int64_t hits;           /* touched experts found resident, summed over forwards */
+    int64_t misses;         /* touched experts copied in */
+    int64_t bytes_filled;   /* bytes those copies moved from host to device memory */
+} k3moe_tier_stats;
+/* Synchronises the device and reads the tier's counters (cumulative since
+ * k3moe_set_expert_tier). K3MOE_ERR_INVALID_ARG for NULL or a wrong struct_size. */
+K3MOE_API int k3moe_get_tier_stats(k3moe *h, k3moe_tier_stats *out);
+
 /* Per-kernel timing: with profiling on, every kernel a forward launches is
  * bracketed by CUDA events on the launching stream. k3moe_profile_read
  * synchronises, aggregates per kernel name and resets the record. */

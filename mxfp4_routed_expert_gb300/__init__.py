@@ -36,7 +36,8 @@ K3MOE_T_Z, K3MOE_T_ACC, K3MOE_T_SHARED, K3MOE_T_LOGITS = 1, 2, 3, 4
 EXPORTS = ("k3moe_create", "k3moe_load_layer", "k3moe_forward", "k3moe_forward_chain",
            "k3moe_forward_host", "k3moe_get_routing", "k3moe_get_intermediate",
            "k3moe_sync_status", "k3moe_set_profiling", "k3moe_profile_read", "k3moe_destroy",
-           "k3moe_strerror", "k3moe_abi_version", "k3moe_route_static", "k3moe_set_expert_path")
+           "k3moe_strerror", "k3moe_abi_version", "k3moe_route_static", "k3moe_set_expert_path",
+           "k3moe_set_expert_tier", "k3moe_get_tier_stats")
 K3MOE_ROUTE_STATIC_MAX_LOGITS = 1 << 20
 K3MOE_EXPERT_AUTO, K3MOE_EXPERT_GEMV, K3MOE_EXPERT_GEMM = 0, 1, 2
 
@@ -69,6 +70,12 @@ class k3moe_layer_weights(ctypes.Structure):
                 ("shared_w3", ctypes.c_void_p), ("shared_w2", ctypes.c_void_p),
                 ("w1_packed", _PP), ("w1_scale", _PP), ("w3_packed", _PP), ("w3_scale", _PP),
                 ("w2_packed", _PP), ("w2_scale", _PP)]
+
+
+class k3moe_tier_stats(ctypes.Structure):
+    _fields_ = [("struct_size", ctypes.c_int32), ("slots", ctypes.c_int32),
+                ("hits", ctypes.c_int64), ("misses", ctypes.c_int64),
+                ("bytes_filled", ctypes.c_int64)]
 
 
 class k3moe_kernel_stat(ctypes.Structure):
@@ -106,6 +113,8 @@ def lib():
         L.k3moe_strerror.restype = ctypes.c_char_p
         L.k3moe_abi_version.restype = i
         L.k3moe_route_static.argtypes = [vp, vp, vp, i, i, i, i, i, ctypes.c_float, vp, vp, vp]
+        L.k3moe_set_expert_tier.argtypes = [vp, i]
+        L.k3moe_get_tier_stats.argtypes = [vp, ctypes.POINTER(k3moe_tier_stats)]
         for n in EXPORTS:
             if n not in ("k3moe_destroy", "k3moe_strerror"):
                 getattr(L, n).restype = i if n != "k3moe_destroy" else None
@@ -254,6 +263,21 @@ def k3moe_set_expert_path(h: int, mode: int) -> int:
     """K3MOE_EXPERT_AUTO / _GEMV / _GEMM: which routed-expert kernels forwards use."""
     return _check(lib().k3moe_set_expert_path(ctypes.c_void_p(h), int(mode)),
                   "k3moe_set_expert_path")
+
+
+def k3moe_set_expert_tier(h: int, slots: int) -> int:
+    """Host memory holds the routed experts of layers loaded afterwards; `slots`
+    device slots cache them (0: off). Call before the first k3moe_load_layer."""
+    return _check(lib().k3moe_set_expert_tier(ctypes.c_void_p(h), int(slots)),
+                  "k3moe_set_expert_tier")
+
+
+def k3moe_get_tier_stats(h: int) -> dict:
+    """Cumulative expert-tier counters: slots, hits, misses, bytes_filled."""
+    st = k3moe_tier_stats()
+    st.struct_size = ctypes.sizeof(k3moe_tier_stats)
+    _check(lib().k3moe_get_tier_stats(ctypes.c_void_p(h), ctypes.byref(st)), "k3moe_get_tier_stats")
+    return dict(slots=st.slots, hits=st.hits, misses=st.misses, bytes_filled=st.bytes_filled)
 
 
 def k3moe_profile_read(h: int, max_entries: int = 32):

@@ -94,6 +94,8 @@ size_t carve_workspace(const k3moe_config &c, char *base, Workspace *ws)
 
 struct LayerSizes {
     size_t router, bias, down, up, gain, sh13, sh2, e13p, e13s, e2p, e2s, e13m, e2m;
+    size_t dense;     // bf16 weights, bias and gain
+    size_t experts;   // the nine routed-expert arrays
     size_t total;
 };
 
@@ -114,9 +116,11 @@ LayerSizes layer_sizes(const k3moe_config &c)
     z.e2s = E * L * (I / kGroup);
     z.e13m = E * I;
     z.e2m = E * L;
-    z.total = al256(z.router) + al256(z.bias) + al256(z.down) + al256(z.up) + al256(z.gain) +
-              2 * al256(z.sh13) + al256(z.sh2) + 2 * al256(z.e13p) + 2 * al256(z.e13s) +
-              al256(z.e2p) + al256(z.e2s) + 2 * al256(z.e13m) + al256(z.e2m);
+    z.dense = al256(z.router) + al256(z.bias) + al256(z.down) + al256(z.up) + al256(z.gain) +
+              2 * al256(z.sh13) + al256(z.sh2);
+    z.experts = 2 * al256(z.e13p) + 2 * al256(z.e13s) + al256(z.e2p) + al256(z.e2s) +
+                2 * al256(z.e13m) + al256(z.e2m);
+    z.total = z.dense + z.experts;
     return z;
 }
 
@@ -200,6 +204,7 @@ int run_layer(k3moe *h, const LayerDev &w, const __nv_bfloat16 *x, __nv_bfloat16
               cudaStream_t s)
 {
     cudaError_t e;
+    const bool tier = h->tier.slots > 0;
 #define K3_STEP(name, call)                        \
     {                                              \
         Prof p_(h, name, s);                       \
@@ -233,6 +238,12 @@ int run_layer(k3moe *h, const LayerDev &w, const __nv_bfloat16 *x, __nv_bfloat16
         K3_STEP("router_down_gemv", tma ? launch_dense_tma(*h, w, x, nullptr, T, s, 0)
                                         : launch_dense_x(*h, w, x, T, s, 0));
         K3_STEP("route_topk", launch_route(*h, w, T, s));
+        if (tier && T == 1) {
+            // the copy of missed experts over the host link overlaps the
+            // shared experts' HBM stream, which launches behind it
+            K3_STEP("tier_plan", launch_tier_plan(*h, w.index, s));
+            K3_STEP("tier_fill", launch_tier_fill(*h, w, s));
+        }
         K3_STEP("shared_gate_up_gemv", tma ? launch_dense_tma(*h, w, x, nullptr, T, s, 1)
                                            : launch_dense_x(*h, w, x, T, s, 1));
     }
@@ -240,6 +251,10 @@ int run_layer(k3moe *h, const LayerDev &w, const __nv_bfloat16 *x, __nv_bfloat16
         K3_STEP("perm_count", launch_perm(*h, T, s, 0));
         K3_STEP("perm_scan", launch_perm(*h, T, s, 1));
         K3_STEP("perm_place", launch_perm(*h, T, s, 2));
+        if (tier) {
+            K3_STEP("tier_plan", launch_tier_plan(*h, w.index, s));
+            K3_STEP("tier_fill", launch_tier_fill(*h, w, s));
+        }
     }
     if (gemm && cudaStreamWaitEvent(s, h->ev_join, 0) != cudaSuccess) return K3MOE_ERR_CUDA;
     if (egemm) {
@@ -272,7 +287,14 @@ bool overlap(const void *a, size_t na, const void *b, size_t nb)
 void free_layer(LayerDev &l)
 {
     if (l.block) cudaFree(l.block);
+    if (l.host_block) cudaFreeHost(l.host_block);
     l = LayerDev();
+}
+
+void free_tier(k3::TierDev &t)
+{
+    if (t.block) cudaFree(t.block);
+    t = k3::TierDev();
 }
 
 }  // namespace
@@ -370,6 +392,7 @@ void k3moe_destroy(k3moe *h)
     if (!h) return;
     cudaSetDevice(h->cfg.device);
     for (auto &l : h->layers) free_layer(l);
+    free_tier(h->tier);
     if (h->ws.block) cudaFree(h->ws.block);
     for (auto &r : h->prof) {
         cudaEventDestroy(r.a);
@@ -404,17 +427,37 @@ int k3moe_load_layer(k3moe *h, int layer, const k3moe_layer_weights *w)
     if (cudaSetDevice(c.device) != cudaSuccess) return K3MOE_ERR_CUDA;
 
     const LayerSizes z = layer_sizes(c);
+    // Expert tier: the routed experts go to one pinned, device-mapped host
+    // block and reach the device through the slots; else all of the layer
+    // lives in device memory.
+    const bool tiered = h->tier.slots > 0;
+    const size_t dev_bytes = tiered ? z.dense : z.total;
     size_t fr = 0, tot = 0;
     if (cudaMemGetInfo(&fr, &tot) != cudaSuccess) return K3MOE_ERR_CUDA;
-    if (z.total + (256u << 20) > fr) return K3MOE_ERR_OOM;   // checked before any allocation
+    if (dev_bytes + (256u << 20) > fr) return K3MOE_ERR_OOM;   // checked before any allocation
     void *blk = nullptr;
-    if (cudaMalloc(&blk, z.total) != cudaSuccess) {
+    if (cudaMalloc(&blk, dev_bytes) != cudaSuccess) {
         cudaGetLastError();
         return K3MOE_ERR_OOM;
     }
+    void *hblk = nullptr, *hdev = nullptr;
+    if (tiered) {
+        if (cudaHostAlloc(&hblk, z.experts, cudaHostAllocMapped) != cudaSuccess) {
+            cudaGetLastError();
+            cudaFree(blk);
+            return K3MOE_ERR_OOM;
+        }
+        if (cudaHostGetDevicePointer(&hdev, hblk, 0) != cudaSuccess) {
+            cudaGetLastError();
+            cudaFreeHost(hblk);
+            cudaFree(blk);
+            return K3MOE_ERR_CUDA;
+        }
+    }
     LayerDev L;
     L.block = blk;
-    L.bytes = z.total;
+    L.bytes = dev_bytes;
+    L.index = layer;
     Carve cv{(char *)blk};
     __nv_bfloat16 *router = cv.take<__nv_bfloat16>(z.router / 2);
     float *bias = cv.take<float>(z.bias / 4);
@@ -424,59 +467,75 @@ int k3moe_load_layer(k3moe *h, int layer, const k3moe_layer_weights *w)
     __nv_bfloat16 *sh1 = cv.take<__nv_bfloat16>(z.sh13 / 2);
     __nv_bfloat16 *sh3 = cv.take<__nv_bfloat16>(z.sh13 / 2);
     __nv_bfloat16 *sh2 = cv.take<__nv_bfloat16>(z.sh2 / 2);
-    uint8_t *w1p = cv.take<uint8_t>(z.e13p), *w1s = cv.take<uint8_t>(z.e13s);
-    uint8_t *w3p = cv.take<uint8_t>(z.e13p), *w3s = cv.take<uint8_t>(z.e13s);
-    uint8_t *w2p = cv.take<uint8_t>(z.e2p), *w2s = cv.take<uint8_t>(z.e2s);
-    uint8_t *w1m = cv.take<uint8_t>(z.e13m), *w3m = cv.take<uint8_t>(z.e13m);
-    uint8_t *w2m = cv.take<uint8_t>(z.e2m);
+    // the nine expert arrays [E][...]: after the dense tensors, or in the host
+    // block (ex: where the copies go; exd: the same arrays as kernels see them)
+    const size_t asz[kTierPieces] = {z.e13p, z.e13s, z.e13p, z.e13s, z.e2p, z.e2s, z.e13m, z.e13m, z.e2m};
+    uint8_t *ex[kTierPieces], *exd[kTierPieces];
+    {
+        Carve ce{tiered ? (char *)hblk : (char *)blk, tiered ? 0 : z.dense};
+        Carve cd{tiered ? (char *)hdev : (char *)blk, tiered ? 0 : z.dense};
+        for (int p = 0; p < kTierPieces; p++) {
+            ex[p] = ce.take<uint8_t>(asz[p]);
+            exd[p] = cd.take<uint8_t>(asz[p]);
+        }
+    }
 
     const cudaMemcpyKind kind =
         w->where == K3MOE_HOST ? cudaMemcpyHostToDevice : cudaMemcpyDeviceToDevice;
+    // expert pieces: into device memory, or into the pinned host block
+    const cudaMemcpyKind ekind = tiered ? cudaMemcpyDefault : kind;
     int rc = K3MOE_OK;
     int *flag = h->ws.err + 2;   // scratch word for the scale scan
-#define K3_CP(dst, src, n)                                               \
-    if (rc == K3MOE_OK && cudaMemcpy((dst), (src), (n), kind) != cudaSuccess) \
+#define K3_CP(dst, src, n, k)                                             \
+    if (rc == K3MOE_OK && cudaMemcpy((dst), (src), (n), (k)) != cudaSuccess) \
         rc = K3MOE_ERR_CUDA;
-    K3_CP(router, w->router_w, z.router);
+    K3_CP(router, w->router_w, z.router, kind);
     if (w->router_bias) {
-        K3_CP(bias, w->router_bias, z.bias);
+        K3_CP(bias, w->router_bias, z.bias, kind);
     } else if (rc == K3MOE_OK && cudaMemset(bias, 0, z.bias) != cudaSuccess) {
         rc = K3MOE_ERR_CUDA;
     }
-    K3_CP(down, w->down_w, z.down);
-    K3_CP(up, w->up_w, z.up);
-    if (w->latent_gain) K3_CP(gain, w->latent_gain, z.gain);
-    K3_CP(sh1, w->shared_w1, z.sh13);
-    K3_CP(sh3, w->shared_w3, z.sh13);
-    K3_CP(sh2, w->shared_w2, z.sh2);
+    K3_CP(down, w->down_w, z.down, kind);
+    K3_CP(up, w->up_w, z.up, kind);
+    if (w->latent_gain) K3_CP(gain, w->latent_gain, z.gain, kind);
+    K3_CP(sh1, w->shared_w1, z.sh13, kind);
+    K3_CP(sh3, w->shared_w3, z.sh13, kind);
+    K3_CP(sh2, w->shared_w2, z.sh2, kind);
     const size_t pe13 = (size_t)c.moe_inter * (c.latent / 2), se13 = (size_t)c.moe_inter * (c.latent / kGroup);
     const size_t pe2 = (size_t)c.latent * (c.moe_inter / 2), se2 = (size_t)c.latent * (c.moe_inter / kGroup);
     for (int e = 0; e < c.n_experts && rc == K3MOE_OK; e++) {
-        K3_CP(w1p + e * pe13, w->w1_packed[e], pe13);
-        K3_CP(w1s + e * se13, w->w1_scale[e], se13);
-        K3_CP(w3p + e * pe13, w->w3_packed[e], pe13);
-        K3_CP(w3s + e * se13, w->w3_scale[e], se13);
-        K3_CP(w2p + e * pe2, w->w2_packed[e], pe2);
-        K3_CP(w2s + e * se2, w->w2_scale[e], se2);
+        K3_CP(ex[0] + e * pe13, w->w1_packed[e], pe13, ekind);
+        K3_CP(ex[1] + e * se13, w->w1_scale[e], se13, ekind);
+        K3_CP(ex[2] + e * pe13, w->w3_packed[e], pe13, ekind);
+        K3_CP(ex[3] + e * se13, w->w3_scale[e], se13, ekind);
+        K3_CP(ex[4] + e * pe2, w->w2_packed[e], pe2, ekind);
+        K3_CP(ex[5] + e * se2, w->w2_scale[e], se2, ekind);
     }
 #undef K3_CP
     if (rc == K3MOE_OK) {
+        // scale checks and row maxima read the arrays where they live (the
+        // host block through its device mapping in the tier)
         int bad = 0;
         if (cudaMemset(flag, 0, sizeof(int)) != cudaSuccess ||
-            launch_scale_scan(w1s, z.e13s, flag, 0) != cudaSuccess ||
-            launch_scale_scan(w3s, z.e13s, flag, 0) != cudaSuccess ||
-            launch_scale_scan(w2s, z.e2s, flag, 0) != cudaSuccess ||
-            launch_row_scale_max(w1s, z.e13m, c.latent / kGroup, w1m) != cudaSuccess ||
-            launch_row_scale_max(w3s, z.e13m, c.latent / kGroup, w3m) != cudaSuccess ||
-            launch_row_scale_max(w2s, z.e2m, c.moe_inter / kGroup, w2m) != cudaSuccess ||
+            launch_scale_scan(exd[1], z.e13s, flag, 0) != cudaSuccess ||
+            launch_scale_scan(exd[3], z.e13s, flag, 0) != cudaSuccess ||
+            launch_scale_scan(exd[5], z.e2s, flag, 0) != cudaSuccess ||
+            launch_row_scale_max(exd[1], z.e13m, c.latent / kGroup, exd[6]) != cudaSuccess ||
+            launch_row_scale_max(exd[3], z.e13m, c.latent / kGroup, exd[7]) != cudaSuccess ||
+            launch_row_scale_max(exd[5], z.e2m, c.moe_inter / kGroup, exd[8]) != cudaSuccess ||
             cudaMemcpy(&bad, flag, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
             rc = K3MOE_ERR_CUDA;
         else if (bad)
             rc = K3MOE_ERR_BAD_SCALE;
         cudaMemset(flag, 0, sizeof(int));
     }
+    // a reloaded tiered layer gives up its slots before its old block goes
+    if (rc == K3MOE_OK && tiered && h->layers[(size_t)layer].loaded &&
+        (launch_tier_forget(*h, layer, 0) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess))
+        rc = K3MOE_ERR_CUDA;
     if (rc != K3MOE_OK) {
         cudaFree(blk);
+        if (hblk) cudaFreeHost(hblk);
         return rc;
     }
     L.router_w = router;
@@ -487,15 +546,27 @@ int k3moe_load_layer(k3moe *h, int layer, const k3moe_layer_weights *w)
     L.sh_w1 = sh1;
     L.sh_w3 = sh3;
     L.sh_w2 = sh2;
-    L.w1p = w1p;
-    L.w1s = w1s;
-    L.w3p = w3p;
-    L.w3s = w3s;
-    L.w2p = w2p;
-    L.w2s = w2s;
-    L.w1max = w1m;
-    L.w3max = w3m;
-    L.w2max = w2m;
+    // expert arrays as the expert kernels address them: the handle's slots
+    // (tier) or the layer's own copy
+    const uint8_t *const *arr = tiered ? (const uint8_t *const *)h->tier.arr : (const uint8_t *const *)exd;
+    L.w1p = arr[0];
+    L.w1s = arr[1];
+    L.w3p = arr[2];
+    L.w3s = arr[3];
+    L.w2p = arr[4];
+    L.w2s = arr[5];
+    L.w1max = arr[6];
+    L.w3max = arr[7];
+    L.w2max = arr[8];
+    if (tiered) {
+        L.wslot = h->tier.slot_of + (size_t)layer * c.n_experts;
+        L.n_wslots = h->tier.slots;
+        L.host_block = hblk;
+        for (int p = 0; p < kTierPieces; p++) L.hsrc[p] = exd[p];
+    } else {
+        L.wslot = nullptr;
+        L.n_wslots = c.n_experts;
+    }
     if (dense_tma_fits(c, 1)) build_dense_tma_maps(c, L);   // else the maps are never used
     L.loaded = true;
     free_layer(h->layers[(size_t)layer]);
@@ -660,6 +731,79 @@ int k3moe_set_expert_path(k3moe *h, int mode)
         return K3MOE_ERR_INVALID_ARG;
     if (mode == K3MOE_EXPERT_GEMM && !h->egemm_ok) return K3MOE_ERR_SHAPE;
     h->expert_path = mode;
+    return K3MOE_OK;
+}
+
+int k3moe_set_expert_tier(k3moe *h, int slots)
+{
+    if (!h) return K3MOE_ERR_INVALID_ARG;
+    for (const auto &l : h->layers)
+        if (l.loaded) return K3MOE_ERR_INVALID_ARG;
+    const k3moe_config &c = h->cfg;
+    if (slots != 0 && (slots < c.n_experts || slots > kTierMaxSlots)) return K3MOE_ERR_INVALID_ARG;
+    if (cudaSetDevice(c.device) != cudaSuccess) return K3MOE_ERR_CUDA;
+    free_tier(h->tier);
+    if (slots == 0) return K3MOE_OK;
+    TierDev t;
+    const size_t I = c.moe_inter, L = c.latent;
+    const size_t piece[kTierPieces] = {I * (L / 2), I * (L / kGroup), I * (L / 2), I * (L / kGroup),
+                                       L * (I / 2), L * (I / kGroup), I, I, L};
+    size_t bytes = 0;
+    for (int p = 0; p < kTierPieces; p++) {
+        if (piece[p] % 16) return K3MOE_ERR_SHAPE;   // the fill copies 16-byte words
+        t.piece[p] = piece[p];
+        t.expert_bytes += piece[p];
+        bytes += al256((size_t)slots * piece[p]);
+    }
+    const size_t E = c.n_experts, tables = al256((size_t)c.max_layers * E * 4) + 2 * al256((size_t)slots * 4) +
+                                               al256(E * sizeof(int2)) + al256(4) + al256(3 * 8);
+    bytes += tables;
+    size_t fr = 0, tot = 0;
+    if (cudaMemGetInfo(&fr, &tot) != cudaSuccess) return K3MOE_ERR_CUDA;
+    if (bytes + (256u << 20) > fr) return K3MOE_ERR_OOM;
+    if (cudaMalloc(&t.block, bytes) != cudaSuccess) {
+        cudaGetLastError();
+        return K3MOE_ERR_OOM;
+    }
+    Carve cv{(char *)t.block};
+    for (int p = 0; p < kTierPieces; p++) t.arr[p] = cv.take<uint8_t>((size_t)slots * piece[p]);
+    char *tab = (char *)t.block + cv.off;
+    t.slot_of = cv.take<int>((size_t)c.max_layers * E);
+    t.slot_key = cv.take<int>((size_t)slots);
+    t.slot_used = cv.take<uint32_t>((size_t)slots);
+    t.fill = cv.take<int2>(E);
+    t.n_fill = cv.take<int>(1);
+    t.stats = cv.take<unsigned long long>(3);
+    // tables: every slot free (key -1, stamp 0), no expert resident
+    if (cudaMemset(tab, 0, tables) != cudaSuccess ||
+        cudaMemset(t.slot_of, 0xFF, (size_t)c.max_layers * E * 4) != cudaSuccess ||
+        cudaMemset(t.slot_key, 0xFF, (size_t)slots * 4) != cudaSuccess ||
+        cudaDeviceSynchronize() != cudaSuccess) {
+        cudaGetLastError();
+        cudaFree(t.block);
+        return K3MOE_ERR_CUDA;
+    }
+    t.slots = slots;
+    h->tier = t;
+    return K3MOE_OK;
+}
+
+int k3moe_get_tier_stats(k3moe *h, k3moe_tier_stats *out)
+{
+    if (!h || !out || out->struct_size != (int32_t)sizeof(k3moe_tier_stats)) return K3MOE_ERR_INVALID_ARG;
+    out->slots = h->tier.slots;
+    out->hits = out->misses = out->bytes_filled = 0;
+    if (h->tier.slots == 0) return K3MOE_OK;
+    if (cudaSetDevice(h->cfg.device) != cudaSuccess) return K3MOE_ERR_CUDA;
+    unsigned long long v[3] = {0, 0, 0};
+    if (cudaDeviceSynchronize() != cudaSuccess ||
+        cudaMemcpy(v, h->tier.stats, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) {
+        cudaGetLastError();
+        return K3MOE_ERR_CUDA;
+    }
+    out->hits = (int64_t)v[0];
+    out->misses = (int64_t)v[1];
+    out->bytes_filled = (int64_t)v[2];
     return K3MOE_OK;
 }
 

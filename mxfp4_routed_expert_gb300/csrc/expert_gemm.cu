@@ -135,8 +135,22 @@ struct EgArgs {
     __half *h16;                 // [T*k, I]
     float *acc;                  // [T, L]
     float b1, b2, ib1, ib2;      // SiTU bounds and their reciprocals
+    const int *wslot;            // expert -> index in the weight arrays (nullptr: the expert)
+    int n_ws;                    // experts the weight arrays hold
     int *err;
 };
+
+// Index of expert e in the weight arrays: its expert-tier slot, or e itself.
+__device__ __forceinline__ int eg_wslot(const EgArgs &g, int e)
+{
+    if (!g.wslot) return e;
+    const int s = g.wslot[e];
+    if (s < 0 || s >= g.n_ws) {
+        set_err(g.err, kErrBounds, 620);
+        return 0;
+    }
+    return s;
+}
 
 // 2^d as an f16x2 bit pattern, d <= 0 (subnormal below 2^-14, zero below 2^-24).
 __device__ __forceinline__ uint32_t f16x2_pow2(int d)
@@ -248,7 +262,7 @@ __device__ __forceinline__ bool epilogue_item(const EgArgs &g, uint32_t tmem, in
     const int n_valid = min(BN, cnt - td.y * BN);
     const int pair0 = g.offsets[td.x] + td.y * BN;
     const int row_in_e = mt * g.mstep + erow;
-    const size_t grow = (size_t)td.x * g.R + row_in_e;
+    const size_t grow = (size_t)eg_wslot(g, td.x) * g.R + row_in_e;
     const float rs0 = pow2_e8m0(g.ma[grow]);
     const float rs1 = GE::NM == 2 ? pow2_e8m0(g.mb[grow + g.mrow]) : 0.f;
     // per-pair factors for the columns of each chunk, one lane each (lanes 16..31 repeat 0..15)
@@ -379,7 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
                 const int tile = item / g.MT, mt = item - tile * g.MT;
                 const int2 td = g.tiles[tile];
-                const int row0 = td.x * g.R + mt * g.mstep;     // row in the [E*R, K/2] view
+                const int row0 = eg_wslot(g, td.x) * g.R + mt * g.mstep;   // row in the [slots*R, K/2] view
                 const int pair0 = g.offsets[td.x] + td.y * BN;
                 const int cnt = g.offsets[td.x + 1] - g.offsets[td.x];
                 const int nv = min(BN, cnt - td.y * BN);
@@ -503,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // item, whose A slot frees up before the previous item's last MMAs end.
         for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, local++) {
             const int tile = item / g.MT, mt = item - tile * g.MT;
-            const size_t grow = (size_t)g.tiles[tile].x * g.R + mt * g.mstep + row + (m ? g.mrow : 0);
+            const size_t grow = (size_t)eg_wslot(g, g.tiles[tile].x) * g.R + mt * g.mstep + row + (m ? g.mrow : 0);
             const int smax = m == 0 ? g.ma[grow] : g.mb[grow];
             const uint8_t *sc = (m == 0 ? g.sa : g.sb) + grow * (size_t)G + grp0;   // G % 4 == 0
             bool epi = kSets == 1 && local > 0;      // previous item's epilogue still to run
@@ -742,6 +756,8 @@ cudaError_t launch_expert_gemm(const k3moe &h, const LayerDev &w, int T, cudaStr
     g.ib1 = 1.f / c.situ_b1;
     g.ib2 = 1.f / c.situ_b2;
     g.err = h.ws.err;
+    g.wslot = w.wslot;
+    g.n_ws = w.n_wslots;
     g.K = w13 ? c.latent : c.moe_inter;
     g.R = w13 ? c.moe_inter : c.latent;
     // W2 takes two adjacent m-tiles per item when its rows allow it
@@ -751,7 +767,7 @@ cudaError_t launch_expert_gemm(const k3moe &h, const LayerDev &w, int T, cudaStr
     g.MT = g.R / g.mstep;
     CUtensorMap ra, rb, bx, bxm, bxf;
     bool ok;
-    const uint64_t rows = (uint64_t)c.n_experts * g.R;
+    const uint64_t rows = (uint64_t)w.n_wslots * g.R;
     if (w13) {
         g.sa = w.w1s;
         g.sb = w.w3s;

@@ -67,6 +67,8 @@ struct ExpTArgs {
     float *acc;            // [T, L]
     float b1, b2;
     long long units;       // T*k*(R/64)
+    const int *wslot;      // expert -> index in the weight arrays (nullptr: the expert itself)
+    int n_ws;              // experts the weight arrays hold
     int *err;
 };
 
@@ -203,11 +205,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tma(ExpTArgs a)
                     set_err(a.err, kErrBounds, (int)u);
                     break;
                 }
+                const int we = a.wslot ? a.wslot[e] : e;
+                if (we < 0 || we >= a.n_ws) {
+                    set_err(a.err, kErrBounds, (int)u);
+                    break;
+                }
                 const float f = w_cur;
                 const uint64_t pol = (cnt == 1) ? pol_stream : pol_keep;
-                const uint8_t *PA = a.pa + (size_t)e * eb, *SA = a.sa + (size_t)e * es;
-                const uint8_t *PB = W13 ? a.pb + (size_t)e * eb : nullptr;
-                const uint8_t *SB = W13 ? a.sb + (size_t)e * es : nullptr;
+                const uint8_t *PA = a.pa + (size_t)we * eb, *SA = a.sa + (size_t)we * es;
+                const uint8_t *PB = W13 ? a.pb + (size_t)we * eb : nullptr;
+                const uint8_t *SB = W13 ? a.sb + (size_t)we * es : nullptr;
                 for (int s = 0; s < kUnitStages; s++) {
                     if (!mbar_wait(&empty[slot], phase ^ 1u, a.err, 100 + slot)) {
                         ok = false;
@@ -390,10 +397,12 @@ bool expert_smem_fits(const k3moe_config &c)
            exp_smem(c.moe_inter, false, c.n_experts) <= 227 * 1024;
 }
 
-static ExpTArgs base_args(const k3moe &h, int T)
+static ExpTArgs base_args(const k3moe &h, const LayerDev &w, int T)
 {
     const k3moe_config &c = h.cfg;
     ExpTArgs a;
+    a.wslot = w.wslot;
+    a.n_ws = w.n_wslots;
     a.L = c.latent;
     a.k = c.topk;
     a.E = c.n_experts;
@@ -412,7 +421,7 @@ static ExpTArgs base_args(const k3moe &h, int T)
 
 cudaError_t launch_expert_w13(const k3moe &h, const LayerDev &w, int T, cudaStream_t s)
 {
-    ExpTArgs a = base_args(h, T);
+    ExpTArgs a = base_args(h, w, T);
     a.pa = w.w1p;
     a.sa = w.w1s;
     a.pb = w.w3p;
@@ -426,7 +435,7 @@ cudaError_t launch_expert_w13(const k3moe &h, const LayerDev &w, int T, cudaStre
 
 cudaError_t launch_expert_w2(const k3moe &h, const LayerDev &w, int T, cudaStream_t s)
 {
-    ExpTArgs a = base_args(h, T);
+    ExpTArgs a = base_args(h, w, T);
     a.pa = w.w2p;
     a.sa = w.w2s;
     a.pb = nullptr;

@@ -28,6 +28,7 @@ enum : int { kErrNone = 0, kErrBounds = 1, kErrTimeout = 2 };
 
 struct LayerDev {
     bool loaded = false;
+    int index = -1;          // layer index in the handle
     void *block = nullptr;   // single allocation holding every tensor below
     size_t bytes = 0;
     const __nv_bfloat16 *router_w = nullptr;   // [E, H]
@@ -48,6 +49,34 @@ struct LayerDev {
     // up+shared down; six each), built once at load
     CUtensorMap dense_maps[3][6];
     bool dense_maps_ok = false;
+    // Expert arrays above hold n_wslots experts; expert e sits at index
+    // wslot[e] (expert tier: a slot of the handle's device pool) or at e
+    // (wslot == nullptr: the layer's own copy of all experts).
+    const int *wslot = nullptr;
+    int n_wslots = 0;
+    // expert tier: the layer's routed experts in one pinned, device-mapped
+    // host block, the nine expert arrays in the layout of the device copy
+    void *host_block = nullptr;
+    const uint8_t *hsrc[9] = {};
+};
+
+// Expert tier (k3moe_set_expert_tier): device slots caching routed experts
+// whose home is pinned host memory.
+constexpr int kTierPieces = 9;          // w1p w1s w3p w3s w2p w2s w1max w3max w2max
+constexpr int kTierMaxSlots = 16384;
+struct TierDev {
+    int slots = 0;
+    void *block = nullptr;              // device: slot arrays, then the tables
+    uint8_t *arr[kTierPieces] = {};     // [slots][piece size]
+    size_t piece[kTierPieces] = {};     // bytes of one expert's piece
+    size_t expert_bytes = 0;
+    int *slot_of = nullptr;             // [max_layers][E]: slot or -1
+    int *slot_key = nullptr;            // [slots]: layer * E + expert, or -1 (free)
+    uint32_t *slot_used = nullptr;      // [slots]: stamp of the last forward that used it
+    int2 *fill = nullptr;               // [E]: (slot, expert) per miss of the current forward
+    int *n_fill = nullptr;
+    unsigned long long *stats = nullptr;   // hits, misses, bytes filled
+    uint32_t stamp = 0;                 // forwards planned so far
 };
 
 // Per-handle scratch, sized for max_tokens (Tm).
@@ -104,6 +133,7 @@ struct k3moe {
     bool gemm_ok = false;                    // tensor-core dense GEMMs usable (T >= 16)
     bool egemm_ok = false;                   // tensor-core expert GEMM usable (shape)
     int expert_path = K3MOE_EXPERT_AUTO;     // k3moe_set_expert_path
+    k3::TierDev tier;                        // k3moe_set_expert_tier
     // per-kernel timing (k3moe_set_profiling)
     bool profiling = false;
     std::deque<k3::ProfRec> prof;
@@ -162,6 +192,11 @@ bool build_dense_tma_maps(const k3moe_config &c, LayerDev &w);
 cudaError_t launch_dense_tma(const k3moe &h, const LayerDev &w, const __nv_bfloat16 *x,
                              __nv_bfloat16 *y, int T, cudaStream_t s, int part);
 bool expert_smem_fits(const k3moe_config &c);
+// expert tier: which touched experts are resident and which slots the others
+// take (one block), then the copy of the missed experts into their slots
+cudaError_t launch_tier_plan(k3moe &h, int layer, cudaStream_t s);
+cudaError_t launch_tier_fill(const k3moe &h, const LayerDev &w, cudaStream_t s);
+cudaError_t launch_tier_forget(const k3moe &h, int layer, cudaStream_t s);
 
 // ---- device helpers -----------------------------------------------------------
 __device__ __forceinline__ void set_err(int *err, int code, int detail)

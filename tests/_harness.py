@@ -67,7 +67,7 @@ class Layer:
     """One library handle with layers loaded from numpy tensors."""
 
     def __init__(self, shape, layers: list, max_tokens: int, device: int = 0,
-                 latent_norm: int = 1):
+                 latent_norm: int = 1, tier_slots: int = 0):
         import torch  # noqa: F401
         import mxfp4_routed_expert_gb300 as km
         self.km = km
@@ -75,6 +75,8 @@ class Layer:
         cfg = km.make_config(shape, max_layers=len(layers), max_tokens=max_tokens, device=device,
                              latent_norm=latent_norm)
         self.h = km.k3moe_create(cfg)
+        if tier_slots:
+            km.k3moe_set_expert_tier(self.h, tier_slots)
         for i, d in enumerate(layers):
             if d is not None:
                 self.load(i, d)

@@ -1,0 +1,177 @@
+"""Expert tier through the C ABI (GPU): routed experts held in pinned host
+memory and cached in device slots.
+
+Every forward through the tier is checked against the fp64 oracle (ids and
+permutation exact, y within the layer tolerance), so an expert read from a
+wrong or stale slot fails at once. The tier's hit/miss counters are checked
+against the cache policy written out on the host (kimi-k3-in-c README,
+Part II section 12, "An LRU cache for the experts": a free slot first, else
+the one used longest ago; here ties go to the lower slot, the slots a forward
+hits are never its victims, and a forward's misses take its victims in
+ascending expert order).
+"""
+import numpy as np
+import pytest
+
+import k3synth
+import oracle
+from _harness import Layer, assert_close, bf16_to_f64, check_routing, guarded_tokens
+
+pytestmark = pytest.mark.gpu
+
+MID = k3synth.Shape(hidden=1024, latent=512, n_experts=64, topk=8, moe_inter=512,
+                    shared_inter=1024)
+WIDE = k3synth.Shape(hidden=1024, latent=512, n_experts=128, topk=8, moe_inter=512,
+                     shared_inter=1024)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from mxfp4_routed_expert_gb300 import build
+    build.build()
+
+
+def expert_bytes(s):
+    I, L, G = s.moe_inter, s.latent, 32
+    return 2 * (I * L // 2 + I * L // G) + (L * I // 2 + L * I // G) + 2 * I + L
+
+
+class LruModel:
+    """The slot policy on the host: which (layer, expert) each slot holds and
+    the stamp of the forward that last used it (0: never)."""
+
+    def __init__(self, slots):
+        self.key = [None] * slots
+        self.used = [0] * slots
+        self.stamp = 0
+        self.hits = 0
+        self.misses = 0
+
+    def forward(self, layer, touched):
+        self.stamp += 1
+        where = {k: s for s, k in enumerate(self.key) if k is not None}
+        miss = []
+        for e in sorted(touched):
+            s = where.get((layer, int(e)))
+            if s is None:
+                miss.append(int(e))
+            else:
+                self.used[s] = self.stamp
+                self.hits += 1
+        cand = sorted((self.used[s], s) for s in range(len(self.key)) if self.used[s] < self.stamp)
+        assert len(cand) >= len(miss)
+        victims = sorted(s for _, s in cand[:len(miss)])
+        for e, s in zip(miss, victims):
+            self.key[s] = (layer, e)
+            self.used[s] = self.stamp
+        self.misses += len(miss)
+
+
+def run_sequence(shape, layers, slots, steps, expert_path=None, max_tokens=64):
+    """Forwards (layer, T, seed) through one tiered handle, each against the
+    oracle; returns the handle's counters and the model's."""
+    import mxfp4_routed_expert_gb300 as km
+    lay = Layer(shape, layers, max_tokens=max_tokens, tier_slots=slots)
+    model = LruModel(slots)
+    try:
+        if expert_path is not None:
+            km.k3moe_set_expert_path(lay.h, expert_path)
+        for layer, T, seed in steps:
+            d = layers[layer]
+            x, _ = guarded_tokens(shape, d, seed, T)
+            y = lay.forward(x, layer=layer)
+            r = lay.routing(T)
+            ref, tr = oracle.layer_forward(shape, d, x, trace=True)
+            check_routing(r, shape, x, tr["ids"], tr["w"])
+            assert_close(bf16_to_f64(y), ref, f"y (layer {layer}, T={T})")
+            model.forward(layer, np.nonzero(r["counts"])[0])
+        st = km.k3moe_get_tier_stats(lay.h)
+    finally:
+        lay.close()
+    return st, model
+
+
+def test_tier_decode_sequence_matches_oracle_and_policy():
+    """Three layers share E slots (one layer's worth) over single-token and
+    3-token forwards (the GEMV path): hits on repeated tokens, free slots taken
+    first, then least-recently-used eviction across layers."""
+    layers = [k3synth.make_layer(MID, 20 + i, 0, k3synth.TINY_RECIPE) for i in range(3)]
+    steps = [(0, 1, 0), (1, 1, 1), (0, 1, 0), (2, 3, 2), (1, 1, 1), (0, 3, 3), (2, 1, 4),
+             (2, 1, 4), (1, 3, 5), (0, 1, 0), (2, 3, 6), (1, 1, 7)]
+    st, model = run_sequence(MID, layers, MID.n_experts, steps)
+    assert st["slots"] == MID.n_experts
+    assert model.hits > 0 and model.misses > MID.n_experts   # both hits and evictions happened
+    assert (st["hits"], st["misses"]) == (model.hits, model.misses)
+    assert st["bytes_filled"] == model.misses * expert_bytes(MID)
+
+
+@pytest.mark.parametrize("path", ["gemm", "gemv"])
+def test_tier_batches_evict_whole_layers(path):
+    """T = 40 on 128 experts touches most of them: with 128 slots every switch
+    of layer evicts most of the other layer's experts. Both expert paths."""
+    import mxfp4_routed_expert_gb300 as km
+    layers = [k3synth.make_layer(WIDE, 30 + i, 0, k3synth.TINY_RECIPE) for i in range(2)]
+    steps = [(0, 40, 0), (1, 40, 1), (0, 40, 0), (0, 17, 2), (1, 40, 3), (1, 40, 3)]
+    mode = km.K3MOE_EXPERT_GEMM if path == "gemm" else km.K3MOE_EXPERT_GEMV
+    st, model = run_sequence(WIDE, layers, WIDE.n_experts, steps, expert_path=mode)
+    assert (st["hits"], st["misses"]) == (model.hits, model.misses)
+    assert st["bytes_filled"] == model.misses * expert_bytes(WIDE)
+
+
+def test_tier_with_room_for_every_layer_only_misses_once():
+    """Slots for both layers: after the first forward of each layer nothing is
+    evicted, so repeating the same tokens only hits."""
+    layers = [k3synth.make_layer(MID, 40 + i, 0, k3synth.TINY_RECIPE) for i in range(2)]
+    steps = [(0, 5, 0), (1, 5, 1), (0, 5, 0), (1, 5, 1), (0, 5, 0)]
+    st, model = run_sequence(MID, layers, 2 * MID.n_experts, steps)
+    assert (st["hits"], st["misses"]) == (model.hits, model.misses)
+    # each (layer, expert) was copied in once and never evicted
+    assert st["misses"] == sum(k is not None for k in model.key)
+    assert st["hits"] > 0
+
+
+def test_tier_reload_forgets_the_old_experts():
+    """Reloading a tiered layer with other weights frees its slots: the next
+    forward misses every touched expert and matches the new weights."""
+    import mxfp4_routed_expert_gb300 as km
+    d0 = k3synth.make_layer(MID, 50, 0, k3synth.TINY_RECIPE)
+    d1 = k3synth.make_layer(MID, 51, 0, k3synth.TINY_RECIPE)
+    lay = Layer(MID, [d0], max_tokens=8, tier_slots=MID.n_experts)
+    try:
+        x, _ = guarded_tokens(MID, d0, 3, 4)
+        lay.forward(x)
+        before = km.k3moe_get_tier_stats(lay.h)
+        lay.load(0, d1)
+        x1, _ = guarded_tokens(MID, d1, 3, 4)
+        y = lay.forward(x1)
+        r = lay.routing(4)
+        after = km.k3moe_get_tier_stats(lay.h)
+    finally:
+        lay.close()
+    ref, tr = oracle.layer_forward(MID, d1, x1, trace=True)
+    check_routing(r, MID, x1, tr["ids"], tr["w"])
+    assert_close(bf16_to_f64(y), ref)
+    assert after["hits"] == before["hits"]
+    assert after["misses"] - before["misses"] == int(np.count_nonzero(r["counts"]))
+
+
+def test_tier_argument_errors():
+    import mxfp4_routed_expert_gb300 as km
+    d = k3synth.make_layer(MID, 52, 0, k3synth.TINY_RECIPE)
+    lay = Layer(MID, [None], max_tokens=4)
+    try:
+        assert km.k3moe_get_tier_stats(lay.h) == dict(slots=0, hits=0, misses=0, bytes_filled=0)
+        for bad in (MID.n_experts - 1, -1, 16385):
+            with pytest.raises(km.K3MoEError) as ei:
+                km.k3moe_set_expert_tier(lay.h, bad)
+            assert ei.value.code == km.K3MOE_ERR_INVALID_ARG
+        km.k3moe_set_expert_tier(lay.h, MID.n_experts)
+        km.k3moe_set_expert_tier(lay.h, 0)                 # off again before any load
+        km.k3moe_set_expert_tier(lay.h, MID.n_experts + 3)
+        lay.load(0, d)
+        with pytest.raises(km.K3MoEError) as ei:            # too late: a layer is loaded
+            km.k3moe_set_expert_tier(lay.h, MID.n_experts)
+        assert ei.value.code == km.K3MOE_ERR_INVALID_ARG
+        assert km.k3moe_get_tier_stats(lay.h)["slots"] == MID.n_experts + 3
+    finally:
+        lay.close()
