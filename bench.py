@@ -65,6 +65,12 @@ WORKLOADS = {
                           "(16 pairs per expert; small case for profiler captures)"),
     "prefill_t512_e64": dict(T=512, layers=1, desc="K3 row shapes with 64 routed experts, T=512 "
                              "(128 pairs per expert; small case for profiler captures)"),
+    # the layer fed from the residual stream: the RMSNorm in front of the MoE
+    # runs inside the first two decode kernels
+    "decode_t1_residual": dict(T=1, layers=1, residual=True,
+                               desc="K3-shape single layer, decode T=1 from fp32 residual-stream "
+                                    "rows (RMSNorm with the post-norm gain fused into the first "
+                                    "kernels; rows rotate through a seeded pool of 64)"),
     # expert tier: routed experts in pinned host memory, 896 device slots
     # shared by two layers; each step is one forward of one layer (alternating)
     "decode_t1_tier": dict(T=1, layers=2, tier=896, alternate=True,
@@ -177,6 +183,8 @@ def make_inputs(workload, seed=0, layer_index=0):
     T = WORKLOADS[workload]["T"]
     if workload in ("decode_t1", "decode_t1_e64"):
         x = k3synth.make_tokens(shape, seed, POOL, stream=7)
+    elif workload == "decode_t1_residual":
+        x = k3synth.make_residual(shape, seed, POOL, stream=7)   # fp32 residual rows
     elif workload == "decode_t1_tier":
         x = k3synth.make_tokens(shape, seed, TIER_POOL, stream=17)
     elif workload in ("decode_t64", "decode_t64_tier"):
@@ -341,7 +349,12 @@ def run_native(args, rank, world):
     if not alternate:
         xpools = xpools[:1]
 
-    xs = [torch.from_numpy(xp.view(np.int16).copy()).cuda() for xp in xpools]
+    residual = wl.get("residual", False)
+    if residual:
+        km.k3moe_load_post_norm(h, 0, k3synth.post_norm_gain(shape, 0))
+        xs = [torch.from_numpy(np.ascontiguousarray(xp, np.float32)).cuda() for xp in xpools]
+    else:
+        xs = [torch.from_numpy(xp.view(np.int16).copy()).cuda() for xp in xpools]
     npool = xs[0].shape[0] // T
     y = torch.empty((T, shape.hidden), dtype=torch.int16, device="cuda")
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
@@ -355,7 +368,9 @@ def run_native(args, rank, world):
             km.k3moe_forward(h, li, xs[li][j * T:j * T + T], y, T, stream)
             return
         xi = xs[0][(i % npool) * T:(i % npool) * T + T]
-        if n_layers > 1:
+        if residual:
+            km.k3moe_forward_residual(h, 0, xi, y, T, stream)
+        elif n_layers > 1:
             km.k3moe_forward_chain(h, 0, n_layers, xi, y, T, stream)
         else:
             km.k3moe_forward(h, 0, xi, y, T, stream)
@@ -459,7 +474,7 @@ def run_native(args, rank, world):
 
     # ---- e2e through the public host-buffer entry point --------------------------------
     e2e = None
-    if n_layers == 1 and not args.no_e2e:
+    if n_layers == 1 and not residual and not args.no_e2e:
         xh = torch.from_numpy(xpool.view(np.int16).copy()).pin_memory()
         yh = torch.empty((T, shape.hidden), dtype=torch.int16).pin_memory()
         for i in range(2):
@@ -480,6 +495,10 @@ def run_native(args, rank, world):
     if rank == 0 and not args.no_cpu_baseline:
         n_tok = 320                      # about 10-20 s of the oracle on the machine's cores
         xs_host = xpool if T == 1 else xpool[:T]
+        if residual:   # the oracle's layer on the oracle's made input
+            import oracle
+            xs_host = oracle.round_bf16(oracle.residual_input(xs_host, k3synth.post_norm_gain(shape, 0),
+                                                              shape.rms_eps))
         nrow, dt = time_oracle(shape, oracle_layer, xs_host, n_tok)
         cpu = {"value": round(nrow / dt / layers_per_step, 4), "unit": UNIT,
                "cores": omp_threads(nrow), "kind": "oracle",

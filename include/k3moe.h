@@ -159,13 +159,38 @@ K3MOE_API int k3moe_forward_host(k3moe *h, int layer, const void *x_host, void *
 K3MOE_API int k3moe_get_routing(k3moe *h, int32_t *ids, float *w, int32_t *counts, int32_t *offsets,
                       int32_t *perm, void *stream);
 
+/* ---- Forward from the residual stream -------------------------------------------
+ * In the model the layer's input is the decoder's residual stream h after the
+ * RMSNorm in front of the MoE (kimi-k3-in-c README, Part II, the decoder layer
+ * applies its post_norm to h and hands the result to k3_moe; k3_rmsnorm in
+ * section 5: x = h * inv * gain, inv = 1/sqrt(mean(h^2) + eps) with the squares
+ * summed in double).
+ *
+ * k3moe_load_post_norm attaches that norm's gain (bf16 [hidden], host or
+ * device memory as `where` says) to a loaded layer; loading the layer again
+ * drops it. K3MOE_ERR_NOT_LOADED when the layer is not loaded.
+ *
+ * k3moe_forward_residual takes h_in fp32 [T, hidden] (device memory, 16-byte
+ * aligned), forms x = bf16(RMSNorm(h_in) * gain) per token (rms_eps of the
+ * configuration) and runs the layer on x as k3moe_forward does. At T <= 2 the
+ * norm runs inside the first two kernels of the layer (x never goes to
+ * memory); otherwise a first kernel writes x to the workspace. The x used can
+ * be read back with k3moe_get_intermediate(K3MOE_T_X). Errors as
+ * k3moe_forward, and K3MOE_ERR_NOT_LOADED when the layer has no post-norm
+ * gain. */
+K3MOE_API int k3moe_load_post_norm(k3moe *h, int layer, const void *gain, int where);
+K3MOE_API int k3moe_forward_residual(k3moe *h, int layer, const float *h_in, void *y, int T,
+                                     void *stream);
+
 /* Intermediates of the last forward, for parity diagnosis. Copies `bytes`
  * bytes (at most the tensor's size for the last T) into caller device memory.
  *   K3MOE_T_Z       fp32 [T, L]   latent down projection
  *   K3MOE_T_ACC     fp32 [T, L]   weighted sum of expert outputs (before the norm)
  *   K3MOE_T_SHARED  fp32 [T, S]   SiTU of the shared experts
- *   K3MOE_T_LOGITS  fp32 [T, E]   router logits */
-enum { K3MOE_T_Z = 1, K3MOE_T_ACC = 2, K3MOE_T_SHARED = 3, K3MOE_T_LOGITS = 4 };
+ *   K3MOE_T_LOGITS  fp32 [T, E]   router logits
+ *   K3MOE_T_X       bf16 [T, H]   the layer input that k3moe_forward_residual made
+ *                                 (K3MOE_ERR_INVALID_ARG after any other forward) */
+enum { K3MOE_T_Z = 1, K3MOE_T_ACC = 2, K3MOE_T_SHARED = 3, K3MOE_T_LOGITS = 4, K3MOE_T_X = 5 };
 K3MOE_API int k3moe_get_intermediate(k3moe *h, int which, void *dst, size_t bytes, void *stream);
 
 /* Synchronises the device and returns (then clears) the first latched

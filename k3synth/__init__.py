@@ -33,6 +33,7 @@ _lib = None
 TX, TROUTER, TBIAS, TDOWN, TUP, TGAIN, TSH1, TSH3, TSH2 = 1, 2, 3, 4, 5, 6, 7, 8, 9
 TW1P, TW1S, TW3P, TW3S, TW2P, TW2S = 10, 11, 12, 13, 14, 15
 TPERM, TCOVER = 16, 17
+TRESID, TRESID_SCALE, TPOSTGAIN = 18, 19, 20
 
 MXFP4_GROUP = 32
 
@@ -240,6 +241,35 @@ def make_tokens(shape: Shape, seed: int, T: int, stream: int = 0,
     return out
 
 
+def make_residual(shape: Shape, seed: int, T: int, stream: int = 0,
+                  attempts: np.ndarray | None = None) -> np.ndarray:
+    """Residual-stream rows h [T, H] fp32 as the decoder hands them to the
+    RMSNorm in front of the MoE: N(0, 1) per element times a per-token scale
+    2^u, u ~ N(1, 1) clipped to [-1, 4] (the pages print per-layer maxima of
+    |h| from about 3 to 76), with four fixed channels ten times larger (the
+    outlier channels of a residual stream). Row t comes from its own stream
+    (seed, stream, t, attempts[t])."""
+    H = shape.hidden
+    att = None
+    if attempts is not None:
+        att = np.ascontiguousarray(attempts, dtype=np.int32)
+        assert att.shape == (T,)
+    rows = np.empty((T, H), dtype=np.float64)
+    _L().k3s_fill_token_rows_f64(_ptr(rows), T, H, seed, TRESID, stream,
+                                 None if att is None else _ptr(att), 0.0, 1.0)
+    u = np.empty((T, 1), dtype=np.float64)
+    _L().k3s_fill_token_rows_f64(_ptr(u), T, 1, seed, TRESID_SCALE, stream,
+                                 None if att is None else _ptr(att), 1.0, 1.0)
+    rows *= np.exp2(np.clip(u, -1.0, 4.0))
+    rows[:, [3, H // 3, H // 2 + 1, H - 5]] *= 10.0
+    return rows.astype(np.float32)
+
+
+def post_norm_gain(shape: Shape, seed: int, layer: int = 0) -> np.ndarray:
+    """bf16 bits [H] of the RMSNorm gain in front of the MoE: 1 + N(0, 0.1)."""
+    return normal_bf16((shape.hidden,), key(seed, TPOSTGAIN, layer), 1.0, 0.1)
+
+
 def covering_tokens(shape: Shape, layer: dict, seed: int, T: int, a: float = 15.0,
                     stream: int = 1, attempts: np.ndarray | None = None) -> np.ndarray:
     """Tokens whose top-k sets tile the expert pool.
@@ -288,5 +318,6 @@ def with_bias(layer: dict, bias: np.ndarray) -> dict:
 
 
 __all__ = ["Shape", "K3", "TINY", "WeightRecipe", "K3_RECIPE", "TINY_RECIPE", "make_layer",
+           "make_residual", "post_norm_gain",
            "make_tokens", "covering_tokens", "zipf_bias", "with_bias", "bf16_bits_to_f32",
            "round_bf16", "build", "key", "replace", "MXFP4_GROUP"]

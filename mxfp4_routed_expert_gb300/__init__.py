@@ -30,14 +30,15 @@ K3MOE_ERR_CUDA = -7
 K3MOE_ERR_TIMEOUT = -8
 K3MOE_ERR_DEVICE = -9
 K3MOE_HOST, K3MOE_DEVICE = 0, 1
-K3MOE_T_Z, K3MOE_T_ACC, K3MOE_T_SHARED, K3MOE_T_LOGITS = 1, 2, 3, 4
+K3MOE_T_Z, K3MOE_T_ACC, K3MOE_T_SHARED, K3MOE_T_LOGITS, K3MOE_T_X = 1, 2, 3, 4, 5
 
 # Every symbol include/k3moe.h declares.
 EXPORTS = ("k3moe_create", "k3moe_load_layer", "k3moe_forward", "k3moe_forward_chain",
            "k3moe_forward_host", "k3moe_get_routing", "k3moe_get_intermediate",
            "k3moe_sync_status", "k3moe_set_profiling", "k3moe_profile_read", "k3moe_destroy",
            "k3moe_strerror", "k3moe_abi_version", "k3moe_route_static", "k3moe_set_expert_path",
-           "k3moe_set_expert_tier", "k3moe_get_tier_stats")
+           "k3moe_set_expert_tier", "k3moe_get_tier_stats", "k3moe_load_post_norm",
+           "k3moe_forward_residual")
 K3MOE_ROUTE_STATIC_MAX_LOGITS = 1 << 20
 K3MOE_EXPERT_AUTO, K3MOE_EXPERT_GEMV, K3MOE_EXPERT_GEMM = 0, 1, 2
 
@@ -114,6 +115,8 @@ def lib():
         L.k3moe_abi_version.restype = i
         L.k3moe_route_static.argtypes = [vp, vp, vp, i, i, i, i, i, ctypes.c_float, vp, vp, vp]
         L.k3moe_set_expert_tier.argtypes = [vp, i]
+        L.k3moe_load_post_norm.argtypes = [vp, i, vp, i]
+        L.k3moe_forward_residual.argtypes = [vp, i, vp, vp, i, vp]
         L.k3moe_get_tier_stats.argtypes = [vp, ctypes.POINTER(k3moe_tier_stats)]
         for n in EXPORTS:
             if n not in ("k3moe_destroy", "k3moe_strerror"):
@@ -225,6 +228,25 @@ def k3moe_load_layer(h: int, layer: int, weights: k3moe_layer_weights) -> int:
 def k3moe_forward(h: int, layer: int, x, y, T: int, stream=None) -> int:
     return _check(lib().k3moe_forward(ctypes.c_void_p(h), layer, _ptr(x), _ptr(y), T,
                                       _stream(stream)), "k3moe_forward")
+
+
+def k3moe_load_post_norm(h: int, layer: int, gain, where: int = K3MOE_HOST) -> int:
+    """The RMSNorm gain (bf16 [hidden]: a numpy uint16 array for HOST, a CUDA
+    tensor for DEVICE) in front of the MoE, for k3moe_forward_residual."""
+    if isinstance(gain, np.ndarray):
+        assert gain.flags["C_CONTIGUOUS"]
+        ptr = gain.ctypes.data
+    else:
+        ptr = _ptr(gain)
+    return _check(lib().k3moe_load_post_norm(ctypes.c_void_p(h), layer, ptr, where),
+                  "k3moe_load_post_norm")
+
+
+def k3moe_forward_residual(h: int, layer: int, h_in, y, T: int, stream=None) -> int:
+    """The layer on x = bf16(RMSNorm(h_in) * post-norm gain); h_in fp32 [T, hidden]."""
+    return _check(lib().k3moe_forward_residual(ctypes.c_void_p(h), layer, _ptr(h_in), _ptr(y), T,
+                                               _stream(stream)),
+                  "k3moe_forward_residual")
 
 
 def k3moe_forward_chain(h: int, first_layer: int, n_layers: int, x, y, T: int, stream=None) -> int:

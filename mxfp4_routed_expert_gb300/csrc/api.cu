@@ -85,6 +85,7 @@ size_t carve_workspace(const k3moe_config &c, char *base, Workspace *ws)
     w.gemm_tiles = cv.take<int>(dense_gemm_tile_counters(c));
     w.xbuf0 = cv.take<__nv_bfloat16>(Tm * H);
     w.xbuf1 = cv.take<__nv_bfloat16>(Tm * H);
+    w.xn = cv.take<__nv_bfloat16>(Tm * H);
     w.err = cv.take<int>(4);
     w.block = base;
     w.bytes = cv.off;
@@ -200,8 +201,11 @@ bool use_expert_gemm(const k3moe &h, int T)
     return h.expert_path == K3MOE_EXPERT_GEMM || T >= kGemmMinTokens;
 }
 
+// hin != nullptr: the layer input is made from the fp32 residual hin by the
+// RMSNorm in front of the MoE (inside the decode dense kernels at T <= 2, else
+// by a first kernel into Workspace::xn); x is then unused.
 int run_layer(k3moe *h, const LayerDev &w, const __nv_bfloat16 *x, __nv_bfloat16 *y, int T,
-              cudaStream_t s)
+              cudaStream_t s, const float *hin = nullptr)
 {
     cudaError_t e;
     const bool tier = h->tier.slots > 0;
@@ -222,6 +226,11 @@ int run_layer(k3moe *h, const LayerDev &w, const __nv_bfloat16 *x, __nv_bfloat16
     const bool tma = T <= 2 && h->dense_tma_ok[T - 1];
     const bool gemm = T >= kGemmMinTokens && h->gemm_ok;
     const bool egemm = use_expert_gemm(*h, T);
+    const float *fused = (hin && tma) ? hin : nullptr;   // made inside the dense kernels
+    if (hin && !tma) {
+        K3_STEP("residual_rmsnorm", launch_residual_norm(*h, hin, w.post_gain, T, s));
+        x = h->ws.xn;
+    }
     if (gemm) {
         K3_STEP("router_down_gemm", launch_dense_gemm(*h, w, x, nullptr, T, s, 0));
         if (cudaEventRecord(h->ev_fork, s) != cudaSuccess ||
@@ -235,7 +244,7 @@ int run_layer(k3moe *h, const LayerDev &w, const __nv_bfloat16 *x, __nv_bfloat16
             return K3MOE_ERR_CUDA;
         K3_STEP("route_topk", launch_route(*h, w, T, s));
     } else {
-        K3_STEP("router_down_gemv", tma ? launch_dense_tma(*h, w, x, nullptr, T, s, 0)
+        K3_STEP("router_down_gemv", tma ? launch_dense_tma(*h, w, x, nullptr, T, s, 0, fused)
                                         : launch_dense_x(*h, w, x, T, s, 0));
         K3_STEP("route_topk", launch_route(*h, w, T, s));
         if (tier && T == 1) {
@@ -244,8 +253,8 @@ int run_layer(k3moe *h, const LayerDev &w, const __nv_bfloat16 *x, __nv_bfloat16
             K3_STEP("tier_plan", launch_tier_plan(*h, w.index, s));
             K3_STEP("tier_fill", launch_tier_fill(*h, w, s));
         }
-        K3_STEP("shared_gate_up_gemv", tma ? launch_dense_tma(*h, w, x, nullptr, T, s, 1)
-                                           : launch_dense_x(*h, w, x, T, s, 1));
+        K3_STEP("shared_gate_up_gemv", tma ? launch_dense_tma(*h, w, x, nullptr, T, s, 1, fused)
+                                           : launch_dense_x(*h, w, x, T, s, 1, hin != nullptr));
     }
     if (T > 1) {   // T == 1: written by route_topk
         K3_STEP("perm_count", launch_perm(*h, T, s, 0));
@@ -275,6 +284,7 @@ int run_layer(k3moe *h, const LayerDev &w, const __nv_bfloat16 *x, __nv_bfloat16
     }
 #undef K3_STEP
     h->last_T = T;
+    h->last_x = hin != nullptr;
     return K3MOE_OK;
 }
 
@@ -288,6 +298,7 @@ void free_layer(LayerDev &l)
 {
     if (l.block) cudaFree(l.block);
     if (l.host_block) cudaFreeHost(l.host_block);
+    if (l.post_block) cudaFree(l.post_block);
     l = LayerDev();
 }
 
@@ -587,6 +598,45 @@ int k3moe_forward(k3moe *h, int layer, const void *x, void *y, int T, void *stre
     return run_layer(h, w, (const __nv_bfloat16 *)x, (__nv_bfloat16 *)y, T, (cudaStream_t)stream);
 }
 
+int k3moe_load_post_norm(k3moe *h, int layer, const void *gain, int where)
+{
+    if (!h || !gain) return K3MOE_ERR_INVALID_ARG;
+    if (layer < 0 || layer >= h->cfg.max_layers) return K3MOE_ERR_INVALID_ARG;
+    if (where != K3MOE_HOST && where != K3MOE_DEVICE) return K3MOE_ERR_INVALID_ARG;
+    LayerDev &w = h->layers[(size_t)layer];
+    if (!w.loaded) return K3MOE_ERR_NOT_LOADED;
+    if (cudaSetDevice(h->cfg.device) != cudaSuccess) return K3MOE_ERR_CUDA;
+    const size_t nb = (size_t)h->cfg.hidden * 2;
+    void *p = w.post_block;
+    if (!p && cudaMalloc(&p, nb) != cudaSuccess) {
+        cudaGetLastError();
+        return K3MOE_ERR_OOM;
+    }
+    if (cudaMemcpy(p, gain, nb, where == K3MOE_HOST ? cudaMemcpyHostToDevice : cudaMemcpyDeviceToDevice) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        if (!w.post_block) cudaFree(p);
+        return K3MOE_ERR_CUDA;
+    }
+    w.post_block = p;
+    w.post_gain = (const __nv_bfloat16 *)p;
+    return K3MOE_OK;
+}
+
+int k3moe_forward_residual(k3moe *h, int layer, const float *h_in, void *y, int T, void *stream)
+{
+    if (!h || !h_in || !y) return K3MOE_ERR_INVALID_ARG;
+    if (layer < 0 || layer >= h->cfg.max_layers) return K3MOE_ERR_INVALID_ARG;
+    if (T < 1 || T > h->cfg.max_tokens) return K3MOE_ERR_INVALID_ARG;
+    if ((uintptr_t)h_in % 16) return K3MOE_ERR_INVALID_ARG;
+    if (overlap(h_in, (size_t)T * h->cfg.hidden * 4, y, (size_t)T * h->cfg.hidden * 2))
+        return K3MOE_ERR_INVALID_ARG;
+    const LayerDev &w = h->layers[(size_t)layer];
+    if (!w.loaded || !w.post_gain) return K3MOE_ERR_NOT_LOADED;
+    if (cudaSetDevice(h->cfg.device) != cudaSuccess) return K3MOE_ERR_CUDA;
+    return run_layer(h, w, nullptr, (__nv_bfloat16 *)y, T, (cudaStream_t)stream, h_in);
+}
+
 int k3moe_forward_chain(k3moe *h, int first_layer, int n_layers, const void *x, void *y, int T,
                         void *stream)
 {
@@ -692,6 +742,11 @@ int k3moe_get_intermediate(k3moe *h, int which, void *dst, size_t bytes, void *s
     case K3MOE_T_LOGITS:
         if (bytes > T * E * 4) return K3MOE_ERR_INVALID_ARG;
         e = cudaMemcpyAsync(dst, h->ws.logits, bytes, cudaMemcpyDeviceToDevice, s);
+        break;
+    case K3MOE_T_X:
+        if (!h->last_x) return K3MOE_ERR_INVALID_ARG;
+        if (bytes > T * h->cfg.hidden * 2) return K3MOE_ERR_INVALID_ARG;
+        e = cudaMemcpyAsync(dst, h->ws.xn, bytes, cudaMemcpyDeviceToDevice, s);
         break;
     case K3MOE_T_SHARED: {
         if (bytes != T * S * 4) return K3MOE_ERR_INVALID_ARG;

@@ -324,7 +324,7 @@ static cudaError_t run_dense_x(const k3moe &h, const DenseXArgs &a, int slot, cu
 }
 
 cudaError_t launch_dense_x(const k3moe &h, const LayerDev &w, const __nv_bfloat16 *x, int T,
-                           cudaStream_t s, int part)
+                           cudaStream_t s, int part, bool wait_x)
 {
     const k3moe_config &c = h.cfg;
     DenseXArgs a;
@@ -347,7 +347,7 @@ cudaError_t launch_dense_x(const k3moe &h, const LayerDev &w, const __nv_bfloat1
     const int nAB = (c.n_experts + 3) / 4 + c.latent / 4, nC = c.shared_inter / 2;
     a.u_begin = part == 1 ? nAB : 0;
     a.u_end = part == 0 ? nAB : nAB + nC;
-    a.wait = part != 1;
+    a.wait = part != 1 || wait_x;
     if (T == 1) return run_dense_x<1>(h, a, 0, s);
     if (T == 2) return run_dense_x<2>(h, a, 1, s);
     return run_dense_x<4>(h, a, 2, s);

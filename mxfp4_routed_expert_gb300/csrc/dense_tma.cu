@@ -57,6 +57,11 @@ struct DenseTArgs {
     int units;                         // rows (RD: E+L, UP: H) or gate/up row pairs (SH: S)
     int wait;                          // consumers wait for the previous kernel (0: they read only x)
     int ns;                            // pipeline stages
+    // RD/SH from the residual: x = bf16(RMSNorm(hin) * pgain) made in the
+    // kernel (x unused); the first CTA of RD also stores it to xout
+    const float *hin;                  // [T, H] fp32
+    const __nv_bfloat16 *pgain;        // [H]
+    __nv_bfloat16 *xout;               // [T, H] or null
     int *err;
 };
 
@@ -126,6 +131,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_dense_tma(const __grid_constant
     uint64_t *full = reinterpret_cast<uint64_t *>(xs + TB * a.K);
     uint64_t *empty = full + NS;
     __shared__ float red[TB][kCW];
+    __shared__ double dred[TB][kCW];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int npieces = npieces_of(a);
 
@@ -196,7 +202,42 @@ __global__ void __launch_bounds__(kThreads, 1) k_dense_tma(const __grid_constant
 
     // ---------------- consumers: stage the activations as bf16 ----------------
     const int nct = kCW * 32;
-    if (a.mode != UP) {
+    if (a.mode != UP && a.hin) {
+        // RMSNorm in front of the MoE (k3_rmsnorm: squares summed in double,
+        // inv = (float)(1 / sqrt(mean + eps)), x = h * inv * gain in float)
+        double ss[TB];
+#pragma unroll
+        for (int t = 0; t < TB; t++) {
+            ss[t] = 0.0;
+            if (t < a.T)
+                for (int i = threadIdx.x; i < a.H / 4; i += nct) {
+                    const float4 v = reinterpret_cast<const float4 *>(a.hin + (size_t)t * a.H)[i];
+                    ss[t] += (double)v.x * v.x + (double)v.y * v.y + (double)v.z * v.z + (double)v.w * v.w;
+                }
+            ss[t] = warp_sum_d(ss[t]);
+            if (lane == 0) dred[t][warp] = ss[t];
+        }
+        asm volatile("bar.sync 1, %0;" ::"r"(nct));
+#pragma unroll
+        for (int t = 0; t < TB; t++) {
+            double tot = 0.0;
+#pragma unroll
+            for (int w = 0; w < kCW; w++) tot += dred[t][w];
+            const float inv = (float)(1.0 / sqrt(tot / (double)a.H + (double)a.eps));
+            const bool store = a.xout && blockIdx.x == 0 && t < a.T;
+            for (int i = threadIdx.x; i < a.H / 2; i += nct) {
+                __nv_bfloat162 xv = __floats2bfloat162_rn(0.f, 0.f);
+                if (t < a.T) {
+                    const float2 v = reinterpret_cast<const float2 *>(a.hin + (size_t)t * a.H)[i];
+                    const __nv_bfloat162 g = reinterpret_cast<const __nv_bfloat162 *>(a.pgain)[i];
+                    xv = __floats2bfloat162_rn(v.x * inv * __low2float(g), v.y * inv * __high2float(g));
+                }
+                reinterpret_cast<__nv_bfloat162 *>(xs + t * a.K)[i] = xv;
+                if (store) reinterpret_cast<__nv_bfloat162 *>(a.xout + (size_t)t * a.H)[i] = xv;
+            }
+        }
+        asm volatile("bar.sync 1, %0;" ::"r"(nct));
+    } else if (a.mode != UP) {
         const int nv = TB * a.H / 8;
         for (int i = threadIdx.x; i < nv; i += nct) {
             const int t = (8 * i) / a.H;
@@ -394,7 +435,7 @@ cudaError_t init_dense_tma(const k3moe_config &c)
 
 // part: 0 = router + down, 1 = shared gate/up, 2 = up (with the latent norm)
 cudaError_t launch_dense_tma(const k3moe &h, const LayerDev &w, const __nv_bfloat16 *x,
-                             __nv_bfloat16 *y, int T, cudaStream_t s, int part)
+                             __nv_bfloat16 *y, int T, cudaStream_t s, int part, const float *hin)
 {
     const k3moe_config &c = h.cfg;
     DenseTArgs a = {};
@@ -408,6 +449,11 @@ cudaError_t launch_dense_tma(const k3moe &h, const LayerDev &w, const __nv_bfloa
     a.eps = c.rms_eps;
     a.err = h.ws.err;
     a.x = x;
+    if (hin && part != 2) {
+        a.hin = hin;
+        a.pgain = w.post_gain;
+        a.xout = part == 0 ? h.ws.xn : nullptr;
+    }
     if (part == 0) {
         a.mode = RD;
         a.K = c.hidden;

@@ -58,6 +58,9 @@ struct LayerDev {
     // host block, the nine expert arrays in the layout of the device copy
     void *host_block = nullptr;
     const uint8_t *hsrc[9] = {};
+    // RMSNorm gain in front of the MoE (k3moe_load_post_norm), own allocation
+    const __nv_bfloat16 *post_gain = nullptr;
+    void *post_block = nullptr;
 };
 
 // Expert tier (k3moe_set_expert_tier): device slots caching routed experts
@@ -107,6 +110,7 @@ struct Workspace {
     int *gemm_tiles = nullptr;        // split-K arrival counters (kept at zero)
     __nv_bfloat16 *xbuf0 = nullptr;   // [Tm, H] staging (host forward, chain)
     __nv_bfloat16 *xbuf1 = nullptr;   // [Tm, H]
+    __nv_bfloat16 *xn = nullptr;      // [Tm, H] layer input made from the residual (forward_residual)
     int *err = nullptr;           // [4] device error word + detail
 };
 
@@ -123,6 +127,7 @@ struct k3moe {
     std::vector<k3::LayerDev> layers;
     k3::Workspace ws;
     int last_T = 0;
+    bool last_x = false;   // the last forward made its input from a residual (Workspace::xn)
     // launch shapes fixed at create time (no per-launch host queries)
     int grid_dense[3] = {0, 0, 0};   // k_dense_x resident-block cap for TB = 1, 2, 4
     // side stream for the shared experts, which overlap routing and permutation
@@ -148,8 +153,10 @@ namespace k3 {
 // ---- launchers (each returns cudaGetLastError()) -----------------------------
 // part 0: router logits and latent down projection; part 1: shared-expert
 // gate/up with SiTU; part 2: both.
+// wait_x: the shared gate/up (part 1) waits for the previous kernel, which
+// wrote its input x (else it reads the caller's x without waiting).
 cudaError_t launch_dense_x(const k3moe &h, const LayerDev &w, const __nv_bfloat16 *x, int T,
-                           cudaStream_t s, int part);
+                           cudaStream_t s, int part, bool wait_x = false);
 cudaError_t launch_route(const k3moe &h, const LayerDev &w, int T, cudaStream_t s);
 cudaError_t launch_perm(const k3moe &h, int T, cudaStream_t s, int step);
 int perm_chunks(int T);
@@ -159,6 +166,10 @@ cudaError_t launch_up(const k3moe &h, const LayerDev &w, __nv_bfloat16 *y, int T
                       cudaStream_t s);
 cudaError_t launch_chain_glue(const k3moe &h, const __nv_bfloat16 *y, __nv_bfloat16 *x_next,
                               int T, cudaStream_t s);
+// x = bf16(RMSNorm(h_in) * gain) per token into Workspace::xn, the layer's
+// first kernel (stream order)
+cudaError_t launch_residual_norm(const k3moe &h, const float *hin, const __nv_bfloat16 *gain, int T,
+                                 cudaStream_t s);
 cudaError_t launch_scale_scan(const uint8_t *p, size_t n, int *flag, cudaStream_t s);
 
 // ---- one-time set-up at k3moe_create (attributes, grid sizes) -------------------
@@ -189,8 +200,12 @@ bool dense_tma_fits(const k3moe_config &c, int TB);
 bool build_dense_tma_maps(const k3moe_config &c, LayerDev &w);
 // TMA-fed dense GEMVs for T <= 2. part 0: router + down; 1: shared gate/up;
 // 2: latent norm + up + shared down.
+// hin (parts 0 and 1): the kernel makes its input x = bf16(RMSNorm(hin) *
+// post_gain) itself from the fp32 residual (x unused); part 0 also stores it
+// in Workspace::xn.
 cudaError_t launch_dense_tma(const k3moe &h, const LayerDev &w, const __nv_bfloat16 *x,
-                             __nv_bfloat16 *y, int T, cudaStream_t s, int part);
+                             __nv_bfloat16 *y, int T, cudaStream_t s, int part,
+                             const float *hin = nullptr);
 bool expert_smem_fits(const k3moe_config &c);
 // expert tier: which touched experts are resident and which slots the others
 // take (one block), then the copy of the missed experts into their slots
@@ -402,6 +417,13 @@ inline cudaError_t launch_ordered(void (*kern)(KArgs...), int grid, int block, s
     cfg.attrs = nullptr;
     cfg.numAttrs = 0;
     return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+__device__ __forceinline__ double warp_sum_d(double v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
 }
 
 __device__ __forceinline__ float warp_sum(float v)

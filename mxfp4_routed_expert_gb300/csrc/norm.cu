@@ -1,7 +1,8 @@
-// The glue between stacked layers and the load-time scale-byte check.
+// The glue between stacked layers, the RMSNorm in front of the MoE and the
+// load-time scale-byte check.
 //
-// RMSNorm: out = x / sqrt(mean(x^2) + eps) (unit gain here), eps inside the
-// square root (kimi-k3-in-c README, Part II section 5, k3_rmsnorm).
+// RMSNorm: out = x / sqrt(mean(x^2) + eps) * gain, eps inside the square root
+// (kimi-k3-in-c README, Part II section 5, k3_rmsnorm).
 #include "k3moe_internal.cuh"
 
 namespace k3 {
@@ -43,6 +44,41 @@ cudaError_t launch_chain_glue(const k3moe &h, const __nv_bfloat16 *y, __nv_bfloa
                               int T, cudaStream_t s)
 {
     return launch_pdl(k_chain_glue, T, 256, 0, s, y, x_next, h.cfg.hidden, h.cfg.rms_eps);
+}
+
+// x[t] = bf16(h[t] * inv * g), inv = (float)(1 / sqrt(mean(h[t]^2) + eps)): the
+// post-attention RMSNorm that feeds the MoE (the decoder layer's post_norm in
+// front of k3_moe, kimi-k3-in-c README, Part II; k3_rmsnorm of section 5 sums
+// the squares in double and forms inv in double).
+__global__ void __launch_bounds__(256) k_residual_norm(const float *hin, const __nv_bfloat16 *g,
+                                                       __nv_bfloat16 *x, int H, float eps)
+{
+    __shared__ double red[8];
+    const int t = blockIdx.x;
+    const float *a = hin + (size_t)t * H;
+    pdl_launch_dependents();
+    double ss = 0.0;
+    for (int i = threadIdx.x; i < H; i += blockDim.x) {
+        const double v = a[i];
+        ss = fma(v, v, ss);
+    }
+    ss = warp_sum_d(ss);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    double tot = 0.0;
+#pragma unroll
+    for (int w = 0; w < 8; w++) tot += red[w];
+    const float inv = (float)(1.0 / sqrt(tot / (double)H + (double)eps));
+    for (int i = threadIdx.x; i < H; i += blockDim.x)
+        x[(size_t)t * H + i] = __float2bfloat16_rn(a[i] * inv * __bfloat162float(g[i]));
+}
+
+cudaError_t launch_residual_norm(const k3moe &h, const float *hin, const __nv_bfloat16 *gain, int T,
+                                 cudaStream_t s)
+{
+    // the layer's first kernel: plain stream order, like every layer's first
+    return launch_ordered(k_residual_norm, T, 256, 0, s, hin, gain, h.ws.xn, h.cfg.hidden,
+                          h.cfg.rms_eps);
 }
 
 // flag[0] += number of bytes equal to 255 in p[0, n).

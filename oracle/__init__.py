@@ -160,6 +160,30 @@ def rmsnorm(x, gain=None, eps: float = 1e-5) -> np.ndarray:
     return out
 
 
+def round_bf16(v) -> np.ndarray:
+    """fp64 -> bf16 bit patterns, round to nearest with ties to even, overflow
+    to infinity: the 8 significant bits of bf16 (7 stored), with the fp32
+    exponent range and subnormals down to 2^-133. The value is rounded once,
+    at its own unit in the last place."""
+    v = np.asarray(v, dtype=np.float64)
+    a = np.abs(v)
+    _, e = np.frexp(a)                                 # a = m * 2^e, m in [0.5, 1)
+    ulp = np.maximum(e - 8, -133)                      # 2^(e-8): the last of 8 bits
+    q = np.ldexp(np.round(np.ldexp(a, -ulp)), ulp)     # np.round: ties to even; exact
+    with np.errstate(over="ignore"):
+        mag = (q.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)   # q fits exactly
+    return np.where(np.signbit(v), mag | np.uint16(0x8000), mag).astype(np.uint16)
+
+
+def residual_input(h, gain_bits, eps: float = 1e-5) -> np.ndarray:
+    """x = RMSNorm(h) * gain per token in fp64, the input the decoder hands to
+    the MoE (kimi-k3-in-c README, Part II: post_norm then k3_moe; section 5
+    k3_rmsnorm). h [T, H] (any float type), gain bf16 bits [H]."""
+    h = np.asarray(h, dtype=np.float64)
+    g = (np.asarray(gain_bits, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return np.stack([rmsnorm(row, g, eps) for row in h])
+
+
 # ---- router / permutation ------------------------------------------------------------
 
 def router_token(x, Wr_bits, bias, k: int, renorm: int = 1, routed_scale: float = 1.0):

@@ -111,6 +111,26 @@ class Layer:
         assert st == 0, self.km.strerror(st)
         return y.cpu().numpy().view(np.uint16)
 
+    def forward_residual(self, h_f32: np.ndarray, layer: int = 0):
+        """y (bf16 bits) of the layer on bf16(RMSNorm(h) * post-norm gain)."""
+        import torch
+        T = h_f32.shape[0]
+        hd = torch.from_numpy(np.ascontiguousarray(h_f32, np.float32)).cuda()
+        y = torch.empty((T, self.shape.hidden), dtype=torch.int16, device="cuda")
+        self.km.k3moe_forward_residual(self.h, layer, hd, y, T)
+        torch.cuda.synchronize()
+        st = self.km.k3moe_sync_status(self.h)
+        assert st == 0, self.km.strerror(st)
+        return y.cpu().numpy().view(np.uint16)
+
+    def layer_input(self, T):
+        """bf16 bits [T, H] of the input the last residual forward made."""
+        import torch
+        buf = torch.empty((T, self.shape.hidden), dtype=torch.int16, device="cuda")
+        self.km.k3moe_get_intermediate(self.h, self.km.K3MOE_T_X, buf, buf.numel() * 2)
+        torch.cuda.synchronize()
+        return buf.cpu().numpy().view(np.uint16)
+
     def routing(self, T):
         import torch
         s = self.shape

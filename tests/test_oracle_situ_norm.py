@@ -108,3 +108,49 @@ def test_rmsnorm_scale_invariant_without_eps():
     x = np.linspace(-2, 3, 37)
     np.testing.assert_allclose(oracle.rmsnorm(7.0 * x, None, 0.0), oracle.rmsnorm(x, None, 0.0),
                                rtol=1e-14)
+
+
+# ---- the layer input made from the residual stream ---------------------------------
+
+def test_round_bf16_exact_values():
+    """Round to nearest, ties to even, at bf16's 8 significant bits."""
+    cases = [
+        (1.0, 0x3F80), (-1.5, 0xBFC0), (3.0, 0x4040), (0.0, 0x0000), (-0.0, 0x8000),
+        (1.0 + 2.0 ** -8, 0x3F80),              # tie between 0x3F80 and 0x3F81: the even one
+        (1.0 + 3 * 2.0 ** -8, 0x3F82),          # tie between 0x3F81 and 0x3F82: the even one
+        (1.0 + 2.0 ** -8 + 2.0 ** -30, 0x3F81), # just above the tie
+        (1.0 - 2.0 ** -10, 0x3F80),             # below 1: ulp 2^-8, rounds up to 1
+        (2.0 ** -130, 0x0008),                  # subnormal: 8 * 2^-133
+        (2.0 ** -134, 0x0000),                  # half of the smallest subnormal, tie to even 0
+        (3 * 2.0 ** -134, 0x0002),              # 1.5 * 2^-133: tie between 1 and 2, even
+        ((2 - 2.0 ** -7) * 2.0 ** 127, 0x7F7F), # the largest finite bf16
+        ((2 - 2.0 ** -8) * 2.0 ** 127, 0x7F80), # tie above it: the even neighbour is infinity
+    ]
+    got = oracle.round_bf16(np.array([v for v, _ in cases], np.float64))
+    for (v, want), g in zip(cases, got):
+        assert int(g) == want, (v, hex(int(g)), hex(want))
+
+
+def test_round_bf16_is_nearest_on_a_sweep():
+    """Every rounded value is a nearest bf16 neighbour (checked by widening the
+    two candidates around it), over a sweep of magnitudes and signs."""
+    v = np.concatenate([np.linspace(-7.3, 9.1, 2001), np.geomspace(1e-30, 1e30, 301)])
+    bits = oracle.round_bf16(v).astype(np.uint32)
+    w = (bits << 16).view(np.float32).astype(np.float64)
+    up = ((bits + 1) << 16).view(np.float32).astype(np.float64)
+    dn = ((bits - 1) << 16).view(np.float32).astype(np.float64)
+    err = np.abs(w - v)
+    assert np.all(err <= np.abs(up - v)) and np.all(err <= np.abs(dn - v))
+
+
+def test_residual_input_closed_form():
+    """x = h / sqrt(mean(h^2) + eps) * gain per row."""
+    h = np.array([[3.0, 4.0, 0.0, 0.0], [1.0, 1.0, 1.0, 1.0]], np.float32)
+    g = np.array([0x3F80, 0x4000, 0xBF80, 0x3F00], np.uint16)   # 1, 2, -1, 0.5
+    eps = 1e-5
+    x = oracle.residual_input(h, g, eps)
+    inv0 = 1 / math.sqrt(25 / 4 + eps)
+    inv1 = 1 / math.sqrt(1 + eps)
+    np.testing.assert_allclose(x[0], [3 * inv0, 8 * inv0, 0.0, 0.0], rtol=1e-15)
+    np.testing.assert_allclose(x[1], [inv1, 2 * inv1, -inv1, 0.5 * inv1], rtol=1e-15)
+
