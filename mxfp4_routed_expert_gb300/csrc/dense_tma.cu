@@ -203,37 +203,38 @@ __global__ void __launch_bounds__(kThreads, 1) k_dense_tma(const __grid_constant
     // ---------------- consumers: stage the activations as bf16 ----------------
     const int nct = kCW * 32;
     if (a.mode != UP && a.hin) {
-        // RMSNorm in front of the MoE (k3_rmsnorm: squares summed in double,
-        // inv = (float)(1 / sqrt(mean + eps)), x = h * inv * gain in float)
-        double ss[TB];
+        // RMSNorm in front of the MoE (k3_rmsnorm sums the squares in double and
+        // forms inv = (float)(1 / sqrt(mean + eps)) in double; x = h * inv *
+        // gain in float). Each thread sums its squares in fp32 and the partial
+        // sums meet in double: this part's fp64 rate is too low for a double
+        // per element.
 #pragma unroll
         for (int t = 0; t < TB; t++) {
-            ss[t] = 0.0;
-            if (t < a.T)
-                for (int i = threadIdx.x; i < a.H / 4; i += nct) {
-                    const float4 v = reinterpret_cast<const float4 *>(a.hin + (size_t)t * a.H)[i];
-                    ss[t] += (double)v.x * v.x + (double)v.y * v.y + (double)v.z * v.z + (double)v.w * v.w;
-                }
-            ss[t] = warp_sum_d(ss[t]);
-            if (lane == 0) dred[t][warp] = ss[t];
+            const float sf = t < a.T ? residual_sumsq<8>(a.hin + (size_t)t * a.H, a.H / 4, threadIdx.x, nct) : 0.f;
+            const double sd = warp_sum_d((double)sf);
+            if (lane == 0) dred[t][warp] = sd;
+        }
+        asm volatile("bar.sync 1, %0;" ::"r"(nct));
+        if (threadIdx.x == 0) {   // one thread: the double divide and root are slow here
+#pragma unroll
+            for (int t = 0; t < TB; t++) {
+                double tot = 0.0;
+#pragma unroll
+                for (int w = 0; w < kCW; w++) tot += dred[t][w];
+                red[t][0] = (float)(1.0 / sqrt(tot / (double)a.H + (double)a.eps));
+            }
         }
         asm volatile("bar.sync 1, %0;" ::"r"(nct));
 #pragma unroll
         for (int t = 0; t < TB; t++) {
-            double tot = 0.0;
-#pragma unroll
-            for (int w = 0; w < kCW; w++) tot += dred[t][w];
-            const float inv = (float)(1.0 / sqrt(tot / (double)a.H + (double)a.eps));
-            const bool store = a.xout && blockIdx.x == 0 && t < a.T;
-            for (int i = threadIdx.x; i < a.H / 2; i += nct) {
-                __nv_bfloat162 xv = __floats2bfloat162_rn(0.f, 0.f);
-                if (t < a.T) {
-                    const float2 v = reinterpret_cast<const float2 *>(a.hin + (size_t)t * a.H)[i];
-                    const __nv_bfloat162 g = reinterpret_cast<const __nv_bfloat162 *>(a.pgain)[i];
-                    xv = __floats2bfloat162_rn(v.x * inv * __low2float(g), v.y * inv * __high2float(g));
-                }
-                reinterpret_cast<__nv_bfloat162 *>(xs + t * a.K)[i] = xv;
-                if (store) reinterpret_cast<__nv_bfloat162 *>(a.xout + (size_t)t * a.H)[i] = xv;
+            if (t < a.T) {
+                const float inv = red[t][0];
+                __nv_bfloat16 *o2 = (a.xout && blockIdx.x == 0) ? a.xout + (size_t)t * a.H : nullptr;
+                residual_write<4>(a.hin + (size_t)t * a.H, a.pgain, inv, xs + t * a.K, o2, a.H / 4,
+                                  threadIdx.x, nct);
+            } else {
+                for (int i = threadIdx.x; i < a.H / 8; i += nct)
+                    reinterpret_cast<uint4 *>(xs + t * a.K)[i] = make_uint4(0u, 0u, 0u, 0u);
             }
         }
         asm volatile("bar.sync 1, %0;" ::"r"(nct));

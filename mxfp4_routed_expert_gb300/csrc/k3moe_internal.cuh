@@ -426,6 +426,74 @@ __device__ __forceinline__ double warp_sum_d(double v)
     return v;
 }
 
+// ---- RMSNorm of one fp32 residual row into bf16 (the norm in front of the MoE)
+// Both passes keep V 16-byte loads in flight per thread (a row is read from
+// L2 by many CTAs; one load at a time would be latency-bound).
+
+// This thread's share of sum(h^2) over a row of n4 float4 (fp32 partial sum).
+template <int V>
+__device__ __forceinline__ float residual_sumsq(const float *row, int n4, int tid, int nthr)
+{
+    const float4 *hp = reinterpret_cast<const float4 *>(row);
+    float sf = 0.f;
+    for (int i0 = tid; i0 < n4; i0 += V * nthr) {
+        float4 v[V];
+#pragma unroll
+        for (int u = 0; u < V; u++) {
+            const int i = i0 + u * nthr;
+            v[u] = i < n4 ? hp[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < V; u++) {
+            sf = fmaf(v[u].x, v[u].x, sf);
+            sf = fmaf(v[u].y, v[u].y, sf);
+            sf = fmaf(v[u].z, v[u].z, sf);
+            sf = fmaf(v[u].w, v[u].w, sf);
+        }
+    }
+    return sf;
+}
+
+// out[i] = bf16(row[i] * inv * gain[i]) for this thread's float4 groups; a
+// second copy goes to out2 when it is not null.
+template <int V>
+__device__ __forceinline__ void residual_write(const float *row, const __nv_bfloat16 *gain, float inv,
+                                               __nv_bfloat16 *out, __nv_bfloat16 *out2, int n4, int tid,
+                                               int nthr)
+{
+    const float4 *hp = reinterpret_cast<const float4 *>(row);
+    const uint2 *gp = reinterpret_cast<const uint2 *>(gain);
+    for (int i0 = tid; i0 < n4; i0 += V * nthr) {
+        float4 v[V];
+        uint2 g[V];
+#pragma unroll
+        for (int u = 0; u < V; u++) {
+            const int i = i0 + u * nthr;
+            if (i < n4) {
+                v[u] = hp[i];
+                g[u] = gp[i];
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < V; u++) {
+            const int i = i0 + u * nthr;
+            if (i < n4) {
+                const __nv_bfloat162 g01 = *reinterpret_cast<const __nv_bfloat162 *>(&g[u].x);
+                const __nv_bfloat162 g23 = *reinterpret_cast<const __nv_bfloat162 *>(&g[u].y);
+                const __nv_bfloat162 a = __floats2bfloat162_rn(v[u].x * inv * __low2float(g01),
+                                                               v[u].y * inv * __high2float(g01));
+                const __nv_bfloat162 b = __floats2bfloat162_rn(v[u].z * inv * __low2float(g23),
+                                                               v[u].w * inv * __high2float(g23));
+                uint2 o;
+                o.x = *reinterpret_cast<const uint32_t *>(&a);
+                o.y = *reinterpret_cast<const uint32_t *>(&b);
+                reinterpret_cast<uint2 *>(out)[i] = o;
+                if (out2) reinterpret_cast<uint2 *>(out2)[i] = o;
+            }
+        }
+    }
+}
+
 __device__ __forceinline__ float warp_sum(float v)
 {
 #pragma unroll

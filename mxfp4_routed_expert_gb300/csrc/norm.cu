@@ -49,28 +49,27 @@ cudaError_t launch_chain_glue(const k3moe &h, const __nv_bfloat16 *y, __nv_bfloa
 // x[t] = bf16(h[t] * inv * g), inv = (float)(1 / sqrt(mean(h[t]^2) + eps)): the
 // post-attention RMSNorm that feeds the MoE (the decoder layer's post_norm in
 // front of k3_moe, kimi-k3-in-c README, Part II; k3_rmsnorm of section 5 sums
-// the squares in double and forms inv in double).
+// the squares in double and forms inv in double). Each thread sums its
+// squares in fp32 and the partial sums meet in double (fp64 is slow here).
 __global__ void __launch_bounds__(256) k_residual_norm(const float *hin, const __nv_bfloat16 *g,
                                                        __nv_bfloat16 *x, int H, float eps)
 {
     __shared__ double red[8];
+    __shared__ float inv_s;
     const int t = blockIdx.x;
     const float *a = hin + (size_t)t * H;
     pdl_launch_dependents();
-    double ss = 0.0;
-    for (int i = threadIdx.x; i < H; i += blockDim.x) {
-        const double v = a[i];
-        ss = fma(v, v, ss);
-    }
-    ss = warp_sum_d(ss);
+    const double ss = warp_sum_d((double)residual_sumsq<8>(a, H / 4, threadIdx.x, blockDim.x));
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
     __syncthreads();
-    double tot = 0.0;
+    if (threadIdx.x == 0) {   // one thread: the double divide and root are slow here
+        double tot = 0.0;
 #pragma unroll
-    for (int w = 0; w < 8; w++) tot += red[w];
-    const float inv = (float)(1.0 / sqrt(tot / (double)H + (double)eps));
-    for (int i = threadIdx.x; i < H; i += blockDim.x)
-        x[(size_t)t * H + i] = __float2bfloat16_rn(a[i] * inv * __bfloat162float(g[i]));
+        for (int w = 0; w < 8; w++) tot += red[w];
+        inv_s = (float)(1.0 / sqrt(tot / (double)H + (double)eps));
+    }
+    __syncthreads();
+    residual_write<8>(a, g, inv_s, x + (size_t)t * H, nullptr, H / 4, threadIdx.x, blockDim.x);
 }
 
 cudaError_t launch_residual_norm(const k3moe &h, const float *hin, const __nv_bfloat16 *gain, int T,
