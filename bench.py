@@ -71,6 +71,13 @@ WORKLOADS = {
                                desc="K3-shape single layer, decode T=1 from fp32 residual-stream "
                                     "rows (RMSNorm with the post-norm gain fused into the first "
                                     "kernels; rows rotate through a seeded pool of 64)"),
+    # the model's dense feed-forward layer 0 (hidden 7168, dense_inter 33792)
+    "dense_t1": dict(T=1, layers=1, dense=True,
+                     desc="K3 dense feed-forward layer 0 (hidden 7168, dense_inter 33792, bf16), "
+                          "decode T=1 (tokens rotate through a seeded pool of 64)"),
+    "dense_t4096": dict(T=4096, layers=1, dense=True,
+                        desc="K3 dense feed-forward layer 0 (hidden 7168, dense_inter 33792, bf16), "
+                             "prefill T=4096"),
     # expert tier: routed experts in pinned host memory, 896 device slots
     # shared by two layers; each step is one forward of one layer (alternating)
     "decode_t1_tier": dict(T=1, layers=2, tier=896, alternate=True,
@@ -161,6 +168,12 @@ def kernel_model(shape, T, n_touched):
         "up_shared_gemm": up,
         "chain_glue_rmsnorm": (4 * T * H, 0),
         "tier_plan": (0, 0), "tier_fill": (0, 0),   # set from the tier's counters
+        # dense feed-forward layer (no routed part): S is its width; per launch
+        "dense_gate_up_gemv": (2 * 2 * S * H + 2 * T * H + 4 * T * S, 0),
+        "dense_down_gemv": (2 * H * S + 4 * T * S + 2 * T * H, 0),
+        "dense_gate_up_gemm": sh,
+        "dense_down_gemm": (2 * H * S + 2 * T * S + 2 * T * H, 2 * T * S * H),
+        "residual_rmsnorm": (4 * T * H + 2 * H + 2 * T * H, 0),
     }
 
 
@@ -169,6 +182,8 @@ def layer_bytes(shape, T, n_touched):
     dense projections, the shared experts and the touched experts) plus the
     layer input and output."""
     H, L, E, I, S = shape.hidden, shape.latent, shape.n_experts, shape.moe_inter, shape.shared_inter
+    if E == 0:   # dense feed-forward layer
+        return 2 * 3 * S * H + 4 * T * H
     dense = 2 * (E * H + L * H + 2 * S * H + H * L + H * S)
     experts = n_touched * (3 * (I * L // 2 + I * L // 32))
     return dense + experts + 4 * T * H
@@ -177,10 +192,15 @@ def layer_bytes(shape, T, n_touched):
 # ---- inputs ----------------------------------------------------------------------
 
 def make_inputs(workload, seed=0, layer_index=0):
+    T = WORKLOADS[workload]["T"]
+    if WORKLOADS[workload].get("dense"):
+        shape = k3synth.K3_DENSE
+        d = k3synth.make_dense_layer(shape, seed)
+        x = k3synth.make_tokens(shape, seed, POOL if T == 1 else T, stream=7 if T == 1 else 13)
+        return shape, d, x
     shape = (k3synth.replace(k3synth.K3, n_experts=64) if workload.endswith("_e64")
              else k3synth.K3)
     d = k3synth.make_layer(shape, seed, layer_index, k3synth.K3_RECIPE)
-    T = WORKLOADS[workload]["T"]
     if workload in ("decode_t1", "decode_t1_e64"):
         x = k3synth.make_tokens(shape, seed, POOL, stream=7)
     elif workload == "decode_t1_residual":
@@ -301,12 +321,30 @@ def host_link_gbs():
 
 # ---- oracle timing (CPU baseline and reference arm) ----------------------------------
 
+def oracle_x(workload, shape, x):
+    """bf16 bits of the layer input the oracle takes: the workload's tokens, or
+    for a residual workload the oracle's own RMSNorm of the residual rows."""
+    if not WORKLOADS[workload].get("residual"):
+        return x
+    import oracle
+    return oracle.round_bf16(oracle.residual_input(x, k3synth.post_norm_gain(shape, 0), shape.rms_eps))
+
+
+def oracle_rows(shape, d, x, rows):
+    """The oracle on tokens `rows` of x: the LatentMoE layer, or the dense
+    feed-forward layer for a configuration without a routed part."""
+    import oracle
+    if shape.n_experts == 0:
+        return oracle.dense_ffn(x[rows], d["sh_w1"], d["sh_w3"], d["sh_w2"], shape.situ_b1, shape.situ_b2)
+    return oracle.layer_forward(shape, d, x, rows=rows)
+
+
 def time_oracle(shape, d, x, n_tokens):
     import oracle
     oracle.build()
     rows = (np.arange(n_tokens) % x.shape[0]).astype(np.int32)   # the pool repeats when it is smaller
     t0 = time.perf_counter()
-    oracle.layer_forward(shape, d, x, rows=rows)
+    oracle_rows(shape, d, x, rows)
     dt = time.perf_counter() - t0
     return rows.size, dt
 
@@ -494,11 +532,7 @@ def run_native(args, rank, world):
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         n_tok = 320                      # about 10-20 s of the oracle on the machine's cores
-        xs_host = xpool if T == 1 else xpool[:T]
-        if residual:   # the oracle's layer on the oracle's made input
-            import oracle
-            xs_host = oracle.round_bf16(oracle.residual_input(xs_host, k3synth.post_norm_gain(shape, 0),
-                                                              shape.rms_eps))
+        xs_host = oracle_x(args.workload, shape, xpool if T == 1 else xpool[:T])
         nrow, dt = time_oracle(shape, oracle_layer, xs_host, n_tok)
         cpu = {"value": round(nrow / dt / layers_per_step, 4), "unit": UNIT,
                "cores": omp_threads(nrow), "kind": "oracle",
@@ -531,23 +565,26 @@ def run_native(args, rank, world):
 
 
 def run_reference(args, rank, world):
-    """The oracle as the reference arm: each step is the oracle on one bounded
-    sample of the workload (T=1: the whole step; larger T: 4 tokens)."""
+    """The oracle as the reference arm: each step is one token of the workload
+    (a bounded sample; one K3 token is seconds of fp64 work). The K steps' tokens
+    go to the oracle as one batch, spread over the host cores by its OpenMP
+    loop over tokens (each token's arithmetic unchanged), so that K steps end
+    within minutes; the value is tokens per second of that batch."""
     wl = WORKLOADS[args.workload]
     T, n_layers = wl["T"], wl["layers"]
+    layers_per_step = 1 if wl.get("alternate") else n_layers
     shape, d, x = make_inputs(args.workload)
+    x = oracle_x(args.workload, shape, x)
     import oracle
     oracle.build()
-    per = 1 if T == 1 else 4
-    for i in range(args.warmup):
-        oracle.layer_forward(shape, d, x, rows=np.array([i % x.shape[0]], np.int32))
+    per = 1
+    oracle_rows(shape, d, x, (np.arange(args.warmup) % x.shape[0]).astype(np.int32))
+    rows = ((np.arange(args.steps * per) + args.warmup) % x.shape[0]).astype(np.int32)
     t0 = time.perf_counter()
-    for i in range(args.steps):
-        rows = (np.arange(per) + i * per) % x.shape[0]
-        oracle.layer_forward(shape, d, x, rows=rows.astype(np.int32))
+    oracle_rows(shape, d, x, rows)
     dt = time.perf_counter() - t0
-    value = per * args.steps / dt / n_layers
-    cores = omp_threads(per)
+    value = per * args.steps / dt / layers_per_step
+    cores = omp_threads(per * args.steps)
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -558,7 +595,8 @@ def run_reference(args, rank, world):
                    "tokens_per_step": T, "layers": n_layers},
         "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "kind": "oracle",
                          "cores": cores,
-                         "sample": f"{per} token(s) per step through one layer (fp64 C oracle)"
+                         "sample": f"{per} token per step through one layer (fp64 C oracle), the "
+                                   f"{args.steps} steps' tokens as one batch over {cores} cores"
                                    + (f"; chain value = per-layer rate / {n_layers}" if layers_per_step > 1 else "")},
         "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},

@@ -34,6 +34,7 @@ TX, TROUTER, TBIAS, TDOWN, TUP, TGAIN, TSH1, TSH3, TSH2 = 1, 2, 3, 4, 5, 6, 7, 8
 TW1P, TW1S, TW3P, TW3S, TW2P, TW2S = 10, 11, 12, 13, 14, 15
 TPERM, TCOVER = 16, 17
 TRESID, TRESID_SCALE, TPOSTGAIN = 18, 19, 20
+TD1, TD3, TD2 = 21, 22, 23
 
 MXFP4_GROUP = 32
 
@@ -163,6 +164,8 @@ class Shape:
 K3 = Shape(hidden=7168, latent=3584, n_experts=896, topk=16, moe_inter=3072, shared_inter=6144)
 # The small layer the oracle runs in well under a second.
 TINY = Shape(hidden=256, latent=128, n_experts=32, topk=4, moe_inter=128, shared_inter=256)
+# The model's dense feed-forward layer 0: hidden 7168, dense_inter 33792.
+K3_DENSE = Shape(hidden=7168, latent=0, n_experts=0, topk=0, moe_inter=0, shared_inter=33792)
 
 
 @dataclass(frozen=True)
@@ -265,6 +268,20 @@ def make_residual(shape: Shape, seed: int, T: int, stream: int = 0,
     return rows.astype(np.float32)
 
 
+def dense_shape(hidden: int, dense_inter: int) -> "Shape":
+    """The configuration of a dense feed-forward layer: no routed part."""
+    return Shape(hidden=hidden, latent=0, n_experts=0, topk=0, moe_inter=0, shared_inter=dense_inter)
+
+
+def make_dense_layer(shape: "Shape", seed: int, sigma: float = 0.02) -> dict:
+    """Weights of a dense feed-forward layer: sh_w1/sh_w3 [F, H], sh_w2 [H, F]
+    bf16 N(0, sigma), F = shape.shared_inter."""
+    H, F = shape.hidden, shape.shared_inter
+    return {"sh_w1": normal_bf16((F, H), key(seed, TD1), 0.0, sigma),
+            "sh_w3": normal_bf16((F, H), key(seed, TD3), 0.0, sigma),
+            "sh_w2": normal_bf16((H, F), key(seed, TD2), 0.0, sigma)}
+
+
 def post_norm_gain(shape: Shape, seed: int, layer: int = 0) -> np.ndarray:
     """bf16 bits [H] of the RMSNorm gain in front of the MoE: 1 + N(0, 0.1)."""
     return normal_bf16((shape.hidden,), key(seed, TPOSTGAIN, layer), 1.0, 0.1)
@@ -318,6 +335,6 @@ def with_bias(layer: dict, bias: np.ndarray) -> dict:
 
 
 __all__ = ["Shape", "K3", "TINY", "WeightRecipe", "K3_RECIPE", "TINY_RECIPE", "make_layer",
-           "make_residual", "post_norm_gain",
+           "make_residual", "post_norm_gain", "dense_shape", "make_dense_layer", "K3_DENSE",
            "make_tokens", "covering_tokens", "zipf_bias", "with_bias", "bf16_bits_to_f32",
            "round_bf16", "build", "key", "replace", "MXFP4_GROUP"]

@@ -205,6 +205,12 @@ def layer_weights(tensors: dict, n_experts: int, where: int = K3MOE_HOST):
     w = k3moe_layer_weights()
     w.struct_size = ctypes.sizeof(k3moe_layer_weights)
     w.where = where
+    if n_experts == 0:   # dense feed-forward layer: the three matrices only
+        w.shared_w1 = addr(tensors["sh_w1"])
+        w.shared_w3 = addr(tensors["sh_w3"])
+        w.shared_w2 = addr(tensors["sh_w2"])
+        keep.append(tensors)
+        return w, keep
     w.router_w = addr(tensors["router_w"])
     w.router_bias = addr(tensors.get("router_bias"))
     w.down_w = addr(tensors["down_w"])

@@ -19,10 +19,13 @@ int check_config(const k3moe_config *c)
 {
     if (!c) return K3MOE_ERR_INVALID_ARG;
     if (c->struct_size != sizeof(k3moe_config)) return K3MOE_ERR_CONFIG;
+    // all four routed-part sizes 0: a dense feed-forward layer
+    const bool dense = c->n_experts == 0 && c->topk == 0 && c->latent == 0 && c->moe_inter == 0;
     const int32_t pos[] = {c->hidden, c->latent, c->n_experts, c->topk, c->moe_inter,
                            c->shared_inter, c->max_layers, c->max_tokens};
     for (int32_t v : pos)
-        if (v <= 0) return K3MOE_ERR_CONFIG;
+        if (v <= 0 && !(dense && v == 0)) return K3MOE_ERR_CONFIG;
+    if (c->hidden <= 0 || c->shared_inter <= 0) return K3MOE_ERR_CONFIG;
     if (c->device < 0) return K3MOE_ERR_CONFIG;
     if ((c->renorm != 0 && c->renorm != 1) || (c->latent_norm != 0 && c->latent_norm != 1))
         return K3MOE_ERR_CONFIG;
@@ -39,6 +42,9 @@ int check_config(const k3moe_config *c)
     if ((long long)c->max_tokens * c->topk > 65536) return K3MOE_ERR_SHAPE;
     // fp16 partial sums in the expert GEMVs: |SiTU| <= b1*b2 must stay small
     if ((double)c->situ_b1 * c->situ_b2 > 512.0) return K3MOE_ERR_SHAPE;
+    // the dense layer runs decode batches through the TMA-fed kernels, two
+    // tokens at a time
+    if (dense && (!dense_tma_fits(*c, 1) || !dense_tma_fits(*c, 2))) return K3MOE_ERR_SHAPE;
     return K3MOE_OK;
 }
 
@@ -223,8 +229,32 @@ int run_layer(k3moe *h, const LayerDev &w, const __nv_bfloat16 *x, __nv_bfloat16
     // overlap (the experts need every SM once the shared experts hold them).
     // Batched (T >= 16): the shared gate/up GEMM on a side stream after
     // router+down, joined before the experts.
-    const bool tma = T <= 2 && h->dense_tma_ok[T - 1];
     const bool gemm = T >= kGemmMinTokens && h->gemm_ok;
+    if (is_dense(h->cfg)) {
+        // dense feed-forward layer: gate/up with SiTU, then the down projection
+        if (hin) {
+            K3_STEP("residual_rmsnorm", launch_residual_norm(*h, hin, w.post_gain, T, s));
+            x = h->ws.xn;
+        }
+        if (gemm) {
+            K3_STEP("dense_gate_up_gemm", launch_dense_gemm(*h, w, x, nullptr, T, s, 1));
+            K3_STEP("dense_down_gemm", launch_dense_gemm(*h, w, nullptr, y, T, s, 2));
+        } else {
+            // decode: two tokens per pass of the TMA-fed kernels; the first
+            // kernel opens the layer in stream order unless it follows the norm
+            const size_t H = h->cfg.hidden;
+            for (int t0 = 0; t0 < T; t0 += 2) {
+                const int n = T - t0 < 2 ? T - t0 : 2;
+                K3_STEP("dense_gate_up_gemv", launch_dense_tma(*h, w, x + t0 * H, nullptr, n, s, 1, nullptr, t0,
+                                                               t0 == 0 && !hin, hin != nullptr));
+                K3_STEP("dense_down_gemv", launch_dense_tma(*h, w, nullptr, y + t0 * H, n, s, 2, nullptr, t0));
+            }
+        }
+        h->last_T = T;
+        h->last_x = hin != nullptr;
+        return K3MOE_OK;
+    }
+    const bool tma = T <= 2 && h->dense_tma_ok[T - 1];
     const bool egemm = use_expert_gemm(*h, T);
     const float *fused = (hin && tma) ? hin : nullptr;   // made inside the dense kernels
     if (hin && !tma) {
@@ -390,8 +420,9 @@ int k3moe_create(const k3moe_config *cfg, k3moe **out)
     h->dense_tma_ok[0] = dense_tma_fits(*cfg, 1);
     h->dense_tma_ok[1] = dense_tma_fits(*cfg, 2);
     // every TMA box of the GEMMs must lie inside its tensor: 128-row weight tiles
-    h->gemm_ok = cfg->n_experts >= 128 && cfg->latent >= 128 && cfg->shared_inter >= 128 &&
-                 cfg->hidden >= 128;
+    h->gemm_ok = is_dense(*cfg) ? (cfg->shared_inter >= 128 && cfg->hidden >= 128)
+                                : (cfg->n_experts >= 128 && cfg->latent >= 128 && cfg->shared_inter >= 128 &&
+                                   cfg->hidden >= 128);
     h->egemm_ok = expert_gemm_ok(*cfg);
     h->layers.resize((size_t)cfg->max_layers);
     *out = h;
@@ -426,11 +457,12 @@ int k3moe_load_layer(k3moe *h, int layer, const k3moe_layer_weights *w)
     if (layer < 0 || layer >= h->cfg.max_layers) return K3MOE_ERR_INVALID_ARG;
     if (w->where != K3MOE_HOST && w->where != K3MOE_DEVICE) return K3MOE_ERR_INVALID_ARG;
     const k3moe_config &c = h->cfg;
-    if (!w->router_w || !w->down_w || !w->up_w || !w->shared_w1 || !w->shared_w3 ||
-        !w->shared_w2 || !w->w1_packed || !w->w1_scale || !w->w3_packed || !w->w3_scale ||
-        !w->w2_packed || !w->w2_scale)
+    const bool dense = is_dense(c);   // only the three feed-forward matrices
+    if (!w->shared_w1 || !w->shared_w3 || !w->shared_w2) return K3MOE_ERR_INVALID_ARG;
+    if (!dense && (!w->router_w || !w->down_w || !w->up_w || !w->w1_packed || !w->w1_scale ||
+                   !w->w3_packed || !w->w3_scale || !w->w2_packed || !w->w2_scale))
         return K3MOE_ERR_INVALID_ARG;
-    if (c.latent_norm && !w->latent_gain) return K3MOE_ERR_INVALID_ARG;
+    if (!dense && c.latent_norm && !w->latent_gain) return K3MOE_ERR_INVALID_ARG;
     for (int e = 0; e < c.n_experts; e++)
         if (!w->w1_packed[e] || !w->w1_scale[e] || !w->w3_packed[e] || !w->w3_scale[e] ||
             !w->w2_packed[e] || !w->w2_scale[e])
@@ -500,15 +532,17 @@ int k3moe_load_layer(k3moe *h, int layer, const k3moe_layer_weights *w)
 #define K3_CP(dst, src, n, k)                                             \
     if (rc == K3MOE_OK && cudaMemcpy((dst), (src), (n), (k)) != cudaSuccess) \
         rc = K3MOE_ERR_CUDA;
-    K3_CP(router, w->router_w, z.router, kind);
-    if (w->router_bias) {
+    if (!dense) K3_CP(router, w->router_w, z.router, kind);
+    if (w->router_bias && !dense) {
         K3_CP(bias, w->router_bias, z.bias, kind);
     } else if (rc == K3MOE_OK && cudaMemset(bias, 0, z.bias) != cudaSuccess) {
         rc = K3MOE_ERR_CUDA;
     }
-    K3_CP(down, w->down_w, z.down, kind);
-    K3_CP(up, w->up_w, z.up, kind);
-    if (w->latent_gain) K3_CP(gain, w->latent_gain, z.gain, kind);
+    if (!dense) {
+        K3_CP(down, w->down_w, z.down, kind);
+        K3_CP(up, w->up_w, z.up, kind);
+        if (w->latent_gain) K3_CP(gain, w->latent_gain, z.gain, kind);
+    }
     K3_CP(sh1, w->shared_w1, z.sh13, kind);
     K3_CP(sh3, w->shared_w3, z.sh13, kind);
     K3_CP(sh2, w->shared_w2, z.sh2, kind);
@@ -523,7 +557,7 @@ int k3moe_load_layer(k3moe *h, int layer, const k3moe_layer_weights *w)
         K3_CP(ex[5] + e * se2, w->w2_scale[e], se2, ekind);
     }
 #undef K3_CP
-    if (rc == K3MOE_OK) {
+    if (rc == K3MOE_OK && !dense) {
         // scale checks and row maxima read the arrays where they live (the
         // host block through its device mapping in the tier)
         int bad = 0;
@@ -795,7 +829,8 @@ int k3moe_set_expert_tier(k3moe *h, int slots)
     for (const auto &l : h->layers)
         if (l.loaded) return K3MOE_ERR_INVALID_ARG;
     const k3moe_config &c = h->cfg;
-    if (slots != 0 && (slots < c.n_experts || slots > kTierMaxSlots)) return K3MOE_ERR_INVALID_ARG;
+    if (slots != 0 && (is_dense(c) || slots < c.n_experts || slots > kTierMaxSlots))
+        return K3MOE_ERR_INVALID_ARG;
     if (cudaSetDevice(c.device) != cudaSuccess) return K3MOE_ERR_CUDA;
     free_tier(h->tier);
     if (slots == 0) return K3MOE_OK;

@@ -332,12 +332,14 @@ cudaError_t launch_dense_gemm(const k3moe &h, const LayerDev &w, const __nv_bflo
         g.BN = pick_bn(T, mtiles, h.sm_count);
         g.KTA = c.latent / BK;
         g.KT = (c.latent + c.shared_inter) / BK;
-        ok = tc::make_map_bf16_sw128(&a0, w.up_w, c.hidden, c.latent, c.latent, BM) &&
+        // a dense feed-forward layer has no latent columns: KTA = 0, a0 unused
+        ok = (is_dense(c) || tc::make_map_bf16_sw128(&a0, w.up_w, c.hidden, c.latent, c.latent, BM)) &&
              tc::make_map_bf16_sw128(&a1, w.sh_w2, c.hidden, c.shared_inter, c.shared_inter, BM) &&
              tc::make_map_bf16_sw128(&b, h.ws.act, T, c.latent + c.shared_inter,
                                      c.latent + c.shared_inter, g.BN);
     }
     if (!ok) return cudaErrorInvalidValue;
+    if (part == 2 && is_dense(c)) a0 = a1;
     const int ntiles = (T + g.BN - 1) / g.BN;
     int splits = 1;
     if (T <= kSplitTokensMax) {

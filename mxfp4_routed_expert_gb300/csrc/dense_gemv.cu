@@ -94,6 +94,7 @@ struct DenseXArgs {
 };
 
 constexpr int kGemvWarps = 8;
+constexpr size_t kGemvSmemMax = 227 * 1024;
 constexpr int kStageUnroll = 8;   // staging loads in flight per thread
 
 template <int TB>
@@ -296,10 +297,15 @@ static cudaError_t init_tb(k3moe &h, int slot)
     const size_t su = (size_t)TB * (c.latent + c.shared_inter) * sizeof(float);
     cudaError_t e = cudaFuncSetAttribute(k_dense_x<TB>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sx);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(k_up<TB>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)su);
-    if (e != cudaSuccess) return e;
     h.grid_dense[slot] = grid_for(h, k_dense_x<TB>, sx, 1 << 30);   // resident-block cap
-    h.grid_up[slot] = grid_for(h, k_up<TB>, su, c.hidden / 4);
+    // k_up stages TB rows of L+S floats: a wide dense feed-forward layer does
+    // not fit (it never runs k_up); grid 0 marks the width unusable
+    h.grid_up[slot] = 0;
+    if (su <= kGemvSmemMax) {
+        e = cudaFuncSetAttribute(k_up<TB>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)su);
+        if (e != cudaSuccess) return e;
+        h.grid_up[slot] = grid_for(h, k_up<TB>, su, c.hidden / 4);
+    }
     return cudaGetLastError();
 }
 
@@ -356,6 +362,7 @@ cudaError_t launch_dense_x(const k3moe &h, const LayerDev &w, const __nv_bfloat1
 template <int TB>
 static cudaError_t run_up(const k3moe &h, const UpArgs &a, int slot, cudaStream_t s)
 {
+    if (h.grid_up[slot] == 0) return cudaErrorInvalidValue;
     const size_t smem = (size_t)TB * (a.L + a.S) * sizeof(float);
     return launch_pdl(k_up<TB>, h.grid_up[slot], kGemvWarps * 32, smem, s, a);
 }

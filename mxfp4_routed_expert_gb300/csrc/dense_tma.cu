@@ -397,6 +397,16 @@ static bool make_row_maps(RowMaps *m, const void *base, int rows, int cols)
 
 static bool make_dense_maps(const k3moe_config &c, const LayerDev &w, int part, DenseMaps *mp)
 {
+    if (is_dense(c)) {   // feed-forward layer: gate/up, then the down matrix alone
+        if (part == 1)
+            return make_row_maps(&mp->a, w.sh_w1, c.shared_inter, c.hidden) &&
+                   make_row_maps(&mp->b, w.sh_w3, c.shared_inter, c.hidden);
+        if (part == 2 && make_row_maps(&mp->b, w.sh_w2, c.hidden, c.shared_inter)) {
+            mp->a = mp->b;   // no latent columns: matrix a is never read
+            return true;
+        }
+        return false;
+    }
     if (part == 0)
         return make_row_maps(&mp->a, w.router_w, c.n_experts, c.hidden) &&
                make_row_maps(&mp->b, w.down_w, c.latent, c.hidden);
@@ -413,7 +423,7 @@ static_assert(sizeof(DenseMaps) == 6 * sizeof(CUtensorMap), "six maps per part")
 bool build_dense_tma_maps(const k3moe_config &c, LayerDev &w)
 {
     w.dense_maps_ok = false;
-    for (int part = 0; part < 3; part++) {
+    for (int part = is_dense(c) ? 1 : 0; part < 3; part++) {
         DenseMaps mp;
         if (!make_dense_maps(c, w, part, &mp)) return false;
         memcpy(w.dense_maps[part], &mp, sizeof(mp));
@@ -436,7 +446,8 @@ cudaError_t init_dense_tma(const k3moe_config &c)
 
 // part: 0 = router + down, 1 = shared gate/up, 2 = up (with the latent norm)
 cudaError_t launch_dense_tma(const k3moe &h, const LayerDev &w, const __nv_bfloat16 *x,
-                             __nv_bfloat16 *y, int T, cudaStream_t s, int part, const float *hin)
+                             __nv_bfloat16 *y, int T, cudaStream_t s, int part, const float *hin,
+                             int t0, bool ordered, bool wait)
 {
     const k3moe_config &c = h.cfg;
     DenseTArgs a = {};
@@ -468,15 +479,15 @@ cudaError_t launch_dense_tma(const k3moe &h, const LayerDev &w, const __nv_bfloa
         a.K = c.hidden;
         a.wa = w.sh_w1;
         a.wb = w.sh_w3;
-        a.out_a = h.ws.cat;
+        a.out_a = h.ws.cat + (size_t)t0 * (c.latent + c.shared_inter);
         a.units = c.shared_inter;
     } else {
         a.mode = UP;
         a.K = c.latent + c.shared_inter;
         a.wa = w.up_w;
         a.wb = w.sh_w2;
-        a.acc = h.ws.acc;
-        a.cat = h.ws.cat;
+        a.acc = h.ws.acc + (size_t)t0 * c.latent;
+        a.cat = h.ws.cat + (size_t)t0 * (c.latent + c.shared_inter);
         a.gain = c.latent_norm ? w.gain : nullptr;
         a.y = y;
         a.units = c.hidden;
@@ -492,8 +503,8 @@ cudaError_t launch_dense_tma(const k3moe &h, const LayerDev &w, const __nv_bfloa
     // The shared gate/up reads only the layer input x and writes its own output
     // rows; the layer's first kernel (router+down, launched in stream order)
     // has already waited for everything the input depends on.
-    a.wait = a.mode != SH;
-    if (a.mode == RD)
+    a.wait = a.mode != SH || wait;
+    if (a.mode == RD || ordered)
         return TB == 1 ? launch_ordered(k_dense_tma<1>, grid, kThreads, smem, s, mp, a)
                        : launch_ordered(k_dense_tma<2>, grid, kThreads, smem, s, mp, a);
     return TB == 1 ? launch_pdl(k_dense_tma<1>, grid, kThreads, smem, s, mp, a)

@@ -23,6 +23,11 @@ constexpr int kZPad = 16;           // fp16 padding after each z16 row (holds it
 constexpr int kSplitTokensMax = 128;  // tensor-core GEMMs split K only up to this many tokens
 constexpr int kGemmMinTokens = 16;    // tensor-core dense GEMMs from this many tokens on
 
+// A configuration with n_experts = topk = latent = moe_inter = 0 is a dense
+// feed-forward layer (the model's layer 0): y = W2 . SiTU(W1 x, W3 x) with
+// the shared-expert weights and width shared_inter.
+inline bool is_dense(const k3moe_config &c) { return c.n_experts == 0; }
+
 // Device error codes latched in Workspace::err (first one wins).
 enum : int { kErrNone = 0, kErrBounds = 1, kErrTimeout = 2 };
 
@@ -203,9 +208,13 @@ bool build_dense_tma_maps(const k3moe_config &c, LayerDev &w);
 // hin (parts 0 and 1): the kernel makes its input x = bf16(RMSNorm(hin) *
 // post_gain) itself from the fp32 residual (x unused); part 0 also stores it
 // in Workspace::xn.
+// t0: the launch covers tokens t0.. of the batch (x and y already offset; the
+// workspace rows are offset here). ordered: launch in plain stream order (the
+// first kernel of a dense feed-forward layer).
 cudaError_t launch_dense_tma(const k3moe &h, const LayerDev &w, const __nv_bfloat16 *x,
                              __nv_bfloat16 *y, int T, cudaStream_t s, int part,
-                             const float *hin = nullptr);
+                             const float *hin = nullptr, int t0 = 0, bool ordered = false,
+                             bool wait = false);
 bool expert_smem_fits(const k3moe_config &c);
 // expert tier: which touched experts are resident and which slots the others
 // take (one block), then the copy of the missed experts into their slots

@@ -83,6 +83,7 @@ def _L():
         lib.orc_layer_forward.argtypes = [p, p, p, i, p, i, p, p]
         lib.orc_route.argtypes = [p, p, p, i, p, p, p, p, p]
         lib.orc_chain_glue.argtypes = [p, p, i, i, d]
+        lib.orc_dense_ffn.argtypes = [p, p, i, p, p, p, i, i, d, d]
         lib.orc_group_size.restype = i
         _lib = lib
     return _lib
@@ -297,6 +298,19 @@ def layer_forward(shape, layer: dict, x_bits, rows=None, trace: bool = False):
                            ctypes.byref(tr) if tr is not None else None)
     del keep
     return (y, arrs) if trace else y
+
+
+def dense_ffn(x_bits, w1_bits, w3_bits, w2_bits, b1: float = 4.0, b2: float = 25.0) -> np.ndarray:
+    """The dense feed-forward layer: y = W2 . SiTU(W1 x, W3 x) per token, fp64.
+    x [T, H], W1/W3 [F, H], W2 [H, F], all bf16 bits."""
+    x = _c(x_bits, np.uint16)
+    W1, W3, W2 = _c(w1_bits, np.uint16), _c(w3_bits, np.uint16), _c(w2_bits, np.uint16)
+    T, H = x.shape
+    F = W1.shape[0]
+    assert W1.shape == (F, H) and W3.shape == (F, H) and W2.shape == (H, F)
+    y = np.empty((T, H), np.float64)
+    _L().orc_dense_ffn(_p(y), _p(x), T, _p(W1), _p(W3), _p(W2), H, F, float(b1), float(b2))
+    return y
 
 
 def chain_glue(y, eps: float = 1e-5) -> np.ndarray:

@@ -334,6 +334,29 @@ void orc_layer_forward(const orc_cfg *c, const orc_layer *lw, const uint16_t *x,
     }
 }
 
+/* The model's dense feed-forward layer (layer 0 of the pages' 93: a plain
+ * dense FFN of width dense_inter = 33792, kimi-k3-in-c README Part II, the
+ * K3Cfg "first_dense"/"dense_inter" fields) in the form of every other MLP of
+ * the model: y = W2 . SiTU(W1 x, W3 x), bf16 weights W1, W3 [F, H] and W2
+ * [H, F], the SiTU-GLU of section 9. x [T, H] bf16, y [T, H] fp64; tokens are
+ * independent (OpenMP over tokens, each token's arithmetic unchanged). */
+void orc_dense_ffn(double *y, const uint16_t *x, int T, const uint16_t *W1, const uint16_t *W3,
+                   const uint16_t *W2, int H, int F, double b1, double b2)
+{
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int t = 0; t < T; t++) {
+        double *xv = (double *)malloc(sizeof(double) * (size_t)H);
+        double *g = (double *)malloc(sizeof(double) * (size_t)F);
+        double *u = (double *)malloc(sizeof(double) * (size_t)F);
+        for (int i = 0; i < H; i++) xv[i] = orc_bf16(x[(size_t)t * (size_t)H + (size_t)i]);
+        orc_bf16_matvec(g, xv, W1, H, F);
+        orc_bf16_matvec(u, xv, W3, H, F);
+        for (int i = 0; i < F; i++) g[i] = orc_situ(g[i], u[i], b1, b2);
+        orc_bf16_matvec(y + (size_t)t * (size_t)H, g, W2, F, H);
+        free(xv); free(g); free(u);
+    }
+}
+
 /* Router only, for all T tokens (ids, weights and margins). */
 void orc_route(const orc_cfg *c, const orc_layer *lw, const uint16_t *x, int T,
                int *ids, double *w, double *margin, double *sc_out, double *ch_out)
