@@ -71,6 +71,10 @@ WORKLOADS = {
                                desc="K3-shape single layer, decode T=1 from fp32 residual-stream "
                                     "rows (RMSNorm with the post-norm gain fused into the first "
                                     "kernels; rows rotate through a seeded pool of 64)"),
+    # the cumulative-weight cut of the picks (fewer experts read per token)
+    "decode_t1_topp": dict(T=1, layers=1, topp=0.8,
+                           desc="K3-shape single layer, decode T=1, picks cut to cumulative "
+                                "weight 0.8 (renormalised; tokens rotate through a seeded pool of 64)"),
     # the model's dense feed-forward layer 0 (hidden 7168, dense_inter 33792)
     "dense_t1": dict(T=1, layers=1, dense=True,
                      desc="K3 dense feed-forward layer 0 (hidden 7168, dense_inter 33792, bf16), "
@@ -201,7 +205,7 @@ def make_inputs(workload, seed=0, layer_index=0):
     shape = (k3synth.replace(k3synth.K3, n_experts=64) if workload.endswith("_e64")
              else k3synth.K3)
     d = k3synth.make_layer(shape, seed, layer_index, k3synth.K3_RECIPE)
-    if workload in ("decode_t1", "decode_t1_e64"):
+    if workload in ("decode_t1", "decode_t1_e64", "decode_t1_topp"):
         x = k3synth.make_tokens(shape, seed, POOL, stream=7)
     elif workload == "decode_t1_residual":
         x = k3synth.make_residual(shape, seed, POOL, stream=7)   # fp32 residual rows
@@ -371,6 +375,8 @@ def run_native(args, rank, world):
     km.k3moe_set_expert_path(h, {"auto": km.K3MOE_EXPERT_AUTO, "gemv": km.K3MOE_EXPERT_GEMV,
                                  "gemm": km.K3MOE_EXPERT_GEMM}[args.expert_path])
     alternate = wl.get("alternate", False)   # one layer per step, layers in turn (else a chain)
+    if wl.get("topp"):
+        km.k3moe_set_topp(h, wl["topp"])
     if wl.get("tier"):
         km.k3moe_set_expert_tier(h, wl["tier"])
     w, keep = km.layer_weights(d0, shape.n_experts, km.K3MOE_HOST)
@@ -510,6 +516,26 @@ def run_native(args, rank, world):
     kernels["_profiled_pass_ms_per_step"] = round(prof_ms / args.steps, 5)
     gpu_launches = sum(l for l, _ in by_name.values())
 
+    # ---- the cut's effect on y over the pool (the pages' check before using a p) -------
+    topp = None
+    if wl.get("topp"):
+        outs = []
+        for p_ in (wl["topp"], 0.0):
+            km.k3moe_set_topp(h, p_)
+            ys = []
+            for i in range(npool):
+                fwd(i)
+                ys.append(y.clone())
+            torch.cuda.synchronize()
+            outs.append(torch.stack(ys).view(torch.bfloat16).float().cpu().numpy().reshape(npool, -1))
+        km.k3moe_set_topp(h, wl["topp"])
+        yc, yf = outs
+        rel = float(np.max(np.abs(yc - yf)) / np.max(np.abs(yf)))
+        cos = [float(np.dot(a, b) / (np.linalg.norm(a) * np.linalg.norm(b))) for a, b in zip(yc, yf)]
+        topp = {"p": wl["topp"], "experts_per_token": n_touched / T,
+                "y_maxrel_vs_all_picks": round(rel, 5), "y_cos_vs_all_picks_min": round(min(cos), 6),
+                "y_cos_vs_all_picks_mean": round(float(np.mean(cos)), 6)}
+
     # ---- e2e through the public host-buffer entry point --------------------------------
     e2e = None
     if n_layers == 1 and not residual and not args.no_e2e:
@@ -561,6 +587,7 @@ def run_native(args, rank, world):
         "roofline": roof, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": gpu_launches, "clocks": clk,
         **({"tier": tier} if tier else {}),
+        **({"topp": topp} if topp else {}),
     }
 
 

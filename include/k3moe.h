@@ -253,6 +253,23 @@ typedef struct {
  * k3moe_set_expert_tier). K3MOE_ERR_INVALID_ARG for NULL or a wrong struct_size. */
 K3MOE_API int k3moe_get_tier_stats(k3moe *h, k3moe_tier_stats *out);
 
+/* ---- Dropping the low-weight tail of the picks --------------------------------------
+ * The pages' optional K3_TOPP (kimi-k3-in-c README, run-time options): of the
+ * topk picks of a token, keep only those up to cumulative weight p and
+ * renormalise. In weight order (larger first, equal weights: lower id first)
+ * a pick is kept while the sum of the weights before it is below p times the
+ * total of all picks; the kept weights are scaled back to that total (with
+ * renorm: the kept unbiased scores renormalised, times routed_scale). The
+ * first pick is always kept. Dropped picks are never read: the experts they
+ * would have touched are skipped. k3moe_get_routing then returns, per token,
+ * the kept picks first (selection order) and -1 with weight 0 in the dropped
+ * slots; counts, offsets and perm cover the kept pairs only. p = 0 (the
+ * default) keeps all topk; with p = 1 only picks of zero weight at the end of
+ * the weight order drop. K3MOE_ERR_INVALID_ARG outside [0, 1] or NaN.
+ * Takes effect at the next forward. This changes what the layer computes: the
+ * pages ask for an accuracy check of any p first. */
+K3MOE_API int k3moe_set_topp(k3moe *h, float p);
+
 /* Per-kernel timing: with profiling on, every kernel a forward launches is
  * bracketed by CUDA events on the launching stream. k3moe_profile_read
  * synchronises, aggregates per kernel name and resets the record. */

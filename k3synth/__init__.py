@@ -153,6 +153,7 @@ class Shape:
     situ_b2: float = 25.0
     routed_scale: float = 1.0
     renorm: int = 1
+    topp: float = 0.0      # cumulative-weight cut of the picks (0: off)
 
     @property
     def expert_bytes(self) -> int:

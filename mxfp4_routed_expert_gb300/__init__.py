@@ -38,7 +38,7 @@ EXPORTS = ("k3moe_create", "k3moe_load_layer", "k3moe_forward", "k3moe_forward_c
            "k3moe_sync_status", "k3moe_set_profiling", "k3moe_profile_read", "k3moe_destroy",
            "k3moe_strerror", "k3moe_abi_version", "k3moe_route_static", "k3moe_set_expert_path",
            "k3moe_set_expert_tier", "k3moe_get_tier_stats", "k3moe_load_post_norm",
-           "k3moe_forward_residual")
+           "k3moe_forward_residual", "k3moe_set_topp")
 K3MOE_ROUTE_STATIC_MAX_LOGITS = 1 << 20
 K3MOE_EXPERT_AUTO, K3MOE_EXPERT_GEMV, K3MOE_EXPERT_GEMM = 0, 1, 2
 
@@ -116,6 +116,7 @@ def lib():
         L.k3moe_route_static.argtypes = [vp, vp, vp, i, i, i, i, i, ctypes.c_float, vp, vp, vp]
         L.k3moe_set_expert_tier.argtypes = [vp, i]
         L.k3moe_load_post_norm.argtypes = [vp, i, vp, i]
+        L.k3moe_set_topp.argtypes = [vp, ctypes.c_float]
         L.k3moe_forward_residual.argtypes = [vp, i, vp, vp, i, vp]
         L.k3moe_get_tier_stats.argtypes = [vp, ctypes.POINTER(k3moe_tier_stats)]
         for n in EXPORTS:
@@ -252,7 +253,7 @@ def k3moe_forward_residual(h: int, layer: int, h_in, y, T: int, stream=None) -> 
     """The layer on x = bf16(RMSNorm(h_in) * post-norm gain); h_in fp32 [T, hidden]."""
     return _check(lib().k3moe_forward_residual(ctypes.c_void_p(h), layer, _ptr(h_in), _ptr(y), T,
                                                _stream(stream)),
-                  "k3moe_forward_residual")
+                  "k3moe_forward_residual", "k3moe_set_topp")
 
 
 def k3moe_forward_chain(h: int, first_layer: int, n_layers: int, x, y, T: int, stream=None) -> int:
@@ -291,6 +292,11 @@ def k3moe_set_expert_path(h: int, mode: int) -> int:
     """K3MOE_EXPERT_AUTO / _GEMV / _GEMM: which routed-expert kernels forwards use."""
     return _check(lib().k3moe_set_expert_path(ctypes.c_void_p(h), int(mode)),
                   "k3moe_set_expert_path")
+
+
+def k3moe_set_topp(h: int, p: float) -> int:
+    """Keep each token's picks up to cumulative weight p (0: all topk)."""
+    return _check(lib().k3moe_set_topp(ctypes.c_void_p(h), float(p)), "k3moe_set_topp")
 
 
 def k3moe_set_expert_tier(h: int, slots: int) -> int:

@@ -897,6 +897,13 @@ int k3moe_get_tier_stats(k3moe *h, k3moe_tier_stats *out)
     return K3MOE_OK;
 }
 
+int k3moe_set_topp(k3moe *h, float p)
+{
+    if (!h || !(p >= 0.f && p <= 1.f)) return K3MOE_ERR_INVALID_ARG;   // NaN fails too
+    h->topp = p;
+    return K3MOE_OK;
+}
+
 int k3moe_set_profiling(k3moe *h, int enable)
 {
     if (!h) return K3MOE_ERR_INVALID_ARG;

@@ -56,6 +56,7 @@ struct RouteArgs {
     __half *z16;           // [T, L + kZPad]: scaled fp16 z, then the exponent (int32)
     float *acc;            // [T, L]
     int L;
+    float topp;            // > 0: keep the picks up to cumulative weight topp (0: all k)
     int fuse_perm;         // T == 1: also write counts/offsets/perm/touched
     int *counts, *offsets, *perm, *touched, *n_touched;
     float *pair_w;
@@ -117,6 +118,7 @@ struct RouteSmem {
     int scan_buf[kRouteWarps];
     float sel_ch[kMaxTopk], sel_sc[kMaxTopk];
     int sel_e[kMaxTopk];
+    int sel_keep[kMaxTopk];   // 1: the pick survives the cumulative-weight cut
 };
 
 // The router epilogue of token t on threads 0 .. kRouteThreads-1 (which all
@@ -131,6 +133,7 @@ __device__ __forceinline__ void route_token(const RouteArgs &a, int t, RouteSmem
     int *scan_buf = rs.scan_buf;
     float *sel_ch = rs.sel_ch, *sel_sc = rs.sel_sc;
     int *sel_e = rs.sel_e;
+    int *sel_keep = rs.sel_keep;
     // the selection bias is a layer weight: read it before waiting on the router
     float bv[kEPer];
 #pragma unroll
@@ -249,24 +252,63 @@ __device__ __forceinline__ void route_token(const RouteArgs &a, int t, RouteSmem
         float ssum = sc;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) ssum += __shfl_xor_sync(0xffffffffu, ssum, o);
-        if (have) {
-            const bool rn = a.renorm && ssum > 0.f;
-            const float wv = (rn ? sc / ssum : sc) * a.routed_scale;
-            a.ids[(size_t)t * a.k + rank] = e;
-            a.wts[(size_t)t * a.k + rank] = wv;
-            if (a.fuse_perm) {   // single token: one pair per picked expert, in id order
-                a.perm[id_rank] = rank;
-                a.pair_w[id_rank] = wv;
-                a.touched[id_rank] = e;
+        const bool rn = a.renorm && ssum > 0.f;
+        float wv = have ? (rn ? sc / ssum : sc) * a.routed_scale : 0.f;
+        // Cumulative-weight cut (the pages' K3_TOPP: the low-weight tail of
+        // the picks is dropped and the rest renormalised): in weight order
+        // (larger first, equal: lower id), a pick is kept while the weight
+        // before it is below topp of the total; the kept weights are scaled
+        // back to the total.
+        bool keep = have;
+        if (a.topp > 0.f) {
+            float total = 0.f, before = 0.f;
+            for (int q = 0; q < a.k; q++) {
+                const float wq = __shfl_sync(0xffffffffu, wv, q);
+                const int eq_ = __shfl_sync(0xffffffffu, e, q);
+                total += wq;
+                if (q != lane && (wq > wv || (wq == wv && eq_ < e))) before += wq;
             }
+            keep = have && (total <= 0.f || before < a.topp * total);
+            float kept = 0.f;
+            for (int q = 0; q < a.k; q++) {
+                const float wq = __shfl_sync(0xffffffffu, wv, q);
+                const bool kq = __shfl_sync(0xffffffffu, keep ? 1 : 0, q) != 0;
+                if (kq) kept += wq;
+            }
+            if (keep && kept > 0.f) wv = wv * (total / kept);
         }
-        if (a.fuse_perm && lane == 0) *a.n_touched = a.k;
+        // positions: kept picks first in selection order, dropped ones after
+        const unsigned kmask = __ballot_sync(0xffffffffu, keep);
+        int pos = 0, kid = 0;
+        for (int q = 0; q < a.k; q++) {
+            const bool kq = (kmask >> q) & 1u;
+            const float vq = __shfl_sync(0xffffffffu, v, q);
+            const int eq_ = __shfl_sync(0xffffffffu, e, q);
+            const bool q_first = vq > v || (vq == v && eq_ < e);   // q before this lane (selection order)
+            if (keep ? (kq && q_first) : (kq || q_first)) pos++;
+            if (kq && eq_ < e) kid++;
+        }
+        const int m_kept = __popc(kmask);
+        if (have) {
+            a.ids[(size_t)t * a.k + pos] = keep ? e : -1;
+            a.wts[(size_t)t * a.k + pos] = keep ? wv : 0.f;
+            if (a.fuse_perm && keep) {   // single token: one pair per kept expert, in id order
+                a.perm[kid] = pos;
+                a.pair_w[kid] = wv;
+                a.touched[kid] = e;
+            }
+            sel_keep[lane] = keep ? 1 : 0;   // lane q holds pick sel_e[q]
+        }
+        if (a.fuse_perm && lane == 0) *a.n_touched = m_kept;
+        (void)id_rank;
     }
     if (a.fuse_perm) {
-        // counts/offsets for every expert: offsets[e] = #picked ids below e
+        sync();   // sel_keep from warp 0
+        // counts/offsets for every expert: offsets[e] = #kept picks below e
         for (int e = tid; e <= a.E; e += kRouteThreads) {
             int below = 0, here = 0;
             for (int q = 0; q < a.k; q++) {
+                if (!sel_keep[q]) continue;
                 below += sel_e[q] < e ? 1 : 0;
                 here += sel_e[q] == e ? 1 : 0;
             }

@@ -618,12 +618,12 @@ __global__ void __launch_bounds__(1024) k_expert_tiles(const int *counts, int E,
 
 // zp[p] = z16[token of pair p] (L values and the exponent padding); one warp per pair.
 __global__ void __launch_bounds__(256) k_gather_latent(const __half *z16, const int *perm, __half *zp,
-                                                       int pairs, int k, int L)
+                                                       int pairs, int k, int L, const int *offsets, int E)
 {
     pdl_launch_dependents();
     pdl_wait();
     const int p = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-    if (p >= pairs) return;
+    if (p >= pairs || p >= offsets[E]) return;   // offsets[E]: the pairs kept this forward
     const int t = perm[p] / k;
     const int nv = (L + kZPad) / 8;
     const uint4 *src = reinterpret_cast<const uint4 *>(z16 + (size_t)t * (L + kZPad));
@@ -729,7 +729,8 @@ cudaError_t launch_gather_latent(const k3moe &h, int T, cudaStream_t s)
 {
     const int pairs = T * h.cfg.topk;
     return launch_pdl(k_gather_latent, (pairs + 7) / 8, 256, 0, s, (const __half *)h.ws.z16,
-                      (const int *)h.ws.perm, h.ws.zperm, pairs, h.cfg.topk, h.cfg.latent);
+                      (const int *)h.ws.perm, h.ws.zperm, pairs, h.cfg.topk, h.cfg.latent,
+                      (const int *)h.ws.offsets, h.cfg.n_experts);
 }
 
 // W1/W3 (w13 = true: gathered latent -> h16) or W2 (h16 -> acc).

@@ -155,9 +155,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tma(ExpTArgs a)
     for (int i = threadIdx.x; i <= a.E; i += blockDim.x) offs[i] = a.offsets[i];
     __syncthreads();
 
-    // balanced contiguous unit range of this CTA
-    const long long u0 = a.units * blockIdx.x / gridDim.x;
-    const long long u1 = a.units * (blockIdx.x + 1) / gridDim.x;
+    // balanced contiguous unit range of this CTA, over the pairs this forward
+    // kept (offsets[E]; every pair unless the routing dropped a weight tail)
+    const long long kept = (long long)offs[a.E] * RB;
+    const long long units = kept < a.units ? kept : a.units;
+    const long long u0 = units * blockIdx.x / gridDim.x;
+    const long long u1 = units * (blockIdx.x + 1) / gridDim.x;
     const size_t eb = (size_t)a.R * lay.kb, es = (size_t)a.R * lay.g;
 
     if (warp == kCW) {

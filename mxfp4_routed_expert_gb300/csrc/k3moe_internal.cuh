@@ -144,6 +144,7 @@ struct k3moe {
     bool egemm_ok = false;                   // tensor-core expert GEMM usable (shape)
     int expert_path = K3MOE_EXPERT_AUTO;     // k3moe_set_expert_path
     k3::TierDev tier;                        // k3moe_set_expert_tier
+    float topp = 0.f;                        // k3moe_set_topp (0: keep every pick)
     // per-kernel timing (k3moe_set_profiling)
     bool profiling = false;
     std::deque<k3::ProfRec> prof;

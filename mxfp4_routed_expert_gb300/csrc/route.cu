@@ -39,6 +39,7 @@ static RouteArgs route_args(const k3moe &h, const LayerDev &w, int T)
     a.k = c.topk;
     a.renorm = c.renorm;
     a.routed_scale = c.routed_scale;
+    a.topp = h.topp;
     a.ids = h.ws.ids;
     a.wts = h.ws.wts;
     a.z = h.ws.z;
@@ -131,7 +132,7 @@ __global__ void __launch_bounds__(kPermWarps * 32) k_perm_hist(PermArgs a, int *
         if (lane < a.k) {
             const int e = a.ids[(size_t)t * a.k + lane];
             if (e >= 0 && e < a.E) h[e] += 1;      // distinct experts within a token
-            else set_err(a.err, kErrBounds, t);
+            else if (e != -1) set_err(a.err, kErrBounds, t);   // -1: dropped by the weight cut
         }
         __syncwarp();
     }

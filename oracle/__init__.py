@@ -44,7 +44,7 @@ class _Cfg(ctypes.Structure):
                 ("topk", ctypes.c_int), ("moe_inter", ctypes.c_int), ("shared_inter", ctypes.c_int),
                 ("renorm", ctypes.c_int), ("rms_eps", ctypes.c_double),
                 ("situ_b1", ctypes.c_double), ("situ_b2", ctypes.c_double),
-                ("routed_scale", ctypes.c_double)]
+                ("routed_scale", ctypes.c_double), ("topp", ctypes.c_double)]
 
 
 class _Layer(ctypes.Structure):
@@ -84,6 +84,8 @@ def _L():
         lib.orc_route.argtypes = [p, p, p, i, p, p, p, p, p]
         lib.orc_chain_glue.argtypes = [p, p, i, i, d]
         lib.orc_dense_ffn.argtypes = [p, p, i, p, p, p, i, i, d, d]
+        lib.orc_topp_cut.restype = i
+        lib.orc_topp_cut.argtypes = [p, p, i, d, p]
         lib.orc_group_size.restype = i
         _lib = lib
     return _lib
@@ -203,6 +205,16 @@ def router_token(x, Wr_bits, bias, k: int, renorm: int = 1, routed_scale: float 
     return ids, w, sc, ch, float(m[0])
 
 
+def topp_cut(ids, w, p: float):
+    """The cumulative-weight cut of one token's picks (ids, w in selection
+    order): returns (ids, w, kept, margin); dropped slots hold -1 and 0."""
+    ids = np.array(ids, dtype=np.int32)
+    w = np.array(w, dtype=np.float64)
+    m = np.empty(1, np.float64)
+    n = _L().orc_topp_cut(_p(ids), _p(w), ids.size, float(p), _p(m))
+    return ids, w, int(n), float(m[0])
+
+
 def permutation(ids, E: int):
     """(counts[E], offsets[E+1], perm[T*k]) of a [T, k] id matrix."""
     ids = _c(ids, np.int32)
@@ -219,7 +231,8 @@ def permutation(ids, E: int):
 def _cfg(shape) -> _Cfg:
     return _Cfg(shape.hidden, shape.latent, shape.n_experts, shape.topk, shape.moe_inter,
                 shape.shared_inter, int(shape.renorm), float(shape.rms_eps),
-                float(shape.situ_b1), float(shape.situ_b2), float(shape.routed_scale))
+                float(shape.situ_b1), float(shape.situ_b2), float(shape.routed_scale),
+                float(getattr(shape, "topp", 0.0)))
 
 
 _LAYER_KEYS = ("router_w", "router_bias", "down_w", "up_w", "latent_gain", "sh_w1", "sh_w3",

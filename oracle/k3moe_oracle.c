@@ -212,6 +212,63 @@ void orc_permutation(const int *ids, int T, int k, int E, int *counts, int *offs
     offsets[E] = pos;
 }
 
+/* The optional cut of a token's picks to cumulative weight p (the README's
+ * K3_TOPP run-time option: drop the low-weight tail of the top-k and
+ * renormalise). ids/w hold the k picks in selection order. In weight order
+ * (larger first, equal weights: lower id first) a pick is kept while the sum
+ * of the weights before it is below p times the total; the kept weights are
+ * scaled back to the total. The kept picks stay in selection order at the
+ * front; the dropped slots become id -1, weight 0. Returns the number kept.
+ * *margin (optional) = the smallest |before - p * total| / total over the
+ * picks after the first in weight order: how far the cut is from moving. */
+int orc_topp_cut(int *ids, double *w, int k, double p, double *margin)
+{
+    int order[64], keep[64];
+    double total = 0.0;
+    for (int j = 0; j < k; j++) {
+        order[j] = j;
+        total += w[j];
+    }
+    for (int a = 1; a < k; a++)   /* insertion sort by (w desc, id asc) */
+        for (int b = a; b > 0; b--) {
+            const int x = order[b - 1], y = order[b];
+            const int swap = w[y] > w[x] || (w[y] == w[x] && ids[y] < ids[x]);
+            if (!swap) break;
+            order[b - 1] = y;
+            order[b] = x;
+        }
+    double before = 0.0, kept = 0.0, mg = INFINITY;
+    for (int r = 0; r < k; r++) {
+        const int j = order[r];
+        keep[j] = total <= 0.0 || before < p * total;
+        if (r > 0 && total > 0.0) {
+            const double d = fabs(before - p * total) / total;
+            if (d < mg) mg = d;
+        }
+        if (keep[j]) kept += w[j];
+        before += w[j];
+    }
+    int tmp_ids[64];
+    double tmp_w[64];
+    int m = 0;
+    for (int j = 0; j < k; j++)
+        if (keep[j]) {
+            tmp_ids[m] = ids[j];
+            tmp_w[m] = kept > 0.0 ? w[j] * (total / kept) : w[j];
+            m++;
+        }
+    for (int j = 0, n = m; j < k; j++)
+        if (!keep[j]) {
+            tmp_ids[n] = -1;
+            tmp_w[n] = 0.0;
+            n++;
+        }
+    memcpy(ids, tmp_ids, sizeof(int) * (size_t)k);
+    memcpy(w, tmp_w, sizeof(double) * (size_t)k);
+    if (margin) *margin = mg;
+    return m;
+}
+
 /* ------------------------------------------------------------------------ */
 /* The layer (README section 9, k3_moe; colibri "Stable LatentMoE")          */
 /* ------------------------------------------------------------------------ */
@@ -220,6 +277,7 @@ typedef struct {
     int hidden, latent, n_experts, topk, moe_inter, shared_inter;
     int renorm;
     double rms_eps, situ_b1, situ_b2, routed_scale;
+    double topp;   /* > 0: the cumulative-weight cut of the picks (0: off) */
 } orc_cfg;
 
 typedef struct {
@@ -280,11 +338,17 @@ static void orc_layer_token(const orc_cfg *c, const orc_layer *lw, const uint16_
     /* 1. router on the full width */
     orc_router_token(ids, w, NULL, NULL, &margin, x, lw->router_w, lw->router_bias,
                      H, E, K, c->renorm, c->routed_scale);
+    if (c->topp > 0.0) {   /* optional cut of the weight tail */
+        double mt;
+        orc_topp_cut(ids, w, K, c->topp, &mt);
+        if (mt < margin) margin = mt;
+    }
     /* 2. latent down projection */
     orc_bf16_matvec(z, x, lw->down_w, H, L);
     /* 3. routed experts in the latent */
     for (int j = 0; j < K; j++) {
         const int e = ids[j];
+        if (e < 0) continue;   /* dropped by the cut */
         orc_mxfp4_matvec(g, z, lw->w1p + (size_t)e * per1, lw->w1s + (size_t)e * per1s, L, I);
         orc_mxfp4_matvec(u, z, lw->w3p + (size_t)e * per1, lw->w3s + (size_t)e * per1s, L, I);
         for (int i = 0; i < I; i++) a[i] = orc_situ(g[i], u[i], c->situ_b1, c->situ_b2);
@@ -371,6 +435,11 @@ void orc_route(const orc_cfg *c, const orc_layer *lw, const uint16_t *x, int T,
                          ch_out ? ch_out + (size_t)t * (size_t)E : NULL,
                          margin ? margin + t : NULL, xd, lw->router_w, lw->router_bias,
                          H, E, K, c->renorm, c->routed_scale);
+        if (c->topp > 0.0) {
+            double mt;
+            orc_topp_cut(ids + (size_t)t * (size_t)K, w + (size_t)t * (size_t)K, K, c->topp, &mt);
+            if (margin && mt < margin[t]) margin[t] = mt;
+        }
         free(xd);
     }
 }

@@ -150,3 +150,35 @@ def test_permutation_of_router_ids():
         seg = perm[offsets[e]:offsets[e + 1]]
         assert np.all(ids.ravel()[seg] == e)
         assert np.all(np.diff(seg // shape.topk) > 0)      # tokens ascending, each once
+
+
+# ---- the cumulative-weight cut of the picks (the pages' K3_TOPP option) ----------------
+
+def test_topp_cut_by_hand():
+    # selection order ids [7, 3, 9, 1], weights 1/2, 1/4, 1/8, 1/8 (exact in binary);
+    # weight order 7, 3, then 1 before 9 (equal weights: lower id first)
+    ids, w = [7, 3, 9, 1], [0.5, 0.25, 0.125, 0.125]
+    i2, w2, m, _ = oracle.topp_cut(ids, w, 0.75)      # before: 0, 1/2, 3/4 (not < 3/4)
+    assert m == 2 and i2.tolist() == [7, 3, -1, -1]
+    np.testing.assert_allclose(w2, [2 / 3, 1 / 3, 0, 0], rtol=1e-15)
+    i3, w3, m3, _ = oracle.topp_cut(ids, w, 0.76)     # 3/4 < 0.76: expert 1 stays too
+    assert m3 == 3 and i3.tolist() == [7, 3, 1, -1]
+    np.testing.assert_allclose(w3, [0.5 / 0.875, 0.25 / 0.875, 0.125 / 0.875, 0], rtol=1e-15)
+
+
+def test_topp_cut_ties_go_to_lower_ids_and_first_pick_stays():
+    i2, w2, m, _ = oracle.topp_cut([5, 2, 8, 4], [0.25] * 4, 0.5)   # order 2, 4, 5, 8
+    assert m == 2 and i2.tolist() == [2, 4, -1, -1]
+    np.testing.assert_allclose(w2, [0.5, 0.5, 0, 0], rtol=1e-15)
+    i1, w1, m1, _ = oracle.topp_cut([5, 2, 8, 4], [0.1, 0.4, 0.3, 0.2], 1e-9)
+    assert m1 == 1 and i1.tolist() == [2, -1, -1, -1]
+    np.testing.assert_allclose(w1, [1.0, 0, 0, 0], rtol=1e-15)        # scaled back to the total
+
+
+def test_topp_cut_one_keeps_all_but_a_zero_tail_and_reports_its_margin():
+    i, w, m, mg = oracle.topp_cut([1, 2, 3], [0.6, 0.4, 0.0], 1.0)   # before 1.0 is not < 1.0
+    assert m == 2 and i.tolist() == [1, 2, -1]
+    np.testing.assert_allclose(w, [0.6, 0.4, 0.0], rtol=1e-15)
+    assert mg == 0.0
+    _, _, _, mg2 = oracle.topp_cut([7, 3, 9, 1], [0.5, 0.25, 0.125, 0.125], 0.7)
+    np.testing.assert_allclose(mg2, 0.05, rtol=1e-12)                   # |3/4 - 0.7|
