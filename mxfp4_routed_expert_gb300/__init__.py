@@ -253,7 +253,7 @@ def k3moe_forward_residual(h: int, layer: int, h_in, y, T: int, stream=None) -> 
     """The layer on x = bf16(RMSNorm(h_in) * post-norm gain); h_in fp32 [T, hidden]."""
     return _check(lib().k3moe_forward_residual(ctypes.c_void_p(h), layer, _ptr(h_in), _ptr(y), T,
                                                _stream(stream)),
-                  "k3moe_forward_residual", "k3moe_set_topp")
+                  "k3moe_forward_residual")
 
 
 def k3moe_forward_chain(h: int, first_layer: int, n_layers: int, x, y, T: int, stream=None) -> int:

@@ -278,15 +278,20 @@ __device__ __forceinline__ void route_token(const RouteArgs &a, int t, RouteSmem
             if (keep && kept > 0.f) wv = wv * (total / kept);
         }
         // positions: kept picks first in selection order, dropped ones after
+        // (without a cut: the selection rank and the id rank)
         const unsigned kmask = __ballot_sync(0xffffffffu, keep);
-        int pos = 0, kid = 0;
-        for (int q = 0; q < a.k; q++) {
-            const bool kq = (kmask >> q) & 1u;
-            const float vq = __shfl_sync(0xffffffffu, v, q);
-            const int eq_ = __shfl_sync(0xffffffffu, e, q);
-            const bool q_first = vq > v || (vq == v && eq_ < e);   // q before this lane (selection order)
-            if (keep ? (kq && q_first) : (kq || q_first)) pos++;
-            if (kq && eq_ < e) kid++;
+        int pos = rank, kid = id_rank;
+        if (a.topp > 0.f) {
+            pos = 0;
+            kid = 0;
+            for (int q = 0; q < a.k; q++) {
+                const bool kq = (kmask >> q) & 1u;
+                const float vq = __shfl_sync(0xffffffffu, v, q);
+                const int eq_ = __shfl_sync(0xffffffffu, e, q);
+                const bool q_first = vq > v || (vq == v && eq_ < e);   // q before this lane (selection order)
+                if (keep ? (kq && q_first) : (kq || q_first)) pos++;
+                if (kq && eq_ < e) kid++;
+            }
         }
         const int m_kept = __popc(kmask);
         if (have) {
@@ -300,17 +305,23 @@ __device__ __forceinline__ void route_token(const RouteArgs &a, int t, RouteSmem
             sel_keep[lane] = keep ? 1 : 0;   // lane q holds pick sel_e[q]
         }
         if (a.fuse_perm && lane == 0) *a.n_touched = m_kept;
-        (void)id_rank;
     }
     if (a.fuse_perm) {
-        sync();   // sel_keep from warp 0
+        if (a.topp > 0.f) sync();   // sel_keep from warp 0
         // counts/offsets for every expert: offsets[e] = #kept picks below e
         for (int e = tid; e <= a.E; e += kRouteThreads) {
             int below = 0, here = 0;
-            for (int q = 0; q < a.k; q++) {
-                if (!sel_keep[q]) continue;
-                below += sel_e[q] < e ? 1 : 0;
-                here += sel_e[q] == e ? 1 : 0;
+            if (a.topp > 0.f) {
+                for (int q = 0; q < a.k; q++) {
+                    const int kq = sel_keep[q];
+                    below += (kq && sel_e[q] < e) ? 1 : 0;
+                    here += (kq && sel_e[q] == e) ? 1 : 0;
+                }
+            } else {
+                for (int q = 0; q < a.k; q++) {
+                    below += sel_e[q] < e ? 1 : 0;
+                    here += sel_e[q] == e ? 1 : 0;
+                }
             }
             a.offsets[e] = below;
             if (e < a.E) a.counts[e] = here;
