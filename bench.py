@@ -306,6 +306,26 @@ def traffic_for(kernel, workload):
     return ent["bytes_per_launch"]
 
 
+def max_over_ranks(value, device="cpu"):
+    """The largest `value` over the ranks of the process group (the slowest
+    rank sets a whole-job time); the value itself without a group or with one
+    rank. `device`: where the reduction runs ("cuda" under NCCL, "cpu" under
+    gloo)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world, tokens_per_step, steps, seconds):
+    """Tokens per second of the whole job: every rank runs `steps` steps of
+    `tokens_per_step` tokens on its own replica, timed by the slowest rank."""
+    return world * tokens_per_step * steps / seconds
+
+
 def host_link_gbs():
     """Pinned host -> device copy bandwidth (1 GiB, best of 3, CUDA events)."""
     import torch
@@ -463,11 +483,9 @@ def run_native(args, rank, world):
     st = km.k3moe_sync_status(h)
     assert st == 0, km.strerror(st)
     if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+        total_ms = max_over_ranks(total_ms, "cuda")
     ms_per_step = total_ms / args.steps
-    value = world * T * args.steps / (total_ms / 1e3)
+    value = whole_job_rate(world, T, args.steps, total_ms / 1e3)
 
     touched = (counts_log.cpu().numpy() > 0).sum(1)
     n_touched = float(touched.mean())
@@ -550,7 +568,9 @@ def run_native(args, rank, world):
             t0 = time.perf_counter()
             km.k3moe_forward_host(h, 0, xh[(i % npool) * T:(i % npool) * T + T], yh, T, stream)
             tot += time.perf_counter() - t0
-        e2e = {"value": round(world * T * args.steps / tot, 2), "unit": UNIT,
+        if world > 1:
+            tot = max_over_ranks(tot, "cuda")
+        e2e = {"value": round(whole_job_rate(world, T, args.steps, tot), 2), "unit": UNIT,
                "h2d_bytes_per_step": T * shape.hidden * 2,
                "d2h_bytes_per_step": T * shape.hidden * 2}
 
