@@ -1,0 +1,82 @@
+"""Sizing the expert tier from a recorded routing trace (host-side utility).
+
+Routing does not depend on the cache, so one run can record every forward's
+(layer, touched experts) and the trace can be replayed at any number of slots
+(kimi-k3-in-c README, Part II section 13, "How big should that cache be? Ask
+the trace"). This module replays such a trace under
+
+- "tier":   the policy of `k3moe_set_expert_tier`: per forward, the touched
+            experts already resident are hits; the others take, in ascending
+            expert order, the slots not used by this forward with the oldest
+            last use (never-used slots first; equal ages: the lower slot);
+- "belady": the offline optimum at forward granularity: a miss evicts the
+            resident expert, not used by this forward, whose next use lies
+            furthest ahead (a ceiling for any policy, not a policy).
+
+A trace is a list of (layer, experts) pairs in forward order; it can be built
+from each forward's expert counts (`k3moe_get_routing`) with
+`trace_from_counts`.
+"""
+from __future__ import annotations
+
+from collections import defaultdict, deque
+
+import numpy as np
+
+
+def trace_from_counts(layer: int, counts) -> tuple:
+    """(layer, touched experts) of one forward from its per-expert pair counts."""
+    return int(layer), tuple(int(e) for e in np.flatnonzero(np.asarray(counts) > 0))
+
+
+def replay(trace, slots: int, policy: str = "tier", expert_bytes: int = 0) -> dict:
+    """Hits, misses and bytes copied when `trace` runs on `slots` slots.
+
+    Every forward's experts must fit at once (slots >= the most experts any one
+    forward touches), as the tier requires. compulsory = the distinct
+    (layer, expert) keys: the misses no policy can avoid."""
+    if policy not in ("tier", "belady"):
+        raise ValueError(f"unknown policy {policy!r}")
+    trace = [(int(layer), tuple(sorted(set(int(e) for e in ex)))) for layer, ex in trace]
+    if any(len(ex) > slots for _, ex in trace):
+        raise ValueError("a forward touches more experts than there are slots")
+    nxt = defaultdict(deque)   # key -> forward indices where it is used
+    for i, (layer, ex) in enumerate(trace):
+        for e in ex:
+            nxt[(layer, e)].append(i)
+    key = [None] * slots       # slot -> (layer, expert) or None
+    used = [0] * slots         # slot -> stamp of its last forward (0: never)
+    where = {}                 # (layer, expert) -> slot
+    hits = misses = 0
+    for i, (layer, ex) in enumerate(trace):
+        stamp = i + 1
+        miss = []
+        for e in ex:
+            k = (layer, e)
+            nxt[k].popleft()
+            if k in where:
+                used[where[k]] = stamp
+                hits += 1
+            else:
+                miss.append(k)
+        free = [s for s in range(slots) if used[s] < stamp]
+        if policy == "tier":
+            chosen = sorted(sorted(free, key=lambda s: (used[s], s))[:len(miss)])
+        else:   # furthest next use first; never used again counts as infinitely far
+            def far(s):
+                k = key[s]
+                if k is None:
+                    return (2, 0, s)
+                return (1, nxt[k][0] if nxt[k] else 1 << 60, -s)
+            chosen = sorted(sorted(free, key=far, reverse=True)[:len(miss)])
+        for k, s in zip(miss, chosen):
+            if key[s] is not None:
+                del where[key[s]]
+            key[s] = k
+            where[k] = s
+            used[s] = stamp
+        misses += len(miss)
+    total = hits + misses
+    return {"slots": slots, "policy": policy, "hits": hits, "misses": misses,
+            "hit_rate": hits / total if total else 0.0, "compulsory": len(nxt),
+            "bytes_copied": misses * int(expert_bytes)}
