@@ -78,3 +78,21 @@ def test_dense_config_errors():
     with pytest.raises(km.K3MoEError) as ei:
         km.k3moe_create(km.make_config(bad))
     assert ei.value.code == km.K3MOE_ERR_CONFIG
+
+
+def test_dense_through_host_buffers():
+    """k3moe_forward_host on the dense layer: pinned host x and y."""
+    import torch
+    import mxfp4_routed_expert_gb300 as km
+    d = k3synth.make_dense_layer(SMALL, 13)
+    x = k3synth.make_tokens(SMALL, 13, 3)
+    lay = Layer(SMALL, [d], max_tokens=3)
+    try:
+        xh = torch.from_numpy(x.view(np.int16).copy()).pin_memory()
+        yh = torch.empty((3, SMALL.hidden), dtype=torch.int16).pin_memory()
+        km.k3moe_forward_host(lay.h, 0, xh, yh, 3)
+        y = yh.numpy().view(np.uint16)
+    finally:
+        lay.close()
+    ref = oracle.dense_ffn(x, d["sh_w1"], d["sh_w3"], d["sh_w2"], SMALL.situ_b1, SMALL.situ_b2)
+    assert_close(bf16_to_f64(y), ref)

@@ -175,3 +175,70 @@ def test_tier_argument_errors():
         assert km.k3moe_get_tier_stats(lay.h)["slots"] == MID.n_experts + 3
     finally:
         lay.close()
+
+
+def test_tier_with_the_topp_cut():
+    """The cut drops picks before the tier plans: only kept experts are
+    copied in, and the counters follow the policy on the kept sets."""
+    import dataclasses
+    import mxfp4_routed_expert_gb300 as km
+    sh = dataclasses.replace(MID, topp=0.5)
+    layers = [k3synth.make_layer(sh, 80 + i, 0, k3synth.TINY_RECIPE) for i in range(2)]
+    lay = Layer(sh, layers, max_tokens=8, tier_slots=sh.n_experts)
+    model = LruModel(sh.n_experts)
+    try:
+        km.k3moe_set_topp(lay.h, 0.5)
+        for layer, T, seed in [(0, 5, 1), (1, 5, 2), (0, 5, 1), (1, 1, 3)]:
+            d = layers[layer]
+            x, _ = guarded_tokens(sh, d, seed, T)
+            y = lay.forward(x, layer=layer)
+            r = lay.routing(T)
+            ref, tr = oracle.layer_forward(sh, d, x, trace=True)
+            check_routing(r, sh, x, tr["ids"], tr["w"])
+            assert_close(bf16_to_f64(y), ref)
+            assert int(np.count_nonzero(r["counts"])) <= T * sh.topk
+            model.forward(layer, np.nonzero(r["counts"])[0])
+        st = km.k3moe_get_tier_stats(lay.h)
+    finally:
+        lay.close()
+    assert (st["hits"], st["misses"]) == (model.hits, model.misses)
+
+
+def test_tier_with_the_residual_forward():
+    import mxfp4_routed_expert_gb300 as km
+    d = k3synth.make_layer(MID, 85, 0, k3synth.TINY_RECIPE)
+    g = k3synth.post_norm_gain(MID, 85)
+    make = lambda att: oracle.round_bf16(   # noqa: E731
+        oracle.residual_input(k3synth.make_residual(MID, 85, 1, 0, att), g, MID.rms_eps))
+    _, att = guarded_tokens(MID, d, 85, 1, make=make)
+    hres = k3synth.make_residual(MID, 85, 1, 0, att)
+    lay = Layer(MID, [d], max_tokens=1, tier_slots=MID.n_experts)
+    try:
+        km.k3moe_load_post_norm(lay.h, 0, g)
+        y = lay.forward_residual(hres)
+        x_gpu = lay.layer_input(1)
+        r = lay.routing(1)
+        st = km.k3moe_get_tier_stats(lay.h)
+    finally:
+        lay.close()
+    ref, tr = oracle.layer_forward(MID, d, x_gpu, trace=True)
+    check_routing(r, MID, x_gpu, tr["ids"], tr["w"])
+    assert_close(bf16_to_f64(y), ref)
+    assert st["misses"] == MID.topk and st["hits"] == 0
+
+
+def test_tier_chain_matches_the_resident_chain():
+    """Two stacked layers through k3moe_forward_chain on a tiered handle (one
+    layer's worth of slots) give the resident handle's output."""
+    layers = [k3synth.make_layer(k3synth.TINY, 86, i, k3synth.TINY_RECIPE) for i in range(2)]
+    x, _ = guarded_tokens(k3synth.TINY, layers[0], 86, 8)
+    ys = []
+    for slots in (0, k3synth.TINY.n_experts):
+        lay = Layer(k3synth.TINY, layers, max_tokens=8, tier_slots=slots)
+        try:
+            ys.append(bf16_to_f64(lay.forward(x, layer=0, chain=2)))
+            ys.append(bf16_to_f64(lay.forward(x, layer=0, chain=2)))   # again: now from the slots
+        finally:
+            lay.close()
+    for y in ys[1:]:
+        assert_close(y, ys[0], "tiered chain vs resident chain", rel=2e-3, cos=0.99999)
