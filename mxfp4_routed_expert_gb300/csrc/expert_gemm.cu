@@ -175,19 +175,6 @@ __device__ __forceinline__ float pow2_e8m0(int s)
     return __uint_as_float((uint32_t)min(max(s, 1), 254) << 23);
 }
 
-__device__ __forceinline__ float tanh_hw(float x)
-{
-    float y;
-    asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
-// SiTU with the hardware tanh (relative error about 2^-11), sigma(g) written
-// as (1 + tanh(g / 2)) / 2: b1 tanh(g / b1) sigma(g) b2 tanh(u / b2).
-__device__ __forceinline__ float situ_hw(float g, float u, float b1, float b2, float ib1, float ib2)
-{
-    return (b1 * b2) * tanh_hw(g * ib1) * tanh_hw(u * ib2) * fmaf(0.5f, tanh_hw(0.5f * g), 0.5f);
-}
 
 // 16 packed bytes (32 columns, one scale group) -> 16 f16x2 scaled by f.
 __device__ __forceinline__ void widen_group(uint4 w, uint32_t f, uint32_t *o)

@@ -23,7 +23,8 @@
 // token of the same expert re-reads rows the L2 has just seen.
 //
 // k_w13_tma: gate row of W1 and up row of W3 against the fp16 latent z of
-//   the pair's token; SiTU-GLU in the epilogue; h written per pair
+//   the pair's token; SiTU-GLU in the epilogue (hardware tanh, as in the
+//   grouped GEMM); h written per pair
 //   (README section 9, k3_moe step 3 and k3_situ_glu).
 // k_w2_tma: h . W2 rows, times the pair's routing weight, scatter-added into
 //   the token's fp32 latent accumulator.
@@ -65,7 +66,7 @@ struct ExpTArgs {
     __half *h16;           // w13 output / w2 input [T*k, I]
     const float *pair_w;   // [T*k] routing weight per pair slot
     float *acc;            // [T, L]
-    float b1, b2;
+    float b1, b2, ib1, ib2;   // SiTU bounds and their reciprocals
     long long units;       // T*k*(R/64)
     const int *wslot;      // expert -> index in the weight arrays (nullptr: the expert itself)
     int n_ws;              // experts the weight arrays hold
@@ -359,7 +360,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tma(ExpTArgs a)
                 const int i = lane >> sft;
                 const int row = rb * kUnitRows + (i / kRowsPerWarp) * kStageRows +
                                 (i % kRowsPerWarp) * kCW + warp;
-                a.h16[(size_t)p * a.R + row] = __float2half_rn(situ_f(r * fz, up * fz, a.b1, a.b2));
+                a.h16[(size_t)p * a.R + row] =
+                    __float2half_rn(situ_hw(r * fz, up * fz, a.b1, a.b2, a.ib1, a.ib2));
             }
         } else {
             constexpr int N = kUnitVals;
@@ -418,6 +420,8 @@ static ExpTArgs base_args(const k3moe &h, const LayerDev &w, int T)
     a.acc = h.ws.acc;
     a.b1 = c.situ_b1;
     a.b2 = c.situ_b2;
+    a.ib1 = 1.f / c.situ_b1;
+    a.ib2 = 1.f / c.situ_b2;
     a.err = h.ws.err;
     return a;
 }

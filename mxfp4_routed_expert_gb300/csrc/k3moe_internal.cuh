@@ -284,6 +284,21 @@ __device__ __forceinline__ float e8m0_to_f32(uint32_t s)
 
 __device__ __forceinline__ float sigmoid_f(float v) { return 1.0f / (1.0f + expf(-v)); }
 
+__device__ __forceinline__ float tanh_hw(float x)
+{
+    float y;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// SiTU with the hardware tanh (relative error about 2^-11), sigma(g) written
+// as (1 + tanh(g / 2)) / 2: b1 tanh(g / b1) sigma(g) b2 tanh(u / b2); ib1 and
+// ib2 are 1/b1 and 1/b2. The routed experts' epilogues use it.
+__device__ __forceinline__ float situ_hw(float g, float u, float b1, float b2, float ib1, float ib2)
+{
+    return (b1 * b2) * tanh_hw(g * ib1) * tanh_hw(u * ib2) * fmaf(0.5f, tanh_hw(0.5f * g), 0.5f);
+}
+
 __device__ __forceinline__ float situ_f(float g, float u, float b1, float b2)
 {
     return (b1 * tanhf(g / b1)) * sigmoid_f(g) * (b2 * tanhf(u / b2));
