@@ -242,6 +242,15 @@ K3MOE_API int k3moe_set_expert_path(k3moe *h, int mode);
  * K3MOE_ERR_CUDA. */
 K3MOE_API int k3moe_set_expert_tier(k3moe *h, int slots);
 
+/* Pins a loaded layer's routed experts in the tier (the pages' pinned slots,
+ * which eviction skips): all n_experts of the layer are copied into slots now
+ * (counted as misses) and stay there; its forwards only hit. Synchronous.
+ * Needs slots >= (pinned layers + 2) * n_experts, so that any other layer's
+ * forward still fits; pinning a pinned layer again does nothing; loading the
+ * layer again unpins it. Errors: K3MOE_ERR_INVALID_ARG (no tier, bad layer,
+ * too few slots), K3MOE_ERR_NOT_LOADED, K3MOE_ERR_DEVICE, K3MOE_ERR_CUDA. */
+K3MOE_API int k3moe_tier_pin_layer(k3moe *h, int layer);
+
 typedef struct {
     int32_t struct_size;    /* sizeof(k3moe_tier_stats), set by the caller */
     int32_t slots;          /* 0: tier off */

@@ -38,7 +38,7 @@ EXPORTS = ("k3moe_create", "k3moe_load_layer", "k3moe_forward", "k3moe_forward_c
            "k3moe_sync_status", "k3moe_set_profiling", "k3moe_profile_read", "k3moe_destroy",
            "k3moe_strerror", "k3moe_abi_version", "k3moe_route_static", "k3moe_set_expert_path",
            "k3moe_set_expert_tier", "k3moe_get_tier_stats", "k3moe_load_post_norm",
-           "k3moe_forward_residual", "k3moe_set_topp")
+           "k3moe_forward_residual", "k3moe_set_topp", "k3moe_tier_pin_layer")
 K3MOE_ROUTE_STATIC_MAX_LOGITS = 1 << 20
 K3MOE_EXPERT_AUTO, K3MOE_EXPERT_GEMV, K3MOE_EXPERT_GEMM = 0, 1, 2
 
@@ -117,6 +117,7 @@ def lib():
         L.k3moe_set_expert_tier.argtypes = [vp, i]
         L.k3moe_load_post_norm.argtypes = [vp, i, vp, i]
         L.k3moe_set_topp.argtypes = [vp, ctypes.c_float]
+        L.k3moe_tier_pin_layer.argtypes = [vp, i]
         L.k3moe_forward_residual.argtypes = [vp, i, vp, vp, i, vp]
         L.k3moe_get_tier_stats.argtypes = [vp, ctypes.POINTER(k3moe_tier_stats)]
         for n in EXPORTS:
@@ -304,6 +305,11 @@ def k3moe_set_expert_tier(h: int, slots: int) -> int:
     device slots cache them (0: off). Call before the first k3moe_load_layer."""
     return _check(lib().k3moe_set_expert_tier(ctypes.c_void_p(h), int(slots)),
                   "k3moe_set_expert_tier")
+
+
+def k3moe_tier_pin_layer(h: int, layer: int) -> int:
+    """Copy a loaded layer's experts into tier slots that eviction skips."""
+    return _check(lib().k3moe_tier_pin_layer(ctypes.c_void_p(h), layer), "k3moe_tier_pin_layer")
 
 
 def k3moe_get_tier_stats(h: int) -> dict:

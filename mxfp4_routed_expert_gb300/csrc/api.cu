@@ -578,6 +578,8 @@ int k3moe_load_layer(k3moe *h, int layer, const k3moe_layer_weights *w)
     if (rc == K3MOE_OK && tiered && h->layers[(size_t)layer].loaded &&
         (launch_tier_forget(*h, layer, 0) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess))
         rc = K3MOE_ERR_CUDA;
+    if (rc == K3MOE_OK && tiered && h->layers[(size_t)layer].pinned)
+        h->tier.pinned -= c.n_experts;   // the forget freed its pinned slots
     if (rc != K3MOE_OK) {
         cudaFree(blk);
         if (hblk) cudaFreeHost(hblk);
@@ -846,7 +848,8 @@ int k3moe_set_expert_tier(k3moe *h, int slots)
         bytes += al256((size_t)slots * piece[p]);
     }
     const size_t E = c.n_experts, tables = al256((size_t)c.max_layers * E * 4) + 2 * al256((size_t)slots * 4) +
-                                               al256(E * sizeof(int2)) + al256(4) + al256(3 * 8);
+                                               al256(E * sizeof(int2)) + al256(4) + al256(3 * 8) +
+                                               al256((E + 1) * 4);
     bytes += tables;
     size_t fr = 0, tot = 0;
     if (cudaMemGetInfo(&fr, &tot) != cudaSuccess) return K3MOE_ERR_CUDA;
@@ -864,17 +867,47 @@ int k3moe_set_expert_tier(k3moe *h, int slots)
     t.fill = cv.take<int2>(E);
     t.n_fill = cv.take<int>(1);
     t.stats = cv.take<unsigned long long>(3);
+    t.all_ids = cv.take<int>(E + 1);
     // tables: every slot free (key -1, stamp 0), no expert resident
     if (cudaMemset(tab, 0, tables) != cudaSuccess ||
         cudaMemset(t.slot_of, 0xFF, (size_t)c.max_layers * E * 4) != cudaSuccess ||
-        cudaMemset(t.slot_key, 0xFF, (size_t)slots * 4) != cudaSuccess ||
-        cudaDeviceSynchronize() != cudaSuccess) {
+        cudaMemset(t.slot_key, 0xFF, (size_t)slots * 4) != cudaSuccess) {
         cudaGetLastError();
         cudaFree(t.block);
         return K3MOE_ERR_CUDA;
     }
     t.slots = slots;
     h->tier = t;
+    if (launch_tier_iota(*h) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+        cudaGetLastError();
+        free_tier(h->tier);
+        return K3MOE_ERR_CUDA;
+    }
+    return K3MOE_OK;
+}
+
+int k3moe_tier_pin_layer(k3moe *h, int layer)
+{
+    if (!h || layer < 0 || layer >= h->cfg.max_layers) return K3MOE_ERR_INVALID_ARG;
+    TierDev &t = h->tier;
+    const int E = h->cfg.n_experts;
+    if (t.slots == 0) return K3MOE_ERR_INVALID_ARG;
+    LayerDev &w = h->layers[(size_t)layer];
+    if (!w.loaded) return K3MOE_ERR_NOT_LOADED;
+    if (w.pinned) return K3MOE_OK;
+    // every forward of an unpinned layer must still find E free-able slots
+    if (t.slots - t.pinned - E < E) return K3MOE_ERR_INVALID_ARG;
+    if (cudaSetDevice(h->cfg.device) != cudaSuccess) return K3MOE_ERR_CUDA;
+    if (launch_tier_plan(*h, layer, 0, true) != cudaSuccess || launch_tier_fill(*h, w, 0) != cudaSuccess ||
+        cudaDeviceSynchronize() != cudaSuccess) {
+        cudaGetLastError();
+        return K3MOE_ERR_CUDA;
+    }
+    int word = 0;
+    if (cudaMemcpy(&word, h->ws.err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return K3MOE_ERR_CUDA;
+    if (word != kErrNone) return K3MOE_ERR_DEVICE;
+    t.pinned += E;
+    w.pinned = true;
     return K3MOE_OK;
 }
 

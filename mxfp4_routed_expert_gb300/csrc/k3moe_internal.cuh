@@ -63,6 +63,7 @@ struct LayerDev {
     // host block, the nine expert arrays in the layout of the device copy
     void *host_block = nullptr;
     const uint8_t *hsrc[9] = {};
+    bool pinned = false;     // k3moe_tier_pin_layer: its experts hold pinned slots
     // RMSNorm gain in front of the MoE (k3moe_load_post_norm), own allocation
     const __nv_bfloat16 *post_gain = nullptr;
     void *post_block = nullptr;
@@ -84,7 +85,9 @@ struct TierDev {
     int2 *fill = nullptr;               // [E]: (slot, expert) per miss of the current forward
     int *n_fill = nullptr;
     unsigned long long *stats = nullptr;   // hits, misses, bytes filled
+    int *all_ids = nullptr;             // [E + 1]: 0 .. E-1, then E (a layer's list, for pinning)
     uint32_t stamp = 0;                 // forwards planned so far
+    int pinned = 0;                     // slots held by pinned layers
 };
 
 // Per-handle scratch, sized for max_tokens (Tm).
@@ -219,7 +222,8 @@ cudaError_t launch_dense_tma(const k3moe &h, const LayerDev &w, const __nv_bfloa
 bool expert_smem_fits(const k3moe_config &c);
 // expert tier: which touched experts are resident and which slots the others
 // take (one block), then the copy of the missed experts into their slots
-cudaError_t launch_tier_plan(k3moe &h, int layer, cudaStream_t s);
+cudaError_t launch_tier_plan(k3moe &h, int layer, cudaStream_t s, bool pin = false);
+cudaError_t launch_tier_iota(const k3moe &h);
 cudaError_t launch_tier_fill(const k3moe &h, const LayerDev &w, cudaStream_t s);
 cudaError_t launch_tier_forget(const k3moe &h, int layer, cudaStream_t s);
 

@@ -30,8 +30,12 @@ constexpr size_t kFillChunk = (size_t)kFillThreads * kFillVec * 16;   // 64 KB
 
 static_assert(kMaxExperts <= kPlanThreads, "one touched expert per plan thread");
 
+// Stamp of a pinned slot: above every forward's stamp, so never a victim.
+constexpr uint32_t kPinned = 0xFFFFFFFFu;
+
 struct TierPlanArgs {
     const int *touched, *n_touched;
+    int pin;                // 1: the listed experts' slots become pinned
     int *slot_of;           // [max_layers * E]
     int *slot_key;          // [slots]
     uint32_t *slot_used;    // [slots]
@@ -106,7 +110,8 @@ __global__ void __launch_bounds__(kPlanThreads) k_tier_plan(TierPlanArgs a)
         } else {
             const int s = slot_of_l[e];
             if (s >= 0 && s < a.slots) {
-                a.slot_used[s] = a.stamp;
+                if (a.pin) a.slot_used[s] = kPinned;
+                else if (a.slot_used[s] != kPinned) a.slot_used[s] = a.stamp;
                 hit = 1;
             } else {
                 miss = 1;
@@ -136,7 +141,7 @@ __global__ void __launch_bounds__(kPlanThreads) k_tier_plan(TierPlanArgs a)
             }
             return;
         }
-        uint32_t lo = 0, hi = a.stamp - 1;   // #{stamp <= hi} >= n_miss
+        uint32_t lo = 0, hi = a.stamp - 1;   // #{stamp <= hi} >= n_miss (pinned slots never count)
         while (lo < hi) {
             const uint32_t mid = lo + (hi - lo) / 2;
             int c = 0;
@@ -177,7 +182,7 @@ __global__ void __launch_bounds__(kPlanThreads) k_tier_plan(TierPlanArgs a)
             if (old >= 0) a.slot_of[old] = -1;
             a.slot_key[s] = a.layer * a.E + e;
             slot_of_l[e] = s;
-            a.slot_used[s] = a.stamp;
+            a.slot_used[s] = a.pin ? kPinned : a.stamp;
             a.fill[rank] = make_int2(s, e);
         }
         if (n_taken != n_miss) {
@@ -249,6 +254,21 @@ __global__ void __launch_bounds__(kFillThreads) k_tier_fill(TierFillArgs a)
     }
 }
 
+// The ids 0 .. E-1 followed by E: the expert list of a whole layer (pinning).
+__global__ void k_tier_iota(int *ids, int E)
+{
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < E) ids[i] = i;
+    if (i == E) ids[E] = E;
+}
+
+cudaError_t launch_tier_iota(const k3moe &h)
+{
+    const int E = h.cfg.n_experts;
+    k_tier_iota<<<(E + 256) / 256, 256>>>(h.tier.all_ids, E);
+    return cudaGetLastError();
+}
+
 // A reloaded layer gives up its slots: they become free and its table empty.
 __global__ void k_tier_forget(int *slot_of, int *slot_key, uint32_t *slot_used, int layer, int E,
                               int slots)
@@ -261,12 +281,15 @@ __global__ void k_tier_forget(int *slot_of, int *slot_key, uint32_t *slot_used, 
     }
 }
 
-cudaError_t launch_tier_plan(k3moe &h, int layer, cudaStream_t s)
+cudaError_t launch_tier_plan(k3moe &h, int layer, cudaStream_t s, bool pin)
 {
     TierDev &t = h.tier;
     TierPlanArgs a;
-    a.touched = h.ws.touched;
-    a.n_touched = h.ws.n_touched;
+    // a pin lists every expert of the layer (the table's iota), else the
+    // forward's touched experts
+    a.touched = pin ? t.all_ids : h.ws.touched;
+    a.n_touched = pin ? t.all_ids + h.cfg.n_experts : h.ws.n_touched;
+    a.pin = pin ? 1 : 0;
     a.slot_of = t.slot_of;
     a.slot_key = t.slot_key;
     a.slot_used = t.slot_used;

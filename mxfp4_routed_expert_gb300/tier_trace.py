@@ -29,12 +29,15 @@ def trace_from_counts(layer: int, counts) -> tuple:
     return int(layer), tuple(int(e) for e in np.flatnonzero(np.asarray(counts) > 0))
 
 
-def replay(trace, slots: int, policy: str = "tier", expert_bytes: int = 0) -> dict:
+def replay(trace, slots: int, policy: str = "tier", expert_bytes: int = 0, pin=()) -> dict:
     """Hits, misses and bytes copied when `trace` runs on `slots` slots.
 
     Every forward's experts must fit at once (slots >= the most experts any one
     forward touches), as the tier requires. compulsory = the distinct
-    (layer, expert) keys: the misses no policy can avoid."""
+    (layer, expert) keys: the misses no policy can avoid. `pin`: (layer,
+    experts) entries placed before the trace in slots no eviction takes (the
+    pages' pinned slots, `k3moe_tier_pin_layer`); their copies are counted in
+    `pin_copies`, not in the misses."""
     if policy not in ("tier", "belady"):
         raise ValueError(f"unknown policy {policy!r}")
     trace = [(int(layer), tuple(sorted(set(int(e) for e in ex)))) for layer, ex in trace]
@@ -48,6 +51,12 @@ def replay(trace, slots: int, policy: str = "tier", expert_bytes: int = 0) -> di
     used = [0] * slots         # slot -> stamp of its last forward (0: never)
     where = {}                 # (layer, expert) -> slot
     hits = misses = 0
+    PIN = float("inf")         # a pinned slot: never below a forward's stamp
+    pin_keys = sorted({(int(l), int(e)) for l, ex in pin for e in ex})
+    if len(pin_keys) > slots:
+        raise ValueError("more pinned experts than slots")
+    for s_, k in enumerate(pin_keys):
+        key[s_], used[s_], where[k] = k, PIN, s_
     for i, (layer, ex) in enumerate(trace):
         stamp = i + 1
         miss = []
@@ -55,11 +64,14 @@ def replay(trace, slots: int, policy: str = "tier", expert_bytes: int = 0) -> di
             k = (layer, e)
             nxt[k].popleft()
             if k in where:
-                used[where[k]] = stamp
+                if used[where[k]] != PIN:
+                    used[where[k]] = stamp
                 hits += 1
             else:
                 miss.append(k)
         free = [s for s in range(slots) if used[s] < stamp]
+        if len(free) < len(miss):
+            raise ValueError("a forward's misses do not fit beside the pinned slots")
         if policy == "tier":
             chosen = sorted(sorted(free, key=lambda s: (used[s], s))[:len(miss)])
         else:   # furthest next use first; never used again counts as infinitely far
@@ -79,4 +91,4 @@ def replay(trace, slots: int, policy: str = "tier", expert_bytes: int = 0) -> di
     total = hits + misses
     return {"slots": slots, "policy": policy, "hits": hits, "misses": misses,
             "hit_rate": hits / total if total else 0.0, "compulsory": len(nxt),
-            "bytes_copied": misses * int(expert_bytes)}
+            "bytes_copied": misses * int(expert_bytes), "pin_copies": len(pin_keys)}

@@ -47,7 +47,9 @@ class LruModel:
         self.hits = 0
         self.misses = 0
 
-    def forward(self, layer, touched):
+    PIN = 1 << 40   # a pinned slot's stamp: above every forward's
+
+    def forward(self, layer, touched, pin=False):
         self.stamp += 1
         where = {k: s for s, k in enumerate(self.key) if k is not None}
         miss = []
@@ -56,14 +58,17 @@ class LruModel:
             if s is None:
                 miss.append(int(e))
             else:
-                self.used[s] = self.stamp
+                if pin:
+                    self.used[s] = self.PIN
+                elif self.used[s] != self.PIN:
+                    self.used[s] = self.stamp
                 self.hits += 1
         cand = sorted((self.used[s], s) for s in range(len(self.key)) if self.used[s] < self.stamp)
         assert len(cand) >= len(miss)
         victims = sorted(s for _, s in cand[:len(miss)])
         for e, s in zip(miss, victims):
             self.key[s] = (layer, e)
-            self.used[s] = self.stamp
+            self.used[s] = self.PIN if pin else self.stamp
         self.misses += len(miss)
 
 
@@ -242,3 +247,48 @@ def test_tier_chain_matches_the_resident_chain():
             lay.close()
     for y in ys[1:]:
         assert_close(y, ys[0], "tiered chain vs resident chain", rel=2e-3, cos=0.99999)
+
+
+def test_tier_pinned_layer_only_hits():
+    """A pinned layer's experts are copied in once and never evicted: its
+    forwards only hit while two other layers churn through the other slots."""
+    import mxfp4_routed_expert_gb300 as km
+    E = MID.n_experts
+    layers = [k3synth.make_layer(MID, 90 + i, 0, k3synth.TINY_RECIPE) for i in range(3)]
+    lay = Layer(MID, layers, max_tokens=8, tier_slots=3 * E)
+    model = LruModel(3 * E)
+    try:
+        km.k3moe_tier_pin_layer(lay.h, 0)
+        km.k3moe_tier_pin_layer(lay.h, 0)       # again: nothing happens
+        model.forward(0, range(E), pin=True)
+        assert km.k3moe_get_tier_stats(lay.h)["misses"] == E
+        for layer, T, seed in [(1, 8, 1), (0, 8, 2), (2, 8, 3), (1, 8, 4), (0, 8, 5), (2, 8, 6)]:
+            d = layers[layer]
+            x, _ = guarded_tokens(MID, d, seed, T)
+            before = km.k3moe_get_tier_stats(lay.h)["misses"]
+            y = lay.forward(x, layer=layer)
+            r = lay.routing(T)
+            ref, tr = oracle.layer_forward(MID, d, x, trace=True)
+            check_routing(r, MID, x, tr["ids"], tr["w"])
+            assert_close(bf16_to_f64(y), ref)
+            if layer == 0:
+                assert km.k3moe_get_tier_stats(lay.h)["misses"] == before
+            model.forward(layer, np.nonzero(r["counts"])[0])
+        st = km.k3moe_get_tier_stats(lay.h)
+    finally:
+        lay.close()
+    assert (st["hits"], st["misses"]) == (model.hits, model.misses)
+
+
+def test_tier_pin_needs_room():
+    import mxfp4_routed_expert_gb300 as km
+    E = MID.n_experts
+    d = k3synth.make_layer(MID, 95, 0, k3synth.TINY_RECIPE)
+    lay = Layer(MID, [d], max_tokens=4, tier_slots=2 * E - 1)   # the first pin needs 2E
+    try:
+        with pytest.raises(km.K3MoEError) as ei:   # a pin leaves fewer than E slots to the rest
+            km.k3moe_tier_pin_layer(lay.h, 0)
+        assert ei.value.code == km.K3MOE_ERR_INVALID_ARG
+    finally:
+        lay.close()
+

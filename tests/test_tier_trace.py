@@ -53,3 +53,19 @@ def test_cyclic_scan_defeats_lru_but_not_the_optimum():
 def test_a_forward_must_fit():
     with pytest.raises(ValueError):
         replay([(0, range(9))], 8)
+
+
+def test_pinned_layer_never_misses_and_survives_the_scan():
+    # the cyclic scan again, with layer 0 pinned: its requests all hit
+    tr = [(l, range(8)) for _ in range(10) for l in range(4)]
+    st = replay(tr, 24, "tier", pin=[(0, range(8))])
+    assert st["pin_copies"] == 8
+    assert st["hits"] >= 10 * 8          # every visit of layer 0
+    plain = replay(tr, 24, "tier")
+    assert st["hits"] > plain["hits"]
+
+
+def test_pins_must_leave_room():
+    with pytest.raises(ValueError):
+        replay([(1, range(8))], 12, "tier", pin=[(0, range(8))])
+
