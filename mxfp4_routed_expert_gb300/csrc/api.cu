@@ -283,7 +283,8 @@ int run_layer(k3moe *h, const LayerDev &w, const __nv_bfloat16 *x, __nv_bfloat16
             K3_STEP("tier_plan", launch_tier_plan(*h, w.index, s));
             K3_STEP("tier_fill", launch_tier_fill(*h, w, s));
         }
-        K3_STEP("shared_gate_up_gemv", tma ? launch_dense_tma(*h, w, x, nullptr, T, s, 1, fused)
+        K3_STEP("shared_gate_up_gemv", tma ? launch_dense_tma(*h, w, x, nullptr, T, s, 1, fused, 0, false,
+                                                              false, tier && T == 1)
                                            : launch_dense_x(*h, w, x, T, s, 1, hin != nullptr));
     }
     if (T > 1) {   // T == 1: written by route_topk

@@ -447,7 +447,7 @@ cudaError_t init_dense_tma(const k3moe_config &c)
 // part: 0 = router + down, 1 = shared gate/up, 2 = up (with the latent norm)
 cudaError_t launch_dense_tma(const k3moe &h, const LayerDev &w, const __nv_bfloat16 *x,
                              __nv_bfloat16 *y, int T, cudaStream_t s, int part, const float *hin,
-                             int t0, bool ordered, bool wait)
+                             int t0, bool ordered, bool wait, bool spare_sm)
 {
     const k3moe_config &c = h.cfg;
     DenseTArgs a = {};
@@ -498,7 +498,8 @@ cudaError_t launch_dense_tma(const k3moe &h, const LayerDev &w, const __nv_bfloa
     const int TB = T == 1 ? 1 : 2;
     a.ns = stages_for(a.mode, a.K, TB);
     const int groups = (a.units + kCW - 1) / kCW;
-    const int grid = groups < h.sm_count ? groups : h.sm_count;
+    const int sms = spare_sm && h.sm_count > 1 ? h.sm_count - 1 : h.sm_count;
+    const int grid = groups < sms ? groups : sms;
     const size_t smem = dense_tma_smem(a.mode, a.K, TB, a.ns);
     // The shared gate/up reads only the layer input x and writes its own output
     // rows; the layer's first kernel (router+down, launched in stream order)

@@ -215,10 +215,12 @@ bool build_dense_tma_maps(const k3moe_config &c, LayerDev &w);
 // t0: the launch covers tokens t0.. of the batch (x and y already offset; the
 // workspace rows are offset here). ordered: launch in plain stream order (the
 // first kernel of a dense feed-forward layer).
+// spare_sm: leave one SM to a block that runs beside this kernel (the
+// expert tier's planning block, which fills an SM's register file).
 cudaError_t launch_dense_tma(const k3moe &h, const LayerDev &w, const __nv_bfloat16 *x,
                              __nv_bfloat16 *y, int T, cudaStream_t s, int part,
                              const float *hin = nullptr, int t0 = 0, bool ordered = false,
-                             bool wait = false);
+                             bool wait = false, bool spare_sm = false);
 bool expert_smem_fits(const k3moe_config &c);
 // expert tier: which touched experts are resident and which slots the others
 // take (one block), then the copy of the missed experts into their slots
