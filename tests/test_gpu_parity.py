@@ -223,10 +223,12 @@ def test_forward_host_matches_device_forward():
         km.k3moe_forward_host(lay.h, 0, x, y_host, 6)
     finally:
         lay.close()
-    # the w2 scatter-add uses fp32 atomics, whose order varies between runs, so an
-    # output may differ by one bf16 unit in the last place
+    # the w2 scatter-add uses fp32 atomics, whose order varies between runs: an
+    # output may differ by one bf16 unit in the last place, and an output that
+    # cancels to near zero by more than one unit of its own, so the two runs
+    # are compared on the output's scale (as the host-buffer tests below do)
     a, b = bf16_to_f64(y_host), bf16_to_f64(y_dev)
-    assert np.all(np.abs(a - b) <= np.abs(b) * 2.0 ** -7 + 1e-30)
+    assert np.max(np.abs(a - b)) <= np.max(np.abs(b)) * 2.0 ** -7
 
 
 @pytest.mark.parametrize("shape_T", [("mid", 1), ("mid", 2), ("wide", 37)])
