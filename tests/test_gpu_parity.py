@@ -336,6 +336,52 @@ def test_k3_decode_T1(k3layer):
         assert_close(bf16_to_f64(y), ref, f"K3 T=1 token {t}")
 
 
+def test_k3_residual_T1(k3layer):
+    """The RMSNorm in front of the MoE fused into the decode kernels at K3 size
+    (hidden 7168: 14 float4 per consumer thread per token)."""
+    import mxfp4_routed_expert_gb300 as km
+    d, lay = k3layer
+    shape = k3synth.K3
+    g = k3synth.post_norm_gain(shape, 1)
+    make = lambda att: oracle.round_bf16(   # noqa: E731
+        oracle.residual_input(k3synth.make_residual(shape, 1, 1, 0, att), g, shape.rms_eps))
+    _, att = guarded_tokens(shape, d, 1, 1, make=make)
+    hres = k3synth.make_residual(shape, 1, 1, 0, att)
+    km.k3moe_load_post_norm(lay.h, 0, g)
+    y = lay.forward_residual(hres)
+    x_gpu = lay.layer_input(1)
+    r = lay.routing(1)
+    v = oracle.residual_input(hres, g, shape.rms_eps)
+    step = np.ldexp(1.0, np.frexp(np.abs(v))[1] - 8)
+    assert np.all(np.abs(bf16_to_f64(x_gpu) - v) <= step)
+    ref, tr = oracle.layer_forward(shape, d, x_gpu, trace=True)
+    check_routing(r, shape, x_gpu, tr["ids"], tr["w"])
+    assert_close(bf16_to_f64(y), ref, "K3 T=1 from the residual")
+
+
+def test_k3_tier_T1(k3layer):
+    """The expert tier at K3 size: the layer's 15.7 GB of experts in pinned host
+    memory, 896 device slots. The first forward of a token copies its 16
+    experts in, the second finds them resident; both match the oracle."""
+    import mxfp4_routed_expert_gb300 as km
+    d, _ = k3layer
+    shape = k3synth.K3
+    pool, _ = guarded_tokens(shape, d, 0, 64, stream=7)
+    x = pool[5:6]
+    ref, tr = oracle.layer_forward(shape, d, x, trace=True)
+    tl = Layer(shape, [d], max_tokens=1, tier_slots=shape.n_experts)
+    try:
+        for want in ((0, 16), (16, 16)):
+            y = tl.forward(x)
+            r = tl.routing(1)
+            check_routing(r, shape, x, tr["ids"], tr["w"])
+            assert_close(bf16_to_f64(y), ref, "K3 T=1 through the tier")
+            st = km.k3moe_get_tier_stats(tl.h)
+            assert (st["hits"], st["misses"]) == want
+    finally:
+        tl.close()
+
+
 def test_k3_T64_covering(k3layer):
     d, lay = k3layer
     shape = k3synth.K3
