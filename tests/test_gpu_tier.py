@@ -76,8 +76,10 @@ def run_sequence(shape, layers, slots, steps, expert_path=None, max_tokens=64):
     """Forwards (layer, T, seed) through one tiered handle, each against the
     oracle; returns the handle's counters and the model's."""
     import mxfp4_routed_expert_gb300 as km
+    from mxfp4_routed_expert_gb300.tier_trace import replay, trace_from_counts
     lay = Layer(shape, layers, max_tokens=max_tokens, tier_slots=slots)
     model = LruModel(slots)
+    trace = []
     try:
         if expert_path is not None:
             km.k3moe_set_expert_path(lay.h, expert_path)
@@ -90,9 +92,13 @@ def run_sequence(shape, layers, slots, steps, expert_path=None, max_tokens=64):
             check_routing(r, shape, x, tr["ids"], tr["w"])
             assert_close(bf16_to_f64(y), ref, f"y (layer {layer}, T={T})")
             model.forward(layer, np.nonzero(r["counts"])[0])
+            trace.append(trace_from_counts(layer, r["counts"]))
         st = km.k3moe_get_tier_stats(lay.h)
     finally:
         lay.close()
+    # the shipped sizing tool replays the same trace to the same counters
+    rp = replay(trace, slots, "tier", expert_bytes=expert_bytes(shape))
+    assert (rp["hits"], rp["misses"], rp["bytes_copied"]) == (st["hits"], st["misses"], st["bytes_filled"])
     return st, model
 
 
