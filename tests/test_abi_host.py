@@ -24,7 +24,7 @@ def declared():
     return sorted(set(re.findall(r"K3MOE_API\s+[\w\s\*]*?\b(k3moe_\w+)\s*\(", src)))
 
 
-def test_header_declares_the_north_star_calls():
+def test_header_declares_the_layer_calls():
     names = declared()
     for n in ("k3moe_create", "k3moe_load_layer", "k3moe_forward", "k3moe_destroy"):
         assert n in names
