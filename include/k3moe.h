@@ -76,7 +76,11 @@ typedef struct k3moe k3moe;
  * situ_b1 * situ_b2 <= 512.
  * K3: hidden 7168, latent 3584, n_experts 896, topk 16, moe_inter 3072,
  * shared_inter 6144 (two shared experts fused), rms_eps 1e-5, situ_b1 4,
- * situ_b2 25, routed_scale 1, renorm 1, latent_norm 1. */
+ * situ_b2 25, routed_scale 1, renorm 1, latent_norm 1.
+ * Dense feed-forward layer (the model's layer 0, y = W2 . SiTU(W1 x, W3 x),
+ * K3: hidden 7168, width 33792): n_experts, topk, latent and moe_inter all 0,
+ * shared_inter the width; load_layer then reads only shared_w1/w3/w2, and the
+ * decode kernels must fit the width (else K3MOE_ERR_SHAPE). */
 typedef struct {
     uint32_t struct_size;   /* sizeof(k3moe_config), checked */
     int32_t hidden;         /* H: width of x and y */
@@ -100,7 +104,8 @@ typedef struct {
  * bf16 tensors are raw bfloat16 bit patterns. The six expert arrays hold one
  * pointer per expert (E entries each; the arrays themselves are host memory);
  * the pointees, like every other pointer here, live where `where` says.
- * Bytes are copied unchanged into library-owned device memory. */
+ * Bytes are copied unchanged into library-owned device memory (with the
+ * expert tier on, the expert arrays into library-owned pinned host memory). */
 typedef struct {
     uint32_t struct_size;          /* sizeof(k3moe_layer_weights), checked */
     int32_t where;                 /* K3MOE_HOST or K3MOE_DEVICE */
@@ -128,7 +133,9 @@ K3MOE_API int k3moe_create(const k3moe_config *cfg, k3moe **out);
  * is checked against the whole layer before anything is allocated
  * (K3MOE_ERR_OOM). Every scale byte is checked: 255 returns
  * K3MOE_ERR_BAD_SCALE and the layer stays unloaded. Reloading a slot replaces
- * it. layer is in [0, max_layers). */
+ * it (and drops its post-norm gain and tier pin). layer is in [0, max_layers).
+ * With the expert tier on, the expert arrays go to pinned host memory instead
+ * (K3MOE_ERR_OOM when it cannot be pinned). */
 K3MOE_API int k3moe_load_layer(k3moe *h, int layer, const k3moe_layer_weights *w);
 
 /* One layer on T tokens: x [T, H] bf16 -> y [T, H] bf16, both device pointers
@@ -152,10 +159,12 @@ K3MOE_API int k3moe_forward_host(k3moe *h, int layer, const void *x_host, void *
 
 /* Copies the routing of the last forward into caller-owned device buffers
  * (any may be NULL), asynchronously on `stream`:
- *   ids [T, k] int32 and w [T, k] fp32, slot j in descending ch order;
+ *   ids [T, k] int32 and w [T, k] fp32, slot j in descending ch order (with
+ *   the top-p cut: the kept picks first, then id -1 / weight 0);
  *   counts [E] int32; offsets [E+1] int32 (exclusive prefix sum of counts);
  *   perm [T*k] int32: flat pair indices t*k+j grouped by expert (ascending),
- *   and by ascending token inside an expert. */
+ *   and by ascending token inside an expert (the first offsets[E] entries).
+ * A dense feed-forward layer has no routing (zero-size tables). */
 K3MOE_API int k3moe_get_routing(k3moe *h, int32_t *ids, float *w, int32_t *counts, int32_t *offsets,
                       int32_t *perm, void *stream);
 
