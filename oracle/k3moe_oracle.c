@@ -19,6 +19,9 @@
  *    ("Kernels with a floating point contract").
  *  - Router, top-k, SiTU-GLU, the layer: kimi-k3-in-c README, section 9
  *    ("Picking 16 experts of 896"); colibri "Stable LatentMoE" bullet.
+ *  - The cut of the picks to cumulative weight p: the README's run-time
+ *    option K3_TOPP. The dense feed-forward layer 0: the README's K3Cfg
+ *    ("first_dense", "dense_inter"), in the model's SiTU-GLU form.
  *
  * Parity pins for every function live in the tests (hand-packed bytes, closed
  * forms, invariants, and a dense fp64 route through the whole layer).
