@@ -138,22 +138,25 @@ K3MOE_API int k3moe_create(const k3moe_config *cfg, k3moe **out);
  * (K3MOE_ERR_OOM when it cannot be pinned). */
 K3MOE_API int k3moe_load_layer(k3moe *h, int layer, const k3moe_layer_weights *w);
 
-/* One layer on T tokens: x [T, H] bf16 -> y [T, H] bf16, both device pointers
- * (x and y must not overlap). Asynchronous on `stream` (a cudaStream_t; NULL
+/* One layer on T tokens: x [T, H] bf16 -> y [T, H] bf16, both device pointers,
+ * 16-byte aligned (the kernels move activations in 16-byte vectors), not
+ * overlapping; K3MOE_ERR_INVALID_ARG otherwise. Asynchronous on `stream` (a cudaStream_t; NULL
  * is the legacy default stream). 1 <= T <= max_tokens. The routing of the
  * call stays readable through k3moe_get_routing until the next forward. */
 K3MOE_API int k3moe_forward(k3moe *h, int layer, const void *x, void *y, int T, void *stream);
 
 /* Layers first_layer .. first_layer + n_layers - 1 applied in sequence, with
  * x_next = bf16(RMSNorm(y) with unit gain and rms_eps) between two layers.
- * x, y: device [T, H] bf16. The routing of the last layer stays readable. */
+ * x, y: device [T, H] bf16, aligned and disjoint as for k3moe_forward. The
+ * routing of the last layer stays readable. */
 K3MOE_API int k3moe_forward_chain(k3moe *h, int first_layer, int n_layers, const void *x, void *y,
                         int T, void *stream);
 
 /* k3moe_forward with HOST buffers: copies x to the device, runs the layer,
  * copies y back and synchronises `stream`. Pinned host memory is faster but
- * not required; a pinned (device-mapped) y is written in place by the
- * layer's last kernel, without a copy back. */
+ * not required; a pinned (device-mapped), 16-byte aligned y is written in
+ * place by the layer's last kernel, without a copy back. Host pointers need
+ * no alignment. */
 K3MOE_API int k3moe_forward_host(k3moe *h, int layer, const void *x_host, void *y_host, int T,
                        void *stream);
 
@@ -180,7 +183,7 @@ K3MOE_API int k3moe_get_routing(k3moe *h, int32_t *ids, float *w, int32_t *count
  * drops it. K3MOE_ERR_NOT_LOADED when the layer is not loaded.
  *
  * k3moe_forward_residual takes h_in fp32 [T, hidden] (device memory, 16-byte
- * aligned), forms x = bf16(RMSNorm(h_in) * gain) per token (rms_eps of the
+ * aligned, as y must be), forms x = bf16(RMSNorm(h_in) * gain) per token (rms_eps of the
  * configuration) and runs the layer on x as k3moe_forward does. At T <= 2 the
  * norm runs inside the first two kernels of the layer (x never goes to
  * memory); otherwise a first kernel writes x to the workspace. The x used can

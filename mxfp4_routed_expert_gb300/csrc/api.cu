@@ -3,6 +3,7 @@
 // launch sequence of one layer, routing/intermediate readback and timing.
 #include <cmath>
 #include <cstdio>
+#include <cstdint>
 #include <cstring>
 #include <new>
 #include <string>
@@ -172,7 +173,10 @@ cudaEvent_t get_event(k3moe *h)
         return e;
     }
     cudaEvent_t e = nullptr;
-    cudaEventCreate(&e);
+    if (cudaEventCreate(&e) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
     return e;
 }
 
@@ -186,16 +190,19 @@ struct Prof {
     {
         if (h->profiling) {
             a = get_event(h);
-            cudaEventRecord(a, s);
+            if (a) cudaEventRecord(a, s);
         }
     }
     ~Prof()
     {
-        if (a) {
-            cudaEvent_t b = get_event(h);
-            cudaEventRecord(b, s);
-            h->prof.push_back({name, a, b});
+        if (!a) return;
+        cudaEvent_t b = get_event(h);
+        if (!b) {   // no event to close the bracket: this launch goes untimed
+            h->event_pool.push_back(a);
+            return;
         }
+        cudaEventRecord(b, s);
+        h->prof.push_back({name, a, b});
     }
 };
 
@@ -324,6 +331,10 @@ bool overlap(const void *a, size_t na, const void *b, size_t nb)
     const char *pa = (const char *)a, *pb = (const char *)b;
     return pa < pb + nb && pb < pa + na;
 }
+
+// The kernels read and write activations in 16-byte vectors (and through TMA
+// maps at T >= 16, whose base must be 16-byte aligned).
+bool misaligned(const void *p) { return (uintptr_t)p % 16 != 0; }
 
 void free_layer(LayerDev &l)
 {
@@ -628,7 +639,7 @@ int k3moe_forward(k3moe *h, int layer, const void *x, void *y, int T, void *stre
     if (layer < 0 || layer >= h->cfg.max_layers) return K3MOE_ERR_INVALID_ARG;
     if (T < 1 || T > h->cfg.max_tokens) return K3MOE_ERR_INVALID_ARG;
     const size_t nb = (size_t)T * h->cfg.hidden * 2;
-    if (overlap(x, nb, y, nb)) return K3MOE_ERR_INVALID_ARG;
+    if (overlap(x, nb, y, nb) || misaligned(x) || misaligned(y)) return K3MOE_ERR_INVALID_ARG;
     const LayerDev &w = h->layers[(size_t)layer];
     if (!w.loaded) return K3MOE_ERR_NOT_LOADED;
     if (cudaSetDevice(h->cfg.device) != cudaSuccess) return K3MOE_ERR_CUDA;
@@ -665,7 +676,7 @@ int k3moe_forward_residual(k3moe *h, int layer, const float *h_in, void *y, int 
     if (!h || !h_in || !y) return K3MOE_ERR_INVALID_ARG;
     if (layer < 0 || layer >= h->cfg.max_layers) return K3MOE_ERR_INVALID_ARG;
     if (T < 1 || T > h->cfg.max_tokens) return K3MOE_ERR_INVALID_ARG;
-    if ((uintptr_t)h_in % 16) return K3MOE_ERR_INVALID_ARG;
+    if (misaligned(h_in) || misaligned(y)) return K3MOE_ERR_INVALID_ARG;
     if (overlap(h_in, (size_t)T * h->cfg.hidden * 4, y, (size_t)T * h->cfg.hidden * 2))
         return K3MOE_ERR_INVALID_ARG;
     const LayerDev &w = h->layers[(size_t)layer];
@@ -681,7 +692,7 @@ int k3moe_forward_chain(k3moe *h, int first_layer, int n_layers, const void *x, 
     if (first_layer < 0 || first_layer + n_layers > h->cfg.max_layers) return K3MOE_ERR_INVALID_ARG;
     if (T < 1 || T > h->cfg.max_tokens) return K3MOE_ERR_INVALID_ARG;
     const size_t nb = (size_t)T * h->cfg.hidden * 2;
-    if (overlap(x, nb, y, nb)) return K3MOE_ERR_INVALID_ARG;
+    if (overlap(x, nb, y, nb) || misaligned(x) || misaligned(y)) return K3MOE_ERR_INVALID_ARG;
     for (int l = first_layer; l < first_layer + n_layers; l++)
         if (!h->layers[(size_t)l].loaded) return K3MOE_ERR_NOT_LOADED;
     if (cudaSetDevice(h->cfg.device) != cudaSuccess) return K3MOE_ERR_CUDA;
@@ -720,7 +731,7 @@ int k3moe_forward_host(k3moe *h, int layer, const void *x_host, void *y_host, in
     {
         cudaPointerAttributes ay{};
         if (cudaPointerGetAttributes(&ay, y_host) == cudaSuccess && ay.type == cudaMemoryTypeHost &&
-            ay.devicePointer) {
+            ay.devicePointer && !misaligned(ay.devicePointer)) {
             if (cudaMemcpyAsync(h->ws.xbuf0, x_host, nb, cudaMemcpyHostToDevice, s) != cudaSuccess)
                 return K3MOE_ERR_CUDA;
             const int rc =
@@ -728,7 +739,7 @@ int k3moe_forward_host(k3moe *h, int layer, const void *x_host, void *y_host, in
             if (rc != K3MOE_OK) return rc;
             return cudaStreamSynchronize(s) == cudaSuccess ? K3MOE_OK : K3MOE_ERR_CUDA;
         }
-        cudaGetLastError();   // pageable y: the copy path below
+        cudaGetLastError();   // pageable or unaligned y: the copy path below
     }
     if (cudaMemcpyAsync(h->ws.xbuf0, x_host, nb, cudaMemcpyHostToDevice, s) != cudaSuccess)
         return K3MOE_ERR_CUDA;

@@ -199,10 +199,13 @@ def test_forward_argument_errors():
     try:
         x = torch.zeros((8, 256), dtype=torch.int16, device="cuda")
         y = torch.zeros_like(x)
+        xo = x.data_ptr() + 2            # inside x, not on a 16-byte boundary
         for args, code in [((1, x, y, 4), km.K3MOE_ERR_INVALID_ARG),     # layer out of range
                            ((0, x, y, 5), km.K3MOE_ERR_INVALID_ARG),     # T > max_tokens
                            ((0, x, y, 0), km.K3MOE_ERR_INVALID_ARG),     # T = 0
-                           ((0, x, x, 4), km.K3MOE_ERR_INVALID_ARG)]:    # x and y overlap
+                           ((0, x, x, 4), km.K3MOE_ERR_INVALID_ARG),     # x and y overlap
+                           ((0, xo, y, 4), km.K3MOE_ERR_INVALID_ARG),    # x unaligned
+                           ((0, x, y.data_ptr() + 8, 4), km.K3MOE_ERR_INVALID_ARG)]:  # y unaligned
             with pytest.raises(km.K3MoEError) as ei:
                 km.k3moe_forward(lay.h, *args)
             assert ei.value.code == code
