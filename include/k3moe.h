@@ -245,6 +245,13 @@ K3MOE_API int k3moe_set_expert_path(k3moe *h, int mode);
  * kernel copies the missed experts from the host block into their slots; the
  * expert kernels then read the slots. The host takes no part (no
  * synchronisation, no copy calls). Results are those of the resident layer.
+ * Ages are 32-bit stamps kept by the host and passed to each forward's plan:
+ * a tiered forward must be launched, not replayed from a captured CUDA
+ * graph. Once the count reaches 2^31 a small kernel shifts the slots' stamps
+ * down, keeping the order of the last 2^24 (older slots tie, the lower slot
+ * going first); the environment variable K3MOE_TIER_REBASE="at,keep", read
+ * here, moves those two counts (1 <= keep < at <= 2^31; else
+ * K3MOE_ERR_INVALID_ARG) so that a short run goes through the shift.
  * slots must be >= n_experts (the most one forward touches) and <= 16384;
  * slots = 0 turns the tier off. Reloading a tiered layer frees its slots.
  * Errors: K3MOE_ERR_INVALID_ARG (NULL handle, a layer already loaded, slots

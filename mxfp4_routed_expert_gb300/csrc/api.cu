@@ -3,6 +3,7 @@
 // launch sequence of one layer, routing/intermediate readback and timing.
 #include <cmath>
 #include <cstdio>
+#include <cstdlib>
 #include <cstdint>
 #include <cstring>
 #include <new>
@@ -887,6 +888,17 @@ int k3moe_set_expert_tier(k3moe *h, int slots)
         cudaGetLastError();
         cudaFree(t.block);
         return K3MOE_ERR_CUDA;
+    }
+    // K3MOE_TIER_REBASE="at,keep" moves the stamp rebase from its defaults
+    // (2^31, 2^24) to small counts, so that a short run goes through it
+    if (const char *env = std::getenv("K3MOE_TIER_REBASE")) {
+        unsigned long at = 0, keep = 0;
+        if (std::sscanf(env, "%lu,%lu", &at, &keep) != 2 || keep < 1 || keep >= at || at > kTierRebaseAt) {
+            cudaFree(t.block);
+            return K3MOE_ERR_INVALID_ARG;
+        }
+        t.rebase_at = (uint32_t)at;
+        t.rebase_keep = (uint32_t)keep;
     }
     t.slots = slots;
     h->tier = t;

@@ -73,6 +73,11 @@ struct LayerDev {
 // whose home is pinned host memory.
 constexpr int kTierPieces = 9;          // w1p w1s w3p w3s w2p w2s w1max w3max w2max
 constexpr int kTierMaxSlots = 16384;
+// Stamps are 32-bit and 0xFFFFFFFF marks a pinned slot: once the counter
+// reaches kTierRebaseAt, the slots' stamps are shifted down so that the last
+// kTierRebaseKeep stamps keep their order (older ones tie at 1).
+constexpr uint32_t kTierRebaseAt = 0x80000000u;
+constexpr uint32_t kTierRebaseKeep = 1u << 24;
 struct TierDev {
     int slots = 0;
     void *block = nullptr;              // device: slot arrays, then the tables
@@ -86,7 +91,9 @@ struct TierDev {
     int *n_fill = nullptr;
     unsigned long long *stats = nullptr;   // hits, misses, bytes filled
     int *all_ids = nullptr;             // [E + 1]: 0 .. E-1, then E (a layer's list, for pinning)
-    uint32_t stamp = 0;                 // forwards planned so far
+    uint32_t stamp = 0;                 // last stamp given to a forward
+    uint32_t rebase_at = kTierRebaseAt;
+    uint32_t rebase_keep = kTierRebaseKeep;
     int pinned = 0;                     // slots held by pinned layers
 };
 

@@ -269,6 +269,16 @@ cudaError_t launch_tier_iota(const k3moe &h)
     return cudaGetLastError();
 }
 
+// Shifts every used, unpinned slot's stamp down by `shift` (stamps at or
+// below it become 1: used, and older than every later stamp).
+__global__ void k_tier_rebase(uint32_t *slot_used, int slots, uint32_t shift)
+{
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= slots) return;
+    const uint32_t u = slot_used[i];
+    if (u != 0u && u != kPinned) slot_used[i] = u > shift ? u - shift : 1u;
+}
+
 // A reloaded layer gives up its slots: they become free and its table empty.
 __global__ void k_tier_forget(int *slot_of, int *slot_key, uint32_t *slot_used, int layer, int E,
                               int slots)
@@ -284,6 +294,15 @@ __global__ void k_tier_forget(int *slot_of, int *slot_key, uint32_t *slot_used, 
 cudaError_t launch_tier_plan(k3moe &h, int layer, cudaStream_t s, bool pin)
 {
     TierDev &t = h.tier;
+    if (t.stamp >= t.rebase_at) {
+        // stream-ordered behind the previous forward's plan (a plain launch
+        // starts after the kernel before it has finished)
+        const uint32_t shift = t.stamp - t.rebase_keep;
+        k_tier_rebase<<<(t.slots + 255) / 256, 256, 0, s>>>(t.slot_used, t.slots, shift);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        t.stamp -= shift;
+    }
     TierPlanArgs a;
     // a pin lists every expert of the layer (the table's iota), else the
     // forward's touched experts

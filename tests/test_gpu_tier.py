@@ -40,16 +40,26 @@ class LruModel:
     """The slot policy on the host: which (layer, expert) each slot holds and
     the stamp of the forward that last used it (0: never)."""
 
-    def __init__(self, slots):
+    def __init__(self, slots, rebase=None):
         self.key = [None] * slots
         self.used = [0] * slots
         self.stamp = 0
         self.hits = 0
         self.misses = 0
+        self.rebase = rebase   # (at, keep) of the stamp shift, or None: never
+        self.rebases = 0
+        self.log = []          # (layer, touched) of every forward
 
     PIN = 1 << 40   # a pinned slot's stamp: above every forward's
 
     def forward(self, layer, touched, pin=False):
+        if self.rebase and self.stamp >= self.rebase[0]:
+            # the last `keep` stamps keep their order, older used slots tie at 1
+            shift = self.stamp - self.rebase[1]
+            self.used = [u if u in (0, self.PIN) else max(u - shift, 1) for u in self.used]
+            self.stamp -= shift
+            self.rebases += 1
+        self.log.append((layer, tuple(int(e) for e in touched)))
         self.stamp += 1
         where = {k: s for s, k in enumerate(self.key) if k is not None}
         miss = []
@@ -72,13 +82,20 @@ class LruModel:
         self.misses += len(miss)
 
 
-def run_sequence(shape, layers, slots, steps, expert_path=None, max_tokens=64):
+def run_sequence(shape, layers, slots, steps, expert_path=None, max_tokens=64, rebase=None):
     """Forwards (layer, T, seed) through one tiered handle, each against the
-    oracle; returns the handle's counters and the model's."""
+    oracle; returns the handle's counters and the model's. rebase: (at, keep)
+    given to the handle through K3MOE_TIER_REBASE."""
+    import os
     import mxfp4_routed_expert_gb300 as km
     from mxfp4_routed_expert_gb300.tier_trace import replay, trace_from_counts
-    lay = Layer(shape, layers, max_tokens=max_tokens, tier_slots=slots)
-    model = LruModel(slots)
+    if rebase:
+        os.environ["K3MOE_TIER_REBASE"] = f"{rebase[0]},{rebase[1]}"
+    try:
+        lay = Layer(shape, layers, max_tokens=max_tokens, tier_slots=slots)
+    finally:
+        os.environ.pop("K3MOE_TIER_REBASE", None)
+    model = LruModel(slots, rebase)
     trace = []
     try:
         if expert_path is not None:
@@ -96,9 +113,9 @@ def run_sequence(shape, layers, slots, steps, expert_path=None, max_tokens=64):
         st = km.k3moe_get_tier_stats(lay.h)
     finally:
         lay.close()
-    # the shipped sizing tool replays the same trace to the same counters
-    rp = replay(trace, slots, "tier", expert_bytes=expert_bytes(shape))
-    assert (rp["hits"], rp["misses"], rp["bytes_copied"]) == (st["hits"], st["misses"], st["bytes_filled"])
+    if not rebase:   # the shipped sizing tool replays the same trace to the same counters
+        rp = replay(trace, slots, "tier", expert_bytes=expert_bytes(shape))
+        assert (rp["hits"], rp["misses"], rp["bytes_copied"]) == (st["hits"], st["misses"], st["bytes_filled"])
     return st, model
 
 
@@ -114,6 +131,42 @@ def test_tier_decode_sequence_matches_oracle_and_policy():
     assert model.hits > 0 and model.misses > MID.n_experts   # both hits and evictions happened
     assert (st["hits"], st["misses"]) == (model.hits, model.misses)
     assert st["bytes_filled"] == model.misses * expert_bytes(MID)
+
+
+def test_tier_stamp_rebase_keeps_the_policy():
+    """The slots' 32-bit stamps are shifted down once the count reaches a
+    limit; with the limit at 4 and 2 stamps kept (a shift every second
+    forward, older slots tied at 1 and taken lower slot first) the handle's
+    counters follow the policy with the same shifts and every forward still
+    matches the oracle."""
+    layers = [k3synth.make_layer(MID, 20 + i, 0, k3synth.TINY_RECIPE) for i in range(3)]
+    steps = [(0, 1, 0), (1, 1, 1), (0, 1, 0), (2, 3, 2), (1, 1, 1), (0, 3, 3), (2, 1, 4),
+             (2, 1, 4), (1, 3, 5), (0, 1, 0), (2, 3, 6), (1, 1, 7), (0, 3, 3), (1, 3, 5)]
+    slots = MID.n_experts + 8
+    st, model = run_sequence(MID, layers, slots, steps, rebase=(4, 2))
+    assert model.rebases >= 5
+    assert (st["hits"], st["misses"]) == (model.hits, model.misses)
+    # the tie at 1 changes a victim here: without the shifts the counters differ
+    plain = LruModel(slots)
+    for layer, touched in model.log:
+        plain.forward(layer, touched)
+    assert (plain.hits, plain.misses) != (model.hits, model.misses)
+
+
+def test_tier_rebase_setting_checked(monkeypatch):
+    import mxfp4_routed_expert_gb300 as km
+    lay = Layer(MID, [None], max_tokens=4)
+    try:
+        for bad in ("2,2", "3,0", "5", "x,y", "4294967295,2"):
+            monkeypatch.setenv("K3MOE_TIER_REBASE", bad)
+            with pytest.raises(km.K3MoEError) as ei:
+                km.k3moe_set_expert_tier(lay.h, MID.n_experts)
+            assert ei.value.code == km.K3MOE_ERR_INVALID_ARG
+        monkeypatch.setenv("K3MOE_TIER_REBASE", "4,2")
+        km.k3moe_set_expert_tier(lay.h, MID.n_experts)
+        assert km.k3moe_get_tier_stats(lay.h)["slots"] == MID.n_experts
+    finally:
+        lay.close()
 
 
 @pytest.mark.parametrize("path", ["gemm", "gemv"])
