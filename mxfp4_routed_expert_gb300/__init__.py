@@ -122,7 +122,7 @@ def lib():
         L.k3moe_get_tier_stats.argtypes = [vp, ctypes.POINTER(k3moe_tier_stats)]
         for n in EXPORTS:
             if n not in ("k3moe_destroy", "k3moe_strerror"):
-                getattr(L, n).restype = i if n != "k3moe_destroy" else None
+                getattr(L, n).restype = i
         _lib = L
     return _lib
 
@@ -131,16 +131,27 @@ def strerror(code: int) -> str:
     return lib().k3moe_strerror(int(code)).decode()
 
 
+def _addr(v) -> int:
+    """Address of a dense, row-major buffer (a torch tensor or numpy array):
+    the library reads every buffer in that layout, so a strided view is refused
+    rather than read as if it were dense."""
+    if hasattr(v, "data_ptr"):
+        if not v.is_contiguous():
+            raise ValueError("tensor is not contiguous (row-major); pass .contiguous()")
+        return v.data_ptr()
+    if isinstance(v, np.ndarray):
+        if not v.flags["C_CONTIGUOUS"]:
+            raise ValueError("array is not C-contiguous; pass np.ascontiguousarray(...)")
+        return v.ctypes.data
+    raise TypeError(f"cannot pass {type(v)} as a pointer")
+
+
 def _ptr(v):
     if v is None:
         return None
     if isinstance(v, int):
         return ctypes.c_void_p(v)
-    if hasattr(v, "data_ptr"):
-        return ctypes.c_void_p(v.data_ptr())
-    if isinstance(v, np.ndarray):
-        return ctypes.c_void_p(v.ctypes.data)
-    raise TypeError(f"cannot pass {type(v)} as a pointer")
+    return ctypes.c_void_p(_addr(v))
 
 
 def _stream(s):
@@ -189,13 +200,7 @@ def layer_weights(tensors: dict, n_experts: int, where: int = K3MOE_HOST):
     keep = []
 
     def addr(v):
-        if v is None:
-            return None
-        if isinstance(v, np.ndarray):
-            assert v.flags["C_CONTIGUOUS"]
-            return v.ctypes.data
-        assert v.is_contiguous()
-        return v.data_ptr()
+        return None if v is None else _addr(v)
 
     def per_expert(v):
         base = addr(v)
@@ -241,12 +246,7 @@ def k3moe_forward(h: int, layer: int, x, y, T: int, stream=None) -> int:
 def k3moe_load_post_norm(h: int, layer: int, gain, where: int = K3MOE_HOST) -> int:
     """The RMSNorm gain (bf16 [hidden]: a numpy uint16 array for HOST, a CUDA
     tensor for DEVICE) in front of the MoE, for k3moe_forward_residual."""
-    if isinstance(gain, np.ndarray):
-        assert gain.flags["C_CONTIGUOUS"]
-        ptr = gain.ctypes.data
-    else:
-        ptr = _ptr(gain)
-    return _check(lib().k3moe_load_post_norm(ctypes.c_void_p(h), layer, ptr, where),
+    return _check(lib().k3moe_load_post_norm(ctypes.c_void_p(h), layer, _ptr(gain), where),
                   "k3moe_load_post_norm")
 
 

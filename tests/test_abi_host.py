@@ -96,3 +96,25 @@ def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(km, "_lib", None)
     with pytest.raises(RuntimeError, match="no fallback"):
         km.lib()
+
+
+def test_binding_refuses_strided_buffers():
+    """The library reads every buffer row-major and dense: the binding passes
+    the address of a contiguous tensor or array (or a plain integer address)
+    and refuses a strided view instead of handing over its first element."""
+    import numpy as np
+    import torch
+    import mxfp4_routed_expert_gb300 as km
+    t = torch.zeros((4, 8), dtype=torch.int16)
+    a = np.zeros((4, 8), dtype=np.uint16)
+    assert km._ptr(t).value == t.data_ptr()
+    assert km._ptr(t[1:3]).value == t[1:3].data_ptr()          # a block of rows is dense
+    assert km._ptr(a).value == a.ctypes.data
+    assert km._ptr(1234).value == 1234 and km._ptr(None) is None
+    for bad in (t[:, ::2], t.t(), a[:, 1:], a.T):
+        with pytest.raises(ValueError):
+            km._ptr(bad)
+    with pytest.raises(TypeError):
+        km._ptr([1, 2, 3])
+    with pytest.raises(ValueError):                             # weights too
+        km.layer_weights({"sh_w1": t.t(), "sh_w3": t, "sh_w2": t}, 0)
