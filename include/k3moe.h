@@ -209,6 +209,17 @@ K3MOE_API int k3moe_get_intermediate(k3moe *h, int which, void *dst, size_t byte
  * device-side error, or the first asynchronous CUDA error. */
 K3MOE_API int k3moe_sync_status(k3moe *h);
 
+/* Check of the device-side failure path (the README's engine reports a
+ * failed step by its exit code rather than hanging or returning a half-done
+ * result; kimi-k3-in-c README, "Exit codes"). Launches on `stream` one
+ * single-thread kernel whose wait on a barrier that nothing completes runs
+ * out after the same bounded limit (about two seconds) as every wait in the
+ * layer's kernels; it latches the time-out, so the next k3moe_sync_status
+ * returns K3MOE_ERR_TIMEOUT and clears it. Nothing faults, traps or hangs;
+ * the handle and its loaded layers stay usable. Errors: K3MOE_ERR_INVALID_ARG
+ * (NULL handle), K3MOE_ERR_CUDA (the launch failed). */
+K3MOE_API int k3moe_check_wait_timeout(k3moe *h, void *stream);
+
 /* Which routed-expert kernels a forward uses (same arithmetic, kimi-k3-in-c
  * README, Part II section 9, k3_moe step 3; results agree to fp32 rounding
  * order and fp16 operand rounding):

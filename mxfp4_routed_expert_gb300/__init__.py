@@ -38,7 +38,8 @@ EXPORTS = ("k3moe_create", "k3moe_load_layer", "k3moe_forward", "k3moe_forward_c
            "k3moe_sync_status", "k3moe_set_profiling", "k3moe_profile_read", "k3moe_destroy",
            "k3moe_strerror", "k3moe_abi_version", "k3moe_route_static", "k3moe_set_expert_path",
            "k3moe_set_expert_tier", "k3moe_get_tier_stats", "k3moe_load_post_norm",
-           "k3moe_forward_residual", "k3moe_set_topp", "k3moe_tier_pin_layer")
+           "k3moe_forward_residual", "k3moe_set_topp", "k3moe_tier_pin_layer",
+           "k3moe_check_wait_timeout")
 K3MOE_ROUTE_STATIC_MAX_LOGITS = 1 << 20
 K3MOE_EXPERT_AUTO, K3MOE_EXPERT_GEMV, K3MOE_EXPERT_GEMM = 0, 1, 2
 
@@ -120,6 +121,7 @@ def lib():
         L.k3moe_tier_pin_layer.argtypes = [vp, i]
         L.k3moe_forward_residual.argtypes = [vp, i, vp, vp, i, vp]
         L.k3moe_get_tier_stats.argtypes = [vp, ctypes.POINTER(k3moe_tier_stats)]
+        L.k3moe_check_wait_timeout.argtypes = [vp, vp]
         for n in EXPORTS:
             if n not in ("k3moe_destroy", "k3moe_strerror"):
                 getattr(L, n).restype = i
@@ -282,6 +284,13 @@ def k3moe_get_intermediate(h: int, which: int, dst, nbytes: int, stream=None) ->
 
 def k3moe_sync_status(h: int) -> int:
     return lib().k3moe_sync_status(ctypes.c_void_p(h))
+
+
+def k3moe_check_wait_timeout(h: int, stream=None) -> int:
+    """Launch a kernel whose one bounded wait runs out: the next
+    k3moe_sync_status returns K3MOE_ERR_TIMEOUT (about two seconds later)."""
+    return _check(lib().k3moe_check_wait_timeout(ctypes.c_void_p(h), _stream(stream)),
+                  "k3moe_check_wait_timeout")
 
 
 def k3moe_set_profiling(h: int, enable: bool) -> int:

@@ -961,6 +961,13 @@ int k3moe_set_topp(k3moe *h, float p)
     return K3MOE_OK;
 }
 
+int k3moe_check_wait_timeout(k3moe *h, void *stream)
+{
+    if (!h) return K3MOE_ERR_INVALID_ARG;
+    if (cudaSetDevice(h->cfg.device) != cudaSuccess) return K3MOE_ERR_CUDA;
+    return launch_wait_check(*h, (cudaStream_t)stream) == cudaSuccess ? K3MOE_OK : K3MOE_ERR_CUDA;
+}
+
 int k3moe_set_profiling(k3moe *h, int enable)
 {
     if (!h) return K3MOE_ERR_INVALID_ARG;

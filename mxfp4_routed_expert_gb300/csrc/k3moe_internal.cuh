@@ -235,6 +235,9 @@ cudaError_t launch_tier_plan(k3moe &h, int layer, cudaStream_t s, bool pin = fal
 cudaError_t launch_tier_iota(const k3moe &h);
 cudaError_t launch_tier_fill(const k3moe &h, const LayerDev &w, cudaStream_t s);
 cudaError_t launch_tier_forget(const k3moe &h, int layer, cudaStream_t s);
+// the detail word a k3moe_check_wait_timeout launch latches
+constexpr int kWaitCheckWhere = 900;
+cudaError_t launch_wait_check(const k3moe &h, cudaStream_t s);
 
 // ---- device helpers -----------------------------------------------------------
 __device__ __forceinline__ void set_err(int *err, int code, int detail)

@@ -214,6 +214,31 @@ def test_forward_argument_errors():
         lay.close()
 
 
+def test_device_wait_timeout_is_reported_and_the_handle_stays_usable():
+    """A kernel whose one bounded wait can never be satisfied latches the
+    time-out (after about two seconds) instead of hanging: k3moe_sync_status
+    returns it once, then the same handle runs a forward that matches the
+    oracle."""
+    import time
+    import mxfp4_routed_expert_gb300 as km
+    shape = k3synth.TINY
+    d = k3synth.make_layer(shape, 7, 0, k3synth.TINY_RECIPE)
+    x, _ = guarded_tokens(shape, d, 7, 4)
+    lay = Layer(shape, [d], max_tokens=4)
+    try:
+        assert km.k3moe_sync_status(lay.h) == 0
+        t0 = time.monotonic()
+        km.k3moe_check_wait_timeout(lay.h)
+        assert km.k3moe_sync_status(lay.h) == km.K3MOE_ERR_TIMEOUT
+        assert 1.5 < time.monotonic() - t0 < 60
+        assert km.k3moe_sync_status(lay.h) == 0          # read once, then cleared
+        y = lay.forward(x)
+        assert km.k3moe_sync_status(lay.h) == 0
+    finally:
+        lay.close()
+    assert_close(bf16_to_f64(y), oracle.layer_forward(shape, d, x))
+
+
 def test_forward_host_matches_device_forward():
     import mxfp4_routed_expert_gb300 as km
     shape = k3synth.TINY
