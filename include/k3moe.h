@@ -29,6 +29,14 @@
  * (an index out of range, a bounded wait that ran out) are latched in a device
  * word and returned by k3moe_sync_status.
  *
+ * Device memory: k3moe_create, k3moe_load_layer and k3moe_set_expert_tier
+ * check what they need (plus a margin: 64 MB for the workspace, 256 MB for a
+ * layer or the tier's slots) against free device memory before allocating,
+ * and return K3MOE_ERR_OOM with nothing allocated when it does not fit. The
+ * environment variable K3MOE_DEVICE_BUDGET_MB, read at each check, caps the
+ * free memory those checks assume at that many megabytes (a budget on a
+ * shared GPU).
+ *
  * Threading: a handle may be used by one host thread at a time.
  */
 #ifndef K3MOE_H

@@ -327,6 +327,24 @@ int run_layer(k3moe *h, const LayerDev &w, const __nv_bfloat16 *x, __nv_bfloat16
     return K3MOE_OK;
 }
 
+// Free device memory as the size checks see it: the runtime's figure, capped
+// at K3MOE_DEVICE_BUDGET_MB megabytes when that variable holds a number.
+cudaError_t free_device_bytes(size_t *fr)
+{
+    size_t tot = 0;
+    const cudaError_t e = cudaMemGetInfo(fr, &tot);
+    if (e != cudaSuccess) return e;
+    if (const char *env = std::getenv("K3MOE_DEVICE_BUDGET_MB")) {
+        char *end = nullptr;
+        const unsigned long long mb = std::strtoull(env, &end, 10);
+        if (end != env && *end == '\0' && mb < (1ull << 40)) {
+            const size_t cap = (size_t)mb << 20;
+            if (cap < *fr) *fr = cap;
+        }
+    }
+    return cudaSuccess;
+}
+
 bool overlap(const void *a, size_t na, const void *b, size_t nb)
 {
     const char *pa = (const char *)a, *pb = (const char *)b;
@@ -388,8 +406,8 @@ int k3moe_create(const k3moe_config *cfg, k3moe **out)
     h->cfg = *cfg;
     cudaDeviceGetAttribute(&h->sm_count, cudaDevAttrMultiProcessorCount, cfg->device);
     const size_t need = carve_workspace(*cfg, nullptr, nullptr);
-    size_t fr = 0, tot = 0;
-    if (cudaMemGetInfo(&fr, &tot) != cudaSuccess) {
+    size_t fr = 0;
+    if (free_device_bytes(&fr) != cudaSuccess) {
         delete h;
         return K3MOE_ERR_CUDA;
     }
@@ -488,8 +506,8 @@ int k3moe_load_layer(k3moe *h, int layer, const k3moe_layer_weights *w)
     // lives in device memory.
     const bool tiered = h->tier.slots > 0;
     const size_t dev_bytes = tiered ? z.dense : z.total;
-    size_t fr = 0, tot = 0;
-    if (cudaMemGetInfo(&fr, &tot) != cudaSuccess) return K3MOE_ERR_CUDA;
+    size_t fr = 0;
+    if (free_device_bytes(&fr) != cudaSuccess) return K3MOE_ERR_CUDA;
     if (dev_bytes + (256u << 20) > fr) return K3MOE_ERR_OOM;   // checked before any allocation
     void *blk = nullptr;
     if (cudaMalloc(&blk, dev_bytes) != cudaSuccess) {
@@ -864,8 +882,8 @@ int k3moe_set_expert_tier(k3moe *h, int slots)
                                                al256(E * sizeof(int2)) + al256(4) + al256(3 * 8) +
                                                al256((E + 1) * 4);
     bytes += tables;
-    size_t fr = 0, tot = 0;
-    if (cudaMemGetInfo(&fr, &tot) != cudaSuccess) return K3MOE_ERR_CUDA;
+    size_t fr = 0;
+    if (free_device_bytes(&fr) != cudaSuccess) return K3MOE_ERR_CUDA;
     if (bytes + (256u << 20) > fr) return K3MOE_ERR_OOM;
     if (cudaMalloc(&t.block, bytes) != cudaSuccess) {
         cudaGetLastError();

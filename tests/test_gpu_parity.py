@@ -239,6 +239,42 @@ def test_device_wait_timeout_is_reported_and_the_handle_stays_usable():
     assert_close(bf16_to_f64(y), oracle.layer_forward(shape, d, x))
 
 
+def test_oversized_requests_refused_before_allocating(monkeypatch):
+    """With the device-memory budget below what a request needs (its bytes
+    plus the margin), create and load return K3MOE_ERR_OOM with nothing
+    allocated: the handle stays as it was, the layer stays unloaded, and the
+    same load goes through once the budget is lifted."""
+    import mxfp4_routed_expert_gb300 as km
+    shape = k3synth.TINY
+    d = k3synth.make_layer(shape, 8, 0, k3synth.TINY_RECIPE)
+    x, _ = guarded_tokens(shape, d, 8, 4)
+    monkeypatch.setenv("K3MOE_DEVICE_BUDGET_MB", "1")       # below the workspace margin
+    with pytest.raises(km.K3MoEError) as ei:
+        Layer(shape, [None], max_tokens=4)
+    assert ei.value.code == km.K3MOE_ERR_OOM
+    monkeypatch.setenv("K3MOE_DEVICE_BUDGET_MB", "128")     # the workspace fits, a layer does not
+    lay = Layer(shape, [None], max_tokens=4)
+    try:
+        with pytest.raises(km.K3MoEError) as ei:
+            lay.load(0, d)
+        assert ei.value.code == km.K3MOE_ERR_OOM
+        with pytest.raises(km.K3MoEError) as ei:
+            km.k3moe_set_expert_tier(lay.h, shape.n_experts)
+        assert ei.value.code == km.K3MOE_ERR_OOM
+        assert km.k3moe_get_tier_stats(lay.h)["slots"] == 0
+        import torch
+        xd = torch.zeros((4, shape.hidden), dtype=torch.int16, device="cuda")
+        with pytest.raises(km.K3MoEError) as ei:
+            km.k3moe_forward(lay.h, 0, xd, torch.zeros_like(xd), 4)
+        assert ei.value.code == km.K3MOE_ERR_NOT_LOADED
+        monkeypatch.delenv("K3MOE_DEVICE_BUDGET_MB")
+        lay.load(0, d)
+        y = lay.forward(x)
+    finally:
+        lay.close()
+    assert_close(bf16_to_f64(y), oracle.layer_forward(shape, d, x))
+
+
 def test_forward_host_matches_device_forward():
     import mxfp4_routed_expert_gb300 as km
     shape = k3synth.TINY
