@@ -39,22 +39,26 @@ TD1, TD3, TD2 = 21, 22, 23
 MXFP4_GROUP = 32
 
 
-def build(force: bool = False) -> str:
-    """Compile libk3synth.so next to its source (atomic rename, so parallel
-    builders never see a half-written file)."""
-    if (not force and os.path.exists(_LIB_PATH)
-            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
-        return _LIB_PATH
-    fd, tmp = tempfile.mkstemp(suffix=".so", dir=_HERE)
+def build(force: bool = False, out: str | None = None, flags=("-O2",)) -> str:
+    """Compile the generator to `out` (default: libk3synth.so next to its
+    source; atomic rename, so parallel builders never see a half-written file).
+    K3SYNTH_LIB names an already built library to load instead."""
+    if out is None and os.environ.get("K3SYNTH_LIB"):
+        return os.environ["K3SYNTH_LIB"]
+    out = out or _LIB_PATH
+    if (not force and os.path.exists(out)
+            and os.path.getmtime(out) >= os.path.getmtime(_SRC)):
+        return out
+    fd, tmp = tempfile.mkstemp(suffix=".so", dir=os.path.dirname(out))
     os.close(fd)
     try:
-        subprocess.check_call(["gcc", "-std=c99", "-O2", "-fPIC", "-shared", "-fopenmp",
+        subprocess.check_call(["gcc", *flags, "-std=c99", "-fPIC", "-shared", "-fopenmp",
                                "-ffp-contract=off", _SRC, "-o", tmp])
-        os.replace(tmp, _LIB_PATH)
+        os.replace(tmp, out)
     finally:
         if os.path.exists(tmp):
             os.unlink(tmp)
-    return _LIB_PATH
+    return out
 
 
 def _L():

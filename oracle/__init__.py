@@ -23,20 +23,31 @@ _LIB_PATH = os.path.join(_HERE, "liboracle.so")
 _lib = None
 
 
-def build(force: bool = False) -> str:
-    if (not force and os.path.exists(_LIB_PATH)
-            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
-        return _LIB_PATH
-    fd, tmp = tempfile.mkstemp(suffix=".so", dir=_HERE)
+_FLAGS = ["-std=c99", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off", "-fno-fast-math"]
+# an instrumented build of the same source: address and undefined-behaviour
+# sanitizers, stopping at the first finding
+SANITIZE_FLAGS = ["-O1", "-g", "-fno-omit-frame-pointer", "-fsanitize=address,undefined",
+                  "-fno-sanitize-recover=all"]
+
+
+def build(force: bool = False, out: str | None = None, flags=("-O2",)) -> str:
+    """Compiles the oracle to `out` (default: liboracle.so beside the source).
+    K3MOE_ORACLE_LIB names an already built library to load instead."""
+    if out is None and os.environ.get("K3MOE_ORACLE_LIB"):
+        return os.environ["K3MOE_ORACLE_LIB"]
+    out = out or _LIB_PATH
+    if (not force and os.path.exists(out)
+            and os.path.getmtime(out) >= os.path.getmtime(_SRC)):
+        return out
+    fd, tmp = tempfile.mkstemp(suffix=".so", dir=os.path.dirname(out))
     os.close(fd)
     try:
-        subprocess.check_call(["gcc", "-std=c99", "-O2", "-fPIC", "-shared", "-fopenmp",
-                               "-ffp-contract=off", "-fno-fast-math", _SRC, "-o", tmp, "-lm"])
-        os.replace(tmp, _LIB_PATH)
+        subprocess.check_call(["gcc", *flags, *_FLAGS, _SRC, "-o", tmp, "-lm"])
+        os.replace(tmp, out)
     finally:
         if os.path.exists(tmp):
             os.unlink(tmp)
-    return _LIB_PATH
+    return out
 
 
 class _Cfg(ctypes.Structure):
