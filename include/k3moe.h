@@ -67,7 +67,8 @@ enum {
     K3MOE_ERR_NOT_LOADED = -6,    /* forward on a layer that was never loaded */
     K3MOE_ERR_CUDA = -7,          /* a CUDA runtime call failed */
     K3MOE_ERR_TIMEOUT = -8,       /* a device-side bounded wait gave up */
-    K3MOE_ERR_DEVICE = -9         /* a device-side index check failed */
+    K3MOE_ERR_DEVICE = -9,        /* a device-side index check failed */
+    K3MOE_ERR_GUARD = -10         /* a guard band after a library buffer was overwritten */
 };
 
 /* Where the pointees of a k3moe_layer_weights live. */
@@ -214,7 +215,11 @@ enum { K3MOE_T_Z = 1, K3MOE_T_ACC = 2, K3MOE_T_SHARED = 3, K3MOE_T_LOGITS = 4, K
 K3MOE_API int k3moe_get_intermediate(k3moe *h, int which, void *dst, size_t bytes, void *stream);
 
 /* Synchronises the device and returns (then clears) the first latched
- * device-side error, or the first asynchronous CUDA error. */
+ * device-side error, or the first asynchronous CUDA error. It then reads the
+ * guard bands (256 bytes of a fixed pattern after every workspace and tier
+ * buffer the kernels write): K3MOE_ERR_GUARD when one has changed, i.e. a
+ * kernel wrote past the end of a buffer (the handle should then be
+ * destroyed). */
 K3MOE_API int k3moe_sync_status(k3moe *h);
 
 /* Check of the device-side failure path (the README's engine reports a

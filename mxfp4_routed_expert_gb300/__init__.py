@@ -29,6 +29,7 @@ K3MOE_ERR_NOT_LOADED = -6
 K3MOE_ERR_CUDA = -7
 K3MOE_ERR_TIMEOUT = -8
 K3MOE_ERR_DEVICE = -9
+K3MOE_ERR_GUARD = -10
 K3MOE_HOST, K3MOE_DEVICE = 0, 1
 K3MOE_T_Z, K3MOE_T_ACC, K3MOE_T_SHARED, K3MOE_T_LOGITS, K3MOE_T_X = 1, 2, 3, 4, 5
 

@@ -53,22 +53,51 @@ int check_config(const k3moe_config *c)
 struct Carve {
     char *base;
     size_t off = 0;
+    std::vector<size_t> *guards = nullptr;   // non-null: a guard band after each buffer
     template <typename T>
     T *take(size_t count)
     {
         T *p = reinterpret_cast<T *>(base ? base + off : nullptr);
         off += al256(count * sizeof(T));
+        if (guards) {
+            if (base) guards->push_back(off);
+            off += kGuardBytes;
+        }
         return p;
     }
 };
+
+// Writes the guard pattern into every band.
+cudaError_t set_guards(void *block, const std::vector<size_t> &guards)
+{
+    for (size_t g : guards) {
+        const cudaError_t e = cudaMemset((char *)block + g, kGuardByte, kGuardBytes);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+// K3MOE_OK when every band still holds the pattern (device idle).
+int check_guards(const void *block, const std::vector<size_t> &guards)
+{
+    unsigned char band[kGuardBytes];
+    for (size_t g : guards) {
+        if (cudaMemcpy(band, (const char *)block + g, kGuardBytes, cudaMemcpyDeviceToHost) != cudaSuccess)
+            return K3MOE_ERR_CUDA;
+        for (size_t i = 0; i < kGuardBytes; i++)
+            if (band[i] != kGuardByte) return K3MOE_ERR_GUARD;
+    }
+    return K3MOE_OK;
+}
 
 // Lays out the workspace; with base == nullptr only measures it.
 size_t carve_workspace(const k3moe_config &c, char *base, Workspace *ws)
 {
     const size_t Tm = (size_t)c.max_tokens, E = c.n_experts, L = c.latent, S = c.shared_inter;
     const size_t H = c.hidden, K = c.topk, I = c.moe_inter;
-    Carve cv{base};
     Workspace w;
+    Carve cv{base};
+    cv.guards = &w.guards;
     w.logits = cv.take<float>(Tm * E);
     w.z = cv.take<float>(Tm * L);
     w.z16 = cv.take<__half>(Tm * (L + kZPad));
@@ -97,7 +126,7 @@ size_t carve_workspace(const k3moe_config &c, char *base, Workspace *ws)
     w.err = cv.take<int>(4);
     w.block = base;
     w.bytes = cv.off;
-    if (ws) *ws = w;
+    if (ws) *ws = std::move(w);
     return cv.off;
 }
 
@@ -388,6 +417,7 @@ const char *k3moe_strerror(int code)
     case K3MOE_ERR_CUDA: return "CUDA runtime error";
     case K3MOE_ERR_TIMEOUT: return "device-side wait timed out";
     case K3MOE_ERR_DEVICE: return "device-side index check failed";
+    case K3MOE_ERR_GUARD: return "guard band after a library buffer overwritten";
     default: return "unknown error";
     }
 }
@@ -435,7 +465,8 @@ int k3moe_create(const k3moe_config *cfg, k3moe **out)
         delete h;
         return K3MOE_ERR_CUDA;
     }
-    if (cudaMemset(blk, 0, need) != cudaSuccess || init_dense_kernels(*h) != cudaSuccess ||
+    if (cudaMemset(blk, 0, need) != cudaSuccess || set_guards(blk, h->ws.guards) != cudaSuccess ||
+        init_dense_kernels(*h) != cudaSuccess ||
         init_route_kernels(*cfg) != cudaSuccess || init_expert_kernels(*cfg) != cudaSuccess ||
         init_dense_tma(*cfg) != cudaSuccess || init_dense_gemm() != cudaSuccess ||
         init_expert_gemm() != cudaSuccess ||
@@ -843,7 +874,9 @@ int k3moe_sync_status(k3moe *h)
         return word[0] == kErrTimeout ? K3MOE_ERR_TIMEOUT : K3MOE_ERR_DEVICE;
     }
     if (cudaGetLastError() != cudaSuccess) return K3MOE_ERR_CUDA;
-    return K3MOE_OK;
+    int rc = check_guards(h->ws.block, h->ws.guards);
+    if (rc == K3MOE_OK && h->tier.block) rc = check_guards(h->tier.block, h->tier.guards);
+    return rc;
 }
 
 int k3moe_set_expert_path(k3moe *h, int mode)
@@ -868,20 +901,30 @@ int k3moe_set_expert_tier(k3moe *h, int slots)
     free_tier(h->tier);
     if (slots == 0) return K3MOE_OK;
     TierDev t;
-    const size_t I = c.moe_inter, L = c.latent;
+    const size_t I = c.moe_inter, L = c.latent, E = c.n_experts;
     const size_t piece[kTierPieces] = {I * (L / 2), I * (L / kGroup), I * (L / 2), I * (L / kGroup),
                                        L * (I / 2), L * (I / kGroup), I, I, L};
-    size_t bytes = 0;
     for (int p = 0; p < kTierPieces; p++) {
         if (piece[p] % 16) return K3MOE_ERR_SHAPE;   // the fill copies 16-byte words
         t.piece[p] = piece[p];
         t.expert_bytes += piece[p];
-        bytes += al256((size_t)slots * piece[p]);
     }
-    const size_t E = c.n_experts, tables = al256((size_t)c.max_layers * E * 4) + 2 * al256((size_t)slots * 4) +
-                                               al256(E * sizeof(int2)) + al256(4) + al256(3 * 8) +
-                                               al256((E + 1) * 4);
-    bytes += tables;
+    // the slot arrays, then the tables, each followed by a guard band; the
+    // first pass (no base) only measures
+    auto carve = [&](char *base) {
+        Carve cv{base};
+        cv.guards = &t.guards;
+        for (int p = 0; p < kTierPieces; p++) t.arr[p] = cv.take<uint8_t>((size_t)slots * piece[p]);
+        t.slot_of = cv.take<int>((size_t)c.max_layers * E);
+        t.slot_key = cv.take<int>((size_t)slots);
+        t.slot_used = cv.take<uint32_t>((size_t)slots);
+        t.fill = cv.take<int2>(E);
+        t.n_fill = cv.take<int>(1);
+        t.stats = cv.take<unsigned long long>(3);
+        t.all_ids = cv.take<int>(E + 1);
+        return cv.off;
+    };
+    const size_t bytes = carve(nullptr);
     size_t fr = 0;
     if (free_device_bytes(&fr) != cudaSuccess) return K3MOE_ERR_CUDA;
     if (bytes + (256u << 20) > fr) return K3MOE_ERR_OOM;
@@ -889,20 +932,12 @@ int k3moe_set_expert_tier(k3moe *h, int slots)
         cudaGetLastError();
         return K3MOE_ERR_OOM;
     }
-    Carve cv{(char *)t.block};
-    for (int p = 0; p < kTierPieces; p++) t.arr[p] = cv.take<uint8_t>((size_t)slots * piece[p]);
-    char *tab = (char *)t.block + cv.off;
-    t.slot_of = cv.take<int>((size_t)c.max_layers * E);
-    t.slot_key = cv.take<int>((size_t)slots);
-    t.slot_used = cv.take<uint32_t>((size_t)slots);
-    t.fill = cv.take<int2>(E);
-    t.n_fill = cv.take<int>(1);
-    t.stats = cv.take<unsigned long long>(3);
-    t.all_ids = cv.take<int>(E + 1);
-    // tables: every slot free (key -1, stamp 0), no expert resident
-    if (cudaMemset(tab, 0, tables) != cudaSuccess ||
+    carve((char *)t.block);
+    // every slot free (key -1, stamp 0), no expert resident, counters 0
+    if (cudaMemset(t.block, 0, bytes) != cudaSuccess ||
         cudaMemset(t.slot_of, 0xFF, (size_t)c.max_layers * E * 4) != cudaSuccess ||
-        cudaMemset(t.slot_key, 0xFF, (size_t)slots * 4) != cudaSuccess) {
+        cudaMemset(t.slot_key, 0xFF, (size_t)slots * 4) != cudaSuccess ||
+        set_guards(t.block, t.guards) != cudaSuccess) {
         cudaGetLastError();
         cudaFree(t.block);
         return K3MOE_ERR_CUDA;

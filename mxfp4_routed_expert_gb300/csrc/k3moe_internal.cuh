@@ -78,6 +78,11 @@ constexpr int kTierMaxSlots = 16384;
 // kTierRebaseKeep stamps keep their order (older ones tie at 1).
 constexpr uint32_t kTierRebaseAt = 0x80000000u;
 constexpr uint32_t kTierRebaseKeep = 1u << 24;
+// Every buffer the kernels write is followed by a band of kGuardBytes bytes
+// set to kGuardByte; k3moe_sync_status reports a changed band.
+constexpr size_t kGuardBytes = 256;
+constexpr unsigned char kGuardByte = 0xA5;
+
 struct TierDev {
     int slots = 0;
     void *block = nullptr;              // device: slot arrays, then the tables
@@ -91,6 +96,7 @@ struct TierDev {
     int *n_fill = nullptr;
     unsigned long long *stats = nullptr;   // hits, misses, bytes filled
     int *all_ids = nullptr;             // [E + 1]: 0 .. E-1, then E (a layer's list, for pinning)
+    std::vector<size_t> guards;         // guard bands after each array of the block
     uint32_t stamp = 0;                 // last stamp given to a forward
     uint32_t rebase_at = kTierRebaseAt;
     uint32_t rebase_keep = kTierRebaseKeep;
@@ -127,6 +133,7 @@ struct Workspace {
     __nv_bfloat16 *xbuf1 = nullptr;   // [Tm, H]
     __nv_bfloat16 *xn = nullptr;      // [Tm, H] layer input made from the residual (forward_residual)
     int *err = nullptr;           // [4] device error word + detail
+    std::vector<size_t> guards;   // byte offsets of the guard bands after each buffer
 };
 
 struct ProfRec {
