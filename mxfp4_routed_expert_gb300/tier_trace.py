@@ -15,10 +15,24 @@ the trace"). This module replays such a trace under
 
 A trace is a list of (layer, experts) pairs in forward order; it can be built
 from each forward's expert counts (`k3moe_get_routing`) with
-`trace_from_counts`.
+`trace_from_counts`, and stored with `save_trace` as JSON lines (one
+`[layer, [experts...]]` per forward) or as an `.npz` holding `layers` [n] and
+`counts` [n, E].
+
+Command line (the pages' "ask the trace" for a slot count):
+
+    python -m mxfp4_routed_expert_gb300.tier_trace TRACE --slots 896,1792,2688
+        [--expert-bytes 17561856] [--pin 0,1] [--json]
+
+prints, per slot count and policy, the hit rate, the misses, the compulsory
+misses and the bytes the misses copy; `--pin` pins whole layers (every expert
+of each listed layer seen in the trace) first.
 """
 from __future__ import annotations
 
+import argparse
+import json
+import sys
 from collections import defaultdict, deque
 
 import numpy as np
@@ -92,3 +106,69 @@ def replay(trace, slots: int, policy: str = "tier", expert_bytes: int = 0, pin=(
     return {"slots": slots, "policy": policy, "hits": hits, "misses": misses,
             "hit_rate": hits / total if total else 0.0, "compulsory": len(nxt),
             "bytes_copied": misses * int(expert_bytes), "pin_copies": len(pin_keys)}
+
+
+def save_trace(path: str, trace) -> None:
+    """Writes a trace as JSON lines, one [layer, [experts...]] per forward."""
+    with open(path, "w") as f:
+        for layer, ex in trace:
+            f.write(json.dumps([int(layer), [int(e) for e in ex]]) + "\n")
+
+
+def load_trace(path: str) -> list:
+    """Reads a trace written by `save_trace`, or an .npz of `layers` [n] and
+    per-forward expert `counts` [n, E]."""
+    if path.endswith(".npz"):
+        z = np.load(path)
+        layers, counts = np.asarray(z["layers"]), np.asarray(z["counts"])
+        if counts.ndim != 2 or layers.shape != (counts.shape[0],):
+            raise ValueError("an .npz trace holds layers [n] and counts [n, E]")
+        return [trace_from_counts(l, c) for l, c in zip(layers, counts)]
+    out = []
+    with open(path) as f:
+        for i, line in enumerate(f):
+            if not line.strip():
+                continue
+            rec = json.loads(line)
+            if (not isinstance(rec, list) or len(rec) != 2 or not isinstance(rec[1], list)):
+                raise ValueError(f"line {i + 1}: expected [layer, [experts...]]")
+            out.append((int(rec[0]), tuple(int(e) for e in rec[1])))
+    return out
+
+
+def main(argv=None) -> int:
+    ap = argparse.ArgumentParser(prog="python -m mxfp4_routed_expert_gb300.tier_trace",
+                                 description="Replay a routing trace at several expert-tier sizes.")
+    ap.add_argument("trace", help="JSON lines of [layer, [experts]] or an .npz of layers, counts")
+    ap.add_argument("--slots", required=True, help="comma-separated slot counts")
+    ap.add_argument("--expert-bytes", type=int, default=0, help="bytes of one expert (copied per miss)")
+    ap.add_argument("--pin", default="", help="comma-separated layers to pin before the trace")
+    ap.add_argument("--json", action="store_true", help="one JSON object per line instead of a table")
+    a = ap.parse_args(argv)
+    trace = load_trace(a.trace)
+    slots = [int(v) for v in a.slots.split(",") if v.strip()]
+    pin_layers = {int(v) for v in a.pin.split(",") if v.strip()}
+    seen = defaultdict(set)
+    for layer, ex in trace:
+        seen[layer].update(ex)
+    pin = [(l, sorted(seen[l])) for l in sorted(pin_layers)]
+    rows = []
+    for n in slots:
+        for policy in ("tier", "belady"):
+            try:
+                rows.append(replay(trace, n, policy, expert_bytes=a.expert_bytes, pin=pin))
+            except ValueError as e:
+                rows.append({"slots": n, "policy": policy, "error": str(e)})
+    for r in rows:
+        if a.json:
+            print(json.dumps(r))
+        elif "error" in r:
+            print(f"{r['slots']:>7} {r['policy']:>7}  {r['error']}")
+        else:
+            print(f"{r['slots']:>7} {r['policy']:>7}  hit rate {r['hit_rate']:.4f}  misses {r['misses']}"
+                  f"  compulsory {r['compulsory']}  copied {r['bytes_copied'] / 1e9:.3f} GB")
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

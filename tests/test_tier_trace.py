@@ -69,3 +69,43 @@ def test_pins_must_leave_room():
     with pytest.raises(ValueError):
         replay([(1, range(8))], 12, "tier", pin=[(0, range(8))])
 
+
+
+def test_trace_files_and_command_line(tmp_path, capsys):
+    """A trace saved as JSON lines or recorded as per-forward counts in an
+    .npz reads back unchanged, and the command line prints the replay of
+    both policies per slot count (pins included)."""
+    import json
+    from mxfp4_routed_expert_gb300 import tier_trace as tt
+    tr = [(l, tuple(sorted(ex))) for l, ex in random_trace(7, n_fwd=30, layers=2, E=24, per=5)]
+    p = tmp_path / "t.jsonl"
+    tt.save_trace(str(p), tr)
+    assert tt.load_trace(str(p)) == tr
+    counts = np.zeros((len(tr), 24), np.int32)
+    for i, (_, ex) in enumerate(tr):
+        counts[i, list(ex)] = 3
+    q = tmp_path / "t.npz"
+    np.savez(q, layers=np.array([l for l, _ in tr]), counts=counts)
+    assert tt.load_trace(str(q)) == tr
+    assert tt.main([str(p), "--slots", "8,24", "--expert-bytes", "10", "--json"]) == 0
+    rows = [json.loads(line) for line in capsys.readouterr().out.splitlines()]
+    assert [(r["slots"], r["policy"]) for r in rows] == [(8, "tier"), (8, "belady"), (24, "tier"),
+                                                         (24, "belady")]
+    for r in rows:
+        ref = replay(tr, r["slots"], r["policy"], expert_bytes=10)
+        assert (r["hits"], r["misses"], r["bytes_copied"]) == (ref["hits"], ref["misses"],
+                                                               ref["bytes_copied"])
+    # pinning layer 0 (all of its experts seen in the trace) on 48 slots: its
+    # forwards never miss, so every miss is one of layer 1's
+    assert tt.main([str(p), "--slots", "48", "--pin", "0", "--json"]) == 0
+    r = json.loads(capsys.readouterr().out.splitlines()[0])
+    seen0 = {e for l, ex in tr if l == 0 for e in ex}
+    assert r["pin_copies"] == len(seen0)
+    assert r["misses"] == len({e for l, ex in tr if l == 1 for e in ex})
+    # too few slots for one forward: reported on its row, not raised
+    assert tt.main([str(p), "--slots", "3"]) == 0
+    assert "more experts than there are slots" in capsys.readouterr().out
+    bad = tmp_path / "bad.jsonl"
+    bad.write_text('{"layer": 0}\n')
+    with pytest.raises(ValueError):
+        tt.load_trace(str(bad))
