@@ -383,6 +383,7 @@ def omp_threads(n_rows):
 def run_native(args, rank, world):
     import torch
     import mxfp4_routed_expert_gb300 as km
+    from mxfp4_routed_expert_gb300 import tier_trace
     from mxfp4_routed_expert_gb300 import build as kbuild
     kbuild.build()
     dev = int(os.environ.get("LOCAL_RANK", 0))
@@ -487,6 +488,10 @@ def run_native(args, rank, world):
     ms_per_step = total_ms / args.steps
     value = whole_job_rate(world, T, args.steps, total_ms / 1e3)
 
+    if args.dump_trace and rank == 0:
+        # one forward per step: its layer (a chain exposes its last layer's routing)
+        step_layer = [(args.warmup + i) % n_layers if alternate else n_layers - 1 for i in range(args.steps)]
+        tier_trace.save_counts(args.dump_trace, step_layer, counts_log.cpu().numpy())
     touched = (counts_log.cpu().numpy() > 0).sum(1)
     n_touched = float(touched.mean())
     hbm_peak, bf16_peak, bf16_sust, peak_src = measured_peaks()
@@ -661,6 +666,9 @@ def main():
                     help="routed-expert kernels: auto (grouped GEMM from T >= 16), per-pair GEMVs, or GEMM")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--dump-trace", default="",
+                    help="write each timed step's layer and expert counts to this .npz (a routing trace "
+                         "for python -m mxfp4_routed_expert_gb300.tier_trace)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

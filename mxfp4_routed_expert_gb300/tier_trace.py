@@ -16,8 +16,8 @@ the trace"). This module replays such a trace under
 A trace is a list of (layer, experts) pairs in forward order; it can be built
 from each forward's expert counts (`k3moe_get_routing`) with
 `trace_from_counts`, and stored with `save_trace` as JSON lines (one
-`[layer, [experts...]]` per forward) or as an `.npz` holding `layers` [n] and
-`counts` [n, E].
+`[layer, [experts...]]` per forward) or, with `save_counts`, as an .npz
+archive of `layers` [n] and `counts` [n, E] (`bench.py --dump-trace`).
 
 Command line (the pages' "ask the trace" for a slot count):
 
@@ -115,10 +115,22 @@ def save_trace(path: str, trace) -> None:
             f.write(json.dumps([int(layer), [int(e) for e in ex]]) + "\n")
 
 
+def save_counts(path: str, layers, counts) -> None:
+    """Writes per-forward expert counts (as `k3moe_get_routing` returns them)
+    and each forward's layer as an .npz trace."""
+    layers, counts = np.asarray(layers, np.int32), np.asarray(counts, np.int32)
+    if counts.ndim != 2 or layers.shape != (counts.shape[0],):
+        raise ValueError("layers [n] and counts [n, E] expected")
+    with open(path, "wb") as f:   # a file object: np.savez adds no suffix
+        np.savez(f, layers=layers, counts=counts)
+
+
 def load_trace(path: str) -> list:
     """Reads a trace written by `save_trace`, or an .npz of `layers` [n] and
     per-forward expert `counts` [n, E]."""
-    if path.endswith(".npz"):
+    with open(path, "rb") as f:
+        is_npz = f.read(2) == b"PK"   # a zip archive
+    if is_npz:
         z = np.load(path)
         layers, counts = np.asarray(z["layers"]), np.asarray(z["counts"])
         if counts.ndim != 2 or layers.shape != (counts.shape[0],):

@@ -87,6 +87,11 @@ def test_trace_files_and_command_line(tmp_path, capsys):
     q = tmp_path / "t.npz"
     np.savez(q, layers=np.array([l for l, _ in tr]), counts=counts)
     assert tt.load_trace(str(q)) == tr
+    q2 = tmp_path / "trace.bin"                    # any name: the reader looks at the bytes
+    tt.save_counts(str(q2), [l for l, _ in tr], counts)
+    assert tt.load_trace(str(q2)) == tr
+    with pytest.raises(ValueError):
+        tt.save_counts(str(q2), [0, 1], counts)
     assert tt.main([str(p), "--slots", "8,24", "--expert-bytes", "10", "--json"]) == 0
     rows = [json.loads(line) for line in capsys.readouterr().out.splitlines()]
     assert [(r["slots"], r["policy"]) for r in rows] == [(8, "tier"), (8, "belady"), (24, "tier"),
