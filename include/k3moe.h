@@ -27,7 +27,8 @@
  * All entry points return 0 (K3MOE_OK) or a negative K3MOE_ERR_* code.
  * Errors found on the host are returned immediately. Errors found by a kernel
  * (an index out of range, a bounded wait that ran out) are latched in a device
- * word and returned by k3moe_sync_status.
+ * word and returned by k3moe_sync_status, which also reports an overwritten
+ * guard band (a write past the end of a library buffer).
  *
  * Device memory: k3moe_create, k3moe_load_layer and k3moe_set_expert_tier
  * check what they need (plus a margin: 64 MB for the workspace, 256 MB for a
