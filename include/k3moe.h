@@ -83,7 +83,7 @@ typedef struct k3moe k3moe;
  * Supported sizes (else K3MOE_ERR_SHAPE): hidden, latent, moe_inter and
  * shared_inter multiples of 64; latent and moe_inter at most 4096;
  * 1 <= topk <= 32; topk <= n_experts <= 1024; max_tokens <= 65536 / topk;
- * situ_b1 * situ_b2 <= 512.
+ * max_layers <= 1024 (the model has 93); situ_b1 * situ_b2 <= 512.
  * K3: hidden 7168, latent 3584, n_experts 896, topk 16, moe_inter 3072,
  * shared_inter 6144 (two shared experts fused), rms_eps 1e-5, situ_b1 4,
  * situ_b2 25, routed_scale 1, renorm 1, latent_norm 1.

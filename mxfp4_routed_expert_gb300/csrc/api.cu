@@ -7,6 +7,7 @@
 #include <cstdint>
 #include <cstring>
 #include <new>
+#include <utility>
 #include <string>
 
 #include "k3moe_internal.cuh"
@@ -42,6 +43,7 @@ int check_config(const k3moe_config *c)
     if (c->latent > 4096 || c->moe_inter > 4096) return K3MOE_ERR_SHAPE;
     if (!expert_smem_fits(*c)) return K3MOE_ERR_SHAPE;
     if ((long long)c->max_tokens * c->topk > 65536) return K3MOE_ERR_SHAPE;
+    if (c->max_layers > kMaxLayers) return K3MOE_ERR_SHAPE;
     // fp16 partial sums in the expert GEMVs: |SiTU| <= b1*b2 must stay small
     if ((double)c->situ_b1 * c->situ_b2 > 512.0) return K3MOE_ERR_SHAPE;
     // the dense layer runs decode batches through the TMA-fed kernels, two
@@ -374,6 +376,19 @@ cudaError_t free_device_bytes(size_t *fr)
     return cudaSuccess;
 }
 
+// The error code for a C++ exception caught at an entry point: host memory
+// ran out (std::bad_alloc), or anything else the runtime's C++ layer threw.
+int abi_exception()
+{
+    try {
+        throw;
+    } catch (const std::bad_alloc &) {
+        return K3MOE_ERR_OOM;
+    } catch (...) {
+        return K3MOE_ERR_CUDA;
+    }
+}
+
 bool overlap(const void *a, size_t na, const void *b, size_t nb)
 {
     const char *pa = (const char *)a, *pb = (const char *)b;
@@ -451,7 +466,13 @@ int k3moe_create(const k3moe_config *cfg, k3moe **out)
         delete h;
         return K3MOE_ERR_OOM;
     }
-    carve_workspace(*cfg, (char *)blk, &h->ws);
+    try {
+        carve_workspace(*cfg, (char *)blk, &h->ws);
+    } catch (const std::bad_alloc &) {   // no C++ exception crosses the C ABI
+        cudaFree(blk);
+        delete h;
+        return K3MOE_ERR_OOM;
+    }
     int prio_lo = 0, prio_hi = 0;
     cudaDeviceGetStreamPriorityRange(&prio_lo, &prio_hi);
     if (cudaStreamCreateWithPriority(&h->side, cudaStreamNonBlocking, prio_lo) != cudaSuccess ||
@@ -486,7 +507,12 @@ int k3moe_create(const k3moe_config *cfg, k3moe **out)
                                 : (cfg->n_experts >= 128 && cfg->latent >= 128 && cfg->shared_inter >= 128 &&
                                    cfg->hidden >= 128);
     h->egemm_ok = expert_gemm_ok(*cfg);
-    h->layers.resize((size_t)cfg->max_layers);
+    try {
+        h->layers.resize((size_t)cfg->max_layers);
+    } catch (const std::bad_alloc &) {   // no C++ exception crosses the C ABI
+        k3moe_destroy(h);
+        return K3MOE_ERR_OOM;
+    }
     *out = h;
     return K3MOE_OK;
 }
@@ -514,186 +540,194 @@ void k3moe_destroy(k3moe *h)
 
 int k3moe_load_layer(k3moe *h, int layer, const k3moe_layer_weights *w)
 {
-    if (!h || !w) return K3MOE_ERR_INVALID_ARG;
-    if (w->struct_size != sizeof(k3moe_layer_weights)) return K3MOE_ERR_INVALID_ARG;
-    if (layer < 0 || layer >= h->cfg.max_layers) return K3MOE_ERR_INVALID_ARG;
-    if (w->where != K3MOE_HOST && w->where != K3MOE_DEVICE) return K3MOE_ERR_INVALID_ARG;
-    const k3moe_config &c = h->cfg;
-    const bool dense = is_dense(c);   // only the three feed-forward matrices
-    if (!w->shared_w1 || !w->shared_w3 || !w->shared_w2) return K3MOE_ERR_INVALID_ARG;
-    if (!dense && (!w->router_w || !w->down_w || !w->up_w || !w->w1_packed || !w->w1_scale ||
-                   !w->w3_packed || !w->w3_scale || !w->w2_packed || !w->w2_scale))
-        return K3MOE_ERR_INVALID_ARG;
-    if (!dense && c.latent_norm && !w->latent_gain) return K3MOE_ERR_INVALID_ARG;
-    for (int e = 0; e < c.n_experts; e++)
-        if (!w->w1_packed[e] || !w->w1_scale[e] || !w->w3_packed[e] || !w->w3_scale[e] ||
-            !w->w2_packed[e] || !w->w2_scale[e])
+    try {
+        if (!h || !w) return K3MOE_ERR_INVALID_ARG;
+        if (w->struct_size != sizeof(k3moe_layer_weights)) return K3MOE_ERR_INVALID_ARG;
+        if (layer < 0 || layer >= h->cfg.max_layers) return K3MOE_ERR_INVALID_ARG;
+        if (w->where != K3MOE_HOST && w->where != K3MOE_DEVICE) return K3MOE_ERR_INVALID_ARG;
+        const k3moe_config &c = h->cfg;
+        const bool dense = is_dense(c);   // only the three feed-forward matrices
+        if (!w->shared_w1 || !w->shared_w3 || !w->shared_w2) return K3MOE_ERR_INVALID_ARG;
+        if (!dense && (!w->router_w || !w->down_w || !w->up_w || !w->w1_packed || !w->w1_scale ||
+                       !w->w3_packed || !w->w3_scale || !w->w2_packed || !w->w2_scale))
             return K3MOE_ERR_INVALID_ARG;
-    if (cudaSetDevice(c.device) != cudaSuccess) return K3MOE_ERR_CUDA;
+        if (!dense && c.latent_norm && !w->latent_gain) return K3MOE_ERR_INVALID_ARG;
+        for (int e = 0; e < c.n_experts; e++)
+            if (!w->w1_packed[e] || !w->w1_scale[e] || !w->w3_packed[e] || !w->w3_scale[e] ||
+                !w->w2_packed[e] || !w->w2_scale[e])
+                return K3MOE_ERR_INVALID_ARG;
+        if (cudaSetDevice(c.device) != cudaSuccess) return K3MOE_ERR_CUDA;
 
-    const LayerSizes z = layer_sizes(c);
-    // Expert tier: the routed experts go to one pinned, device-mapped host
-    // block and reach the device through the slots; else all of the layer
-    // lives in device memory.
-    const bool tiered = h->tier.slots > 0;
-    const size_t dev_bytes = tiered ? z.dense : z.total;
-    size_t fr = 0;
-    if (free_device_bytes(&fr) != cudaSuccess) return K3MOE_ERR_CUDA;
-    if (dev_bytes + (256u << 20) > fr) return K3MOE_ERR_OOM;   // checked before any allocation
-    void *blk = nullptr;
-    if (cudaMalloc(&blk, dev_bytes) != cudaSuccess) {
-        cudaGetLastError();
-        return K3MOE_ERR_OOM;
-    }
-    void *hblk = nullptr, *hdev = nullptr;
-    if (tiered) {
-        if (cudaHostAlloc(&hblk, z.experts, cudaHostAllocMapped) != cudaSuccess) {
+        const LayerSizes z = layer_sizes(c);
+        // Expert tier: the routed experts go to one pinned, device-mapped host
+        // block and reach the device through the slots; else all of the layer
+        // lives in device memory.
+        const bool tiered = h->tier.slots > 0;
+        const size_t dev_bytes = tiered ? z.dense : z.total;
+        size_t fr = 0;
+        if (free_device_bytes(&fr) != cudaSuccess) return K3MOE_ERR_CUDA;
+        if (dev_bytes + (256u << 20) > fr) return K3MOE_ERR_OOM;   // checked before any allocation
+        void *blk = nullptr;
+        if (cudaMalloc(&blk, dev_bytes) != cudaSuccess) {
             cudaGetLastError();
-            cudaFree(blk);
             return K3MOE_ERR_OOM;
         }
-        if (cudaHostGetDevicePointer(&hdev, hblk, 0) != cudaSuccess) {
-            cudaGetLastError();
-            cudaFreeHost(hblk);
-            cudaFree(blk);
-            return K3MOE_ERR_CUDA;
+        void *hblk = nullptr, *hdev = nullptr;
+        if (tiered) {
+            if (cudaHostAlloc(&hblk, z.experts, cudaHostAllocMapped) != cudaSuccess) {
+                cudaGetLastError();
+                cudaFree(blk);
+                return K3MOE_ERR_OOM;
+            }
+            if (cudaHostGetDevicePointer(&hdev, hblk, 0) != cudaSuccess) {
+                cudaGetLastError();
+                cudaFreeHost(hblk);
+                cudaFree(blk);
+                return K3MOE_ERR_CUDA;
+            }
         }
-    }
-    LayerDev L;
-    L.block = blk;
-    L.bytes = dev_bytes;
-    L.index = layer;
-    Carve cv{(char *)blk};
-    __nv_bfloat16 *router = cv.take<__nv_bfloat16>(z.router / 2);
-    float *bias = cv.take<float>(z.bias / 4);
-    __nv_bfloat16 *down = cv.take<__nv_bfloat16>(z.down / 2);
-    __nv_bfloat16 *up = cv.take<__nv_bfloat16>(z.up / 2);
-    __nv_bfloat16 *gain = cv.take<__nv_bfloat16>(z.gain / 2);
-    __nv_bfloat16 *sh1 = cv.take<__nv_bfloat16>(z.sh13 / 2);
-    __nv_bfloat16 *sh3 = cv.take<__nv_bfloat16>(z.sh13 / 2);
-    __nv_bfloat16 *sh2 = cv.take<__nv_bfloat16>(z.sh2 / 2);
-    // the nine expert arrays [E][...]: after the dense tensors, or in the host
-    // block (ex: where the copies go; exd: the same arrays as kernels see them)
-    const size_t asz[kTierPieces] = {z.e13p, z.e13s, z.e13p, z.e13s, z.e2p, z.e2s, z.e13m, z.e13m, z.e2m};
-    uint8_t *ex[kTierPieces], *exd[kTierPieces];
-    {
-        Carve ce{tiered ? (char *)hblk : (char *)blk, tiered ? 0 : z.dense};
-        Carve cd{tiered ? (char *)hdev : (char *)blk, tiered ? 0 : z.dense};
-        for (int p = 0; p < kTierPieces; p++) {
-            ex[p] = ce.take<uint8_t>(asz[p]);
-            exd[p] = cd.take<uint8_t>(asz[p]);
+        LayerDev L;
+        L.block = blk;
+        L.bytes = dev_bytes;
+        L.index = layer;
+        Carve cv{(char *)blk};
+        __nv_bfloat16 *router = cv.take<__nv_bfloat16>(z.router / 2);
+        float *bias = cv.take<float>(z.bias / 4);
+        __nv_bfloat16 *down = cv.take<__nv_bfloat16>(z.down / 2);
+        __nv_bfloat16 *up = cv.take<__nv_bfloat16>(z.up / 2);
+        __nv_bfloat16 *gain = cv.take<__nv_bfloat16>(z.gain / 2);
+        __nv_bfloat16 *sh1 = cv.take<__nv_bfloat16>(z.sh13 / 2);
+        __nv_bfloat16 *sh3 = cv.take<__nv_bfloat16>(z.sh13 / 2);
+        __nv_bfloat16 *sh2 = cv.take<__nv_bfloat16>(z.sh2 / 2);
+        // the nine expert arrays [E][...]: after the dense tensors, or in the host
+        // block (ex: where the copies go; exd: the same arrays as kernels see them)
+        const size_t asz[kTierPieces] = {z.e13p, z.e13s, z.e13p, z.e13s, z.e2p, z.e2s, z.e13m, z.e13m, z.e2m};
+        uint8_t *ex[kTierPieces], *exd[kTierPieces];
+        {
+            Carve ce{tiered ? (char *)hblk : (char *)blk, tiered ? 0 : z.dense};
+            Carve cd{tiered ? (char *)hdev : (char *)blk, tiered ? 0 : z.dense};
+            for (int p = 0; p < kTierPieces; p++) {
+                ex[p] = ce.take<uint8_t>(asz[p]);
+                exd[p] = cd.take<uint8_t>(asz[p]);
+            }
         }
-    }
 
-    const cudaMemcpyKind kind =
-        w->where == K3MOE_HOST ? cudaMemcpyHostToDevice : cudaMemcpyDeviceToDevice;
-    // expert pieces: into device memory, or into the pinned host block
-    const cudaMemcpyKind ekind = tiered ? cudaMemcpyDefault : kind;
-    int rc = K3MOE_OK;
-    int *flag = h->ws.err + 2;   // scratch word for the scale scan
-#define K3_CP(dst, src, n, k)                                             \
-    if (rc == K3MOE_OK && cudaMemcpy((dst), (src), (n), (k)) != cudaSuccess) \
-        rc = K3MOE_ERR_CUDA;
-    if (!dense) K3_CP(router, w->router_w, z.router, kind);
-    if (w->router_bias && !dense) {
-        K3_CP(bias, w->router_bias, z.bias, kind);
-    } else if (rc == K3MOE_OK && cudaMemset(bias, 0, z.bias) != cudaSuccess) {
-        rc = K3MOE_ERR_CUDA;
-    }
-    if (!dense) {
-        K3_CP(down, w->down_w, z.down, kind);
-        K3_CP(up, w->up_w, z.up, kind);
-        if (w->latent_gain) K3_CP(gain, w->latent_gain, z.gain, kind);
-    }
-    K3_CP(sh1, w->shared_w1, z.sh13, kind);
-    K3_CP(sh3, w->shared_w3, z.sh13, kind);
-    K3_CP(sh2, w->shared_w2, z.sh2, kind);
-    const size_t pe13 = (size_t)c.moe_inter * (c.latent / 2), se13 = (size_t)c.moe_inter * (c.latent / kGroup);
-    const size_t pe2 = (size_t)c.latent * (c.moe_inter / 2), se2 = (size_t)c.latent * (c.moe_inter / kGroup);
-    for (int e = 0; e < c.n_experts && rc == K3MOE_OK; e++) {
-        K3_CP(ex[0] + e * pe13, w->w1_packed[e], pe13, ekind);
-        K3_CP(ex[1] + e * se13, w->w1_scale[e], se13, ekind);
-        K3_CP(ex[2] + e * pe13, w->w3_packed[e], pe13, ekind);
-        K3_CP(ex[3] + e * se13, w->w3_scale[e], se13, ekind);
-        K3_CP(ex[4] + e * pe2, w->w2_packed[e], pe2, ekind);
-        K3_CP(ex[5] + e * se2, w->w2_scale[e], se2, ekind);
-    }
-#undef K3_CP
-    if (rc == K3MOE_OK && !dense) {
-        // scale checks and row maxima read the arrays where they live (the
-        // host block through its device mapping in the tier)
-        int bad = 0;
-        if (cudaMemset(flag, 0, sizeof(int)) != cudaSuccess ||
-            launch_scale_scan(exd[1], z.e13s, flag, 0) != cudaSuccess ||
-            launch_scale_scan(exd[3], z.e13s, flag, 0) != cudaSuccess ||
-            launch_scale_scan(exd[5], z.e2s, flag, 0) != cudaSuccess ||
-            launch_row_scale_max(exd[1], z.e13m, c.latent / kGroup, exd[6]) != cudaSuccess ||
-            launch_row_scale_max(exd[3], z.e13m, c.latent / kGroup, exd[7]) != cudaSuccess ||
-            launch_row_scale_max(exd[5], z.e2m, c.moe_inter / kGroup, exd[8]) != cudaSuccess ||
-            cudaMemcpy(&bad, flag, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+        const cudaMemcpyKind kind =
+            w->where == K3MOE_HOST ? cudaMemcpyHostToDevice : cudaMemcpyDeviceToDevice;
+        // expert pieces: into device memory, or into the pinned host block
+        const cudaMemcpyKind ekind = tiered ? cudaMemcpyDefault : kind;
+        int rc = K3MOE_OK;
+        int *flag = h->ws.err + 2;   // scratch word for the scale scan
+    #define K3_CP(dst, src, n, k)                                             \
+        if (rc == K3MOE_OK && cudaMemcpy((dst), (src), (n), (k)) != cudaSuccess) \
             rc = K3MOE_ERR_CUDA;
-        else if (bad)
-            rc = K3MOE_ERR_BAD_SCALE;
-        cudaMemset(flag, 0, sizeof(int));
+        if (!dense) K3_CP(router, w->router_w, z.router, kind);
+        if (w->router_bias && !dense) {
+            K3_CP(bias, w->router_bias, z.bias, kind);
+        } else if (rc == K3MOE_OK && cudaMemset(bias, 0, z.bias) != cudaSuccess) {
+            rc = K3MOE_ERR_CUDA;
+        }
+        if (!dense) {
+            K3_CP(down, w->down_w, z.down, kind);
+            K3_CP(up, w->up_w, z.up, kind);
+            if (w->latent_gain) K3_CP(gain, w->latent_gain, z.gain, kind);
+        }
+        K3_CP(sh1, w->shared_w1, z.sh13, kind);
+        K3_CP(sh3, w->shared_w3, z.sh13, kind);
+        K3_CP(sh2, w->shared_w2, z.sh2, kind);
+        const size_t pe13 = (size_t)c.moe_inter * (c.latent / 2), se13 = (size_t)c.moe_inter * (c.latent / kGroup);
+        const size_t pe2 = (size_t)c.latent * (c.moe_inter / 2), se2 = (size_t)c.latent * (c.moe_inter / kGroup);
+        for (int e = 0; e < c.n_experts && rc == K3MOE_OK; e++) {
+            K3_CP(ex[0] + e * pe13, w->w1_packed[e], pe13, ekind);
+            K3_CP(ex[1] + e * se13, w->w1_scale[e], se13, ekind);
+            K3_CP(ex[2] + e * pe13, w->w3_packed[e], pe13, ekind);
+            K3_CP(ex[3] + e * se13, w->w3_scale[e], se13, ekind);
+            K3_CP(ex[4] + e * pe2, w->w2_packed[e], pe2, ekind);
+            K3_CP(ex[5] + e * se2, w->w2_scale[e], se2, ekind);
+        }
+    #undef K3_CP
+        if (rc == K3MOE_OK && !dense) {
+            // scale checks and row maxima read the arrays where they live (the
+            // host block through its device mapping in the tier)
+            int bad = 0;
+            if (cudaMemset(flag, 0, sizeof(int)) != cudaSuccess ||
+                launch_scale_scan(exd[1], z.e13s, flag, 0) != cudaSuccess ||
+                launch_scale_scan(exd[3], z.e13s, flag, 0) != cudaSuccess ||
+                launch_scale_scan(exd[5], z.e2s, flag, 0) != cudaSuccess ||
+                launch_row_scale_max(exd[1], z.e13m, c.latent / kGroup, exd[6]) != cudaSuccess ||
+                launch_row_scale_max(exd[3], z.e13m, c.latent / kGroup, exd[7]) != cudaSuccess ||
+                launch_row_scale_max(exd[5], z.e2m, c.moe_inter / kGroup, exd[8]) != cudaSuccess ||
+                cudaMemcpy(&bad, flag, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+                rc = K3MOE_ERR_CUDA;
+            else if (bad)
+                rc = K3MOE_ERR_BAD_SCALE;
+            cudaMemset(flag, 0, sizeof(int));
+        }
+        // a reloaded tiered layer gives up its slots before its old block goes
+        if (rc == K3MOE_OK && tiered && h->layers[(size_t)layer].loaded &&
+            (launch_tier_forget(*h, layer, 0) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess))
+            rc = K3MOE_ERR_CUDA;
+        if (rc == K3MOE_OK && tiered && h->layers[(size_t)layer].pinned)
+            h->tier.pinned -= c.n_experts;   // the forget freed its pinned slots
+        if (rc != K3MOE_OK) {
+            cudaFree(blk);
+            if (hblk) cudaFreeHost(hblk);
+            return rc;
+        }
+        L.router_w = router;
+        L.bias = bias;
+        L.down_w = down;
+        L.up_w = up;
+        L.gain = c.latent_norm ? gain : nullptr;
+        L.sh_w1 = sh1;
+        L.sh_w3 = sh3;
+        L.sh_w2 = sh2;
+        // expert arrays as the expert kernels address them: the handle's slots
+        // (tier) or the layer's own copy
+        const uint8_t *const *arr = tiered ? (const uint8_t *const *)h->tier.arr : (const uint8_t *const *)exd;
+        L.w1p = arr[0];
+        L.w1s = arr[1];
+        L.w3p = arr[2];
+        L.w3s = arr[3];
+        L.w2p = arr[4];
+        L.w2s = arr[5];
+        L.w1max = arr[6];
+        L.w3max = arr[7];
+        L.w2max = arr[8];
+        if (tiered) {
+            L.wslot = h->tier.slot_of + (size_t)layer * c.n_experts;
+            L.n_wslots = h->tier.slots;
+            L.host_block = hblk;
+            for (int p = 0; p < kTierPieces; p++) L.hsrc[p] = exd[p];
+        } else {
+            L.wslot = nullptr;
+            L.n_wslots = c.n_experts;
+        }
+        if (dense_tma_fits(c, 1)) build_dense_tma_maps(c, L);   // else the maps are never used
+        L.loaded = true;
+        free_layer(h->layers[(size_t)layer]);
+        h->layers[(size_t)layer] = L;
+        return K3MOE_OK;
+    } catch (...) {   // no C++ exception crosses the C ABI
+        return abi_exception();
     }
-    // a reloaded tiered layer gives up its slots before its old block goes
-    if (rc == K3MOE_OK && tiered && h->layers[(size_t)layer].loaded &&
-        (launch_tier_forget(*h, layer, 0) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess))
-        rc = K3MOE_ERR_CUDA;
-    if (rc == K3MOE_OK && tiered && h->layers[(size_t)layer].pinned)
-        h->tier.pinned -= c.n_experts;   // the forget freed its pinned slots
-    if (rc != K3MOE_OK) {
-        cudaFree(blk);
-        if (hblk) cudaFreeHost(hblk);
-        return rc;
-    }
-    L.router_w = router;
-    L.bias = bias;
-    L.down_w = down;
-    L.up_w = up;
-    L.gain = c.latent_norm ? gain : nullptr;
-    L.sh_w1 = sh1;
-    L.sh_w3 = sh3;
-    L.sh_w2 = sh2;
-    // expert arrays as the expert kernels address them: the handle's slots
-    // (tier) or the layer's own copy
-    const uint8_t *const *arr = tiered ? (const uint8_t *const *)h->tier.arr : (const uint8_t *const *)exd;
-    L.w1p = arr[0];
-    L.w1s = arr[1];
-    L.w3p = arr[2];
-    L.w3s = arr[3];
-    L.w2p = arr[4];
-    L.w2s = arr[5];
-    L.w1max = arr[6];
-    L.w3max = arr[7];
-    L.w2max = arr[8];
-    if (tiered) {
-        L.wslot = h->tier.slot_of + (size_t)layer * c.n_experts;
-        L.n_wslots = h->tier.slots;
-        L.host_block = hblk;
-        for (int p = 0; p < kTierPieces; p++) L.hsrc[p] = exd[p];
-    } else {
-        L.wslot = nullptr;
-        L.n_wslots = c.n_experts;
-    }
-    if (dense_tma_fits(c, 1)) build_dense_tma_maps(c, L);   // else the maps are never used
-    L.loaded = true;
-    free_layer(h->layers[(size_t)layer]);
-    h->layers[(size_t)layer] = L;
-    return K3MOE_OK;
 }
 
 int k3moe_forward(k3moe *h, int layer, const void *x, void *y, int T, void *stream)
 {
-    if (!h || !x || !y) return K3MOE_ERR_INVALID_ARG;
-    if (layer < 0 || layer >= h->cfg.max_layers) return K3MOE_ERR_INVALID_ARG;
-    if (T < 1 || T > h->cfg.max_tokens) return K3MOE_ERR_INVALID_ARG;
-    const size_t nb = (size_t)T * h->cfg.hidden * 2;
-    if (overlap(x, nb, y, nb) || misaligned(x) || misaligned(y)) return K3MOE_ERR_INVALID_ARG;
-    const LayerDev &w = h->layers[(size_t)layer];
-    if (!w.loaded) return K3MOE_ERR_NOT_LOADED;
-    if (cudaSetDevice(h->cfg.device) != cudaSuccess) return K3MOE_ERR_CUDA;
-    return run_layer(h, w, (const __nv_bfloat16 *)x, (__nv_bfloat16 *)y, T, (cudaStream_t)stream);
+    try {
+        if (!h || !x || !y) return K3MOE_ERR_INVALID_ARG;
+        if (layer < 0 || layer >= h->cfg.max_layers) return K3MOE_ERR_INVALID_ARG;
+        if (T < 1 || T > h->cfg.max_tokens) return K3MOE_ERR_INVALID_ARG;
+        const size_t nb = (size_t)T * h->cfg.hidden * 2;
+        if (overlap(x, nb, y, nb) || misaligned(x) || misaligned(y)) return K3MOE_ERR_INVALID_ARG;
+        const LayerDev &w = h->layers[(size_t)layer];
+        if (!w.loaded) return K3MOE_ERR_NOT_LOADED;
+        if (cudaSetDevice(h->cfg.device) != cudaSuccess) return K3MOE_ERR_CUDA;
+        return run_layer(h, w, (const __nv_bfloat16 *)x, (__nv_bfloat16 *)y, T, (cudaStream_t)stream);
+    } catch (...) {   // no C++ exception crosses the C ABI
+        return abi_exception();
+    }
 }
 
 int k3moe_load_post_norm(k3moe *h, int layer, const void *gain, int where)
@@ -723,82 +757,94 @@ int k3moe_load_post_norm(k3moe *h, int layer, const void *gain, int where)
 
 int k3moe_forward_residual(k3moe *h, int layer, const float *h_in, void *y, int T, void *stream)
 {
-    if (!h || !h_in || !y) return K3MOE_ERR_INVALID_ARG;
-    if (layer < 0 || layer >= h->cfg.max_layers) return K3MOE_ERR_INVALID_ARG;
-    if (T < 1 || T > h->cfg.max_tokens) return K3MOE_ERR_INVALID_ARG;
-    if (misaligned(h_in) || misaligned(y)) return K3MOE_ERR_INVALID_ARG;
-    if (overlap(h_in, (size_t)T * h->cfg.hidden * 4, y, (size_t)T * h->cfg.hidden * 2))
-        return K3MOE_ERR_INVALID_ARG;
-    const LayerDev &w = h->layers[(size_t)layer];
-    if (!w.loaded || !w.post_gain) return K3MOE_ERR_NOT_LOADED;
-    if (cudaSetDevice(h->cfg.device) != cudaSuccess) return K3MOE_ERR_CUDA;
-    return run_layer(h, w, nullptr, (__nv_bfloat16 *)y, T, (cudaStream_t)stream, h_in);
+    try {
+        if (!h || !h_in || !y) return K3MOE_ERR_INVALID_ARG;
+        if (layer < 0 || layer >= h->cfg.max_layers) return K3MOE_ERR_INVALID_ARG;
+        if (T < 1 || T > h->cfg.max_tokens) return K3MOE_ERR_INVALID_ARG;
+        if (misaligned(h_in) || misaligned(y)) return K3MOE_ERR_INVALID_ARG;
+        if (overlap(h_in, (size_t)T * h->cfg.hidden * 4, y, (size_t)T * h->cfg.hidden * 2))
+            return K3MOE_ERR_INVALID_ARG;
+        const LayerDev &w = h->layers[(size_t)layer];
+        if (!w.loaded || !w.post_gain) return K3MOE_ERR_NOT_LOADED;
+        if (cudaSetDevice(h->cfg.device) != cudaSuccess) return K3MOE_ERR_CUDA;
+        return run_layer(h, w, nullptr, (__nv_bfloat16 *)y, T, (cudaStream_t)stream, h_in);
+    } catch (...) {   // no C++ exception crosses the C ABI
+        return abi_exception();
+    }
 }
 
 int k3moe_forward_chain(k3moe *h, int first_layer, int n_layers, const void *x, void *y, int T,
                         void *stream)
 {
-    if (!h || !x || !y || n_layers < 1) return K3MOE_ERR_INVALID_ARG;
-    if (first_layer < 0 || first_layer + n_layers > h->cfg.max_layers) return K3MOE_ERR_INVALID_ARG;
-    if (T < 1 || T > h->cfg.max_tokens) return K3MOE_ERR_INVALID_ARG;
-    const size_t nb = (size_t)T * h->cfg.hidden * 2;
-    if (overlap(x, nb, y, nb) || misaligned(x) || misaligned(y)) return K3MOE_ERR_INVALID_ARG;
-    for (int l = first_layer; l < first_layer + n_layers; l++)
-        if (!h->layers[(size_t)l].loaded) return K3MOE_ERR_NOT_LOADED;
-    if (cudaSetDevice(h->cfg.device) != cudaSuccess) return K3MOE_ERR_CUDA;
-    cudaStream_t s = (cudaStream_t)stream;
-    const __nv_bfloat16 *cur = (const __nv_bfloat16 *)x;
-    for (int i = 0; i < n_layers; i++) {
-        const bool last = i == n_layers - 1;
-        __nv_bfloat16 *out = last ? (__nv_bfloat16 *)y : h->ws.xbuf0;
-        int rc = run_layer(h, h->layers[(size_t)(first_layer + i)], cur, out, T, s);
-        if (rc != K3MOE_OK) return rc;
-        if (!last) {
-            cudaError_t e;
-            {
-                Prof p(h, "chain_glue_rmsnorm", s);
-                e = launch_chain_glue(*h, h->ws.xbuf0, h->ws.xbuf1, T, s);
+    try {
+        if (!h || !x || !y || n_layers < 1) return K3MOE_ERR_INVALID_ARG;
+        if (first_layer < 0 || first_layer + n_layers > h->cfg.max_layers) return K3MOE_ERR_INVALID_ARG;
+        if (T < 1 || T > h->cfg.max_tokens) return K3MOE_ERR_INVALID_ARG;
+        const size_t nb = (size_t)T * h->cfg.hidden * 2;
+        if (overlap(x, nb, y, nb) || misaligned(x) || misaligned(y)) return K3MOE_ERR_INVALID_ARG;
+        for (int l = first_layer; l < first_layer + n_layers; l++)
+            if (!h->layers[(size_t)l].loaded) return K3MOE_ERR_NOT_LOADED;
+        if (cudaSetDevice(h->cfg.device) != cudaSuccess) return K3MOE_ERR_CUDA;
+        cudaStream_t s = (cudaStream_t)stream;
+        const __nv_bfloat16 *cur = (const __nv_bfloat16 *)x;
+        for (int i = 0; i < n_layers; i++) {
+            const bool last = i == n_layers - 1;
+            __nv_bfloat16 *out = last ? (__nv_bfloat16 *)y : h->ws.xbuf0;
+            int rc = run_layer(h, h->layers[(size_t)(first_layer + i)], cur, out, T, s);
+            if (rc != K3MOE_OK) return rc;
+            if (!last) {
+                cudaError_t e;
+                {
+                    Prof p(h, "chain_glue_rmsnorm", s);
+                    e = launch_chain_glue(*h, h->ws.xbuf0, h->ws.xbuf1, T, s);
+                }
+                if (e != cudaSuccess) return K3MOE_ERR_CUDA;
+                cur = h->ws.xbuf1;
             }
-            if (e != cudaSuccess) return K3MOE_ERR_CUDA;
-            cur = h->ws.xbuf1;
         }
+        return K3MOE_OK;
+    } catch (...) {   // no C++ exception crosses the C ABI
+        return abi_exception();
     }
-    return K3MOE_OK;
 }
 
 int k3moe_forward_host(k3moe *h, int layer, const void *x_host, void *y_host, int T, void *stream)
 {
-    if (!h || !x_host || !y_host) return K3MOE_ERR_INVALID_ARG;
-    if (layer < 0 || layer >= h->cfg.max_layers) return K3MOE_ERR_INVALID_ARG;
-    if (T < 1 || T > h->cfg.max_tokens) return K3MOE_ERR_INVALID_ARG;
-    if (!h->layers[(size_t)layer].loaded) return K3MOE_ERR_NOT_LOADED;
-    if (cudaSetDevice(h->cfg.device) != cudaSuccess) return K3MOE_ERR_CUDA;
-    cudaStream_t s = (cudaStream_t)stream;
-    const size_t nb = (size_t)T * h->cfg.hidden * 2;
-    // The layer's last kernel writes each output element once with a plain
-    // store: a pinned (device-mapped) y is written in place, saving the copy
-    // back. (x stays a copy: the first kernels read it from many CTAs.)
-    {
-        cudaPointerAttributes ay{};
-        if (cudaPointerGetAttributes(&ay, y_host) == cudaSuccess && ay.type == cudaMemoryTypeHost &&
-            ay.devicePointer && !misaligned(ay.devicePointer)) {
-            if (cudaMemcpyAsync(h->ws.xbuf0, x_host, nb, cudaMemcpyHostToDevice, s) != cudaSuccess)
-                return K3MOE_ERR_CUDA;
-            const int rc =
-                run_layer(h, h->layers[(size_t)layer], h->ws.xbuf0, (__nv_bfloat16 *)ay.devicePointer, T, s);
-            if (rc != K3MOE_OK) return rc;
-            return cudaStreamSynchronize(s) == cudaSuccess ? K3MOE_OK : K3MOE_ERR_CUDA;
+    try {
+        if (!h || !x_host || !y_host) return K3MOE_ERR_INVALID_ARG;
+        if (layer < 0 || layer >= h->cfg.max_layers) return K3MOE_ERR_INVALID_ARG;
+        if (T < 1 || T > h->cfg.max_tokens) return K3MOE_ERR_INVALID_ARG;
+        if (!h->layers[(size_t)layer].loaded) return K3MOE_ERR_NOT_LOADED;
+        if (cudaSetDevice(h->cfg.device) != cudaSuccess) return K3MOE_ERR_CUDA;
+        cudaStream_t s = (cudaStream_t)stream;
+        const size_t nb = (size_t)T * h->cfg.hidden * 2;
+        // The layer's last kernel writes each output element once with a plain
+        // store: a pinned (device-mapped) y is written in place, saving the copy
+        // back. (x stays a copy: the first kernels read it from many CTAs.)
+        {
+            cudaPointerAttributes ay{};
+            if (cudaPointerGetAttributes(&ay, y_host) == cudaSuccess && ay.type == cudaMemoryTypeHost &&
+                ay.devicePointer && !misaligned(ay.devicePointer)) {
+                if (cudaMemcpyAsync(h->ws.xbuf0, x_host, nb, cudaMemcpyHostToDevice, s) != cudaSuccess)
+                    return K3MOE_ERR_CUDA;
+                const int rc =
+                    run_layer(h, h->layers[(size_t)layer], h->ws.xbuf0, (__nv_bfloat16 *)ay.devicePointer, T, s);
+                if (rc != K3MOE_OK) return rc;
+                return cudaStreamSynchronize(s) == cudaSuccess ? K3MOE_OK : K3MOE_ERR_CUDA;
+            }
+            cudaGetLastError();   // pageable or unaligned y: the copy path below
         }
-        cudaGetLastError();   // pageable or unaligned y: the copy path below
+        if (cudaMemcpyAsync(h->ws.xbuf0, x_host, nb, cudaMemcpyHostToDevice, s) != cudaSuccess)
+            return K3MOE_ERR_CUDA;
+        int rc = run_layer(h, h->layers[(size_t)layer], h->ws.xbuf0, h->ws.xbuf1, T, s);
+        if (rc != K3MOE_OK) return rc;
+        if (cudaMemcpyAsync(y_host, h->ws.xbuf1, nb, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+            return K3MOE_ERR_CUDA;
+        if (cudaStreamSynchronize(s) != cudaSuccess) return K3MOE_ERR_CUDA;
+        return K3MOE_OK;
+    } catch (...) {   // no C++ exception crosses the C ABI
+        return abi_exception();
     }
-    if (cudaMemcpyAsync(h->ws.xbuf0, x_host, nb, cudaMemcpyHostToDevice, s) != cudaSuccess)
-        return K3MOE_ERR_CUDA;
-    int rc = run_layer(h, h->layers[(size_t)layer], h->ws.xbuf0, h->ws.xbuf1, T, s);
-    if (rc != K3MOE_OK) return rc;
-    if (cudaMemcpyAsync(y_host, h->ws.xbuf1, nb, cudaMemcpyDeviceToHost, s) != cudaSuccess)
-        return K3MOE_ERR_CUDA;
-    if (cudaStreamSynchronize(s) != cudaSuccess) return K3MOE_ERR_CUDA;
-    return K3MOE_OK;
 }
 
 int k3moe_get_routing(k3moe *h, int32_t *ids, float *w, int32_t *counts, int32_t *offsets,
@@ -891,101 +937,114 @@ int k3moe_set_expert_path(k3moe *h, int mode)
 
 int k3moe_set_expert_tier(k3moe *h, int slots)
 {
-    if (!h) return K3MOE_ERR_INVALID_ARG;
-    for (const auto &l : h->layers)
-        if (l.loaded) return K3MOE_ERR_INVALID_ARG;
-    const k3moe_config &c = h->cfg;
-    if (slots != 0 && (is_dense(c) || slots < c.n_experts || slots > kTierMaxSlots))
-        return K3MOE_ERR_INVALID_ARG;
-    if (cudaSetDevice(c.device) != cudaSuccess) return K3MOE_ERR_CUDA;
-    free_tier(h->tier);
-    if (slots == 0) return K3MOE_OK;
-    TierDev t;
-    const size_t I = c.moe_inter, L = c.latent, E = c.n_experts;
-    const size_t piece[kTierPieces] = {I * (L / 2), I * (L / kGroup), I * (L / 2), I * (L / kGroup),
-                                       L * (I / 2), L * (I / kGroup), I, I, L};
-    for (int p = 0; p < kTierPieces; p++) {
-        if (piece[p] % 16) return K3MOE_ERR_SHAPE;   // the fill copies 16-byte words
-        t.piece[p] = piece[p];
-        t.expert_bytes += piece[p];
-    }
-    // the slot arrays, then the tables, each followed by a guard band; the
-    // first pass (no base) only measures
-    auto carve = [&](char *base) {
-        Carve cv{base};
-        cv.guards = &t.guards;
-        for (int p = 0; p < kTierPieces; p++) t.arr[p] = cv.take<uint8_t>((size_t)slots * piece[p]);
-        t.slot_of = cv.take<int>((size_t)c.max_layers * E);
-        t.slot_key = cv.take<int>((size_t)slots);
-        t.slot_used = cv.take<uint32_t>((size_t)slots);
-        t.fill = cv.take<int2>(E);
-        t.n_fill = cv.take<int>(1);
-        t.stats = cv.take<unsigned long long>(3);
-        t.all_ids = cv.take<int>(E + 1);
-        return cv.off;
-    };
-    const size_t bytes = carve(nullptr);
-    size_t fr = 0;
-    if (free_device_bytes(&fr) != cudaSuccess) return K3MOE_ERR_CUDA;
-    if (bytes + (256u << 20) > fr) return K3MOE_ERR_OOM;
-    if (cudaMalloc(&t.block, bytes) != cudaSuccess) {
-        cudaGetLastError();
-        return K3MOE_ERR_OOM;
-    }
-    carve((char *)t.block);
-    // every slot free (key -1, stamp 0), no expert resident, counters 0
-    if (cudaMemset(t.block, 0, bytes) != cudaSuccess ||
-        cudaMemset(t.slot_of, 0xFF, (size_t)c.max_layers * E * 4) != cudaSuccess ||
-        cudaMemset(t.slot_key, 0xFF, (size_t)slots * 4) != cudaSuccess ||
-        set_guards(t.block, t.guards) != cudaSuccess) {
-        cudaGetLastError();
-        cudaFree(t.block);
-        return K3MOE_ERR_CUDA;
-    }
-    // K3MOE_TIER_REBASE="at,keep" moves the stamp rebase from its defaults
-    // (2^31, 2^24) to small counts, so that a short run goes through it
-    if (const char *env = std::getenv("K3MOE_TIER_REBASE")) {
-        unsigned long at = 0, keep = 0;
-        if (std::sscanf(env, "%lu,%lu", &at, &keep) != 2 || keep < 1 || keep >= at || at > kTierRebaseAt) {
-            cudaFree(t.block);
+    try {
+        if (!h) return K3MOE_ERR_INVALID_ARG;
+        for (const auto &l : h->layers)
+            if (l.loaded) return K3MOE_ERR_INVALID_ARG;
+        const k3moe_config &c = h->cfg;
+        if (slots != 0 && (is_dense(c) || slots < c.n_experts || slots > kTierMaxSlots))
             return K3MOE_ERR_INVALID_ARG;
-        }
-        t.rebase_at = (uint32_t)at;
-        t.rebase_keep = (uint32_t)keep;
-    }
-    t.slots = slots;
-    h->tier = t;
-    if (launch_tier_iota(*h) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
-        cudaGetLastError();
+        if (cudaSetDevice(c.device) != cudaSuccess) return K3MOE_ERR_CUDA;
         free_tier(h->tier);
-        return K3MOE_ERR_CUDA;
+        if (slots == 0) return K3MOE_OK;
+        TierDev t;
+        const size_t I = c.moe_inter, L = c.latent, E = c.n_experts;
+        const size_t piece[kTierPieces] = {I * (L / 2), I * (L / kGroup), I * (L / 2), I * (L / kGroup),
+                                           L * (I / 2), L * (I / kGroup), I, I, L};
+        for (int p = 0; p < kTierPieces; p++) {
+            if (piece[p] % 16) return K3MOE_ERR_SHAPE;   // the fill copies 16-byte words
+            t.piece[p] = piece[p];
+            t.expert_bytes += piece[p];
+        }
+        // the slot arrays, then the tables, each followed by a guard band; the
+        // first pass (no base) only measures
+        auto carve = [&](char *base) {
+            Carve cv{base};
+            cv.guards = &t.guards;
+            for (int p = 0; p < kTierPieces; p++) t.arr[p] = cv.take<uint8_t>((size_t)slots * piece[p]);
+            t.slot_of = cv.take<int>((size_t)c.max_layers * E);
+            t.slot_key = cv.take<int>((size_t)slots);
+            t.slot_used = cv.take<uint32_t>((size_t)slots);
+            t.fill = cv.take<int2>(E);
+            t.n_fill = cv.take<int>(1);
+            t.stats = cv.take<unsigned long long>(3);
+            t.all_ids = cv.take<int>(E + 1);
+            return cv.off;
+        };
+        const size_t bytes = carve(nullptr);
+        size_t fr = 0;
+        if (free_device_bytes(&fr) != cudaSuccess) return K3MOE_ERR_CUDA;
+        if (bytes + (256u << 20) > fr) return K3MOE_ERR_OOM;
+        if (cudaMalloc(&t.block, bytes) != cudaSuccess) {
+            cudaGetLastError();
+            return K3MOE_ERR_OOM;
+        }
+        try {
+            carve((char *)t.block);   // records the guard offsets (host memory)
+        } catch (const std::bad_alloc &) {
+            cudaFree(t.block);
+            return K3MOE_ERR_OOM;
+        }
+        // every slot free (key -1, stamp 0), no expert resident, counters 0
+        if (cudaMemset(t.block, 0, bytes) != cudaSuccess ||
+            cudaMemset(t.slot_of, 0xFF, (size_t)c.max_layers * E * 4) != cudaSuccess ||
+            cudaMemset(t.slot_key, 0xFF, (size_t)slots * 4) != cudaSuccess ||
+            set_guards(t.block, t.guards) != cudaSuccess) {
+            cudaGetLastError();
+            cudaFree(t.block);
+            return K3MOE_ERR_CUDA;
+        }
+        // K3MOE_TIER_REBASE="at,keep" moves the stamp rebase from its defaults
+        // (2^31, 2^24) to small counts, so that a short run goes through it
+        if (const char *env = std::getenv("K3MOE_TIER_REBASE")) {
+            unsigned long at = 0, keep = 0;
+            if (std::sscanf(env, "%lu,%lu", &at, &keep) != 2 || keep < 1 || keep >= at || at > kTierRebaseAt) {
+                cudaFree(t.block);
+                return K3MOE_ERR_INVALID_ARG;
+            }
+            t.rebase_at = (uint32_t)at;
+            t.rebase_keep = (uint32_t)keep;
+        }
+        t.slots = slots;
+        h->tier = std::move(t);
+        if (launch_tier_iota(*h) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+            cudaGetLastError();
+            free_tier(h->tier);
+            return K3MOE_ERR_CUDA;
+        }
+        return K3MOE_OK;
+    } catch (...) {   // no C++ exception crosses the C ABI
+        return abi_exception();
     }
-    return K3MOE_OK;
 }
 
 int k3moe_tier_pin_layer(k3moe *h, int layer)
 {
-    if (!h || layer < 0 || layer >= h->cfg.max_layers) return K3MOE_ERR_INVALID_ARG;
-    TierDev &t = h->tier;
-    const int E = h->cfg.n_experts;
-    if (t.slots == 0) return K3MOE_ERR_INVALID_ARG;
-    LayerDev &w = h->layers[(size_t)layer];
-    if (!w.loaded) return K3MOE_ERR_NOT_LOADED;
-    if (w.pinned) return K3MOE_OK;
-    // every forward of an unpinned layer must still find E free-able slots
-    if (t.slots - t.pinned - E < E) return K3MOE_ERR_INVALID_ARG;
-    if (cudaSetDevice(h->cfg.device) != cudaSuccess) return K3MOE_ERR_CUDA;
-    if (launch_tier_plan(*h, layer, 0, true) != cudaSuccess || launch_tier_fill(*h, w, 0) != cudaSuccess ||
-        cudaDeviceSynchronize() != cudaSuccess) {
-        cudaGetLastError();
-        return K3MOE_ERR_CUDA;
+    try {
+        if (!h || layer < 0 || layer >= h->cfg.max_layers) return K3MOE_ERR_INVALID_ARG;
+        TierDev &t = h->tier;
+        const int E = h->cfg.n_experts;
+        if (t.slots == 0) return K3MOE_ERR_INVALID_ARG;
+        LayerDev &w = h->layers[(size_t)layer];
+        if (!w.loaded) return K3MOE_ERR_NOT_LOADED;
+        if (w.pinned) return K3MOE_OK;
+        // every forward of an unpinned layer must still find E free-able slots
+        if (t.slots - t.pinned - E < E) return K3MOE_ERR_INVALID_ARG;
+        if (cudaSetDevice(h->cfg.device) != cudaSuccess) return K3MOE_ERR_CUDA;
+        if (launch_tier_plan(*h, layer, 0, true) != cudaSuccess || launch_tier_fill(*h, w, 0) != cudaSuccess ||
+            cudaDeviceSynchronize() != cudaSuccess) {
+            cudaGetLastError();
+            return K3MOE_ERR_CUDA;
+        }
+        int word = 0;
+        if (cudaMemcpy(&word, h->ws.err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return K3MOE_ERR_CUDA;
+        if (word != kErrNone) return K3MOE_ERR_DEVICE;
+        t.pinned += E;
+        w.pinned = true;
+        return K3MOE_OK;
+    } catch (...) {   // no C++ exception crosses the C ABI
+        return abi_exception();
     }
-    int word = 0;
-    if (cudaMemcpy(&word, h->ws.err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return K3MOE_ERR_CUDA;
-    if (word != kErrNone) return K3MOE_ERR_DEVICE;
-    t.pinned += E;
-    w.pinned = true;
-    return K3MOE_OK;
 }
 
 int k3moe_get_tier_stats(k3moe *h, k3moe_tier_stats *out)
@@ -1023,34 +1082,42 @@ int k3moe_check_wait_timeout(k3moe *h, void *stream)
 
 int k3moe_set_profiling(k3moe *h, int enable)
 {
-    if (!h) return K3MOE_ERR_INVALID_ARG;
-    if (cudaSetDevice(h->cfg.device) != cudaSuccess) return K3MOE_ERR_CUDA;
-    h->profiling = enable != 0;
-    while (h->profiling && h->event_pool.size() < 512) {   // created outside any timed region
-        cudaEvent_t e = nullptr;
-        if (cudaEventCreate(&e) != cudaSuccess) return K3MOE_ERR_CUDA;
-        h->event_pool.push_back(e);
+    try {
+        if (!h) return K3MOE_ERR_INVALID_ARG;
+        if (cudaSetDevice(h->cfg.device) != cudaSuccess) return K3MOE_ERR_CUDA;
+        h->profiling = enable != 0;
+        while (h->profiling && h->event_pool.size() < 512) {   // created outside any timed region
+            cudaEvent_t e = nullptr;
+            if (cudaEventCreate(&e) != cudaSuccess) return K3MOE_ERR_CUDA;
+            h->event_pool.push_back(e);
+        }
+        return K3MOE_OK;
+    } catch (...) {   // no C++ exception crosses the C ABI
+        return abi_exception();
     }
-    return K3MOE_OK;
 }
 
 int k3moe_profile_read(k3moe *h, k3moe_kernel_stat *out, int max_entries, int *n_entries)
 {
-    if (!h || (!out && max_entries > 0)) return K3MOE_ERR_INVALID_ARG;
-    if (cudaSetDevice(h->cfg.device) != cudaSuccess) return K3MOE_ERR_CUDA;
-    const int rc = harvest(h, true);
-    const int n = (int)h->prof_names.size();
-    for (int i = 0; i < n && i < max_entries; i++) {
-        std::memset(&out[i], 0, sizeof(k3moe_kernel_stat));
-        std::strncpy(out[i].name, h->prof_names[(size_t)i].c_str(), sizeof(out[i].name) - 1);
-        out[i].launches = h->prof_launches[(size_t)i];
-        out[i].total_ms = h->prof_ms[(size_t)i];
+    try {
+        if (!h || (!out && max_entries > 0)) return K3MOE_ERR_INVALID_ARG;
+        if (cudaSetDevice(h->cfg.device) != cudaSuccess) return K3MOE_ERR_CUDA;
+        const int rc = harvest(h, true);
+        const int n = (int)h->prof_names.size();
+        for (int i = 0; i < n && i < max_entries; i++) {
+            std::memset(&out[i], 0, sizeof(k3moe_kernel_stat));
+            std::strncpy(out[i].name, h->prof_names[(size_t)i].c_str(), sizeof(out[i].name) - 1);
+            out[i].launches = h->prof_launches[(size_t)i];
+            out[i].total_ms = h->prof_ms[(size_t)i];
+        }
+        if (n_entries) *n_entries = n;
+        h->prof_names.clear();
+        h->prof_launches.clear();
+        h->prof_ms.clear();
+        return rc;
+    } catch (...) {   // no C++ exception crosses the C ABI
+        return abi_exception();
     }
-    if (n_entries) *n_entries = n;
-    h->prof_names.clear();
-    h->prof_launches.clear();
-    h->prof_ms.clear();
-    return rc;
 }
 
 }  // extern "C"

@@ -19,6 +19,7 @@ namespace k3 {
 constexpr int kGroup = 32;          // MXFP4 columns per ue8m0 scale
 constexpr int kMaxExperts = 1024;   // router select keeps 32 scores per lane
 constexpr int kMaxTopk = 32;
+constexpr int kMaxLayers = 1024;     // per handle (the model has 93)
 constexpr int kZPad = 16;           // fp16 padding after each z16 row (holds its exponent)
 constexpr int kSplitTokensMax = 128;  // tensor-core GEMMs split K only up to this many tokens
 constexpr int kGemmMinTokens = 16;    // tensor-core dense GEMMs from this many tokens on

@@ -68,7 +68,7 @@ def _create(km, cfg):
     ("topk", 0, -2), ("max_tokens", 0, -2), ("rms_eps", 0.0, -2), ("situ_b1", float("nan"), -2),
     ("routed_scale", -1.0, -2), ("renorm", 2, -2), ("latent_norm", -1, -2),
     ("hidden", 100, -3), ("topk", 33, -3), ("n_experts", 2048, -3), ("latent", 8192, -3), ("moe_inter", 8192, -3),
-    ("situ_b1", 100.0, -3)])
+    ("situ_b1", 100.0, -3), ("max_layers", 0, -2), ("max_layers", 1025, -3)])
 def test_create_refuses_bad_config(km, field, value, code):
     rc, h = _create(km, _cfg(km, **{field: value}))
     assert rc == code and not h
