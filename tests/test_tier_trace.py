@@ -114,3 +114,42 @@ def test_trace_files_and_command_line(tmp_path, capsys):
     bad.write_text('{"layer": 0}\n')
     with pytest.raises(ValueError):
         tt.load_trace(str(bad))
+
+
+def brute_force_min_misses(trace, slots):
+    """The fewest misses any eviction choice reaches: every forward's experts
+    must be resident together; on a miss with the slots full, any resident
+    expert not used by this forward may go (all subsets tried)."""
+    from functools import lru_cache
+    from itertools import combinations
+    tr = [frozenset((l, e) for e in ex) for l, ex in trace]
+
+    @lru_cache(maxsize=None)
+    def best(i, resident):
+        if i == len(tr):
+            return 0
+        need = tr[i]
+        miss = need - resident
+        over = len(resident) + len(miss) - slots
+        if over <= 0:
+            return len(miss) + best(i + 1, resident | need)
+        out = None
+        for gone in combinations(sorted(resident - need), over):
+            v = best(i + 1, (resident - frozenset(gone)) | need)
+            out = v if out is None else min(out, v)
+        return len(miss) + out
+
+    return best(0, frozenset())
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_belady_is_the_optimum_on_small_traces(seed):
+    """On traces small enough to search exhaustively, the offline policy's
+    misses equal the fewest any policy can reach, and the tier's are never
+    fewer."""
+    r = random.Random(100 + seed)
+    E, layers, per, slots = 5, 2, r.choice([1, 2, 3]), r.choice([3, 4, 5])
+    tr = [(r.randrange(layers), r.sample(range(E), per)) for _ in range(9)]
+    opt = brute_force_min_misses(tr, slots)
+    assert replay(tr, slots, "belady")["misses"] == opt
+    assert replay(tr, slots, "tier")["misses"] >= opt
