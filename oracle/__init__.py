@@ -4,7 +4,9 @@ TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the
 CPU-baseline leg of ``bench.py`` may call it. The CUDA library never does and
 shares nothing with it. The arithmetic lives in ``k3moe_oracle.c``; this
 module compiles it with gcc (no fast-math, no FMA contraction) and marshals
-numpy arrays through ctypes.
+numpy arrays through ctypes. `build(out=..., flags=SANITIZE_FLAGS)` makes an
+AddressSanitizer/UBSan build of the same source, and K3MOE_ORACLE_LIB makes
+the loader use such a build (tests/test_oracle_sanitized.py).
 
 Parity status of each function is recorded where it is pinned (tests/).
 """
