@@ -363,12 +363,18 @@ K3MOE_API int k3moe_abi_version(void);
  * library keeps until the process exits. T * n_experts above that limit
  * returns K3MOE_ERR_SHAPE. The first call on a device looks up the array's
  * device address (cudaGetSymbolAddress); make that first call before any
- * stream capture. All calls share the array, so calls that overlap on the GPU
+ * stream capture. The address is cached for the life of the process and does
+ * not follow a cudaDeviceReset: make no further call on a device after
+ * resetting it. All calls share the array, so calls that overlap on the GPU
  * (other streams or host threads) race on it; nothing in it needs to start at
- * zero. Errors: K3MOE_ERR_INVALID_ARG (NULL pointer, T < 1, hidden not a
- * positive multiple of 8), K3MOE_ERR_CONFIG (renorm not 0/1, routed_scale not
- * finite and > 0), K3MOE_ERR_SHAPE (topk not in [1, 32], topk > n_experts,
- * n_experts > 1024, or the size limit), K3MOE_ERR_CUDA. */
+ * zero. A NaN score (from NaN or infinite inputs) ranks below every finite
+ * one; the ids stay a set of distinct experts, the weights are then
+ * undefined. Errors: K3MOE_ERR_INVALID_ARG (NULL pointer, x or router_w not
+ * on a 16-byte boundary, T < 1, hidden not a positive multiple of 8; nothing
+ * is launched), K3MOE_ERR_CONFIG (renorm not 0/1, routed_scale not finite and
+ * > 0), K3MOE_ERR_SHAPE (topk not in [1, 32], topk > n_experts, n_experts >
+ * 1024, or the size limit), K3MOE_ERR_CUDA (address lookup or launch
+ * failed). */
 #define K3MOE_ROUTE_STATIC_MAX_LOGITS (1u << 20)
 K3MOE_API int k3moe_route_static(const void *x, const void *router_w, const float *router_bias,
                                  int T, int hidden, int n_experts, int topk, int renorm,

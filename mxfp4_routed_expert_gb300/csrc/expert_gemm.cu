@@ -20,7 +20,8 @@
 //     with cvt.rn.f16x2.e2m1x2 and multiply each 32-column group by
 //     2^(s - smax_row), smax_row being the row's largest scale byte: every
 //     factor is a power of two <= 1, so the f16 operand is the exact weight /
-//     2^(smax_row - 127) unless a row spans more than 24 binades of scales.
+//     2^(smax_row - 127) unless a row spans more than 23 binades of scales
+//     (0.5 and 1.5 times 2^-24 fall between f16 subnormals).
 //     They store it straight into tensor memory (tcgen05.st: row m in lane m,
 //     column c = columns 2c, 2c+1), the MMA's A operand, so that shared memory
 //     carries only packed weights and activations;
@@ -169,10 +170,11 @@ __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b)
     return d;
 }
 
-// 2^(s - 127) for a scale byte in [1, 254] (0 and 255 clamp; 255 is refused at load).
+// 2^(s - 127) for a scale byte in [0, 254]; 0 gives the subnormal 2^-127 (255 is
+// refused at load).
 __device__ __forceinline__ float pow2_e8m0(int s)
 {
-    return __uint_as_float((uint32_t)min(max(s, 1), 254) << 23);
+    return e8m0_to_f32((uint32_t)s);
 }
 
 

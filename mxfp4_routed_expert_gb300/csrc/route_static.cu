@@ -13,7 +13,10 @@
 // exits. Host code may not use the array's name as a device address (in host
 // code it names a host-side stand-in), so the first call on each device looks
 // the address up with cudaGetSymbolAddress while that device is current and
-// caches it. Every call shares the array: two calls that overlap on the GPU
+// caches it for the life of the process (the cache does not follow a
+// cudaDeviceReset, after which the array may sit elsewhere: call no further
+// k3moe_route_static on a device after resetting it). Every call shares the
+// array: two calls that overlap on the GPU
 // (on different streams, or on different host threads) overwrite each
 // other's logits. Each call writes every logit it later reads, so nothing in
 // the array has to start at zero.
@@ -100,6 +103,10 @@ __global__ void __launch_bounds__(32) k_static_topk(const float *logits, const f
         const int e = lane + 32 * i;
         sc[i] = e < E ? k3::sigmoid_f(logits[(size_t)t * E + e]) : 0.f;
         ch[i] = e < E ? sc[i] + (bias ? bias[e] : 0.f) : 0.f;
+        // a NaN score (from a NaN or infinite input) ranks below every number, so
+        // that the comparisons below stay a total order and all lanes agree on
+        // every pick
+        if (isnan(ch[i])) ch[i] = -INFINITY;
     }
     uint32_t taken = 0u;
     float wsum = 0.f, wsel = 0.f;
@@ -149,6 +156,9 @@ extern "C" int k3moe_route_static(const void *x, const void *router_w, const flo
 {
     if (!x || !router_w || !ids || !w) return K3MOE_ERR_INVALID_ARG;
     if (T < 1 || hidden < 8 || hidden % 8 || n_experts < 1) return K3MOE_ERR_INVALID_ARG;
+    // the dot products read x and Wr in 16-byte chunks
+    if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(router_w)) % 16 != 0)
+        return K3MOE_ERR_INVALID_ARG;
     if ((renorm != 0 && renorm != 1) || !std::isfinite(routed_scale) || routed_scale <= 0.f)
         return K3MOE_ERR_CONFIG;
     if (topk < 1 || topk > k3::kMaxTopk || topk > n_experts || n_experts > k3::kMaxExperts)
@@ -161,9 +171,11 @@ extern "C" int k3moe_route_static(const void *x, const void *router_w, const flo
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const long long rows = (long long)T * n_experts;
     const int grid = (int)((rows + 7) / 8 < 4096 ? (rows + 7) / 8 : 4096);
+    // each launch's own error is taken right after it (a launch error is not sticky)
     k_static_logits<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(x),
                                          static_cast<const __nv_bfloat16 *>(router_w), logits, T,
                                          hidden, n_experts);
+    if (cudaGetLastError() != cudaSuccess) return K3MOE_ERR_CUDA;
     k_static_topk<<<T, 32, 0, s>>>(logits, router_bias, n_experts, topk, renorm, routed_scale, ids,
                                    w);
     return cudaGetLastError() == cudaSuccess ? K3MOE_OK : K3MOE_ERR_CUDA;

@@ -2,7 +2,7 @@
 the parity metrics, and thin wrappers that move numpy inputs through the
 C ABI with torch-allocated device memory.
 
-Tolerances (BASELINE north star): expert ids and the permutation bit-exact;
+Tolerances of the layer: expert ids and the permutation bit-exact;
 floating-point outputs within normwise max relative error 2e-2
 (max_i |y_i - y*_i| / max_i |y*_i|, the pages' "relative to max|ref|" logit
 metric) and cosine similarity >= 0.9995 against the fp64 oracle.
@@ -51,6 +51,23 @@ def guarded_tokens(shape, layer, seed, T, stream=0, tau=MARGIN_TAU, make=None, m
         att[bad] += 1
         x = make(att)
     raise RuntimeError("margin guard did not converge")
+
+
+def router_only_layer(shape, router: dict):
+    """(shape, layer) for oracle.route from the router tensors alone: the route
+    reads only router_w and router_bias, so the other tensors are zeros of a
+    layer whose latent, expert and shared widths are 32 (a few hundred KB
+    instead of the full layer)."""
+    small = k3synth.replace(shape, latent=32, moe_inter=32, shared_inter=32)
+    H, L, E, I, S = small.hidden, small.latent, small.n_experts, small.moe_inter, small.shared_inter
+    z16 = lambda *s: np.zeros(s, np.uint16)   # noqa: E731
+    z8 = lambda *s: np.zeros(s, np.uint8)     # noqa: E731
+    d = {"router_w": router["router_w"], "router_bias": router["router_bias"],
+         "down_w": z16(L, H), "up_w": z16(H, L), "latent_gain": z16(L), "sh_w1": z16(S, H),
+         "sh_w3": z16(S, H), "sh_w2": z16(H, S), "w1p": z8(E, I, L // 2), "w1s": z8(E, I, L // 32),
+         "w3p": z8(E, I, L // 2), "w3s": z8(E, I, L // 32), "w2p": z8(E, L, I // 2),
+         "w2s": z8(E, L, I // 32)}
+    return small, d
 
 
 def ids_match(ids_gpu, ids_ref):
@@ -154,6 +171,15 @@ class Layer:
 
 def bf16_to_f64(bits):
     return k3synth.bf16_bits_to_f32(bits).astype(np.float64)
+
+
+def check_ids_and_weights(ids_gpu, w_gpu, oracle_ids, oracle_w, tol=1e-5):
+    """Exact id sets per token; each picked expert's weight within tol."""
+    assert ids_match(ids_gpu, oracle_ids), "expert id sets differ"
+    for t in range(np.asarray(ids_gpu).shape[0]):
+        og = dict(zip(np.asarray(oracle_ids)[t].tolist(), np.asarray(oracle_w)[t].tolist()))
+        for e, wv in zip(np.asarray(ids_gpu)[t].tolist(), np.asarray(w_gpu)[t].tolist()):
+            assert abs(wv - og[e]) < tol, (t, e, wv, og[e])
 
 
 def check_routing(gpu: dict, shape, x_bits, oracle_ids, oracle_w):

@@ -400,6 +400,30 @@ def test_k3_decode_T1(k3layer):
         assert_close(bf16_to_f64(y), ref, f"K3 T=1 token {t}")
 
 
+@pytest.mark.parametrize("T", [2, 5, 8, 16])
+def test_k3_decode_batches(k3layer, T):
+    """K3 width at the batch sizes between one token and T=64: T=2 runs the
+    TMA-fed dense GEMVs, 3 <= T <= 15 the register GEMVs, T=16 the smallest
+    tensor-core batch (split-K dense GEMMs; 256 pairs, so the automatic expert
+    path is the grouped GEMM, and the per-pair GEMVs are checked on the same
+    tokens)."""
+    import mxfp4_routed_expert_gb300 as km
+    d, lay = k3layer
+    shape = k3synth.K3
+    x, _ = guarded_tokens(shape, d, 0, T, stream=20 + T)
+    ref, tr = oracle.layer_forward(shape, d, x, trace=True)
+    modes = (km.K3MOE_EXPERT_AUTO, km.K3MOE_EXPERT_GEMV) if T >= 16 else (km.K3MOE_EXPERT_AUTO,)
+    try:
+        for mode in modes:
+            km.k3moe_set_expert_path(lay.h, mode)
+            y = lay.forward(x)
+            r = lay.routing(T)
+            check_routing(r, shape, x, tr["ids"], tr["w"])
+            assert_close(bf16_to_f64(y), ref, f"K3 T={T}, expert path {mode}")
+    finally:
+        km.k3moe_set_expert_path(lay.h, km.K3MOE_EXPERT_AUTO)
+
+
 def test_k3_residual_T1(k3layer):
     """The RMSNorm in front of the MoE fused into the decode kernels at K3 size
     (hidden 7168: 14 float4 per consumer thread per token)."""
