@@ -394,7 +394,7 @@ def run_native(args, rank, world):
     shape, d0, xpool = make_inputs(args.workload)
     h = km.k3moe_create(km.make_config(shape, max_layers=n_layers, max_tokens=T, device=dev))
     km.k3moe_set_expert_path(h, {"auto": km.K3MOE_EXPERT_AUTO, "gemv": km.K3MOE_EXPERT_GEMV,
-                                 "gemm": km.K3MOE_EXPERT_GEMM}[args.expert_path])
+                                 "gemm": km.K3MOE_EXPERT_GEMM, "mx": km.K3MOE_EXPERT_MX}[args.expert_path])
     alternate = wl.get("alternate", False)   # one layer per step, layers in turn (else a chain)
     if wl.get("topp"):
         km.k3moe_set_topp(h, wl["topp"])
@@ -662,8 +662,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--workload", choices=list(WORKLOADS), default="decode_t1")
-    ap.add_argument("--expert-path", choices=["auto", "gemv", "gemm"], default="auto",
-                    help="routed-expert kernels: auto (grouped GEMM from T >= 16), per-pair GEMVs, or GEMM")
+    ap.add_argument("--expert-path", choices=["auto", "gemv", "gemm", "mx"], default="auto",
+                    help="routed-expert kernels: auto (grouped GEMM from T >= 16), per-pair GEMVs, the "
+                         "grouped GEMM, or its block-scaled form (mxf8f6f4, two-term MXFP8 activations)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--dump-trace", default="",

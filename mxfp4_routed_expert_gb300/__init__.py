@@ -42,7 +42,7 @@ EXPORTS = ("k3moe_create", "k3moe_load_layer", "k3moe_forward", "k3moe_forward_c
            "k3moe_forward_residual", "k3moe_set_topp", "k3moe_tier_pin_layer",
            "k3moe_check_wait_timeout")
 K3MOE_ROUTE_STATIC_MAX_LOGITS = 1 << 20
-K3MOE_EXPERT_AUTO, K3MOE_EXPERT_GEMV, K3MOE_EXPERT_GEMM = 0, 1, 2
+K3MOE_EXPERT_AUTO, K3MOE_EXPERT_GEMV, K3MOE_EXPERT_GEMM, K3MOE_EXPERT_MX = 0, 1, 2, 3
 
 
 class K3MoEError(RuntimeError):
@@ -300,7 +300,7 @@ def k3moe_set_profiling(h: int, enable: bool) -> int:
 
 
 def k3moe_set_expert_path(h: int, mode: int) -> int:
-    """K3MOE_EXPERT_AUTO / _GEMV / _GEMM: which routed-expert kernels forwards use."""
+    """K3MOE_EXPERT_AUTO / _GEMV / _GEMM / _MX: which routed-expert kernels forwards use."""
     return _check(lib().k3moe_set_expert_path(ctypes.c_void_p(h), int(mode)),
                   "k3moe_set_expert_path")
 

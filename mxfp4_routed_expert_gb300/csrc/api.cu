@@ -116,6 +116,13 @@ size_t carve_workspace(const k3moe_config &c, char *base, Workspace *ws)
     w.acc = cv.take<float>(Tm * L);
     const bool eg = expert_gemm_ok(c);
     w.zperm = cv.take<__half>(eg ? Tm * K * (L + kZPad) : 0);
+    // two-term MXFP8 activations of the block-scaled grouped expert path
+    w.zq = cv.take<uint8_t>(eg ? 2 * Tm * L : 0);
+    w.zqs = cv.take<uint8_t>(eg ? 2 * Tm * L / kGroup : 0);
+    w.zp8 = cv.take<uint8_t>(eg ? 2 * Tm * K * L : 0);
+    w.zps = cv.take<uint8_t>(eg ? 2 * Tm * K * L / kGroup : 0);
+    w.h8 = cv.take<uint8_t>(eg ? 2 * Tm * K * I : 0);
+    w.h8s = cv.take<uint8_t>(eg ? 2 * Tm * K * I / kGroup : 0);
     w.tiles = cv.take<int2>(eg ? expert_gemm_max_tiles(c) : 0);
     w.n_tiles = cv.take<int>(1);
     w.perm_hist = cv.take<int>((size_t)perm_chunks(c.max_tokens) * E);
@@ -243,7 +250,7 @@ bool use_expert_gemm(const k3moe &h, int T)
 {
     if (!h.egemm_ok || h.expert_path == K3MOE_EXPERT_GEMV) return false;
     if (T * h.cfg.topk < expert_gemm_min_pairs()) return false;
-    return h.expert_path == K3MOE_EXPERT_GEMM || T >= kGemmMinTokens;
+    return h.expert_path == K3MOE_EXPERT_GEMM || h.expert_path == K3MOE_EXPERT_MX || T >= kGemmMinTokens;
 }
 
 // hin != nullptr: the layer input is made from the fp32 residual hin by the
@@ -336,8 +343,13 @@ int run_layer(k3moe *h, const LayerDev &w, const __nv_bfloat16 *x, __nv_bfloat16
         }
     }
     if (gemm && cudaStreamWaitEvent(s, h->ev_join, 0) != cudaSuccess) return K3MOE_ERR_CUDA;
-    if (egemm) {
-        K3_STEP("expert_tiles", launch_expert_tiles(*h, T, s));
+    if (egemm && h->expert_path == K3MOE_EXPERT_MX) {
+        K3_STEP("expert_tiles", launch_expert_tiles(*h, T, s, true));
+        K3_STEP("gather_latent", launch_gather_zq(*h, T, s));
+        K3_STEP("expert_w13_gemm", launch_expert_mx(*h, w, T, s, true));
+        K3_STEP("expert_w2_gemm", launch_expert_mx(*h, w, T, s, false));
+    } else if (egemm) {
+        K3_STEP("expert_tiles", launch_expert_tiles(*h, T, s, false));
         K3_STEP("gather_latent", launch_gather_latent(*h, T, s));
         K3_STEP("expert_w13_gemm", launch_expert_gemm(*h, w, T, s, true));
         K3_STEP("expert_w2_gemm", launch_expert_gemm(*h, w, T, s, false));
@@ -490,7 +502,7 @@ int k3moe_create(const k3moe_config *cfg, k3moe **out)
         init_dense_kernels(*h) != cudaSuccess ||
         init_route_kernels(*cfg) != cudaSuccess || init_expert_kernels(*cfg) != cudaSuccess ||
         init_dense_tma(*cfg) != cudaSuccess || init_dense_gemm() != cudaSuccess ||
-        init_expert_gemm() != cudaSuccess ||
+        init_expert_gemm() != cudaSuccess || init_expert_mx() != cudaSuccess ||
         cudaDeviceSynchronize() != cudaSuccess) {
         cudaGetLastError();
         cudaStreamDestroy(h->side);
@@ -928,9 +940,10 @@ int k3moe_sync_status(k3moe *h)
 int k3moe_set_expert_path(k3moe *h, int mode)
 {
     if (!h) return K3MOE_ERR_INVALID_ARG;
-    if (mode != K3MOE_EXPERT_AUTO && mode != K3MOE_EXPERT_GEMV && mode != K3MOE_EXPERT_GEMM)
+    if (mode != K3MOE_EXPERT_AUTO && mode != K3MOE_EXPERT_GEMV && mode != K3MOE_EXPERT_GEMM &&
+        mode != K3MOE_EXPERT_MX)
         return K3MOE_ERR_INVALID_ARG;
-    if (mode == K3MOE_EXPERT_GEMM && !h->egemm_ok) return K3MOE_ERR_SHAPE;
+    if ((mode == K3MOE_EXPERT_GEMM || mode == K3MOE_EXPERT_MX) && !h->egemm_ok) return K3MOE_ERR_SHAPE;
     h->expert_path = mode;
     return K3MOE_OK;
 }

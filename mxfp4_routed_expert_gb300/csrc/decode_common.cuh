@@ -54,6 +54,8 @@ struct RouteArgs {
     float *wts;            // [T, k]
     const float *z;        // [T, L]
     __half *z16;           // [T, L + kZPad]: scaled fp16 z, then the exponent (int32)
+    uint8_t *zq, *zqs;     // null, or two-term MXFP8 z: [2][zq_rows][L] e4m3, [2][zq_rows][L/32] scales
+    int zq_rows;
     float *acc;            // [T, L]
     int L;
     float topp;            // > 0: keep the picks up to cumulative weight topp (0: all k)
@@ -231,6 +233,27 @@ __device__ __forceinline__ void route_token(const RouteArgs &a, int t, RouteSmem
         if (i < a.L) {
             a.z16[(size_t)t * (a.L + kZPad) + i] = __float2half_rn(zv[q] * zsc);
             a.acc[(size_t)t * a.L + i] = 0.f;
+        }
+    }
+    if (a.zq) {
+        // the tensor-core expert path's copy of z: the 32 lanes of a warp hold
+        // 32 consecutive latent values, one scale group (L % 32 == 0)
+        const size_t pl = (size_t)a.zq_rows * a.L;
+#pragma unroll
+        for (int q = 0; q < kZPer; q++) {
+            const int i0 = (tid & ~31) + q * kRouteThreads;
+            if (i0 < a.L) {
+                const int i = i0 + (tid & 31);
+                uint32_t qh, ql;
+                int eh, el;
+                mx8_hilo(zv[q], qh, ql, eh, el);
+                a.zq[(size_t)t * a.L + i] = (uint8_t)qh;
+                a.zq[pl + (size_t)t * a.L + i] = (uint8_t)ql;
+                if ((tid & 31) == 0) {
+                    a.zqs[((size_t)t * a.L + i) / kGroup] = (uint8_t)(eh + 127);
+                    a.zqs[(pl + (size_t)t * a.L + i) / kGroup] = (uint8_t)(el + 127);
+                }
+            }
         }
     }
     if (tid == 0) *reinterpret_cast<int *>(a.z16 + (size_t)t * (a.L + kZPad) + a.L) = ex;

@@ -108,20 +108,6 @@ struct Geo {
     static_assert(SMEM <= (size_t)kSmemBudget && NR >= 4, "shared memory");
 };
 
-// Position in a ring of N slots: slot index and the parity of its current use.
-template <int N>
-struct RingPos {
-    int slot = 0;
-    uint32_t phase = 0;
-    __device__ __forceinline__ void next()
-    {
-        if (++slot == N) {
-            slot = 0;
-            phase ^= 1u;
-        }
-    }
-};
-
 struct EgArgs {
     const uint8_t *sa, *sb;      // scale rows [E*R, K/32] (W1 and W3, or W2)
     const uint8_t *ma, *mb;      // largest scale byte per row [E*R]
@@ -191,22 +177,6 @@ __device__ __forceinline__ void widen_group(uint4 w, uint32_t f, uint32_t *o)
         o[4 * j + 2] = hmul2(h2, f);
         o[4 * j + 3] = hmul2(h3, f);
     }
-}
-
-// One lane of a converged warp.
-__device__ __forceinline__ bool elect_one()
-{
-    uint32_t p;
-    asm volatile("{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\tselp.u32 %0, 1, 0, e;\n\t}" : "=r"(p));
-    return p != 0;
-}
-
-// A bounded barrier wait by every lane of a converged warp, which takes the
-// outcome only if all lanes saw the phase complete.
-__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, int *err, int where)
-{
-    const bool ok = mbar_wait(bar, parity, err, where);
-    return __all_sync(0xffffffffu, ok) != 0;
 }
 
 // A from tensor memory, B from shared memory.
@@ -434,8 +404,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q = warp - 1;
         {
             int local = 0;
-            RingPos<NB> bp;
-            RingPos<NSA> ap;
+            tc::RingPos<NB> bp;
+            tc::RingPos<NSA> ap;
             const uint64_t db0 = tc::desc_sw128(tc::su32(bring));
             const int kk0 = DUAL ? 0 : 4 * q;            // first k-step (of 16 columns)
             constexpr int NK = DUAL ? BK / 16 : BK / 32; // k-steps per k-stage for this issuer
@@ -448,19 +418,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t idesc =
                     (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);  // f16 x f16 -> f32
                 const int b = local % kSets;
-                if (!warp_wait(&tempty[b], ((uint32_t)(local / kSets) & 1u) ^ 1u, g.err, 601)) break;
+                if (!tc::warp_wait(&tempty[b], ((uint32_t)(local / kSets) & 1u) ^ 1u, g.err, 601)) break;
                 tc::fence_after();
                 const uint32_t d = tmem + (uint32_t)b * kSetCols + (uint32_t)q * BN;
                 for (int kt = 0; kt < KT; kt++, bp.next(), ap.next()) {
-                    if (!warp_wait(&aready[ap.slot], ap.phase, g.err, 603) ||
-                        !warp_wait(&bfull[bp.slot], bp.phase, g.err, 609)) {
+                    if (!tc::warp_wait(&aready[ap.slot], ap.phase, g.err, 603) ||
+                        !tc::warp_wait(&bfull[bp.slot], bp.phase, g.err, 609)) {
                         ok = false;
                         break;
                     }
                     tc::fence_after();
                     const uint32_t a0 = tmem + kARing0 + (uint32_t)(ap.slot * ACOLS) + (DUAL ? (uint32_t)q * (BK / 2) : 0u);
                     const uint64_t db = db0 + (uint64_t)((bp.slot * kBBytes) >> 4);
-                    if (elect_one()) {
+                    if (tc::elect_one()) {
 #pragma unroll
                         for (int i = 0; i < NK; i++) {
                             const int kk = kk0 + i;
@@ -472,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     __syncwarp();
                 }
-                if (ok && elect_one()) tc::commit(&tfull[b]);
+                if (ok && tc::elect_one()) tc::commit(&tfull[b]);
                 __syncwarp();
             }
         }
@@ -493,9 +463,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tlane = (uint32_t)(qd * 32) << 16;
         const int G = g.K / kGroup;
         const int swz = (row >> 1) & 3;              // 64-byte swizzle of the packed tile
-        RingPos<NR> wp;           // weight stage of this k-stage
-        RingPos<NB> rq;           // activation stage of the k-stage NSA back (its MMAs free the A slot)
-        RingPos<NSA> ap;
+        tc::RingPos<NR> wp;           // weight stage of this k-stage
+        tc::RingPos<NB> rq;           // activation stage of the k-stage NSA back (its MMAs free the A slot)
+        tc::RingPos<NSA> ap;
         int done = 0;             // k-stages of this CTA so far
         int local = 0;            // items of this CTA so far
         bool ok = true;
@@ -702,16 +672,18 @@ cudaError_t init_expert_gemm()
 // experts see a few tokens each (narrow accumulators leave TMEM for a third A
 // slot), 64 below 64 pairs (two accumulator sets), else 128 (every converted
 // weight tile then feeds twice the MMA work, with one set).
-int expert_gemm_bn(const k3moe &h, int T)
+// The block-scaled path (mx) takes 96 in place of 128: the widest tile for
+// which two W1/W3 accumulator sets and its scale-factor ring fit in TMEM.
+int expert_gemm_bn(const k3moe &h, int T, bool mx)
 {
     const long long pairs = (long long)T * h.cfg.topk, E = h.cfg.n_experts;
-    return pairs <= 4 * E ? 32 : (pairs < 64 * E ? 64 : 128);
+    return pairs <= 4 * E ? 32 : (pairs < 64 * E ? 64 : (mx ? 96 : 128));
 }
 
-cudaError_t launch_expert_tiles(const k3moe &h, int T, cudaStream_t s)
+cudaError_t launch_expert_tiles(const k3moe &h, int T, cudaStream_t s, bool mx)
 {
     return launch_pdl(k_expert_tiles, 1, 1024, 0, s, (const int *)h.ws.counts, h.cfg.n_experts,
-                      expert_gemm_bn(h, T), h.ws.tiles, h.ws.n_tiles);
+                      expert_gemm_bn(h, T, mx), h.ws.tiles, h.ws.n_tiles);
 }
 
 cudaError_t launch_gather_latent(const k3moe &h, int T, cudaStream_t s)
@@ -727,7 +699,7 @@ cudaError_t launch_expert_gemm(const k3moe &h, const LayerDev &w, int T, cudaStr
 {
     const k3moe_config &c = h.cfg;
     const int pairs = T * c.topk;
-    const int bn = expert_gemm_bn(h, T);   // the width the tile list was built for
+    const int bn = expert_gemm_bn(h, T, false);   // the width the tile list was built for
     if (pairs < kMinPairs) return cudaErrorInvalidValue;
     EgArgs g = {};
     g.k = c.topk;

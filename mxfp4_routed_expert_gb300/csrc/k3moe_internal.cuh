@@ -122,8 +122,13 @@ struct Workspace {
     int *touched = nullptr;       // [E]  experts with at least one token, ascending
     int *n_touched = nullptr;     // [1]
     __half *h16 = nullptr;        // [Tm*k, I] SiTU output per (token, expert) pair, perm order
-    float *acc = nullptr;         // [Tm, L]
     __half *zperm = nullptr;      // [Tm*k, L + kZPad] z16 rows gathered in pair order (expert GEMM)
+    // Block-scaled expert path activations in two-term MXFP8 (plane 0: hi,
+    // plane 1: lo; e4m3 bytes, then one ue8m0 scale byte per 32 of them):
+    uint8_t *zq = nullptr, *zqs = nullptr;   // latent per token [2][Tm][L], [2][Tm][L/32]
+    uint8_t *zp8 = nullptr, *zps = nullptr;  // latent per pair  [2][Tm*k][L], [2][Tm*k][L/32]
+    uint8_t *h8 = nullptr, *h8s = nullptr;   // SiTU per pair    [2][Tm*k][I], [2][Tm*k][I/32]
+    float *acc = nullptr;         // [Tm, L]
     int2 *tiles = nullptr;        // (expert, n-tile) list of the expert GEMM
     int *perm_hist = nullptr;     // [ceil(Tm/32), E] per-chunk expert counts, then chunk bases
     int *n_tiles = nullptr;       // length of the list
@@ -215,11 +220,18 @@ bool expert_gemm_ok(const k3moe_config &c);
 size_t expert_gemm_max_tiles(const k3moe_config &c);
 int expert_gemm_min_pairs();
 cudaError_t init_expert_gemm();
-int expert_gemm_bn(const k3moe &h, int T);
-cudaError_t launch_expert_tiles(const k3moe &h, int T, cudaStream_t s);
+// n-tile width for a batch of T tokens (mx: the block-scaled path's widths)
+int expert_gemm_bn(const k3moe &h, int T, bool mx);
+cudaError_t launch_expert_tiles(const k3moe &h, int T, cudaStream_t s, bool mx);
 cudaError_t launch_gather_latent(const k3moe &h, int T, cudaStream_t s);
 cudaError_t launch_expert_gemm(const k3moe &h, const LayerDev &w, int T, cudaStream_t s, bool w13);
 cudaError_t launch_row_scale_max(const uint8_t *s, size_t rows, int G, uint8_t *out);
+// The grouped expert GEMM on block-scaled tensor cores (MXFP4 weights x
+// two-term MXFP8 activations): the latent gathered into pair order, then
+// W1/W3 with SiTU (w13) or W2 with the weighted scatter-add.
+cudaError_t init_expert_mx();
+cudaError_t launch_gather_zq(const k3moe &h, int T, cudaStream_t s);
+cudaError_t launch_expert_mx(const k3moe &h, const LayerDev &w, int T, cudaStream_t s, bool w13);
 bool dense_tma_fits(const k3moe_config &c, int TB);
 bool build_dense_tma_maps(const k3moe_config &c, LayerDev &w);
 // TMA-fed dense GEMVs for T <= 2. part 0: router + down; 1: shared gate/up;
@@ -304,6 +316,59 @@ __device__ __forceinline__ float f16x2_sum(uint32_t v)
 __device__ __forceinline__ float e8m0_to_f32(uint32_t s)
 {
     return s == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(s << 23);
+}
+
+// 2^n for an integer n in [-127, 127] (n = -127 gives the subnormal 2^-127).
+__device__ __forceinline__ float exp2i(int n)
+{
+    return n >= -126 ? __uint_as_float((uint32_t)(n + 127) << 23) : __uint_as_float(0x00400000u);
+}
+
+// ---- MXFP8 activations: e4m3 elements, one ue8m0 scale per 32 ----------------
+// Exponent e of the scale 2^e of a group whose largest magnitude has the fp32
+// bit pattern amax: the smallest e with amax <= 448 * 2^e (448 = 1.75 * 2^8,
+// the largest e4m3 value), so that no element saturates; clamped to the
+// ue8m0 range [-127, 127] (byte = e + 127).
+__device__ __forceinline__ int mx_group_exponent(uint32_t amax)
+{
+    if (amax == 0u) return -127;
+    const int e = (int)(amax >> 23) - 127 - 8 + ((amax & 0x7FFFFFu) > 0x600000u ? 1 : 0);
+    return max(-127, min(127, e));
+}
+
+// fp32 -> e4m3 byte, round to nearest even (both lanes of the x2 conversion
+// get v, so the byte order of the pair does not matter).
+__device__ __forceinline__ uint32_t f32_to_e4m3(float v)
+{
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(v), "f"(v));
+    return r & 0xFFu;
+}
+
+// e4m3 byte -> fp32 (exact; through f16, which holds every e4m3 value).
+__device__ __forceinline__ float e4m3_to_f32(uint32_t q)
+{
+    uint32_t h2;
+    const uint16_t b = (uint16_t)(q | (q << 8));
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(b));
+    return __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu)));
+}
+
+// Two-term MXFP8 of v, one value per lane of a converged warp whose 32 lanes
+// hold one scale group: hi = e4m3(v / 2^eh), eh chosen by mx_group_exponent
+// over the group, and lo = e4m3((v - hi 2^eh) / 2^el) with el = eh - 4. The
+// scaled values of hi lie within 448, so their rounding error is at most 16
+// (half the e4m3 spacing 32 of the top binade); times 2^4 that stays within
+// 448 and keeps the residual's own e4m3 precision without a second group
+// maximum. hi 2^eh + lo 2^el carries about 8 significant bits more than hi
+// alone.
+__device__ __forceinline__ void mx8_hilo(float v, uint32_t &qh, uint32_t &ql, int &eh, int &el)
+{
+    eh = mx_group_exponent(__reduce_max_sync(0xffffffffu, __float_as_uint(v) & 0x7fffffffu));
+    el = max(eh - 4, -127);
+    qh = f32_to_e4m3(v * exp2i(-eh));
+    const float r = v - e4m3_to_f32(qh) * exp2i(eh);
+    ql = f32_to_e4m3(r * exp2i(-el));
 }
 
 __device__ __forceinline__ float sigmoid_f(float v) { return 1.0f / (1.0f + expf(-v)); }

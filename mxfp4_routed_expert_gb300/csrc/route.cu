@@ -6,8 +6,9 @@
 // going to the lower expert id), and the renormalised UNBIASED weights.
 // kimi-k3-in-c README, Part II section 9 (k3_router); colibri
 // docs/kimi_k3.md "Stable LatentMoE". The same block prepares the expert GEMV
-// input: z scaled by a per-token power of two into fp16, and clears the
-// token's fp32 accumulator row.
+// input: z scaled by a per-token power of two into fp16 (and, for the grouped
+// block-scaled path, z in two-term MXFP8), and clears the token's fp32
+// accumulator row.
 //
 // Permutation (three launches over 32-token chunks, T > 1): per-expert
 // counts, exclusive offsets, and the pair list grouped by expert with tokens
@@ -44,6 +45,11 @@ static RouteArgs route_args(const k3moe &h, const LayerDev &w, int T)
     a.wts = h.ws.wts;
     a.z = h.ws.z;
     a.z16 = h.ws.z16;
+    // the block-scaled grouped expert path reads z in two-term MXFP8
+    const bool mx = h.egemm_ok && h.expert_path == K3MOE_EXPERT_MX && T * c.topk >= expert_gemm_min_pairs();
+    a.zq = mx ? h.ws.zq : nullptr;
+    a.zqs = mx ? h.ws.zqs : nullptr;
+    a.zq_rows = c.max_tokens;
     a.acc = h.ws.acc;
     a.L = c.latent;
     a.fuse_perm = T == 1;

@@ -165,5 +165,35 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16])
     for (int i = 0; i < 16; i++) v[i] = __uint_as_float(r[i]);
 }
 
+// Position in a ring of N slots: slot index and the parity of its current use.
+template <int N>
+struct RingPos {
+    int slot = 0;
+    uint32_t phase = 0;
+    __device__ __forceinline__ void next()
+    {
+        if (++slot == N) {
+            slot = 0;
+            phase ^= 1u;
+        }
+    }
+};
+
+// One lane of a converged warp.
+__device__ __forceinline__ bool elect_one()
+{
+    uint32_t p;
+    asm volatile("{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\tselp.u32 %0, 1, 0, e;\n\t}" : "=r"(p));
+    return p != 0;
+}
+
+// A bounded barrier wait by every lane of a converged warp, which takes the
+// outcome only if all lanes saw the phase complete. Needs k3moe_internal.cuh.
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, int *err, int where)
+{
+    const bool ok = mbar_wait(bar, parity, err, where);
+    return __all_sync(0xffffffffu, ok) != 0;
+}
+
 }  // namespace tc
 }  // namespace k3

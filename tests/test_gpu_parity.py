@@ -70,16 +70,21 @@ def test_tensor_core_dense_path(T):
     run_case(WIDE, k3synth.TINY_RECIPE, 6, T)
 
 
-@pytest.mark.parametrize("T,path", [(16, "gemm"), (37, "gemv"), (300, "gemv"), (20, "gemm")])
-def test_expert_paths(T, path):
-    """Both routed-expert paths against the oracle: the per-pair GEMVs and the
-    grouped tcgen05 GEMM (T=16 with topk 8 is its smallest batch, 128 pairs)."""
+def _mode(path):
     import mxfp4_routed_expert_gb300 as km
-    mode = km.K3MOE_EXPERT_GEMM if path == "gemm" else km.K3MOE_EXPERT_GEMV
-    run_case(WIDE, k3synth.TINY_RECIPE, 6, T, expert_path=mode)
+    return {"gemm": km.K3MOE_EXPERT_GEMM, "gemv": km.K3MOE_EXPERT_GEMV, "mx": km.K3MOE_EXPERT_MX}[path]
 
 
-@pytest.mark.parametrize("path", ["gemm", "gemv"])
+@pytest.mark.parametrize("T,path", [(16, "gemm"), (37, "gemv"), (300, "gemv"), (20, "gemm"), (16, "mx"),
+                                    (300, "mx")])
+def test_expert_paths(T, path):
+    """The routed-expert paths against the oracle: the per-pair GEMVs, the
+    grouped tcgen05 GEMM and its block-scaled form (T=16 with topk 8 is the
+    grouped GEMMs' smallest batch, 128 pairs)."""
+    run_case(WIDE, k3synth.TINY_RECIPE, 6, T, expert_path=_mode(path))
+
+
+@pytest.mark.parametrize("path", ["gemm", "gemv", "mx"])
 def test_expert_gemm_multi_tile(path):
     """Four experts forced into every token's selection (+10 router bias): each
     holds all 300 tokens, five n-tiles of the grouped GEMM (2400 pairs on 128
@@ -89,12 +94,11 @@ def test_expert_gemm_multi_tile(path):
     bias = np.asarray(d["router_bias"], np.float32).copy()
     bias[[3, 40, 77, 127]] += 10.0
     d = k3synth.with_bias(d, bias)
-    mode = km.K3MOE_EXPERT_GEMM if path == "gemm" else km.K3MOE_EXPERT_GEMV
-    run_case(WIDE, k3synth.TINY_RECIPE, 8, 300, expert_path=mode, d=d)
+    run_case(WIDE, k3synth.TINY_RECIPE, 8, 300, expert_path=_mode(path), d=d)
 
 
-@pytest.mark.parametrize("T", [40, 64])
-def test_expert_gemm_narrow_ntiles(T):
+@pytest.mark.parametrize("T,path", [(40, "gemm"), (64, "gemm"), (40, "mx"), (64, "mx")])
+def test_expert_gemm_narrow_ntiles(T, path):
     """At most four pairs per expert on average (T*8 <= 4*128) selects 32-pair
     n-tiles; four experts forced into every selection then hold T pairs each,
     two n-tiles (32 + 8 at T=40, 32 + 32 at T=64)."""
@@ -103,7 +107,7 @@ def test_expert_gemm_narrow_ntiles(T):
     bias = np.asarray(d["router_bias"], np.float32).copy()
     bias[[5, 50, 90, 126]] += 10.0
     d = k3synth.with_bias(d, bias)
-    run_case(WIDE, k3synth.TINY_RECIPE, 10, T, expert_path=km.K3MOE_EXPERT_GEMM, d=d)
+    run_case(WIDE, k3synth.TINY_RECIPE, 10, T, expert_path=_mode(path), d=d)
 
 
 # latent 384: three 128-row m-tiles of W2, which the grouped GEMM runs one per
@@ -112,15 +116,14 @@ ODD_LATENT = k3synth.Shape(hidden=1024, latent=384, n_experts=128, topk=8, moe_i
                            shared_inter=1024)
 
 
-@pytest.mark.parametrize("T", [48, 200])
-def test_expert_gemm_unpaired_w2(T):
+@pytest.mark.parametrize("T,path", [(48, "gemm"), (200, "gemm"), (48, "mx"), (200, "mx")])
+def test_expert_gemm_unpaired_w2(T, path):
     """The unpaired W2 mode at 32-pair (T=48) and 64-pair (T=200) n-tiles."""
-    import mxfp4_routed_expert_gb300 as km
-    run_case(ODD_LATENT, k3synth.TINY_RECIPE, 11, T, expert_path=km.K3MOE_EXPERT_GEMM)
+    run_case(ODD_LATENT, k3synth.TINY_RECIPE, 11, T, expert_path=_mode(path))
 
 
-@pytest.mark.parametrize("hot", [False, True])
-def test_expert_gemm_wide_ntiles(hot):
+@pytest.mark.parametrize("hot,path", [(False, "gemm"), (True, "gemm"), (False, "mx"), (True, "mx")])
+def test_expert_gemm_wide_ntiles(hot, path):
     """T=1100 on the 128-expert shape: 8800 pairs, at least 64 per expert on
     average, so the grouped GEMM cuts 128-pair n-tiles. With four experts forced
     into every selection each of them holds 1100 pairs (nine n-tiles)."""
@@ -130,7 +133,7 @@ def test_expert_gemm_wide_ntiles(hot):
         bias = np.asarray(d["router_bias"], np.float32).copy()
         bias[[0, 31, 64, 100]] += 10.0
         d = k3synth.with_bias(d, bias)
-    run_case(WIDE, k3synth.TINY_RECIPE, 9, 1100, expert_path=km.K3MOE_EXPERT_GEMM, d=d,
+    run_case(WIDE, k3synth.TINY_RECIPE, 9, 1100, expert_path=_mode(path), d=d,
              check_intermediates=not hot)
 
 
@@ -471,6 +474,8 @@ def test_k3_tier_T1(k3layer):
 
 
 def test_k3_T64_covering(k3layer):
+    """Every expert touched, on the grouped GEMM (auto) and its block-scaled form."""
+    import mxfp4_routed_expert_gb300 as km
     d, lay = k3layer
     shape = k3synth.K3
     d0 = k3synth.with_bias(d, np.zeros(shape.n_experts, np.float32))
@@ -479,13 +484,16 @@ def test_k3_T64_covering(k3layer):
         x, _ = guarded_tokens(shape, d0, 0, 64,
                               make=lambda att: k3synth.covering_tokens(shape, d0, 0, 64,
                                                                        attempts=att))
-        y = lay.forward(x)
-        r = lay.routing(64)
-        assert (r["counts"] > 0).sum() == shape.n_experts       # every expert touched
         ref, tr = oracle.layer_forward(shape, d0, x, trace=True)
-        check_routing(r, shape, x, tr["ids"], tr["w"])
-        assert_close(bf16_to_f64(y), ref, "K3 T=64 covering")
+        for mode in (km.K3MOE_EXPERT_AUTO, km.K3MOE_EXPERT_MX):
+            km.k3moe_set_expert_path(lay.h, mode)
+            y = lay.forward(x)
+            r = lay.routing(64)
+            assert (r["counts"] > 0).sum() == shape.n_experts       # every expert touched
+            check_routing(r, shape, x, tr["ids"], tr["w"])
+            assert_close(bf16_to_f64(y), ref, f"K3 T=64 covering, expert path {mode}")
     finally:
+        km.k3moe_set_expert_path(lay.h, km.K3MOE_EXPERT_AUTO)
         lay.load(0, d)
 
 
@@ -497,7 +505,7 @@ def test_k3_T64_random(k3layer):
     x, _ = guarded_tokens(shape, d, 0, 64, stream=9)
     ref, tr = oracle.layer_forward(shape, d, x, trace=True)
     try:
-        for mode in (km.K3MOE_EXPERT_AUTO, km.K3MOE_EXPERT_GEMV):
+        for mode in (km.K3MOE_EXPERT_AUTO, km.K3MOE_EXPERT_GEMV, km.K3MOE_EXPERT_MX):
             km.k3moe_set_expert_path(lay.h, mode)
             y = lay.forward(x)
             r = lay.routing(64)
@@ -512,7 +520,8 @@ def test_k3_T4096_zipf_prefill(k3layer):
     bias. Ids and the permutation are checked on every token; y against the
     oracle on every 16th token, on every token of the 4 least-picked experts
     (ragged n-tiles) and on 32 tokens of each of the 4 most-picked ones (many
-    n-tiles)."""
+    n-tiles). Both grouped GEMMs: the f16 one (auto) and the block-scaled one."""
+    import mxfp4_routed_expert_gb300 as km
     d, lay = k3layer
     shape = k3synth.K3
     dz = k3synth.with_bias(d, k3synth.zipf_bias(shape, 0, 0, k3synth.K3_ZIPF_ALPHA))
@@ -536,7 +545,12 @@ def test_k3_T4096_zipf_prefill(k3layer):
         rows = np.array(sorted(rows), dtype=np.int32)
         ref = oracle.layer_forward(shape, dz, x, rows=rows)
         assert_close(bf16_to_f64(y)[rows], ref, f"K3 T=4096 Zipf ({rows.size} sampled rows)")
+        km.k3moe_set_expert_path(lay.h, km.K3MOE_EXPERT_MX)
+        y = lay.forward(x)
+        check_routing(lay.routing(T), shape, x, ids, w)
+        assert_close(bf16_to_f64(y)[rows], ref, f"K3 T=4096 Zipf, block-scaled ({rows.size} sampled rows)")
     finally:
+        km.k3moe_set_expert_path(lay.h, km.K3MOE_EXPERT_AUTO)
         lay.load(0, d)
 
 
