@@ -110,10 +110,16 @@ def measured_peaks():
 FP4_NOMINAL_TFLOPS = 13500.0      # dense FP4 tensor peak (nominal), context only
 
 
-def roofline(kernel, model, avg_ms, hbm_peak, tc_peak, peak_src, workload):
+def roofline(kernel, model, avg_ms, hbm_peak, tc_peak, peak_src, workload, mx=False):
     """The dominant kernel against the roof it is closer to: HBM bandwidth for
-    its algorithmic bytes, or the f16/bf16 tensor peak (measured, sustained:
-    the kernel runs inside a long step) for its FLOPs."""
+    its algorithmic bytes, or the tensor peak of its operand types for its
+    FLOPs: the measured sustained bf16 rate (the kernel runs inside a long
+    step) for the f16/bf16 kernels, twice that (the nominal fp8 : bf16 ratio)
+    for the block-scaled expert GEMMs (mx), whose two-term activations run two
+    fp8 MMAs per product, so that their useful rate is at most half of it."""
+    if mx and kernel in ("expert_w13_gemm", "expert_w2_gemm"):
+        tc_peak = 2.0 * tc_peak
+        peak_src = f"2 x {peak_src}"
     if not model:
         return {"kernel": kernel, "bound": "hbm", "achieved": None, "peak": hbm_peak,
                 "unit": "GB/s", "frac": None, "traffic": None}
@@ -125,7 +131,9 @@ def roofline(kernel, model, avg_ms, hbm_peak, tc_peak, peak_src, workload):
     if f_tc > f_hbm:
         roof = {"kernel": kernel, "bound": "tensor", "achieved": round(tfl, 2), "peak": tc_peak,
                 "unit": "TFLOP/s", "frac": round(f_tc, 4),
-                "peak_source": f"{peak_src} bf16_tflops_sustained (the kernel computes f16 x f16 -> f32)"}
+                "peak_source": (f"{peak_src} bf16_tflops_sustained (fp8 rate: e2m1 x e4m3 -> f32, two MMAs "
+                                "per product)" if mx and kernel in ("expert_w13_gemm", "expert_w2_gemm")
+                                else f"{peak_src} bf16_tflops_sustained (the kernel computes f16 x f16 -> f32)")}
     else:
         roof = {"kernel": kernel, "bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak,
                 "unit": "GB/s", "frac": round(f_hbm, 4), "peak_source": f"{peak_src} hbm_gbs"}
@@ -495,6 +503,11 @@ def run_native(args, rank, world):
     touched = (counts_log.cpu().numpy() > 0).sum(1)
     n_touched = float(touched.mean())
     hbm_peak, bf16_peak, bf16_sust, peak_src = measured_peaks()
+    # whether the grouped expert GEMM ran in its block-scaled form (the
+    # library's automatic choice: fewer than 64 pairs per expert on average)
+    P_ = T * shape.topk
+    mx_path = shape.n_experts > 0 and P_ >= 128 and (
+        args.expert_path == "mx" or (args.expert_path == "auto" and T >= 16 and P_ < 64 * shape.n_experts))
     model = kernel_model(shape, T, n_touched)
     tier = None
     if wl.get("tier"):
@@ -522,7 +535,8 @@ def run_native(args, rank, world):
                 "alg_bytes_per_launch": int(model["tier_fill"][0] / 2), "flops_per_launch": 0,
                 "avg_launch_ms": round(avg_ms, 5)}
     else:
-        roof = roofline(dom, model.get(dom), avg_ms, hbm_peak, bf16_sust, peak_src, args.workload)
+        roof = roofline(dom, model.get(dom), avg_ms, hbm_peak, bf16_sust, peak_src, args.workload,
+                        mx=mx_path)
     layers_per_step = 1 if alternate else n_layers
     step_bytes = layer_bytes(shape, T, n_touched) * layers_per_step
     layer_gbs = step_bytes / (ms_per_step / 1e3) / 1e9
@@ -605,6 +619,10 @@ def run_native(args, rank, world):
                    "parallelism": f"replicas x{world}",
                    "l2": "256 MB flush between timed steps; working set > L2",
                    "experts_touched_per_step": n_touched},
+        "expert_gemm": None if shape.n_experts == 0 else
+                       ("block-scaled (kind::mxf8f6f4, two-term MXFP8 activations)" if mx_path else
+                        ("f16 (e2m1 widened on the SM)" if shape.n_experts and T * shape.topk >= 128 and
+                         args.expert_path != "gemv" and (T >= 16 or args.expert_path == "gemm") else "per-pair GEMVs")),
         "hbm_gbs_layer": round(layer_gbs, 1), "hbm_frac_layer": round(layer_gbs / hbm_peak, 4),
         "step_ms": {"median": round(float(np.median(step_times)), 5),
                     "p10": round(float(np.percentile(step_times, 10)), 5),
@@ -614,6 +632,34 @@ def run_native(args, rank, world):
         **({"tier": tier} if tier else {}),
         **({"topp": topp} if topp else {}),
     }
+
+
+# The K3 configurations timed beside the decode T=1 headline, each with at
+# most this many timed steps (a step of the chain is eight layers).
+EXTRA_CONFIGS = (("decode_t64", 30), ("prefill_t4096", 15), ("chain8_t256", 6))
+EXTRA_KEYS = ("value", "unit", "ms_per_step", "steps", "warmup", "expert_gemm", "hbm_gbs_layer", "hbm_frac_layer", "step_ms",
+              "roofline", "kernels", "e2e", "gpu_launches", "clocks", "config")
+
+
+def run_extra_configs(args, rank, world):
+    """The other K3 configurations, each timed like the headline (warm-up,
+    L2 flush between steps, CUDA events, clocks sampled, a profiled second
+    pass for the per-kernel table), in the same process one after another;
+    no CPU baseline (the headline carries it)."""
+    import torch
+    extra = {}
+    for wl, cap in EXTRA_CONFIGS:
+        sub = argparse.Namespace(**vars(args))
+        sub.workload = wl
+        sub.steps = max(5, min(args.steps, cap))
+        sub.no_cpu_baseline = True
+        sub.dump_trace = ""
+        r = run_native(sub, rank, world)
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        if r is not None:
+            extra[wl] = {k: r[k] for k in EXTRA_KEYS if k in r}
+    return extra
 
 
 def run_reference(args, rank, world):
@@ -670,6 +716,9 @@ def main():
     ap.add_argument("--dump-trace", default="",
                     help="write each timed step's layer and expert counts to this .npz (a routing trace "
                          "for python -m mxfp4_routed_expert_gb300.tier_trace)")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="with the default workload, skip the other K3 configurations (decode T=64, "
+                         "prefill T=4096, 8-layer chain) that the line otherwise carries under 'configs'")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -685,6 +734,10 @@ def main():
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
         torch.distributed.init_process_group("nccl")
     out = run_native(args, rank, world)
+    if args.workload == "decode_t1" and not args.no_extra:
+        extra = run_extra_configs(args, rank, world)
+        if out is not None:
+            out["configs"] = extra
     if world > 1:
         import torch
         torch.distributed.destroy_process_group()

@@ -237,12 +237,17 @@ K3MOE_API int k3moe_check_wait_timeout(k3moe *h, void *stream);
 /* Which routed-expert kernels a forward uses (same arithmetic, kimi-k3-in-c
  * README, Part II section 9, k3_moe step 3; results agree to fp32 rounding
  * order and fp16 operand rounding):
- *   K3MOE_EXPERT_AUTO  (default) the grouped tensor-core GEMM when the batch
+ *   K3MOE_EXPERT_AUTO  (default) a grouped tensor-core GEMM when the batch
  *                      holds at least 128 (token, expert) pairs and T >= 16,
- *                      else the per-pair GEMVs;
+ *                      else the per-pair GEMVs; the grouped GEMM is the
+ *                      block-scaled one (K3MOE_EXPERT_MX) while the experts
+ *                      see fewer than 64 pairs each on average, else the f16
+ *                      one (K3MOE_EXPERT_GEMM);
  *   K3MOE_EXPERT_GEMV  always the per-pair GEMVs (streaming dequantisation);
- *   K3MOE_EXPERT_GEMM  the grouped GEMM whenever T * topk >= 128 (below that
- *                      the GEMVs run: its n-tile needs 128 pair rows);
+ *   K3MOE_EXPERT_GEMM  the grouped GEMM with f16 operands (the nibbles and
+ *                      activations widened on the SM) whenever T * topk >= 128
+ *                      (below that the GEMVs run: its n-tile needs 128 pair
+ *                      rows);
  *   K3MOE_EXPERT_MX    the same batches on the grouped GEMM of the
  *                      block-scaled tensor cores (tcgen05 kind::mxf8f6f4):
  *                      the stored e2m1 weights and their ue8m0 scales go to

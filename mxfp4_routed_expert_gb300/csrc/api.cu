@@ -343,7 +343,7 @@ int run_layer(k3moe *h, const LayerDev &w, const __nv_bfloat16 *x, __nv_bfloat16
         }
     }
     if (gemm && cudaStreamWaitEvent(s, h->ev_join, 0) != cudaSuccess) return K3MOE_ERR_CUDA;
-    if (egemm && h->expert_path == K3MOE_EXPERT_MX) {
+    if (egemm && expert_gemm_mx(*h, T)) {
         K3_STEP("expert_tiles", launch_expert_tiles(*h, T, s, true));
         K3_STEP("gather_latent", launch_gather_zq(*h, T, s));
         K3_STEP("expert_w13_gemm", launch_expert_mx(*h, w, T, s, true));

@@ -672,6 +672,20 @@ cudaError_t init_expert_gemm()
 // experts see a few tokens each (narrow accumulators leave TMEM for a third A
 // slot), 64 below 64 pairs (two accumulator sets), else 128 (every converted
 // weight tile then feeds twice the MMA work, with one set).
+// Which grouped GEMM a batch that takes the grouped path runs: the
+// block-scaled one when asked for, or automatically while the experts see
+// fewer than 64 pairs each on average (the weights dominate the bytes each SM
+// takes in, and the block-scaled kernel streams them with no conversion);
+// above that the f16 one, whose operands take fewer bytes per pair (its
+// packed weights are widened in registers, the block-scaled MMA's stay one
+// byte per nibble in shared memory).
+bool expert_gemm_mx(const k3moe &h, int T)
+{
+    if (h.expert_path == K3MOE_EXPERT_MX) return true;
+    if (h.expert_path != K3MOE_EXPERT_AUTO) return false;
+    return (long long)T * h.cfg.topk < 64LL * h.cfg.n_experts;
+}
+
 // The block-scaled path (mx) takes 96 in place of 128: the widest tile for
 // which two W1/W3 accumulator sets and its scale-factor ring fit in TMEM.
 int expert_gemm_bn(const k3moe &h, int T, bool mx)

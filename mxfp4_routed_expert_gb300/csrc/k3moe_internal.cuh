@@ -220,6 +220,8 @@ bool expert_gemm_ok(const k3moe_config &c);
 size_t expert_gemm_max_tiles(const k3moe_config &c);
 int expert_gemm_min_pairs();
 cudaError_t init_expert_gemm();
+// whether a grouped batch of T tokens runs the block-scaled GEMM (else the f16 one)
+bool expert_gemm_mx(const k3moe &h, int T);
 // n-tile width for a batch of T tokens (mx: the block-scaled path's widths)
 int expert_gemm_bn(const k3moe &h, int T, bool mx);
 cudaError_t launch_expert_tiles(const k3moe &h, int T, cudaStream_t s, bool mx);

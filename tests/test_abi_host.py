@@ -42,6 +42,16 @@ def test_every_declared_symbol_is_exported(km):
         assert hasattr(lib, n)
 
 
+def test_library_leaves_no_own_symbol_unresolved(km):
+    """Every function of the library's own namespace is defined inside it: an
+    internal helper left out of a translation unit would otherwise surface
+    only when its first call tries to bind (no GPU needed to see it)."""
+    out = subprocess.run(["nm", "-D", "--undefined-only", "-C", km.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    own = [ln for ln in out.splitlines() if "k3::" in ln or "k3moe" in ln]
+    assert not own, own
+
+
 def test_abi_version_and_strerror(km):
     assert km.k3moe_abi_version() == 1
     for code in range(0, -11, -1):
