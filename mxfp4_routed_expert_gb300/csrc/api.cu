@@ -666,9 +666,9 @@ int k3moe_load_layer(k3moe *h, int layer, const k3moe_layer_weights *w)
                 launch_scale_scan(exd[1], z.e13s, flag, 0) != cudaSuccess ||
                 launch_scale_scan(exd[3], z.e13s, flag, 0) != cudaSuccess ||
                 launch_scale_scan(exd[5], z.e2s, flag, 0) != cudaSuccess ||
-                launch_row_scale_max(exd[1], z.e13m, c.latent / kGroup, exd[6]) != cudaSuccess ||
-                launch_row_scale_max(exd[3], z.e13m, c.latent / kGroup, exd[7]) != cudaSuccess ||
-                launch_row_scale_max(exd[5], z.e2m, c.moe_inter / kGroup, exd[8]) != cudaSuccess ||
+                launch_row_scale_max(exd[0], exd[1], z.e13m, c.latent / kGroup, exd[6]) != cudaSuccess ||
+                launch_row_scale_max(exd[2], exd[3], z.e13m, c.latent / kGroup, exd[7]) != cudaSuccess ||
+                launch_row_scale_max(exd[4], exd[5], z.e2m, c.moe_inter / kGroup, exd[8]) != cudaSuccess ||
                 cudaMemcpy(&bad, flag, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
                 rc = K3MOE_ERR_CUDA;
             else if (bad)

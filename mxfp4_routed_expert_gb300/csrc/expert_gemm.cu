@@ -509,7 +509,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int i = 0; i < NGRP; i++) {
                     uint32_t v[16];
-                    widen_group(w[i], f16x2_pow2((int)((sv4 >> (8 * i)) & 0xffu) - smax), v);
+                    // groups above the row's largest scale hold only zeros (the row
+                    // maximum skips them): any factor <= 1 leaves them zero
+                    widen_group(w[i], f16x2_pow2(min((int)((sv4 >> (8 * i)) & 0xffu) - smax, 0)), v);
                     tmem_st16(tmem + tlane + acol + (uint32_t)(16 * (grp0 + i)), v);
                 }
                 asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
@@ -591,14 +593,25 @@ __global__ void __launch_bounds__(256) k_gather_latent(const __half *z16, const 
 }
 
 // Largest scale byte of every row of an expert matrix stack [rows, G]; load time.
-__global__ void k_row_scale_max(const uint8_t *s, size_t rows, int G, uint8_t *out)
+// Only groups with a nonzero nibble count (magnitude bits 0-2 of either
+// nibble): a group of zeros contributes nothing whatever its scale, so a large
+// scale byte on it must not push the row's real groups below the f16 range.
+// One warp per row; a row without any nonzero nibble gets 0. Load time.
+__global__ void __launch_bounds__(256) k_row_scale_max(const uint8_t *packed, const uint8_t *s, size_t rows, int G,
+                                                       uint8_t *out)
 {
-    const size_t r = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const size_t r = (size_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
     if (r >= rows) return;
-    const uint8_t *p = s + r * (size_t)G;
+    const uint4 *pr = reinterpret_cast<const uint4 *>(packed + r * (size_t)G * 16);
+    const uint8_t *sr = s + r * (size_t)G;
     int m = 0;
-    for (int i = 0; i < G; i++) m = max(m, (int)p[i]);
-    out[r] = (uint8_t)m;
+    for (int i = lane; i < G; i += 32) {
+        const uint4 v = pr[i];
+        if (((v.x | v.y | v.z | v.w) & 0x77777777u) != 0u) m = max(m, (int)sr[i]);
+    }
+    m = (int)__reduce_max_sync(0xffffffffu, (unsigned)m);
+    if (lane == 0) out[r] = (uint8_t)m;
 }
 
 // Packed weights [rows, cols bytes], boxes of box_cols x box_rows with the
@@ -773,9 +786,9 @@ cudaError_t launch_expert_gemm(const k3moe &h, const LayerDev &w, int T, cudaStr
 #undef K3_EG_LAUNCH
 }
 
-cudaError_t launch_row_scale_max(const uint8_t *s, size_t rows, int G, uint8_t *out)
+cudaError_t launch_row_scale_max(const uint8_t *packed, const uint8_t *s, size_t rows, int G, uint8_t *out)
 {
-    k_row_scale_max<<<(unsigned)((rows + 255) / 256), 256>>>(s, rows, G, out);
+    k_row_scale_max<<<(unsigned)((rows + 7) / 8), 256>>>(packed, s, rows, G, out);
     return cudaGetLastError();
 }
 

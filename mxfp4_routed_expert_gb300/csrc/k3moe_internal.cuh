@@ -227,7 +227,8 @@ int expert_gemm_bn(const k3moe &h, int T, bool mx);
 cudaError_t launch_expert_tiles(const k3moe &h, int T, cudaStream_t s, bool mx);
 cudaError_t launch_gather_latent(const k3moe &h, int T, cudaStream_t s);
 cudaError_t launch_expert_gemm(const k3moe &h, const LayerDev &w, int T, cudaStream_t s, bool w13);
-cudaError_t launch_row_scale_max(const uint8_t *s, size_t rows, int G, uint8_t *out);
+// largest scale byte over each row's groups that hold a nonzero nibble
+cudaError_t launch_row_scale_max(const uint8_t *packed, const uint8_t *s, size_t rows, int G, uint8_t *out);
 // The grouped expert GEMM on block-scaled tensor cores (MXFP4 weights x
 // two-term MXFP8 activations): the latent gathered into pair order, then
 // W1/W3 with SiTU (w13) or W2 with the weighted scatter-add.
