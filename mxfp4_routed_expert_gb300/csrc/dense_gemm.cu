@@ -243,7 +243,13 @@ int pick_bn(int T, int mtiles, int sms)
 {
     int bn = (T / 16) * 16;
     if (bn > 256) bn = 256;
-    if (T < 512) return bn;
+    if (T < 512) {
+        // past the split-K range: narrower tiles while the grid would leave
+        // half the SMs idle (the second n-tile reads the weights from L2)
+        if (T > kSplitTokensMax)
+            while (bn > 128 && (long long)mtiles * ((T + bn - 1) / bn) * 2 <= sms) bn = ((bn / 2 + 15) / 16) * 16;
+        return bn;
+    }
     long long best = -1;
     int pick = bn;
     for (int c = bn; c >= 128; c -= 16) {
