@@ -266,9 +266,12 @@ def k3moe_forward_chain(h: int, first_layer: int, n_layers: int, x, y, T: int, s
 
 
 def k3moe_forward_host(h: int, layer: int, x_host, y_host, T: int, stream=None) -> int:
-    return _check(lib().k3moe_forward_host(ctypes.c_void_p(h), layer, _ptr(x_host),
-                                           _ptr(y_host), T, _stream(stream)),
-                  "k3moe_forward_host")
+    """The layer on host buffers (x in, y out); returns once y is written. The
+    per-token decode loop calls it once per token, so its marshalling is kept
+    to the checks the library needs (dense buffers)."""
+    rc = lib().k3moe_forward_host(h, layer, _addr(x_host), _addr(y_host), T,
+                                  stream.cuda_stream if hasattr(stream, "cuda_stream") else stream)
+    return rc if rc == K3MOE_OK else _check(rc, "k3moe_forward_host")
 
 
 def k3moe_get_routing(h: int, ids=None, w=None, counts=None, offsets=None, perm=None,
