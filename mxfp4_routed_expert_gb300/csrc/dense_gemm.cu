@@ -214,15 +214,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncthreads();
         if (last_flag) {
             __threadfence();
-            for (int c = 0; c < g.BN; c++) {
-                const int n = n0 + c;
-                if (row_ok && n < g.T) {
-                    float *pp = &g.part[(size_t)n * 2 * R];
-                    const float v0 = __ldcg(&pp[row]);
-                    const float v1 = dual ? __ldcg(&pp[R + row]) : 0.f;
-                    pp[row] = 0.f;          // leave the partials zeroed for the next launch
-                    if (dual) pp[R + row] = 0.f;
-                    epilogue_store(g, row, n, v0, v1);
+            // 16 columns at a time: all their loads in flight before any use,
+            // so that the tile costs BN / 16 L2 round trips, not BN
+            for (int c = 0; c < g.BN; c += 16) {
+                float v0[16], v1[16];
+#pragma unroll
+                for (int j = 0; j < 16; j++) {
+                    const int n = n0 + c + j;
+                    v0[j] = 0.f;
+                    v1[j] = 0.f;
+                    if (row_ok && n < g.T) {
+                        const float *pp = &g.part[(size_t)n * 2 * R];
+                        v0[j] = __ldcg(&pp[row]);
+                        if (dual) v1[j] = __ldcg(&pp[R + row]);
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < 16; j++) {
+                    const int n = n0 + c + j;
+                    if (row_ok && n < g.T) {
+                        float *pp = &g.part[(size_t)n * 2 * R];
+                        pp[row] = 0.f;          // leave the partials zeroed for the next launch
+                        if (dual) pp[R + row] = 0.f;
+                        epilogue_store(g, row, n, v0[j], v1[j]);
+                    }
                 }
             }
         }
