@@ -125,6 +125,7 @@ size_t carve_workspace(const k3moe_config &c, char *base, Workspace *ws)
     w.h8s = cv.take<uint8_t>(eg ? 2 * Tm * K * I / kGroup : 0);
     w.tiles = cv.take<int2>(eg ? expert_gemm_max_tiles(c) : 0);
     w.n_tiles = cv.take<int>(1);
+    w.eg_ticket = cv.take<int>(eg ? 2 : 0);
     w.perm_hist = cv.take<int>((size_t)perm_chunks(c.max_tokens) * E);
     w.act = cv.take<__nv_bfloat16>(Tm * (L + S));
     w.gemm_part = cv.take<float>(dense_gemm_part_floats(c));

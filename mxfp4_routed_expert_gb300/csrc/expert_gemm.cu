@@ -89,8 +89,9 @@ struct Geo {
     static constexpr int RBYTES = NM * kRawBytes;            // one weight stage [packed W per matrix]
     static constexpr size_t smem(int nb, int nr)
     {
-        return (size_t)nb * BBYTES + (size_t)nr * RBYTES + (size_t)(2 * nb + 2 * nr + NSA + 2 * SETS) * 8 + 16 +
-               1024;
+        return (size_t)nb * BBYTES + (size_t)nr * RBYTES +
+               (size_t)(2 * nb + 2 * nr + NSA + 2 * SETS + 2 * tc::ItemQueue::kQ) * 8 + 16 +
+               4 * tc::ItemQueue::kQ + 1024;
     }
     // activation stages: deep enough to cover an L2 fetch under load (about
     // 2k cycles for a 32 KB stage) at the tensor-bound stage time
@@ -123,6 +124,7 @@ struct EgArgs {
     float *acc;                  // [T, L]
     float b1, b2, ib1, ib2;      // SiTU bounds and their reciprocals
     const int *wslot;            // expert -> index in the weight arrays (nullptr: the expert)
+    int *ticket;                 // items handed out so far (zero at launch)
     int n_ws;                    // experts the weight arrays hold
     int *err;
 };
@@ -302,7 +304,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *aready = wfree + NR;                            // [NSA] A slot written
     uint64_t *tfull = aready + NSA;                           // [kSets] accumulator set complete
     uint64_t *tempty = tfull + kSets;                         // [kSets] epilogue drained it
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(tempty + kSets);
+    tc::ItemQueue iq;                                         // items of this CTA, in order
+    iq.full = tempty + kSets;
+    iq.empty = iq.full + tc::ItemQueue::kQ;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(iq.empty + tc::ItemQueue::kQ);
+    iq.item = reinterpret_cast<int *>(tslot + 4);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
@@ -319,6 +325,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&tfull[i], 2);
             mbar_init(&tempty[i], kSets == 2 ? kEpiWarps : kConvWarps);
         }
+        // the weight producer claims the items; the activation producer, the
+        // two MMA issuers, the converters and (two sets) the epilogue warps read them
+        iq.init(3 + kConvWarps + (kSets == 2 ? kEpiWarps : 0));
         fence_mbar_init();
         tc::prefetch_map(&ra);
         if (DUAL) tc::prefetch_map(&rb);
@@ -349,7 +358,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             int it = 0, slot = 0;
             uint32_t phase = 0;
             bool ok = true;
-            for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+            for (int i = 0; ok; i++) {
+                const int item = wts ? iq.claim(g.ticket, n_items, i, g.err, 630) : iq.read_one(i, g.err, 631);
+                if (item < 0) break;
                 const int tile = item / g.MT, mt = item - tile * g.MT;
                 const int2 td = g.tiles[tile];
                 const int row0 = eg_wslot(g, td.x) * g.R + mt * g.mstep;   // row in the [slots*R, K/2] view
@@ -410,7 +421,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int kk0 = DUAL ? 0 : 4 * q;            // first k-step (of 16 columns)
             constexpr int NK = DUAL ? BK / 16 : BK / 32; // k-steps per k-stage for this issuer
             bool ok = true;
-            for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, local++) {
+            for (; ok; local++) {
+                const int item = iq.read_warp(local, g.err, 632);
+                if (item < 0) break;
                 const int tile = item / g.MT;
                 const int2 td = g.tiles[tile];
                 const int cnt = g.offsets[td.x + 1] - g.offsets[td.x];
@@ -474,7 +487,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // themselves (each warp a quarter of the pair columns of its lane
         // quadrant) right after converting their first k-stage of the next
         // item, whose A slot frees up before the previous item's last MMAs end.
-        for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, local++) {
+        int prev_item = -1;       // the item before this one (its epilogue may still be due)
+        for (; ok; local++) {
+            const int item = iq.read_warp(local, g.err, 633);
+            if (item < 0) break;
             const int tile = item / g.MT, mt = item - tile * g.MT;
             const size_t grow = (size_t)eg_wslot(g, g.tiles[tile].x) * g.R + mt * g.mstep + row + (m ? g.mrow : 0);
             const int smax = m == 0 ? g.ma[grow] : g.mb[grow];
@@ -520,25 +536,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) mbar_arrive(&aready[ap.slot]);
                 if (epi) {
                     epi = false;
-                    if (!epilogue_item<MODE, BN, 64>(g, tmem, item - (int)gridDim.x, local - 1, tfull, tempty,
-                                                     16 * sl)) {
+                    if (!epilogue_item<MODE, BN, 64>(g, tmem, prev_item, local - 1, tfull, tempty, 16 * sl)) {
                         ok = false;
                         break;
                     }
                 }
             }
             if (ok && epi &&   // an item with no k-stage of this warp's parity
-                !epilogue_item<MODE, BN, 64>(g, tmem, item - (int)gridDim.x, local - 1, tfull, tempty, 16 * sl))
+                !epilogue_item<MODE, BN, 64>(g, tmem, prev_item, local - 1, tfull, tempty, 16 * sl))
                 ok = false;
+            prev_item = item;
         }
         if (kSets == 1 && ok && local > 0)
-            epilogue_item<MODE, BN, 64>(g, tmem, blockIdx.x + (local - 1) * (int)gridDim.x, local - 1, tfull, tempty,
-                                        16 * sl);
+            epilogue_item<MODE, BN, 64>(g, tmem, prev_item, local - 1, tfull, tempty, 16 * sl);
     } else if (kSets == 2 && warp >= kEpiWarp0) {
         // ---------------- epilogue (two accumulator sets) ----------------
-        int local = 0;
-        for (int item = blockIdx.x; item < n_items; item += gridDim.x, local++)
-            if (!epilogue_item<MODE, BN, 16>(g, tmem, item, local, tfull, tempty, 0)) break;
+        for (int local = 0;; local++) {
+            const int item = iq.read_warp(local, g.err, 634);
+            if (item < 0 || !epilogue_item<MODE, BN, 16>(g, tmem, item, local, tfull, tempty, 0)) break;
+        }
     }
 
     tc::fence_before();
@@ -550,8 +566,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // n-tiles of at most bn pairs: (expert, j) for j < ceil(count_e / bn),
-// experts ascending. One block.
-__global__ void __launch_bounds__(1024) k_expert_tiles(const int *counts, int E, int bn, int2 *tiles, int *n_tiles)
+// experts ascending; also zeroes the grouped GEMMs' item counters. One block.
+__global__ void __launch_bounds__(1024) k_expert_tiles(const int *counts, int E, int bn, int2 *tiles, int *n_tiles,
+                                                      int *ticket)
 {
     __shared__ int wsum[32];
     pdl_launch_dependents();
@@ -574,7 +591,11 @@ __global__ void __launch_bounds__(1024) k_expert_tiles(const int *counts, int E,
     }
     const int first = base + incl - nt;
     for (int j = 0; j < nt; j++) tiles[first + j] = make_int2(e, j);
-    if (threadIdx.x == 0) *n_tiles = total;
+    if (threadIdx.x == 0) {
+        *n_tiles = total;
+        ticket[0] = 0;   // the two grouped GEMM launches that follow hand out items from 0
+        ticket[1] = 0;
+    }
 }
 
 // zp[p] = z16[token of pair p] (L values and the exponent padding); one warp per pair.
@@ -710,7 +731,7 @@ int expert_gemm_bn(const k3moe &h, int T, bool mx)
 cudaError_t launch_expert_tiles(const k3moe &h, int T, cudaStream_t s, bool mx)
 {
     return launch_pdl(k_expert_tiles, 1, 1024, 0, s, (const int *)h.ws.counts, h.cfg.n_experts,
-                      expert_gemm_bn(h, T, mx), h.ws.tiles, h.ws.n_tiles);
+                      expert_gemm_bn(h, T, mx), h.ws.tiles, h.ws.n_tiles, h.ws.eg_ticket);
 }
 
 cudaError_t launch_gather_latent(const k3moe &h, int T, cudaStream_t s)
@@ -745,6 +766,7 @@ cudaError_t launch_expert_gemm(const k3moe &h, const LayerDev &w, int T, cudaStr
     g.ib1 = 1.f / c.situ_b1;
     g.ib2 = 1.f / c.situ_b2;
     g.err = h.ws.err;
+    g.ticket = h.ws.eg_ticket + (w13 ? 0 : 1);
     g.wslot = w.wslot;
     g.n_ws = w.n_wslots;
     g.K = w13 ? c.latent : c.moe_inter;

@@ -99,7 +99,7 @@ struct MxGeo {
     static_assert(SF0 + kSfSlots * kSfCols <= kTmemCols, "tensor memory");
     static_assert(SMEM <= (size_t)kSmemBudget && NAS >= 3, "shared memory");
     static_assert(D >= NBS, "stage barriers cover every ring");
-    static_assert((2 * D + 4) * 8 + 16 <= 512, "barriers");
+    static_assert((2 * D + 4 + 2 * tc::ItemQueue::kQ) * 8 + 16 + 4 * tc::ItemQueue::kQ <= 512, "barriers");
 };
 
 struct MxArgs {
@@ -118,6 +118,7 @@ struct MxArgs {
     float b1, b2, ib1, ib2;      // SiTU bounds and their reciprocals
     const int *wslot;            // expert -> index in the weight arrays (nullptr: the expert)
     int n_ws;
+    int *ticket;                 // items handed out so far (zero at launch)
     int *err;
 };
 
@@ -304,7 +305,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *done = ready + D;
     uint64_t *tfull = done + D;                                  // [2] accumulator set complete
     uint64_t *tempty = tfull + 2;                                // [2] epilogue drained it
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(tempty + 2);
+    tc::ItemQueue iq;                                            // items of this CTA, in order
+    iq.full = tempty + 2;
+    iq.empty = iq.full + tc::ItemQueue::kQ;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(iq.empty + tc::ItemQueue::kQ);
+    iq.item = reinterpret_cast<int *>(tslot + 4);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
@@ -316,6 +321,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&tfull[i], 1);
             mbar_init(&tempty[i], 8);
         }
+        // the weight producer claims the items; the activation producer, the
+        // MMA warp, the eight scale writers and the eight epilogue warps read them
+        iq.init(18);
         fence_mbar_init();
         tc::prefetch_map(&ra);
         if (NA == 2) tc::prefetch_map(&rb);
@@ -341,7 +349,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int depth = wts ? NAS : NBS;
             int st = 0;
             bool ok = true;
-            for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+            for (int i = 0; ok; i++) {
+                const int item = wts ? iq.claim(g.ticket, n_items, i, g.err, 730) : iq.read_one(i, g.err, 731);
+                if (item < 0) break;
                 const MxItem m = mx_item<BN>(g, item);
                 // activation rows: up to 32 pairs in 16-row boxes, else one box of
                 // 64 or BN rows (rows past the tile's pairs are never used)
@@ -384,7 +394,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         const uint64_t da0 = tc::desc_sw128(tc::su32(aring));
         const uint64_t db0 = tc::desc_sw128(tc::su32(bring));
-        for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, local++) {
+        for (; ok; local++) {
+            const int item = iq.read_warp(local, g.err, 732);
+            if (item < 0) break;
             const MxItem m = mx_item<BN>(g, item);
             const int n = ((m.nv + 15) / 16) * 16;
             const int b = local % SETS;
@@ -432,7 +444,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int par = warp >= kWriter2Warp0 ? 1 : 0;
         int st = 0;
         bool ok = true;
-        for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+        for (int i = 0; ok; i++) {
+            const int item = iq.read_warp(i, g.err, 733);
+            if (item < 0) break;
             const MxItem m = mx_item<BN>(g, item);
             const uint8_t *arow0 = g.sa + (size_t)(m.row0 + lane) * G;
             const uint8_t *arow1 = g.sb + (size_t)(m.row0 + g.mrow + lane) * G;
@@ -476,7 +490,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tl = (uint32_t)(q * 32) << 16;
         constexpr int CH = ((BN / 2 + 15) / 16) * 16;   // pair columns per half, whole chunks of 16
         int local = 0;
-        for (int item = blockIdx.x; item < n_items; item += gridDim.x, local++) {
+        for (;; local++) {
+            const int item = iq.read_warp(local, g.err, 734);
+            if (item < 0) break;
             const MxItem m = mx_item<BN>(g, item);
             const int b = local % SETS;
             if (!mbar_wait(&tfull[b], (uint32_t)(local / SETS) & 1u, g.err, 708)) break;
@@ -609,6 +625,7 @@ cudaError_t launch_expert_mx(const k3moe &h, const LayerDev &w, int T, cudaStrea
     g.wslot = w.wslot;
     g.n_ws = w.n_wslots;
     g.err = h.ws.err;
+    g.ticket = h.ws.eg_ticket + (w13 ? 0 : 1);
     g.K = w13 ? c.latent : c.moe_inter;
     g.R = w13 ? c.moe_inter : c.latent;
     // W2 takes two adjacent m-tiles per item when its rows allow it

@@ -132,6 +132,8 @@ struct Workspace {
     int2 *tiles = nullptr;        // (expert, n-tile) list of the expert GEMM
     int *perm_hist = nullptr;     // [ceil(Tm/32), E] per-chunk expert counts, then chunk bases
     int *n_tiles = nullptr;       // length of the list
+    int *eg_ticket = nullptr;     // [2] items handed out so far by the W1/W3 and the W2 grouped
+                                  //   GEMM launch (zeroed with the tile list)
     __nv_bfloat16 *act = nullptr;     // [Tm, L+S] bf16 [normed latent | shared SiTU] (GEMM path)
     float *gemm_part = nullptr;       // split-K partial sums (kept zeroed between launches)
     int *gemm_tiles = nullptr;        // split-K arrival counters (kept at zero)

@@ -195,5 +195,57 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, int *e
     return __all_sync(0xffffffffu, ok) != 0;
 }
 
+// Work items handed out at run time. One thread of the CTA (the writer)
+// claims the next item number from a counter in global memory that every CTA
+// of the launch shares, when it is ready to start that item, and publishes it
+// to the CTA's other roles through a ring of kQ entries in shared memory; -1
+// ends the sequence. An SM that HBM
+// serves faster than another thereby takes more items, instead of every SM
+// taking a fixed share. Every role reads the same sequence, entry i at the
+// start of its i-th item, and each reading warp frees the entry once it has
+// read it; the writer refills an entry only after all of them have, and it
+// runs less than one item ahead of the roles it feeds, so the ring never
+// holds it up for long. Waits are bounded as everywhere else.
+struct ItemQueue {
+    static constexpr int kQ = 4;
+    int *item;              // [kQ] in shared memory
+    uint64_t *full, *empty; // [kQ] each: full by the writer, empty by the readers
+    __device__ __forceinline__ void init(int readers)
+    {
+        for (int i = 0; i < kQ; i++) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], (uint32_t)readers);
+        }
+    }
+    // writer: claims the CTA's i-th item (-1 once the counter has passed n)
+    __device__ __forceinline__ int claim(int *counter, int n, int i, int *err, int where)
+    {
+        const int v = atomicAdd(counter, 1);
+        const int it = v < n ? v : -1;
+        if (!mbar_wait(&empty[i % kQ], ((uint32_t)(i / kQ) & 1u) ^ 1u, err, where)) return -1;
+        item[i % kQ] = it;
+        mbar_arrive(&full[i % kQ]);
+        return it;
+    }
+    // a reading warp (every lane gets the item; lane 0 frees the entry);
+    // -1 at the end of the sequence or after a time-out
+    __device__ __forceinline__ int read_warp(int i, int *err, int where)
+    {
+        if (!warp_wait(&full[i % kQ], (uint32_t)(i / kQ) & 1u, err, where)) return -1;
+        const int it = *reinterpret_cast<volatile int *>(&item[i % kQ]);
+        __syncwarp();
+        if ((threadIdx.x & 31) == 0) mbar_arrive(&empty[i % kQ]);
+        return it;
+    }
+    // a reading thread that stands for its warp (the warp's other lanes do not read)
+    __device__ __forceinline__ int read_one(int i, int *err, int where)
+    {
+        if (!mbar_wait(&full[i % kQ], (uint32_t)(i / kQ) & 1u, err, where)) return -1;
+        const int it = *reinterpret_cast<volatile int *>(&item[i % kQ]);
+        mbar_arrive(&empty[i % kQ]);
+        return it;
+    }
+};
+
 }  // namespace tc
 }  // namespace k3
