@@ -260,9 +260,9 @@ int pick_bn(int T, int mtiles, int sms)
     if (bn > 256) bn = 256;
     if (T < 512) {
         // past the split-K range: narrower tiles while the grid would leave
-        // half the SMs idle (the second n-tile reads the weights from L2)
+        // half the SMs idle (the other n-tiles read the weights from L2)
         if (T > kSplitTokensMax)
-            while (bn > 128 && (long long)mtiles * ((T + bn - 1) / bn) * 2 <= sms) bn = ((bn / 2 + 15) / 16) * 16;
+            while (bn > 64 && (long long)mtiles * ((T + bn - 1) / bn) * 2 <= sms) bn = ((bn / 2 + 15) / 16) * 16;
         return bn;
     }
     long long best = -1;
