@@ -114,18 +114,20 @@ size_t carve_workspace(const k3moe_config &c, char *base, Workspace *ws)
     w.n_touched = cv.take<int>(1);
     w.h16 = cv.take<__half>(Tm * K * I);
     w.acc = cv.take<float>(Tm * L);
-    const bool eg = expert_gemm_ok(c);
+    const bool eg = expert_gemm_ok(c), mx = expert_mx_ok(c);
     w.zperm = cv.take<__half>(eg ? Tm * K * (L + kZPad) : 0);
     // two-term MXFP8 activations of the block-scaled grouped expert path
-    w.zq = cv.take<uint8_t>(eg ? 2 * Tm * L : 0);
-    w.zqs = cv.take<uint8_t>(eg ? 2 * Tm * L / kGroup : 0);
-    w.zp8 = cv.take<uint8_t>(eg ? 2 * Tm * K * L : 0);
-    w.zps = cv.take<uint8_t>(eg ? 2 * Tm * K * L / kGroup : 0);
-    w.h8 = cv.take<uint8_t>(eg ? 2 * Tm * K * I : 0);
-    w.h8s = cv.take<uint8_t>(eg ? 2 * Tm * K * I / kGroup : 0);
-    w.tiles = cv.take<int2>(eg ? expert_gemm_max_tiles(c) : 0);
+    w.zq = cv.take<uint8_t>(mx ? 2 * Tm * L : 0);
+    w.zqs = cv.take<uint8_t>(mx ? 2 * Tm * L / kGroup : 0);
+    w.zp8 = cv.take<uint8_t>(mx ? 2 * Tm * K * L : 0);
+    w.zps = cv.take<uint8_t>(mx ? 2 * Tm * K * L / kGroup : 0);
+    w.h8 = cv.take<uint8_t>(mx ? 2 * Tm * K * I : 0);
+    w.h8s = cv.take<uint8_t>(mx ? 2 * Tm * K * I / kGroup : 0);
+    w.tiles = cv.take<int2>(mx ? expert_gemm_max_tiles(c) : 0);
     w.n_tiles = cv.take<int>(1);
-    w.eg_ticket = cv.take<int>(eg ? 2 : 0);
+    w.eg_ticket = cv.take<int>(mx ? 2 : 0);
+    w.gu = cv.take<float>(mx ? std::min<size_t>(Tm * K, kSplitPairsMax) * 2 * I : 0);
+    w.gu_cnt = cv.take<int>(mx ? expert_gemm_max_tiles(c) * (I / 128) : 0);
     w.perm_hist = cv.take<int>((size_t)perm_chunks(c.max_tokens) * E);
     w.act = cv.take<__nv_bfloat16>(Tm * (L + S));
     w.gemm_part = cv.take<float>(dense_gemm_part_floats(c));
@@ -354,6 +356,11 @@ int run_layer(k3moe *h, const LayerDev &w, const __nv_bfloat16 *x, __nv_bfloat16
         K3_STEP("gather_latent", launch_gather_latent(*h, T, s));
         K3_STEP("expert_w13_gemm", launch_expert_gemm(*h, w, T, s, true));
         K3_STEP("expert_w2_gemm", launch_expert_gemm(*h, w, T, s, false));
+    } else if (use_expert_split(*h, T)) {
+        K3_STEP("expert_tiles", launch_expert_tiles(*h, T, s, true));
+        K3_STEP("gather_latent", launch_gather_zq(*h, T, s));
+        K3_STEP("expert_w13_gemm", launch_expert_mx(*h, w, T, s, true));
+        K3_STEP("expert_w2_gemm", launch_expert_mx(*h, w, T, s, false));
     } else {
         K3_STEP("expert_w13_gemv", launch_expert_w13(*h, w, T, s));
         K3_STEP("expert_w2_gemv", launch_expert_w2(*h, w, T, s));
@@ -520,6 +527,7 @@ int k3moe_create(const k3moe_config *cfg, k3moe **out)
                                 : (cfg->n_experts >= 128 && cfg->latent >= 128 && cfg->shared_inter >= 128 &&
                                    cfg->hidden >= 128);
     h->egemm_ok = expert_gemm_ok(*cfg);
+    h->mx_ok = expert_mx_ok(*cfg);
     try {
         h->layers.resize((size_t)cfg->max_layers);
     } catch (const std::bad_alloc &) {   // no C++ exception crosses the C ABI
@@ -944,7 +952,8 @@ int k3moe_set_expert_path(k3moe *h, int mode)
     if (mode != K3MOE_EXPERT_AUTO && mode != K3MOE_EXPERT_GEMV && mode != K3MOE_EXPERT_GEMM &&
         mode != K3MOE_EXPERT_MX)
         return K3MOE_ERR_INVALID_ARG;
-    if ((mode == K3MOE_EXPERT_GEMM || mode == K3MOE_EXPERT_MX) && !h->egemm_ok) return K3MOE_ERR_SHAPE;
+    if (mode == K3MOE_EXPERT_GEMM && !h->egemm_ok) return K3MOE_ERR_SHAPE;
+    if (mode == K3MOE_EXPERT_MX && !h->mx_ok) return K3MOE_ERR_SHAPE;
     h->expert_path = mode;
     return K3MOE_OK;
 }

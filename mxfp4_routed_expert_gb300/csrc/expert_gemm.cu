@@ -674,6 +674,12 @@ bool expert_gemm_ok(const k3moe_config &c)
            (long long)c.max_tokens * c.topk >= kMinPairs;
 }
 
+bool expert_mx_ok(const k3moe_config &c)
+{
+    return c.latent > 0 && c.moe_inter > 0 && c.latent % BK == 0 && c.moe_inter % BK == 0 &&
+           c.latent % BM == 0 && c.moe_inter % BM == 0;
+}
+
 size_t expert_gemm_max_tiles(const k3moe_config &c)
 {
     return (size_t)((long long)c.max_tokens * c.topk / 32 + c.n_experts + 1);   // the narrowest n-tile
@@ -706,6 +712,12 @@ cudaError_t init_expert_gemm()
 // experts see a few tokens each (narrow accumulators leave TMEM for a third A
 // slot), 64 below 64 pairs (two accumulator sets), else 128 (every converted
 // weight tile then feeds twice the MMA work, with one set).
+bool use_expert_split(const k3moe &h, int T)
+{
+    const long long pairs = (long long)T * h.cfg.topk;
+    return h.mx_ok && h.expert_path == K3MOE_EXPERT_MX && pairs < kMinPairs && pairs <= kSplitPairsMax;
+}
+
 // Which grouped GEMM a batch that takes the grouped path runs: the
 // block-scaled one when asked for, or automatically while the experts see
 // fewer than 64 pairs each on average (the weights dominate the bytes each SM

@@ -119,6 +119,13 @@ struct MxArgs {
     const int *wslot;            // expert -> index in the weight arrays (nullptr: the expert)
     int n_ws;
     int *ticket;                 // items handed out so far (zero at launch)
+    // K split over KS items (small batches): an item is (n-tile, m-tile, K
+    // range). W2 items add their partial products into acc like whole ones;
+    // W1/W3 items add their partial gate and up sums into gu, and the last of
+    // the 8 * KS epilogue warps of an (n-tile, m-tile) applies SiTU
+    int KS;
+    float *gu;                   // [pairs][2][I] partial W1 and W3 sums (zero between launches)
+    int *gu_cnt;                 // [n-tiles * MT] epilogue warps arrived (zero between launches)
     int *err;
 };
 
@@ -280,6 +287,67 @@ __device__ __forceinline__ void mx_epilogue(const MxArgs &g, const MxItem &m, ui
     }
 }
 
+// W1/W3 epilogue of one warp of an item whose K range is a part of the
+// whole: its lane quadrant's rows x the pair columns [c_lo, c_hi) of the
+// partial gate and up sums are added into g.gu. The warp that completes the
+// (n-tile, m-tile)'s 8 * KS arrivals then finishes the whole tile from g.gu:
+// SiTU, h in two-term MXFP8 (one scale group = 32 rows of one pair, one warp
+// at a time), g.gu and the counter left zeroed for the next launch.
+template <int BN>
+__device__ __forceinline__ void mx_epilogue_split(const MxArgs &g, const MxItem &m, int base, uint32_t tacc, int q,
+                                                  int c_lo, int c_hi)
+{
+    const int lane = threadIdx.x & 31;
+    const int row = m.mt * g.mstep + q * 32 + lane;
+    for (int c0 = c_lo; c0 < c_hi && c0 < m.nv; c0 += 16) {
+        float v0[16], v1[16];
+        tc::tmem_ld16(tacc + (uint32_t)c0, v0);
+        tc::tmem_ld16(tacc + (uint32_t)(BN + c0), v1);
+#pragma unroll
+        for (int j = 0; j < 16; j++) {
+            if (c0 + j < m.nv) {
+                float *gp = g.gu + (size_t)(m.pair0 + c0 + j) * 2 * g.I + row;
+                atomicAdd(gp, v0[j]);
+                atomicAdd(gp + g.I, v1[j]);
+            }
+        }
+    }
+    __threadfence();
+    __syncwarp();
+    int last = 0;
+    if (lane == 0) last = atomicAdd(&g.gu_cnt[base], 1) == 8 * g.KS - 1;
+    if (!__shfl_sync(0xffffffffu, last, 0)) return;
+    __threadfence();
+    const size_t gs = (size_t)g.I / kGroup;
+    for (int c = 0; c < m.nv; c++) {
+        const int p = m.pair0 + c;
+        float gv[4], uv[4];
+#pragma unroll
+        for (int grp = 0; grp < 4; grp++) {          // the tile's 128 rows: four scale groups
+            const float *gp = g.gu + (size_t)p * 2 * g.I + m.mt * g.mstep + grp * 32 + lane;
+            gv[grp] = __ldcg(gp);
+            uv[grp] = __ldcg(gp + g.I);
+        }
+#pragma unroll
+        for (int grp = 0; grp < 4; grp++) {
+            const int r = m.mt * g.mstep + grp * 32 + lane;
+            float *gp = g.gu + (size_t)p * 2 * g.I + r;
+            gp[0] = 0.f;
+            gp[g.I] = 0.f;
+            uint32_t qh, ql;
+            int eh, el;
+            mx8_hilo(situ_hw(gv[grp], uv[grp], g.b1, g.b2, g.ib1, g.ib2), qh, ql, eh, el);
+            g.h8[(size_t)p * g.I + r] = (uint8_t)qh;
+            g.h8[((size_t)g.P + p) * g.I + r] = (uint8_t)ql;
+            if (lane == 0) {
+                g.h8s[(size_t)p * gs + r / kGroup] = (uint8_t)(eh + 127);
+                g.h8s[((size_t)g.P + p) * gs + r / kGroup] = (uint8_t)(el + 127);
+            }
+        }
+    }
+    if (lane == 0) g.gu_cnt[base] = 0;
+}
+
 template <int MODE, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     k_expert_mx(const __grid_constant__ CUtensorMap ra, const __grid_constant__ CUtensorMap rb,
@@ -338,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     pdl_launch_dependents();
     pdl_wait();
     const uint32_t tmem = *tslot;
-    const int n_items = *g.n_tiles * g.MT;
+    const int n_items = *g.n_tiles * g.MT * g.KS;
     const int KT = g.K / BK;
     const int G = g.K / kGroup;
 
@@ -352,7 +420,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; ok; i++) {
                 const int item = wts ? iq.claim(g.ticket, n_items, i, g.err, 730) : iq.read_one(i, g.err, 731);
                 if (item < 0) break;
-                const MxItem m = mx_item<BN>(g, item);
+                const int base = item / g.KS, ks = item - base * g.KS;   // (n-tile, m-tile), K part
+                const MxItem m = mx_item<BN>(g, base);
+                const int kt0 = KT * ks / g.KS, kt1 = KT * (ks + 1) / g.KS;
                 // activation rows: up to 32 pairs in 16-row boxes, else one box of
                 // 64 or BN rows (rows past the tile's pairs are never used)
                 const int nb = m.nv <= 32 ? (m.nv + kBoxRows - 1) / kBoxRows : 1;
@@ -360,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const CUtensorMap *bmap = m.nv <= 32 ? &b16 : (m.nv <= 64 ? &b64 : &bfull_map);
                 // a 4-bit tile counts its packed bytes
                 const uint32_t tx = wts ? (uint32_t)(NA * BM * 64) : (uint32_t)(2 * brows * 128);
-                for (int kt = 0; kt < KT; kt++, st++) {
+                for (int kt = kt0; kt < kt1; kt++, st++) {
                     if (st >= depth && !mbar_wait(&done[(st - depth) % D], (uint32_t)((st - depth) / D) & 1u, g.err,
                                                   wts ? 700 : 701)) {
                         ok = false;
@@ -397,13 +467,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (; ok; local++) {
             const int item = iq.read_warp(local, g.err, 732);
             if (item < 0) break;
-            const MxItem m = mx_item<BN>(g, item);
+            const int base = item / g.KS, ks = item - base * g.KS;   // (n-tile, m-tile), K part
+            const MxItem m = mx_item<BN>(g, base);
+            const int kt0 = KT * ks / g.KS, kt1 = KT * (ks + 1) / g.KS;
             const int n = ((m.nv + 15) / 16) * 16;
             const int b = local % SETS;
             if (!tc::warp_wait(&tempty[b], ((uint32_t)(local / SETS) & 1u) ^ 1u, g.err, 703)) break;
             tc::fence_after();
             const uint32_t d = tmem + (uint32_t)b * GE::SET_COLS;
-            for (int kt = 0; kt < KT; kt++, st++) {
+            for (int kt = kt0; kt < kt1; kt++, st++) {
                 if (!tc::warp_wait(&ready[st % D], (uint32_t)(st / D) & 1u, g.err, 704)) {
                     ok = false;
                     break;
@@ -420,7 +492,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int a = 0; a < NA; a++) {   // hi term (A kept), then lo term
                             const uint32_t da_ = d + (uint32_t)(a * BN);
                             const uint64_t aa = da + (uint64_t)((a * BM * 128) >> 4) + 2 * j;
-                            mma_mx<1>(da_, aa, db + 2 * j, id, sf + 4 * a, sf + 8, (kt > 0 || j > 0) ? 1u : 0u);
+                            mma_mx<1>(da_, aa, db + 2 * j, id, sf + 4 * a, sf + 8, (kt > kt0 || j > 0) ? 1u : 0u);
                             mma_mx<2>(da_, aa, db + (uint64_t)(GE::BHALF >> 4) + 2 * j, id, sf + 4 * a, sf + 12, 1u);
                         }
                     }
@@ -447,10 +519,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; ok; i++) {
             const int item = iq.read_warp(i, g.err, 733);
             if (item < 0) break;
-            const MxItem m = mx_item<BN>(g, item);
+            const int base = item / g.KS, ks = item - base * g.KS;   // (n-tile, m-tile), K part
+            const MxItem m = mx_item<BN>(g, base);
+            const int kt0 = KT * ks / g.KS, kt1 = KT * (ks + 1) / g.KS;
             const uint8_t *arow0 = g.sa + (size_t)(m.row0 + lane) * G;
             const uint8_t *arow1 = g.sb + (size_t)(m.row0 + g.mrow + lane) * G;
-            for (int kt = 0; kt < KT; kt++, st++) {
+            for (int kt = kt0; kt < kt1; kt++, st++) {
                 if ((st & 1) != par) continue;
                 uint32_t wa[2][4], hb[2][4];
 #pragma unroll
@@ -493,12 +567,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (;; local++) {
             const int item = iq.read_warp(local, g.err, 734);
             if (item < 0) break;
-            const MxItem m = mx_item<BN>(g, item);
+            const int base = item / g.KS;                            // (n-tile, m-tile)
+            const MxItem m = mx_item<BN>(g, base);
             const int b = local % SETS;
             if (!mbar_wait(&tfull[b], (uint32_t)(local / SETS) & 1u, g.err, 708)) break;
             tc::fence_after();
-            mx_epilogue<MODE, BN>(g, m, tmem + tl + (uint32_t)b * GE::SET_COLS, q, half * CH,
-                                  min(BN, (half + 1) * CH), estage + (warp - kEpiWarp0) * 1024);
+            if (MODE == kW13 && g.KS > 1)
+                mx_epilogue_split<BN>(g, m, base, tmem + tl + (uint32_t)b * GE::SET_COLS, q, half * CH,
+                                      min(BN, (half + 1) * CH));
+            else
+                mx_epilogue<MODE, BN>(g, m, tmem + tl + (uint32_t)b * GE::SET_COLS, q, half * CH,
+                                      min(BN, (half + 1) * CH), estage + (warp - kEpiWarp0) * 1024);
             tc::fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty[b]);
@@ -604,7 +683,8 @@ cudaError_t launch_expert_mx(const k3moe &h, const LayerDev &w, int T, cudaStrea
     const k3moe_config &c = h.cfg;
     const int pairs = T * c.topk;
     const int bn = expert_gemm_bn(h, T, true);   // the width the tile list was built for
-    if (pairs < expert_gemm_min_pairs()) return cudaErrorInvalidValue;
+    const bool split = pairs < expert_gemm_min_pairs();
+    if (split && (pairs > kSplitPairsMax || !use_expert_split(h, T))) return cudaErrorInvalidValue;
     MxArgs g = {};
     g.P = c.max_tokens * c.topk;
     g.k = c.topk;
@@ -633,6 +713,19 @@ cudaError_t launch_expert_mx(const k3moe &h, const LayerDev &w, int T, cudaStrea
     g.mstep = mode == kW2Pair ? 2 * BM : BM;
     g.mrow = mode == kW2Pair ? BM : 0;
     g.MT = g.R / g.mstep;
+    // K split for small batches: about two items per SM, counting one n-tile
+    // per pair (the most a batch of few pairs per expert has). Measured at K3
+    // T = 1 (16 pairs): W1/W3 55 / 61 / 70 us with 1 / 2 / 4 parts per item,
+    // W2 31 / 29 / 33 us with 1 / 2 / 6 parts; every item part carries a
+    // fixed cost (its scale words, its accumulator hand-off, the partial sums)
+    g.KS = 1;
+    if (split) {
+        const long long whole = (long long)pairs * g.MT;
+        const long long want = (2LL * h.sm_count + whole - 1) / whole;
+        g.KS = (int)std::max<long long>(1, std::min<long long>(want, g.K / BK));
+    }
+    g.gu = h.ws.gu;
+    g.gu_cnt = h.ws.gu_cnt;
     const uint64_t rows = (uint64_t)w.n_wslots * g.R;
     const uint8_t *act = w13 ? h.ws.zp8 : h.ws.h8;
     g.bs = w13 ? h.ws.zps : h.ws.h8s;

@@ -134,6 +134,8 @@ struct Workspace {
     int *n_tiles = nullptr;       // length of the list
     int *eg_ticket = nullptr;     // [2] items handed out so far by the W1/W3 and the W2 grouped
                                   //   GEMM launch (zeroed with the tile list)
+    float *gu = nullptr;          // [min(Tm*k, kSplitPairsMax), 2, I] K-split W1/W3 partial sums (kept zeroed)
+    int *gu_cnt = nullptr;        // [max tiles * I/128] their arrival counters (kept at zero)
     __nv_bfloat16 *act = nullptr;     // [Tm, L+S] bf16 [normed latent | shared SiTU] (GEMM path)
     float *gemm_part = nullptr;       // split-K partial sums (kept zeroed between launches)
     int *gemm_tiles = nullptr;        // split-K arrival counters (kept at zero)
@@ -167,6 +169,7 @@ struct k3moe {
     bool dense_tma_ok[2] = {false, false};   // TMA-fed dense GEMVs usable for T = 1, 2
     bool gemm_ok = false;                    // tensor-core dense GEMMs usable (T >= 16)
     bool egemm_ok = false;                   // tensor-core expert GEMM usable (shape)
+    bool mx_ok = false;                      // block-scaled expert path usable at any batch (shape)
     int expert_path = K3MOE_EXPERT_AUTO;     // k3moe_set_expert_path
     k3::TierDev tier;                        // k3moe_set_expert_tier
     float topp = 0.f;                        // k3moe_set_topp (0: keep every pick)
@@ -220,10 +223,16 @@ cudaError_t launch_norm_act(const k3moe &h, const LayerDev &w, int T, cudaStream
 // latent gathered into pair order, then W1/W3 (w13) or W2.
 bool expert_gemm_ok(const k3moe_config &c);
 size_t expert_gemm_max_tiles(const k3moe_config &c);
+// the block-scaled grouped GEMM's shapes (weight rows and widths in whole tiles)
+bool expert_mx_ok(const k3moe_config &c);
 int expert_gemm_min_pairs();
 cudaError_t init_expert_gemm();
 // whether a grouped batch of T tokens runs the block-scaled GEMM (else the f16 one)
 bool expert_gemm_mx(const k3moe &h, int T);
+// Batches below the grouped GEMMs' smallest (decode): the block-scaled grouped
+// GEMM with each item's K range split (true), or the per-pair GEMVs (false)
+bool use_expert_split(const k3moe &h, int T);
+constexpr int kSplitPairsMax = 256;   // largest batch (pairs) the K-split path takes
 // n-tile width for a batch of T tokens (mx: the block-scaled path's widths)
 int expert_gemm_bn(const k3moe &h, int T, bool mx);
 cudaError_t launch_expert_tiles(const k3moe &h, int T, cudaStream_t s, bool mx);

@@ -46,7 +46,8 @@ static RouteArgs route_args(const k3moe &h, const LayerDev &w, int T)
     a.z = h.ws.z;
     a.z16 = h.ws.z16;
     // the block-scaled grouped expert path reads z in two-term MXFP8
-    const bool mx = h.egemm_ok && expert_gemm_mx(h, T) && T * c.topk >= expert_gemm_min_pairs();
+    const bool mx = (h.egemm_ok && expert_gemm_mx(h, T) && T * c.topk >= expert_gemm_min_pairs()) ||
+                    use_expert_split(h, T);
     a.zq = mx ? h.ws.zq : nullptr;
     a.zqs = mx ? h.ws.zqs : nullptr;
     a.zq_rows = c.max_tokens;

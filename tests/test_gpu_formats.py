@@ -68,10 +68,11 @@ def edge_layer(seed):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("path", ["gemv", "gemm", "mx"])
-def test_scale_edges_every_path(built, path):
+@pytest.mark.parametrize("path,T", [("gemv", 48), ("gemm", 48), ("mx", 48), ("mx", 8)])
+def test_scale_edges_every_path(built, path, T):
+    """T = 8 (64 pairs) runs the block-scaled kernel with split K ranges."""
     d = edge_layer(21)
-    run_case(WIDE, k3synth.TINY_RECIPE, 21, 48, expert_path=_mode(path), d=d)
+    run_case(WIDE, k3synth.TINY_RECIPE, 21, T, expert_path=_mode(path), d=d)
 
 
 def test_edge_layer_has_the_edges():

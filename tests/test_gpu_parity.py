@@ -84,6 +84,18 @@ def test_expert_paths(T, path):
     run_case(WIDE, k3synth.TINY_RECIPE, 6, T, expert_path=_mode(path))
 
 
+@pytest.mark.parametrize("shape,T", [("tiny", 1), ("tiny", 4), ("mid", 1), ("mid", 5), ("wide", 1),
+                                     ("wide", 7), ("wide", 15)])
+def test_block_scaled_small_batches(shape, T):
+    """The block-scaled grouped GEMM below its whole-item range (fewer than
+    128 pairs): every item's K range is split, W2 parts add into the latent
+    aggregate like whole items and W1/W3 parts meet in a partial-sum buffer
+    whose last arrival applies SiTU. 4 to 120 pairs, one to several pairs per
+    expert, against the oracle."""
+    sh = {"tiny": k3synth.TINY, "mid": MID, "wide": WIDE}[shape]
+    run_case(sh, k3synth.TINY_RECIPE, 9, T, expert_path=_mode("mx"))
+
+
 @pytest.mark.parametrize("path", ["gemm", "gemv", "mx"])
 def test_expert_gemm_multi_tile(path):
     """Four experts forced into every token's selection (+10 router bias): each
@@ -403,6 +415,28 @@ def test_k3_decode_T1(k3layer):
         assert_close(bf16_to_f64(y), ref, f"K3 T=1 token {t}")
 
 
+def test_k3_decode_T1_block_scaled(k3layer):
+    """K3 T=1 on the block-scaled grouped GEMM with split K ranges (16 pairs,
+    W1/W3 in 4 parts and W2 in 6 per item)."""
+    import mxfp4_routed_expert_gb300 as km
+    d, lay = k3layer
+    shape = k3synth.K3
+    pool, _ = guarded_tokens(shape, d, 0, 64, stream=7)
+    try:
+        km.k3moe_set_expert_path(lay.h, km.K3MOE_EXPERT_MX)
+        for t in (0, 13, 63):
+            x = pool[t:t + 1]
+            y = lay.forward(x)
+            r = lay.routing(1)
+            acc = lay.intermediate(km.K3MOE_T_ACC, 1, shape.latent)
+            ref, tr = oracle.layer_forward(shape, d, x, trace=True)
+            check_routing(r, shape, x, tr["ids"], tr["w"])
+            assert_close(acc, tr["acc"], f"K3 T=1 token {t} latent aggregate")
+            assert_close(bf16_to_f64(y), ref, f"K3 T=1 token {t}")
+    finally:
+        km.k3moe_set_expert_path(lay.h, km.K3MOE_EXPERT_AUTO)
+
+
 @pytest.mark.parametrize("T", [2, 5, 8, 16])
 def test_k3_decode_batches(k3layer, T):
     """K3 width at the batch sizes between one token and T=64: T=2 runs the
@@ -415,7 +449,9 @@ def test_k3_decode_batches(k3layer, T):
     shape = k3synth.K3
     x, _ = guarded_tokens(shape, d, 0, T, stream=20 + T)
     ref, tr = oracle.layer_forward(shape, d, x, trace=True)
-    modes = (km.K3MOE_EXPERT_AUTO, km.K3MOE_EXPERT_GEMV) if T >= 16 else (km.K3MOE_EXPERT_AUTO,)
+    # the block-scaled grouped GEMM at every batch (K ranges split below 128 pairs)
+    modes = ((km.K3MOE_EXPERT_AUTO, km.K3MOE_EXPERT_GEMV, km.K3MOE_EXPERT_MX) if T >= 16
+             else (km.K3MOE_EXPERT_AUTO, km.K3MOE_EXPERT_MX))
     try:
         for mode in modes:
             km.k3moe_set_expert_path(lay.h, mode)
