@@ -248,17 +248,21 @@ K3MOE_API int k3moe_check_wait_timeout(k3moe *h, void *stream);
  *                      activations widened on the SM) whenever T * topk >= 128
  *                      (below that the GEMVs run: its n-tile needs 128 pair
  *                      rows);
- *   K3MOE_EXPERT_MX    the same batches on the grouped GEMM of the
- *                      block-scaled tensor cores (tcgen05 kind::mxf8f6f4):
- *                      the stored e2m1 weights and their ue8m0 scales go to
- *                      the tensor core as they are, against activations in
- *                      two-term MXFP8 (hi + lo e4m3 with a ue8m0 scale per 32,
- *                      about 12 significant bits); every scale byte is applied
- *                      exactly, whatever a row's scale range.
- * The grouped GEMMs need latent and moe_inter to be multiples of 128 and
- * max_tokens * topk >= 128; asking for K3MOE_EXPERT_GEMM or K3MOE_EXPERT_MX on
- * a handle whose shape does not allow it returns K3MOE_ERR_SHAPE and leaves
- * the mode as it was. Returns K3MOE_ERR_INVALID_ARG for an unknown mode. Takes
+ *   K3MOE_EXPERT_MX    every batch on the grouped GEMM of the block-scaled
+ *                      tensor cores (tcgen05 kind::mxf8f6f4): the stored e2m1
+ *                      weights and their ue8m0 scales go to the tensor core as
+ *                      they are, against activations in two-term MXFP8 (hi +
+ *                      lo e4m3 with a ue8m0 scale per 32, about 12 significant
+ *                      bits); every scale byte is applied exactly, whatever a
+ *                      row's scale range. Below 128 pairs each work item's K
+ *                      range may be split over several items (partial sums
+ *                      meet in device memory); at decode sizes this is slower
+ *                      than the GEMVs, which is why the automatic choice keeps
+ *                      them there.
+ * Both grouped GEMMs need latent and moe_inter to be multiples of 128; the f16
+ * one also needs max_tokens * topk >= 128. Asking for K3MOE_EXPERT_GEMM or
+ * K3MOE_EXPERT_MX on a handle whose shape does not allow it returns
+ * K3MOE_ERR_SHAPE and leaves the mode as it was. Returns K3MOE_ERR_INVALID_ARG for an unknown mode. Takes
  * effect at the next forward; not thread-safe with a forward on the same
  * handle. */
 enum { K3MOE_EXPERT_AUTO = 0, K3MOE_EXPERT_GEMV = 1, K3MOE_EXPERT_GEMM = 2, K3MOE_EXPERT_MX = 3 };
