@@ -38,6 +38,7 @@ struct GemmArgs {
     int KT;          // k-tiles in total
     int KTA;         // UP: k-tiles taken from map a0 (the rest from a1); RD: m-tiles of map a0
     int splits;      // split-K factor
+    int mpair;       // RD/UP: each CTA takes two adjacent 128-row m-tiles against one activation tile
     int ns;          // pipeline stages
     int E, L, S, H;
     float *logits, *z;          // RD outputs (fp32 [T,E], [T,L])
@@ -71,7 +72,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ unsigned char raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    const bool dual = g.mode == SH;
+    // two accumulators: gate and up (SH), or two m-tiles (RD/UP with mpair)
+    const bool dual = g.mode == SH || g.mpair;
     const int a_bytes = BM * BK * 2, b_bytes = g.BN * BK * 2;
     const int stage_bytes = (dual ? 2 : 1) * a_bytes + b_bytes;
     uint64_t *full = reinterpret_cast<uint64_t *>(sm + g.ns * stage_bytes);
@@ -80,7 +82,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t *tslot = reinterpret_cast<uint32_t *>(done + 1);
     __shared__ int last_flag;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nt = blockIdx.x, mt = blockIdx.y, ks = blockIdx.z;
+    const int nt = blockIdx.x, mt = g.mpair ? 2 * (int)blockIdx.y : (int)blockIdx.y, ks = blockIdx.z;
     const uint32_t tcols = dual ? 2u * (uint32_t)g.BN : (uint32_t)g.BN;
     uint32_t alloc_cols = 32;
     while (alloc_cols < tcols) alloc_cols <<= 1;
@@ -115,6 +117,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         amap = &a1;
         arow = (mt - g.KTA) * BM;
     }
+    // the second m-tile of an mpair CTA (rows past the matrix load as zeros
+    // and are never stored)
+    const CUtensorMap *amap2 = &a0;
+    int arow2 = (mt + 1) * BM;
+    if (g.mode == RD && mt + 1 >= g.KTA) {
+        amap2 = &a1;
+        arow2 = (mt + 1 - g.KTA) * BM;
+    }
 
     if (warp == 0 && lane == 0) {
         // ---------------- TMA producer ----------------
@@ -126,10 +136,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_expect_tx(&full[s], (uint32_t)stage_bytes);
             if (g.mode == UP) {
                 const bool first = kt < g.KTA;
-                tc::tma_load_2d(st, first ? &a0 : &a1, (first ? kt : kt - g.KTA) * BK, arow, &full[s]);
+                const CUtensorMap *m = first ? &a0 : &a1;
+                const int kc = (first ? kt : kt - g.KTA) * BK;
+                tc::tma_load_2d(st, m, kc, arow, &full[s]);
+                if (g.mpair) tc::tma_load_2d(st + a_bytes, m, kc, arow + BM, &full[s]);
             } else {
                 tc::tma_load_2d(st, amap, kt * BK, arow, &full[s]);
-                if (dual) tc::tma_load_2d(st + a_bytes, &a1, kt * BK, arow, &full[s]);
+                if (g.mpair) tc::tma_load_2d(st + a_bytes, amap2, kt * BK, arow2, &full[s]);
+                else if (dual) tc::tma_load_2d(st + a_bytes, &a1, kt * BK, arow, &full[s]);
             }
             tc::tma_load_2d(st + (dual ? 2 : 1) * a_bytes, &b, kt * BK, n0, &full[s]);
         }
@@ -165,13 +179,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     // rows of this tile in the mode's row numbering
     int row;
     bool row_ok;
-    if (g.mode == RD) {
-        row = mt < g.KTA ? mt * BM + row_in_tile : g.E + (mt - g.KTA) * BM + row_in_tile;
-        row_ok = mt < g.KTA ? row < g.E : (row - g.E) < g.L;
-    } else {
-        row = mt * BM + row_in_tile;
-        row_ok = row < (g.mode == SH ? g.S : g.H);
-    }
+    auto tile_row = [&](int m, int &r, bool &ok) {
+        if (g.mode == RD) {
+            r = m < g.KTA ? m * BM + row_in_tile : g.E + (m - g.KTA) * BM + row_in_tile;
+            ok = m < g.KTA ? r < g.E : (r - g.E) < g.L;
+        } else {
+            r = m * BM + row_in_tile;
+            ok = r < (g.mode == SH ? g.S : g.H);
+        }
+    };
+    tile_row(mt, row, row_ok);
+    int row2 = 0;                 // mpair: the row of the second m-tile
+    bool row2_ok = false;
+    if (g.mpair) tile_row(mt + 1, row2, row2_ok);
     const int R = g.mode == RD ? g.E + g.L : (g.mode == SH ? g.S : g.H);
     const uint32_t tbase = tmem + ((uint32_t)(warp * 32) << 16);
 
@@ -183,7 +203,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int j = 0; j < 16; j++) {
                 const int n = n0 + c + j;
-                if (row_ok && n < g.T) epilogue_store(g, row, n, v0[j], dual ? v1[j] : 0.f);
+                if (n >= g.T) continue;
+                if (g.mpair) {
+                    if (row_ok) epilogue_store(g, row, n, v0[j], 0.f);
+                    if (row2_ok) epilogue_store(g, row2, n, v1[j], 0.f);
+                } else if (row_ok) {
+                    epilogue_store(g, row, n, v0[j], dual ? v1[j] : 0.f);
+                }
             }
         }
     } else {
@@ -278,9 +304,9 @@ int pick_bn(int T, int mtiles, int sms)
     return pick;
 }
 
-int stages_for(int mode, int BN)
+int stages_for(bool dual, int BN)
 {
-    const int stage = (mode == SH ? 2 : 1) * BM * BK * 2 + BN * BK * 2;
+    const int stage = (dual ? 2 : 1) * BM * BK * 2 + BN * BK * 2;
     int ns = (kSmemBudget - 2048) / stage;
     return ns > 8 ? 8 : ns;
 }
@@ -332,10 +358,16 @@ cudaError_t launch_dense_gemm(const k3moe &h, const LayerDev &w, const __nv_bflo
     CUtensorMap a0, a1, b;
     int mtiles;
     bool ok = true;
+    // From 512 tokens the single-matrix projections (router+down, up+shared
+    // down) take two adjacent m-tiles per CTA, so that one activation tile
+    // feeds 256 weight rows as the shared gate/up's does: the operand bytes
+    // each SM takes in per MMA are what bounds these GEMMs at large T.
+    const bool mpair = part != 1 && T >= 512;
+    auto grid_m = [&](int mt) { return mpair ? (mt + 1) / 2 : mt; };
     if (part == 0) {
         const int mta = (c.n_experts + BM - 1) / BM;
         mtiles = mta + (c.latent + BM - 1) / BM;
-        g.BN = pick_bn(T, mtiles, h.sm_count);
+        g.BN = pick_bn(T, grid_m(mtiles), h.sm_count);
         g.KTA = mta;
         g.KT = c.hidden / BK;
         ok = tc::make_map_bf16_sw128(&a0, w.router_w, c.n_experts, c.hidden, c.hidden, BM) &&
@@ -350,7 +382,7 @@ cudaError_t launch_dense_gemm(const k3moe &h, const LayerDev &w, const __nv_bflo
              tc::make_map_bf16_sw128(&b, x, T, c.hidden, c.hidden, g.BN);
     } else {
         mtiles = (c.hidden + BM - 1) / BM;
-        g.BN = pick_bn(T, mtiles, h.sm_count);
+        g.BN = pick_bn(T, grid_m(mtiles), h.sm_count);
         g.KTA = c.latent / BK;
         g.KT = (c.latent + c.shared_inter) / BK;
         // a dense feed-forward layer has no latent columns: KTA = 0, a0 unused
@@ -368,10 +400,12 @@ cudaError_t launch_dense_gemm(const k3moe &h, const LayerDev &w, const __nv_bflo
             splits *= 2;
     }
     g.splits = splits;
-    g.ns = stages_for(part, g.BN);
-    const size_t smem = (size_t)g.ns * ((part == 1 ? 2 : 1) * BM * BK * 2 + g.BN * BK * 2) + 1024 + 256;
+    g.mpair = mpair ? 1 : 0;   // T >= 512: never split
+    const bool dual = part == 1 || mpair;
+    g.ns = stages_for(dual, g.BN);
+    const size_t smem = (size_t)g.ns * ((dual ? 2 : 1) * BM * BK * 2 + g.BN * BK * 2) + 1024 + 256;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)ntiles, (unsigned)mtiles, (unsigned)splits);
+    cfg.gridDim = dim3((unsigned)ntiles, (unsigned)grid_m(mtiles), (unsigned)splits);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;

@@ -65,8 +65,11 @@ WIDE = k3synth.Shape(hidden=1024, latent=512, n_experts=128, topk=8, moe_inter=5
                      shared_inter=1024)
 
 
-@pytest.mark.parametrize("T", [16, 37, 100, 300])
+@pytest.mark.parametrize("T", [16, 37, 100, 300, 600, 1030])
 def test_tensor_core_dense_path(T):
+    """From 512 tokens router+down and up+shared-down take two m-tiles per CTA
+    (WIDE: 5 router+down m-tiles, so the last pair's second tile lies past the
+    matrix and reads zeros)."""
     run_case(WIDE, k3synth.TINY_RECIPE, 6, T)
 
 
