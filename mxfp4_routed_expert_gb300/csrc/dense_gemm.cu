@@ -38,7 +38,6 @@ struct GemmArgs {
     int KT;          // k-tiles in total
     int KTA;         // UP: k-tiles taken from map a0 (the rest from a1); RD: m-tiles of map a0
     int splits;      // split-K factor
-    int mpair;       // RD/UP: each CTA takes two adjacent 128-row m-tiles against one activation tile
     int ns;          // pipeline stages
     int E, L, S, H;
     float *logits, *z;          // RD outputs (fp32 [T,E], [T,L])
@@ -65,6 +64,9 @@ __device__ __forceinline__ void epilogue_store(const GemmArgs &g, int row, int n
     }
 }
 
+// MPAIR: RD/UP with two m-tiles per CTA (its own instantiation, so that the
+// one-tile kernel compiles as if the pairing did not exist)
+template <bool MPAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     k_dense_gemm(const __grid_constant__ CUtensorMap a0, const __grid_constant__ CUtensorMap a1,
                  const __grid_constant__ CUtensorMap b, GemmArgs g)
@@ -73,7 +75,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     unsigned char *sm = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(raw) + 1023) & ~static_cast<uintptr_t>(1023));
     // two accumulators: gate and up (SH), or two m-tiles (RD/UP with mpair)
-    const bool dual = g.mode == SH || g.mpair;
+    const bool dual = g.mode == SH || MPAIR;
     const int a_bytes = BM * BK * 2, b_bytes = g.BN * BK * 2;
     const int stage_bytes = (dual ? 2 : 1) * a_bytes + b_bytes;
     uint64_t *full = reinterpret_cast<uint64_t *>(sm + g.ns * stage_bytes);
@@ -82,7 +84,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t *tslot = reinterpret_cast<uint32_t *>(done + 1);
     __shared__ int last_flag;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nt = blockIdx.x, mt = g.mpair ? 2 * (int)blockIdx.y : (int)blockIdx.y, ks = blockIdx.z;
+    const int nt = blockIdx.x, mt = MPAIR ? 2 * (int)blockIdx.y : (int)blockIdx.y, ks = blockIdx.z;
     const uint32_t tcols = dual ? 2u * (uint32_t)g.BN : (uint32_t)g.BN;
     uint32_t alloc_cols = 32;
     while (alloc_cols < tcols) alloc_cols <<= 1;
@@ -139,10 +141,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const CUtensorMap *m = first ? &a0 : &a1;
                 const int kc = (first ? kt : kt - g.KTA) * BK;
                 tc::tma_load_2d(st, m, kc, arow, &full[s]);
-                if (g.mpair) tc::tma_load_2d(st + a_bytes, m, kc, arow + BM, &full[s]);
+                if (MPAIR) tc::tma_load_2d(st + a_bytes, m, kc, arow + BM, &full[s]);
             } else {
                 tc::tma_load_2d(st, amap, kt * BK, arow, &full[s]);
-                if (g.mpair) tc::tma_load_2d(st + a_bytes, amap2, kt * BK, arow2, &full[s]);
+                if (MPAIR) tc::tma_load_2d(st + a_bytes, amap2, kt * BK, arow2, &full[s]);
                 else if (dual) tc::tma_load_2d(st + a_bytes, &a1, kt * BK, arow, &full[s]);
             }
             tc::tma_load_2d(st + (dual ? 2 : 1) * a_bytes, &b, kt * BK, n0, &full[s]);
@@ -191,7 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tile_row(mt, row, row_ok);
     int row2 = 0;                 // mpair: the row of the second m-tile
     bool row2_ok = false;
-    if (g.mpair) tile_row(mt + 1, row2, row2_ok);
+    if (MPAIR) tile_row(mt + 1, row2, row2_ok);
     const int R = g.mode == RD ? g.E + g.L : (g.mode == SH ? g.S : g.H);
     const uint32_t tbase = tmem + ((uint32_t)(warp * 32) << 16);
 
@@ -204,7 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < 16; j++) {
                 const int n = n0 + c + j;
                 if (n >= g.T) continue;
-                if (g.mpair) {
+                if (MPAIR) {
                     if (row_ok) epilogue_store(g, row, n, v0[j], 0.f);
                     if (row2_ok) epilogue_store(g, row2, n, v1[j], 0.f);
                 } else if (row_ok) {
@@ -315,7 +317,10 @@ int stages_for(bool dual, int BN)
 
 cudaError_t init_dense_gemm()
 {
-    return cudaFuncSetAttribute(k_dense_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const cudaError_t e = cudaFuncSetAttribute(k_dense_gemm<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               kSmemBudget - 1024);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(k_dense_gemm<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 kSmemBudget - 1024);
 }
 
@@ -400,7 +405,6 @@ cudaError_t launch_dense_gemm(const k3moe &h, const LayerDev &w, const __nv_bflo
             splits *= 2;
     }
     g.splits = splits;
-    g.mpair = mpair ? 1 : 0;   // T >= 512: never split
     const bool dual = part == 1 || mpair;
     g.ns = stages_for(dual, g.BN);
     const size_t smem = (size_t)g.ns * ((dual ? 2 : 1) * BM * BK * 2 + g.BN * BK * 2) + 1024 + 256;
@@ -414,7 +418,8 @@ cudaError_t launch_dense_gemm(const k3moe &h, const LayerDev &w, const __nv_bflo
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k_dense_gemm, a0, a1, b, g);
+    return mpair ? cudaLaunchKernelEx(&cfg, k_dense_gemm<true>, a0, a1, b, g)
+                 : cudaLaunchKernelEx(&cfg, k_dense_gemm<false>, a0, a1, b, g);
 }
 
 // act[t, 0:L] = bf16(acc[t] / sqrt(mean(acc[t]^2) + eps) * gain): the latent
