@@ -87,3 +87,30 @@ def test_route_static_matches_oracle(shape, seed, T):
         ids_g, w_g = ids.cpu().numpy(), w.cpu().numpy()
         check_ids_and_weights(ids_g, w_g, ids_ref, w_ref)
         _order_agrees(ids_g, ids_ref, ch, MARGIN_TAU)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("case", ["flat", "cut"])
+def test_route_static_exact_ties(case):
+    """Zero router weights: every score is sigmoid(0) = 0.5 exactly and every
+    selection key 0.5 + bias, so experts tie in groups (the bias cases of
+    tests/test_gpu_router_ties.py). The picks must be the larger keys first
+    and the lower ids among equal keys, in that order, with equal weights."""
+    import torch
+    from test_gpu_router_ties import expected_ids, tie_bias
+    km, _ = _lib()
+    shape, T = MID, 5
+    bias_np = tie_bias(shape.n_experts, case)
+    wr = torch.zeros((shape.n_experts, shape.hidden), dtype=torch.int16, device="cuda")
+    bias = torch.from_numpy(bias_np).cuda()
+    x = torch.from_numpy(k3synth.make_tokens(shape, 5, T, stream=4).view(np.int16).copy()).cuda()
+    ids = torch.full((T, shape.topk), -1, dtype=torch.int32, device="cuda")
+    w = torch.full((T, shape.topk), -1.0, dtype=torch.float32, device="cuda")
+    km.k3moe_route_static(x, wr, bias, T, shape.hidden, shape.n_experts, shape.topk,
+                          shape.renorm, shape.routed_scale, ids, w)
+    torch.cuda.synchronize()
+    want = expected_ids(bias_np, shape.topk)
+    ids_g, w_g = ids.cpu().numpy(), w.cpu().numpy()
+    for t in range(T):
+        np.testing.assert_array_equal(ids_g[t], want, err_msg=f"token {t}")
+    np.testing.assert_allclose(w_g, shape.routed_scale / shape.topk, rtol=1e-6)
