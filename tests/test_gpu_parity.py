@@ -87,6 +87,19 @@ def test_expert_paths(T, path):
     run_case(WIDE, k3synth.TINY_RECIPE, 6, T, expert_path=_mode(path))
 
 
+@pytest.mark.parametrize("E,k,T,path", [(16, 16, 1, None), (16, 16, 5, None), (16, 16, 16, "mx"),
+                                        (16, 16, 16, "gemm"), (32, 1, 1, None), (32, 1, 3, None),
+                                        (32, 1, 130, "mx"), (32, 1, 130, "gemm")])
+def test_degenerate_topk(E, k, T, path):
+    """The degenerate selections: every expert picked (k = E, so the weights
+    are all experts' renormalised scores and every expert holds every token)
+    and a single pick (k = 1, weight 1 after renormalisation). T = 1 writes
+    the permutation in the router epilogue, small batches run the GEMVs, and
+    128 pairs and more the grouped GEMMs."""
+    sh = k3synth.Shape(hidden=256, latent=128, n_experts=E, topk=k, moe_inter=128, shared_inter=256)
+    run_case(sh, k3synth.TINY_RECIPE, 14, T, expert_path=_mode(path) if path else None)
+
+
 @pytest.mark.parametrize("shape,T", [("tiny", 1), ("tiny", 4), ("mid", 1), ("mid", 5), ("wide", 1),
                                      ("wide", 7), ("wide", 15)])
 def test_block_scaled_small_batches(shape, T):
