@@ -44,11 +44,122 @@ struct GemmArgs {
     float *cat;                 // SH: fp32 copy of the shared SiTU at cat[:, L:] (pitch L+S)
     __nv_bfloat16 *act;         // SH: bf16 shared SiTU at act[:, L:] (pitch L+S)
     __nv_bfloat16 *y;           // UP output [T, H]
-    float b1, b2;
+    float b1, b2, ib1, ib2;     // SiTU bounds and their reciprocals
     float *part;                // split-K partials [T, 2*R] fp32 (zeroed), R = rows of the mode
     int *tile_count;            // split-K arrival counters per (m-tile, n-tile), left at 0
     int *err;
 };
+
+// One output run of an m-tile: for token n, nrows consecutive elements of
+// esz bytes at base + (n * pitch + r0) * esz (vec: every run starts on 16 bytes).
+struct OutRun {
+    unsigned char *base;
+    int pitch, r0, nrows, esz;
+    bool vec;
+};
+
+__device__ __forceinline__ OutRun out_run(unsigned char *base, int pitch, int r0, int rows, int esz)
+{
+    OutRun o;
+    o.base = base;
+    o.pitch = pitch;
+    o.r0 = r0;
+    o.nrows = rows - r0 < BM ? rows - r0 : BM;
+    o.esz = esz;
+    o.vec = ((reinterpret_cast<uintptr_t>(base) + (uintptr_t)r0 * esz) % 16 == 0) &&
+            ((size_t)pitch * esz) % 16 == 0;
+    return o;
+}
+
+// The output runs of slab k of this CTA's tile: the m-tile mt + k (router+down
+// and up+shared-down), or for the shared gate/up the fp32 and bf16 copies of
+// the SiTU of its one m-tile.
+__device__ __forceinline__ OutRun tile_run(const GemmArgs &g, int mt, int k)
+{
+    if (g.mode == SH) {
+        return k == 0 ? out_run(reinterpret_cast<unsigned char *>(g.cat + g.L), g.L + g.S, mt * BM, g.S, 4)
+                      : out_run(reinterpret_cast<unsigned char *>(g.act + g.L), g.L + g.S, mt * BM, g.S, 2);
+    }
+    const int m = mt + k;
+    if (g.mode == RD) {
+        return m < g.KTA ? out_run(reinterpret_cast<unsigned char *>(g.logits), g.E, m * BM, g.E, 4)
+                         : out_run(reinterpret_cast<unsigned char *>(g.z), g.L, (m - g.KTA) * BM, g.L, 4);
+    }
+    return out_run(reinterpret_cast<unsigned char *>(g.y), g.H, m * BM, g.H, 2);
+}
+
+// Epilogue of an unsplit tile, staged through shared memory (the operand ring
+// is idle once the MMAs are done): each round, the four warps write CW
+// tokens' values of their rows (TMEM lane = row) into slabs laid out
+// [token][128 rows], then all threads copy every token's row run to global
+// memory in 16-byte pieces. Element-wise stores (one 2- or 4-byte element per
+// lane, 32 rows of one token per warp instruction) ran the epilogue at about
+// 45 us per 256-token tile; staged, a warp instruction writes whole runs.
+constexpr int kStageTokens = 32;
+constexpr int kSlabBytes = kStageTokens * BM * 4;
+constexpr int kStageBytes = 2 * kSlabBytes;
+
+template <bool MPAIR>
+__device__ __forceinline__ void epilogue_staged(const GemmArgs &g, unsigned char *stage, uint32_t tbase,
+                                                bool dual, int mt, int n0, int rit)
+{
+    const int nslab = (g.mode == SH || MPAIR) ? 2 : 1;
+    OutRun run[2];
+    run[0] = tile_run(g, mt, 0);
+    run[1] = tile_run(g, mt, nslab > 1 ? 1 : 0);
+    float *f0 = reinterpret_cast<float *>(stage);
+    float *f1 = reinterpret_cast<float *>(stage + kSlabBytes);
+    __nv_bfloat16 *b0 = reinterpret_cast<__nv_bfloat16 *>(stage);
+    __nv_bfloat16 *b1 = reinterpret_cast<__nv_bfloat16 *>(stage + kSlabBytes);
+    for (int c0 = 0; c0 < g.BN; c0 += kStageTokens) {
+        const int cw = g.BN - c0 < kStageTokens ? g.BN - c0 : kStageTokens;   // a multiple of 16
+        for (int c = 0; c < cw; c += 16) {
+            float v0[16], v1[16];
+            tc::tmem_ld16(tbase + (uint32_t)(c0 + c), v0);
+            if (dual) tc::tmem_ld16(tbase + (uint32_t)(g.BN + c0 + c), v1);
+#pragma unroll
+            for (int j = 0; j < 16; j++) {
+                const int at = (c + j) * BM + rit;
+                if (g.mode == SH) {
+                    const float sv = situ_exp(v0[j], v1[j], g.b1, g.b2, g.ib1, g.ib2);
+                    f0[at] = sv;
+                    b1[at] = __float2bfloat16_rn(sv);
+                } else if (g.mode == RD) {
+                    f0[at] = v0[j];
+                    if (MPAIR) f1[at] = v1[j];
+                } else {
+                    b0[at] = __float2bfloat16_rn(v0[j]);
+                    if (MPAIR) b1[at] = __float2bfloat16_rn(v1[j]);
+                }
+            }
+        }
+        __syncthreads();
+        for (int k = 0; k < nslab; k++) {
+            const OutRun o = run[k];
+            if (o.nrows <= 0) continue;   // a second m-tile past the matrix
+            const int epp = 16 / o.esz;   // elements per 16-byte piece
+            const int ppr = BM / epp;     // pieces per token
+            const unsigned char *slab = stage + k * kSlabBytes;
+            for (int i = threadIdx.x; i < cw * ppr; i += kThreads) {
+                const int tk = i / ppr, e0 = (i - tk * ppr) * epp;
+                const int n = n0 + c0 + tk;
+                if (n >= g.T || e0 >= o.nrows) continue;
+                unsigned char *dst = o.base + ((size_t)n * o.pitch + o.r0 + e0) * o.esz;
+                const unsigned char *src = slab + (size_t)(tk * BM + e0) * o.esz;
+                if (o.vec && e0 + epp <= o.nrows) {
+                    *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<const uint4 *>(src);
+                } else if (o.esz == 4) {
+                    for (int e = 0; e < epp && e0 + e < o.nrows; e++)
+                        reinterpret_cast<uint32_t *>(dst)[e] = reinterpret_cast<const uint32_t *>(src)[e];
+                } else {
+                    for (int e = 0; e < epp && e0 + e < o.nrows; e++)
+                        reinterpret_cast<uint16_t *>(dst)[e] = reinterpret_cast<const uint16_t *>(src)[e];
+                }
+            }
+        }
+        __syncthreads();
+    }
+}
 
 __device__ __forceinline__ void epilogue_store(const GemmArgs &g, int row, int n, float v0, float v1)
 {
@@ -56,7 +167,7 @@ __device__ __forceinline__ void epilogue_store(const GemmArgs &g, int row, int n
         if (row < g.E) g.logits[(size_t)n * g.E + row] = v0;
         else g.z[(size_t)n * g.L + (row - g.E)] = v0;
     } else if (g.mode == SH) {
-        const float s = situ_f(v0, v1, g.b1, g.b2);
+        const float s = situ_exp(v0, v1, g.b1, g.b2, g.ib1, g.ib2);
         g.cat[(size_t)n * (g.L + g.S) + g.L + row] = s;
         g.act[(size_t)n * (g.L + g.S) + g.L + row] = __float2bfloat16_rn(s);
     } else {
@@ -191,29 +302,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     };
     tile_row(mt, row, row_ok);
-    int row2 = 0;                 // mpair: the row of the second m-tile
-    bool row2_ok = false;
-    if (MPAIR) tile_row(mt + 1, row2, row2_ok);
     const int R = g.mode == RD ? g.E + g.L : (g.mode == SH ? g.S : g.H);
     const uint32_t tbase = tmem + ((uint32_t)(warp * 32) << 16);
 
     if (g.splits == 1) {
-        for (int c = 0; c < g.BN; c += 16) {
-            float v0[16], v1[16];
-            tc::tmem_ld16(tbase + (uint32_t)c, v0);
-            if (dual) tc::tmem_ld16(tbase + (uint32_t)(g.BN + c), v1);
-#pragma unroll
-            for (int j = 0; j < 16; j++) {
-                const int n = n0 + c + j;
-                if (n >= g.T) continue;
-                if (MPAIR) {
-                    if (row_ok) epilogue_store(g, row, n, v0[j], 0.f);
-                    if (row2_ok) epilogue_store(g, row2, n, v1[j], 0.f);
-                } else if (row_ok) {
-                    epilogue_store(g, row, n, v0[j], dual ? v1[j] : 0.f);
-                }
-            }
-        }
+        // every MMA has completed (done), so the ring's shared memory is free
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        epilogue_staged<MPAIR>(g, sm, tbase, dual, mt, n0, row_in_tile);
     } else {
         // partial sums meet in g.part; the last CTA of the tile finishes it
         if (have_acc) {
@@ -357,6 +452,8 @@ cudaError_t launch_dense_gemm(const k3moe &h, const LayerDev &w, const __nv_bflo
     g.y = y;
     g.b1 = c.situ_b1;
     g.b2 = c.situ_b2;
+    g.ib1 = 1.0f / c.situ_b1;
+    g.ib2 = 1.0f / c.situ_b2;
     g.part = h.ws.gemm_part;
     g.tile_count = h.ws.gemm_tiles;
     g.err = h.ws.err;
@@ -407,7 +504,9 @@ cudaError_t launch_dense_gemm(const k3moe &h, const LayerDev &w, const __nv_bflo
     g.splits = splits;
     const bool dual = part == 1 || mpair;
     g.ns = stages_for(dual, g.BN);
-    const size_t smem = (size_t)g.ns * ((dual ? 2 : 1) * BM * BK * 2 + g.BN * BK * 2) + 1024 + 256;
+    const size_t ring = (size_t)g.ns * ((dual ? 2 : 1) * BM * BK * 2 + g.BN * BK * 2);
+    if (ring < (size_t)kStageBytes) return cudaErrorInvalidValue;   // the epilogue stages in the ring
+    const size_t smem = ring + 1024 + 256;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)ntiles, (unsigned)grid_m(mtiles), (unsigned)splits);
     cfg.blockDim = dim3(kThreads);

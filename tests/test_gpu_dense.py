@@ -49,9 +49,20 @@ def run_dense(shape, d, T, seed, residual=False):
     return assert_close(bf16_to_f64(y), ref)
 
 
-@pytest.mark.parametrize("T", [1, 2, 3, 7, 16, 40])
+@pytest.mark.parametrize("T", [1, 2, 3, 7, 16, 40, 300, 600])
 def test_dense_small(T):
     run_dense(SMALL, k3synth.make_dense_layer(SMALL, 11), T, 11 + T)
+
+
+# dense_inter 4160 = 32.5 row tiles of 128, hidden 1152 = 9 (the last pair of
+# the down projection's paired tiles has its second tile past the matrix):
+# the GEMM epilogues write partial row runs
+RAGGED = k3synth.dense_shape(1152, 4160)
+
+
+@pytest.mark.parametrize("T", [300, 600])
+def test_dense_ragged_rows(T):
+    run_dense(RAGGED, k3synth.make_dense_layer(RAGGED, 13), T, 50 + T)
 
 
 @pytest.mark.parametrize("T", [1, 2, 5, 20])
