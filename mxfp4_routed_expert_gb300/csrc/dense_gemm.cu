@@ -10,9 +10,10 @@
 // the tokens its N (B operand, 16..256 per tile), so small token counts waste
 // no tensor work on padding rows. A and B are K-major bf16 tiles of 64 columns
 // (128 bytes, 128-byte swizzle) loaded by TMA into a ring of shared-memory
-// stages; one thread issues tcgen05.mma (kind::f16, fp32 accumulators in
+// stages; one warp issues tcgen05.mma (kind::f16, fp32 accumulators in
 // TMEM) and commits each stage back to the producer; after the last k-tile all
-// four warps read the accumulators with tcgen05.ld and run the epilogue. When
+// eight warps read the accumulators with tcgen05.ld (two warps per TMEM lane
+// quadrant, alternate 16-column groups) and run the epilogue. When
 // the (M, N) tile grid is too small to occupy the GPU, K is split across CTAs
 // whose fp32 partials meet in global memory by atomic addition; the last CTA
 // of a tile (counted in global memory) applies the epilogue.
@@ -26,7 +27,7 @@ namespace k3 {
 namespace {
 
 constexpr int BM = 128, BK = 64;
-constexpr int kThreads = 128;
+constexpr int kThreads = 256;   // warps 0 and 1 also produce and issue; all eight run the epilogue
 constexpr int kSmemBudget = 227 * 1024;
 
 enum Mode : int { RD = 0, SH = 1, UP = 2 };
@@ -89,7 +90,7 @@ __device__ __forceinline__ OutRun tile_run(const GemmArgs &g, int mt, int k)
 }
 
 // Epilogue of an unsplit tile, staged through shared memory (the operand ring
-// is idle once the MMAs are done): each round, the four warps write CW
+// is idle once the MMAs are done): each round, the eight warps write CW
 // tokens' values of their rows (TMEM lane = row) into slabs laid out
 // [token][128 rows], then all threads copy every token's row run to global
 // memory in 16-byte pieces. Element-wise stores (one 2- or 4-byte element per
@@ -101,7 +102,7 @@ constexpr int kStageBytes = 2 * kSlabBytes;
 
 template <bool MPAIR>
 __device__ __forceinline__ void epilogue_staged(const GemmArgs &g, unsigned char *stage, uint32_t tbase,
-                                                bool dual, int mt, int n0, int rit)
+                                                bool dual, int mt, int n0, int rit, int half)
 {
     const int nslab = (g.mode == SH || MPAIR) ? 2 : 1;
     OutRun run[2];
@@ -113,7 +114,7 @@ __device__ __forceinline__ void epilogue_staged(const GemmArgs &g, unsigned char
     __nv_bfloat16 *b1 = reinterpret_cast<__nv_bfloat16 *>(stage + kSlabBytes);
     for (int c0 = 0; c0 < g.BN; c0 += kStageTokens) {
         const int cw = g.BN - c0 < kStageTokens ? g.BN - c0 : kStageTokens;   // a multiple of 16
-        for (int c = 0; c < cw; c += 16) {
+        for (int c = 16 * half; c < cw; c += 32) {
             float v0[16], v1[16];
             tc::tmem_ld16(tbase + (uint32_t)(c0 + c), v0);
             if (dual) tc::tmem_ld16(tbase + (uint32_t)(g.BN + c0 + c), v1);
@@ -176,8 +177,10 @@ __device__ __forceinline__ void epilogue_store(const GemmArgs &g, int row, int n
 }
 
 // MPAIR: RD/UP with two m-tiles per CTA (its own instantiation, so that the
-// one-tile kernel compiles as if the pairing did not exist)
-template <bool MPAIR>
+// one-tile kernel compiles as if the pairing did not exist). WIDE: the
+// producer and the MMA issuer are whole warps (below 512 tokens), else lone
+// threads (see the roles below).
+template <bool MPAIR, bool WIDE>
 __global__ void __launch_bounds__(kThreads, 1)
     k_dense_gemm(const __grid_constant__ CUtensorMap a0, const __grid_constant__ CUtensorMap a1,
                  const __grid_constant__ CUtensorMap b, GemmArgs g)
@@ -239,56 +242,73 @@ __global__ void __launch_bounds__(kThreads, 1)
         arow2 = (mt + 1 - g.KTA) * BM;
     }
 
-    if (warp == 0 && lane == 0) {
+    // Roles. With few tokens per tile (WIDE) the producer and the MMA issuer
+    // are whole warps: every lane runs the loop, so that the descriptors and
+    // coordinates are warp-uniform, lane 0 polls the barrier and one elected
+    // lane issues; a lone issuing thread spent about 250 cycles per
+    // tcgen05.mma there whatever its N. With 256-token tiles the MMAs bound
+    // the stage and lone threads measured faster (dense gate/up at 4096
+    // tokens 2.27 against 2.46 ms).
+    if (warp == 0 && (WIDE || lane == 0)) {
         // ---------------- TMA producer ----------------
         for (int kt = kt0; kt < kt1; kt++) {
             const int i = kt - kt0, s = i % g.ns;
             const uint32_t ph = (uint32_t)(i / g.ns) & 1u;
-            if (!mbar_wait(&empty[s], ph ^ 1u, g.err, 500)) break;
-            unsigned char *st = sm + s * stage_bytes;
-            mbar_expect_tx(&full[s], (uint32_t)stage_bytes);
-            if (g.mode == UP) {
-                const bool first = kt < g.KTA;
-                const CUtensorMap *m = first ? &a0 : &a1;
-                const int kc = (first ? kt : kt - g.KTA) * BK;
-                tc::tma_load_2d(st, m, kc, arow, &full[s]);
-                if (MPAIR) tc::tma_load_2d(st + a_bytes, m, kc, arow + BM, &full[s]);
-            } else {
-                tc::tma_load_2d(st, amap, kt * BK, arow, &full[s]);
-                if (MPAIR) tc::tma_load_2d(st + a_bytes, amap2, kt * BK, arow2, &full[s]);
-                else if (dual) tc::tma_load_2d(st + a_bytes, &a1, kt * BK, arow, &full[s]);
+            if (WIDE ? !tc::lane0_wait(&empty[s], ph ^ 1u, g.err, 500) : !mbar_wait(&empty[s], ph ^ 1u, g.err, 500))
+                break;
+            if (!WIDE || tc::elect_one()) {
+                unsigned char *st = sm + s * stage_bytes;
+                mbar_expect_tx(&full[s], (uint32_t)stage_bytes);
+                if (g.mode == UP) {
+                    const bool first = kt < g.KTA;
+                    const CUtensorMap *m = first ? &a0 : &a1;
+                    const int kc = (first ? kt : kt - g.KTA) * BK;
+                    tc::tma_load_2d(st, m, kc, arow, &full[s]);
+                    if (MPAIR) tc::tma_load_2d(st + a_bytes, m, kc, arow + BM, &full[s]);
+                } else {
+                    tc::tma_load_2d(st, amap, kt * BK, arow, &full[s]);
+                    if (MPAIR) tc::tma_load_2d(st + a_bytes, amap2, kt * BK, arow2, &full[s]);
+                    else if (dual) tc::tma_load_2d(st + a_bytes, &a1, kt * BK, arow, &full[s]);
+                }
+                tc::tma_load_2d(st + (dual ? 2 : 1) * a_bytes, &b, kt * BK, n0, &full[s]);
             }
-            tc::tma_load_2d(st + (dual ? 2 : 1) * a_bytes, &b, kt * BK, n0, &full[s]);
+            if (WIDE) __syncwarp();
         }
-    } else if (warp == 1 && lane == 0) {
+    } else if (warp == 1 && (WIDE || lane == 0)) {
         // ---------------- MMA issuer ----------------
         const uint32_t idesc = tc::idesc_bf16(BM, g.BN);
         for (int kt = kt0; kt < kt1; kt++) {
             const int i = kt - kt0, s = i % g.ns;
             const uint32_t ph = (uint32_t)(i / g.ns) & 1u;
-            if (!mbar_wait(&full[s], ph, g.err, 501)) break;
+            if (WIDE ? !tc::lane0_wait(&full[s], ph, g.err, 501) : !mbar_wait(&full[s], ph, g.err, 501)) break;
             tc::fence_after();
             const uint32_t sa = tc::su32(sm + s * stage_bytes);
             const uint32_t sb = sa + (dual ? 2 : 1) * a_bytes;
+            if (!WIDE || tc::elect_one()) {
 #pragma unroll
-            for (int kk = 0; kk < BK / 16; kk++) {
-                const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
-                tc::mma_bf16(tmem, tc::desc_sw128(sa + kk * 32), tc::desc_sw128(sb + kk * 32), idesc, acc);
-                if (dual)
-                    tc::mma_bf16(tmem + (uint32_t)g.BN, tc::desc_sw128(sa + a_bytes + kk * 32),
-                                 tc::desc_sw128(sb + kk * 32), idesc, acc);
+                for (int kk = 0; kk < BK / 16; kk++) {
+                    const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
+                    tc::mma_bf16(tmem, tc::desc_sw128(sa + kk * 32), tc::desc_sw128(sb + kk * 32), idesc, acc);
+                    if (dual)
+                        tc::mma_bf16(tmem + (uint32_t)g.BN, tc::desc_sw128(sa + a_bytes + kk * 32),
+                                     tc::desc_sw128(sb + kk * 32), idesc, acc);
+                }
+                tc::commit(&empty[s]);
             }
-            tc::commit(&empty[s]);
+            if (WIDE) __syncwarp();
         }
-        tc::commit(done);
+        if (!WIDE || tc::elect_one()) tc::commit(done);
     }
     __syncwarp();
 
-    // ---------------- epilogue: all four warps ----------------
+    // ---------------- epilogue: all eight warps ----------------
     const bool have_acc = kt1 > kt0;
     if (have_acc) mbar_wait(done, 0, g.err, 502);
     tc::fence_after();
-    const int row_in_tile = warp * 32 + lane;
+    // warp w reads TMEM lanes 32 (w % 4) .. + 31; the two halves of the CTA
+    // take alternate 16-column groups
+    const int quad = warp & 3, half = warp >> 2;
+    const int row_in_tile = quad * 32 + lane;
     // rows of this tile in the mode's row numbering
     int row;
     bool row_ok;
@@ -303,16 +323,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     tile_row(mt, row, row_ok);
     const int R = g.mode == RD ? g.E + g.L : (g.mode == SH ? g.S : g.H);
-    const uint32_t tbase = tmem + ((uint32_t)(warp * 32) << 16);
+    const uint32_t tbase = tmem + ((uint32_t)(quad * 32) << 16);
 
     if (g.splits == 1) {
         // every MMA has completed (done), so the ring's shared memory is free
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        epilogue_staged<MPAIR>(g, sm, tbase, dual, mt, n0, row_in_tile);
+        epilogue_staged<MPAIR>(g, sm, tbase, dual, mt, n0, row_in_tile, half);
     } else {
         // partial sums meet in g.part; the last CTA of the tile finishes it
         if (have_acc) {
-            for (int c = 0; c < g.BN; c += 16) {
+            for (int c = 16 * half; c < g.BN; c += 32) {
                 float v0[16], v1[16];
                 tc::tmem_ld16(tbase + (uint32_t)c, v0);
                 if (dual) tc::tmem_ld16(tbase + (uint32_t)(g.BN + c), v1);
@@ -339,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             __threadfence();
             // 16 columns at a time: all their loads in flight before any use,
             // so that the tile costs BN / 16 L2 round trips, not BN
-            for (int c = 0; c < g.BN; c += 16) {
+            for (int c = 16 * half; c < g.BN; c += 32) {
                 float v0[16], v1[16];
 #pragma unroll
                 for (int j = 0; j < 16; j++) {
@@ -412,11 +432,11 @@ int stages_for(bool dual, int BN)
 
 cudaError_t init_dense_gemm()
 {
-    const cudaError_t e = cudaFuncSetAttribute(k_dense_gemm<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               kSmemBudget - 1024);
-    if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(k_dense_gemm<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                kSmemBudget - 1024);
+    for (auto *k : {k_dense_gemm<true, false>, k_dense_gemm<false, false>, k_dense_gemm<false, true>}) {
+        const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget - 1024);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 size_t dense_gemm_part_floats(const k3moe_config &c)
@@ -517,8 +537,10 @@ cudaError_t launch_dense_gemm(const k3moe &h, const LayerDev &w, const __nv_bflo
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return mpair ? cudaLaunchKernelEx(&cfg, k_dense_gemm<true>, a0, a1, b, g)
-                 : cudaLaunchKernelEx(&cfg, k_dense_gemm<false>, a0, a1, b, g);
+    // the paired tiles run from 512 tokens, where the roles are lone threads
+    if (mpair) return cudaLaunchKernelEx(&cfg, k_dense_gemm<true, false>, a0, a1, b, g);
+    if (T >= 512) return cudaLaunchKernelEx(&cfg, k_dense_gemm<false, false>, a0, a1, b, g);
+    return cudaLaunchKernelEx(&cfg, k_dense_gemm<false, true>, a0, a1, b, g);
 }
 
 // act[t, 0:L] = bf16(acc[t] / sqrt(mean(acc[t]^2) + eps) * gain): the latent

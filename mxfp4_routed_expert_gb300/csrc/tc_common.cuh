@@ -195,6 +195,15 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, int *e
     return __all_sync(0xffffffffu, ok) != 0;
 }
 
+// A bounded barrier wait by lane 0 of a converged warp, its outcome
+// broadcast: the other lanes wait at the shuffle instead of polling.
+__device__ __forceinline__ bool lane0_wait(uint64_t *bar, uint32_t parity, int *err, int where)
+{
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, err, where) ? 1 : 0;
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
 // Work items handed out at run time. One thread of the CTA (the writer)
 // claims the next item number from a counter in global memory that every CTA
 // of the launch shares, when it is ready to start that item, and publishes it
