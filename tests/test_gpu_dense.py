@@ -49,7 +49,7 @@ def run_dense(shape, d, T, seed, residual=False):
     return assert_close(bf16_to_f64(y), ref)
 
 
-@pytest.mark.parametrize("T", [1, 2, 3, 7, 16, 40, 300, 600])
+@pytest.mark.parametrize("T", [1, 2, 3, 7, 16, 40, 200, 256, 300, 600])
 def test_dense_small(T):
     run_dense(SMALL, k3synth.make_dense_layer(SMALL, 11), T, 11 + T)
 
@@ -60,7 +60,7 @@ def test_dense_small(T):
 RAGGED = k3synth.dense_shape(1152, 4160)
 
 
-@pytest.mark.parametrize("T", [300, 600])
+@pytest.mark.parametrize("T", [200, 300, 600])
 def test_dense_ragged_rows(T):
     run_dense(RAGGED, k3synth.make_dense_layer(RAGGED, 13), T, 50 + T)
 

@@ -75,13 +75,14 @@ def test_tensor_core_dense_path(T):
 
 # Row counts that are not multiples of the 128-row tiles: 130 experts (a
 # router tile of 2 rows, whose fp32 logit rows of 520 bytes are not 16-byte
-# multiples), latent 576, shared 1088, hidden 1152 (9 row tiles, so the last
-# pair of paired tiles has its second tile past the matrix)
+# multiples, and router+down partial sums of 706 rows that are not either),
+# latent 576, shared 1088, hidden 1152 (9 row tiles, so the last pair of
+# paired tiles has its second tile past the matrix); T = 40 and 200 split K
 RAGGED = k3synth.Shape(hidden=1152, latent=576, n_experts=130, topk=8, moe_inter=512,
                        shared_inter=1088)
 
 
-@pytest.mark.parametrize("T", [300, 600])
+@pytest.mark.parametrize("T", [40, 200, 300, 600])
 def test_tensor_core_dense_ragged_rows(T):
     run_case(RAGGED, k3synth.TINY_RECIPE, 8, T)
 
