@@ -119,27 +119,39 @@ __device__ __forceinline__ int block_excl_scan(int v, int *wsum, int *total)
 //   3. per chunk (one warp), its pairs placed in token order. The k experts of
 //      one token are distinct, so the lanes of a step never share a counter and
 //      tokens stay ascending inside every expert's run.
+// Steps 1 and 3 first copy the chunk's ids (and weights) to shared memory with
+// all their loads in flight, so that the serial pass over the chunk's tokens
+// waits on no global load.
 constexpr int kPermChunk = 32;
 constexpr int kPermWarps = 8;            // chunks per block in steps 1 and 3
 
+// shared memory of steps 1 (place = false) and 3: per warp the expert
+// counters [E], then the chunk's ids [kPermChunk * k] (and weights)
+size_t perm_smem(const k3moe_config &c, bool place)
+{
+    return (size_t)kPermWarps * ((size_t)c.n_experts + (size_t)kPermChunk * c.topk * (place ? 2 : 1)) * sizeof(int);
+}
+
 __global__ void __launch_bounds__(kPermWarps * 32) k_perm_hist(PermArgs a, int *hist)
 {
-    extern __shared__ int sh[];          // [kPermWarps][E]
+    extern __shared__ int sh[];          // per warp: [E] counters, [kPermChunk * k] ids
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    int *h = sh + warp * a.E;
+    int *h = sh + (size_t)warp * (a.E + kPermChunk * a.k);
+    int *ids = h + a.E;
     pdl_launch_dependents();
     pdl_wait();
     const int chunk = blockIdx.x * kPermWarps + warp;
     const int t0 = chunk * kPermChunk;
     if (t0 >= a.T) return;
+    const int nt = min(a.T, t0 + kPermChunk) - t0;
+    for (int i = lane; i < nt * a.k; i += 32) ids[i] = a.ids[(size_t)t0 * a.k + i];
     for (int e = lane; e < a.E; e += 32) h[e] = 0;
     __syncwarp();
-    const int t1 = min(a.T, t0 + kPermChunk);
-    for (int t = t0; t < t1; t++) {
+    for (int t = 0; t < nt; t++) {
         if (lane < a.k) {
-            const int e = a.ids[(size_t)t * a.k + lane];
+            const int e = ids[t * a.k + lane];
             if (e >= 0 && e < a.E) h[e] += 1;      // distinct experts within a token
-            else if (e != -1) set_err(a.err, kErrBounds, t);   // -1: dropped by the weight cut
+            else if (e != -1) set_err(a.err, kErrBounds, t0 + t);   // -1: dropped by the weight cut
         }
         __syncwarp();
     }
@@ -189,25 +201,31 @@ __global__ void __launch_bounds__(1024) k_perm_scan(PermArgs a, int *hist, int n
 
 __global__ void __launch_bounds__(kPermWarps * 32) k_perm_place(PermArgs a, const int *hist)
 {
-    extern __shared__ int sh[];          // [kPermWarps][E]: next position per expert
+    extern __shared__ int sh[];          // per warp: [E] next position per expert, the chunk's ids and weights
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    int *pos = sh + warp * a.E;
+    int *pos = sh + (size_t)warp * (a.E + 2 * kPermChunk * a.k);
+    int *ids = pos + a.E;
+    float *wv = reinterpret_cast<float *>(ids + kPermChunk * a.k);
     pdl_launch_dependents();
     pdl_wait();
     const int chunk = blockIdx.x * kPermWarps + warp;
     const int t0 = chunk * kPermChunk;
     if (t0 >= a.T) return;
+    const int nt = min(a.T, t0 + kPermChunk) - t0;
+    for (int i = lane; i < nt * a.k; i += 32) {
+        ids[i] = a.ids[(size_t)t0 * a.k + i];
+        wv[i] = a.wts[(size_t)t0 * a.k + i];
+    }
     const int *base = hist + (size_t)chunk * a.E;
     for (int e = lane; e < a.E; e += 32) pos[e] = a.offsets[e] + base[e];
     __syncwarp();
-    const int t1 = min(a.T, t0 + kPermChunk);
-    for (int t = t0; t < t1; t++) {
+    for (int t = 0; t < nt; t++) {
         if (lane < a.k) {
-            const int e = a.ids[(size_t)t * a.k + lane];
+            const int e = ids[t * a.k + lane];
             if (e >= 0 && e < a.E) {
                 const int p = pos[e]++;
-                a.perm[p] = t * a.k + lane;
-                a.pair_w[p] = a.wts[(size_t)t * a.k + lane];
+                a.perm[p] = (t0 + t) * a.k + lane;
+                a.pair_w[p] = wv[t * a.k + lane];
             }
         }
         __syncwarp();
@@ -236,18 +254,18 @@ cudaError_t launch_perm(const k3moe &h, int T, cudaStream_t s, int step)
     a.err = h.ws.err;
     const int nch = perm_chunks(T);
     const int blocks = (nch + kPermWarps - 1) / kPermWarps;
-    const size_t smem = (size_t)kPermWarps * c.n_experts * sizeof(int);
-    if (step == 0) return launch_pdl(k_perm_hist, blocks, kPermWarps * 32, smem, s, a, h.ws.perm_hist);
+    if (step == 0) return launch_pdl(k_perm_hist, blocks, kPermWarps * 32, perm_smem(c, false), s, a, h.ws.perm_hist);
     if (step == 1) return launch_pdl(k_perm_scan, 1, 1024, 0, s, a, h.ws.perm_hist, nch);
-    return launch_pdl(k_perm_place, blocks, kPermWarps * 32, smem, s, a, (const int *)h.ws.perm_hist);
+    return launch_pdl(k_perm_place, blocks, kPermWarps * 32, perm_smem(c, true), s, a,
+                      (const int *)h.ws.perm_hist);
 }
 
 cudaError_t init_route_kernels(const k3moe_config &c)
 {
-    const int smem = (int)((size_t)kPermWarps * c.n_experts * sizeof(int));
-    cudaError_t e = cudaFuncSetAttribute(k_perm_hist, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = cudaFuncSetAttribute(k_perm_hist, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)perm_smem(c, false));
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(k_perm_place, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    return cudaFuncSetAttribute(k_perm_place, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)perm_smem(c, true));
 }
 
 }  // namespace k3
