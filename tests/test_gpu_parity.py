@@ -114,6 +114,16 @@ def test_degenerate_topk(E, k, T, path):
     run_case(sh, k3synth.TINY_RECIPE, 14, T, expert_path=_mode(path) if path else None)
 
 
+@pytest.mark.parametrize("T,path", [(1, None), (5, None), (40, None), (40, "mx"), (40, "gemm")])
+def test_max_routing_shape(T, path):
+    """The largest routing the library accepts: 1024 experts, top-32 (the
+    router keeps 32 scores per lane; the permutation's histogram and placement
+    warps then stage 32-token chunks of 32 ids and weights each beside 1024
+    counters)."""
+    sh = k3synth.Shape(hidden=256, latent=128, n_experts=1024, topk=32, moe_inter=128, shared_inter=256)
+    run_case(sh, k3synth.TINY_RECIPE, 15, T, expert_path=_mode(path) if path else None)
+
+
 @pytest.mark.parametrize("shape,T", [("tiny", 1), ("tiny", 4), ("mid", 1), ("mid", 5), ("wide", 1),
                                      ("wide", 7), ("wide", 15)])
 def test_block_scaled_small_batches(shape, T):
