@@ -20,7 +20,7 @@ oracle on the host cores on a bounded sample of the same workload.
 
 With torchrun (N > 1) every rank runs an independent replica of the layer
 (the layer does not shard across GPUs); rank 0 prints the line.
---impl reference times the CPU oracle (the reference arm of this build).
+--impl reference times the fp64 CPU oracle as the reference arm, on the same workload.
 """
 from __future__ import annotations
 
