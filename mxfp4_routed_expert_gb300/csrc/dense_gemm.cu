@@ -90,8 +90,8 @@ __device__ __forceinline__ OutRun tile_run(const GemmArgs &g, int mt, int k)
 }
 
 // Epilogue of an unsplit tile, staged through shared memory (the operand ring
-// is idle once the MMAs are done): each round, the eight warps write CW
-// tokens' values of their rows (TMEM lane = row) into slabs laid out
+// is idle once the MMAs are done): each round, the eight warps write
+// kStageTokens tokens' values of their rows (TMEM lane = row) into slabs laid out
 // [token][128 rows], then all threads copy every token's row run to global
 // memory in 16-byte pieces. Element-wise stores (one 2- or 4-byte element per
 // lane, 32 rows of one token per warp instruction) ran the epilogue at about
